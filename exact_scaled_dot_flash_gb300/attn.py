@@ -1,0 +1,183 @@
+"""ctypes binding of libattn.so (``include/attn.h``): argument marshalling only.
+
+Every arithmetic step runs in the CUDA kernels behind ``attn_fwd``; this
+module checks tensor devices, dtypes and contiguity, allocates the output with
+PyTorch (PyTorch is used for device memory and streams only) and passes raw
+pointers plus the current CUDA stream. When the library is missing the call
+raises; there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIBNAME = "libattn.so"
+_lock = threading.Lock()
+_lib = None
+
+ATTN_F32, ATTN_F16, ATTN_BF16 = 0, 1, 2
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING = 0, 1, 2
+
+
+class AttnError(RuntimeError):
+    """Raised when attn_fwd returns an error code or the library is missing."""
+
+    def __init__(self, msg, code=None):
+        super().__init__(msg)
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    """attn_shape_t."""
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "Hq", "Hkv", "Sq", "Sk", "D", "bias_b", "bias_h")]
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIBNAME)
+
+
+def load_library():
+    """Open libattn.so once; raise AttnError if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise AttnError(f"{path} is missing: build the CUDA library first "
+                            "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        vp = ctypes.c_void_p
+        lib.attn_fwd.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, ctypes.c_int, vp, vp,
+                                 ctypes.c_float, ctypes.c_int, vp, vp]
+        lib.attn_fwd.restype = ctypes.c_int
+        lib.attn_strerror.argtypes = [ctypes.c_int]
+        lib.attn_strerror.restype = ctypes.c_char_p
+        lib.attn_last_cuda_error.argtypes = []
+        lib.attn_last_cuda_error.restype = ctypes.c_int
+        lib.attn_device_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int]
+        lib.attn_device_status.restype = ctypes.c_int
+        lib.attn_version.argtypes = []
+        lib.attn_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def strerror(code: int) -> str:
+    return load_library().attn_strerror(int(code)).decode()
+
+
+def check(code: int):
+    if code != 0:
+        lib = load_library()
+        extra = ""
+        if code == -9:
+            extra = f" (cudaError {lib.attn_last_cuda_error()})"
+        raise AttnError(f"attn_fwd failed: {strerror(code)}{extra}", code)
+
+
+def device_status(device: int = 0, clear: bool = False) -> int:
+    """Sticky kernel error flags of ``device`` (0 = no bounded wait expired)."""
+    flags = ctypes.c_int(0)
+    check(load_library().attn_device_status(int(device), ctypes.byref(flags), int(bool(clear))))
+    return flags.value
+
+
+def _dtype_code(t):
+    import torch
+    codes = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16}
+    if t.dtype not in codes:
+        raise AttnError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def call(shape: Shape, q_ptr, k_ptr, v_ptr, mask: int, kv_lens_ptr, bias_ptr, scale: float,
+         dtype: int, out_ptr, stream_handle) -> None:
+    """Raw attn_fwd call with integer pointers (0 for NULL); raises on error."""
+    lib = load_library()
+    check(lib.attn_fwd(ctypes.byref(shape), q_ptr or None, k_ptr or None, v_ptr or None, int(mask),
+                       kv_lens_ptr or None, bias_ptr or None, float(scale), int(dtype),
+                       out_ptr or None, stream_handle or None))
+
+
+def fwd(q, k, v, *, causal: bool = False, kv_lens=None, bias=None, scale: float | None = None,
+        out=None, stream=None):
+    """O = softmax(Q K^T * scale + mask + bias) V on the GPU.
+
+    q: [B,Hq,Sq,D]; k, v: [B,Hkv,Sk,D]; float32, float16 or bfloat16, contiguous.
+    kv_lens: int32 [B] valid key counts (enables the key-padding mask).
+    bias: float32 [bias_b, bias_h, Sq, Sk], bias_b in {1,B}, bias_h in {1,Hq}.
+    scale: defaults to 1/sqrt(D).
+    Tensors on a CUDA device run on ``stream`` (default: the current stream)
+    and the result is returned without synchronising. Host tensors are copied
+    to the current CUDA device, computed there, and the result is copied back
+    (synchronising); pinned host memory makes the copies asynchronous DMA.
+    """
+    import torch
+
+    if q.device.type == "cpu":
+        return _fwd_host(q, k, v, causal=causal, kv_lens=kv_lens, bias=bias, scale=scale, out=out)
+    dev = q.device
+    for name, t in (("k", k), ("v", v)):
+        if t.device != dev:
+            raise AttnError(f"{name} is on {t.device}, q on {dev}")
+        if t.dtype != q.dtype:
+            raise AttnError(f"{name} dtype {t.dtype} differs from q dtype {q.dtype}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dim() != 4:
+            raise AttnError(f"{name} must be 4-D [B, H, S, D]")
+        if not t.is_contiguous():
+            raise AttnError(f"{name} must be contiguous")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    if tuple(k.shape) != (B, Hkv, Sk, D) or tuple(v.shape) != tuple(k.shape):
+        raise AttnError("k and v must be [B, Hkv, Sk, D] matching q")
+    mask = MASK_CAUSAL if causal else MASK_NONE
+    kv_ptr = 0
+    if kv_lens is not None:
+        if kv_lens.device != dev or kv_lens.dtype != torch.int32 or tuple(kv_lens.shape) != (B,):
+            raise AttnError("kv_lens must be int32 [B] on q's device")
+        kv_lens = kv_lens.contiguous()
+        mask |= MASK_KEY_PADDING
+        kv_ptr = kv_lens.data_ptr()
+    bb = bh = 1
+    b_ptr = 0
+    if bias is not None:
+        if bias.device != dev or bias.dtype != torch.float32 or bias.dim() != 4 or not bias.is_contiguous():
+            raise AttnError("bias must be a contiguous float32 [bias_b, bias_h, Sq, Sk] tensor on q's device")
+        bb, bh = int(bias.shape[0]), int(bias.shape[1])
+        if tuple(bias.shape[2:]) != (Sq, Sk):
+            raise AttnError("bias must be [bias_b, bias_h, Sq, Sk]")
+        b_ptr = bias.data_ptr()
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or out.device != dev or not out.is_contiguous():
+        raise AttnError("out must be a contiguous tensor like q")
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    shape = Shape(B, Hq, Hkv, Sq, Sk, D, bb, bh)
+    call(shape, q.data_ptr(), k.data_ptr(), v.data_ptr(), mask, kv_ptr, b_ptr, scale,
+         _dtype_code(q), out.data_ptr(), stream.cuda_stream)
+    return out
+
+
+def _fwd_host(q, k, v, *, causal, kv_lens, bias, scale, out):
+    """Host tensors in, host tensor out: H2D copies, the GPU kernel, a D2H copy."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def up(t):
+        return None if t is None else t.to(dev, non_blocking=True)
+
+    o_dev = fwd(up(q), up(k), up(v), causal=causal, kv_lens=up(kv_lens), bias=up(bias), scale=scale)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    out.copy_(o_dev, non_blocking=True)
+    torch.cuda.current_stream(dev).synchronize()
+    return out

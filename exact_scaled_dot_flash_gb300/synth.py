@@ -1,0 +1,159 @@
+"""Seeded synthetic inputs for exact scaled-dot-product attention.
+
+This module is the one piece shared by the GPU path's tests/bench and by the
+float64 oracle: it draws Q, K, V (and, for the key-padding workload, the
+per-batch valid lengths and the additive fp32 bias) and rounds them to the
+storage dtype. It holds none of the attention arithmetic.
+
+Recipe (identical on both sides, stated once here):
+  * bit generator: numpy's Philox-4x64 counter-based generator, keyed by the
+    pair (seed, stream) through ``np.random.SeedSequence``; each tensor has its
+    own stream (0 = Q, 1 = K, 2 = V, 3 = kv_lens, 4 = bias), so every tensor
+    is independent of the shapes of the others;
+  * values: standard normal draws in float32 times sigma, then rounded
+    round-to-nearest-even to the storage dtype (fp32 stays as drawn; fp16 via
+    numpy's IEEE conversion; bf16 by rounding the fp32 bit pattern);
+  * key-padding lengths: integers uniform on [lo, hi] inclusive;
+  * bias: fp32 standard normal, never rounded.
+
+Storage format returned to callers: ``np.float32`` for F32, ``np.float16``
+for F16, and ``np.uint16`` bit patterns for BF16 (numpy has no bfloat16).
+
+The workload table ``WORKLOADS`` describes the benchmark shapes of the
+attention pages: a small F32 causal case, a char-transformer-sized BF16 block
+(B=8, H=8, S=128, D in {32, 64}), a long-context causal MHA (B=4, H=32,
+S=4096, D=128, plus a wide-score variant with Q,K ~ N(0, 3^2)), a GQA case
+(Hq=32, Hkv=8, S=8192) and an F16 key-padding + bias case.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+F32, F16, BF16 = "f32", "f16", "bf16"
+DTYPES = (F32, F16, BF16)
+
+# Mask kinds are bit flags, the same values the C ABI uses.
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING = 0, 1, 2
+
+STREAM_Q, STREAM_K, STREAM_V, STREAM_LENS, STREAM_BIAS = 0, 1, 2, 3, 4
+
+
+def _gen(seed: int, stream: int) -> np.random.Generator:
+    return np.random.Generator(np.random.Philox(np.random.SeedSequence([int(seed), int(stream)])))
+
+
+def normal_f32(seed: int, stream: int, shape, sigma: float = 1.0) -> np.ndarray:
+    """float32 N(0, sigma^2) draws for (seed, stream), C-contiguous."""
+    x = _gen(seed, stream).standard_normal(size=tuple(shape), dtype=np.float32)
+    if sigma != 1.0:
+        x *= np.float32(sigma)
+    return x
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round finite float32 values to bfloat16 (nearest, ties to even); returns uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return r.astype(np.uint16)
+
+
+def to_storage(x_f32: np.ndarray, dtype: str) -> np.ndarray:
+    """Round a float32 array to the storage dtype (see module docstring)."""
+    if dtype == F32:
+        return np.ascontiguousarray(x_f32, dtype=np.float32)
+    if dtype == F16:
+        return np.ascontiguousarray(x_f32.astype(np.float16))
+    if dtype == BF16:
+        return f32_to_bf16_bits(x_f32)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One attention problem: shapes, dtype, mask, bias layout and input recipe."""
+    name: str
+    dtype: str
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    Sk: int
+    D: int
+    mask: int = MASK_NONE
+    bias: bool = False
+    bias_b: int = 1
+    bias_h: int = 1
+    seed: int = 0
+    sigma_qk: float = 1.0
+    sigma_v: float = 1.0
+    kv_len_range: tuple | None = None   # (lo, hi) inclusive, key-padding only
+    scale: float | None = None          # default 1/sqrt(D)
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale is not None else 1.0 / math.sqrt(self.D)
+
+    @property
+    def causal(self) -> bool:
+        return bool(self.mask & MASK_CAUSAL)
+
+    def flops(self) -> float:
+        """Nominal attention FLOPs 4*B*Hq*Sq*Sk*D, halved for a causal mask."""
+        f = 4.0 * self.B * self.Hq * self.Sq * self.Sk * self.D
+        return f / 2.0 if self.causal else f
+
+    def io_bytes(self) -> int:
+        """Bytes read and written once: Q, K, V, O (+ bias, + kv_lens)."""
+        es = {F32: 4, F16: 2, BF16: 2}[self.dtype]
+        n = (2 * self.B * self.Hq * self.Sq + 2 * self.B * self.Hkv * self.Sk) * self.D * es
+        if self.bias:
+            n += self.bias_b * self.bias_h * self.Sq * self.Sk * 4
+        if self.mask & MASK_KEY_PADDING:
+            n += 4 * self.B
+        return n
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    "f32_causal_small": Workload("f32_causal_small", F32, 2, 2, 2, 64, 64, 16,
+                                 mask=MASK_CAUSAL, seed=0),
+    "bf16_block_d32": Workload("bf16_block_d32", BF16, 8, 8, 8, 128, 128, 32,
+                               mask=MASK_CAUSAL, seed=1),
+    "bf16_block_d64": Workload("bf16_block_d64", BF16, 8, 8, 8, 128, 128, 64,
+                               mask=MASK_CAUSAL, seed=1),
+    "bf16_causal_4k": Workload("bf16_causal_4k", BF16, 4, 32, 32, 4096, 4096, 128,
+                               mask=MASK_CAUSAL, seed=2),
+    "bf16_causal_4k_wide": Workload("bf16_causal_4k_wide", BF16, 4, 32, 32, 4096, 4096, 128,
+                                    mask=MASK_CAUSAL, seed=3, sigma_qk=3.0),
+    "bf16_gqa_8k": Workload("bf16_gqa_8k", BF16, 2, 32, 8, 8192, 8192, 128,
+                            mask=MASK_CAUSAL, seed=4),
+    "f16_padding_bias": Workload("f16_padding_bias", F16, 16, 16, 16, 1024, 1024, 64,
+                                 mask=MASK_KEY_PADDING, bias=True, bias_b=1, bias_h=16,
+                                 seed=5, kv_len_range=(256, 1024)),
+}
+
+
+def make_inputs(w: Workload) -> dict:
+    """Draw the inputs of workload ``w``.
+
+    Returns a dict with ``q`` [B,Hq,Sq,D], ``k``/``v`` [B,Hkv,Sk,D] in storage
+    format, ``kv_lens`` int32 [B] or None, ``bias`` float32
+    [bias_b,bias_h,Sq,Sk] or None, plus ``scale`` (float) and ``mask`` (int).
+    """
+    q = to_storage(normal_f32(w.seed, STREAM_Q, (w.B, w.Hq, w.Sq, w.D), w.sigma_qk), w.dtype)
+    k = to_storage(normal_f32(w.seed, STREAM_K, (w.B, w.Hkv, w.Sk, w.D), w.sigma_qk), w.dtype)
+    v = to_storage(normal_f32(w.seed, STREAM_V, (w.B, w.Hkv, w.Sk, w.D), w.sigma_v), w.dtype)
+    kv_lens = None
+    if w.mask & MASK_KEY_PADDING:
+        lo, hi = w.kv_len_range if w.kv_len_range is not None else (0, w.Sk)
+        kv_lens = _gen(w.seed, STREAM_LENS).integers(lo, hi, size=w.B, endpoint=True).astype(np.int32)
+    bias = None
+    if w.bias:
+        bias = normal_f32(w.seed, STREAM_BIAS, (w.bias_b, w.bias_h, w.Sq, w.Sk))
+    return {"q": q, "k": k, "v": v, "kv_lens": kv_lens, "bias": bias,
+            "scale": w.softmax_scale, "mask": w.mask}

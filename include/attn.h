@@ -1,0 +1,127 @@
+/*
+ * attn.h - C ABI of the exact scaled-dot-product attention forward library
+ * (libattn.so) for GB300 / sm_103a.
+ *
+ * The operation, per batch b, query head hq and query row i:
+ *
+ *   s_j = scale * dot(Q[b,hq,i,:], K[b,hk,j,:]) + bias[b,hq,i,j]   (visible j)
+ *   s_j = -inf                                                      (masked j)
+ *   O[b,hq,i,:] = sum_j softmax_j(s) * V[b,hk,j,:],   hk = hq / (Hq / Hkv)
+ *
+ * Definition sources (page title, section):
+ *  - "RustによるHOF認知Flash Attention実装の手引き" (HOF cognitive Flash
+ *    Attention in Rust), section 4 "Kernel": exact scaled dot-product
+ *    attention; exp of the scores divided by the row sum gives row-stochastic
+ *    weights A; the output is A.V. Sections 2 and 4: a tiled FlashAttention
+ *    kernel gives the same exact result without materialising the n x n
+ *    score matrix in HBM (this library never writes it).
+ *  - tensai autograd guide, "Attention の組み立て": (batch, head, seq,
+ *    headDim) layout; scale Q.K^T, then add the mask, then softmax over the
+ *    last axis; causal mask 0 on/below the diagonal, -inf above.
+ *  - ruDNN user guide, section 2 (Attention): query, key, value, optional
+ *    mask, optional attn_bias, options; errors are returned, not raised.
+ *    Section 9: contiguous unquantised F32/F16/BF16 inputs of one dtype,
+ *    Hq divisible by Hkv, a finite positive scale. Section 7: statistics in
+ *    FP32, the output cast to the input dtype.
+ *
+ * Readings where the pages are silent: the causal diagonal is aligned
+ * bottom-right (key j visible to row i when j <= i + Sk - Sq); key padding
+ * masks keys j >= clamp(kv_lens[b], 0, Sk) and never query rows; a masked
+ * position stays -inf whatever the bias; a row with no visible key has an
+ * undefined softmax and its output is NaN.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of Q, K, V and O. */
+typedef enum { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 } attn_dtype_t;
+
+/* Mask kinds: bit flags, ATTN_MASK_CAUSAL | ATTN_MASK_KEY_PADDING = both. */
+enum {
+  ATTN_MASK_NONE = 0,
+  ATTN_MASK_CAUSAL = 1,
+  ATTN_MASK_KEY_PADDING = 2
+};
+
+/* Status codes: 0 is success, errors are negative. */
+enum {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL = -1,      /* a required pointer is NULL                              */
+  ATTN_ERR_SHAPE = -2,     /* a dimension is out of range, Hq % Hkv != 0, bad bias dims */
+  ATTN_ERR_DTYPE = -3,     /* unknown dtype                                           */
+  ATTN_ERR_HEAD_DIM = -4,  /* D has no compiled kernel for this dtype                 */
+  ATTN_ERR_ALIGN = -5,     /* a pointer is not 16-byte aligned                        */
+  ATTN_ERR_SCALE = -6,     /* scale is not finite and positive                        */
+  ATTN_ERR_MASK = -7,      /* unknown mask bits, or KEY_PADDING with kv_lens == NULL  */
+  ATTN_ERR_OVERLAP = -8,   /* out overlaps q, k, v, kv_lens or bias                   */
+  ATTN_ERR_CUDA = -9,      /* a CUDA call failed; see attn_last_cuda_error()          */
+  ATTN_ERR_TIMEOUT = -10   /* a kernel gave up on a bounded wait (see attn_device_status) */
+};
+
+/* Problem shape. All counts are elements.
+ *   Q   [B, Hq,  Sq, D]   contiguous, row-major
+ *   K,V [B, Hkv, Sk, D]   contiguous, row-major
+ *   O   [B, Hq,  Sq, D]   contiguous, row-major
+ *   bias (fp32) [bias_b, bias_h, Sq, Sk] with bias_b in {1, B}, bias_h in {1, Hq};
+ *   a size-1 axis broadcasts. bias_b / bias_h are read only when bias != NULL. */
+typedef struct {
+  int32_t B, Hq, Hkv, Sq, Sk, D;
+  int32_t bias_b, bias_h;
+} attn_shape_t;
+
+/* attn_fwd - exact attention forward on the GPU, asynchronous on `stream`.
+ *
+ * q, k, v, out: device pointers to contiguous tensors of `dtype` (layouts
+ *   above), each 16-byte aligned. `out` is written entirely (rows with no
+ *   visible key become NaN) and must not overlap any input.
+ * mask_kind: ATTN_MASK_* bits. ATTN_MASK_KEY_PADDING needs kv_lens.
+ * kv_lens: device int32[B] valid key counts (clamped to [0, Sk] on the
+ *   device), or NULL without ATTN_MASK_KEY_PADDING.
+ * bias: device fp32 [bias_b, bias_h, Sq, Sk] (16-byte aligned) or NULL; it is
+ *   added to the scaled scores and indexed by the query head.
+ * scale: multiplies Q.K^T; finite and > 0 (typically 1/sqrt(D)).
+ * stream: a cudaStream_t, or NULL for the legacy default stream.
+ *
+ * Supported head dims: D in {32, 64, 128} for F16/BF16 (tensor-core path),
+ * D in {16, 32, 64, 128} for F32 (fp32 FMA path). B or Sq equal to 0 is a
+ * no-op; Sk equal to 0 gives NaN rows. Hq, Hkv, D must be positive.
+ *
+ * Ownership: the caller owns every buffer; the library keeps no pointer after
+ * returning and allocates no device memory. The call does not synchronise;
+ * argument errors are reported before anything is launched. Thread-safe.
+ * Returns ATTN_OK or a negative ATTN_ERR_* code. */
+int attn_fwd(const attn_shape_t* shape,
+             const void* q, const void* k, const void* v,
+             int mask_kind, const int32_t* kv_lens,
+             const float* bias,
+             float scale, attn_dtype_t dtype,
+             void* out,
+             void* stream);
+
+/* attn_strerror - static English text for a status code (never NULL). */
+const char* attn_strerror(int code);
+
+/* attn_last_cuda_error - the cudaError_t value of the last CUDA failure seen
+ * by attn_fwd on the calling thread (0 if none). */
+int attn_last_cuda_error(void);
+
+/* attn_device_status - read (and, when clear != 0, reset) the sticky error
+ * word that kernels on `device` set when a bounded wait expires. Writes the
+ * flags to *flags (0 = no failure seen). Synchronises with the device.
+ * Returns ATTN_OK, ATTN_ERR_NULL or ATTN_ERR_CUDA. */
+int attn_device_status(int device, int* flags, int clear);
+
+/* attn_version - library version as major*10000 + minor*100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

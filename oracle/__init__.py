@@ -1,0 +1,156 @@
+"""Float64 CPU oracle for exact scaled-dot-product attention.
+
+TEST INFRASTRUCTURE ONLY: the slow, plain definition the CUDA kernels are
+checked against. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import it. It shares no
+code with the CUDA library and never consumes a value the CUDA path produced;
+the one thing both sides share is the seeded input generator
+(``exact_scaled_dot_flash_gb300.synth``), which holds no attention arithmetic.
+
+The arithmetic lives in ``attn_ref.c`` (plain C, float64, threaded over
+heads); this module widens the stored inputs exactly to float64, compiles the
+C file on first use (gcc) and calls it through ctypes.
+
+Every function is pinned by ``tests/test_oracle_pins.py`` against closed
+forms, invariants, a 50-digit brute force of the pages' raw-exp kernel, and a
+textbook single-head reduction; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_ref.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+MASK_CAUSAL, MASK_KEY_PADDING = 1, 2
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("B", "Hq", "Hkv", "Sq", "Sk", "D", "bias_b", "bias_h")]
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_ref.c into liboracle.so (skipped when up to date)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            dp = ctypes.POINTER(ctypes.c_double)
+            lib.oracle_attention.argtypes = [ctypes.POINTER(_Shape), dp, dp, dp, ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_int32), dp, ctypes.c_double,
+                                             dp, dp, ctypes.c_int]
+            lib.oracle_attention.restype = ctypes.c_int
+            lib.oracle_attention_rows.argtypes = [ctypes.POINTER(_Shape), dp, dp, dp, ctypes.c_int,
+                                                  ctypes.POINTER(ctypes.c_int32), dp, ctypes.c_double,
+                                                  ctypes.c_int64, ctypes.POINTER(ctypes.c_int64),
+                                                  dp, ctypes.c_int]
+            lib.oracle_attention_rows.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def widen(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Exactly widen stored values to float64.
+
+    ``dtype`` is "f32", "f16" or "bf16"; bf16 values arrive as uint16 bit
+    patterns and become float32 by placing them in the high half of the word.
+    """
+    if dtype == "bf16":
+        bits = np.ascontiguousarray(x, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+        return bits.view(np.float32).astype(np.float64)
+    if dtype in ("f16", "f32", "f64"):
+        return np.ascontiguousarray(x).astype(np.float64)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def _dptr(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double)) if a is not None else None
+
+
+def _prepare(q, k, v, kv_lens, bias, dtype):
+    q64 = widen(q, dtype) if dtype else np.ascontiguousarray(q, dtype=np.float64)
+    k64 = widen(k, dtype) if dtype else np.ascontiguousarray(k, dtype=np.float64)
+    v64 = widen(v, dtype) if dtype else np.ascontiguousarray(v, dtype=np.float64)
+    B, Hq, Sq, D = q64.shape
+    Bk, Hkv, Sk, Dk = k64.shape
+    if (Bk, Dk) != (B, D) or v64.shape != k64.shape:
+        raise ValueError("shape mismatch between q, k and v")
+    shape = _Shape(B, Hq, Hkv, Sq, Sk, D, 1, 1)
+    b64 = None
+    if bias is not None:
+        b64 = np.ascontiguousarray(bias, dtype=np.float64)
+        if b64.ndim != 4 or b64.shape[2:] != (Sq, Sk):
+            raise ValueError("bias must be [bias_b, bias_h, Sq, Sk]")
+        shape.bias_b, shape.bias_h = b64.shape[0], b64.shape[1]
+    lens = None
+    if kv_lens is not None:
+        lens = np.ascontiguousarray(kv_lens, dtype=np.int32)
+    return q64, k64, v64, lens, b64, shape
+
+
+def attention(q, k, v, *, mask: int = 0, kv_lens=None, bias=None, scale: float,
+              dtype: str | None = None, weights: bool = False, threads: int = 0):
+    """Float64 attention output for every row.
+
+    q: [B,Hq,Sq,D], k/v: [B,Hkv,Sk,D] in storage format of ``dtype`` (or any
+    float array when ``dtype`` is None); kv_lens: int32 [B] (key padding);
+    bias: float [bias_b,bias_h,Sq,Sk]. Returns O [B,Hq,Sq,D] float64, and the
+    weights [B,Hq,Sq,Sk] too when ``weights`` is True.
+    """
+    lib = _load()
+    q64, k64, v64, lens, b64, shape = _prepare(q, k, v, kv_lens, bias, dtype)
+    out = np.empty(q64.shape, dtype=np.float64)
+    w = np.empty(q64.shape[:3] + (k64.shape[2],), dtype=np.float64) if weights else None
+    rc = lib.oracle_attention(ctypes.byref(shape), _dptr(q64), _dptr(k64), _dptr(v64), int(mask),
+                              lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if lens is not None else None,
+                              _dptr(b64), float(scale), _dptr(out), _dptr(w), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention rejected its arguments (rc={rc})")
+    return (out, w) if weights else out
+
+
+def attention_rows(q, k, v, rows, *, mask: int = 0, kv_lens=None, bias=None, scale: float,
+                   dtype: str | None = None, threads: int = 0, widened=None):
+    """Float64 output rows O[b,hq,i,:] for the (b, hq, i) triples in ``rows``.
+
+    ``widened`` may carry a tuple from :func:`prepare` to avoid re-widening
+    large inputs between calls. Returns [len(rows), D] float64.
+    """
+    lib = _load()
+    if widened is None:
+        widened = prepare(q, k, v, kv_lens=kv_lens, bias=bias, dtype=dtype)
+    q64, k64, v64, lens, b64, shape = widened
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    out = np.empty((r.shape[0], q64.shape[3]), dtype=np.float64)
+    rc = lib.oracle_attention_rows(ctypes.byref(shape), _dptr(q64), _dptr(k64), _dptr(v64), int(mask),
+                                   lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if lens is not None else None,
+                                   _dptr(b64), float(scale), r.shape[0],
+                                   r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _dptr(out), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_rows rejected its arguments (rc={rc})")
+    return out
+
+
+def prepare(q, k, v, *, kv_lens=None, bias=None, dtype: str | None = None):
+    """Widen inputs once for repeated :func:`attention_rows` calls."""
+    return _prepare(q, k, v, kv_lens, bias, dtype)

@@ -1,0 +1,248 @@
+/*
+ * Float64 CPU oracle for exact scaled-dot-product attention (forward).
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the slow, plain definition that the
+ * GPU kernels are checked against. Only the test suite, the smoke check and
+ * the CPU-baseline leg of the benchmark may load it. It shares no code,
+ * header, table or helper with the CUDA library, and it never reads a value
+ * produced by the CUDA path.
+ *
+ * What it computes, for every batch b, query head hq and query row i:
+ *
+ *   s_j = scale * sum_d Q[b,hq,i,d] * K[b,hk,j,d] + bias[b,hq,i,j]   (visible j)
+ *   s_j = -inf                                                        (masked j)
+ *   w_j = exp(s_j - max_j s_j) / sum_j exp(s_j - max_j s_j)
+ *   O[b,hq,i,:] = sum_j w_j * V[b,hk,j,:]
+ *
+ * Sources (by page title and section):
+ *  - "RustによるHOF認知Flash Attention実装の手引き" (HOF cognitive Flash
+ *    Attention in Rust), section 4 "Kernel": scores are Q.K^T times a scale,
+ *    exponentiated, divided by the row sum to give row-stochastic weights A,
+ *    and the result is A.V. Section 2 and section 4: the FlashAttention
+ *    tiling computes the same exact result, so the oracle is the untiled
+ *    definition.
+ *  - tensai autograd guide, "Attention の組み立て" (assembling attention):
+ *    layout (batch, head, seq, headDim); the scale is applied to Q.K^T before
+ *    the additive mask; softmax over the last axis; the causal mask is 0 on
+ *    and below the diagonal and -Inf above it.
+ *  - ruDNN user guide, section 9 (paged attention and MLA): Hq must be a
+ *    multiple of Hkv (GQA); inputs are F32/F16/BF16; scale finite and
+ *    positive. Section 2: the attention op takes an optional mask and an
+ *    optional additive attn_bias.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - the row maximum is subtracted before exp (softmax is shift invariant, so
+ *    this is the same value as the page's raw exp, without overflow);
+ *  - scale multiplies Q.K^T only; the fp32 bias is added after scaling;
+ *  - a masked position is -inf whatever the bias;
+ *  - causal alignment is bottom-right: key j is visible to row i when
+ *    j <= i + (Sk - Sq);
+ *  - key padding masks keys j >= clamp(kv_lens[b], 0, Sk); query rows are
+ *    not masked;
+ *  - GQA maps query head hq to key/value head hq / (Hq / Hkv);
+ *  - the bias has shape [bias_b, bias_h, Sq, Sk] with bias_b in {1, B} and
+ *    bias_h in {1, Hq}, broadcast over the size-1 axes;
+ *  - a row with no visible key has undefined weights: the oracle returns NaN
+ *    for its weights and its output (exp(-inf - (-inf)) in the plain form).
+ *
+ * Inputs are float64 arrays holding the already dtype-rounded values,
+ * widened exactly; accumulation is in float64 throughout.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORACLE_MASK_CAUSAL 1
+#define ORACLE_MASK_KEY_PADDING 2
+
+typedef struct {
+  int64_t B, Hq, Hkv, Sq, Sk, D;
+  int64_t bias_b, bias_h; /* ignored when bias == NULL */
+} oracle_shape;
+
+typedef struct {
+  const oracle_shape* s;
+  const double *q, *k, *v, *bias;
+  const int32_t* kv_lens;
+  int mask;
+  double scale;
+} problem;
+
+/* One output row (b, hq, i): writes D outputs, and Sk weights when w != NULL.
+ * `sc` is caller scratch of Sk doubles. */
+static void attention_row(const problem* P, int64_t b, int64_t hq, int64_t i,
+                          double* o, double* w, double* sc) {
+  const oracle_shape* s = P->s;
+  const int64_t D = s->D, Sk = s->Sk, Sq = s->Sq;
+  const int64_t group = s->Hq / s->Hkv;
+  const int64_t hk = hq / group;
+
+  int64_t key_limit = Sk;
+  if (P->mask & ORACLE_MASK_KEY_PADDING) {
+    int64_t L = P->kv_lens[b];
+    key_limit = L < 0 ? 0 : (L > Sk ? Sk : L);
+  }
+  const double* qi = P->q + ((b * s->Hq + hq) * Sq + i) * D;
+  const double* kh = P->k + (b * s->Hkv + hk) * Sk * D;
+  const double* vh = P->v + (b * s->Hkv + hk) * Sk * D;
+  const double* brow = NULL;
+  if (P->bias) {
+    int64_t bb = (s->bias_b == 1) ? 0 : b;
+    int64_t bh = (s->bias_h == 1) ? 0 : hq;
+    brow = P->bias + ((bb * s->bias_h + bh) * Sq + i) * Sk;
+  }
+
+  /* scores, with the mask as -inf */
+  double m = -INFINITY;
+  for (int64_t j = 0; j < Sk; ++j) {
+    int visible = j < key_limit;
+    if ((P->mask & ORACLE_MASK_CAUSAL) && !(j <= i + (Sk - Sq))) visible = 0;
+    double sj = -INFINITY;
+    if (visible) {
+      double dot = 0.0;
+      for (int64_t d = 0; d < D; ++d) dot += qi[d] * kh[j * D + d];
+      sj = P->scale * dot + (brow ? brow[j] : 0.0);
+    }
+    sc[j] = sj;
+    if (sj > m) m = sj;
+  }
+
+  if (m == -INFINITY) { /* no visible key: undefined softmax -> NaN */
+    for (int64_t d = 0; d < D; ++d) o[d] = NAN;
+    if (w) for (int64_t j = 0; j < Sk; ++j) w[j] = NAN;
+    return;
+  }
+
+  /* exp and row sum */
+  double l = 0.0;
+  for (int64_t j = 0; j < Sk; ++j) {
+    double p = exp(sc[j] - m); /* exp(-inf) == 0 for masked keys */
+    sc[j] = p;
+    l += p;
+  }
+  /* row-stochastic weights and the weighted sum of V */
+  for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+  for (int64_t j = 0; j < Sk; ++j) {
+    double wj = sc[j] / l;
+    if (w) w[j] = wj;
+    for (int64_t d = 0; d < D; ++d) o[d] += wj * vh[j * D + d];
+  }
+}
+
+/* ---- threading: a shared counter hands out work items ---- */
+typedef struct {
+  const problem* P;
+  int64_t n_items;
+  const int64_t* rows; /* NULL: items are (b, hq) heads; else (b, hq, i) triples */
+  double* out;
+  double* weights;
+  int64_t next;
+  pthread_mutex_t lock;
+  int failed;
+} job;
+
+static int64_t take(job* J) {
+  pthread_mutex_lock(&J->lock);
+  int64_t t = J->next++;
+  pthread_mutex_unlock(&J->lock);
+  return t;
+}
+
+static void* worker(void* arg) {
+  job* J = (job*)arg;
+  const oracle_shape* s = J->P->s;
+  double* sc = (double*)malloc(sizeof(double) * (size_t)(s->Sk > 0 ? s->Sk : 1));
+  if (!sc) {
+    pthread_mutex_lock(&J->lock);
+    J->failed = 1;
+    pthread_mutex_unlock(&J->lock);
+    return NULL;
+  }
+  for (int64_t t = take(J); t < J->n_items; t = take(J)) {
+    if (J->rows) {
+      const int64_t* r = J->rows + 3 * t;
+      attention_row(J->P, r[0], r[1], r[2], J->out + t * s->D, NULL, sc);
+    } else {
+      int64_t b = t / s->Hq, hq = t % s->Hq;
+      for (int64_t i = 0; i < s->Sq; ++i) {
+        int64_t row = (b * s->Hq + hq) * s->Sq + i;
+        attention_row(J->P, b, hq, i, J->out + row * s->D,
+                      J->weights ? J->weights + row * s->Sk : NULL, sc);
+      }
+    }
+  }
+  free(sc);
+  return NULL;
+}
+
+static int run(job* J, int nthreads) {
+  if (nthreads <= 0) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    nthreads = n > 0 ? (int)n : 1;
+  }
+  if (nthreads > J->n_items) nthreads = J->n_items > 0 ? (int)J->n_items : 1;
+  J->next = 0;
+  J->failed = 0;
+  pthread_mutex_init(&J->lock, NULL);
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  if (!th) return -2;
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t)
+    if (pthread_create(&th[t], NULL, worker, J) == 0) ++started;
+  if (started == 0) worker(J);
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  free(th);
+  pthread_mutex_destroy(&J->lock);
+  return J->failed ? -2 : 0;
+}
+
+static int check_shape(const oracle_shape* s, int mask, const int32_t* kv_lens) {
+  if (!s) return -1;
+  if (s->B < 0 || s->Hq <= 0 || s->Hkv <= 0 || s->Sq < 0 || s->Sk < 0 || s->D <= 0) return -1;
+  if (s->Hq % s->Hkv) return -1;
+  if ((mask & ORACLE_MASK_KEY_PADDING) && !kv_lens) return -1;
+  if (mask & ~(ORACLE_MASK_CAUSAL | ORACLE_MASK_KEY_PADDING)) return -1;
+  return 0;
+}
+
+/* Full problem. out: [B,Hq,Sq,D]; weights (optional): [B,Hq,Sq,Sk].
+ * Returns 0, -1 on a bad argument, -2 when memory runs out. */
+int oracle_attention(const oracle_shape* s, const double* q, const double* k, const double* v,
+                     int mask, const int32_t* kv_lens, const double* bias, double scale,
+                     double* out, double* weights, int nthreads) {
+  if (check_shape(s, mask, kv_lens)) return -1;
+  if (bias && !((s->bias_b == 1 || s->bias_b == s->B) && (s->bias_h == 1 || s->bias_h == s->Hq)))
+    return -1;
+  problem P = {s, q, k, v, bias, kv_lens, mask, scale};
+  job J;
+  memset(&J, 0, sizeof J);
+  J.P = &P;
+  J.n_items = s->B * s->Hq;
+  J.out = out;
+  J.weights = weights;
+  return run(&J, nthreads);
+}
+
+/* Selected rows only. rows: nrows triples (b, hq, i); out: [nrows, D]. */
+int oracle_attention_rows(const oracle_shape* s, const double* q, const double* k, const double* v,
+                          int mask, const int32_t* kv_lens, const double* bias, double scale,
+                          int64_t nrows, const int64_t* rows, double* out, int nthreads) {
+  if (check_shape(s, mask, kv_lens)) return -1;
+  if (bias && !((s->bias_b == 1 || s->bias_b == s->B) && (s->bias_h == 1 || s->bias_h == s->Hq)))
+    return -1;
+  for (int64_t t = 0; t < nrows; ++t) {
+    const int64_t* r = rows + 3 * t;
+    if (r[0] < 0 || r[0] >= s->B || r[1] < 0 || r[1] >= s->Hq || r[2] < 0 || r[2] >= s->Sq) return -1;
+  }
+  problem P = {s, q, k, v, bias, kv_lens, mask, scale};
+  job J;
+  memset(&J, 0, sizeof J);
+  J.P = &P;
+  J.n_items = nrows;
+  J.rows = rows;
+  J.out = out;
+  return run(&J, nthreads);
+}

@@ -1,0 +1,78 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a private copy of the oracle's C source (a
+dropped term, a wrong sign, a wrong index or head mapping, an off-by-one mask
+edge, a swapped operand), compiles it on the CPU, and checks that at least one
+pin from test_oracle_pins fails against it. The real oracle is untouched.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_ref.c")
+
+MUTANTS = {
+    "scale_dropped": ("sj = P->scale * dot + (brow ? brow[j] : 0.0);", "sj = dot + (brow ? brow[j] : 0.0);"),
+    "bias_dropped": ("sj = P->scale * dot + (brow ? brow[j] : 0.0);", "sj = P->scale * dot;"),
+    "bias_scaled": ("sj = P->scale * dot + (brow ? brow[j] : 0.0);",
+                    "sj = P->scale * (dot + (brow ? brow[j] : 0.0));"),
+    "exp_sign": ("double p = exp(sc[j] - m);", "double p = exp(m - sc[j]);"),
+    "no_normalise": ("double wj = sc[j] / l;", "double wj = sc[j];"),
+    "k_for_v": ("o[d] += wj * vh[j * D + d];", "o[d] += wj * kh[j * D + d];"),
+    "gqa_modulo": ("const int64_t hk = hq / group;", "const int64_t hk = hq % s->Hkv;"),
+    "causal_strict": ("!(j <= i + (Sk - Sq))", "!(j < i + (Sk - Sq))"),
+    "causal_top_left": ("!(j <= i + (Sk - Sq))", "!(j <= i)"),
+    "padding_inclusive": ("int visible = j < key_limit;", "int visible = j <= key_limit;"),
+    "bias_row_index": ("brow = P->bias + ((bb * s->bias_h + bh) * Sq + i) * Sk;",
+                       "brow = P->bias + ((bb * s->bias_h + bh) * Sq + (Sq - 1 - i)) * Sk;"),
+    "bias_head_ignored": ("int64_t bh = (s->bias_h == 1) ? 0 : hq;", "int64_t bh = 0;"),
+    "q_head_index": ("const double* qi = P->q + ((b * s->Hq + hq) * Sq + i) * D;",
+                     "const double* qi = P->q + ((b * s->Hq + hk) * Sq + i) * D;"),
+}
+
+
+def _pins():
+    yield pins.test_golden_single_row_service_example
+    yield pins.test_golden_tensai_causal_mask_pattern
+    yield pins.test_hand_solved_two_by_two
+    yield pins.test_single_head_textbook_softmax
+    yield pins.test_gqa_equals_mha_with_repeated_kv_heads
+    for mask in (0, pins.CAUSAL, pins.PAD, pins.CAUSAL | pins.PAD):
+        yield lambda m=mask: pins.test_identical_keys_give_mean_of_visible_values(m)
+        yield lambda m=mask: pins.test_weights_are_row_stochastic_and_zero_where_masked(m)
+        for bshape in (None, (1, 4), (2, 1)):
+            for sq_sk in ((3, 3), (2, 5), (5, 3)):
+                yield lambda m=mask, b=bshape, s=sq_sk: pins.test_brute_force_tiny(m, b, s)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path, monkeypatch):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mut = tmp_path / "attn_mut.c"
+    mut.write_text(src.replace(old, new))
+    so = tmp_path / "libmut.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-shared", "-fPIC", "-pthread", "-o", str(so), str(mut), "-lm"],
+                   check=True)
+    oracle._load()  # make sure the real one is configured, then swap the handle's functions
+    import ctypes
+    lib = ctypes.CDLL(str(so))
+    real = oracle._lib
+    lib.oracle_attention.argtypes = real.oracle_attention.argtypes
+    lib.oracle_attention.restype = ctypes.c_int
+    lib.oracle_attention_rows.argtypes = real.oracle_attention_rows.argtypes
+    lib.oracle_attention_rows.restype = ctypes.c_int
+    monkeypatch.setattr(oracle, "_lib", lib)
+    caught = []
+    for pin in _pins():
+        try:
+            pin()
+        except AssertionError:
+            caught.append(pin)
+            break
+    assert caught, f"no pin detects the planted mistake {name!r}"
