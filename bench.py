@@ -1,0 +1,337 @@
+"""Benchmark: exact attention forward, BF16, B=4, H=32, S=4096, D=128, causal.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+One step = one attn_fwd launch over the whole workload (inputs resident in
+HBM). Prints ONE JSON line on rank 0 with the metric (TFLOP/s, FLOPs counted
+as 4*B*Hq*Sq*Sk*D halved for causal), the roofline of the kernel against the
+measured BF16 tensor peak, the end-to-end number through the public API with
+host buffers (H2D of Q/K/V and D2H of O inside the timed region), the float64
+CPU oracle timed on a bounded sample as a baseline, and the SM clocks sampled
+during the timed region.
+
+Multi-GPU (torchrun, one rank per GPU) runs independent replicas of the same
+workload: attention forward shards with no exchange, so no data-path
+collective exists; ranks only meet at barriers and a max over their times.
+``--impl reference`` times the float64 oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from exact_scaled_dot_flash_gb300 import synth  # noqa: E402
+
+WORKLOAD = "bf16_causal_4k"
+METRIC = "attention fwd TFLOP/s and % of GB300 BF16 peak (causal, S=4096, D=128)"
+KERNEL_NAME = "attn_fwd_tc_kernel"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[3], f[4:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, val in zip(names[1:], r[3][1:]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        loaded = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def make_device_inputs(w, device):
+    import torch
+    x = synth.make_inputs(w)
+
+    def dev(a, kind):
+        if a is None:
+            return None
+        if kind == "bf16":
+            t = torch.from_numpy(a.view("int16")).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(a)
+        return t.to(device)
+
+    return x, {"q": dev(x["q"], w.dtype), "k": dev(x["k"], w.dtype), "v": dev(x["v"], w.dtype),
+               "kv_lens": dev(x["kv_lens"], "i32"), "bias": dev(x["bias"], "f32")}
+
+
+def read_traffic(w):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the kernel."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{w.name}.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        from exact_scaled_dot_flash_gb300 import build
+        if d.get("kernel_source_sha") != build.kernel_source_digest():
+            return None
+        return d.get("dram_bytes_per_launch")
+    except (OSError, ValueError, AttributeError):
+        return None
+
+
+def cpu_baseline(w, x, budget_s=12.0):
+    """Float64 oracle on whole heads of the same workload, on all host cores."""
+    import numpy as np
+    import oracle
+    wid = oracle.prepare(x["q"], x["k"], x["v"], kv_lens=x["kv_lens"], bias=x["bias"], dtype=w.dtype)
+    per_head = w.flops() / (w.B * w.Hq)
+    heads = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+
+    def run(hs):
+        rows = np.array([(b, h, i) for b, h in hs for i in range(w.Sq)], dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.attention_rows(None, None, None, rows, mask=w.mask, scale=x["scale"], widened=wid)
+        return time.perf_counter() - t0
+
+    t1 = run(heads[:1])
+    n = max(1, min(len(heads) - 1, int(budget_s / max(t1, 1e-3))))
+    t = run(heads[1:1 + n])
+    return {"value": n * per_head / t / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{n} whole (batch, head) slices of {w.name} ({w.Sq} query rows each, all "
+                      f"{w.Sk} keys, causal), float64, {t:.1f} s on {os.cpu_count()} threads"}
+
+
+def bench_reference(args):
+    """Reference arm: the float64 oracle on the host cores, per-step bounded sample."""
+    import numpy as np
+    import oracle
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[WORKLOAD]
+    x = synth.make_inputs(w)
+    wid = oracle.prepare(x["q"], x["k"], x["v"], kv_lens=x["kv_lens"], bias=x["bias"], dtype=w.dtype)
+    # per step: the last `nrows` query rows of head (0, 0) -- the heaviest causal rows
+    rows_all = np.array([(0, 0, i) for i in range(w.Sq)], dtype=np.int64)
+
+    def flops_of(rows):
+        return float(sum(4.0 * (r[2] + 1) * w.D for r in rows))  # causal: row i sees i+1 keys
+
+    probe = rows_all[-64:]
+    t0 = time.perf_counter()
+    oracle.attention_rows(None, None, None, probe, mask=w.mask, scale=x["scale"], widened=wid)
+    tp = max(time.perf_counter() - t0, 1e-4)
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    nrows = int(max(16, min(w.Sq, 64 * budget / tp)))
+    rows = rows_all[-nrows:]
+    for _ in range(args.warmup):
+        oracle.attention_rows(None, None, None, rows, mask=w.mask, scale=x["scale"], widened=wid)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention_rows(None, None, None, rows, mask=w.mask, scale=x["scale"], widened=wid)
+    dt = time.perf_counter() - t0
+    value = flops_of(rows) * args.steps / dt / 1e12
+    sample = (f"the last {nrows} query rows of head (0,0) of {w.name} per step (all their visible "
+              f"keys), float64 oracle on {os.cpu_count()} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
+                       "D": w.D, "causal": True},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def bench_gpu(args):
+    import torch
+    from exact_scaled_dot_flash_gb300 import attn
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    w = synth.WORKLOADS[WORKLOAD]
+    x, t = make_device_inputs(w, device)
+    q, k, v = t["q"], t["k"], t["v"]
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(device)
+    scale = x["scale"]
+
+    def step():
+        attn.fwd(q, k, v, causal=True, scale=scale, out=out, stream=stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    attn.device_status(device.index, clear=True)
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_id = vis.split(",")[device.index] if vis else str(device.index)
+    with ClockSampler(smi_id) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    elapsed_ms = start.elapsed_time(end)
+    status = attn.device_status(device.index, clear=True)
+    if status:
+        raise RuntimeError(f"kernel status flags {status:#x} during the timed region")
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    ms = elapsed_ms / args.steps
+    flops = w.flops()
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers (pinned), copies inside
+    qh, kh, vh = (a.cpu().pin_memory() for a in (q, k, v))
+    oh = torch.empty(qh.shape, dtype=qh.dtype, pin_memory=True)
+    e2e_steps = max(3, min(20, args.steps))
+    for _ in range(2):
+        attn.fwd(qh, kh, vh, causal=True, scale=scale, out=oh)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        attn.fwd(qh, kh, vh, causal=True, scale=scale, out=oh)
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_s], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    h2d = sum(a.numel() * a.element_size() for a in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size()
+
+    if rank != 0:
+        return
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (ms * 1e-3) / 1e12
+    traffic = read_traffic(w)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
+                   "causal": True, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: Q+K+V+O = 512 MiB per step vs 129 MB L2, no flush"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_kind": f"{peak_kind} bf16 dense burst",
+                     "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                     "kernel": KERNEL_NAME},
+        "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+                "path": "attn.fwd on pinned host tensors: H2D copies, attn_fwd, D2H copy, sync"},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, x)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

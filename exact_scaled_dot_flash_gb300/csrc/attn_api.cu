@@ -1,0 +1,217 @@
+// attn_api.cu - the C ABI of libattn.so (declared in include/attn.h):
+// argument validation, per-device state, and dispatch to the kernels.
+//
+// Contract sources (page title, section): ruDNN user guide section 2 (the
+// attention entry takes query, key, value, an optional mask and an optional
+// attn_bias and returns a setup error instead of failing later) and section 9
+// (contiguous F32/F16/BF16 inputs of one dtype, Hq divisible by Hkv, a finite
+// positive scale); section 7 (statistics in FP32, output in the input dtype).
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "attn.h"
+#include "params.h"
+
+namespace {
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int kMaxDevices = 64;
+
+thread_local int g_last_cuda_error = 0;
+
+// Sticky per-device status word that kernels OR STATUS_* bits into.
+__device__ int g_status_word;
+
+struct DeviceState {
+  std::once_flag once;
+  int* status = nullptr;
+};
+DeviceState g_devices[kMaxDevices];
+
+std::once_flag g_encode_once;
+attn::EncodeTiledFn g_encode = nullptr;
+
+attn::EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qres = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &qres) == cudaSuccess &&
+        qres == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<attn::EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// Device address of g_status_word on the current device (looked up once).
+int* status_ptr(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceState& st = g_devices[dev];
+  std::call_once(st.once, [&st] {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) st.status = static_cast<int*>(p);
+  });
+  return st.status;
+}
+
+int fail_cuda(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return ATTN_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+  if (!a || !b || na <= 0 || nb <= 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + static_cast<uintptr_t>(nb) && b0 < a0 + static_cast<uintptr_t>(na);
+}
+
+int elem_size(attn_dtype_t d) { return d == ATTN_F32 ? 4 : 2; }
+
+}  // namespace
+
+extern "C" {
+
+int attn_version(void) { return kVersion; }
+
+int attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* attn_strerror(int code) {
+  switch (code) {
+    case ATTN_OK: return "success";
+    case ATTN_ERR_NULL: return "a required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "invalid shape (dims, Hq % Hkv, or bias dims)";
+    case ATTN_ERR_DTYPE: return "unknown dtype";
+    case ATTN_ERR_HEAD_DIM: return "head dim D has no compiled kernel for this dtype";
+    case ATTN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case ATTN_ERR_SCALE: return "scale must be finite and positive";
+    case ATTN_ERR_MASK: return "invalid mask_kind, or key padding without kv_lens";
+    case ATTN_ERR_OVERLAP: return "out overlaps an input";
+    case ATTN_ERR_CUDA: return "CUDA call failed";
+    case ATTN_ERR_TIMEOUT: return "a kernel wait timed out";
+    default: return "unknown status code";
+  }
+}
+
+int attn_device_status(int device, int* flags, int clear) {
+  if (!flags) return ATTN_ERR_NULL;
+  int old = 0;
+  cudaError_t e = cudaGetDevice(&old);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (device != old && (e = cudaSetDevice(device)) != cudaSuccess) return fail_cuda(e);
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int));
+  if (e == cudaSuccess && clear) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
+  }
+  if (device != old) cudaSetDevice(old);
+  if (e != cudaSuccess) return fail_cuda(e);
+  *flags = v;
+  return ATTN_OK;
+}
+
+int attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void* v,
+             int mask_kind, const int32_t* kv_lens, const float* bias, float scale,
+             attn_dtype_t dtype, void* out, void* stream) {
+  // ---- validation: everything is checked before any CUDA call
+  if (!shape) return ATTN_ERR_NULL;
+  const attn_shape_t s = *shape;
+  if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+  if (s.B < 0 || s.Sq < 0 || s.Sk < 0 || s.Hq <= 0 || s.Hkv <= 0 || s.D <= 0)
+    return ATTN_ERR_SHAPE;
+  if (s.Hq % s.Hkv != 0) return ATTN_ERR_SHAPE;
+  if (mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_KEY_PADDING)) return ATTN_ERR_MASK;
+  if ((mask_kind & ATTN_MASK_KEY_PADDING) && !kv_lens) return ATTN_ERR_MASK;
+  if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_SCALE;
+  if (bias && !((s.bias_b == 1 || s.bias_b == s.B) && (s.bias_h == 1 || s.bias_h == s.Hq)))
+    return ATTN_ERR_SHAPE;
+  const bool tensor_core = dtype != ATTN_F32;
+  if (tensor_core ? !(s.D == 32 || s.D == 64 || s.D == 128)
+                  : !(s.D == 16 || s.D == 32 || s.D == 64 || s.D == 128))
+    return ATTN_ERR_HEAD_DIM;
+  // grid limits: x = B*Hq (< 2^31), y = query blocks (<= 65535)
+  const int64_t bhq = static_cast<int64_t>(s.B) * s.Hq;
+  const int64_t bhk = static_cast<int64_t>(s.B) * s.Hkv;
+  if (bhq > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  const int rows_per_cta = tensor_core ? 256 : 64;
+  if ((static_cast<int64_t>(s.Sq) + rows_per_cta - 1) / rows_per_cta > 65535) return ATTN_ERR_SHAPE;
+  if (s.B == 0 || s.Sq == 0) return ATTN_OK;  // nothing to compute
+  if (!q || !out || (s.Sk > 0 && (!k || !v))) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_ALIGN;
+  if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return ATTN_ERR_ALIGN;
+  if (kv_lens && (reinterpret_cast<uintptr_t>(kv_lens) & 3u)) return ATTN_ERR_ALIGN;
+  const int es = elem_size(dtype);
+  const int64_t out_bytes = bhq * s.Sq * s.D * es;
+  const int64_t kv_bytes = bhk * s.Sk * s.D * es;
+  const int64_t bias_bytes =
+      bias ? static_cast<int64_t>(s.bias_b) * s.bias_h * s.Sq * static_cast<int64_t>(s.Sk) * 4 : 0;
+  if (overlaps(out, out_bytes, q, out_bytes) || overlaps(out, out_bytes, k, kv_bytes) ||
+      overlaps(out, out_bytes, v, kv_bytes) || overlaps(out, out_bytes, bias, bias_bytes) ||
+      overlaps(out, out_bytes, kv_lens, static_cast<int64_t>(s.B) * 4))
+    return ATTN_ERR_OVERLAP;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (s.Sk == 0) {  // no key at all: every row is undefined
+    cudaError_t e = attn::launch_nan_fill(out, bhq * s.Sq * s.D,
+                                          dtype == ATTN_F32 ? 4 : (dtype == ATTN_F16 ? 2 : 3), st);
+    return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+  }
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+
+  attn::KernelParams p;
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.Sq = s.Sq;
+  p.Sk = s.Sk;
+  p.group = s.Hq / s.Hkv;
+  p.causal = (mask_kind & ATTN_MASK_CAUSAL) ? 1 : 0;
+  p.padding = (mask_kind & ATTN_MASK_KEY_PADDING) ? 1 : 0;
+  p.kv_lens = p.padding ? kv_lens : nullptr;
+  p.bias = bias;
+  p.bias_b = bias ? s.bias_b : 1;
+  p.bias_h = bias ? s.bias_h : 1;
+  p.bias_vec4 = bias && aligned16(bias) && (s.Sk % 4 == 0);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = status_ptr(dev);
+
+  if (!tensor_core) {
+    int unsupported = 0;
+    e = attn::launch_f32(s.D, bias != nullptr, p, static_cast<const float*>(q),
+                         static_cast<const float*>(k), static_cast<const float*>(v),
+                         static_cast<float*>(out), st, &unsupported);
+    if (unsupported) return ATTN_ERR_HEAD_DIM;
+    return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+  }
+
+  attn::EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail_cuda(cudaErrorNotSupported);
+  const bool bf16 = dtype == ATTN_BF16;
+  const bool hb = bias != nullptr;
+  using namespace attn::tc;
+#define ATTN_TC_DISPATCH(DD)                                                                   \
+  case DD:                                                                                     \
+    e = bf16 ? (hb ? launch_tc_instance<DD, true, true>(enc, q, k, v, out, p, st)              \
+                   : launch_tc_instance<DD, true, false>(enc, q, k, v, out, p, st))            \
+             : (hb ? launch_tc_instance<DD, false, true>(enc, q, k, v, out, p, st)             \
+                   : launch_tc_instance<DD, false, false>(enc, q, k, v, out, p, st));          \
+    break;
+  switch (s.D) {
+    ATTN_TC_DISPATCH(32)
+    ATTN_TC_DISPATCH(64)
+    ATTN_TC_DISPATCH(128)
+    default:
+      return ATTN_ERR_HEAD_DIM;
+  }
+#undef ATTN_TC_DISPATCH
+  return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+}
+
+}  // extern "C"

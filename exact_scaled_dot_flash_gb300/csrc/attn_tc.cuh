@@ -1,0 +1,497 @@
+// attn_tc.cuh - exact attention forward on the 5th-generation tensor cores
+// (tcgen05) of sm_103a, F16/BF16 inputs, fp32 statistics and accumulation.
+//
+// Algorithm: the tiled, single-pass exact attention that the FlashAttention
+// paper describes (cited by "HOF cognitive Flash Attention in Rust", sections
+// 2 and 4, as computing the same exact result as the dense kernel without the
+// n x n score matrix in HBM): for each query tile, stream K/V tiles, keep a
+// running row maximum m and row sum l, rescale the output accumulator when m
+// grows, and divide by l at the end. The scores never leave the SM.
+//
+// One CTA owns NQ = 2 query tiles of BM = 128 rows of one (batch, query head)
+// and streams the key/value tiles they need once for both:
+//   warp 8      TMA producer: Q tiles once, then K_j, V_j into a ring of
+//               STAGES shared-memory slots (mbarrier full/empty pairs);
+//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory
+//               (SS form), then O_t += P_t V_j with P_t read from tensor
+//               memory (TS form); allocates/frees the 512 TMEM columns;
+//   warps 0-7   two softmax warpgroups, one per query tile: thread r owns
+//               TMEM lane r = query row r. Each pulls its 128 scores of the
+//               tile with tcgen05.ld, applies scale, bias and mask, updates m
+//               and l, writes P (16-bit) back into tensor memory, rescales
+//               its O row when m grew, and finally normalises O, stages it
+//               in shared memory and stores it with TMA.
+// Tensor-memory map (fp32 columns): S_0 [0,128), S_1 [128,256), O_0 at 256,
+// O_1 at 256 + D; P_t aliases the upper half of S_t (the MMA that next
+// overwrites S_t is issued after the PV MMA that reads P_t, and tcgen05 MMAs
+// from one thread execute in issue order).
+// Every mbarrier wait is bounded; on expiry the CTA records STATUS_TIMEOUT in
+// the device status word, drains its own copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include "params.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace tc {
+
+constexpr int BM = 128;           // query rows per Q tile = TMEM lanes
+constexpr int BN = 128;           // keys per K/V tile
+constexpr int NQ = 2;             // Q tiles per CTA
+constexpr int NUM_THREADS = 320;  // 8 softmax warps + TMA warp + MMA warp
+constexpr int WARP_TMA = 8;
+constexpr int WARP_MMA = 9;
+constexpr int TMEM_COLS = 512;
+constexpr float LOG2E = 1.4426950408889634f;
+
+template <int D>
+struct Cfg {
+  static_assert(D == 32 || D == 64 || D == 128, "compiled head dims are 32, 64, 128");
+  static constexpr int SWIZZLE = D >= 64 ? 128 : 64;  // bytes per swizzled smem row
+  static constexpr int BOX_D = SWIZZLE / 2;           // 16-bit elements per TMA box row
+  static constexpr int NCHUNK = D / BOX_D;            // boxes per tile along D
+  static constexpr int ROW_BYTES = SWIZZLE;
+  static constexpr int CHUNK_BYTES = BN * ROW_BYTES;  // one box: 128 rows
+  static constexpr int TILE_BYTES = NCHUNK * CHUNK_BYTES;
+  static constexpr int STAGES = D == 128 ? 4 : (D == 64 ? 8 : 12);
+  static constexpr uint32_t LAYOUT = SWIZZLE == 128 ? 2u : 4u;  // UMMA swizzle code
+  static constexpr int SBO = 8 * ROW_BYTES;                      // 8-row group stride
+  static constexpr int KSTEPS_QK = D / 16;
+  static constexpr int KSTEPS_PER_CHUNK = BOX_D / 16;
+  static constexpr int KSTEPS_PV = BN / 16;
+  static constexpr int COL_P = 64;  // P_t at S_t + 64 (16-bit pairs, 64 columns)
+  static constexpr int OFF_KV = NQ * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + STAGES * TILE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 * NQ + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  // +1024 for aligning the dynamic window; at least 120 KB so that one CTA
+  // (which takes all 512 TMEM columns) is resident per SM.
+  static constexpr int SMEM_BYTES =
+      (SMEM_USED + 1024) > 120 * 1024 ? (SMEM_USED + 1024) : 120 * 1024;
+  static constexpr int BAR_FULL = 0;
+  static constexpr int BAR_EMPTY = STAGES;
+  static constexpr int BAR_Q = 2 * STAGES;
+  static constexpr int BAR_S = BAR_Q + NQ;
+  static constexpr int BAR_P = BAR_S + NQ;
+  static constexpr int BAR_O = BAR_P + NQ;
+  static constexpr int BAR_DONE = BAR_O + NQ;
+};
+
+// Per-CTA work description, computed identically by every thread.
+struct Work {
+  int b, hq, bh, bhk, q0;
+  int key_limit;   // keys >= key_limit are padding (<= Sk)
+  int diag;        // Sk - Sq: causal offset (bottom-right alignment)
+  int n[NQ];       // K/V tiles Q tile t needs (0: no visible key at all)
+  int nfull[NQ];   // leading K/V tiles of Q tile t with no masked element
+  int nmax;
+};
+
+__device__ __forceinline__ Work make_work(const KernelParams& p) {
+  Work w;
+  w.bh = blockIdx.x;
+  w.b = w.bh / p.Hq;
+  w.hq = w.bh - w.b * p.Hq;
+  w.bhk = w.b * p.Hkv + w.hq / p.group;
+  const int qb = p.causal ? (gridDim.y - 1 - blockIdx.y) : blockIdx.y;  // heavy tiles first
+  w.q0 = qb * (NQ * BM);
+  w.diag = p.Sk - p.Sq;
+  int lim = p.Sk;
+  if (p.padding) {
+    int L = __ldg(p.kv_lens + w.b);
+    lim = L < 0 ? 0 : (L > p.Sk ? p.Sk : L);
+  }
+  w.key_limit = lim;
+  w.nmax = 0;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    const int r0 = w.q0 + t * BM;
+    w.n[t] = 0;
+    w.nfull[t] = 0;
+    if (r0 < p.Sq) {
+      const int rlast = min(r0 + BM - 1, p.Sq - 1);
+      int hi = lim;   // keys [0, hi) are visible to some row of the tile
+      int lo = lim;   // keys [0, lo) are visible to every row of the tile
+      if (p.causal) {
+        hi = min(hi, rlast + w.diag + 1);
+        lo = min(lo, r0 + w.diag + 1);
+      }
+      w.n[t] = hi > 0 ? (hi + BN - 1) / BN : 0;
+      w.nfull[t] = lo > 0 ? lo / BN : 0;
+    }
+    w.nmax = max(w.nmax, w.n[t]);
+  }
+  return w;
+}
+
+template <int D, bool BF16, bool BIAS>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_o, const KernelParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Work w = make_work(p);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar(C::BAR_FULL + s), 1);
+      mbar_init(bar(C::BAR_EMPTY + s), 1);
+    }
+    for (int t = 0; t < NQ; ++t) {
+      mbar_init(bar(C::BAR_Q + t), 1);
+      mbar_init(bar(C::BAR_S + t), 1);
+      mbar_init(bar(C::BAR_P + t), BM);
+      mbar_init(bar(C::BAR_O + t), 1);
+    }
+    mbar_init(bar(C::BAR_DONE), 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    if (p.status) atomicOr(p.status, STATUS_TIMEOUT);
+  };
+
+  if (warp == WARP_TMA) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_o);
+      for (int t = 0; t < NQ; ++t) {
+        if (w.n[t] == 0) continue;
+        mbar_arrive_expect_tx(bar(C::BAR_Q + t), C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(sb + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::BAR_Q + t),
+                      c * C::BOX_D, w.q0 + t * BM, w.bh);
+      }
+      int it = 0;
+      for (int j = 0; j < w.nmax && !*abort_flag; ++j) {
+        for (int kv = 0; kv < 2; ++kv, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          if (!mbar_wait(bar(C::BAR_EMPTY + s), ph ^ 1)) {
+            fail();
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::BAR_FULL + s), C::TILE_BYTES);
+          const CUtensorMap* m = kv == 0 ? &tm_k : &tm_v;
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d(sb + C::OFF_KV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, m,
+                        bar(C::BAR_FULL + s), c * C::BOX_D, j * BN, w.bhk);
+        }
+      }
+      // Drain: every copy this thread issued has landed before the CTA exits.
+      for (int s = 0; s < C::STAGES && s < it; ++s) {
+        const int fills = (it - s + C::STAGES - 1) / C::STAGES;
+        if (!mbar_wait(bar(C::BAR_FULL + s), (fills - 1) & 1)) fail();
+      }
+      for (int t = 0; t < NQ; ++t)
+        if (w.n[t] > 0 && !mbar_wait(bar(C::BAR_Q + t), 0)) fail();
+    }
+    __syncwarp();
+  } else if (warp == WARP_MMA) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = make_idesc_f16(BF16, BM, BN, false);
+      constexpr uint32_t idesc_pv = make_idesc_f16(BF16, BM, D, true);
+      bool ok = true;
+      for (int t = 0; t < NQ && ok; ++t)
+        if (w.n[t] > 0 && !mbar_wait(bar(C::BAR_Q + t), 0)) ok = false;
+      int it = 0;
+      for (int j = 0; j < w.nmax && ok && !*abort_flag; ++j) {
+        // S_t = Q_t K_j^T
+        {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          ++it;
+          if (!mbar_wait(bar(C::BAR_FULL + s), ph)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kbase = sb + C::OFF_KV + s * C::TILE_BYTES;
+          for (int t = 0; t < NQ; ++t) {
+            if (j >= w.n[t]) continue;
+            const uint32_t qbase = sb + t * C::TILE_BYTES;
+#pragma unroll
+            for (int k = 0; k < C::KSTEPS_QK; ++k) {
+              const uint32_t off = (k / C::KSTEPS_PER_CHUNK) * C::CHUNK_BYTES +
+                                   (k % C::KSTEPS_PER_CHUNK) * 32;
+              umma_ss(tmem + t * BN, smem_desc(qbase + off, 16, C::SBO, C::LAYOUT),
+                      smem_desc(kbase + off, 16, C::SBO, C::LAYOUT), idesc_qk, k > 0);
+            }
+            umma_commit(bar(C::BAR_S + t));
+          }
+          umma_commit(bar(C::BAR_EMPTY + s));
+        }
+        // O_t += P_t V_j
+        {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          ++it;
+          if (!mbar_wait(bar(C::BAR_FULL + s), ph)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t vbase = sb + C::OFF_KV + s * C::TILE_BYTES;
+          for (int t = 0; t < NQ; ++t) {
+            if (j >= w.n[t]) continue;
+            if (!mbar_wait(bar(C::BAR_P + t), j & 1)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < C::KSTEPS_PV; ++k) {
+              umma_ts(tmem + 256 + t * D, tmem + t * BN + C::COL_P + k * 8,
+                      smem_desc(vbase + k * 16 * C::ROW_BYTES, C::CHUNK_BYTES, C::SBO, C::LAYOUT),
+                      idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+            }
+            if (j == w.n[t] - 1) umma_commit(bar(C::BAR_O + t));
+          }
+          umma_commit(bar(C::BAR_EMPTY + s));
+          if (!ok) break;
+        }
+      }
+      if (!ok) fail();
+      // Drain: all MMAs issued above have completed before TMEM is freed.
+      umma_commit(bar(C::BAR_DONE));
+      if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- softmax
+    const int t = warp >> 2;                 // query tile of this warpgroup
+    const int row = ((warp & 3) << 5) + lane;  // TMEM lane = row within the tile
+    const int r0 = w.q0 + t * BM;
+    const int row_g = r0 + row;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    const uint32_t tS = tmem + lane_off + t * BN;
+    const uint32_t tP = tS + C::COL_P;
+    const uint32_t tO = tmem + lane_off + 256 + t * D;
+    const int n_t = w.n[t];
+    const int nfull_t = w.nfull[t];
+
+    const float* brow = nullptr;
+    if constexpr (BIAS) {
+      if (row_g < p.Sq) {
+        const int bb = p.bias_b == 1 ? 0 : w.b;
+        const int bh = p.bias_h == 1 ? 0 : w.hq;
+        brow = p.bias + ((static_cast<size_t>(bb) * p.bias_h + bh) * p.Sq + row_g) *
+                            static_cast<size_t>(p.Sk);
+      }
+    }
+    const int causal_lim = p.causal ? row_g + w.diag : 0x7fffffff;  // last visible key
+    const int key_lim = w.key_limit;
+
+    float m_run = -INFINITY;  // running max of scaled scores (log2 domain)
+    float l_run = 0.f;        // running sum of 2^(s - m_run)
+    bool failed = false;
+
+    for (int j = 0; j < n_t; ++j) {
+      const bool ok = mbar_wait(bar(C::BAR_S + t), j & 1);
+      if (__any_sync(0xffffffffu, !ok)) { failed = true; break; }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
+      tmem_wait_ld();
+      float s[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
+
+      const int key0 = j * BN;
+      if constexpr (BIAS) {
+        // scores -> log2 domain with the bias folded in
+        if (brow != nullptr) {
+          const float* bp = brow + key0;
+          if (j < nfull_t && p.bias_vec4) {
+#pragma unroll
+            for (int i = 0; i < 128; i += 4) {
+              const float4 b4 = __ldg(reinterpret_cast<const float4*>(bp + i));
+              s[i + 0] = fmaf(s[i + 0], p.scale_log2, b4.x * LOG2E);
+              s[i + 1] = fmaf(s[i + 1], p.scale_log2, b4.y * LOG2E);
+              s[i + 2] = fmaf(s[i + 2], p.scale_log2, b4.z * LOG2E);
+              s[i + 3] = fmaf(s[i + 3], p.scale_log2, b4.w * LOG2E);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 128; ++i) {
+              const float bv = (key0 + i < key_lim) ? __ldg(bp + i) : 0.f;
+              s[i] = fmaf(s[i], p.scale_log2, bv * LOG2E);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) s[i] *= p.scale_log2;
+        }
+      }
+      if (j >= nfull_t) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          const int key = key0 + i;
+          if (key >= key_lim || key > causal_lim) s[i] = -INFINITY;
+        }
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      const float m_tile = BIAS ? mx : mx * p.scale_log2;
+      const float m_new = fmaxf(m_run, m_tile);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = fast_exp2(m_run - m_use);
+      float sum = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float x0 = s[64 * h + 2 * c], x1 = s[64 * h + 2 * c + 1];
+          const float p0 = fast_exp2(BIAS ? x0 - m_use : fmaf(x0, p.scale_log2, -m_use));
+          const float p1 = fast_exp2(BIAS ? x1 - m_use : fmaf(x1, p.scale_log2, -m_use));
+          sum += p0 + p1;
+          pk[c] = pack2<BF16>(p0, p1);
+        }
+        tmem_st32(tP + 32 * h, pk);
+      }
+      l_run = l_run * alpha + sum;
+      m_run = m_new;
+      // O_t was last written by the PV MMA of tile j-1, which completed before
+      // S_t of tile j was signalled; rescale it before PV of tile j is issued.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + 32 * c, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::BAR_P + t));
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    // Every warp of the warpgroup reaches the named barrier, failed or not, so
+    // that a timeout in one warp can never leave the others waiting on it.
+    if (r0 < p.Sq) {
+      const bool have = n_t > 0;
+      if (!failed && have) {
+        const bool ok = mbar_wait(bar(C::BAR_O + t), 0);
+        if (__any_sync(0xffffffffu, !ok)) failed = true;
+      }
+      if (failed) {
+        if (lane == 0) fail();
+      } else {
+        tc_fence_after();
+        // rows with no visible key have an undefined softmax: NaN
+        const float inv = (have && l_run > 0.f) ? 1.f / l_run : __int_as_float(0x7fc00000);
+        uint8_t* stage = smem + t * C::TILE_BYTES;  // Q_t is dead: reuse it for O_t
+        const int swz = C::SWIZZLE == 128 ? (row & 7) : ((row >> 1) & 3);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          if (have) {
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+          const int col0 = 32 * c;
+          const int box = col0 / C::BOX_D;
+          const int ch0 = ((col0 % C::BOX_D) * 2) / 16;
+          uint8_t* rowp = stage + box * C::CHUNK_BYTES + row * C::ROW_BYTES;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int ch = (ch0 + u) ^ swz;
+            *reinterpret_cast<uint4*>(rowp + ch * 16) =
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(1 + t, BM);
+      if (row == 0 && !*abort_flag) {
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_store_3d(&tm_o, sb + t * C::TILE_BYTES + c * C::CHUNK_BYTES, c * C::BOX_D, r0,
+                       w.bh);
+        tma_store_commit();
+        tma_store_wait_all();
+      }
+    } else if (failed && lane == 0) {
+      fail();
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// Host side: encode the four 3-D tensor maps and launch. Q/O are viewed as
+// [B*Hq, Sq, D] and K/V as [B*Hkv, Sk, D] (x = D innermost), so a box that
+// runs past S is zero-filled on load and clipped on store, per head.
+template <int D>
+static CUresult encode_3d(EncodeTiledFn enc, CUtensorMap* m, bool bf16, const void* ptr,
+                          uint64_t S, uint64_t BH) {
+  using C = Cfg<D>;
+  const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(D), S, BH};
+  const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(D) * 2, S * D * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(C::BOX_D), static_cast<cuuint32_t>(BM), 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+             const_cast<void*>(ptr), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             C::SWIZZLE == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <int D, bool BF16, bool BIAS>
+cudaError_t launch_tc_instance(EncodeTiledFn enc, const void* q, const void* k, const void* v,
+                               void* out, const KernelParams& p, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, to;
+  const uint64_t bhq = static_cast<uint64_t>(p.B) * p.Hq, bhk = static_cast<uint64_t>(p.B) * p.Hkv;
+  if (encode_3d<D>(enc, &tq, BF16, q, p.Sq, bhq) != CUDA_SUCCESS ||
+      encode_3d<D>(enc, &tk, BF16, k, p.Sk, bhk) != CUDA_SUCCESS ||
+      encode_3d<D>(enc, &tv, BF16, v, p.Sk, bhk) != CUDA_SUCCESS ||
+      encode_3d<D>(enc, &to, BF16, out, p.Sq, bhq) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  auto kern = attn_fwd_tc_kernel<D, BF16, BIAS>;
+  constexpr int smem = Cfg<D>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const unsigned qblocks = static_cast<unsigned>((p.Sq + NQ * BM - 1) / (NQ * BM));
+  dim3 grid(static_cast<unsigned>(bhq), qblocks);
+  kern<<<grid, NUM_THREADS, smem, stream>>>(tq, tk, tv, to, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+}  // namespace attn
