@@ -221,15 +221,16 @@ def bench_gpu(args):
     else:
         torch.cuda.set_device(0)
     device = torch.device("cuda", torch.cuda.current_device())
-    w = synth.WORKLOADS[WORKLOAD]
+    w = synth.WORKLOADS[args.workload]
     x, t = make_device_inputs(w, device)
-    q, k, v = t["q"], t["k"], t["v"]
+    q, k, v, lens, bias = t["q"], t["k"], t["v"], t["kv_lens"], t["bias"]
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(device)
     scale = x["scale"]
+    causal = w.causal
 
     def step():
-        attn.fwd(q, k, v, causal=True, scale=scale, out=out, stream=stream)
+        attn.fwd(q, k, v, causal=causal, kv_lens=lens, bias=bias, scale=scale, out=out, stream=stream)
 
     def barrier():
         if world > 1:
@@ -267,25 +268,35 @@ def bench_gpu(args):
     value = world * flops / (ms * 1e-3) / 1e12
 
     # end to end through the public API with host buffers (pinned), copies inside
-    qh, kh, vh = (a.cpu().pin_memory() for a in (q, k, v))
-    oh = torch.empty(qh.shape, dtype=qh.dtype, pin_memory=True)
-    e2e_steps = max(3, min(20, args.steps))
-    for _ in range(2):
-        attn.fwd(qh, kh, vh, causal=True, scale=scale, out=oh)
-    barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        attn.fwd(qh, kh, vh, causal=True, scale=scale, out=oh)
-    torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_s], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
-    h2d = sum(a.numel() * a.element_size() for a in (qh, kh, vh))
-    d2h = oh.numel() * oh.element_size()
+    e2e = None
+    if not args.no_e2e:
+        hosts = [None if a is None else a.cpu().pin_memory() for a in (q, k, v, lens, bias)]
+        qh, kh, vh, lh, bh = hosts
+        oh = torch.empty(qh.shape, dtype=qh.dtype, pin_memory=True)
+        e2e_steps = max(3, min(20, args.steps))
+
+        def e2e_step():
+            attn.fwd(qh, kh, vh, causal=causal, kv_lens=lh, bias=bh, scale=scale, out=oh)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        if world > 1:
+            import torch.distributed as dist
+            tt = torch.tensor([e2e_s], device=device)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_s = float(tt.item())
+        h2d = sum(a.numel() * a.element_size() for a in hosts if a is not None)
+        d2h = oh.numel() * oh.element_size()
+        e2e = {"value": world * w.flops() / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+               "path": "attn.fwd on pinned host tensors: H2D copies, attn_fwd, D2H copy, sync"}
 
     if rank != 0:
         return
@@ -293,25 +304,29 @@ def bench_gpu(args):
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (ms * 1e-3) / 1e12
     traffic = read_traffic(w)
+    hbm_gbs = w.io_bytes() / (ms * 1e-3) / 1e9
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if w.name == WORKLOAD else f"attention fwd TFLOP/s ({w.name})", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
-                   "causal": True, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2: Q+K+V+O = 512 MiB per step vs 129 MB L2, no flush"},
+                   "causal": w.causal, "key_padding": bool(w.mask & synth.MASK_KEY_PADDING),
+                   "bias": [w.bias_b, w.bias_h] if w.bias else None, "parallelism": f"replicas x{world}",
+                   "l2": (f"inputs larger than L2: {w.io_bytes() / 2**20:.0f} MiB per step vs 129 MB L2, no flush"
+                          if w.io_bytes() > 129e6 else
+                          f"working set {w.io_bytes() / 2**20:.1f} MiB fits in L2 (L2-hot steps)")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_kind": f"{peak_kind} bf16 dense burst",
                      "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
-                     "kernel": KERNEL_NAME},
-        "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
-                "path": "attn.fwd on pinned host tensors: H2D copies, attn_fwd, D2H copy, sync"},
+                     "kernel": KERNEL_NAME if w.dtype != "f32" else "attn_fwd_f32_kernel",
+                     "hbm_gbs_algorithmic": hbm_gbs,
+                     "hbm_frac": hbm_gbs / float(peaks["hbm_gbs"])},
+        "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and w.name == WORKLOAD:
         line["cpu_baseline"] = cpu_baseline(w, x)
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -322,10 +337,12 @@ def bench_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     args = ap.parse_args()
     if args.impl == "reference":
         bench_reference(args)

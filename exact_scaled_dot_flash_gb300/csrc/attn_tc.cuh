@@ -9,22 +9,30 @@
 // grows, and divide by l at the end. The scores never leave the SM.
 //
 // One CTA owns NQ = 2 query tiles of BM = 128 rows of one (batch, query head)
-// and streams the key/value tiles they need once for both:
-//   warp 8      TMA producer: Q tiles once, then K_j, V_j into a ring of
-//               STAGES shared-memory slots (mbarrier full/empty pairs);
-//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory
-//               (SS form), then O_t += P_t V_j with P_t read from tensor
-//               memory (TS form); allocates/frees the 512 TMEM columns;
-//   warps 0-7   two softmax warpgroups, one per query tile: thread r owns
-//               TMEM lane r = query row r. Each pulls its 128 scores of the
-//               tile with tcgen05.ld, applies scale, bias and mask, updates m
-//               and l, writes P (16-bit) back into tensor memory, rescales
-//               its O row when m grew, and finally normalises O, stages it
-//               in shared memory and stores it with TMA.
+// and streams the key/value tiles they need once for both. 384 threads:
+//   warpgroup 0, 1  softmax for query tile 0 / 1: thread r owns TMEM lane r =
+//                   query row r. It pulls its 128 scores of the tile with
+//                   tcgen05.ld, applies scale, bias and mask, keeps m and l
+//                   in registers, writes P (16-bit) back into tensor memory,
+//                   rescales its O row when needed, and in the end normalises
+//                   O, stages it in shared memory and stores it with TMA.
+//   warp 8          TMA producer: Q tiles once, then K_j, V_j in order into a
+//                   ring of STAGES shared-memory slots (full/empty mbarriers).
+//   warp 9          MMA issuer (one thread); allocates the 512 TMEM columns.
+//   warps 10, 11    idle (they complete the third warpgroup, whose registers
+//                   are handed to the softmax warpgroups with setmaxnreg).
+// MMA issue order per K/V tile j:  S_0(j), PV_1(j-1), S_1(j), PV_0(j), with
+// S_t = Q_t K_j^T (SS form) and O_t += P_t V_j (P_t read from tensor memory,
+// TS form). Softmax t therefore has two MMA slots (the other tile's PV and S)
+// to turn S_t into P_t before the tensor core needs it.
 // Tensor-memory map (fp32 columns): S_0 [0,128), S_1 [128,256), O_0 at 256,
-// O_1 at 256 + D; P_t aliases the upper half of S_t (the MMA that next
-// overwrites S_t is issued after the PV MMA that reads P_t, and tcgen05 MMAs
-// from one thread execute in issue order).
+// O_1 at 256 + D; P_t (16-bit pairs) aliases columns [64,128) of S_t. The MMA
+// that next overwrites S_t is issued after the PV MMA that reads P_t, and
+// tcgen05 MMAs from one thread execute in issue order.
+// Rescaling is lazy: a row's reference maximum moves only when the tile max
+// exceeds it by more than 2^8; probabilities are then at most 256, well inside
+// the 16-bit and fp32 ranges, and the final O / l uses the same reference, so
+// the result is unchanged.
 // Every mbarrier wait is bounded; on expiry the CTA records STATUS_TIMEOUT in
 // the device status word, drains its own copies and MMAs, frees TMEM and exits.
 #pragma once
@@ -38,11 +46,15 @@ namespace tc {
 constexpr int BM = 128;           // query rows per Q tile = TMEM lanes
 constexpr int BN = 128;           // keys per K/V tile
 constexpr int NQ = 2;             // Q tiles per CTA
-constexpr int NUM_THREADS = 320;  // 8 softmax warps + TMA warp + MMA warp
+constexpr int NUM_THREADS = 384;  // 2 softmax warpgroups + producer/MMA warpgroup
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 constexpr int TMEM_COLS = 512;
+constexpr int REG_SOFTMAX = 216;  // 2*128*216 + 128*56 <= 384 * 168 (launch allocation)
+constexpr int REG_OTHER = 56;
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr float RESCALE_LOG2 = 8.0f;  // lazy-rescale threshold (log2 units)
+constexpr int HEAD_GROUP = 16;        // heads scheduled together so their K/V stay in L2
 
 template <int D>
 struct Cfg {
@@ -88,13 +100,24 @@ struct Work {
   int nmax;
 };
 
+// Linear CTA index -> (head, query block). Heads are taken HEAD_GROUP at a
+// time; inside a group the query blocks of all its heads are interleaved,
+// heaviest causal block first, so the K/V of the heads in flight stay in L2
+// and the long blocks start before the short ones.
 __device__ __forceinline__ Work make_work(const KernelParams& p) {
   Work w;
-  w.bh = blockIdx.x;
+  const int qblocks = (p.Sq + NQ * BM - 1) / (NQ * BM);
+  const int bhq = p.B * p.Hq;
+  const int per_group = qblocks * HEAD_GROUP;
+  const int g = static_cast<int>(blockIdx.x) / per_group;
+  const int within = static_cast<int>(blockIdx.x) - g * per_group;
+  const int hg = min(HEAD_GROUP, bhq - g * HEAD_GROUP);
+  const int rank = within / hg;
+  w.bh = g * HEAD_GROUP + (within - rank * hg);
+  const int qb = p.causal ? (qblocks - 1 - rank) : rank;
   w.b = w.bh / p.Hq;
   w.hq = w.bh - w.b * p.Hq;
   w.bhk = w.b * p.Hkv + w.hq / p.group;
-  const int qb = p.causal ? (gridDim.y - 1 - blockIdx.y) : blockIdx.y;  // heavy tiles first
   w.q0 = qb * (NQ * BM);
   w.diag = p.Sk - p.Sq;
   int lim = p.Sk;
@@ -173,110 +196,114 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (p.status) atomicOr(p.status, STATUS_TIMEOUT);
   };
 
-  if (warp == WARP_TMA) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_o);
-      for (int t = 0; t < NQ; ++t) {
-        if (w.n[t] == 0) continue;
-        mbar_arrive_expect_tx(bar(C::BAR_Q + t), C::TILE_BYTES);
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(sb + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::BAR_Q + t),
-                      c * C::BOX_D, w.q0 + t * BM, w.bh);
-      }
-      int it = 0;
-      for (int j = 0; j < w.nmax && !*abort_flag; ++j) {
-        for (int kv = 0; kv < 2; ++kv, ++it) {
-          const int s = it % C::STAGES;
-          const uint32_t ph = (it / C::STAGES) & 1;
-          if (!mbar_wait(bar(C::BAR_EMPTY + s), ph ^ 1)) {
-            fail();
-            break;
-          }
-          mbar_arrive_expect_tx(bar(C::BAR_FULL + s), C::TILE_BYTES);
-          const CUtensorMap* m = kv == 0 ? &tm_k : &tm_v;
+  if (warp >= 2 * 4) {
+    setmaxnreg_dec<REG_OTHER>();
+    if (warp == WARP_TMA) {
+      // -------------------------------------------------------------- producer
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_o);
+        for (int t = 0; t < NQ; ++t) {
+          if (w.n[t] == 0) continue;
+          mbar_arrive_expect_tx(bar(C::BAR_Q + t), C::TILE_BYTES);
           for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_3d(sb + C::OFF_KV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, m,
-                        bar(C::BAR_FULL + s), c * C::BOX_D, j * BN, w.bhk);
+            tma_load_3d(sb + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::BAR_Q + t),
+                        c * C::BOX_D, w.q0 + t * BM, w.bh);
         }
-      }
-      // Drain: every copy this thread issued has landed before the CTA exits.
-      for (int s = 0; s < C::STAGES && s < it; ++s) {
-        const int fills = (it - s + C::STAGES - 1) / C::STAGES;
-        if (!mbar_wait(bar(C::BAR_FULL + s), (fills - 1) & 1)) fail();
-      }
-      for (int t = 0; t < NQ; ++t)
-        if (w.n[t] > 0 && !mbar_wait(bar(C::BAR_Q + t), 0)) fail();
-    }
-    __syncwarp();
-  } else if (warp == WARP_MMA) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc_f16(BF16, BM, BN, false);
-      constexpr uint32_t idesc_pv = make_idesc_f16(BF16, BM, D, true);
-      bool ok = true;
-      for (int t = 0; t < NQ && ok; ++t)
-        if (w.n[t] > 0 && !mbar_wait(bar(C::BAR_Q + t), 0)) ok = false;
-      int it = 0;
-      for (int j = 0; j < w.nmax && ok && !*abort_flag; ++j) {
-        // S_t = Q_t K_j^T
-        {
-          const int s = it % C::STAGES;
-          const uint32_t ph = (it / C::STAGES) & 1;
-          ++it;
-          if (!mbar_wait(bar(C::BAR_FULL + s), ph)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t kbase = sb + C::OFF_KV + s * C::TILE_BYTES;
-          for (int t = 0; t < NQ; ++t) {
-            if (j >= w.n[t]) continue;
-            const uint32_t qbase = sb + t * C::TILE_BYTES;
-#pragma unroll
-            for (int k = 0; k < C::KSTEPS_QK; ++k) {
-              const uint32_t off = (k / C::KSTEPS_PER_CHUNK) * C::CHUNK_BYTES +
-                                   (k % C::KSTEPS_PER_CHUNK) * 32;
-              umma_ss(tmem + t * BN, smem_desc(qbase + off, 16, C::SBO, C::LAYOUT),
-                      smem_desc(kbase + off, 16, C::SBO, C::LAYOUT), idesc_qk, k > 0);
+        int it = 0;  // ring position: K_j at 2j, V_j at 2j + 1
+        for (int j = 0; j < w.nmax && !*abort_flag; ++j) {
+          for (int kv = 0; kv < 2; ++kv, ++it) {
+            const int s = it % C::STAGES;
+            const uint32_t ph = (it / C::STAGES) & 1;
+            if (!mbar_wait(bar(C::BAR_EMPTY + s), ph ^ 1)) {
+              fail();
+              break;
             }
-            umma_commit(bar(C::BAR_S + t));
+            mbar_arrive_expect_tx(bar(C::BAR_FULL + s), C::TILE_BYTES);
+            const CUtensorMap* m = kv == 0 ? &tm_k : &tm_v;
+            for (int c = 0; c < C::NCHUNK; ++c)
+              tma_load_3d(sb + C::OFF_KV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, m,
+                          bar(C::BAR_FULL + s), c * C::BOX_D, j * BN, w.bhk);
           }
-          umma_commit(bar(C::BAR_EMPTY + s));
         }
-        // O_t += P_t V_j
-        {
-          const int s = it % C::STAGES;
-          const uint32_t ph = (it / C::STAGES) & 1;
-          ++it;
-          if (!mbar_wait(bar(C::BAR_FULL + s), ph)) { ok = false; break; }
+        // Drain: every copy this thread issued has landed before the CTA exits.
+        for (int s = 0; s < C::STAGES && s < it; ++s) {
+          const int fills = (it - s + C::STAGES - 1) / C::STAGES;
+          if (!mbar_wait(bar(C::BAR_FULL + s), (fills - 1) & 1)) fail();
+        }
+        for (int t = 0; t < NQ; ++t)
+          if (w.n[t] > 0 && !mbar_wait(bar(C::BAR_Q + t), 0)) fail();
+      }
+      __syncwarp();
+    } else if (warp == WARP_MMA) {
+      // -------------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = make_idesc_f16(BF16, BM, BN, false);
+        constexpr uint32_t idesc_pv = make_idesc_f16(BF16, BM, D, true);
+        const int n0 = w.n[0], n1 = w.n[1], nmax = w.nmax;
+        bool ok = true;
+        for (int t = 0; t < NQ && ok; ++t)
+          if (w.n[t] > 0 && !mbar_wait(bar(C::BAR_Q + t), 0)) ok = false;
+
+        auto stage_of = [&](int idx) { return idx % C::STAGES; };
+        auto wait_full = [&](int idx) {
+          return mbar_wait(bar(C::BAR_FULL + idx % C::STAGES), (idx / C::STAGES) & 1);
+        };
+        auto issue_s = [&](int t, int kidx) {
+          const uint32_t kbase = sb + C::OFF_KV + stage_of(kidx) * C::TILE_BYTES;
+          const uint32_t qbase = sb + t * C::TILE_BYTES;
+#pragma unroll
+          for (int k = 0; k < C::KSTEPS_QK; ++k) {
+            const uint32_t off =
+                (k / C::KSTEPS_PER_CHUNK) * C::CHUNK_BYTES + (k % C::KSTEPS_PER_CHUNK) * 32;
+            umma_ss(tmem + t * BN, smem_desc(qbase + off, 16, C::SBO, C::LAYOUT),
+                    smem_desc(kbase + off, 16, C::SBO, C::LAYOUT), idesc_qk, k > 0);
+          }
+          umma_commit(bar(C::BAR_S + t));
+        };
+        // O_t += P_t V_j, after P_t of tile j is in tensor memory.
+        auto issue_pv = [&](int t, int j) -> bool {
+          const int vidx = 2 * j + 1;
+          if (!wait_full(vidx)) return false;
+          if (!mbar_wait(bar(C::BAR_P + t), j & 1)) return false;
           tc_fence_after();
-          const uint32_t vbase = sb + C::OFF_KV + s * C::TILE_BYTES;
-          for (int t = 0; t < NQ; ++t) {
-            if (j >= w.n[t]) continue;
-            if (!mbar_wait(bar(C::BAR_P + t), j & 1)) { ok = false; break; }
+          const uint32_t vbase = sb + C::OFF_KV + stage_of(vidx) * C::TILE_BYTES;
+#pragma unroll
+          for (int k = 0; k < C::KSTEPS_PV; ++k)
+            umma_ts(tmem + 256 + t * D, tmem + t * BN + C::COL_P + k * 8,
+                    smem_desc(vbase + k * 16 * C::ROW_BYTES, C::CHUNK_BYTES, C::SBO, C::LAYOUT),
+                    idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          if (j == w.n[t] - 1) umma_commit(bar(C::BAR_O + t));
+          return true;
+        };
+
+        for (int j = 0; j <= nmax && ok && !*abort_flag; ++j) {
+          if (j < nmax) {
+            if (!wait_full(2 * j)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < C::KSTEPS_PV; ++k) {
-              umma_ts(tmem + 256 + t * D, tmem + t * BN + C::COL_P + k * 8,
-                      smem_desc(vbase + k * 16 * C::ROW_BYTES, C::CHUNK_BYTES, C::SBO, C::LAYOUT),
-                      idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
-            }
-            if (j == w.n[t] - 1) umma_commit(bar(C::BAR_O + t));
+            if (j < n0) issue_s(0, 2 * j);
           }
-          umma_commit(bar(C::BAR_EMPTY + s));
-          if (!ok) break;
+          if (j >= 1 && j - 1 < n1 && !issue_pv(1, j - 1)) { ok = false; break; }
+          if (j >= 1) umma_commit(bar(C::BAR_EMPTY + stage_of(2 * (j - 1) + 1)));  // V_{j-1} free
+          if (j < nmax) {
+            if (j < n1) issue_s(1, 2 * j);
+            umma_commit(bar(C::BAR_EMPTY + stage_of(2 * j)));  // K_j free
+            if (j < n0 && !issue_pv(0, j)) { ok = false; break; }
+          }
         }
+        if (!ok) fail();
+        // Drain: all MMAs issued above have completed before TMEM is freed.
+        umma_commit(bar(C::BAR_DONE));
+        if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
       }
-      if (!ok) fail();
-      // Drain: all MMAs issued above have completed before TMEM is freed.
-      umma_commit(bar(C::BAR_DONE));
-      if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
+      __syncwarp();
     }
-    __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax
-    const int t = warp >> 2;                 // query tile of this warpgroup
+    setmaxnreg_inc<REG_SOFTMAX>();
+    const int t = warp >> 2;                   // query tile of this warpgroup
     const int row = ((warp & 3) << 5) + lane;  // TMEM lane = row within the tile
     const int r0 = w.q0 + t * BM;
     const int row_g = r0 + row;
@@ -286,6 +313,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tO = tmem + lane_off + 256 + t * D;
     const int n_t = w.n[t];
     const int nfull_t = w.nfull[t];
+    const float sc = p.scale_log2;
 
     const float* brow = nullptr;
     if constexpr (BIAS) {
@@ -299,22 +327,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int causal_lim = p.causal ? row_g + w.diag : 0x7fffffff;  // last visible key
     const int key_lim = w.key_limit;
 
-    float m_run = -INFINITY;  // running max of scaled scores (log2 domain)
-    float l_run = 0.f;        // running sum of 2^(s - m_run)
+    float m_run = -INFINITY;  // reference max of the row (log2 domain)
+    float l_run = 0.f;        // sum of 2^(s - m_run) over the keys seen
     bool failed = false;
 
     for (int j = 0; j < n_t; ++j) {
       const bool ok = mbar_wait(bar(C::BAR_S + t), j & 1);
       if (__any_sync(0xffffffffu, !ok)) { failed = true; break; }
       tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
-      tmem_wait_ld();
       float s[128];
+      {
+        uint32_t sr[4][32];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
-
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
+      }
       const int key0 = j * BN;
       if constexpr (BIAS) {
         // scores -> log2 domain with the bias folded in
@@ -324,21 +353,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 128; i += 4) {
               const float4 b4 = __ldg(reinterpret_cast<const float4*>(bp + i));
-              s[i + 0] = fmaf(s[i + 0], p.scale_log2, b4.x * LOG2E);
-              s[i + 1] = fmaf(s[i + 1], p.scale_log2, b4.y * LOG2E);
-              s[i + 2] = fmaf(s[i + 2], p.scale_log2, b4.z * LOG2E);
-              s[i + 3] = fmaf(s[i + 3], p.scale_log2, b4.w * LOG2E);
+              const float2 lo = ffma2(make_float2(s[i], s[i + 1]), make_float2(sc, sc),
+                                      fmul2(make_float2(b4.x, b4.y), make_float2(LOG2E, LOG2E)));
+              const float2 hi = ffma2(make_float2(s[i + 2], s[i + 3]), make_float2(sc, sc),
+                                      fmul2(make_float2(b4.z, b4.w), make_float2(LOG2E, LOG2E)));
+              s[i] = lo.x; s[i + 1] = lo.y; s[i + 2] = hi.x; s[i + 3] = hi.y;
             }
           } else {
 #pragma unroll
             for (int i = 0; i < 128; ++i) {
               const float bv = (key0 + i < key_lim) ? __ldg(bp + i) : 0.f;
-              s[i] = fmaf(s[i], p.scale_log2, bv * LOG2E);
+              s[i] = fmaf(s[i], sc, bv * LOG2E);
             }
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 128; ++i) s[i] *= p.scale_log2;
+          for (int i = 0; i < 128; i += 2) {
+            const float2 x = fmul2(make_float2(s[i], s[i + 1]), make_float2(sc, sc));
+            s[i] = x.x; s[i + 1] = x.y;
+          }
         }
       }
       if (j >= nfull_t) {
@@ -348,39 +381,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (key >= key_lim || key > causal_lim) s[i] = -INFINITY;
         }
       }
-      float mx = s[0];
+      // row max: four independent chains of 3-input max
+      float c0 = fmax3(s[0], s[1], s[2]), c1 = fmax3(s[3], s[4], s[5]);
+      float c2 = fmax3(s[6], s[7], s[8]), c3 = fmax3(s[9], s[10], s[11]);
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
-      const float m_tile = BIAS ? mx : mx * p.scale_log2;
-      const float m_new = fmaxf(m_run, m_tile);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = fast_exp2(m_run - m_use);
-      float sum = 0.f;
+      for (int i = 12; i < 124; i += 8) {
+        c0 = fmax3(c0, s[i], s[i + 1]);
+        c1 = fmax3(c1, s[i + 2], s[i + 3]);
+        c2 = fmax3(c2, s[i + 4], s[i + 5]);
+        c3 = fmax3(c3, s[i + 6], s[i + 7]);
+      }
+      c0 = fmax3(c0, s[124], s[125]);
+      c1 = fmax3(c1, s[126], s[127]);
+      const float mx = fmax3(c0, c1, fmaxf(c2, c3));
+      const float m_tile = BIAS ? mx : mx * sc;
+      // lazy rescale: move the reference max only when it grew by > 2^8
+      const bool need = m_tile > m_run + RESCALE_LOG2;
+      float alpha = 1.f;
+      if (need) {
+        alpha = fast_exp2(m_run - m_tile);  // 0 when m_run is -inf
+        m_run = m_tile;
+        l_run *= alpha;
+      }
+      const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+      float2 sum_a = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float x0 = s[64 * h + 2 * c], x1 = s[64 * h + 2 * c + 1];
-          const float p0 = fast_exp2(BIAS ? x0 - m_use : fmaf(x0, p.scale_log2, -m_use));
-          const float p1 = fast_exp2(BIAS ? x1 - m_use : fmaf(x1, p.scale_log2, -m_use));
-          sum += p0 + p1;
-          pk[c] = pack2<BF16>(p0, p1);
+        for (int c = 0; c < 32; c += 2) {
+          const int i = 64 * h + 2 * c;
+          float2 xa, xb;
+          if constexpr (BIAS) {
+            xa = fadd2(make_float2(s[i], s[i + 1]), make_float2(neg_m, neg_m));
+            xb = fadd2(make_float2(s[i + 2], s[i + 3]), make_float2(neg_m, neg_m));
+          } else {
+            xa = ffma2(make_float2(s[i], s[i + 1]), make_float2(sc, sc), make_float2(neg_m, neg_m));
+            xb = ffma2(make_float2(s[i + 2], s[i + 3]), make_float2(sc, sc),
+                       make_float2(neg_m, neg_m));
+          }
+          const float2 pa = make_float2(fast_exp2(xa.x), fast_exp2(xa.y));
+          const float2 pb = make_float2(fast_exp2(xb.x), fast_exp2(xb.y));
+          sum_a = fadd2(sum_a, pa);
+          sum_b = fadd2(sum_b, pb);
+          pk[c] = pack2<BF16>(pa.x, pa.y);
+          pk[c + 1] = pack2<BF16>(pb.x, pb.y);
         }
         tmem_st32(tP + 32 * h, pk);
       }
-      l_run = l_run * alpha + sum;
-      m_run = m_new;
-      // O_t was last written by the PV MMA of tile j-1, which completed before
-      // S_t of tile j was signalled; rescale it before PV of tile j is issued.
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      l_run += (sum_a.x + sum_a.y) + (sum_b.x + sum_b.y);
+      // O_t was last written by PV of tile j-1, complete before S_t of tile j
+      // was signalled; rescale it before PV of tile j is issued.
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + 32 * c, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 x = fmul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                   make_float2(alpha, alpha));
+            o[i] = __float_as_uint(x.x);
+            o[i + 1] = __float_as_uint(x.y);
+          }
           tmem_st32(tO + 32 * c, o);
         }
       }
@@ -418,8 +482,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+          for (int i = 0; i < 16; ++i) {
+            const float2 x = fmul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
+                                   make_float2(inv, inv));
+            pk[i] = pack2<BF16>(x.x, x.y);
+          }
           const int col0 = 32 * c;
           const int box = col0 / C::BOX_D;
           const int ch0 = ((col0 % C::BOX_D) * 2) / 16;
@@ -487,9 +554,10 @@ cudaError_t launch_tc_instance(EncodeTiledFn enc, const void* q, const void* k, 
   constexpr int smem = Cfg<D>::SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned qblocks = static_cast<unsigned>((p.Sq + NQ * BM - 1) / (NQ * BM));
-  dim3 grid(static_cast<unsigned>(bhq), qblocks);
-  kern<<<grid, NUM_THREADS, smem, stream>>>(tq, tk, tv, to, p);
+  const uint64_t qblocks = (static_cast<uint64_t>(p.Sq) + NQ * BM - 1) / (NQ * BM);
+  const uint64_t ctas = bhq * qblocks;
+  if (ctas > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(ctas), NUM_THREADS, smem, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 

@@ -44,4 +44,11 @@ def run_gpu(x, dtype, causal=None, stream=None):
     lens = to_device(x["kv_lens"], "i32") if x["kv_lens"] is not None else None
     bias = to_device(x["bias"], "f32") if x["bias"] is not None else None
     causal = bool(x["mask"] & 1) if causal is None else causal
-    return attn.fwd(q, k, v, causal=causal, kv_lens=lens, bias=bias, scale=x["scale"], stream=stream)
+    out = torch_full_like(q, 777.0)  # sentinel: a tile the kernel skips cannot pass as a result
+    return attn.fwd(q, k, v, causal=causal, kv_lens=lens, bias=bias, scale=x["scale"], stream=stream,
+                    out=out)
+
+
+def torch_full_like(t, value):
+    import torch
+    return torch.full_like(t, value)
