@@ -50,8 +50,8 @@ constexpr int NUM_THREADS = 384;  // 2 softmax warpgroups + producer/MMA warpgro
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 constexpr int TMEM_COLS = 512;
-constexpr int REG_SOFTMAX = 216;  // 2*128*216 + 128*56 <= 384 * 168 (launch allocation)
-constexpr int REG_OTHER = 56;
+constexpr int REG_SOFTMAX = 200;  // 2*128*200 + 128*96 <= 384 * 168 (launch allocation)
+constexpr int REG_OTHER = 96;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;  // lazy-rescale threshold (log2 units)
 constexpr int HEAD_GROUP = 16;        // heads scheduled together so their K/V stay in L2
@@ -242,55 +242,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) {
         constexpr uint32_t idesc_qk = make_idesc_f16(BF16, BM, BN, false);
         constexpr uint32_t idesc_pv = make_idesc_f16(BF16, BM, D, true);
+        constexpr int ST = C::STAGES;
         const int n0 = w.n[0], n1 = w.n[1], nmax = w.nmax;
         bool ok = true;
         for (int t = 0; t < NQ && ok; ++t)
           if (w.n[t] > 0 && !mbar_wait(bar(C::BAR_Q + t), 0)) ok = false;
 
-        auto stage_of = [&](int idx) { return idx % C::STAGES; };
-        auto wait_full = [&](int idx) {
-          return mbar_wait(bar(C::BAR_FULL + idx % C::STAGES), (idx / C::STAGES) & 1);
+        // Descriptors of the first K-step of Q_0, of ring stage 0 as a K tile
+        // (K-major) and as a V tile (MN-major). Other tiles, stages and K-steps
+        // only move the start address, a plain addition to the low field.
+        const uint64_t dq0 = smem_desc(sb, 16, C::SBO, C::LAYOUT);
+        const uint64_t dk0 = smem_desc(sb + C::OFF_KV, 16, C::SBO, C::LAYOUT);
+        const uint64_t dv0 = smem_desc(sb + C::OFF_KV, C::CHUNK_BYTES, C::SBO, C::LAYOUT);
+        constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
+        constexpr uint32_t CHUNK16 = C::CHUNK_BYTES >> 4;
+        constexpr uint32_t VSTEP16 = (16 * C::ROW_BYTES) >> 4;  // 16 keys of V
+        auto kstep = [](int k) -> uint32_t {
+          return (k / C::KSTEPS_PER_CHUNK) * CHUNK16 + (k % C::KSTEPS_PER_CHUNK) * 2;
         };
-        auto issue_s = [&](int t, int kidx) {
-          const uint32_t kbase = sb + C::OFF_KV + stage_of(kidx) * C::TILE_BYTES;
-          const uint32_t qbase = sb + t * C::TILE_BYTES;
+        auto wait_full = [&](int idx) {
+          return mbar_wait(bar(C::BAR_FULL + idx % ST), (idx / ST) & 1);
+        };
+        // S_t = Q_t K_j^T
+        auto issue_s = [&](int t, int j) {
+          const uint64_t a = dq0 + t * TILE16;
+          const uint64_t b = dk0 + ((2 * j) % ST) * TILE16;
 #pragma unroll
-          for (int k = 0; k < C::KSTEPS_QK; ++k) {
-            const uint32_t off =
-                (k / C::KSTEPS_PER_CHUNK) * C::CHUNK_BYTES + (k % C::KSTEPS_PER_CHUNK) * 32;
-            umma_ss(tmem + t * BN, smem_desc(qbase + off, 16, C::SBO, C::LAYOUT),
-                    smem_desc(kbase + off, 16, C::SBO, C::LAYOUT), idesc_qk, k > 0);
-          }
+          for (int k = 0; k < C::KSTEPS_QK; ++k)
+            umma_ss(tmem + t * BN, a + kstep(k), b + kstep(k), idesc_qk, k > 0 ? 1u : 0u);
           umma_commit(bar(C::BAR_S + t));
         };
-        // O_t += P_t V_j, after P_t of tile j is in tensor memory.
-        auto issue_pv = [&](int t, int j) -> bool {
-          const int vidx = 2 * j + 1;
-          if (!wait_full(vidx)) return false;
-          if (!mbar_wait(bar(C::BAR_P + t), j & 1)) return false;
-          tc_fence_after();
-          const uint32_t vbase = sb + C::OFF_KV + stage_of(vidx) * C::TILE_BYTES;
+        // O_t += P_t V_j (P_t of tile j is in tensor memory)
+        auto issue_pv = [&](int t, int j) {
+          const uint64_t b = dv0 + ((2 * j + 1) % ST) * TILE16;
+          const uint32_t d = tmem + 256 + t * D;
+          const uint32_t a = tmem + t * BN + C::COL_P;
+          umma_ts(d, a, b, idesc_pv, j > 0 ? 1u : 0u);
 #pragma unroll
-          for (int k = 0; k < C::KSTEPS_PV; ++k)
-            umma_ts(tmem + 256 + t * D, tmem + t * BN + C::COL_P + k * 8,
-                    smem_desc(vbase + k * 16 * C::ROW_BYTES, C::CHUNK_BYTES, C::SBO, C::LAYOUT),
-                    idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          for (int k = 1; k < C::KSTEPS_PV; ++k) umma_ts(d, a + k * 8, b + k * VSTEP16, idesc_pv, 1u);
           if (j == w.n[t] - 1) umma_commit(bar(C::BAR_O + t));
-          return true;
         };
 
-        for (int j = 0; j <= nmax && ok && !*abort_flag; ++j) {
+        for (int j = 0; j <= nmax && ok; ++j) {
+          if (*abort_flag) { ok = false; break; }
           if (j < nmax) {
-            if (!wait_full(2 * j)) { ok = false; break; }
+            if (!wait_full(2 * j)) { ok = false; break; }  // K_j
             tc_fence_after();
-            if (j < n0) issue_s(0, 2 * j);
+            if (j < n0) issue_s(0, j);
           }
-          if (j >= 1 && j - 1 < n1 && !issue_pv(1, j - 1)) { ok = false; break; }
-          if (j >= 1) umma_commit(bar(C::BAR_EMPTY + stage_of(2 * (j - 1) + 1)));  // V_{j-1} free
+          if (j >= 1 && j - 1 < n1) {
+            // V_{j-1} was already waited for by PV_0(j-1) unless tile 0 skipped it
+            if (j - 1 >= n0 && !wait_full(2 * (j - 1) + 1)) { ok = false; break; }
+            if (!mbar_wait(bar(C::BAR_P + 1), (j - 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(1, j - 1);
+          }
+          if (j >= 1) umma_commit(bar(C::BAR_EMPTY + (2 * (j - 1) + 1) % ST));  // V_{j-1} free
           if (j < nmax) {
-            if (j < n1) issue_s(1, 2 * j);
-            umma_commit(bar(C::BAR_EMPTY + stage_of(2 * j)));  // K_j free
-            if (j < n0 && !issue_pv(0, j)) { ok = false; break; }
+            if (j < n1) issue_s(1, j);
+            umma_commit(bar(C::BAR_EMPTY + (2 * j) % ST));  // K_j free
+            if (j < n0) {
+              if (!wait_full(2 * j + 1) || !mbar_wait(bar(C::BAR_P + 0), j & 1)) { ok = false; break; }
+              tc_fence_after();
+              issue_pv(0, j);
+            }
           }
         }
         if (!ok) fail();
