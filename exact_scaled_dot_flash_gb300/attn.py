@@ -60,6 +60,8 @@ def load_library():
         lib.attn_last_cuda_error.restype = ctypes.c_int
         lib.attn_device_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int]
         lib.attn_device_status.restype = ctypes.c_int
+        lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, ctypes.c_void_p]
+        lib.attn_selftest_wait_timeout.restype = ctypes.c_int
         lib.attn_version.argtypes = []
         lib.attn_version.restype = ctypes.c_int
         _lib = lib

@@ -114,6 +114,17 @@ int attn_device_status(int device, int* flags, int clear) {
   return ATTN_OK;
 }
 
+int attn_selftest_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 5000000u) return ATTN_ERR_SHAPE;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  int* st = status_ptr(dev);
+  if (!st) return fail_cuda(cudaErrorInvalidDevice);
+  e = attn::launch_wait_timeout_probe(st, 1000ull * limit_us, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+}
+
 int attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void* v,
              int mask_kind, const int32_t* kv_lens, const float* bias, float scale,
              attn_dtype_t dtype, void* out, void* stream) {
@@ -194,22 +205,28 @@ int attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void
   attn::EncodeTiledFn enc = encode_fn();
   if (!enc) return fail_cuda(cudaErrorNotSupported);
   const bool bf16 = dtype == ATTN_BF16;
-  const bool hb = bias != nullptr;
+  // bias: none; staged through shared memory by TMA when D <= 64 and the rows
+  // allow 16-byte TMA strides; otherwise read directly by the softmax threads
+  const int bmode = !bias ? 0 : ((s.D <= 64 && p.bias_vec4) ? 2 : 1);
   using namespace attn::tc;
-#define ATTN_TC_DISPATCH(DD)                                                                   \
+#define ATTN_TC_CALL(DD, BB, MM) launch_tc_instance<DD, BB, MM>(enc, q, k, v, out, p, st)
+#define ATTN_TC_DISPATCH(DD, STAGED)                                                           \
   case DD:                                                                                     \
-    e = bf16 ? (hb ? launch_tc_instance<DD, true, true>(enc, q, k, v, out, p, st)              \
-                   : launch_tc_instance<DD, true, false>(enc, q, k, v, out, p, st))            \
-             : (hb ? launch_tc_instance<DD, false, true>(enc, q, k, v, out, p, st)             \
-                   : launch_tc_instance<DD, false, false>(enc, q, k, v, out, p, st));          \
+    if (bmode == 2)                                                                            \
+      e = bf16 ? ATTN_TC_CALL(DD, true, STAGED) : ATTN_TC_CALL(DD, false, STAGED);             \
+    else if (bmode == 1)                                                                       \
+      e = bf16 ? ATTN_TC_CALL(DD, true, BIAS_DIRECT) : ATTN_TC_CALL(DD, false, BIAS_DIRECT);   \
+    else                                                                                       \
+      e = bf16 ? ATTN_TC_CALL(DD, true, BIAS_NONE) : ATTN_TC_CALL(DD, false, BIAS_NONE);       \
     break;
   switch (s.D) {
-    ATTN_TC_DISPATCH(32)
-    ATTN_TC_DISPATCH(64)
-    ATTN_TC_DISPATCH(128)
+    ATTN_TC_DISPATCH(32, BIAS_STAGED)
+    ATTN_TC_DISPATCH(64, BIAS_STAGED)
+    ATTN_TC_DISPATCH(128, BIAS_DIRECT)
     default:
       return ATTN_ERR_HEAD_DIM;
   }
+#undef ATTN_TC_CALL
 #undef ATTN_TC_DISPATCH
   return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
 }

@@ -55,17 +55,22 @@ constexpr int REG_OTHER = 96;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;  // lazy-rescale threshold (log2 units)
 constexpr int HEAD_GROUP = 16;        // heads scheduled together so their K/V stay in L2
+constexpr int BIAS_CHUNK = 32;                     // keys per staged bias chunk
+constexpr int BIAS_SLOTS = BN / BIAS_CHUNK;        // ring slots per query tile (one K/V tile)
+constexpr int BIAS_SLOT_BYTES = BM * BIAS_CHUNK * 4;  // 16 KB, 128-byte rows
 
-template <int D>
+template <int D, int BMODE = BIAS_NONE>
 struct Cfg {
   static_assert(D == 32 || D == 64 || D == 128, "compiled head dims are 32, 64, 128");
+  static_assert(BMODE != BIAS_STAGED || D <= 64, "the staged bias ring fits for D <= 64");
   static constexpr int SWIZZLE = D >= 64 ? 128 : 64;  // bytes per swizzled smem row
   static constexpr int BOX_D = SWIZZLE / 2;           // 16-bit elements per TMA box row
   static constexpr int NCHUNK = D / BOX_D;            // boxes per tile along D
   static constexpr int ROW_BYTES = SWIZZLE;
   static constexpr int CHUNK_BYTES = BN * ROW_BYTES;  // one box: 128 rows
   static constexpr int TILE_BYTES = NCHUNK * CHUNK_BYTES;
-  static constexpr int STAGES = D == 128 ? 4 : (D == 64 ? 8 : 12);
+  static constexpr int STAGES =
+      BMODE == BIAS_STAGED ? (D == 64 ? 4 : 6) : (D == 128 ? 4 : (D == 64 ? 8 : 12));
   static constexpr uint32_t LAYOUT = SWIZZLE == 128 ? 2u : 4u;  // UMMA swizzle code
   static constexpr int SBO = 8 * ROW_BYTES;                      // 8-row group stride
   static constexpr int KSTEPS_QK = D / 16;
@@ -73,8 +78,11 @@ struct Cfg {
   static constexpr int KSTEPS_PV = BN / 16;
   static constexpr int COL_P = 64;  // P_t at S_t + 64 (16-bit pairs, 64 columns)
   static constexpr int OFF_KV = NQ * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_KV + STAGES * TILE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 4 * NQ + 1;
+  static constexpr int OFF_BIAS = OFF_KV + STAGES * TILE_BYTES;
+  static constexpr int BIAS_RING_BYTES = BMODE == BIAS_STAGED ? NQ * BIAS_SLOTS * BIAS_SLOT_BYTES : 0;
+  static constexpr int OFF_BAR = OFF_BIAS + BIAS_RING_BYTES;
+  static constexpr int NUM_BIAS_BARS = BMODE == BIAS_STAGED ? 2 * NQ * BIAS_SLOTS : 0;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 * NQ + 1 + NUM_BIAS_BARS;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   // +1024 for aligning the dynamic window; at least 120 KB so that one CTA
@@ -88,6 +96,8 @@ struct Cfg {
   static constexpr int BAR_P = BAR_S + NQ;
   static constexpr int BAR_O = BAR_P + NQ;
   static constexpr int BAR_DONE = BAR_O + NQ;
+  static constexpr int BAR_BFULL = BAR_DONE + 1;                  // bias slot loaded
+  static constexpr int BAR_BEMPTY = BAR_BFULL + NQ * BIAS_SLOTS;  // bias slot read by softmax
 };
 
 // Per-CTA work description, computed identically by every thread.
@@ -148,13 +158,15 @@ __device__ __forceinline__ Work make_work(const KernelParams& p) {
   return w;
 }
 
-template <int D, bool BF16, bool BIAS>
+template <int D, bool BF16, int BMODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
-                       const __grid_constant__ CUtensorMap tm_o, const KernelParams p) {
-  using C = Cfg<D>;
+                       const __grid_constant__ CUtensorMap tm_o,
+                       const __grid_constant__ CUtensorMap tm_b, const KernelParams p) {
+  using C = Cfg<D, BMODE>;
+  constexpr bool BIAS = BMODE != BIAS_NONE;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -179,6 +191,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(C::BAR_O + t), 1);
     }
     mbar_init(bar(C::BAR_DONE), 1);
+    if constexpr (BMODE == BIAS_STAGED) {
+      for (int i = 0; i < NQ * BIAS_SLOTS; ++i) {
+        mbar_init(bar(C::BAR_BFULL + i), 1);
+        mbar_init(bar(C::BAR_BEMPTY + i), BM);
+      }
+    }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -235,6 +253,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int t = 0; t < NQ; ++t)
           if (w.n[t] > 0 && !mbar_wait(bar(C::BAR_Q + t), 0)) fail();
+      }
+      __syncwarp();
+    } else if (BMODE == BIAS_STAGED && warp == WARP_MMA + 1) {
+      // -------------------------------------------------------------- bias producer
+      // Chunk c of key tile j for query tile t: bias rows [r0, r0+128), keys
+      // [128j + 32c, +32), into ring slot (count_t mod 4) of tile t's ring.
+      if (lane == 0) {
+        const int bz = (p.bias_b == 1 ? 0 : w.b) * p.bias_h + (p.bias_h == 1 ? 0 : w.hq);
+        int cnt[NQ] = {0, 0};
+        bool ok = true;
+        for (int j = 0; j < w.nmax && ok; ++j) {
+          for (int t = 0; t < NQ && ok; ++t) {
+            if (j >= w.n[t]) continue;
+            for (int c = 0; c < BIAS_SLOTS; ++c, ++cnt[t]) {
+              if (*abort_flag) { ok = false; break; }
+              const int slot = t * BIAS_SLOTS + cnt[t] % BIAS_SLOTS;
+              if (!mbar_wait(bar(C::BAR_BEMPTY + slot), ((cnt[t] / BIAS_SLOTS) & 1) ^ 1)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(bar(C::BAR_BFULL + slot), BIAS_SLOT_BYTES);
+              tma_load_3d(sb + C::OFF_BIAS + slot * BIAS_SLOT_BYTES, &tm_b, bar(C::BAR_BFULL + slot),
+                          j * BN + c * BIAS_CHUNK, w.q0 + t * BM, bz);
+            }
+          }
+        }
+        if (!ok) fail();
+        // Drain: every bias copy issued has landed before the CTA exits.
+        for (int t = 0; t < NQ; ++t)
+          for (int s2 = 0; s2 < BIAS_SLOTS && s2 < cnt[t]; ++s2) {
+            const int fills = (cnt[t] - s2 + BIAS_SLOTS - 1) / BIAS_SLOTS;
+            if (!mbar_wait(bar(C::BAR_BFULL + t * BIAS_SLOTS + s2), (fills - 1) & 1)) fail();
+          }
       }
       __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -342,6 +393,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int causal_lim = p.causal ? row_g + w.diag : 0x7fffffff;  // last visible key
     const int key_lim = w.key_limit;
 
+    bool bias_failed = false;  // a staged bias chunk never arrived
     float m_run = -INFINITY;  // reference max of the row (log2 domain)
     float l_run = 0.f;        // sum of 2^(s - m_run) over the keys seen
     bool failed = false;
@@ -360,7 +412,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
       }
       const int key0 = j * BN;
-      if constexpr (BIAS) {
+      if constexpr (BMODE == BIAS_STAGED) {
+        // bias chunks from the shared-memory ring (128-byte swizzled rows)
+        const uint8_t* ring = smem + C::OFF_BIAS + t * BIAS_SLOTS * BIAS_SLOT_BYTES;
+#pragma unroll
+        for (int c = 0; c < BIAS_SLOTS; ++c) {
+          const int cnt = j * BIAS_SLOTS + c;
+          const int slot = cnt % BIAS_SLOTS;
+          if (!mbar_wait(bar(C::BAR_BFULL + t * BIAS_SLOTS + slot), (cnt / BIAS_SLOTS) & 1))
+            bias_failed = true;
+          const uint8_t* rowp = ring + slot * BIAS_SLOT_BYTES + row * 128;
+          float bv[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 b4 = *reinterpret_cast<const float4*>(rowp + ((q ^ (row & 7)) << 4));
+            bv[4 * q] = b4.x; bv[4 * q + 1] = b4.y; bv[4 * q + 2] = b4.z; bv[4 * q + 3] = b4.w;
+          }
+          mbar_arrive(bar(C::BAR_BEMPTY + t * BIAS_SLOTS + slot));
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 x = ffma2(make_float2(s[32 * c + i], s[32 * c + i + 1]), make_float2(sc, sc),
+                                   fmul2(make_float2(bv[i], bv[i + 1]), make_float2(LOG2E, LOG2E)));
+            s[32 * c + i] = x.x;
+            s[32 * c + i + 1] = x.y;
+          }
+        }
+      } else if constexpr (BIAS) {
         // scores -> log2 domain with the bias folded in
         if (brow != nullptr) {
           const float* bp = brow + key0;
@@ -466,6 +543,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::BAR_P + t));
+      if (__any_sync(0xffffffffu, bias_failed)) { failed = true; break; }
     }
 
     // ---------------------------------------------------------------- epilogue
@@ -555,24 +633,38 @@ static CUresult encode_3d(EncodeTiledFn enc, CUtensorMap* m, bool bf16, const vo
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <int D, bool BF16, bool BIAS>
+template <int D, bool BF16, int BMODE>
 cudaError_t launch_tc_instance(EncodeTiledFn enc, const void* q, const void* k, const void* v,
                                void* out, const KernelParams& p, cudaStream_t stream) {
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv, to, tb;
   const uint64_t bhq = static_cast<uint64_t>(p.B) * p.Hq, bhk = static_cast<uint64_t>(p.B) * p.Hkv;
   if (encode_3d<D>(enc, &tq, BF16, q, p.Sq, bhq) != CUDA_SUCCESS ||
       encode_3d<D>(enc, &tk, BF16, k, p.Sk, bhk) != CUDA_SUCCESS ||
       encode_3d<D>(enc, &tv, BF16, v, p.Sk, bhk) != CUDA_SUCCESS ||
       encode_3d<D>(enc, &to, BF16, out, p.Sq, bhq) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  auto kern = attn_fwd_tc_kernel<D, BF16, BIAS>;
-  constexpr int smem = Cfg<D>::SMEM_BYTES;
+  tb = tq;  // placeholder unless the bias is staged
+  if constexpr (BMODE == BIAS_STAGED) {
+    // bias viewed as [bias_b * bias_h, Sq, Sk] fp32; boxes of 32 keys x 128 rows
+    const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(p.Sk), static_cast<cuuint64_t>(p.Sq),
+                                static_cast<cuuint64_t>(p.bias_b) * p.bias_h};
+    const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(p.Sk) * 4,
+                                   static_cast<cuuint64_t>(p.Sq) * p.Sk * 4};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(BIAS_CHUNK), static_cast<cuuint32_t>(BM), 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    if (enc(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(p.bias), gdim, gstride, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  auto kern = attn_fwd_tc_kernel<D, BF16, BMODE>;
+  constexpr int smem = Cfg<D, BMODE>::SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const uint64_t qblocks = (static_cast<uint64_t>(p.Sq) + NQ * BM - 1) / (NQ * BM);
   const uint64_t ctas = bhq * qblocks;
   if (ctas > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(ctas), NUM_THREADS, smem, stream>>>(tq, tk, tv, to, p);
+  kern<<<static_cast<unsigned>(ctas), NUM_THREADS, smem, stream>>>(tq, tk, tv, to, tb, p);
   return cudaGetLastError();
 }
 

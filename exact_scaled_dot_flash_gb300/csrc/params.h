@@ -29,7 +29,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 namespace tc {
-template <int D, bool BF16, bool BIAS>
+// How the additive bias reaches the softmax: none; read by each thread from
+// global memory; or staged by TMA through a shared-memory ring (D <= 64).
+constexpr int BIAS_NONE = 0, BIAS_DIRECT = 1, BIAS_STAGED = 2;
+template <int D, bool BF16, int BMODE>
 cudaError_t launch_tc_instance(EncodeTiledFn enc, const void* q, const void* k, const void* v,
                                void* out, const KernelParams& p, cudaStream_t stream);
 }  // namespace tc
@@ -39,5 +42,7 @@ cudaError_t launch_f32(int D, bool has_bias, const KernelParams& p, const float*
                        const float* k, const float* v, float* out, cudaStream_t stream,
                        int* unsupported);
 cudaError_t launch_nan_fill(void* out, int64_t count, int elem_bytes, cudaStream_t stream);
+cudaError_t launch_wait_timeout_probe(int* status, unsigned long long limit_ns,
+                                      cudaStream_t stream);
 
 }  // namespace attn

@@ -60,16 +60,21 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of parity `parity` to complete. Returns false if it did
-// not complete within WAIT_LIMIT_NS (the caller then unwinds).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// not complete within `limit_ns` (the caller then unwinds).
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity,
+                                              unsigned long long limit_ns) {
   if (mbar_test(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 256; ++i)
       if (mbar_test(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, WAIT_LIMIT_NS);
 }
 
 // ------------------------------------------------------------------ TMA

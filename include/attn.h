@@ -117,6 +117,16 @@ int attn_last_cuda_error(void);
  * Returns ATTN_OK, ATTN_ERR_NULL or ATTN_ERR_CUDA. */
 int attn_device_status(int device, int* flags, int clear);
 
+/* attn_selftest_wait_timeout - failure-path self-test (the pages have no
+ * counterpart; it checks this library's own error reporting). Launches, on
+ * `stream`, a one-thread kernel that waits on an mbarrier phase nothing
+ * completes, with the same bounded-wait code the attention kernels use but a
+ * limit of `limit_us` microseconds (1..5,000,000). On expiry the kernel sets
+ * the timeout bit of the device status word (read it with attn_device_status)
+ * and returns; the GPU context stays usable. Asynchronous; returns ATTN_OK,
+ * ATTN_ERR_SHAPE for an out-of-range limit, or ATTN_ERR_CUDA. */
+int attn_selftest_wait_timeout(unsigned int limit_us, void* stream);
+
 /* attn_version - library version as major*10000 + minor*100 + patch. */
 int attn_version(void);
 

@@ -239,3 +239,15 @@ def test_binding_rejects_bad_tensors():
         attn.fwd(q, q, q, scale=-1.0)  # C-ABI scale check
     with pytest.raises(attn.AttnError):
         attn.fwd(q[..., :48].contiguous(), q[..., :48].contiguous(), q[..., :48].contiguous())  # D=48
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("D,Sk,path", [(32, 300, "staged"), (64, 516, "staged"), (64, 259, "direct"),
+                                       (128, 260, "direct"), (128, 131, "direct")])
+def test_bias_staged_and_direct_paths(dtype, D, Sk, path):
+    """The bias goes through a TMA-staged shared-memory ring for D <= 64 with
+    16-byte rows, and is read directly otherwise; both must match the oracle,
+    with key padding, causal masking and per-head bias on several key tiles."""
+    w = synth.Workload("biaspath", dtype, 2, 4, 2, 290, Sk, D, mask=CAUSAL | PAD, bias=True,
+                       bias_b=2, bias_h=4, seed=111 + D + Sk, kv_len_range=(Sk // 3, Sk))
+    full_check(w)
