@@ -192,6 +192,7 @@ int attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void
   p.bias_vec4 = bias && aligned16(bias) && (s.Sk % 4 == 0);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status_ptr(dev);
+  p.device = dev;
 
   if (!tensor_core) {
     int unsupported = 0;

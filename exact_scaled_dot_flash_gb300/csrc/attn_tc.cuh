@@ -37,6 +37,8 @@
 // the device status word, drains its own copies and MMAs, frees TMEM and exits.
 #pragma once
 
+#include <atomic>
+
 #include "params.h"
 #include "ptx.cuh"
 
@@ -659,8 +661,14 @@ cudaError_t launch_tc_instance(EncodeTiledFn enc, const void* q, const void* k, 
   }
   auto kern = attn_fwd_tc_kernel<D, BF16, BMODE>;
   constexpr int smem = Cfg<D, BMODE>::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
+  // The shared-memory opt-in is per device and per kernel: set it once.
+  static std::atomic<unsigned long long> configured{0};
+  const unsigned long long bit = p.device >= 0 && p.device < 64 ? 1ull << p.device : 0ull;
+  if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
   const uint64_t qblocks = (static_cast<uint64_t>(p.Sq) + NQ * BM - 1) / (NQ * BM);
   const uint64_t ctas = bhq * qblocks;
   if (ctas > 0x7fffffffull) return cudaErrorInvalidConfiguration;

@@ -19,6 +19,7 @@ struct KernelParams {
   int bias_vec4;          // bias rows may be read as float4
   float scale_log2;       // scale * log2(e): scores are kept in the log2 domain
   int* status;            // device status word (STATUS_* bits)
+  int device;             // CUDA device the launch runs on
 };
 
 // cuTensorMapEncodeTiled, resolved at run time through the runtime's

@@ -58,12 +58,12 @@ def _load():
             dp = ctypes.POINTER(ctypes.c_double)
             lib.oracle_attention.argtypes = [ctypes.POINTER(_Shape), dp, dp, dp, ctypes.c_int,
                                              ctypes.POINTER(ctypes.c_int32), dp, ctypes.c_double,
-                                             dp, dp, ctypes.c_int]
+                                             dp, dp, dp, ctypes.c_int]
             lib.oracle_attention.restype = ctypes.c_int
             lib.oracle_attention_rows.argtypes = [ctypes.POINTER(_Shape), dp, dp, dp, ctypes.c_int,
                                                   ctypes.POINTER(ctypes.c_int32), dp, ctypes.c_double,
                                                   ctypes.c_int64, ctypes.POINTER(ctypes.c_int64),
-                                                  dp, ctypes.c_int]
+                                                  dp, dp, ctypes.c_int]
             lib.oracle_attention_rows.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -109,28 +109,31 @@ def _prepare(q, k, v, kv_lens, bias, dtype):
 
 
 def attention(q, k, v, *, mask: int = 0, kv_lens=None, bias=None, scale: float,
-              dtype: str | None = None, weights: bool = False, threads: int = 0):
+              dtype: str | None = None, weights: bool = False, lse: bool = False, threads: int = 0):
     """Float64 attention output for every row.
 
     q: [B,Hq,Sq,D], k/v: [B,Hkv,Sk,D] in storage format of ``dtype`` (or any
     float array when ``dtype`` is None); kv_lens: int32 [B] (key padding);
-    bias: float [bias_b,bias_h,Sq,Sk]. Returns O [B,Hq,Sq,D] float64, and the
-    weights [B,Hq,Sq,Sk] too when ``weights`` is True.
+    bias: float [bias_b,bias_h,Sq,Sk]. Returns O [B,Hq,Sq,D] float64; with
+    ``weights`` also the weights [B,Hq,Sq,Sk]; with ``lse`` also the row
+    log-sum-exp [B,Hq,Sq] (natural log, -inf for a row with no visible key).
     """
     lib = _load()
     q64, k64, v64, lens, b64, shape = _prepare(q, k, v, kv_lens, bias, dtype)
     out = np.empty(q64.shape, dtype=np.float64)
     w = np.empty(q64.shape[:3] + (k64.shape[2],), dtype=np.float64) if weights else None
+    ls = np.empty(q64.shape[:3], dtype=np.float64) if lse else None
     rc = lib.oracle_attention(ctypes.byref(shape), _dptr(q64), _dptr(k64), _dptr(v64), int(mask),
                               lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if lens is not None else None,
-                              _dptr(b64), float(scale), _dptr(out), _dptr(w), int(threads))
+                              _dptr(b64), float(scale), _dptr(out), _dptr(w), _dptr(ls), int(threads))
     if rc != 0:
         raise ValueError(f"oracle_attention rejected its arguments (rc={rc})")
-    return (out, w) if weights else out
+    res = (out,) + ((w,) if weights else ()) + ((ls,) if lse else ())
+    return res if len(res) > 1 else out
 
 
 def attention_rows(q, k, v, rows, *, mask: int = 0, kv_lens=None, bias=None, scale: float,
-                   dtype: str | None = None, threads: int = 0, widened=None):
+                   dtype: str | None = None, threads: int = 0, widened=None, lse: bool = False):
     """Float64 output rows O[b,hq,i,:] for the (b, hq, i) triples in ``rows``.
 
     ``widened`` may carry a tuple from :func:`prepare` to avoid re-widening
@@ -142,13 +145,15 @@ def attention_rows(q, k, v, rows, *, mask: int = 0, kv_lens=None, bias=None, sca
     q64, k64, v64, lens, b64, shape = widened
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
     out = np.empty((r.shape[0], q64.shape[3]), dtype=np.float64)
+    ls = np.empty(r.shape[0], dtype=np.float64) if lse else None
     rc = lib.oracle_attention_rows(ctypes.byref(shape), _dptr(q64), _dptr(k64), _dptr(v64), int(mask),
                                    lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if lens is not None else None,
                                    _dptr(b64), float(scale), r.shape[0],
-                                   r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _dptr(out), int(threads))
+                                   r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _dptr(out), _dptr(ls),
+                                   int(threads))
     if rc != 0:
         raise ValueError(f"oracle_attention_rows rejected its arguments (rc={rc})")
-    return out
+    return (out, ls) if lse else out
 
 
 def prepare(q, k, v, *, kv_lens=None, bias=None, dtype: str | None = None):

@@ -45,6 +45,12 @@
  *  - a row with no visible key has undefined weights: the oracle returns NaN
  *    for its weights and its output (exp(-inf - (-inf)) in the plain form).
  *
+ * Log-sum-exp of a row (ruDNN user guide, section 9: a split history keeps
+ * FP32 partial statistics that are merged afterwards; the statistic that makes
+ * two partial softmaxes mergeable is the log of the row's exp-sum):
+ *
+ *   lse = log(sum_j exp(s_j))  over the visible j,   -inf for an empty row.
+ *
  * Inputs are float64 arrays holding the already dtype-rounded values,
  * widened exactly; accumulation is in float64 throughout.
  */
@@ -71,10 +77,10 @@ typedef struct {
   double scale;
 } problem;
 
-/* One output row (b, hq, i): writes D outputs, and Sk weights when w != NULL.
- * `sc` is caller scratch of Sk doubles. */
+/* One output row (b, hq, i): writes D outputs, Sk weights when w != NULL and
+ * the row's log-sum-exp when lse != NULL. `sc` is caller scratch of Sk doubles. */
 static void attention_row(const problem* P, int64_t b, int64_t hq, int64_t i,
-                          double* o, double* w, double* sc) {
+                          double* o, double* w, double* lse, double* sc) {
   const oracle_shape* s = P->s;
   const int64_t D = s->D, Sk = s->Sk, Sq = s->Sq;
   const int64_t group = s->Hq / s->Hkv;
@@ -113,6 +119,7 @@ static void attention_row(const problem* P, int64_t b, int64_t hq, int64_t i,
   if (m == -INFINITY) { /* no visible key: undefined softmax -> NaN */
     for (int64_t d = 0; d < D; ++d) o[d] = NAN;
     if (w) for (int64_t j = 0; j < Sk; ++j) w[j] = NAN;
+    if (lse) *lse = -INFINITY;
     return;
   }
 
@@ -123,6 +130,7 @@ static void attention_row(const problem* P, int64_t b, int64_t hq, int64_t i,
     sc[j] = p;
     l += p;
   }
+  if (lse) *lse = m + log(l);
   /* row-stochastic weights and the weighted sum of V */
   for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
   for (int64_t j = 0; j < Sk; ++j) {
@@ -139,6 +147,7 @@ typedef struct {
   const int64_t* rows; /* NULL: items are (b, hq) heads; else (b, hq, i) triples */
   double* out;
   double* weights;
+  double* lse;
   int64_t next;
   pthread_mutex_t lock;
   int failed;
@@ -164,13 +173,13 @@ static void* worker(void* arg) {
   for (int64_t t = take(J); t < J->n_items; t = take(J)) {
     if (J->rows) {
       const int64_t* r = J->rows + 3 * t;
-      attention_row(J->P, r[0], r[1], r[2], J->out + t * s->D, NULL, sc);
+      attention_row(J->P, r[0], r[1], r[2], J->out + t * s->D, NULL, J->lse ? J->lse + t : NULL, sc);
     } else {
       int64_t b = t / s->Hq, hq = t % s->Hq;
       for (int64_t i = 0; i < s->Sq; ++i) {
         int64_t row = (b * s->Hq + hq) * s->Sq + i;
         attention_row(J->P, b, hq, i, J->out + row * s->D,
-                      J->weights ? J->weights + row * s->Sk : NULL, sc);
+                      J->weights ? J->weights + row * s->Sk : NULL, J->lse ? J->lse + row : NULL, sc);
       }
     }
   }
@@ -208,11 +217,11 @@ static int check_shape(const oracle_shape* s, int mask, const int32_t* kv_lens) 
   return 0;
 }
 
-/* Full problem. out: [B,Hq,Sq,D]; weights (optional): [B,Hq,Sq,Sk].
- * Returns 0, -1 on a bad argument, -2 when memory runs out. */
+/* Full problem. out: [B,Hq,Sq,D]; weights (optional): [B,Hq,Sq,Sk]; lse
+ * (optional): [B,Hq,Sq]. Returns 0, -1 on a bad argument, -2 when memory runs out. */
 int oracle_attention(const oracle_shape* s, const double* q, const double* k, const double* v,
                      int mask, const int32_t* kv_lens, const double* bias, double scale,
-                     double* out, double* weights, int nthreads) {
+                     double* out, double* weights, double* lse, int nthreads) {
   if (check_shape(s, mask, kv_lens)) return -1;
   if (bias && !((s->bias_b == 1 || s->bias_b == s->B) && (s->bias_h == 1 || s->bias_h == s->Hq)))
     return -1;
@@ -223,13 +232,16 @@ int oracle_attention(const oracle_shape* s, const double* q, const double* k, co
   J.n_items = s->B * s->Hq;
   J.out = out;
   J.weights = weights;
+  J.lse = lse;
   return run(&J, nthreads);
 }
 
-/* Selected rows only. rows: nrows triples (b, hq, i); out: [nrows, D]. */
+/* Selected rows only. rows: nrows triples (b, hq, i); out: [nrows, D]; lse
+ * (optional): [nrows]. */
 int oracle_attention_rows(const oracle_shape* s, const double* q, const double* k, const double* v,
                           int mask, const int32_t* kv_lens, const double* bias, double scale,
-                          int64_t nrows, const int64_t* rows, double* out, int nthreads) {
+                          int64_t nrows, const int64_t* rows, double* out, double* lse,
+                          int nthreads) {
   if (check_shape(s, mask, kv_lens)) return -1;
   if (bias && !((s->bias_b == 1 || s->bias_b == s->B) && (s->bias_h == 1 || s->bias_h == s->Hq)))
     return -1;
@@ -244,5 +256,6 @@ int oracle_attention_rows(const oracle_shape* s, const double* q, const double* 
   J.n_items = nrows;
   J.rows = rows;
   J.out = out;
+  J.lse = lse;
   return run(&J, nthreads);
 }

@@ -30,6 +30,8 @@ MUTANTS = {
     "bias_row_index": ("brow = P->bias + ((bb * s->bias_h + bh) * Sq + i) * Sk;",
                        "brow = P->bias + ((bb * s->bias_h + bh) * Sq + (Sq - 1 - i)) * Sk;"),
     "bias_head_ignored": ("int64_t bh = (s->bias_h == 1) ? 0 : hq;", "int64_t bh = 0;"),
+    "lse_no_max": ("if (lse) *lse = m + log(l);", "if (lse) *lse = log(l);"),
+    "lse_log2": ("if (lse) *lse = m + log(l);", "if (lse) *lse = m + log2(l);"),
     "q_head_index": ("const double* qi = P->q + ((b * s->Hq + hq) * Sq + i) * D;",
                      "const double* qi = P->q + ((b * s->Hq + hk) * Sq + i) * D;"),
 }
@@ -41,6 +43,8 @@ def _pins():
     yield pins.test_hand_solved_two_by_two
     yield pins.test_single_head_textbook_softmax
     yield pins.test_gqa_equals_mha_with_repeated_kv_heads
+    yield pins.test_lse_hand_solved_and_single_key
+    yield pins.test_lse_merges_two_key_halves
     for mask in (0, pins.CAUSAL, pins.PAD, pins.CAUSAL | pins.PAD):
         yield lambda m=mask: pins.test_identical_keys_give_mean_of_visible_values(m)
         yield lambda m=mask: pins.test_weights_are_row_stochastic_and_zero_where_masked(m)

@@ -334,3 +334,82 @@ def test_widen_is_exact():
     # 1.00390625 = 1 + 2^-8 is a tie between bf16 neighbours 1 and 1 + 2^-7: even -> 1.0
     # 1.01171875 = 1 + 3*2^-8 ties between 1 + 2^-7 and 1 + 2^-6: even mantissa -> 1 + 2^-6
     np.testing.assert_array_equal(oracle.widen(bits, "bf16"), [1.0, -2.5, 3.140625, 1.0, 1.015625])
+
+
+# --------------------------------------------------------------- log-sum-exp
+def test_lse_hand_solved_and_single_key():
+    """Row log-sum-exp: the 2x2 hand case gives log(e + 1) and log 2; one key gives its score."""
+    q = np.array([[[[1.0, 0.0], [0.0, 1.0]]]])
+    k = np.array([[[[1.0, 0.0], [0.0, 0.0]]]])
+    v = np.array([[[[1.0, 2.0], [3.0, 4.0]]]])
+    _, lse = run(q, k, v, scale=1.0, lse=True)
+    np.testing.assert_allclose(lse[0, 0], [math.log(math.e + 1.0), math.log(2.0)], rtol=0, atol=1e-15)
+    _, lse_c = run(q, k, v, scale=1.0, mask=CAUSAL, lse=True)
+    np.testing.assert_allclose(lse_c[0, 0], [1.0, math.log(2.0)], rtol=0, atol=1e-15)
+    q1, k1, v1 = rnd(60, 1, 2, 3, 4), rnd(61, 1, 2, 1, 4), rnd(62, 1, 2, 1, 4)
+    _, lse1 = run(q1, k1, v1, scale=0.7, lse=True)
+    np.testing.assert_allclose(lse1, 0.7 * np.einsum("bhid,bhjd->bhi", q1, k1), rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("mask", [0, CAUSAL, PAD])
+def test_lse_identical_keys_is_score_plus_log_count(mask):
+    B, H, S, D = 2, 2, 20, 8
+    q = rnd(63, B, H, S, D)
+    k = np.broadcast_to(rnd(64, 1, 1, 1, D), (B, H, S, D)).copy()
+    v = rnd(65, B, H, S, D)
+    lens = np.array([S, 7], dtype=np.int32)
+    _, lse = run(q, k, v, mask=mask, kv_lens=lens if mask & PAD else None, scale=0.3, lse=True)
+    s = 0.3 * np.einsum("bhid,d->bhi", q, k[0, 0, 0])
+    for b in range(B):
+        L = int(lens[b]) if mask & PAD else S
+        n = np.array([min(L, i + 1) if mask & CAUSAL else L for i in range(S)])
+        np.testing.assert_allclose(lse[b], s[b] + np.log(n)[None, :], rtol=0, atol=1e-13)
+
+
+def test_lse_merges_two_key_halves():
+    """Splitting the keys into two ranges and merging by log-sum-exp gives the whole row:
+    lse = log(e^lseA + e^lseB), O = (e^lseA O_A + e^lseB O_B) / e^lse."""
+    B, H, Sk, D = 2, 3, 50, 8
+    q, k, v = rnd(66, B, H, 7, D, scale=2), rnd(67, B, H, Sk, D, scale=2), rnd(68, B, H, Sk, D)
+    o, lse = run(q, k, v, lse=True)
+    oa, la = run(q, k[:, :, :21], v[:, :, :21], lse=True)
+    ob, lb = run(q, k[:, :, 21:], v[:, :, 21:], lse=True)
+    m = np.maximum(la, lb)
+    wa, wb = np.exp(la - m), np.exp(lb - m)
+    np.testing.assert_allclose(lse, m + np.log(wa + wb), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(o, (wa[..., None] * oa + wb[..., None] * ob) / (wa + wb)[..., None],
+                               rtol=0, atol=1e-13)
+
+
+def test_lse_empty_row_is_minus_inf():
+    q, k, v = rnd(69, 1, 1, 5, 4), rnd(70, 1, 1, 3, 4), rnd(71, 1, 1, 3, 4)
+    _, lse = run(q, k, v, mask=CAUSAL, lse=True)  # rows 0, 1 see no key (bottom-right)
+    assert np.all(lse[0, 0, :2] == -np.inf) and np.all(np.isfinite(lse[0, 0, 2:]))
+
+
+def test_lse_brute_force_tiny():
+    """50-digit log of the raw exp-sum, all masks and a per-head bias."""
+    import mpmath
+    mpmath.mp.dps = 50
+    B, Hq, Hkv, Sq, Sk, D = 2, 4, 2, 4, 6, 3
+    q, k = rnd(72, B, Hq, Sq, D, scale=0.8), rnd(73, B, Hkv, Sk, D, scale=0.8)
+    v = rnd(74, B, Hkv, Sk, D)
+    bias = rnd(75, 1, Hq, Sq, Sk, scale=0.5)
+    lens = np.array([6, 3], dtype=np.int32)
+    for mask in (0, CAUSAL, PAD, CAUSAL | PAD):
+        _, lse = run(q, k, v, mask=mask, kv_lens=lens if mask & PAD else None, bias=bias, scale=0.45, lse=True)
+        kk = np.repeat(k, Hq // Hkv, axis=1)
+        for b in range(B):
+            for h in range(Hq):
+                for i in range(Sq):
+                    terms = []
+                    for j in range(Sk):
+                        if (mask & CAUSAL) and j - i > Sk - Sq:
+                            continue
+                        if (mask & PAD) and j >= lens[b]:
+                            continue
+                        dot = mpmath.fsum(mpmath.mpf(float(q[b, h, i, d])) * mpmath.mpf(float(kk[b, h, j, d]))
+                                          for d in range(D))
+                        terms.append(mpmath.exp(mpmath.mpf(0.45) * dot + mpmath.mpf(float(bias[0, h, i, j]))))
+                    ref = float(mpmath.log(mpmath.fsum(terms))) if terms else -math.inf
+                    assert abs(lse[b, h, i] - ref) <= 1e-13 or lse[b, h, i] == ref
