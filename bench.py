@@ -35,6 +35,8 @@ from exact_scaled_dot_flash_gb300 import synth  # noqa: E402
 WORKLOAD = "bf16_causal_4k"
 METRIC = "attention fwd TFLOP/s and % of GB300 BF16 peak (causal, S=4096, D=128)"
 KERNEL_NAME = "attn_fwd_tc_kernel"
+# key-range splits per workload (1 when absent): enough CTAs for 152 SMs
+SPLITS = {"bf16_gqa_chunk_32k": 4}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -209,6 +211,22 @@ def bench_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def step_flops(w):
+    """FLOPs of one step and their basis.
+
+    Square causal problems use the nominal count 4*B*Hq*Sq*Sk*D / 2 of the
+    headline metric. Otherwise (a causal window with Sq != Sk) the count is
+    exact: 4*D per visible (query, key) pair, row i seeing min(Sk, i + Sk - Sq + 1)
+    keys under the bottom-right causal mask.
+    """
+    if not w.causal or w.Sq == w.Sk:
+        return w.flops(), "nominal 4*B*Hq*Sq*Sk*D" + (" / 2 (causal)" if w.causal else "")
+    import numpy as np
+    i = np.arange(w.Sq, dtype=np.int64)
+    pairs = int(np.clip(i + (w.Sk - w.Sq) + 1, 0, w.Sk).sum())
+    return 4.0 * w.B * w.Hq * w.D * pairs, "exact: 4*D per visible (query, key) pair"
+
+
 def bench_gpu(args):
     import torch
     from exact_scaled_dot_flash_gb300 import attn
@@ -229,8 +247,15 @@ def bench_gpu(args):
     scale = x["scale"]
     causal = w.causal
 
+    splits = args.splits if args.splits else SPLITS.get(w.name, 1)
+    ws = None
+    if splits > 1:
+        shp = attn.Shape(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, 1, 1)
+        ws = torch.empty(attn.split_workspace_bytes(shp, splits), dtype=torch.uint8, device=device)
+
     def step():
-        attn.fwd(q, k, v, causal=causal, kv_lens=lens, bias=bias, scale=scale, out=out, stream=stream)
+        attn.fwd(q, k, v, causal=causal, kv_lens=lens, bias=bias, scale=scale, out=out, stream=stream,
+                 num_splits=splits, workspace=ws)
 
     def barrier():
         if world > 1:
@@ -264,7 +289,7 @@ def bench_gpu(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         elapsed_ms = float(tt.item())
     ms = elapsed_ms / args.steps
-    flops = w.flops()
+    flops, flops_basis = step_flops(w)
     value = world * flops / (ms * 1e-3) / 1e12
 
     # end to end through the public API with host buffers (pinned), copies inside
@@ -276,7 +301,14 @@ def bench_gpu(args):
         e2e_steps = max(3, min(20, args.steps))
 
         def e2e_step():
-            attn.fwd(qh, kh, vh, causal=causal, kv_lens=lh, bias=bh, scale=scale, out=oh)
+            if splits == 1:
+                attn.fwd(qh, kh, vh, causal=causal, kv_lens=lh, bias=bh, scale=scale, out=oh)
+            else:  # the same public call on device copies made inside the step
+                up = [None if a is None else a.to(device, non_blocking=True) for a in (qh, kh, vh, lh, bh)]
+                o = attn.fwd(up[0], up[1], up[2], causal=causal, kv_lens=up[3], bias=up[4], scale=scale,
+                             num_splits=splits, workspace=ws)
+                oh.copy_(o, non_blocking=True)
+                torch.cuda.current_stream(device).synchronize()
 
         for _ in range(2):
             e2e_step()
@@ -294,7 +326,7 @@ def bench_gpu(args):
             e2e_s = float(tt.item())
         h2d = sum(a.numel() * a.element_size() for a in hosts if a is not None)
         d2h = oh.numel() * oh.element_size()
-        e2e = {"value": world * w.flops() / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
                "path": "attn.fwd on pinned host tensors: H2D copies, attn_fwd, D2H copy, sync"}
 
@@ -312,6 +344,7 @@ def bench_gpu(args):
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
                    "causal": w.causal, "key_padding": bool(w.mask & synth.MASK_KEY_PADDING),
                    "bias": [w.bias_b, w.bias_h] if w.bias else None, "parallelism": f"replicas x{world}",
+                   "num_splits": splits, "flops_basis": flops_basis,
                    "l2": (f"inputs larger than L2: {w.io_bytes() / 2**20:.0f} MiB per step vs 129 MB L2, no flush"
                           if w.io_bytes() > 129e6 else
                           f"working set {w.io_bytes() / 2**20:.1f} MiB fits in L2 (L2-hot steps)")},
@@ -323,7 +356,7 @@ def bench_gpu(args):
                      "hbm_gbs_algorithmic": hbm_gbs,
                      "hbm_frac": hbm_gbs / float(peaks["hbm_gbs"])},
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if splits > 1 else 1),
         "clocks": clocks.summary(),
     }
     if world == 1 and not args.no_cpu_baseline and w.name == WORKLOAD:
@@ -343,6 +376,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--splits", type=int, default=0,
+                    help="key-range splits (attn_fwd_split); 0 = the workload's default")
     args = ap.parse_args()
     if args.impl == "reference":
         bench_reference(args)

@@ -54,6 +54,13 @@ def load_library():
         lib.attn_fwd.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, ctypes.c_int, vp, vp,
                                  ctypes.c_float, ctypes.c_int, vp, vp]
         lib.attn_fwd.restype = ctypes.c_int
+        lib.attn_fwd_split.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, ctypes.c_int, vp, vp,
+                                       ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t,
+                                       vp, vp, vp]
+        lib.attn_fwd_split.restype = ctypes.c_int
+        lib.attn_split_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.c_int,
+                                                   ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_split_workspace_bytes.restype = ctypes.c_int
         lib.attn_strerror.argtypes = [ctypes.c_int]
         lib.attn_strerror.restype = ctypes.c_char_p
         lib.attn_last_cuda_error.argtypes = []
@@ -105,14 +112,36 @@ def call(shape: Shape, q_ptr, k_ptr, v_ptr, mask: int, kv_lens_ptr, bias_ptr, sc
                        out_ptr or None, stream_handle or None))
 
 
+def call_split(shape: Shape, q_ptr, k_ptr, v_ptr, mask: int, kv_lens_ptr, bias_ptr, scale: float,
+               dtype: int, num_splits: int, ws_ptr, ws_bytes: int, out_ptr, lse_ptr,
+               stream_handle) -> None:
+    """Raw attn_fwd_split call with integer pointers (0 for NULL); raises on error."""
+    lib = load_library()
+    check(lib.attn_fwd_split(ctypes.byref(shape), q_ptr or None, k_ptr or None, v_ptr or None,
+                             int(mask), kv_lens_ptr or None, bias_ptr or None, float(scale), int(dtype),
+                             int(num_splits), ws_ptr or None, int(ws_bytes), out_ptr or None,
+                             lse_ptr or None, stream_handle or None))
+
+
+def split_workspace_bytes(shape: Shape, num_splits: int) -> int:
+    """Workspace bytes attn_fwd_split needs for ``shape`` and ``num_splits``."""
+    n = ctypes.c_size_t(0)
+    check(load_library().attn_split_workspace_bytes(ctypes.byref(shape), int(num_splits),
+                                                    ctypes.byref(n)))
+    return n.value
+
+
 def fwd(q, k, v, *, causal: bool = False, kv_lens=None, bias=None, scale: float | None = None,
-        out=None, stream=None):
+        out=None, stream=None, num_splits: int = 1, return_lse: bool = False, workspace=None):
     """O = softmax(Q K^T * scale + mask + bias) V on the GPU.
 
     q: [B,Hq,Sq,D]; k, v: [B,Hkv,Sk,D]; float32, float16 or bfloat16, contiguous.
     kv_lens: int32 [B] valid key counts (enables the key-padding mask).
     bias: float32 [bias_b, bias_h, Sq, Sk], bias_b in {1,B}, bias_h in {1,Hq}.
     scale: defaults to 1/sqrt(D).
+    num_splits: 1..32 key-range splits (attn_fwd_split); the fp32 workspace is
+    taken from ``workspace`` (a CUDA uint8 tensor) or allocated here.
+    return_lse: also return the float32 [B,Hq,Sq] row log-sum-exp.
     Tensors on a CUDA device run on ``stream`` (default: the current stream)
     and the result is returned without synchronising. Host tensors are copied
     to the current CUDA device, computed there, and the result is copied back
@@ -121,6 +150,8 @@ def fwd(q, k, v, *, causal: bool = False, kv_lens=None, bias=None, scale: float 
     import torch
 
     if q.device.type == "cpu":
+        if num_splits != 1 or return_lse:
+            raise AttnError("host tensors support num_splits=1 without lse only")
         return _fwd_host(q, k, v, causal=causal, kv_lens=kv_lens, bias=bias, scale=scale, out=out)
     dev = q.device
     for name, t in (("k", k), ("v", v)):
@@ -163,9 +194,20 @@ def fwd(q, k, v, *, causal: bool = False, kv_lens=None, bias=None, scale: float 
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     shape = Shape(B, Hq, Hkv, Sq, Sk, D, bb, bh)
-    call(shape, q.data_ptr(), k.data_ptr(), v.data_ptr(), mask, kv_ptr, b_ptr, scale,
-         _dtype_code(q), out.data_ptr(), stream.cuda_stream)
-    return out
+    if num_splits == 1 and not return_lse:
+        call(shape, q.data_ptr(), k.data_ptr(), v.data_ptr(), mask, kv_ptr, b_ptr, scale,
+             _dtype_code(q), out.data_ptr(), stream.cuda_stream)
+        return out
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=dev) if return_lse else None
+    need = split_workspace_bytes(shape, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    elif workspace.device != dev or workspace.numel() * workspace.element_size() < need:
+        raise AttnError(f"workspace must hold {need} bytes on q's device")
+    call_split(shape, q.data_ptr(), k.data_ptr(), v.data_ptr(), mask, kv_ptr, b_ptr, scale,
+               _dtype_code(q), num_splits, workspace.data_ptr() if need else 0, need,
+               out.data_ptr(), lse.data_ptr() if lse is not None else 0, stream.cuda_stream)
+    return (out, lse) if return_lse else out
 
 
 def _fwd_host(q, k, v, *, causal, kv_lens, bias, scale, out):

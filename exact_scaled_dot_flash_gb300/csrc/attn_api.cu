@@ -71,6 +71,27 @@ bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
 
 int elem_size(attn_dtype_t d) { return d == ATTN_F32 ? 4 : 2; }
 
+
+// Workspace of a split-KV call: fp32 partial O [num_splits, B*Hq, Sq, D], then
+// (at the next 256-byte boundary) the (m, l) float pairs [num_splits, B*Hq, Sq].
+struct SplitLayout {
+  int64_t o_bytes = 0, ml_offset = 0, total = 0;
+};
+SplitLayout split_layout(const attn_shape_t& s, int num_splits) {
+  SplitLayout L;
+  if (num_splits <= 1) return L;
+  const int64_t rows = static_cast<int64_t>(num_splits) * s.B * s.Hq * s.Sq;
+  L.o_bytes = rows * s.D * 4;
+  L.ml_offset = (L.o_bytes + 255) / 256 * 256;
+  L.total = L.ml_offset + rows * 8;
+  return L;
+}
+
+int run(const attn_shape_t* shape, const void* q, const void* k, const void* v, int mask_kind,
+        const int32_t* kv_lens, const float* bias, float scale, attn_dtype_t dtype,
+        int num_splits, void* workspace, size_t workspace_bytes, void* out, float* lse,
+        void* stream);
+
 }  // namespace
 
 extern "C" {
@@ -92,6 +113,8 @@ const char* attn_strerror(int code) {
     case ATTN_ERR_OVERLAP: return "out overlaps an input";
     case ATTN_ERR_CUDA: return "CUDA call failed";
     case ATTN_ERR_TIMEOUT: return "a kernel wait timed out";
+    case ATTN_ERR_SPLITS: return "num_splits must be in [1, 32]";
+    case ATTN_ERR_WORKSPACE: return "split workspace is NULL or smaller than attn_split_workspace_bytes";
     default: return "unknown status code";
   }
 }
@@ -128,6 +151,35 @@ int attn_selftest_wait_timeout(unsigned int limit_us, void* stream) {
 int attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void* v,
              int mask_kind, const int32_t* kv_lens, const float* bias, float scale,
              attn_dtype_t dtype, void* out, void* stream) {
+  return run(shape, q, k, v, mask_kind, kv_lens, bias, scale, dtype, 1, nullptr, 0, out, nullptr,
+             stream);
+}
+
+int attn_split_workspace_bytes(const attn_shape_t* shape, int num_splits, size_t* bytes) {
+  if (!shape || !bytes) return ATTN_ERR_NULL;
+  const attn_shape_t s = *shape;
+  if (s.B < 0 || s.Sq < 0 || s.Hq <= 0 || s.D <= 0) return ATTN_ERR_SHAPE;
+  if (num_splits < 1 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
+  *bytes = static_cast<size_t>(split_layout(s, num_splits).total);
+  return ATTN_OK;
+}
+
+int attn_fwd_split(const attn_shape_t* shape, const void* q, const void* k, const void* v,
+                   int mask_kind, const int32_t* kv_lens, const float* bias, float scale,
+                   attn_dtype_t dtype, int num_splits, void* workspace, size_t workspace_bytes,
+                   void* out, float* lse, void* stream) {
+  return run(shape, q, k, v, mask_kind, kv_lens, bias, scale, dtype, num_splits, workspace,
+             workspace_bytes, out, lse, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int run(const attn_shape_t* shape, const void* q, const void* k, const void* v, int mask_kind,
+        const int32_t* kv_lens, const float* bias, float scale, attn_dtype_t dtype,
+        int num_splits, void* workspace, size_t workspace_bytes, void* out, float* lse,
+        void* stream) {
   // ---- validation: everything is checked before any CUDA call
   if (!shape) return ATTN_ERR_NULL;
   const attn_shape_t s = *shape;
@@ -150,6 +202,10 @@ int attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void
   if (bhq > 0x7fffffffLL) return ATTN_ERR_SHAPE;
   const int rows_per_cta = tensor_core ? 256 : 64;
   if ((static_cast<int64_t>(s.Sq) + rows_per_cta - 1) / rows_per_cta > 65535) return ATTN_ERR_SHAPE;
+  if (num_splits < 1 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
+  if (tensor_core && bhq * ((static_cast<int64_t>(s.Sq) + 255) / 256) * num_splits > 0x7fffffffLL)
+    return ATTN_ERR_SHAPE;
+  if (num_splits > 1 && bhq * s.Sq * (s.D / 4) / 256 >= 0x7fffffffLL) return ATTN_ERR_SHAPE;
   if (s.B == 0 || s.Sq == 0) return ATTN_OK;  // nothing to compute
   if (!q || !out || (s.Sk > 0 && (!k || !v))) return ATTN_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_ALIGN;
@@ -164,11 +220,34 @@ int attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void
       overlaps(out, out_bytes, v, kv_bytes) || overlaps(out, out_bytes, bias, bias_bytes) ||
       overlaps(out, out_bytes, kv_lens, static_cast<int64_t>(s.B) * 4))
     return ATTN_ERR_OVERLAP;
+  // every buffer the call writes (out, lse, workspace) is disjoint from every
+  // other buffer it touches
+  const int64_t lse_bytes = lse ? bhq * s.Sq * 4 : 0;
+  if (lse) {
+    if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_ALIGN;
+    if (overlaps(lse, lse_bytes, q, out_bytes) || overlaps(lse, lse_bytes, k, kv_bytes) ||
+        overlaps(lse, lse_bytes, v, kv_bytes) || overlaps(lse, lse_bytes, bias, bias_bytes) ||
+        overlaps(lse, lse_bytes, kv_lens, static_cast<int64_t>(s.B) * 4) ||
+        overlaps(lse, lse_bytes, out, out_bytes))
+      return ATTN_ERR_OVERLAP;
+  }
+  const SplitLayout lay = split_layout(s, num_splits);
+  if (num_splits > 1 && s.Sk > 0) {
+    if (!workspace || workspace_bytes < static_cast<size_t>(lay.total)) return ATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+    const int64_t wb = lay.total;
+    if (overlaps(workspace, wb, q, out_bytes) || overlaps(workspace, wb, k, kv_bytes) ||
+        overlaps(workspace, wb, v, kv_bytes) || overlaps(workspace, wb, bias, bias_bytes) ||
+        overlaps(workspace, wb, kv_lens, static_cast<int64_t>(s.B) * 4) ||
+        overlaps(workspace, wb, out, out_bytes) || overlaps(workspace, wb, lse, lse_bytes))
+      return ATTN_ERR_OVERLAP;
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (s.Sk == 0) {  // no key at all: every row is undefined
     cudaError_t e = attn::launch_nan_fill(out, bhq * s.Sq * s.D,
                                           dtype == ATTN_F32 ? 4 : (dtype == ATTN_F16 ? 2 : 3), st);
+    if (e == cudaSuccess && lse) e = attn::launch_f32_fill(lse, bhq * s.Sq, -INFINITY, st);
     return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
   }
 
@@ -193,6 +272,18 @@ int attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status_ptr(dev);
   p.device = dev;
+  p.num_splits = num_splits;
+  p.ws_o = num_splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  p.ws_ml = num_splits > 1
+                ? reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + lay.ml_offset)
+                : nullptr;
+  p.lse = lse;
+  // after the partial kernel, the merge: O and lse from the split partials
+  auto finish = [&](cudaError_t err) -> int {
+    if (err == cudaSuccess && num_splits > 1)
+      err = attn::launch_split_merge(p, s.D, static_cast<int>(dtype), out, st);
+    return err == cudaSuccess ? ATTN_OK : fail_cuda(err);
+  };
 
   if (!tensor_core) {
     int unsupported = 0;
@@ -200,7 +291,7 @@ int attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void
                          static_cast<const float*>(k), static_cast<const float*>(v),
                          static_cast<float*>(out), st, &unsupported);
     if (unsupported) return ATTN_ERR_HEAD_DIM;
-    return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+    return finish(e);
   }
 
   attn::EncodeTiledFn enc = encode_fn();
@@ -210,7 +301,10 @@ int attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void
   // allow 16-byte TMA strides; otherwise read directly by the softmax threads
   const int bmode = !bias ? 0 : ((s.D <= 64 && p.bias_vec4) ? 2 : 1);
   using namespace attn::tc;
-#define ATTN_TC_CALL(DD, BB, MM) launch_tc_instance<DD, BB, MM>(enc, q, k, v, out, p, st)
+#define ATTN_TC_CALL(DD, BB, MM)                                                                \
+  (num_splits > 1 ? launch_tc_instance<DD, BB, MM, EPI_PARTIAL>(enc, q, k, v, out, p, st)      \
+   : lse          ? launch_tc_instance<DD, BB, MM, EPI_O_LSE>(enc, q, k, v, out, p, st)        \
+                  : launch_tc_instance<DD, BB, MM, EPI_O>(enc, q, k, v, out, p, st))
 #define ATTN_TC_DISPATCH(DD, STAGED)                                                           \
   case DD:                                                                                     \
     if (bmode == 2)                                                                            \
@@ -229,7 +323,7 @@ int attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void
   }
 #undef ATTN_TC_CALL
 #undef ATTN_TC_DISPATCH
-  return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+  return finish(e);
 }
 
-}  // extern "C"
+}  // namespace

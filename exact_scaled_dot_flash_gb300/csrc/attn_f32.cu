@@ -10,6 +10,9 @@
 // thread computes its quad's 32 scores (partial dot products reduced with two
 // xor shuffles), keeps the running max m and sum l in the log2 domain, and
 // rescales its accumulator when m grows.
+// Split-KV (blockIdx.z = split): the CTA's visible key range is cut into
+// num_splits runs of whole key tiles; a split CTA writes its unnormalised
+// accumulator and (m, l) to the workspace for the merge kernel.
 #include "params.h"
 #include "ptx.cuh"
 
@@ -20,6 +23,7 @@ constexpr int ROWS = 64;
 constexpr int THREADS = 256;
 constexpr int KT = 32;  // keys per shared-memory tile
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
 
 template <int D, bool BIAS>
 __global__ void __launch_bounds__(THREADS)
@@ -52,6 +56,14 @@ __global__ void __launch_bounds__(THREADS)
   int hi = key_lim;  // keys any row of this CTA may see
   if (p.causal) hi = min(hi, min(q0 + ROWS - 1, p.Sq - 1) + diag + 1);
   const int causal_lim = p.causal ? row_g + diag : 0x7fffffff;
+  // this split's keys: whole tiles [klo, khi) of the CTA's range [0, hi)
+  int klo = 0, khi = hi;
+  if (p.num_splits > 1) {
+    const int64_t nt = hi > 0 ? (hi + KT - 1) / KT : 0;
+    const int64_t split = blockIdx.z;
+    klo = static_cast<int>(split * nt / p.num_splits) * KT;
+    khi = min(hi, static_cast<int>((split + 1) * nt / p.num_splits) * KT);
+  }
 
   float4 qr[GPT], acc[GPT];
   const float4* qrow = reinterpret_cast<const float4*>(q + ((size_t)bh * p.Sq + row_g) * D);
@@ -72,11 +84,11 @@ __global__ void __launch_bounds__(THREADS)
   const float4* vh = reinterpret_cast<const float4*>(v + (size_t)bhk * p.Sk * D);
 
   float m_run = -INFINITY, l_run = 0.f;
-  for (int key0 = 0; key0 < hi; key0 += KT) {
+  for (int key0 = klo; key0 < khi; key0 += KT) {
     __syncthreads();
     for (int e = tid; e < KT * G; e += THREADS) {
       const int r = e / G, g = e - (e / G) * G;
-      const bool in = key0 + r < hi;
+      const bool in = key0 + r < khi;
       ks[r][g] = in ? __ldg(kh + (size_t)(key0 + r) * G + g) : make_float4(0.f, 0.f, 0.f, 0.f);
       vs[r][g] = in ? __ldg(vh + (size_t)(key0 + r) * G + g) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -132,6 +144,18 @@ __global__ void __launch_bounds__(THREADS)
     }
   }
   if (!row_ok) return;
+  if (p.num_splits > 1) {
+    // partial result: accumulator relative to 2^m_run, and (m_run, l_run)
+    const size_t r = (static_cast<size_t>(blockIdx.z) * p.B * p.Hq + bh) * p.Sq + row_g;
+    float4* wrow = reinterpret_cast<float4*>(p.ws_o + r * D);
+#pragma unroll
+    for (int i = 0; i < GPT; ++i) wrow[part + 4 * i] = acc[i];
+    if (part == 0) p.ws_ml[r] = make_float2(m_run, l_run);
+    return;
+  }
+  if (p.lse != nullptr && part == 0)
+    p.lse[static_cast<size_t>(bh) * p.Sq + row_g] =
+        l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
   const float inv = l_run > 0.f ? 1.f / l_run : __int_as_float(0x7fc00000);
   float4* orow = reinterpret_cast<float4*>(out + ((size_t)bh * p.Sq + row_g) * D);
 #pragma unroll
@@ -146,7 +170,7 @@ template <int D, bool BIAS>
 static cudaError_t launch_one(const KernelParams& p, const float* q, const float* k,
                               const float* v, float* out, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(p.B) * static_cast<unsigned>(p.Hq),
-            static_cast<unsigned>((p.Sq + ROWS - 1) / ROWS));
+            static_cast<unsigned>((p.Sq + ROWS - 1) / ROWS), static_cast<unsigned>(p.num_splits));
   attn_fwd_f32_kernel<D, BIAS><<<grid, THREADS, 0, stream>>>(q, k, v, out, p);
   return cudaGetLastError();
 }

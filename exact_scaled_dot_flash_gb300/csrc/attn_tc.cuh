@@ -35,6 +35,12 @@
 // the result is unchanged.
 // Every mbarrier wait is bounded; on expiry the CTA records STATUS_TIMEOUT in
 // the device status word, drains its own copies and MMAs, frees TMEM and exits.
+// Split-KV: with num_splits > 1 the grid has one CTA per (work item, split);
+// a CTA runs the key tiles of its split only (tile counters stay local to the
+// split, key positions absolute) and writes its unnormalised O rows with their
+// (m, l) to the workspace instead of O; launch_split_merge combines them. With
+// one split the epilogue writes O, and with EPI_O_LSE also the row log-sum-exp
+// (a separate instance: the extra store costs the O-only kernel registers).
 #pragma once
 
 #include <atomic>
@@ -55,6 +61,7 @@ constexpr int TMEM_COLS = 512;
 constexpr int REG_SOFTMAX = 200;  // 2*128*200 + 128*96 <= 384 * 168 (launch allocation)
 constexpr int REG_OTHER = 96;
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
 constexpr float RESCALE_LOG2 = 8.0f;  // lazy-rescale threshold (log2 units)
 constexpr int HEAD_GROUP = 16;        // heads scheduled together so their K/V stay in L2
 constexpr int BIAS_CHUNK = 32;                     // keys per staged bias chunk
@@ -110,19 +117,24 @@ struct Work {
   int n[NQ];       // K/V tiles Q tile t needs (0: no visible key at all)
   int nfull[NQ];   // leading K/V tiles of Q tile t with no masked element
   int nmax;
+  int j0;          // first K/V tile of this CTA's split (tile indices above are relative)
 };
 
 // Linear CTA index -> (head, query block). Heads are taken HEAD_GROUP at a
 // time; inside a group the query blocks of all its heads are interleaved,
 // heaviest causal block first, so the K/V of the heads in flight stay in L2
 // and the long blocks start before the short ones.
+// With split-KV (SPLIT) the splits of one work item are adjacent CTAs.
+template <bool SPLIT>
 __device__ __forceinline__ Work make_work(const KernelParams& p) {
   Work w;
   const int qblocks = (p.Sq + NQ * BM - 1) / (NQ * BM);
   const int bhq = p.B * p.Hq;
   const int per_group = qblocks * HEAD_GROUP;
-  const int g = static_cast<int>(blockIdx.x) / per_group;
-  const int within = static_cast<int>(blockIdx.x) - g * per_group;
+  const int item = SPLIT ? static_cast<int>(blockIdx.x) / p.num_splits : static_cast<int>(blockIdx.x);
+  const int split = SPLIT ? static_cast<int>(blockIdx.x) - item * p.num_splits : 0;
+  const int g = item / per_group;
+  const int within = item - g * per_group;
   const int hg = min(HEAD_GROUP, bhq - g * HEAD_GROUP);
   const int rank = within / hg;
   w.bh = g * HEAD_GROUP + (within - rank * hg);
@@ -157,10 +169,23 @@ __device__ __forceinline__ Work make_work(const KernelParams& p) {
     }
     w.nmax = max(w.nmax, w.n[t]);
   }
+  w.j0 = 0;
+  if constexpr (SPLIT) {
+    // balanced contiguous runs of the item's tiles [0, nmax)
+    const int jlo = static_cast<int>(static_cast<int64_t>(split) * w.nmax / p.num_splits);
+    const int jhi = static_cast<int>(static_cast<int64_t>(split + 1) * w.nmax / p.num_splits);
+#pragma unroll
+    for (int t = 0; t < NQ; ++t) {
+      w.n[t] = max(0, min(jhi, w.n[t]) - jlo);
+      w.nfull[t] = max(0, w.nfull[t] - jlo);
+    }
+    w.j0 = jlo;
+    w.nmax = jhi - jlo;
+  }
   return w;
 }
 
-template <int D, bool BF16, int BMODE>
+template <int D, bool BF16, int BMODE, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -169,6 +194,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        const __grid_constant__ CUtensorMap tm_b, const KernelParams p) {
   using C = Cfg<D, BMODE>;
   constexpr bool BIAS = BMODE != BIAS_NONE;
+  constexpr bool SPLIT = EPI == EPI_PARTIAL;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -179,7 +205,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const Work w = make_work(p);
+  const Work w = make_work<SPLIT>(p);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -245,7 +271,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const CUtensorMap* m = kv == 0 ? &tm_k : &tm_v;
             for (int c = 0; c < C::NCHUNK; ++c)
               tma_load_3d(sb + C::OFF_KV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, m,
-                          bar(C::BAR_FULL + s), c * C::BOX_D, j * BN, w.bhk);
+                          bar(C::BAR_FULL + s), c * C::BOX_D, (w.j0 + j) * BN, w.bhk);
           }
         }
         // Drain: every copy this thread issued has landed before the CTA exits.
@@ -277,7 +303,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
               mbar_arrive_expect_tx(bar(C::BAR_BFULL + slot), BIAS_SLOT_BYTES);
               tma_load_3d(sb + C::OFF_BIAS + slot * BIAS_SLOT_BYTES, &tm_b, bar(C::BAR_BFULL + slot),
-                          j * BN + c * BIAS_CHUNK, w.q0 + t * BM, bz);
+                          (w.j0 + j) * BN + c * BIAS_CHUNK, w.q0 + t * BM, bz);
             }
           }
         }
@@ -413,7 +439,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
       }
-      const int key0 = j * BN;
+      const int key0 = (w.j0 + j) * BN;
       if constexpr (BMODE == BIAS_STAGED) {
         // bias chunks from the shared-memory ring (128-byte swizzled rows)
         const uint8_t* ring = smem + C::OFF_BIAS + t * BIAS_SLOTS * BIAS_SLOT_BYTES;
@@ -551,7 +577,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------------------------------------------------------- epilogue
     // Every warp of the warpgroup reaches the named barrier, failed or not, so
     // that a timeout in one warp can never leave the others waiting on it.
-    if (r0 < p.Sq) {
+    if (SPLIT && r0 < p.Sq) {
+      // split partial: unnormalised O row and (m, l), straight to the workspace
+      const bool have = n_t > 0;
+      if (!failed && have) {
+        const bool ok = mbar_wait(bar(C::BAR_O + t), 0);
+        if (__any_sync(0xffffffffu, !ok)) failed = true;
+      }
+      if (failed) {
+        if (lane == 0) fail();
+      } else {
+        tc_fence_after();
+        const size_t rr =
+            (static_cast<size_t>(blockIdx.x % p.num_splits) * p.B * p.Hq + w.bh) * p.Sq +
+            static_cast<size_t>(row_g);
+        float4* wrow = reinterpret_cast<float4*>(p.ws_o + rr * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          if (have) {
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+          if (row_g < p.Sq) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              wrow[8 * c + i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                            __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+          }
+        }
+        if (row_g < p.Sq) p.ws_ml[rr] = have ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
+      }
+    } else if (!SPLIT && r0 < p.Sq) {
       const bool have = n_t > 0;
       if (!failed && have) {
         const bool ok = mbar_wait(bar(C::BAR_O + t), 0);
@@ -563,6 +623,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         // rows with no visible key have an undefined softmax: NaN
         const float inv = (have && l_run > 0.f) ? 1.f / l_run : __int_as_float(0x7fc00000);
+        if (EPI == EPI_O_LSE && row_g < p.Sq)
+          p.lse[static_cast<size_t>(w.bh) * p.Sq + row_g] =
+              (have && l_run > 0.f) ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
         uint8_t* stage = smem + t * C::TILE_BYTES;  // Q_t is dead: reuse it for O_t
         const int swz = C::SWIZZLE == 128 ? (row & 7) : ((row >> 1) & 3);
 #pragma unroll
@@ -635,7 +698,7 @@ static CUresult encode_3d(EncodeTiledFn enc, CUtensorMap* m, bool bf16, const vo
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <int D, bool BF16, int BMODE>
+template <int D, bool BF16, int BMODE, int EPI>
 cudaError_t launch_tc_instance(EncodeTiledFn enc, const void* q, const void* k, const void* v,
                                void* out, const KernelParams& p, cudaStream_t stream) {
   CUtensorMap tq, tk, tv, to, tb;
@@ -659,7 +722,7 @@ cudaError_t launch_tc_instance(EncodeTiledFn enc, const void* q, const void* k, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  auto kern = attn_fwd_tc_kernel<D, BF16, BMODE>;
+  auto kern = attn_fwd_tc_kernel<D, BF16, BMODE, EPI>;
   constexpr int smem = Cfg<D, BMODE>::SMEM_BYTES;
   // The shared-memory opt-in is per device and per kernel: set it once.
   static std::atomic<unsigned long long> configured{0};
@@ -670,7 +733,7 @@ cudaError_t launch_tc_instance(EncodeTiledFn enc, const void* q, const void* k, 
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   const uint64_t qblocks = (static_cast<uint64_t>(p.Sq) + NQ * BM - 1) / (NQ * BM);
-  const uint64_t ctas = bhq * qblocks;
+  const uint64_t ctas = bhq * qblocks * static_cast<uint64_t>(p.num_splits);
   if (ctas > 0x7fffffffull) return cudaErrorInvalidConfiguration;
   kern<<<static_cast<unsigned>(ctas), NUM_THREADS, smem, stream>>>(tq, tk, tv, to, tb, p);
   return cudaGetLastError();

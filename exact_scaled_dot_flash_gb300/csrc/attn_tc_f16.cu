@@ -1,13 +1,13 @@
 // attn_tc_f16.cu - explicit instantiations of the tensor-core kernel for
-// F16 inputs (head dims 32, 64, 128; no bias, bias read directly, bias staged through
-// shared memory for D <= 64).
+// F16 inputs, writing O: head dims 32, 64, 128; no bias, bias read
+// directly, bias staged through shared memory for D <= 64.
 #include "attn_tc.cuh"
 
 namespace attn {
 namespace tc {
 
 #define ATTN_TC_INST(D, MODE)                                                             \
-  template cudaError_t launch_tc_instance<D, false, MODE>(                                  \
+  template cudaError_t launch_tc_instance<D, false, MODE, EPI_O>(                       \
       EncodeTiledFn, const void*, const void*, const void*, void*, const KernelParams&,  \
       cudaStream_t);
 ATTN_TC_INST(32, BIAS_NONE)

@@ -20,6 +20,15 @@ struct KernelParams {
   float scale_log2;       // scale * log2(e): scores are kept in the log2 domain
   int* status;            // device status word (STATUS_* bits)
   int device;             // CUDA device the launch runs on
+  // Split-KV: the visible key range of every work item is cut into
+  // num_splits contiguous parts, one CTA each. With num_splits == 1 the
+  // kernel writes O (and lse, when set) itself; otherwise it writes the
+  // unnormalised partial output and its (m, l) statistics, and
+  // launch_split_merge combines them.
+  int num_splits;
+  float* ws_o;            // [num_splits, B*Hq, Sq, D] fp32 partial O (relative to m)
+  float2* ws_ml;          // [num_splits, B*Hq, Sq] (m in log2 units, l)
+  float* lse;             // [B*Hq*Sq] natural-log row log-sum-exp, or nullptr
 };
 
 // cuTensorMapEncodeTiled, resolved at run time through the runtime's
@@ -33,7 +42,10 @@ namespace tc {
 // How the additive bias reaches the softmax: none; read by each thread from
 // global memory; or staged by TMA through a shared-memory ring (D <= 64).
 constexpr int BIAS_NONE = 0, BIAS_DIRECT = 1, BIAS_STAGED = 2;
-template <int D, bool BF16, int BMODE>
+// What the epilogue writes: O; O and the row log-sum-exp; or, for split-KV
+// (p.num_splits > 1), the unnormalised partials for launch_split_merge.
+constexpr int EPI_O = 0, EPI_O_LSE = 1, EPI_PARTIAL = 2;
+template <int D, bool BF16, int BMODE, int EPI>
 cudaError_t launch_tc_instance(EncodeTiledFn enc, const void* q, const void* k, const void* v,
                                void* out, const KernelParams& p, cudaStream_t stream);
 }  // namespace tc
@@ -43,6 +55,11 @@ cudaError_t launch_f32(int D, bool has_bias, const KernelParams& p, const float*
                        const float* k, const float* v, float* out, cudaStream_t stream,
                        int* unsupported);
 cudaError_t launch_nan_fill(void* out, int64_t count, int elem_bytes, cudaStream_t stream);
+cudaError_t launch_f32_fill(float* out, int64_t count, float value, cudaStream_t stream);
+// O[r,:] = sum_s 2^(m_s - M) O_s[r,:] / sum_s 2^(m_s - M) l_s,  M = max_s m_s;
+// lse[r] = (M + log2 sum_s 2^(m_s - M) l_s) ln 2.  dtype: 0 f32, 1 f16, 2 bf16.
+cudaError_t launch_split_merge(const KernelParams& p, int D, int dtype, void* out,
+                               cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(int* status, unsigned long long limit_ns,
                                       cudaStream_t stream);
 

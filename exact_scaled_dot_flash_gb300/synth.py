@@ -23,7 +23,10 @@ The workload table ``WORKLOADS`` describes the benchmark shapes of the
 attention pages: a small F32 causal case, a char-transformer-sized BF16 block
 (B=8, H=8, S=128, D in {32, 64}), a long-context causal MHA (B=4, H=32,
 S=4096, D=128, plus a wide-score variant with Q,K ~ N(0, 3^2)), a GQA case
-(Hq=32, Hkv=8, S=8192) and an F16 key-padding + bias case.
+(Hq=32, Hkv=8, S=8192) and an F16 key-padding + bias case. One more shape
+exercises split-KV: the newest 256 query rows of a 32768-key GQA context
+(B=1, Hq=32, Hkv=8, D=128, bottom-right causal), where one CTA per 256-row
+block would leave most of the GPU idle.
 """
 from __future__ import annotations
 
@@ -135,6 +138,8 @@ WORKLOADS = {
     "f16_padding_bias": Workload("f16_padding_bias", F16, 16, 16, 16, 1024, 1024, 64,
                                  mask=MASK_KEY_PADDING, bias=True, bias_b=1, bias_h=16,
                                  seed=5, kv_len_range=(256, 1024)),
+    "bf16_gqa_chunk_32k": Workload("bf16_gqa_chunk_32k", BF16, 1, 32, 8, 256, 32768, 128,
+                                   mask=MASK_CAUSAL, seed=6),
 }
 
 

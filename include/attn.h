@@ -33,7 +33,17 @@
 #ifndef ATTN_H_
 #define ATTN_H_
 
+#include <stddef.h>
 #include <stdint.h>
+
+/* The library is built with hidden visibility; only these entry points are
+ * exported, so two copies of it loaded in one process never resolve each
+ * other's internal (kernel) symbols. */
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -61,8 +71,13 @@ enum {
   ATTN_ERR_MASK = -7,      /* unknown mask bits, or KEY_PADDING with kv_lens == NULL  */
   ATTN_ERR_OVERLAP = -8,   /* out overlaps q, k, v, kv_lens or bias                   */
   ATTN_ERR_CUDA = -9,      /* a CUDA call failed; see attn_last_cuda_error()          */
-  ATTN_ERR_TIMEOUT = -10   /* a kernel gave up on a bounded wait (see attn_device_status) */
+  ATTN_ERR_TIMEOUT = -10,  /* a kernel gave up on a bounded wait (see attn_device_status) */
+  ATTN_ERR_SPLITS = -11,   /* num_splits outside [1, ATTN_MAX_SPLITS]                 */
+  ATTN_ERR_WORKSPACE = -12 /* split workspace NULL or smaller than required           */
 };
+
+/* Largest num_splits attn_fwd_split accepts. */
+#define ATTN_MAX_SPLITS 32
 
 /* Problem shape. All counts are elements.
  *   Q   [B, Hq,  Sq, D]   contiguous, row-major
@@ -96,7 +111,7 @@ typedef struct {
  * returning and allocates no device memory. The call does not synchronise;
  * argument errors are reported before anything is launched. Thread-safe.
  * Returns ATTN_OK or a negative ATTN_ERR_* code. */
-int attn_fwd(const attn_shape_t* shape,
+ATTN_API int attn_fwd(const attn_shape_t* shape,
              const void* q, const void* k, const void* v,
              int mask_kind, const int32_t* kv_lens,
              const float* bias,
@@ -104,18 +119,66 @@ int attn_fwd(const attn_shape_t* shape,
              void* out,
              void* stream);
 
+/* attn_fwd_split - attn_fwd with the key range of each query row cut into
+ * `num_splits` parts that run as separate CTAs, and an optional row
+ * log-sum-exp output.
+ *
+ * Source: ruDNN user guide, section 9: a long key history is split into
+ * parts, each part keeps FP32 partial statistics, and the parts are merged.
+ * Part s of a row keeps its running maximum m_s, its exp-sum l_s and its
+ * unnormalised output O_s; the merge rescales each part by exp(m_s - M),
+ * M = max_s m_s, and divides by the rescaled sum, which equals the softmax
+ * over all keys. Splitting gives the GPU enough CTAs when B*Hq*ceil(Sq/256)
+ * is small (few long rows: chunked prefill, decode).
+ *
+ * Arguments are those of attn_fwd, plus:
+ * num_splits: 1..ATTN_MAX_SPLITS. Each (batch, head, 256-row query block)
+ *   cuts its visible key tiles into num_splits balanced contiguous runs
+ *   (a run may be empty when there are fewer tiles than splits). 1 runs the
+ *   attn_fwd kernel unchanged and needs no workspace.
+ * workspace, workspace_bytes: device scratch of at least
+ *   attn_split_workspace_bytes(shape, num_splits) bytes, 16-byte aligned,
+ *   owned by the caller, disjoint from every other buffer; ignored (may be
+ *   NULL) when num_splits == 1. Its contents on entry do not matter and are
+ *   meaningless afterwards; two calls in flight at once need two workspaces.
+ * lse: NULL, or device float [B, Hq, Sq] (4-byte aligned, disjoint from the
+ *   rest) that receives the natural-log row log-sum-exp
+ *   lse = log sum_j exp(s_j) over the visible keys (-inf for a row with no
+ *   visible key, whose output is NaN).
+ *
+ * With num_splits > 1 the result is the same softmax evaluated in a
+ * different summation order, so it agrees with attn_fwd to rounding, not
+ * bit for bit. Asynchronous on `stream` (two kernels when num_splits > 1).
+ * Returns ATTN_OK or a negative ATTN_ERR_* code (ATTN_ERR_SPLITS,
+ * ATTN_ERR_WORKSPACE in addition to attn_fwd's). */
+ATTN_API int attn_fwd_split(const attn_shape_t* shape,
+                   const void* q, const void* k, const void* v,
+                   int mask_kind, const int32_t* kv_lens,
+                   const float* bias,
+                   float scale, attn_dtype_t dtype,
+                   int num_splits, void* workspace, size_t workspace_bytes,
+                   void* out, float* lse,
+                   void* stream);
+
+/* attn_split_workspace_bytes - bytes of workspace attn_fwd_split needs for
+ * `shape` and `num_splits` (0 when num_splits == 1):
+ * num_splits*B*Hq*Sq*(4*D + 8) plus up to 255 bytes of alignment padding.
+ * Writes *bytes. Returns ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_SHAPE or
+ * ATTN_ERR_SPLITS. */
+ATTN_API int attn_split_workspace_bytes(const attn_shape_t* shape, int num_splits, size_t* bytes);
+
 /* attn_strerror - static English text for a status code (never NULL). */
-const char* attn_strerror(int code);
+ATTN_API const char* attn_strerror(int code);
 
 /* attn_last_cuda_error - the cudaError_t value of the last CUDA failure seen
  * by attn_fwd on the calling thread (0 if none). */
-int attn_last_cuda_error(void);
+ATTN_API int attn_last_cuda_error(void);
 
 /* attn_device_status - read (and, when clear != 0, reset) the sticky error
  * word that kernels on `device` set when a bounded wait expires. Writes the
  * flags to *flags (0 = no failure seen). Synchronises with the device.
  * Returns ATTN_OK, ATTN_ERR_NULL or ATTN_ERR_CUDA. */
-int attn_device_status(int device, int* flags, int clear);
+ATTN_API int attn_device_status(int device, int* flags, int clear);
 
 /* attn_selftest_wait_timeout - failure-path self-test (the pages have no
  * counterpart; it checks this library's own error reporting). Launches, on
@@ -125,10 +188,10 @@ int attn_device_status(int device, int* flags, int clear);
  * the timeout bit of the device status word (read it with attn_device_status)
  * and returns; the GPU context stays usable. Asynchronous; returns ATTN_OK,
  * ATTN_ERR_SHAPE for an out-of-range limit, or ATTN_ERR_CUDA. */
-int attn_selftest_wait_timeout(unsigned int limit_us, void* stream);
+ATTN_API int attn_selftest_wait_timeout(unsigned int limit_us, void* stream);
 
 /* attn_version - library version as major*10000 + minor*100 + patch. */
-int attn_version(void);
+ATTN_API int attn_version(void);
 
 #ifdef __cplusplus
 }

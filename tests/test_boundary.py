@@ -132,3 +132,77 @@ def test_python_binding_missing_library_is_an_error(tmp_path, monkeypatch):
     monkeypatch.setattr(A, "_HERE", str(tmp_path))
     with pytest.raises(A.AttnError):
         A.load_library()
+
+
+def call_split(shape, ns=2, ws=FAKE * 512, ws_bytes=1 << 30, lse=0, **kw):
+    """attn_fwd_split with fake, never-dereferenced pointers (validation only)."""
+    lib = A.load_library()
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, mask=0, lens=0, bias=0, scale=0.125, dtype=A.ATTN_BF16,
+             out=FAKE * 64)
+    a.update(kw)
+    return lib.attn_fwd_split(ctypes.byref(shape), a["q"] or None, a["k"] or None, a["v"] or None, a["mask"],
+                              a["lens"] or None, a["bias"] or None, ctypes.c_float(a["scale"]), a["dtype"],
+                              ns, ws or None, ws_bytes, a["out"] or None, lse or None, None)
+
+
+def ws_bytes(shape, ns):
+    n = ctypes.c_size_t(0)
+    rc = A.load_library().attn_split_workspace_bytes(ctypes.byref(shape), ns, ctypes.byref(n))
+    return rc, n.value
+
+
+def test_split_workspace_size(lib):
+    s = _shape(B=2, Hq=3, Hkv=1, Sq=5, Sk=100, D=32)
+    assert ws_bytes(s, 1) == (0, 0)
+    rc, n = ws_bytes(s, 3)
+    rows = 3 * 2 * 3 * 5
+    o_bytes = rows * 32 * 4
+    assert rc == 0 and n == (o_bytes + 255) // 256 * 256 + rows * 8
+    assert ws_bytes(s, 0)[0] == codes["ATTN_ERR_SPLITS"]
+    assert ws_bytes(s, 33)[0] == codes["ATTN_ERR_SPLITS"]
+    assert ws_bytes(_shape(D=0), 2)[0] == codes["ATTN_ERR_SHAPE"]
+    assert lib.attn_split_workspace_bytes(ctypes.byref(s), 2, None) == codes["ATTN_ERR_NULL"]
+
+
+@pytest.mark.parametrize("ns", [0, -1, 33, 1000])
+def test_split_count_out_of_range(lib, ns):
+    assert call_split(_shape(), ns=ns) == codes["ATTN_ERR_SPLITS"]
+
+
+def test_split_workspace_errors(lib):
+    s = _shape()
+    need = ws_bytes(s, 4)[1]
+    assert call_split(s, ns=4, ws=0) == codes["ATTN_ERR_WORKSPACE"]
+    assert call_split(s, ns=4, ws_bytes=need - 1) == codes["ATTN_ERR_WORKSPACE"]
+    assert call_split(s, ns=4, ws=FAKE * 512 + 8, ws_bytes=need) == codes["ATTN_ERR_ALIGN"]
+    # the workspace overlapping q, or the output
+    assert call_split(s, ns=4, ws=FAKE, ws_bytes=need) == codes["ATTN_ERR_OVERLAP"]
+    assert call_split(s, ns=4, ws=FAKE * 64, ws_bytes=need) == codes["ATTN_ERR_OVERLAP"]
+
+
+def test_split_lse_errors(lib):
+    s = _shape()
+    assert call_split(s, ns=1, ws=0, lse=FAKE * 300 + 2) == codes["ATTN_ERR_ALIGN"]
+    assert call_split(s, ns=1, ws=0, lse=FAKE * 64) == codes["ATTN_ERR_OVERLAP"]  # lse inside out
+    assert call_split(s, ns=2, ws=FAKE * 300, ws_bytes=1 << 20, lse=FAKE * 300 + 64) == \
+        codes["ATTN_ERR_OVERLAP"]  # lse inside the workspace
+
+
+def test_split_empty_problem_is_noop(lib):
+    assert call_split(_shape(B=0), ns=8, ws=0) == codes["ATTN_OK"]
+    assert call_split(_shape(Sq=0), ns=8, ws=0) == codes["ATTN_OK"]
+
+
+def test_library_exports_only_the_c_abi(lib):
+    # hidden visibility: kernels and helpers stay internal, so two builds of
+    # the library loaded in one process never bind to each other's kernels
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", A.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    names = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    names = {n for n in names if not n.startswith("_")}  # linker-provided markers
+    assert names == set(declared_functions())
