@@ -115,6 +115,8 @@ const char* attn_strerror(int code) {
     case ATTN_ERR_TIMEOUT: return "a kernel wait timed out";
     case ATTN_ERR_SPLITS: return "num_splits must be in [1, 32]";
     case ATTN_ERR_WORKSPACE: return "split workspace is NULL or smaller than attn_split_workspace_bytes";
+    case ATTN_ERR_SCRATCH:
+      return "problem needs more split scratch than ATTN_NOALLOC_SCRATCH_BYTES (use fewer splits or a workspace)";
     default: return "unknown status code";
   }
 }

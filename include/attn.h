@@ -73,7 +73,9 @@ enum {
   ATTN_ERR_CUDA = -9,      /* a CUDA call failed; see attn_last_cuda_error()          */
   ATTN_ERR_TIMEOUT = -10,  /* a kernel gave up on a bounded wait (see attn_device_status) */
   ATTN_ERR_SPLITS = -11,   /* num_splits outside [1, ATTN_MAX_SPLITS]                 */
-  ATTN_ERR_WORKSPACE = -12 /* split workspace NULL or smaller than required           */
+  ATTN_ERR_WORKSPACE = -12,/* split workspace NULL or smaller than required           */
+  ATTN_ERR_SCRATCH = -13   /* attn_fwd_split_noalloc: problem needs more scratch than
+                              ATTN_NOALLOC_SCRATCH_BYTES                              */
 };
 
 /* Largest num_splits attn_fwd_split accepts. */
@@ -166,6 +168,53 @@ ATTN_API int attn_fwd_split(const attn_shape_t* shape,
  * Writes *bytes. Returns ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_SHAPE or
  * ATTN_ERR_SPLITS. */
 ATTN_API int attn_split_workspace_bytes(const attn_shape_t* shape, int num_splits, size_t* bytes);
+
+/* Size of the device scratch array built into the library for
+ * attn_fwd_split_noalloc (32 MiB per GPU that loads the library). */
+#define ATTN_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* attn_fwd_split_noalloc - attn_fwd_split for callers that cannot allocate
+ * device memory. (The pages have no counterpart; this is a calling
+ * convention of this library.)
+ *
+ * Who needs it: code that may not call cudaMalloc, such as a plugin whose host
+ * application passes it input and output buffers but no allocator, or a
+ * service that forbids device allocation after start-up because cudaMalloc
+ * and cudaFree can block and synchronise the device. Such a caller cannot
+ * provide the workspace attn_fwd_split needs for num_splits > 1.
+ *
+ * Arguments and results are those of attn_fwd_split without the workspace:
+ * the split partials go to a static device array of
+ * ATTN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits. The call allocates nothing.
+ * The caller still owns and passes q, k, v, kv_lens, bias, out and lse.
+ *
+ * Limit: problems with attn_split_workspace_bytes(shape, num_splits) above
+ * ATTN_NOALLOC_SCRATCH_BYTES are rejected with ATTN_ERR_SCRATCH before
+ * anything runs; lower num_splits, or use attn_fwd_split with a workspace.
+ * num_splits == 1 uses no scratch.
+ *
+ * Shared state: all calls on a device use the same array, which keeps what
+ * the last call wrote. Nothing in it has to start at zero: each call writes
+ * every partial it later reads. Two calls whose kernels overlap on the GPU
+ * (different streams, or different host threads, without ordering between
+ * them) race on the array and may return wrong results; order them, for
+ * example on one stream.
+ *
+ * Set-up: the first call with num_splits > 1 on a device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current)
+ * and caches it; make that first call before any stream capture begins.
+ *
+ * Returns ATTN_OK, ATTN_ERR_SCRATCH, ATTN_ERR_CUDA if the set-up fails, or
+ * any code of attn_fwd_split. */
+ATTN_API int attn_fwd_split_noalloc(const attn_shape_t* shape,
+                                    const void* q, const void* k, const void* v,
+                                    int mask_kind, const int32_t* kv_lens,
+                                    const float* bias,
+                                    float scale, attn_dtype_t dtype,
+                                    int num_splits,
+                                    void* out, float* lse,
+                                    void* stream);
 
 /* attn_strerror - static English text for a status code (never NULL). */
 ATTN_API const char* attn_strerror(int code);
