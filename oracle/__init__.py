@@ -11,9 +11,10 @@ The arithmetic lives in ``attn_ref.c`` (plain C, float64, threaded over
 heads); this module widens the stored inputs exactly to float64, compiles the
 C file on first use (gcc) and calls it through ctypes.
 
-Every function is pinned by ``tests/test_oracle_pins.py`` against closed
-forms, invariants, a 50-digit brute force of the pages' raw-exp kernel, and a
-textbook single-head reduction; none is "parity unpinned".
+Every function is pinned by ``tests/test_oracle_pins.py`` (forward, LSE) and
+``tests/test_oracle_bwd_pins.py`` (backward) against closed forms, invariants,
+a 50-digit brute force of the pages' raw-exp kernel, finite differences of the
+forward, and textbook reductions; none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -65,6 +66,10 @@ def _load():
                                                   ctypes.c_int64, ctypes.POINTER(ctypes.c_int64),
                                                   dp, dp, ctypes.c_int]
             lib.oracle_attention_rows.restype = ctypes.c_int
+            lib.oracle_attention_bwd.argtypes = [ctypes.POINTER(_Shape), dp, dp, dp, ctypes.c_int,
+                                                 ctypes.POINTER(ctypes.c_int32), dp, ctypes.c_double,
+                                                 dp, dp, dp, dp, ctypes.c_int]
+            lib.oracle_attention_bwd.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -154,6 +159,32 @@ def attention_rows(q, k, v, rows, *, mask: int = 0, kv_lens=None, bias=None, sca
     if rc != 0:
         raise ValueError(f"oracle_attention_rows rejected its arguments (rc={rc})")
     return (out, ls) if lse else out
+
+
+def attention_bwd(q, k, v, dout, *, mask: int = 0, kv_lens=None, bias=None, scale: float,
+                  dtype: str | None = None, threads: int = 0):
+    """Float64 gradients (dq, dk, dv) of a loss whose gradient w.r.t. O is ``dout``.
+
+    Inputs as for :func:`attention`; ``dout`` [B,Hq,Sq,D] in the same storage
+    format (widened exactly). Returns dq [B,Hq,Sq,D] and dk, dv [B,Hkv,Sk,D]
+    in float64; dk and dv sum over the query heads of a GQA group. The bias is
+    a constant. A row with no visible key contributes nothing (its dq is 0).
+    """
+    lib = _load()
+    q64, k64, v64, lens, b64, shape = _prepare(q, k, v, kv_lens, bias, dtype)
+    g64 = widen(dout, dtype) if dtype else np.ascontiguousarray(dout, dtype=np.float64)
+    if g64.shape != q64.shape:
+        raise ValueError("dout must have the shape of q")
+    dq = np.empty(q64.shape, dtype=np.float64)
+    dk = np.empty(k64.shape, dtype=np.float64)
+    dv = np.empty(v64.shape, dtype=np.float64)
+    rc = lib.oracle_attention_bwd(ctypes.byref(shape), _dptr(q64), _dptr(k64), _dptr(v64), int(mask),
+                                  lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if lens is not None else None,
+                                  _dptr(b64), float(scale), _dptr(g64), _dptr(dq), _dptr(dk), _dptr(dv),
+                                  int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd rejected its arguments (rc={rc})")
+    return dq, dk, dv
 
 
 def prepare(q, k, v, *, kv_lens=None, bias=None, dtype: str | None = None):

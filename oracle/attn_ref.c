@@ -1,5 +1,6 @@
 /*
- * Float64 CPU oracle for exact scaled-dot-product attention (forward).
+ * Float64 CPU oracle for exact scaled-dot-product attention (forward, and
+ * the first-order backward at the end of this file).
  *
  * TEST INFRASTRUCTURE ONLY. This file is the slow, plain definition that the
  * GPU kernels are checked against. Only the test suite, the smoke check and
@@ -258,4 +259,142 @@ int oracle_attention_rows(const oracle_shape* s, const double* q, const double* 
   J.out = out;
   J.lse = lse;
   return run(&J, nthreads);
+}
+
+/*
+ * Backward (first-order gradients) of the same operation, in float64.
+ *
+ * Source: ruDNN user guide, section 11 (backward of paged attention): the
+ * backward returns dq, dk and dv and recomputes the probabilities instead of
+ * storing the score matrix. The oracle writes out the chain rule of the
+ * forward definition above for a loss L with dL/dO = dout, row by row:
+ *
+ *   w_j   = softmax weights of the row (as in the forward)
+ *   dv_j += w_j * dout_i                       (O_i = sum_j w_j v_j)
+ *   dw_j  = dout_i . v_j
+ *   ds_j  = w_j * (dw_j - sum_k w_k dw_k)      (Jacobian of the softmax)
+ *   dq_i  = scale * sum_j ds_j k_j             (s_j = scale q_i.k_j + bias)
+ *   dk_j += scale * ds_j q_i
+ *
+ * with GQA summing dk and dv over the query heads that share a key/value
+ * head. The bias is a constant (the page's backward returns no bias
+ * gradient). Reading where the pages are silent: a row with no visible key
+ * (output NaN in the forward) contributes nothing; its dq row is 0.
+ */
+typedef struct {
+  const problem* P;
+  const double* dout;
+  double *dq, *dk, *dv;
+  int64_t next;
+  pthread_mutex_t lock;
+  int failed;
+} bwd_job;
+
+static int64_t bwd_take(bwd_job* J) {
+  pthread_mutex_lock(&J->lock);
+  int64_t t = J->next++;
+  pthread_mutex_unlock(&J->lock);
+  return t;
+}
+
+/* One (b, hk): every query row of the heads that share hk. */
+static void backward_group(const problem* P, const double* dout, double* dq, double* dk,
+                           double* dv, int64_t b, int64_t hk, double* w, double* sc, double* o,
+                           double* dw) {
+  const oracle_shape* s = P->s;
+  const int64_t D = s->D, Sk = s->Sk, Sq = s->Sq;
+  const int64_t group = s->Hq / s->Hkv;
+  const double* kh = P->k + (b * s->Hkv + hk) * Sk * D;
+  const double* vh = P->v + (b * s->Hkv + hk) * Sk * D;
+  double* dkh = dk + (b * s->Hkv + hk) * Sk * D;
+  double* dvh = dv + (b * s->Hkv + hk) * Sk * D;
+  for (int64_t x = 0; x < Sk * D; ++x) dkh[x] = dvh[x] = 0.0;
+  for (int64_t hq = hk * group; hq < (hk + 1) * group; ++hq) {
+    for (int64_t i = 0; i < Sq; ++i) {
+      const int64_t row = (b * s->Hq + hq) * Sq + i;
+      const double* qi = P->q + row * D;
+      const double* gi = dout + row * D;
+      double* dqi = dq + row * D;
+      for (int64_t d = 0; d < D; ++d) dqi[d] = 0.0;
+      attention_row(P, b, hq, i, o, w, NULL, sc);
+      if (Sk == 0 || isnan(w[0])) continue; /* no visible key: no contribution */
+      double wdw = 0.0;
+      for (int64_t j = 0; j < Sk; ++j) {
+        double g = 0.0;
+        for (int64_t d = 0; d < D; ++d) g += gi[d] * vh[j * D + d];
+        dw[j] = g;
+        wdw += w[j] * g;
+      }
+      for (int64_t j = 0; j < Sk; ++j) {
+        if (w[j] == 0.0) continue; /* masked, or exp underflow: zero weight, zero terms */
+        const double ds = w[j] * (dw[j] - wdw);
+        for (int64_t d = 0; d < D; ++d) {
+          dqi[d] += P->scale * ds * kh[j * D + d];
+          dkh[j * D + d] += P->scale * ds * qi[d];
+          dvh[j * D + d] += w[j] * gi[d];
+        }
+      }
+    }
+  }
+}
+
+static void* bwd_worker(void* arg) {
+  bwd_job* J = (bwd_job*)arg;
+  const oracle_shape* s = J->P->s;
+  const size_t sk = (size_t)(s->Sk > 0 ? s->Sk : 1);
+  double* w = (double*)malloc(sizeof(double) * sk);
+  double* sc = (double*)malloc(sizeof(double) * sk);
+  double* dw = (double*)malloc(sizeof(double) * sk);
+  double* o = (double*)malloc(sizeof(double) * (size_t)s->D);
+  if (!w || !sc || !dw || !o) {
+    pthread_mutex_lock(&J->lock);
+    J->failed = 1;
+    pthread_mutex_unlock(&J->lock);
+  } else {
+    for (int64_t t = bwd_take(J); t < s->B * s->Hkv; t = bwd_take(J))
+      backward_group(J->P, J->dout, J->dq, J->dk, J->dv, t / s->Hkv, t % s->Hkv, w, sc, o, dw);
+  }
+  free(w);
+  free(sc);
+  free(dw);
+  free(o);
+  return NULL;
+}
+
+/* dout: [B,Hq,Sq,D]; writes dq [B,Hq,Sq,D], dk and dv [B,Hkv,Sk,D].
+ * Returns 0, -1 on a bad argument, -2 when memory runs out. */
+int oracle_attention_bwd(const oracle_shape* s, const double* q, const double* k, const double* v,
+                         int mask, const int32_t* kv_lens, const double* bias, double scale,
+                         const double* dout, double* dq, double* dk, double* dv, int nthreads) {
+  if (check_shape(s, mask, kv_lens) || !dout || !dq || !dk || !dv) return -1;
+  if (bias && !((s->bias_b == 1 || s->bias_b == s->B) && (s->bias_h == 1 || s->bias_h == s->Hq)))
+    return -1;
+  problem P = {s, q, k, v, bias, kv_lens, mask, scale};
+  bwd_job J;
+  memset(&J, 0, sizeof J);
+  J.P = &P;
+  J.dout = dout;
+  J.dq = dq;
+  J.dk = dk;
+  J.dv = dv;
+  const int64_t items = s->B * s->Hkv;
+  if (nthreads <= 0) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    nthreads = n > 0 ? (int)n : 1;
+  }
+  if (nthreads > items) nthreads = items > 0 ? (int)items : 1;
+  pthread_mutex_init(&J.lock, NULL);
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  if (!th) {
+    pthread_mutex_destroy(&J.lock);
+    return -2;
+  }
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t)
+    if (pthread_create(&th[t], NULL, bwd_worker, &J) == 0) ++started;
+  if (started == 0) bwd_worker(&J);
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  free(th);
+  pthread_mutex_destroy(&J.lock);
+  return J.failed ? -2 : 0;
 }

@@ -11,6 +11,7 @@ import subprocess
 import pytest
 
 import oracle
+from tests import test_oracle_bwd_pins as bpins
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_ref.c")
@@ -37,6 +38,28 @@ MUTANTS = {
 }
 
 
+# Mistakes in the backward, caught by the backward pins.
+MUTANTS_BWD = {
+    "bwd_no_row_term": ("const double ds = w[j] * (dw[j] - wdw);", "const double ds = w[j] * dw[j];"),
+    "bwd_dq_unscaled": ("dqi[d] += P->scale * ds * kh[j * D + d];", "dqi[d] += ds * kh[j * D + d];"),
+    "bwd_dk_uses_k": ("dkh[j * D + d] += P->scale * ds * qi[d];", "dkh[j * D + d] += P->scale * ds * kh[j * D + d];"),
+    "bwd_dv_uses_ds": ("dvh[j * D + d] += w[j] * gi[d];", "dvh[j * D + d] += ds * gi[d];"),
+    "bwd_dw_uses_k": ("for (int64_t d = 0; d < D; ++d) g += gi[d] * vh[j * D + d];",
+                      "for (int64_t d = 0; d < D; ++d) g += gi[d] * kh[j * D + d];"),
+    "bwd_gqa_first_head_only": ("for (int64_t hq = hk * group; hq < (hk + 1) * group; ++hq) {",
+                                "for (int64_t hq = hk * group; hq < hk * group + 1; ++hq) {"),
+    "bwd_dv_sign": ("dvh[j * D + d] += w[j] * gi[d];", "dvh[j * D + d] -= w[j] * gi[d];"),
+}
+
+
+def _bwd_pins():
+    yield bpins.test_single_key
+    yield bpins.test_identical_keys_give_zero_query_gradient
+    yield lambda: bpins.test_key_gradients_sum_to_zero(0)
+    yield lambda: bpins.test_matches_finite_differences_of_the_forward(0, None, (4, 4))
+    yield lambda: bpins.test_matches_finite_differences_of_the_forward(pins.CAUSAL, (1, 4), (3, 6))
+
+
 def _pins():
     yield pins.test_golden_single_row_service_example
     yield pins.test_golden_tensai_causal_mask_pattern
@@ -53,9 +76,9 @@ def _pins():
                 yield lambda m=mask, b=bshape, s=sq_sk: pins.test_brute_force_tiny(m, b, s)
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
+@pytest.mark.parametrize("name", sorted(MUTANTS) + sorted(MUTANTS_BWD))
 def test_pins_catch_mutant(name, tmp_path, monkeypatch):
-    old, new = MUTANTS[name]
+    old, new = MUTANTS[name] if name in MUTANTS else MUTANTS_BWD[name]
     src = open(SRC).read()
     assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
     mut = tmp_path / "attn_mut.c"
@@ -71,9 +94,11 @@ def test_pins_catch_mutant(name, tmp_path, monkeypatch):
     lib.oracle_attention.restype = ctypes.c_int
     lib.oracle_attention_rows.argtypes = real.oracle_attention_rows.argtypes
     lib.oracle_attention_rows.restype = ctypes.c_int
+    lib.oracle_attention_bwd.argtypes = real.oracle_attention_bwd.argtypes
+    lib.oracle_attention_bwd.restype = ctypes.c_int
     monkeypatch.setattr(oracle, "_lib", lib)
     caught = []
-    for pin in _pins():
+    for pin in (_pins() if name in MUTANTS else _bwd_pins()):
         try:
             pin()
         except AssertionError:
