@@ -112,6 +112,12 @@ class ClockSampler:
                 "samples": len(rows), "reasons": sorted(reasons)}
 
 
+def make_device_tensor(a, kind, device):
+    import torch
+    t = torch.from_numpy(a.view("int16")).view(torch.bfloat16) if kind == "bf16" else torch.from_numpy(a)
+    return t.to(device)
+
+
 def make_device_inputs(w, device):
     import torch
     x = synth.make_inputs(w)
@@ -257,6 +263,22 @@ def bench_gpu(args):
         attn.fwd(q, k, v, causal=causal, kv_lens=lens, bias=bias, scale=scale, out=out, stream=stream,
                  num_splits=splits, workspace=ws)
 
+    bwd_bufs = None
+    if args.pass_ == "bwd":
+        # inputs of the backward: the forward's output and LSE, and a seeded dL/dO
+        g = make_device_tensor(synth.to_storage(synth.normal_f32(w.seed, 7, (w.B, w.Hq, w.Sq, w.D)), w.dtype),
+                               w.dtype, device)
+        fo, flse = attn.fwd(q, k, v, causal=causal, kv_lens=lens, bias=bias, scale=scale, return_lse=True)
+        bshp = attn.Shape(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, *(x["bias"].shape[:2] if w.bias else (1, 1)))
+        bws = torch.empty(max(1, attn.bwd_workspace_bytes(bshp)), dtype=torch.uint8, device=device)
+        bwd_bufs = dict(out=fo, dout=g, lse=flse, dq=torch.empty_like(q), dk=torch.empty_like(k),
+                        dv=torch.empty_like(v))
+
+        def step():  # noqa: F811 - the timed step is the backward
+            attn.bwd(q, k, v, bwd_bufs["out"], bwd_bufs["dout"], bwd_bufs["lse"], causal=causal, kv_lens=lens,
+                     bias=bias, scale=scale, workspace=bws, stream=stream, dq=bwd_bufs["dq"],
+                     dk=bwd_bufs["dk"], dv=bwd_bufs["dv"])
+
     def barrier():
         if world > 1:
             import torch.distributed as dist
@@ -290,11 +312,13 @@ def bench_gpu(args):
         elapsed_ms = float(tt.item())
     ms = elapsed_ms / args.steps
     flops, flops_basis = step_flops(w)
+    if args.pass_ == "bwd":  # nominal backward work: 2.5x the forward's (5 matmuls for 2)
+        flops, flops_basis = 2.5 * flops, "2.5 x forward (" + flops_basis + ")"
     value = world * flops / (ms * 1e-3) / 1e12
 
     # end to end through the public API with host buffers (pinned), copies inside
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.pass_ == "fwd":
         hosts = [None if a is None else a.cpu().pin_memory() for a in (q, k, v, lens, bias)]
         qh, kh, vh, lh, bh = hosts
         oh = torch.empty(qh.shape, dtype=qh.dtype, pin_memory=True)
@@ -338,7 +362,8 @@ def bench_gpu(args):
     traffic = read_traffic(w)
     hbm_gbs = w.io_bytes() / (ms * 1e-3) / 1e9
     line = {
-        "metric": METRIC if w.name == WORKLOAD else f"attention fwd TFLOP/s ({w.name})", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": (METRIC if w.name == WORKLOAD and args.pass_ == "fwd"
+                   else f"attention {args.pass_} TFLOP/s ({w.name})"), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
@@ -356,10 +381,19 @@ def bench_gpu(args):
                      "hbm_gbs_algorithmic": hbm_gbs,
                      "hbm_frac": hbm_gbs / float(peaks["hbm_gbs"])},
         "e2e": e2e,
-        "gpu_launches": args.steps * (2 if splits > 1 else 1),
+        "gpu_launches": args.steps * (3 if args.pass_ == "bwd" else (2 if splits > 1 else 1)),
         "clocks": clocks.summary(),
     }
-    if world == 1 and not args.no_cpu_baseline and w.name == WORKLOAD:
+    if args.pass_ == "bwd":
+        # the backward runs on the fp32 FMA pipes: its roofline is their peak,
+        # 152 SMs x 128 lanes x 2 FLOP x the SM clock seen under load
+        mhz = (line["clocks"] or {}).get("sm_mhz") or 2070.0
+        alu_peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
+        line["roofline"].update({"bound": "alu", "peak": alu_peak, "frac": achieved / alu_peak,
+                                 "peak_kind": f"fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x {mhz:.0f} MHz",
+                                 "frac_of_sustained": None, "kernel": "dkdv_kernel + dq_kernel",
+                                 "traffic": None})
+    if world == 1 and not args.no_cpu_baseline and w.name == WORKLOAD and args.pass_ == "fwd":
         line["cpu_baseline"] = cpu_baseline(w, x)
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -376,6 +410,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"],
+                    help="time the forward (default) or the backward (attn_bwd) of the workload")
     ap.add_argument("--splits", type=int, default=0,
                     help="key-range splits (attn_fwd_split); 0 = the workload's default")
     args = ap.parse_args()

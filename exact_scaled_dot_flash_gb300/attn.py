@@ -61,6 +61,11 @@ def load_library():
         lib.attn_split_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.c_int,
                                                    ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_split_workspace_bytes.restype = ctypes.c_int
+        lib.attn_bwd.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp,
+                                 ctypes.c_float, ctypes.c_int, vp, ctypes.c_size_t, vp, vp, vp, vp]
+        lib.attn_bwd.restype = ctypes.c_int
+        lib.attn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_bwd_workspace_bytes.restype = ctypes.c_int
         lib.attn_strerror.argtypes = [ctypes.c_int]
         lib.attn_strerror.restype = ctypes.c_char_p
         lib.attn_last_cuda_error.argtypes = []
@@ -225,3 +230,75 @@ def _fwd_host(q, k, v, *, causal, kv_lens, bias, scale, out):
     out.copy_(o_dev, non_blocking=True)
     torch.cuda.current_stream(dev).synchronize()
     return out
+
+
+def bwd_workspace_bytes(shape: Shape) -> int:
+    """Workspace bytes attn_bwd needs for ``shape``."""
+    n = ctypes.c_size_t(0)
+    check(load_library().attn_bwd_workspace_bytes(ctypes.byref(shape), ctypes.byref(n)))
+    return n.value
+
+
+def bwd(q, k, v, out, dout, lse, *, causal: bool = False, kv_lens=None, bias=None,
+        scale: float | None = None, workspace=None, stream=None, dq=None, dk=None, dv=None):
+    """Gradients (dq, dk, dv) of attention for dL/dO = ``dout`` (attn_bwd).
+
+    q, k, v, kv_lens, bias, scale, causal: as given to the forward; ``out`` its
+    output and ``lse`` its float32 [B,Hq,Sq] row log-sum-exp (``fwd(...,
+    return_lse=True)``); ``dout`` like ``out``. All on one CUDA device,
+    contiguous. Returns dq (like q), dk and dv (like k and v): the given
+    ``dq``/``dk``/``dv`` tensors when passed, else new ones.
+    """
+    import torch
+
+    dev = q.device
+    for name, t in (("k", k), ("v", v), ("out", out), ("dout", dout)):
+        if t.device != dev or t.dtype != q.dtype or not t.is_contiguous():
+            raise AttnError(f"{name} must be a contiguous {q.dtype} tensor on {dev}")
+    if not q.is_contiguous() or q.dim() != 4 or k.dim() != 4:
+        raise AttnError("q, k, v must be contiguous 4-D tensors")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    if tuple(out.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape) or tuple(v.shape) != tuple(k.shape):
+        raise AttnError("out and dout must be like q, v like k")
+    if lse.device != dev or lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Sq) or not lse.is_contiguous():
+        raise AttnError("lse must be a contiguous float32 [B, Hq, Sq] tensor on q's device")
+    mask = MASK_CAUSAL if causal else MASK_NONE
+    kv_ptr = 0
+    if kv_lens is not None:
+        if kv_lens.device != dev or kv_lens.dtype != torch.int32 or tuple(kv_lens.shape) != (B,):
+            raise AttnError("kv_lens must be int32 [B] on q's device")
+        kv_lens = kv_lens.contiguous()
+        mask |= MASK_KEY_PADDING
+        kv_ptr = kv_lens.data_ptr()
+    bb = bh = 1
+    b_ptr = 0
+    if bias is not None:
+        if bias.device != dev or bias.dtype != torch.float32 or bias.dim() != 4 or not bias.is_contiguous():
+            raise AttnError("bias must be a contiguous float32 [bias_b, bias_h, Sq, Sk] tensor on q's device")
+        bb, bh = int(bias.shape[0]), int(bias.shape[1])
+        b_ptr = bias.data_ptr()
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    shape = Shape(B, Hq, Hkv, Sq, Sk, D, bb, bh)
+    need = bwd_workspace_bytes(shape)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    elif workspace.device != dev or workspace.numel() * workspace.element_size() < need:
+        raise AttnError(f"workspace must hold {need} bytes on q's device")
+    for name, t, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if t is not None and (t.shape != like.shape or t.dtype != like.dtype or t.device != dev
+                              or not t.is_contiguous()):
+            raise AttnError(f"{name} must be a contiguous tensor like {'q' if like is q else 'k'}")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    check(load_library().attn_bwd(ctypes.byref(shape), q.data_ptr() or None, k.data_ptr() or None,
+                                  v.data_ptr() or None, out.data_ptr() or None, dout.data_ptr() or None,
+                                  lse.data_ptr() or None, mask, kv_ptr or None, b_ptr or None, float(scale),
+                                  _dtype_code(q), workspace.data_ptr() if need else None, need,
+                                  dq.data_ptr() or None, dk.data_ptr() or None, dv.data_ptr() or None,
+                                  stream.cuda_stream or None))
+    return dq, dk, dv

@@ -329,3 +329,119 @@ int run(const attn_shape_t* shape, const void* q, const void* k, const void* v, 
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------- backward
+namespace {
+
+int64_t bwd_workspace_total(const attn_shape_t& s) {
+  const int64_t rows = static_cast<int64_t>(s.B) * s.Hq * s.Sq;
+  return ((rows * 4 + 255) / 256 * 256) * 2;  // D_i, then lse_i in log2 units
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_bwd_workspace_bytes(const attn_shape_t* shape, size_t* bytes) {
+  if (!shape || !bytes) return ATTN_ERR_NULL;
+  const attn_shape_t s = *shape;
+  if (s.B < 0 || s.Sq < 0 || s.Hq <= 0) return ATTN_ERR_SHAPE;
+  *bytes = static_cast<size_t>(bwd_workspace_total(s));
+  return ATTN_OK;
+}
+
+int attn_bwd(const attn_shape_t* shape, const void* q, const void* k, const void* v,
+             const void* out, const void* dout, const float* lse, int mask_kind,
+             const int32_t* kv_lens, const float* bias, float scale, attn_dtype_t dtype,
+             void* workspace, size_t workspace_bytes, void* dq, void* dk, void* dv,
+             void* stream) {
+  // ---- validation: everything is checked before any CUDA call
+  if (!shape) return ATTN_ERR_NULL;
+  const attn_shape_t s = *shape;
+  if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+  if (s.B < 0 || s.Sq < 0 || s.Sk < 0 || s.Hq <= 0 || s.Hkv <= 0 || s.D <= 0) return ATTN_ERR_SHAPE;
+  if (s.Hq % s.Hkv != 0) return ATTN_ERR_SHAPE;
+  if (mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_KEY_PADDING)) return ATTN_ERR_MASK;
+  if ((mask_kind & ATTN_MASK_KEY_PADDING) && !kv_lens) return ATTN_ERR_MASK;
+  if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_SCALE;
+  if (bias && !((s.bias_b == 1 || s.bias_b == s.B) && (s.bias_h == 1 || s.bias_h == s.Hq)))
+    return ATTN_ERR_SHAPE;
+  if (!(s.D == 16 || s.D == 32 || s.D == 64 || s.D == 128)) return ATTN_ERR_HEAD_DIM;
+  const int64_t bhq = static_cast<int64_t>(s.B) * s.Hq;
+  const int64_t bhk = static_cast<int64_t>(s.B) * s.Hkv;
+  if (bhq > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  if ((static_cast<int64_t>(s.Sq) + 63) / 64 > 65535 || (static_cast<int64_t>(s.Sk) + 63) / 64 > 65535)
+    return ATTN_ERR_SHAPE;
+  if (s.B == 0) return ATTN_OK;
+  const int es = elem_size(dtype);
+  const int64_t q_bytes = bhq * s.Sq * s.D * es;
+  const int64_t kv_bytes = bhk * s.Sk * s.D * es;
+  const int64_t lse_bytes = bhq * s.Sq * 4;
+  const int64_t bias_bytes =
+      bias ? static_cast<int64_t>(s.bias_b) * s.bias_h * s.Sq * static_cast<int64_t>(s.Sk) * 4 : 0;
+  const bool rows = s.Sq > 0, keys = s.Sk > 0;
+  if ((rows && (!q || !out || !dout || !lse || !dq)) || (keys && (!k || !v || !dk || !dv)))
+    return ATTN_ERR_NULL;
+  if ((rows && (!aligned16(q) || !aligned16(out) || !aligned16(dout) || !aligned16(dq))) ||
+      (keys && (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv))))
+    return ATTN_ERR_ALIGN;
+  if ((lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) || (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) ||
+      (kv_lens && (reinterpret_cast<uintptr_t>(kv_lens) & 3u)))
+    return ATTN_ERR_ALIGN;
+  const int64_t ws_need = (rows && keys) ? bwd_workspace_total(s) : 0;
+  if (ws_need > 0) {
+    if (!workspace || workspace_bytes < static_cast<size_t>(ws_need)) return ATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  }
+  // every buffer the call writes is disjoint from every other buffer it touches
+  struct Buf { const void* p; int64_t n; };
+  const Buf ins[] = {{q, q_bytes}, {k, kv_bytes}, {v, kv_bytes}, {out, q_bytes}, {dout, q_bytes},
+                     {lse, lse_bytes}, {bias, bias_bytes}, {kv_lens, static_cast<int64_t>(s.B) * 4}};
+  const Buf outs[] = {{dq, q_bytes}, {dk, kv_bytes}, {dv, kv_bytes}, {ws_need ? workspace : nullptr, ws_need}};
+  for (int a = 0; a < 4; ++a) {
+    for (const Buf& b : ins)
+      if (overlaps(outs[a].p, outs[a].n, b.p, b.n)) return ATTN_ERR_OVERLAP;
+    for (int c = a + 1; c < 4; ++c)
+      if (overlaps(outs[a].p, outs[a].n, outs[c].p, outs[c].n)) return ATTN_ERR_OVERLAP;
+  }
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (!rows || !keys) {  // no query rows: dk = dv = 0; no keys: dq = 0
+    if (keys) {
+      if ((e = cudaMemsetAsync(dk, 0, static_cast<size_t>(kv_bytes), st)) == cudaSuccess)
+        e = cudaMemsetAsync(dv, 0, static_cast<size_t>(kv_bytes), st);
+    }
+    if (rows && e == cudaSuccess) e = cudaMemsetAsync(dq, 0, static_cast<size_t>(q_bytes), st);
+    return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+  }
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return fail_cuda(e);
+  attn::KernelParams p{};
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.Sq = s.Sq;
+  p.Sk = s.Sk;
+  p.group = s.Hq / s.Hkv;
+  p.causal = (mask_kind & ATTN_MASK_CAUSAL) ? 1 : 0;
+  p.padding = (mask_kind & ATTN_MASK_KEY_PADDING) ? 1 : 0;
+  p.kv_lens = p.padding ? kv_lens : nullptr;
+  p.bias = bias;
+  p.bias_b = bias ? s.bias_b : 1;
+  p.bias_h = bias ? s.bias_h : 1;
+  p.bias_vec4 = 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = status_ptr(dev);
+  p.device = dev;
+  p.num_splits = 1;
+  float* dsum = static_cast<float*>(workspace);
+  float* lse2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_need / 2);
+  int unsupported = 0;
+  e = attn::launch_bwd_simt(s.D, static_cast<int>(dtype), p, q, k, v, out, dout, lse, dsum, lse2, dq,
+                            dk, dv, scale, st, &unsupported);
+  if (unsupported) return ATTN_ERR_HEAD_DIM;
+  return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+}
+
+}  // extern "C"

@@ -56,6 +56,12 @@ cudaError_t launch_f32(int D, bool has_bias, const KernelParams& p, const float*
                        int* unsupported);
 cudaError_t launch_nan_fill(void* out, int64_t count, int elem_bytes, cudaStream_t stream);
 cudaError_t launch_f32_fill(float* out, int64_t count, float value, cudaStream_t stream);
+// Backward, fp32 FMA path for every dtype (dtype: 0 f32, 1 f16, 2 bf16): the
+// preprocess (dsum = rowsum(dout * out), lse2 = lse * log2 e), then dk/dv and dq.
+cudaError_t launch_bwd_simt(int D, int dtype, const KernelParams& p, const void* q, const void* k,
+                            const void* v, const void* out, const void* dout, const float* lse,
+                            float* dsum, float* lse2, void* dq, void* dk, void* dv, float scale,
+                            cudaStream_t stream, int* unsupported);
 // O[r,:] = sum_s 2^(m_s - M) O_s[r,:] / sum_s 2^(m_s - M) l_s,  M = max_s m_s;
 // lse[r] = (M + log2 sum_s 2^(m_s - M) l_s) ln 2.  dtype: 0 f32, 1 f16, 2 bf16.
 cudaError_t launch_split_merge(const KernelParams& p, int D, int dtype, void* out,

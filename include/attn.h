@@ -169,6 +169,49 @@ ATTN_API int attn_fwd_split(const attn_shape_t* shape,
  * ATTN_ERR_SPLITS. */
 ATTN_API int attn_split_workspace_bytes(const attn_shape_t* shape, int num_splits, size_t* bytes);
 
+/* attn_bwd - gradients of attention: dq, dk, dv for a loss whose gradient
+ * with respect to the output is `dout`. Asynchronous on `stream`.
+ *
+ * Source: ruDNN user guide, section 11: the backward returns dq, dk and dv and
+ * recomputes the probabilities instead of storing the score matrix; its
+ * ordered variant accumulates without atomics in a fixed order, which this
+ * call does (bit-identical results on repeated calls). With the forward's row
+ * log-sum-exp lse_i, for every visible (i, j):
+ *   p_ij = exp(scale*q_i.k_j + bias_ij - lse_i),  dp_ij = dout_i . v_j,
+ *   D_i = dout_i . out_i,  ds_ij = p_ij * (dp_ij - D_i),
+ *   dv_j = sum_i p_ij dout_i,  dk_j = scale * sum_i ds_ij q_i,
+ *   dq_i = scale * sum_j ds_ij k_j,
+ * dk and dv summed over the query heads that share a key/value head (GQA).
+ * The bias is a constant (no bias gradient). A row with no visible key
+ * (lse = -inf) contributes nothing and gets dq = 0.
+ *
+ * shape, q, k, v, mask_kind, kv_lens, bias, scale, dtype: exactly as given to
+ *   the forward call.
+ * out: the forward output O [B, Hq, Sq, D] (dtype); dout: dL/dO, same layout.
+ * lse: the forward's row log-sum-exp, float [B, Hq, Sq] (from attn_fwd_split).
+ * workspace, workspace_bytes: device scratch of at least
+ *   attn_bwd_workspace_bytes(shape) bytes, 16-byte aligned, caller-owned.
+ * dq [B, Hq, Sq, D], dk, dv [B, Hkv, Sk, D]: outputs in dtype, 16-byte aligned,
+ *   written entirely, disjoint from every input, each other and the workspace.
+ *
+ * Head dims: D in {16, 32, 64, 128} for every dtype. B = 0 is a no-op; Sq = 0
+ * gives dk = dv = 0; Sk = 0 gives dq = 0. Returns ATTN_OK or a negative
+ * ATTN_ERR_* code (validation before any launch). */
+ATTN_API int attn_bwd(const attn_shape_t* shape,
+                      const void* q, const void* k, const void* v,
+                      const void* out, const void* dout, const float* lse,
+                      int mask_kind, const int32_t* kv_lens,
+                      const float* bias,
+                      float scale, attn_dtype_t dtype,
+                      void* workspace, size_t workspace_bytes,
+                      void* dq, void* dk, void* dv,
+                      void* stream);
+
+/* attn_bwd_workspace_bytes - workspace attn_bwd needs for `shape`: two float
+ * arrays of B*Hq*Sq, each rounded up to 256 bytes. Writes *bytes. Returns
+ * ATTN_OK, ATTN_ERR_NULL or ATTN_ERR_SHAPE. */
+ATTN_API int attn_bwd_workspace_bytes(const attn_shape_t* shape, size_t* bytes);
+
 /* Size of the device scratch array built into the library for
  * attn_fwd_split_noalloc (32 MiB per GPU that loads the library). */
 #define ATTN_NOALLOC_SCRATCH_BYTES (32u << 20)
