@@ -384,8 +384,10 @@ def bench_gpu(args):
         "gpu_launches": args.steps * (3 if args.pass_ == "bwd" else (2 if splits > 1 else 1)),
         "clocks": clocks.summary(),
     }
-    if args.pass_ == "bwd":
-        # the backward runs on the fp32 FMA pipes: its roofline is their peak,
+    if args.pass_ == "bwd" and w.dtype != "f32" and w.D in (64, 128):
+        line["roofline"].update({"kernel": "dkdv_tc_kernel + dq_tc_kernel", "traffic": None})
+    elif args.pass_ == "bwd":
+        # the fp32 FMA backward: its roofline is the FMA pipes' peak,
         # 152 SMs x 128 lanes x 2 FLOP x the SM clock seen under load
         mhz = (line["clocks"] or {}).get("sm_mhz") or 2070.0
         alu_peak = 152 * 128 * 2 * mhz * 1e6 / 1e12

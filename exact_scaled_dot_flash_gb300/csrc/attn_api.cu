@@ -437,6 +437,24 @@ int attn_bwd(const attn_shape_t* shape, const void* q, const void* k, const void
   p.num_splits = 1;
   float* dsum = static_cast<float*>(workspace);
   float* lse2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_need / 2);
+  // F16/BF16 with D in {64, 128}: tensor cores; otherwise the fp32 FMA path
+  const bool tc = dtype != ATTN_F32 && (s.D == 64 || s.D == 128) && bhq <= 65535 && bhk <= 65535;
+  if (tc) {
+    attn::EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail_cuda(cudaErrorNotSupported);
+    e = attn::launch_bwd_preprocess(s.D, static_cast<int>(dtype), out, dout, lse, dsum, lse2, bhq * s.Sq, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+    attn::BwdArgs a{lse2, dsum, dq, dk, dv, scale};
+    const bool bf = dtype == ATTN_BF16;
+    using namespace attn::bwdtc;
+#define ATTN_BWD_TC(DD, BB) \
+  (bias ? launch_bwd_tc_instance<DD, BB, true>(enc, q, k, v, dout, p, a, st) \
+        : launch_bwd_tc_instance<DD, BB, false>(enc, q, k, v, dout, p, a, st))
+    if (s.D == 128) e = bf ? ATTN_BWD_TC(128, true) : ATTN_BWD_TC(128, false);
+    else e = bf ? ATTN_BWD_TC(64, true) : ATTN_BWD_TC(64, false);
+#undef ATTN_BWD_TC
+    return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+  }
   int unsupported = 0;
   e = attn::launch_bwd_simt(s.D, static_cast<int>(dtype), p, q, k, v, out, dout, lse, dsum, lse2, dq,
                             dk, dv, scale, st, &unsupported);

@@ -328,6 +328,27 @@ static cudaError_t launch_dt(int D, const KernelParams& p, const void* q, const 
 
 }  // namespace bwd
 
+cudaError_t launch_bwd_preprocess(int D, int dtype, const void* out, const void* dout, const float* lse,
+                                  float* dsum, float* lse2, int64_t rows, cudaStream_t st) {
+  const int64_t blocks = (rows * 32 + 255) / 256;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const unsigned nb = static_cast<unsigned>(blocks);
+#define ATTN_PRE(DD, TT) bwd::preprocess_kernel<DD, TT><<<nb, 256, 0, st>>>(out, dout, lse, dsum, lse2, rows)
+#define ATTN_PRE_D(DD) \
+  case DD: if (dtype == 0) ATTN_PRE(DD, 0); else if (dtype == 1) ATTN_PRE(DD, 1); else ATTN_PRE(DD, 2); break;
+  switch (D) {
+    ATTN_PRE_D(16)
+    ATTN_PRE_D(32)
+    ATTN_PRE_D(64)
+    ATTN_PRE_D(128)
+    default: return cudaErrorInvalidValue;
+  }
+#undef ATTN_PRE_D
+#undef ATTN_PRE
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_simt(int D, int dtype, const KernelParams& p, const void* q, const void* k,
                             const void* v, const void* out, const void* dout, const float* lse,
                             float* dsum, float* lse2, void* dq, void* dk, void* dv, float scale,

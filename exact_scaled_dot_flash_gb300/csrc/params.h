@@ -56,6 +56,26 @@ cudaError_t launch_f32(int D, bool has_bias, const KernelParams& p, const float*
                        int* unsupported);
 cudaError_t launch_nan_fill(void* out, int64_t count, int elem_bytes, cudaStream_t stream);
 cudaError_t launch_f32_fill(float* out, int64_t count, float value, cudaStream_t stream);
+// Arguments of the backward kernels beyond KernelParams.
+struct BwdArgs {
+  const float* lse2;  // [B*Hq*Sq] row log-sum-exp in log2 units
+  const float* dsum;  // [B*Hq*Sq] D_i = dout_i . o_i
+  void* dq;
+  void* dk;
+  void* dv;
+  float scale;        // natural scale (dk and dq are scaled by it)
+};
+namespace bwdtc {
+// Tensor-core backward (F16/BF16, D in {64, 128}): dk/dv then dq; the
+// preprocess (launch_bwd_preprocess) must have filled lse2 and dsum.
+template <int D, bool BF16, bool BIAS>
+cudaError_t launch_bwd_tc_instance(EncodeTiledFn enc, const void* q, const void* k, const void* v,
+                                   const void* dout, const KernelParams& p, const BwdArgs& a,
+                                   cudaStream_t stream);
+}  // namespace bwdtc
+cudaError_t launch_bwd_preprocess(int D, int dtype, const void* out, const void* dout, const float* lse,
+                                  float* dsum, float* lse2, int64_t rows, cudaStream_t stream);
+
 // Backward, fp32 FMA path for every dtype (dtype: 0 f32, 1 f16, 2 bf16): the
 // preprocess (dsum = rowsum(dout * out), lse2 = lse * log2 e), then dk/dv and dq.
 cudaError_t launch_bwd_simt(int D, int dtype, const KernelParams& p, const void* q, const void* k,
