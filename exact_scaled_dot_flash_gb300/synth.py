@@ -162,3 +162,69 @@ def make_inputs(w: Workload) -> dict:
         bias = normal_f32(w.seed, STREAM_BIAS, (w.bias_b, w.bias_h, w.Sq, w.Sk))
     return {"q": q, "k": k, "v": v, "kv_lens": kv_lens, "bias": bias,
             "scale": w.softmax_scale, "mask": w.mask}
+
+
+# --------------------------------------------------------------- paged caches
+STREAM_PAGED_Q, STREAM_PAGED_K, STREAM_PAGED_V, STREAM_PAGED_META = 8, 9, 10, 11
+
+
+@dataclasses.dataclass(frozen=True)
+class PagedWorkload:
+    """Packed queries over a paged key/value cache (serving-shaped inputs)."""
+    name: str
+    dtype: str
+    num_seqs: int
+    Hq: int
+    Hkv: int
+    D: int
+    page_size: int
+    ctx_range: tuple          # (lo, hi) inclusive key lengths per sequence
+    q_range: tuple            # (lo, hi) inclusive new queries per sequence (capped by its length)
+    seed: int = 0
+    causal: bool = True
+    explicit_positions: bool = False  # random increasing positions instead of the newest tokens
+    spare_pages: int = 3              # unused physical pages mixed into the cache
+    scale: float | None = None
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale is not None else 1.0 / math.sqrt(self.D)
+
+    def replace(self, **kw) -> "PagedWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+def make_paged_inputs(w: PagedWorkload) -> dict:
+    """Draw a paged problem: per-sequence key lengths and query counts, a cache
+    whose physical pages are a random permutation (so page tables scatter), and
+    packed queries. Unused page-table entries are -1. Returns q [queries, Hq, D],
+    k_cache/v_cache [pages, page_size, Hkv, D] in storage format, block_table
+    int32 [num_seqs, max_pages], seq_lens, q_offsets [num_seqs + 1], positions
+    (int32 [queries] or None) and scale.
+    """
+    g = _gen(w.seed, STREAM_PAGED_META)
+    lens = g.integers(w.ctx_range[0], w.ctx_range[1], size=w.num_seqs, endpoint=True).astype(np.int32)
+    nq = np.array([g.integers(min(w.q_range[0], L), min(w.q_range[1], L), endpoint=True) if L > 0 else 0
+                   for L in lens], dtype=np.int32)
+    P = w.page_size
+    need = (lens + P - 1) // P
+    max_pages = max(1, int(need.max()) if w.num_seqs else 1)
+    pages = int(need.sum()) + w.spare_pages
+    perm = g.permutation(pages).astype(np.int32)
+    table = np.full((w.num_seqs, max_pages), -1, dtype=np.int32)
+    at = 0
+    for s in range(w.num_seqs):
+        table[s, :need[s]] = perm[at:at + need[s]]
+        at += need[s]
+    q_off = np.zeros(w.num_seqs + 1, dtype=np.int32)
+    q_off[1:] = np.cumsum(nq)
+    positions = None
+    if w.explicit_positions:
+        positions = np.concatenate([np.sort(g.choice(int(L), size=int(n), replace=False)) if n else
+                                    np.zeros(0, dtype=np.int64) for L, n in zip(lens, nq)]).astype(np.int32)
+    total_q = int(q_off[-1])
+    q = to_storage(normal_f32(w.seed, STREAM_PAGED_Q, (total_q, w.Hq, w.D)), w.dtype)
+    k = to_storage(normal_f32(w.seed, STREAM_PAGED_K, (pages, P, w.Hkv, w.D)), w.dtype)
+    v = to_storage(normal_f32(w.seed, STREAM_PAGED_V, (pages, P, w.Hkv, w.D)), w.dtype)
+    return {"q": q, "k_cache": k, "v_cache": v, "block_table": table, "seq_lens": lens, "q_offsets": q_off,
+            "positions": positions, "scale": w.softmax_scale}

@@ -70,6 +70,11 @@ def _load():
                                                  ctypes.POINTER(ctypes.c_int32), dp, ctypes.c_double,
                                                  dp, dp, dp, dp, ctypes.c_int]
             lib.oracle_attention_bwd.restype = ctypes.c_int
+            ip = ctypes.POINTER(ctypes.c_int32)
+            i64 = ctypes.c_int64
+            lib.oracle_paged_attention.argtypes = [i64, i64, i64, i64, i64, i64, dp, dp, dp, ip, ip, ip, ip,
+                                                   ctypes.c_int, ctypes.c_double, dp, dp]
+            lib.oracle_paged_attention.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -185,6 +190,47 @@ def attention_bwd(q, k, v, dout, *, mask: int = 0, kv_lens=None, bias=None, scal
     if rc != 0:
         raise ValueError(f"oracle_attention_bwd rejected its arguments (rc={rc})")
     return dq, dk, dv
+
+
+def paged_attention(q, k_cache, v_cache, block_table, seq_lens, q_offsets, *, positions=None,
+                    causal: bool = True, scale: float, dtype: str | None = None, lse: bool = False):
+    """Float64 attention over a paged key/value cache with packed queries.
+
+    q [queries, Hq, D]; k_cache, v_cache [pages, page_size, Hkv, D];
+    block_table int32 [num_seqs, max_pages]; seq_lens int32 [num_seqs];
+    q_offsets int32 [num_seqs + 1] (queries of sequence s are rows
+    q_offsets[s]..q_offsets[s+1]-1); positions int32 [queries] or None (the
+    newest tokens). Returns out [queries, Hq, D] (and lse [queries, Hq]).
+    """
+    lib = _load()
+    q64 = widen(q, dtype) if dtype else np.ascontiguousarray(q, dtype=np.float64)
+    k64 = widen(k_cache, dtype) if dtype else np.ascontiguousarray(k_cache, dtype=np.float64)
+    v64 = widen(v_cache, dtype) if dtype else np.ascontiguousarray(v_cache, dtype=np.float64)
+    nq, Hq, D = q64.shape
+    pages, P, Hkv, Dk = k64.shape
+    if Dk != D or v64.shape != k64.shape:
+        raise ValueError("k_cache and v_cache must be [pages, page_size, Hkv, D]")
+    tab = np.ascontiguousarray(block_table, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    offs = np.ascontiguousarray(q_offsets, dtype=np.int32)
+    ns = lens.shape[0]
+    if tab.ndim != 2 or tab.shape[0] != ns or offs.shape != (ns + 1,) or offs[-1] != nq:
+        raise ValueError("block_table [num_seqs, max_pages], q_offsets [num_seqs + 1] ending at queries")
+    for s_ in range(ns):
+        used = tab[s_, :(int(lens[s_]) + P - 1) // P]
+        if lens[s_] > tab.shape[1] * P or ((used < 0) | (used >= pages)).any():
+            raise ValueError("block_table does not cover the sequence inside the cache")
+    pos = None if positions is None else np.ascontiguousarray(positions, dtype=np.int32)
+    out = np.empty((nq, Hq, D), dtype=np.float64)
+    ls = np.empty((nq, Hq), dtype=np.float64) if lse else None
+    ip = ctypes.POINTER(ctypes.c_int32)
+    rc = lib.oracle_paged_attention(ns, Hq, Hkv, D, P, tab.shape[1], _dptr(q64), _dptr(k64), _dptr(v64),
+                                    tab.ctypes.data_as(ip), lens.ctypes.data_as(ip), offs.ctypes.data_as(ip),
+                                    pos.ctypes.data_as(ip) if pos is not None else None, int(bool(causal)),
+                                    float(scale), _dptr(out), _dptr(ls))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_attention rejected its arguments (rc={rc})")
+    return (out, ls) if lse else out
 
 
 def prepare(q, k, v, *, kv_lens=None, bias=None, dtype: str | None = None):

@@ -398,3 +398,85 @@ int oracle_attention_bwd(const oracle_shape* s, const double* q, const double* k
   pthread_mutex_destroy(&J.lock);
   return J.failed ? -2 : 0;
 }
+
+/*
+ * Paged key/value cache, packed variable-length queries.
+ *
+ * Source: ruDNN user guide, section 9 (paged attention): keys and values live
+ * in physical pages K [pages, page_size, Hkv, D] and V [pages, page_size, Hkv,
+ * D]; each sequence has a page table, a key length and queries at zero-based
+ * absolute positions; queries are packed as Q [queries, Hq, D] and the output
+ * is [queries, Hq, D]; causal attention compares absolute positions.
+ *
+ * Readings: the queries of sequence s are rows q_off[s] .. q_off[s+1]-1 of Q
+ * (packed in sequence order); key j of sequence s is row j % page_size of page
+ * table[s * max_pages + j / page_size]; keys j < seq_len[s] exist; under the
+ * causal mask the query at position pos sees keys j <= pos. When `positions`
+ * is NULL, the n queries of a sequence of length L are its newest tokens, at
+ * positions L - n .. L - 1. Everything else (max subtraction, GQA mapping, an
+ * empty row giving NaN and lse = -inf) is as in the dense definition above.
+ */
+int oracle_paged_attention(int64_t num_seqs, int64_t Hq, int64_t Hkv, int64_t D, int64_t page_size,
+                           int64_t max_pages, const double* q, const double* kc, const double* vc,
+                           const int32_t* table, const int32_t* seq_len, const int32_t* q_off,
+                           const int32_t* positions, int causal, double scale, double* out,
+                           double* lse) {
+  if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || page_size <= 0 || max_pages < 0)
+    return -1;
+  const int64_t group = Hq / Hkv;
+  int64_t cap = 1;
+  for (int64_t s = 0; s < num_seqs; ++s)
+    if (seq_len[s] > cap) cap = seq_len[s];
+  double* sc = (double*)malloc(sizeof(double) * (size_t)cap);
+  if (!sc) return -2;
+  for (int64_t s = 0; s < num_seqs; ++s) {
+    const int64_t L = seq_len[s];
+    const int64_t n = q_off[s + 1] - q_off[s];
+    if (L < 0 || n < 0 || L > max_pages * page_size) {
+      free(sc);
+      return -1;
+    }
+    for (int64_t t = q_off[s]; t < q_off[s + 1]; ++t) {
+      const int64_t pos = positions ? positions[t] : L - n + (t - q_off[s]);
+      for (int64_t h = 0; h < Hq; ++h) {
+        const int64_t hk = h / group;
+        const double* qi = q + (t * Hq + h) * D;
+        double* o = out + (t * Hq + h) * D;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < L; ++j) {
+          double sj = -INFINITY;
+          if (!causal || j <= pos) {
+            const int64_t page = table[s * max_pages + j / page_size];
+            const double* kj = kc + ((page * page_size + j % page_size) * Hkv + hk) * D;
+            double dot = 0.0;
+            for (int64_t d = 0; d < D; ++d) dot += qi[d] * kj[d];
+            sj = scale * dot;
+          }
+          sc[j] = sj;
+          if (sj > m) m = sj;
+        }
+        if (m == -INFINITY) {
+          for (int64_t d = 0; d < D; ++d) o[d] = NAN;
+          if (lse) lse[t * Hq + h] = -INFINITY;
+          continue;
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < L; ++j) {
+          sc[j] = exp(sc[j] - m);
+          l += sc[j];
+        }
+        if (lse) lse[t * Hq + h] = m + log(l);
+        for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+        for (int64_t j = 0; j < L; ++j) {
+          if (sc[j] == 0.0) continue;
+          const int64_t page = table[s * max_pages + j / page_size];
+          const double* vj = vc + ((page * page_size + j % page_size) * Hkv + hk) * D;
+          const double w = sc[j] / l;
+          for (int64_t d = 0; d < D; ++d) o[d] += w * vj[d];
+        }
+      }
+    }
+  }
+  free(sc);
+  return 0;
+}

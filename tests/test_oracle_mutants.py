@@ -12,6 +12,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_bwd_pins as bpins
+from tests import test_oracle_paged_pins as ppins
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_ref.c")
@@ -52,6 +53,28 @@ MUTANTS_BWD = {
 }
 
 
+# Mistakes in the paged-cache attention, caught by the paged pins.
+MUTANTS_PAGED = {
+    "paged_row_reversed": ("const double* kj = kc + ((page * page_size + j % page_size) * Hkv + hk) * D;",
+                           "const double* kj = kc + ((page * page_size + (page_size - 1 - j % page_size)) * Hkv + hk) * D;"),
+    "paged_table_stride": ("if (!causal || j <= pos) {\n            const int64_t page = table[s * max_pages + j / page_size];",
+                           "if (!causal || j <= pos) {\n            const int64_t page = table[s + j / page_size];"),
+    "paged_causal_strict": ("if (!causal || j <= pos) {", "if (!causal || j < pos) {"),
+    "paged_default_positions": ("const int64_t pos = positions ? positions[t] : L - n + (t - q_off[s]);",
+                                "const int64_t pos = positions ? positions[t] : L - n + (t - q_off[s]) - 1;"),
+    "paged_v_head": ("const double* vj = vc + ((page * page_size + j % page_size) * Hkv + hk) * D;",
+                     "const double* vj = vc + ((page * page_size + j % page_size) * Hkv + 0) * D;"),
+}
+
+
+def _paged_pins():
+    for ps in (1, 4, 16):
+        for sq_sk in ((5, 5), (3, 11), (1, 9)):
+            yield lambda p=ps, s=sq_sk: ppins.test_equal_lengths_equal_dense_bottom_right_causal(p, s)
+    yield ppins.test_variable_lengths_non_causal_equal_dense_key_padding
+    yield ppins.test_decode_step_sees_every_key
+
+
 def _bwd_pins():
     yield bpins.test_single_key
     yield bpins.test_identical_keys_give_zero_query_gradient
@@ -76,9 +99,9 @@ def _pins():
                 yield lambda m=mask, b=bshape, s=sq_sk: pins.test_brute_force_tiny(m, b, s)
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS) + sorted(MUTANTS_BWD))
+@pytest.mark.parametrize("name", sorted(MUTANTS) + sorted(MUTANTS_BWD) + sorted(MUTANTS_PAGED))
 def test_pins_catch_mutant(name, tmp_path, monkeypatch):
-    old, new = MUTANTS[name] if name in MUTANTS else MUTANTS_BWD[name]
+    old, new = {**MUTANTS, **MUTANTS_BWD, **MUTANTS_PAGED}[name]
     src = open(SRC).read()
     assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
     mut = tmp_path / "attn_mut.c"
@@ -96,9 +119,12 @@ def test_pins_catch_mutant(name, tmp_path, monkeypatch):
     lib.oracle_attention_rows.restype = ctypes.c_int
     lib.oracle_attention_bwd.argtypes = real.oracle_attention_bwd.argtypes
     lib.oracle_attention_bwd.restype = ctypes.c_int
+    lib.oracle_paged_attention.argtypes = real.oracle_paged_attention.argtypes
+    lib.oracle_paged_attention.restype = ctypes.c_int
     monkeypatch.setattr(oracle, "_lib", lib)
     caught = []
-    for pin in (_pins() if name in MUTANTS else _bwd_pins()):
+    pins_for = _pins if name in MUTANTS else (_bwd_pins if name in MUTANTS_BWD else _paged_pins)
+    for pin in pins_for():
         try:
             pin()
         except AssertionError:
