@@ -35,6 +35,12 @@ class Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("B", "Hq", "Hkv", "Sq", "Sk", "D", "bias_b", "bias_h")]
 
 
+class PagedShape(ctypes.Structure):
+    """attn_paged_shape_t."""
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_seqs", "num_queries", "Hq", "Hkv", "D", "page_size",
+                                               "num_pages", "max_pages", "max_queries")]
+
+
 def library_path() -> str:
     return os.path.join(_HERE, _LIBNAME)
 
@@ -66,6 +72,9 @@ def load_library():
         lib.attn_bwd.restype = ctypes.c_int
         lib.attn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_bwd_workspace_bytes.restype = ctypes.c_int
+        lib.attn_paged_fwd.argtypes = [ctypes.POINTER(PagedShape), vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                       ctypes.c_float, ctypes.c_int, vp, vp, vp]
+        lib.attn_paged_fwd.restype = ctypes.c_int
         lib.attn_strerror.argtypes = [ctypes.c_int]
         lib.attn_strerror.restype = ctypes.c_char_p
         lib.attn_last_cuda_error.argtypes = []
@@ -302,3 +311,57 @@ def bwd(q, k, v, out, dout, lse, *, causal: bool = False, kv_lens=None, bias=Non
                                   dq.data_ptr() or None, dk.data_ptr() or None, dv.data_ptr() or None,
                                   stream.cuda_stream or None))
     return dq, dk, dv
+
+
+def paged_fwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, *, positions=None, causal: bool = True,
+              scale: float | None = None, max_queries: int | None = None, return_lse: bool = False, out=None,
+              stream=None):
+    """Attention of packed queries over a paged key/value cache (attn_paged_fwd).
+
+    q [queries, Hq, D]; k_cache, v_cache [pages, page_size, Hkv, D] (same
+    dtype, CUDA, contiguous); block_table int32 [num_seqs, max_pages];
+    seq_lens int32 [num_seqs]; q_offsets int32 [num_seqs + 1]; positions
+    int32 [queries] or None. ``max_queries`` bounds the queries of one
+    sequence (computed from q_offsets, with a host sync, when None).
+    Returns out [queries, Hq, D] (and lse float32 [queries, Hq]).
+    """
+    import torch
+
+    dev = q.device
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if t.device != dev or t.dtype != q.dtype or not t.is_contiguous() or t.dim() != 4:
+            raise AttnError(f"{name} must be a contiguous 4-D {q.dtype} tensor on {dev}")
+    if q.dim() != 3 or not q.is_contiguous():
+        raise AttnError("q must be a contiguous [queries, Hq, D] tensor")
+    nq, Hq, D = q.shape
+    pages, P, Hkv, Dk = k_cache.shape
+    if Dk != D or v_cache.shape != k_cache.shape:
+        raise AttnError("k_cache and v_cache must be [pages, page_size, Hkv, D] with q's D")
+    ints = {}
+    for name, t in (("block_table", block_table), ("seq_lens", seq_lens), ("q_offsets", q_offsets),
+                    ("positions", positions)):
+        if t is None:
+            continue
+        if t.device != dev or t.dtype != torch.int32 or not t.is_contiguous():
+            raise AttnError(f"{name} must be a contiguous int32 tensor on q's device")
+        ints[name] = t
+    ns = int(seq_lens.shape[0])
+    if block_table.dim() != 2 or block_table.shape[0] != ns or tuple(q_offsets.shape) != (ns + 1,):
+        raise AttnError("block_table must be [num_seqs, max_pages] and q_offsets [num_seqs + 1]")
+    if positions is not None and tuple(positions.shape) != (nq,):
+        raise AttnError("positions must be int32 [queries]")
+    if max_queries is None:
+        max_queries = int((q_offsets[1:] - q_offsets[:-1]).max().item()) if ns else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    lse = torch.empty((nq, Hq), dtype=torch.float32, device=dev) if return_lse else None
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    shape = PagedShape(ns, nq, Hq, Hkv, D, P, pages, int(block_table.shape[1]), int(max_queries))
+    ptr = lambda t: (t.data_ptr() or None) if t is not None else None
+    check(load_library().attn_paged_fwd(ctypes.byref(shape), ptr(q), ptr(k_cache), ptr(v_cache), ptr(block_table),
+                                        ptr(seq_lens), ptr(q_offsets), ptr(positions), int(bool(causal)),
+                                        float(scale), _dtype_code(q), ptr(out), ptr(lse), stream.cuda_stream or None))
+    return (out, lse) if return_lse else out

@@ -463,3 +463,77 @@ int attn_bwd(const attn_shape_t* shape, const void* q, const void* k, const void
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- paged cache
+extern "C" {
+
+int attn_paged_fwd(const attn_paged_shape_t* shape, const void* q, const void* k_cache,
+                   const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+                   const int32_t* q_offsets, const int32_t* positions, int causal, float scale,
+                   attn_dtype_t dtype, void* out, float* lse, void* stream) {
+  if (!shape) return ATTN_ERR_NULL;
+  const attn_paged_shape_t s = *shape;
+  if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+  if (s.num_seqs < 0 || s.num_queries < 0 || s.Hq <= 0 || s.Hkv <= 0 || s.D <= 0 || s.page_size <= 0 ||
+      s.num_pages < 0 || s.max_pages < 0 || s.max_queries < 0 || s.Hq % s.Hkv != 0)
+    return ATTN_ERR_SHAPE;
+  if (causal != 0 && causal != 1) return ATTN_ERR_MASK;
+  if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_SCALE;
+  if (!(s.D == 16 || s.D == 32 || s.D == 64 || s.D == 128)) return ATTN_ERR_HEAD_DIM;
+  const int64_t group = s.Hq / s.Hkv;
+  if (static_cast<int64_t>(s.num_seqs) * s.Hkv > 0x7fffffffLL ||
+      (static_cast<int64_t>(s.max_queries) * group + 63) / 64 > 65535 ||
+      static_cast<int64_t>(s.max_pages) * s.page_size > 0x7fffffffLL)
+    return ATTN_ERR_SHAPE;
+  if (s.num_queries == 0 || s.num_seqs == 0) return ATTN_OK;
+  if (!q || !out || !seq_lens || !q_offsets || (s.max_pages > 0 && !block_table) ||
+      (s.num_pages > 0 && (!k_cache || !v_cache)))
+    return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out) || (k_cache && !aligned16(k_cache)) || (v_cache && !aligned16(v_cache)))
+    return ATTN_ERR_ALIGN;
+  for (const void* pi : {static_cast<const void*>(block_table), static_cast<const void*>(seq_lens),
+                         static_cast<const void*>(q_offsets), static_cast<const void*>(positions),
+                         static_cast<const void*>(lse)})
+    if (pi && (reinterpret_cast<uintptr_t>(pi) & 3u)) return ATTN_ERR_ALIGN;
+  const int es = elem_size(dtype);
+  const int64_t q_bytes = static_cast<int64_t>(s.num_queries) * s.Hq * s.D * es;
+  const int64_t kv_bytes = static_cast<int64_t>(s.num_pages) * s.page_size * s.Hkv * s.D * es;
+  const int64_t lse_bytes = lse ? static_cast<int64_t>(s.num_queries) * s.Hq * 4 : 0;
+  struct Buf { const void* p; int64_t n; };
+  const Buf ins[] = {{q, q_bytes}, {k_cache, kv_bytes}, {v_cache, kv_bytes},
+                     {block_table, static_cast<int64_t>(s.num_seqs) * s.max_pages * 4},
+                     {seq_lens, static_cast<int64_t>(s.num_seqs) * 4},
+                     {q_offsets, static_cast<int64_t>(s.num_seqs + 1) * 4},
+                     {positions, positions ? static_cast<int64_t>(s.num_queries) * 4 : 0}};
+  for (const Buf& b : ins)
+    if (overlaps(out, q_bytes, b.p, b.n) || overlaps(lse, lse_bytes, b.p, b.n)) return ATTN_ERR_OVERLAP;
+  if (overlaps(out, q_bytes, lse, lse_bytes)) return ATTN_ERR_OVERLAP;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  attn::PagedParams pp{};
+  pp.num_seqs = s.num_seqs;
+  pp.num_queries = s.num_queries;
+  pp.Hq = s.Hq;
+  pp.Hkv = s.Hkv;
+  pp.page_size = s.page_size;
+  pp.num_pages = s.num_pages;
+  pp.max_pages = s.max_pages;
+  pp.max_queries = s.max_queries;
+  pp.block_table = block_table;
+  pp.seq_lens = seq_lens;
+  pp.q_offsets = q_offsets;
+  pp.positions = positions;
+  pp.causal = causal;
+  pp.scale_log2 = scale * 1.4426950408889634f;
+  pp.status = status_ptr(dev);
+  pp.device = dev;
+  int unsupported = 0;
+  e = attn::launch_paged_simt(s.D, static_cast<int>(dtype), pp, q, k_cache, v_cache, out, lse,
+                              static_cast<cudaStream_t>(stream), &unsupported);
+  if (unsupported) return ATTN_ERR_HEAD_DIM;
+  return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,169 @@
+// attn_paged.cu - attention over a paged key/value cache with packed
+// variable-length queries, fp32 FMA arithmetic for every dtype.
+//
+// Source: ruDNN user guide, section 9 (paged attention): the kernel reads the
+// physical cache pages directly (K and V [pages, page_size, Hkv, D]) through
+// per-sequence page tables, handles packed prefill and decode queries
+// ([queries, Hq, D], output likewise), and compares absolute positions for
+// the causal mask. Key j of sequence s is row j % page_size of page
+// table[s][j / page_size]; the queries of sequence s are rows
+// q_offsets[s] .. q_offsets[s+1]-1; a query at position pos sees keys
+// j < seq_len[s] (and j <= pos when causal); without explicit positions the
+// n queries of a sequence of length L sit at L - n .. L - 1.
+//
+// CTA = one (sequence, kv head) and 64 rows, a row being a (query, query
+// head of the GQA group) pair, so every key/value row gathered into shared
+// memory serves all the heads that share it. 4 threads per row, as in the
+// F32 kernel; keys stream 32 at a time.
+//
+// Metadata is trusted only as far as memory safety: a page index outside
+// [0, num_pages) reads as zeros, lengths are clamped to the table's capacity
+// and query offsets to [0, num_queries].
+#include "params.h"
+#include "ptx.cuh"
+#include "simt.cuh"
+
+namespace attn {
+namespace paged {
+
+using simt::axpy4;
+using simt::dot4;
+using simt::load4;
+using simt::store4;
+
+constexpr int ROWS = 64;
+constexpr int THREADS = 256;
+constexpr int KT = 32;
+constexpr float LN2 = 0.6931471805599453f;
+
+template <int D, int DT>
+__global__ void __launch_bounds__(THREADS) paged_fwd_kernel(const void* __restrict__ q,
+                                                            const void* __restrict__ kc,
+                                                            const void* __restrict__ vc,
+                                                            void* __restrict__ out, float* __restrict__ lse,
+                                                            const PagedParams pp) {
+  constexpr int G = D / 4;
+  constexpr int GPT = G / 4;
+  __shared__ float4 ks[KT][G];
+  __shared__ float4 vs[KT][G];
+
+  const int tid = threadIdx.x, part = tid & 3, rl = tid >> 2;
+  const int s = blockIdx.x / pp.Hkv, hk = blockIdx.x - s * pp.Hkv;
+  const int group = pp.Hq / pp.Hkv;
+  const int q_lo = min(max(__ldg(pp.q_offsets + s), 0), pp.num_queries);
+  const int q_hi = min(max(__ldg(pp.q_offsets + s + 1), q_lo), pp.num_queries);
+  const int nq = q_hi - q_lo;
+  const int r = blockIdx.y * ROWS + rl;  // row = (query, head of the group)
+  if (blockIdx.y * ROWS >= nq * group) return;  // CTA-uniform
+  const int tq = r / group;
+  const int h = hk * group + (r - tq * group);
+  const bool row_ok = tq < nq;
+  const int t = q_lo + (row_ok ? tq : 0);
+  const int L = min(max(__ldg(pp.seq_lens + s), 0), pp.max_pages * pp.page_size);
+  const int pos = pp.positions ? __ldg(pp.positions + t) : L - nq + tq;
+  const int key_hi_row = pp.causal ? min(L, pos + 1) : L;  // keys [0, key_hi_row) are visible to this row
+  // keys any row of this CTA may see
+  int key_hi = L;
+  if (pp.causal && !pp.positions) {
+    const int last = min(nq - 1, (blockIdx.y * ROWS + ROWS - 1) / group);
+    key_hi = min(L, L - nq + last + 1);
+  }
+
+  const size_t qrow = (static_cast<size_t>(t) * pp.Hq + h) * G;
+  float4 qr[GPT], acc[GPT];
+#pragma unroll
+  for (int i = 0; i < GPT; ++i) {
+    qr[i] = row_ok ? load4<DT>(q, qrow + part + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int32_t* table = pp.block_table + static_cast<size_t>(s) * pp.max_pages;
+  float m_run = -INFINITY, l_run = 0.f;
+  for (int key0 = 0; key0 < key_hi; key0 += KT) {
+    __syncthreads();
+    for (int e = tid; e < KT * G; e += THREADS) {
+      const int kr = e / G, c = e - (e / G) * G;
+      const int j = key0 + kr;
+      float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+      if (j < key_hi) {
+        const int page = __ldg(table + j / pp.page_size);
+        if (page >= 0 && page < pp.num_pages) {
+          const size_t idx = ((static_cast<size_t>(page) * pp.page_size + j % pp.page_size) * pp.Hkv + hk) * G + c;
+          kv = load4<DT>(kc, idx);
+          vv = load4<DT>(vc, idx);
+        }
+      }
+      ks[kr][c] = kv;
+      vs[kr][c] = vv;
+    }
+    __syncthreads();
+    float sreg[KT];
+#pragma unroll
+    for (int c = 0; c < KT; ++c) {
+      float d = 0.f;
+#pragma unroll
+      for (int i = 0; i < GPT; ++i) d = dot4(qr[i], ks[c][part + 4 * i], d);
+      d += __shfl_xor_sync(0xffffffffu, d, 1);
+      d += __shfl_xor_sync(0xffffffffu, d, 2);
+      sreg[c] = (row_ok && key0 + c < key_hi_row) ? d * pp.scale_log2 : -INFINITY;
+    }
+    float mx = sreg[0];
+#pragma unroll
+    for (int c = 1; c < KT; ++c) mx = fmaxf(mx, sreg[c]);
+    const float m_new = fmaxf(m_run, mx);
+    const float m_use = m_new == -INFINITY ? 0.f : m_new;
+    const float alpha = fast_exp2(m_run - m_use);
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < KT; ++c) {
+      sreg[c] = fast_exp2(sreg[c] - m_use);
+      sum += sreg[c];
+    }
+    l_run = l_run * alpha + sum;
+    m_run = m_new;
+#pragma unroll
+    for (int i = 0; i < GPT; ++i) {
+      float4 a = acc[i];
+      a.x *= alpha; a.y *= alpha; a.z *= alpha; a.w *= alpha;
+#pragma unroll
+      for (int c = 0; c < KT; ++c) a = axpy4(sreg[c], vs[c][part + 4 * i], a);
+      acc[i] = a;
+    }
+  }
+  if (!row_ok) return;
+  const float inv = l_run > 0.f ? 1.f / l_run : __int_as_float(0x7fc00000);
+#pragma unroll
+  for (int i = 0; i < GPT; ++i) {
+    const float4 a = acc[i];
+    store4<DT>(out, qrow + part + 4 * i, make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
+  }
+  if (lse && part == 0)
+    lse[static_cast<size_t>(t) * pp.Hq + h] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+}
+
+template <int DT>
+static cudaError_t launch_dt(int D, const PagedParams& pp, const void* q, const void* k, const void* v,
+                             void* out, float* lse, cudaStream_t st, int* unsupported) {
+  const int group = pp.Hq / pp.Hkv;
+  const int64_t ry = (static_cast<int64_t>(pp.max_queries) * group + ROWS - 1) / ROWS;
+  const dim3 grid(static_cast<unsigned>(pp.num_seqs) * pp.Hkv, static_cast<unsigned>(ry > 0 ? ry : 1));
+  switch (D) {
+    case 16: paged_fwd_kernel<16, DT><<<grid, THREADS, 0, st>>>(q, k, v, out, lse, pp); break;
+    case 32: paged_fwd_kernel<32, DT><<<grid, THREADS, 0, st>>>(q, k, v, out, lse, pp); break;
+    case 64: paged_fwd_kernel<64, DT><<<grid, THREADS, 0, st>>>(q, k, v, out, lse, pp); break;
+    case 128: paged_fwd_kernel<128, DT><<<grid, THREADS, 0, st>>>(q, k, v, out, lse, pp); break;
+    default: *unsupported = 1; return cudaSuccess;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace paged
+
+cudaError_t launch_paged_simt(int D, int dtype, const PagedParams& pp, const void* q, const void* k,
+                              const void* v, void* out, float* lse, cudaStream_t stream, int* unsupported) {
+  *unsupported = 0;
+  if (dtype == 0) return paged::launch_dt<0>(D, pp, q, k, v, out, lse, stream, unsupported);
+  if (dtype == 1) return paged::launch_dt<1>(D, pp, q, k, v, out, lse, stream, unsupported);
+  return paged::launch_dt<2>(D, pp, q, k, v, out, lse, stream, unsupported);
+}
+
+}  // namespace attn

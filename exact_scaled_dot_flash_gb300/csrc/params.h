@@ -76,6 +76,21 @@ cudaError_t launch_bwd_tc_instance(EncodeTiledFn enc, const void* q, const void*
 cudaError_t launch_bwd_preprocess(int D, int dtype, const void* out, const void* dout, const float* lse,
                                   float* dsum, float* lse2, int64_t rows, cudaStream_t stream);
 
+// Paged key/value cache with packed variable-length queries.
+struct PagedParams {
+  int num_seqs, num_queries, Hq, Hkv, page_size, num_pages, max_pages, max_queries;
+  const int32_t* block_table;  // [num_seqs, max_pages] physical page of each key block
+  const int32_t* seq_lens;     // [num_seqs] keys of each sequence
+  const int32_t* q_offsets;    // [num_seqs + 1] query rows of sequence s: [q_offsets[s], q_offsets[s+1])
+  const int32_t* positions;    // [num_queries] absolute positions, or nullptr (the newest tokens)
+  int causal;
+  float scale_log2;
+  int* status;
+  int device;
+};
+cudaError_t launch_paged_simt(int D, int dtype, const PagedParams& pp, const void* q, const void* k,
+                              const void* v, void* out, float* lse, cudaStream_t stream, int* unsupported);
+
 // Backward, fp32 FMA path for every dtype (dtype: 0 f32, 1 f16, 2 bf16): the
 // preprocess (dsum = rowsum(dout * out), lse2 = lse * log2 e), then dk/dv and dq.
 cudaError_t launch_bwd_simt(int D, int dtype, const KernelParams& p, const void* q, const void* k,

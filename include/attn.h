@@ -212,6 +212,48 @@ ATTN_API int attn_bwd(const attn_shape_t* shape,
  * ATTN_OK, ATTN_ERR_NULL or ATTN_ERR_SHAPE. */
 ATTN_API int attn_bwd_workspace_bytes(const attn_shape_t* shape, size_t* bytes);
 
+/* Shape of a paged-cache call. Counts are elements.
+ *   q, out  [num_queries, Hq, D]           packed queries, sequence by sequence
+ *   k_cache, v_cache [num_pages, page_size, Hkv, D]   physical pages
+ *   block_table [num_seqs, max_pages] int32   physical page of key block b of sequence s
+ *   max_queries: an upper bound on the queries of one sequence (sizes the grid). */
+typedef struct {
+  int32_t num_seqs, num_queries, Hq, Hkv, D;
+  int32_t page_size, num_pages, max_pages, max_queries;
+} attn_paged_shape_t;
+
+/* attn_paged_fwd - attention of packed variable-length queries over a paged
+ * key/value cache (prefill chunks and decode steps in one call).
+ *
+ * Source: ruDNN user guide, section 9 (paged attention): the call reads the
+ * physical cache pages through per-sequence page tables, handles packed
+ * prefill and decode, maps query head hq to key/value head hq / (Hq / Hkv),
+ * and applies the causal mask by absolute position.
+ *
+ * Key j of sequence s is row j % page_size of page block_table[s][j / page_size];
+ * sequence s has seq_lens[s] keys (clamped to [0, max_pages * page_size]). Its
+ * queries are rows q_offsets[s] .. q_offsets[s+1]-1 of q (offsets clamped to
+ * [0, num_queries]); a query row outside every range is not written. With
+ * causal = 1 the query at position p sees keys j <= p; positions (int32
+ * [num_queries], zero-based, absolute within the sequence) may be NULL, which
+ * places the n queries of a sequence of length L at L - n .. L - 1. A row that
+ * sees no key is NaN (lse -inf). lse: NULL or float [num_queries, Hq] natural
+ * log-sum-exp.
+ *
+ * All pointers are device pointers: q, k_cache, v_cache, out 16-byte aligned;
+ * the int32 arrays and lse 4-byte aligned; out and lse disjoint from every
+ * input. Page-table entries outside [0, num_pages) read as zero keys and
+ * values (no out-of-bounds access). D in {16, 32, 64, 128}, every dtype.
+ * Asynchronous on `stream`; returns ATTN_OK or a negative ATTN_ERR_* code
+ * (ATTN_ERR_MASK for causal not in {0, 1}). */
+ATTN_API int attn_paged_fwd(const attn_paged_shape_t* shape,
+                            const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_table, const int32_t* seq_lens,
+                            const int32_t* q_offsets, const int32_t* positions,
+                            int causal, float scale, attn_dtype_t dtype,
+                            void* out, float* lse,
+                            void* stream);
+
 /* Size of the device scratch array built into the library for
  * attn_fwd_split_noalloc (32 MiB per GPU that loads the library). */
 #define ATTN_NOALLOC_SCRATCH_BYTES (32u << 20)
