@@ -403,6 +403,99 @@ def bench_gpu(args):
         dist.destroy_process_group()
 
 
+def bench_paged(args):
+    """Paged-cache attention (attn_paged_fwd) on a serving-shaped workload: one
+    step = one call over the packed queries of every sequence."""
+    import numpy as np
+    import torch
+    from exact_scaled_dot_flash_gb300 import attn
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    w = synth.PAGED_WORKLOADS[args.workload]
+    x = synth.make_paged_inputs(w)
+    q, kc, vc = (make_device_tensor(x[n], w.dtype, device) for n in ("q", "k_cache", "v_cache"))
+    ints = {n: torch.from_numpy(x[n]).to(device) for n in ("block_table", "seq_lens", "q_offsets")}
+    pos = torch.from_numpy(x["positions"]).to(device) if x["positions"] is not None else None
+    nq_s = np.diff(x["q_offsets"])
+    max_q = int(nq_s.max()) if len(nq_s) else 0
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        attn.paged_fwd(q, kc, vc, ints["block_table"], ints["seq_lens"], ints["q_offsets"], positions=pos,
+                       causal=w.causal, scale=x["scale"], max_queries=max_q, out=out, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    attn.device_status(device.index, clear=True)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_id = vis.split(",")[device.index] if vis else str(device.index)
+    with ClockSampler(smi_id) as clocks:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+    elapsed_ms = start.elapsed_time(end)
+    if attn.device_status(device.index, clear=True):
+        raise RuntimeError("kernel status flags set during the timed region")
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    ms = elapsed_ms / args.steps
+    # exact work: 4*D FLOP per visible (query, key) pair and query head
+    pairs = 0
+    for s_, L in enumerate(x["seq_lens"]):
+        n = int(nq_s[s_])
+        pq = (x["positions"][x["q_offsets"][s_]:x["q_offsets"][s_ + 1]] if x["positions"] is not None
+              else np.arange(L - n, L))
+        pairs += int(np.minimum(L, np.asarray(pq, dtype=np.int64) + 1).clip(min=0).sum()) if w.causal else n * int(L)
+    flops = 4.0 * w.D * w.Hq * pairs
+    es = {"f32": 4, "f16": 2, "bf16": 2}[w.dtype]
+    nbytes = (2 * int(x["seq_lens"].sum()) * w.Hkv * w.D + 2 * int(x["q_offsets"][-1]) * w.Hq * w.D) * es
+    value = world * flops / (ms * 1e-3) / 1e12
+    if rank != 0:
+        return
+    peaks, peak_kind = load_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    mhz = (clocks.summary() or {}).get("sm_mhz") or 2070.0
+    alu_peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
+    tf = flops / (ms * 1e-3) / 1e12
+    hbm_bound = flops / nbytes < alu_peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+    roof = ({"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+             "frac": gbs / float(peaks["hbm_gbs"]), "peak_kind": f"{peak_kind} HBM copy"} if hbm_bound else
+            {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
+             "peak_kind": f"fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x {mhz:.0f} MHz"})
+    roof.update({"traffic": None, "kernel": "paged_fwd_kernel", "algorithmic_bytes": nbytes})
+    line = {
+        "metric": f"paged attention TFLOP/s ({w.name})", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "num_seqs": w.num_seqs, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "page_size": w.page_size, "ctx_range": list(w.ctx_range), "q_range": list(w.q_range),
+                   "queries": int(x["q_offsets"][-1]), "keys": int(x["seq_lens"].sum()),
+                   "parallelism": f"replicas x{world}", "flops_basis": "exact: 4*D per visible (query, key) pair",
+                   "l2": f"K/V {2 * int(x['seq_lens'].sum()) * w.Hkv * w.D * es / 2**20:.0f} MiB per step"},
+        "roofline": roof, "hbm_gbs_algorithmic": gbs, "e2e": None,
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -411,14 +504,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS) + sorted(synth.PAGED_WORKLOADS))
     ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"],
                     help="time the forward (default) or the backward (attn_bwd) of the workload")
     ap.add_argument("--splits", type=int, default=0,
                     help="key-range splits (attn_fwd_split); 0 = the workload's default")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.impl == "reference" and args.workload in synth.PAGED_WORKLOADS:
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the dense workloads"}))
+    elif args.impl == "reference":
         bench_reference(args)
+    elif args.workload in synth.PAGED_WORKLOADS:
+        bench_paged(args)
     else:
         bench_gpu(args)
 

@@ -228,3 +228,13 @@ def make_paged_inputs(w: PagedWorkload) -> dict:
     v = to_storage(normal_f32(w.seed, STREAM_PAGED_V, (pages, P, w.Hkv, w.D)), w.dtype)
     return {"q": q, "k_cache": k, "v_cache": v, "block_table": table, "seq_lens": lens, "q_offsets": q_off,
             "positions": positions, "scale": w.softmax_scale}
+
+
+PAGED_WORKLOADS = {
+    # serving decode step: one new token per sequence over 1k-8k keys
+    "bf16_paged_decode": PagedWorkload("bf16_paged_decode", BF16, 64, 32, 8, 128, 64, (1024, 8192), (1, 1),
+                                       seed=20),
+    # chunked prefill: 128-512 new tokens per sequence over 0.5k-4k keys
+    "bf16_paged_prefill": PagedWorkload("bf16_paged_prefill", BF16, 16, 32, 8, 128, 64, (512, 4096),
+                                        (128, 512), seed=21),
+}
