@@ -166,6 +166,7 @@ def make_inputs(w: Workload) -> dict:
 
 # --------------------------------------------------------------- paged caches
 STREAM_PAGED_Q, STREAM_PAGED_K, STREAM_PAGED_V, STREAM_PAGED_META = 8, 9, 10, 11
+STREAM_MLA_QP, STREAM_MLA_KP = 12, 13
 
 
 @dataclasses.dataclass(frozen=True)
@@ -202,6 +203,17 @@ def make_paged_inputs(w: PagedWorkload) -> dict:
     int32 [num_seqs, max_pages], seq_lens, q_offsets [num_seqs + 1], positions
     (int32 [queries] or None) and scale.
     """
+    meta = _paged_meta(w)
+    total_q, pages, P = int(meta["q_offsets"][-1]), meta.pop("pages"), w.page_size
+    q = to_storage(normal_f32(w.seed, STREAM_PAGED_Q, (total_q, w.Hq, w.D)), w.dtype)
+    k = to_storage(normal_f32(w.seed, STREAM_PAGED_K, (pages, P, w.Hkv, w.D)), w.dtype)
+    v = to_storage(normal_f32(w.seed, STREAM_PAGED_V, (pages, P, w.Hkv, w.D)), w.dtype)
+    return {"q": q, "k_cache": k, "v_cache": v, **meta, "scale": w.softmax_scale}
+
+
+def _paged_meta(w) -> dict:
+    """Sequence lengths, query counts, scattered page tables, query offsets and
+    (optional) explicit positions of a paged workload ``w``."""
     g = _gen(w.seed, STREAM_PAGED_META)
     lens = g.integers(w.ctx_range[0], w.ctx_range[1], size=w.num_seqs, endpoint=True).astype(np.int32)
     nq = np.array([g.integers(min(w.q_range[0], L), min(w.q_range[1], L), endpoint=True) if L > 0 else 0
@@ -222,12 +234,45 @@ def make_paged_inputs(w: PagedWorkload) -> dict:
     if w.explicit_positions:
         positions = np.concatenate([np.sort(g.choice(int(L), size=int(n), replace=False)) if n else
                                     np.zeros(0, dtype=np.int64) for L, n in zip(lens, nq)]).astype(np.int32)
-    total_q = int(q_off[-1])
-    q = to_storage(normal_f32(w.seed, STREAM_PAGED_Q, (total_q, w.Hq, w.D)), w.dtype)
-    k = to_storage(normal_f32(w.seed, STREAM_PAGED_K, (pages, P, w.Hkv, w.D)), w.dtype)
-    v = to_storage(normal_f32(w.seed, STREAM_PAGED_V, (pages, P, w.Hkv, w.D)), w.dtype)
-    return {"q": q, "k_cache": k, "v_cache": v, "block_table": table, "seq_lens": lens, "q_offsets": q_off,
-            "positions": positions, "scale": w.softmax_scale}
+    return {"block_table": table, "seq_lens": lens, "q_offsets": q_off, "positions": positions, "pages": pages}
+
+
+@dataclasses.dataclass(frozen=True)
+class MlaWorkload:
+    """MLA with absorbed projections over a paged latent cache."""
+    name: str
+    dtype: str
+    num_seqs: int
+    H: int
+    R: int                    # latent rank (query, latent and output width)
+    Pd: int                   # positional (rope) width
+    page_size: int
+    ctx_range: tuple
+    q_range: tuple
+    seed: int = 0
+    causal: bool = True
+    explicit_positions: bool = False
+    spare_pages: int = 3
+    scale: float | None = None  # the original model's QK scale; default 1/sqrt(R + Pd)
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale is not None else 1.0 / math.sqrt(self.R + self.Pd)
+
+    def replace(self, **kw) -> "MlaWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+def make_mla_inputs(w: MlaWorkload) -> dict:
+    """q [queries, H, R], qp [queries, H, Pd], latent [pages, page_size, 1, R],
+    kpos [pages, page_size, 1, Pd] in storage format, plus the paged metadata."""
+    meta = _paged_meta(w)
+    total_q, pages, P = int(meta["q_offsets"][-1]), meta.pop("pages"), w.page_size
+    q = to_storage(normal_f32(w.seed, STREAM_PAGED_Q, (total_q, w.H, w.R)), w.dtype)
+    qp = to_storage(normal_f32(w.seed, STREAM_MLA_QP, (total_q, w.H, w.Pd)), w.dtype)
+    lat = to_storage(normal_f32(w.seed, STREAM_PAGED_K, (pages, P, 1, w.R)), w.dtype)
+    kp = to_storage(normal_f32(w.seed, STREAM_MLA_KP, (pages, P, 1, w.Pd)), w.dtype)
+    return {"q": q, "qp": qp, "latent": lat, "kpos": kp, **meta, "scale": w.softmax_scale}
 
 
 PAGED_WORKLOADS = {

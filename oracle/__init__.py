@@ -75,6 +75,9 @@ def _load():
             lib.oracle_paged_attention.argtypes = [i64, i64, i64, i64, i64, i64, dp, dp, dp, ip, ip, ip, ip,
                                                    ctypes.c_int, ctypes.c_double, dp, dp]
             lib.oracle_paged_attention.restype = ctypes.c_int
+            lib.oracle_paged_mla.argtypes = [i64, i64, i64, i64, i64, i64, dp, dp, dp, dp, ip, ip, ip, ip,
+                                             ctypes.c_int, ctypes.c_double, dp, dp]
+            lib.oracle_paged_mla.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -230,6 +233,45 @@ def paged_attention(q, k_cache, v_cache, block_table, seq_lens, q_offsets, *, po
                                     float(scale), _dptr(out), _dptr(ls))
     if rc != 0:
         raise ValueError(f"oracle_paged_attention rejected its arguments (rc={rc})")
+    return (out, ls) if lse else out
+
+
+def paged_mla(q, qp, latent, kpos, block_table, seq_lens, q_offsets, *, positions=None, causal: bool = True,
+              scale: float, dtype: str | None = None, lse: bool = False):
+    """Float64 MLA over a paged latent cache (absorbed projections).
+
+    q [queries, H, R]; qp [queries, H, P]; latent [pages, page_size, 1, R];
+    kpos [pages, page_size, 1, P]; paging, packing and positions as in
+    :func:`paged_attention`. Returns out [queries, H, R] (and lse [queries, H]).
+    """
+    lib = _load()
+    w = (lambda a: widen(a, dtype)) if dtype else (lambda a: np.ascontiguousarray(a, dtype=np.float64))
+    q64, qp64, lat64, kp64 = w(q), w(qp), w(latent), w(kpos)
+    nq, H, R = q64.shape
+    pages, P, one, R2 = lat64.shape
+    Pd = qp64.shape[2]
+    if one != 1 or R2 != R or kp64.shape != (pages, P, 1, Pd) or qp64.shape[:2] != (nq, H):
+        raise ValueError("latent [pages, page_size, 1, R], kpos [pages, page_size, 1, P], qp [queries, H, P]")
+    tab = np.ascontiguousarray(block_table, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    offs = np.ascontiguousarray(q_offsets, dtype=np.int32)
+    ns = lens.shape[0]
+    if tab.ndim != 2 or tab.shape[0] != ns or offs.shape != (ns + 1,) or offs[-1] != nq:
+        raise ValueError("block_table [num_seqs, max_pages], q_offsets [num_seqs + 1] ending at queries")
+    for s_ in range(ns):
+        used = tab[s_, :(int(lens[s_]) + P - 1) // P]
+        if lens[s_] > tab.shape[1] * P or ((used < 0) | (used >= pages)).any():
+            raise ValueError("block_table does not cover the sequence inside the cache")
+    pos = None if positions is None else np.ascontiguousarray(positions, dtype=np.int32)
+    out = np.empty((nq, H, R), dtype=np.float64)
+    ls = np.empty((nq, H), dtype=np.float64) if lse else None
+    ip = ctypes.POINTER(ctypes.c_int32)
+    rc = lib.oracle_paged_mla(ns, H, R, Pd, P, tab.shape[1], _dptr(q64), _dptr(qp64), _dptr(lat64), _dptr(kp64),
+                              tab.ctypes.data_as(ip), lens.ctypes.data_as(ip), offs.ctypes.data_as(ip),
+                              pos.ctypes.data_as(ip) if pos is not None else None, int(bool(causal)),
+                              float(scale), _dptr(out), _dptr(ls))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_mla rejected its arguments (rc={rc})")
     return (out, ls) if lse else out
 
 

@@ -480,3 +480,81 @@ int oracle_paged_attention(int64_t num_seqs, int64_t Hq, int64_t Hkv, int64_t D,
   free(sc);
   return 0;
 }
+
+/*
+ * Multi-head latent attention (MLA) with absorbed projections over a paged
+ * latent cache.
+ *
+ * Source: ruDNN user guide, section 9 (paged attention and MLA): the query is
+ * given with the key projection absorbed, q [queries, H, R], plus a positional
+ * query qp [queries, H, P]; the cache holds one shared latent row c_j
+ * [pages, page_size, 1, R] and one positional key row kp_j [pages, page_size,
+ * 1, P] per token; the output is the compressed context [queries, H, R]
+ * (value and output projections are applied by the caller); the scale is the
+ * original model's QK scale. So, for query t, head h and visible key j:
+ *
+ *   s_j = scale * (q_t,h . c_j + qp_t,h . kp_j),   out_t,h = sum_j softmax_j(s) c_j.
+ *
+ * Paging, packing, positions, the causal mask and empty rows are as in
+ * oracle_paged_attention (every head reads the same single latent head).
+ */
+int oracle_paged_mla(int64_t num_seqs, int64_t H, int64_t R, int64_t Pd, int64_t page_size, int64_t max_pages,
+                     const double* q, const double* qp, const double* lat, const double* kp, const int32_t* table,
+                     const int32_t* seq_len, const int32_t* q_off, const int32_t* positions, int causal,
+                     double scale, double* out, double* lse) {
+  if (num_seqs < 0 || H <= 0 || R <= 0 || Pd < 0 || page_size <= 0 || max_pages < 0) return -1;
+  int64_t cap = 1;
+  for (int64_t s = 0; s < num_seqs; ++s)
+    if (seq_len[s] > cap) cap = seq_len[s];
+  double* sc = (double*)malloc(sizeof(double) * (size_t)cap);
+  if (!sc) return -2;
+  for (int64_t s = 0; s < num_seqs; ++s) {
+    const int64_t L = seq_len[s];
+    const int64_t n = q_off[s + 1] - q_off[s];
+    if (L < 0 || n < 0 || L > max_pages * page_size) {
+      free(sc);
+      return -1;
+    }
+    for (int64_t t = q_off[s]; t < q_off[s + 1]; ++t) {
+      const int64_t pos = positions ? positions[t] : L - n + (t - q_off[s]);
+      for (int64_t h = 0; h < H; ++h) {
+        const double* qi = q + (t * H + h) * R;
+        const double* qpi = qp + (t * H + h) * Pd;
+        double* o = out + (t * H + h) * R;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < L; ++j) {
+          double sj = -INFINITY;
+          if (!causal || j <= pos) {
+            const int64_t row = table[s * max_pages + j / page_size] * page_size + j % page_size;
+            double dot = 0.0;
+            for (int64_t d = 0; d < R; ++d) dot += qi[d] * lat[row * R + d];
+            for (int64_t d = 0; d < Pd; ++d) dot += qpi[d] * kp[row * Pd + d];
+            sj = scale * dot;
+          }
+          sc[j] = sj;
+          if (sj > m) m = sj;
+        }
+        if (m == -INFINITY) {
+          for (int64_t d = 0; d < R; ++d) o[d] = NAN;
+          if (lse) lse[t * H + h] = -INFINITY;
+          continue;
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < L; ++j) {
+          sc[j] = exp(sc[j] - m);
+          l += sc[j];
+        }
+        if (lse) lse[t * H + h] = m + log(l);
+        for (int64_t d = 0; d < R; ++d) o[d] = 0.0;
+        for (int64_t j = 0; j < L; ++j) {
+          if (sc[j] == 0.0) continue;
+          const int64_t row = table[s * max_pages + j / page_size] * page_size + j % page_size;
+          const double w = sc[j] / l;
+          for (int64_t d = 0; d < R; ++d) o[d] += w * lat[row * R + d];
+        }
+      }
+    }
+  }
+  free(sc);
+  return 0;
+}

@@ -12,6 +12,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_bwd_pins as bpins
+from tests import test_oracle_mla_pins as mpins
 from tests import test_oracle_paged_pins as ppins
 from tests import test_oracle_pins as pins
 
@@ -59,12 +60,32 @@ MUTANTS_PAGED = {
                            "const double* kj = kc + ((page * page_size + (page_size - 1 - j % page_size)) * Hkv + hk) * D;"),
     "paged_table_stride": ("if (!causal || j <= pos) {\n            const int64_t page = table[s * max_pages + j / page_size];",
                            "if (!causal || j <= pos) {\n            const int64_t page = table[s + j / page_size];"),
-    "paged_causal_strict": ("if (!causal || j <= pos) {", "if (!causal || j < pos) {"),
-    "paged_default_positions": ("const int64_t pos = positions ? positions[t] : L - n + (t - q_off[s]);",
-                                "const int64_t pos = positions ? positions[t] : L - n + (t - q_off[s]) - 1;"),
+    "paged_causal_strict": ("if (!causal || j <= pos) {\n            const int64_t page",
+                            "if (!causal || j < pos) {\n            const int64_t page"),
+    "paged_default_positions": ("const int64_t pos = positions ? positions[t] : L - n + (t - q_off[s]);\n"
+                                "      for (int64_t h = 0; h < Hq; ++h) {",
+                                "const int64_t pos = positions ? positions[t] : L - n + (t - q_off[s]) - 1;\n"
+                                "      for (int64_t h = 0; h < Hq; ++h) {"),
     "paged_v_head": ("const double* vj = vc + ((page * page_size + j % page_size) * Hkv + hk) * D;",
                      "const double* vj = vc + ((page * page_size + j % page_size) * Hkv + 0) * D;"),
 }
+
+
+# Mistakes in MLA, caught by the MLA pins.
+MUTANTS_MLA = {
+    "mla_no_positional_term": ("for (int64_t d = 0; d < Pd; ++d) dot += qpi[d] * kp[row * Pd + d];",
+                               "for (int64_t d = 0; d < Pd; ++d) dot += 0.0 * qpi[d] * kp[row * Pd + d];"),
+    "mla_value_from_query": ("for (int64_t d = 0; d < R; ++d) o[d] += w * lat[row * R + d];",
+                             "for (int64_t d = 0; d < R; ++d) o[d] += w * qi[d];"),
+    "mla_head_stride": ("const double* qpi = qp + (t * H + h) * Pd;", "const double* qpi = qp + (t * H) * Pd;"),
+}
+
+
+def _mla_pins():
+    yield mpins.test_mla_single_key_returns_its_latent_row
+    for causal in (True, False):
+        for positions in (False, True):
+            yield lambda c=causal, p=positions: mpins.test_mla_is_single_head_attention_over_concatenated_keys(c, p, 16)
 
 
 def _paged_pins():
@@ -99,9 +120,9 @@ def _pins():
                 yield lambda m=mask, b=bshape, s=sq_sk: pins.test_brute_force_tiny(m, b, s)
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS) + sorted(MUTANTS_BWD) + sorted(MUTANTS_PAGED))
+@pytest.mark.parametrize("name", sorted(MUTANTS) + sorted(MUTANTS_BWD) + sorted(MUTANTS_PAGED) + sorted(MUTANTS_MLA))
 def test_pins_catch_mutant(name, tmp_path, monkeypatch):
-    old, new = {**MUTANTS, **MUTANTS_BWD, **MUTANTS_PAGED}[name]
+    old, new = {**MUTANTS, **MUTANTS_BWD, **MUTANTS_PAGED, **MUTANTS_MLA}[name]
     src = open(SRC).read()
     assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
     mut = tmp_path / "attn_mut.c"
@@ -121,9 +142,12 @@ def test_pins_catch_mutant(name, tmp_path, monkeypatch):
     lib.oracle_attention_bwd.restype = ctypes.c_int
     lib.oracle_paged_attention.argtypes = real.oracle_paged_attention.argtypes
     lib.oracle_paged_attention.restype = ctypes.c_int
+    lib.oracle_paged_mla.argtypes = real.oracle_paged_mla.argtypes
+    lib.oracle_paged_mla.restype = ctypes.c_int
     monkeypatch.setattr(oracle, "_lib", lib)
     caught = []
-    pins_for = _pins if name in MUTANTS else (_bwd_pins if name in MUTANTS_BWD else _paged_pins)
+    pins_for = (_pins if name in MUTANTS else _bwd_pins if name in MUTANTS_BWD
+                else _paged_pins if name in MUTANTS_PAGED else _mla_pins)
     for pin in pins_for():
         try:
             pin()
