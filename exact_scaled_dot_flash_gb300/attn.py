@@ -41,6 +41,12 @@ class PagedShape(ctypes.Structure):
                                                "num_pages", "max_pages", "max_queries")]
 
 
+class MlaShape(ctypes.Structure):
+    """attn_mla_shape_t."""
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_seqs", "num_queries", "H", "R", "Pd", "page_size",
+                                               "num_pages", "max_pages", "max_queries")]
+
+
 def library_path() -> str:
     return os.path.join(_HERE, _LIBNAME)
 
@@ -75,6 +81,9 @@ def load_library():
         lib.attn_paged_fwd.argtypes = [ctypes.POINTER(PagedShape), vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                        ctypes.c_float, ctypes.c_int, vp, vp, vp]
         lib.attn_paged_fwd.restype = ctypes.c_int
+        lib.attn_paged_mla.argtypes = [ctypes.POINTER(MlaShape), vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                       ctypes.c_float, ctypes.c_int, vp, vp, vp]
+        lib.attn_paged_mla.restype = ctypes.c_int
         lib.attn_strerror.argtypes = [ctypes.c_int]
         lib.attn_strerror.restype = ctypes.c_char_p
         lib.attn_last_cuda_error.argtypes = []
@@ -364,4 +373,48 @@ def paged_fwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, *, position
     check(load_library().attn_paged_fwd(ctypes.byref(shape), ptr(q), ptr(k_cache), ptr(v_cache), ptr(block_table),
                                         ptr(seq_lens), ptr(q_offsets), ptr(positions), int(bool(causal)),
                                         float(scale), _dtype_code(q), ptr(out), ptr(lse), stream.cuda_stream or None))
+    return (out, lse) if return_lse else out
+
+
+def paged_mla(q, qp, latent, kpos, block_table, seq_lens, q_offsets, *, positions=None, causal: bool = True,
+              scale: float, max_queries: int | None = None, return_lse: bool = False, out=None, stream=None):
+    """MLA with absorbed projections over a paged latent cache (attn_paged_mla).
+
+    q [queries, H, R]; qp [queries, H, Pd]; latent [pages, page_size, 1, R];
+    kpos [pages, page_size, 1, Pd]; metadata as for :func:`paged_fwd`;
+    ``scale`` is the original model's QK scale. Returns out [queries, H, R]
+    (and lse float32 [queries, H]).
+    """
+    import torch
+
+    dev = q.device
+    for name, t in (("qp", qp), ("latent", latent), ("kpos", kpos)):
+        if t.device != dev or t.dtype != q.dtype or not t.is_contiguous():
+            raise AttnError(f"{name} must be a contiguous {q.dtype} tensor on {dev}")
+    if q.dim() != 3 or not q.is_contiguous() or latent.dim() != 4 or latent.shape[2] != 1:
+        raise AttnError("q [queries, H, R] and latent [pages, page_size, 1, R]")
+    nq, H, R = q.shape
+    pages, P = int(latent.shape[0]), int(latent.shape[1])
+    Pd = int(qp.shape[2])
+    if tuple(latent.shape) != (pages, P, 1, R) or tuple(kpos.shape) != (pages, P, 1, Pd) or \
+            tuple(qp.shape) != (nq, H, Pd):
+        raise AttnError("qp [queries, H, Pd], kpos [pages, page_size, 1, Pd] must match q and latent")
+    for name, t in (("block_table", block_table), ("seq_lens", seq_lens), ("q_offsets", q_offsets),
+                    ("positions", positions)):
+        if t is not None and (t.device != dev or t.dtype != torch.int32 or not t.is_contiguous()):
+            raise AttnError(f"{name} must be a contiguous int32 tensor on q's device")
+    ns = int(seq_lens.shape[0])
+    if max_queries is None:
+        max_queries = int((q_offsets[1:] - q_offsets[:-1]).max().item()) if ns else 0
+    if out is None:
+        out = torch.empty_like(q)
+    lse = torch.empty((nq, H), dtype=torch.float32, device=dev) if return_lse else None
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    shape = MlaShape(ns, nq, H, R, Pd, P, pages, int(block_table.shape[1]), int(max_queries))
+    ptr = lambda t: (t.data_ptr() or None) if t is not None else None
+    check(load_library().attn_paged_mla(ctypes.byref(shape), ptr(q), ptr(qp), ptr(latent), ptr(kpos),
+                                        ptr(block_table), ptr(seq_lens), ptr(q_offsets), ptr(positions),
+                                        int(bool(causal)), float(scale), _dtype_code(q), ptr(out), ptr(lse),
+                                        stream.cuda_stream or None))
     return (out, lse) if return_lse else out

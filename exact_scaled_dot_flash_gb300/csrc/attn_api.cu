@@ -537,3 +537,78 @@ int attn_paged_fwd(const attn_paged_shape_t* shape, const void* q, const void* k
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- MLA
+extern "C" {
+
+int attn_paged_mla(const attn_mla_shape_t* shape, const void* q, const void* qp, const void* latent,
+                   const void* kpos, const int32_t* block_table, const int32_t* seq_lens,
+                   const int32_t* q_offsets, const int32_t* positions, int causal, float scale,
+                   attn_dtype_t dtype, void* out, float* lse, void* stream) {
+  if (!shape) return ATTN_ERR_NULL;
+  const attn_mla_shape_t s = *shape;
+  if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+  if (s.num_seqs < 0 || s.num_queries < 0 || s.H <= 0 || s.R <= 0 || s.Pd < 0 || s.page_size <= 0 ||
+      s.num_pages < 0 || s.max_pages < 0 || s.max_queries < 0)
+    return ATTN_ERR_SHAPE;
+  if (causal != 0 && causal != 1) return ATTN_ERR_MASK;
+  if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_SCALE;
+  if (!(s.R == 128 || s.R == 256 || s.R == 512) || !(s.Pd == 0 || s.Pd == 16 || s.Pd == 32 || s.Pd == 64))
+    return ATTN_ERR_HEAD_DIM;
+  if ((static_cast<int64_t>(s.max_queries) * s.H + 7) / 8 > 65535 ||
+      static_cast<int64_t>(s.max_pages) * s.page_size > 0x7fffffffLL)
+    return ATTN_ERR_SHAPE;
+  if (s.num_queries == 0 || s.num_seqs == 0) return ATTN_OK;
+  if (!q || !out || !seq_lens || !q_offsets || (s.max_pages > 0 && !block_table) ||
+      (s.num_pages > 0 && !latent) || (s.Pd > 0 && (!qp || (s.num_pages > 0 && !kpos))))
+    return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out) || (qp && !aligned16(qp)) || (latent && !aligned16(latent)) ||
+      (kpos && !aligned16(kpos)))
+    return ATTN_ERR_ALIGN;
+  for (const void* pi : {static_cast<const void*>(block_table), static_cast<const void*>(seq_lens),
+                         static_cast<const void*>(q_offsets), static_cast<const void*>(positions),
+                         static_cast<const void*>(lse)})
+    if (pi && (reinterpret_cast<uintptr_t>(pi) & 3u)) return ATTN_ERR_ALIGN;
+  const int es = elem_size(dtype);
+  const int64_t rows = static_cast<int64_t>(s.num_queries) * s.H;
+  const int64_t out_bytes = rows * s.R * es;
+  const int64_t lse_bytes = lse ? rows * 4 : 0;
+  const int64_t tok = static_cast<int64_t>(s.num_pages) * s.page_size;
+  struct Buf { const void* p; int64_t n; };
+  const Buf ins[] = {{q, out_bytes}, {qp, rows * s.Pd * es}, {latent, tok * s.R * es}, {kpos, tok * s.Pd * es},
+                     {block_table, static_cast<int64_t>(s.num_seqs) * s.max_pages * 4},
+                     {seq_lens, static_cast<int64_t>(s.num_seqs) * 4},
+                     {q_offsets, static_cast<int64_t>(s.num_seqs + 1) * 4},
+                     {positions, positions ? static_cast<int64_t>(s.num_queries) * 4 : 0}};
+  for (const Buf& b : ins)
+    if (overlaps(out, out_bytes, b.p, b.n) || overlaps(lse, lse_bytes, b.p, b.n)) return ATTN_ERR_OVERLAP;
+  if (overlaps(out, out_bytes, lse, lse_bytes)) return ATTN_ERR_OVERLAP;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  attn::PagedParams pp{};
+  pp.num_seqs = s.num_seqs;
+  pp.num_queries = s.num_queries;
+  pp.Hq = s.H;
+  pp.Hkv = 1;
+  pp.page_size = s.page_size;
+  pp.num_pages = s.num_pages;
+  pp.max_pages = s.max_pages;
+  pp.max_queries = s.max_queries;
+  pp.block_table = block_table;
+  pp.seq_lens = seq_lens;
+  pp.q_offsets = q_offsets;
+  pp.positions = positions;
+  pp.causal = causal;
+  pp.scale_log2 = scale * 1.4426950408889634f;
+  pp.status = status_ptr(dev);
+  pp.device = dev;
+  int unsupported = 0;
+  e = attn::launch_mla_simt(s.R, s.Pd, static_cast<int>(dtype), pp, q, qp, latent, kpos, out, lse,
+                            static_cast<cudaStream_t>(stream), &unsupported);
+  if (unsupported) return ATTN_ERR_HEAD_DIM;
+  return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+}
+
+}  // extern "C"

@@ -88,6 +88,10 @@ struct PagedParams {
   int* status;
   int device;
 };
+// MLA over a paged latent cache (PagedParams with Hq = heads, Hkv = 1).
+cudaError_t launch_mla_simt(int R, int Pd, int dtype, const PagedParams& pp, const void* q, const void* qp,
+                            const void* lat, const void* kp, void* out, float* lse, cudaStream_t stream,
+                            int* unsupported);
 cudaError_t launch_paged_simt(int D, int dtype, const PagedParams& pp, const void* q, const void* k,
                               const void* v, void* out, float* lse, cudaStream_t stream, int* unsupported);
 

@@ -254,6 +254,41 @@ ATTN_API int attn_paged_fwd(const attn_paged_shape_t* shape,
                             void* out, float* lse,
                             void* stream);
 
+/* Shape of an MLA call: q [num_queries, H, R], qp [num_queries, H, Pd],
+ * latent [num_pages, page_size, 1, R], kpos [num_pages, page_size, 1, Pd],
+ * out [num_queries, H, R]; block_table [num_seqs, max_pages]. */
+typedef struct {
+  int32_t num_seqs, num_queries, H, R, Pd;
+  int32_t page_size, num_pages, max_pages, max_queries;
+} attn_mla_shape_t;
+
+/* attn_paged_mla - multi-head latent attention with absorbed projections over
+ * a paged latent cache.
+ *
+ * Source: ruDNN user guide, section 9 (MLA): the query with the key
+ * projection absorbed (q, width R, the latent rank) and a positional query
+ * (qp, width Pd) attend over a cache of one shared latent row c_j and one
+ * positional key kp_j per token; the output is the compressed context
+ * out = sum_j softmax_j(scale * (q . c_j + qp . kp_j)) c_j, width R. Position
+ * encoding is applied by the caller before the call, the value and output
+ * projections after it; scale is the original model's QK scale.
+ *
+ * Paging, packed queries, positions (NULL = the newest tokens), the causal
+ * mask, empty rows (NaN, lse -inf) and the trust in metadata are those of
+ * attn_paged_fwd, with one key/value head shared by all H heads.
+ * Supported: R in {128, 256, 512}, Pd in {0, 16, 32, 64}; every dtype. q, qp,
+ * latent, kpos, out 16-byte aligned device pointers (qp, kpos may be NULL when
+ * Pd == 0); lse NULL or float [num_queries, H]. Asynchronous on `stream`;
+ * returns ATTN_OK or a negative ATTN_ERR_* code. */
+ATTN_API int attn_paged_mla(const attn_mla_shape_t* shape,
+                            const void* q, const void* qp,
+                            const void* latent, const void* kpos,
+                            const int32_t* block_table, const int32_t* seq_lens,
+                            const int32_t* q_offsets, const int32_t* positions,
+                            int causal, float scale, attn_dtype_t dtype,
+                            void* out, float* lse,
+                            void* stream);
+
 /* Size of the device scratch array built into the library for
  * attn_fwd_split_noalloc (32 MiB per GPU that loads the library). */
 #define ATTN_NOALLOC_SCRATCH_BYTES (32u << 20)
