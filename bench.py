@@ -418,19 +418,22 @@ def bench_paged(args):
     else:
         torch.cuda.set_device(0)
     device = torch.device("cuda", torch.cuda.current_device())
-    w = synth.PAGED_WORKLOADS[args.workload]
-    x = synth.make_paged_inputs(w)
-    q, kc, vc = (make_device_tensor(x[n], w.dtype, device) for n in ("q", "k_cache", "v_cache"))
+    is_mla = args.workload in synth.MLA_WORKLOADS
+    w = synth.MLA_WORKLOADS[args.workload] if is_mla else synth.PAGED_WORKLOADS[args.workload]
+    x = synth.make_mla_inputs(w) if is_mla else synth.make_paged_inputs(w)
+    names = ("q", "qp", "latent", "kpos") if is_mla else ("q", "k_cache", "v_cache")
+    t = [make_device_tensor(x[n], w.dtype, device) for n in names]
     ints = {n: torch.from_numpy(x[n]).to(device) for n in ("block_table", "seq_lens", "q_offsets")}
     pos = torch.from_numpy(x["positions"]).to(device) if x["positions"] is not None else None
     nq_s = np.diff(x["q_offsets"])
     max_q = int(nq_s.max()) if len(nq_s) else 0
-    out = torch.empty_like(q)
+    out = torch.empty_like(t[0])
     stream = torch.cuda.current_stream(device)
 
     def step():
-        attn.paged_fwd(q, kc, vc, ints["block_table"], ints["seq_lens"], ints["q_offsets"], positions=pos,
-                       causal=w.causal, scale=x["scale"], max_queries=max_q, out=out, stream=stream)
+        call = attn.paged_mla if is_mla else attn.paged_fwd
+        call(*t, ints["block_table"], ints["seq_lens"], ints["q_offsets"], positions=pos, causal=w.causal,
+             scale=x["scale"], max_queries=max_q, out=out, stream=stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -464,9 +467,14 @@ def bench_paged(args):
         pq = (x["positions"][x["q_offsets"][s_]:x["q_offsets"][s_ + 1]] if x["positions"] is not None
               else np.arange(L - n, L))
         pairs += int(np.minimum(L, np.asarray(pq, dtype=np.int64) + 1).clip(min=0).sum()) if w.causal else n * int(L)
-    flops = 4.0 * w.D * w.Hq * pairs
     es = {"f32": 4, "f16": 2, "bf16": 2}[w.dtype]
-    nbytes = (2 * int(x["seq_lens"].sum()) * w.Hkv * w.D + 2 * int(x["q_offsets"][-1]) * w.Hq * w.D) * es
+    nqt, nkt = int(x["q_offsets"][-1]), int(x["seq_lens"].sum())
+    if is_mla:  # 2(R + Pd) for the score, 2R for the latent sum, per pair and head
+        flops = (2.0 * (w.R + w.Pd) + 2.0 * w.R) * w.H * pairs
+        nbytes = (nkt * (w.R + w.Pd) + nqt * w.H * (2 * w.R + w.Pd)) * es
+    else:
+        flops = 4.0 * w.D * w.Hq * pairs
+        nbytes = (2 * nkt * w.Hkv * w.D + 2 * nqt * w.Hq * w.D) * es
     value = world * flops / (ms * 1e-3) / 1e12
     if rank != 0:
         return
@@ -480,16 +488,18 @@ def bench_paged(args):
              "frac": gbs / float(peaks["hbm_gbs"]), "peak_kind": f"{peak_kind} HBM copy"} if hbm_bound else
             {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
              "peak_kind": f"fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x {mhz:.0f} MHz"})
-    roof.update({"traffic": None, "kernel": "paged_fwd_kernel", "algorithmic_bytes": nbytes})
+    roof.update({"traffic": None, "kernel": "mla_fwd_kernel" if is_mla else "paged_fwd_kernel",
+                 "algorithmic_bytes": nbytes})
+    heads = {"H": w.H, "R": w.R, "Pd": w.Pd} if is_mla else {"Hq": w.Hq, "Hkv": w.Hkv, "D": w.D}
     line = {
-        "metric": f"paged attention TFLOP/s ({w.name})", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "metric": f"{'MLA' if is_mla else 'paged attention'} TFLOP/s ({w.name})", "value": value, "unit": "TFLOP/s",
+        "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "num_seqs": w.num_seqs, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-                   "page_size": w.page_size, "ctx_range": list(w.ctx_range), "q_range": list(w.q_range),
+        "config": {"workload": w.name, "num_seqs": w.num_seqs, **heads, "page_size": w.page_size, "ctx_range": list(w.ctx_range), "q_range": list(w.q_range),
                    "queries": int(x["q_offsets"][-1]), "keys": int(x["seq_lens"].sum()),
-                   "parallelism": f"replicas x{world}", "flops_basis": "exact: 4*D per visible (query, key) pair",
-                   "l2": f"K/V {2 * int(x['seq_lens'].sum()) * w.Hkv * w.D * es / 2**20:.0f} MiB per step"},
+                   "parallelism": f"replicas x{world}", "flops_basis": "exact: per visible (query, key) pair and head",
+                   "l2": f"cache read {nbytes / 2**20:.0f} MiB per step"},
         "roofline": roof, "hbm_gbs_algorithmic": gbs, "e2e": None,
         "gpu_launches": args.steps, "clocks": clocks.summary(),
     }
@@ -504,17 +514,19 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS) + sorted(synth.PAGED_WORKLOADS))
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=sorted(synth.WORKLOADS) + sorted(synth.PAGED_WORKLOADS) + sorted(synth.MLA_WORKLOADS))
     ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"],
                     help="time the forward (default) or the backward (attn_bwd) of the workload")
     ap.add_argument("--splits", type=int, default=0,
                     help="key-range splits (attn_fwd_split); 0 = the workload's default")
     args = ap.parse_args()
-    if args.impl == "reference" and args.workload in synth.PAGED_WORKLOADS:
+    paged = args.workload in synth.PAGED_WORKLOADS or args.workload in synth.MLA_WORKLOADS
+    if args.impl == "reference" and paged:
         print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the dense workloads"}))
     elif args.impl == "reference":
         bench_reference(args)
-    elif args.workload in synth.PAGED_WORKLOADS:
+    elif paged:
         bench_paged(args)
     else:
         bench_gpu(args)

@@ -283,3 +283,9 @@ PAGED_WORKLOADS = {
     "bf16_paged_prefill": PagedWorkload("bf16_paged_prefill", BF16, 16, 32, 8, 128, 64, (512, 4096),
                                         (128, 512), seed=21),
 }
+
+
+MLA_WORKLOADS = {
+    # MLA decode step: 128 heads over a 512-rank latent (+64 positional) cache, 1k-8k tokens
+    "bf16_mla_decode": MlaWorkload("bf16_mla_decode", BF16, 64, 128, 512, 64, 64, (1024, 8192), (1, 1), seed=30),
+}
