@@ -140,10 +140,194 @@ __global__ void __launch_bounds__(THREADS) paged_fwd_kernel(const void* __restri
     lse[static_cast<size_t>(t) * pp.Hq + h] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
 }
 
+// Decode-shaped calls (at most RMAX rows = queries x group heads per
+// (sequence, kv head)): one CTA of 4 warps per (sequence, kv head). Each lane
+// owns one key of a 32-key chunk and computes its scores against every row
+// (queries in shared memory, broadcast reads); each row keeps an online
+// softmax per warp (warp max and sum by shuffles); P V then runs with lanes
+// over dimensions, the probabilities shuffled out key by key and the value
+// rows read coalesced, VB rows per batch of independent loads. The warps take
+// interleaved chunks and are combined
+// through shared memory at the end. Bandwidth-bound: every key row is read
+// once for all the heads of its group.
+constexpr int RMAX = 8;
+constexpr int DEC_WARPS = 8;
+constexpr int VB = 8;  // value rows loaded together in P V
+
+template <int D, int DT>
+__global__ void __launch_bounds__(DEC_WARPS * 32) paged_decode_kernel(const void* __restrict__ q,
+                                                                      const void* __restrict__ kc,
+                                                                      const void* __restrict__ vc,
+                                                                      void* __restrict__ out,
+                                                                      float* __restrict__ lse,
+                                                                      const PagedParams pp) {
+  constexpr int G = D / 4;             // float4 groups of a row
+  constexpr int LG = (G + 31) / 32;    // float4 groups of a row per lane in P V
+  __shared__ float4 qs[RMAX][G];
+  __shared__ float sm_m[DEC_WARPS][RMAX], sm_l[DEC_WARPS][RMAX];
+  __shared__ float4 sm_acc[DEC_WARPS][RMAX][G];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.x / pp.Hkv, hk = blockIdx.x - s * pp.Hkv;
+  const int group = pp.Hq / pp.Hkv;
+  const int q_lo = min(max(__ldg(pp.q_offsets + s), 0), pp.num_queries);
+  const int q_hi = min(max(__ldg(pp.q_offsets + s + 1), q_lo), pp.num_queries);
+  const int nq = q_hi - q_lo;
+  // rows of this CTA: <= RMAX when max_queries bounds every sequence, as the
+  // call requires; clamped so that a wrong bound cannot index past RMAX
+  const int R = min(nq * group, RMAX);
+  if (R <= 0) return;
+  const int L = min(max(__ldg(pp.seq_lens + s), 0), pp.max_pages * pp.page_size);
+  // rows' positions and the CTA's key range
+  int pos[RMAX];
+  int key_hi = 0;
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r) {
+    const int tq = r / group;
+    pos[r] = r < R ? (pp.positions ? __ldg(pp.positions + q_lo + tq) : L - nq + tq) : -1;
+    if (r < R) key_hi = max(key_hi, pp.causal ? min(L, pos[r] + 1) : L);
+  }
+  for (int e = threadIdx.x; e < RMAX * G; e += DEC_WARPS * 32) {
+    const int r = e / G, c = e - (e / G) * G;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < R) {
+      const int t = q_lo + r / group, h = hk * group + r % group;
+      v = load4<DT>(q, (static_cast<size_t>(t) * pp.Hq + h) * G + c);
+    }
+    qs[r][c] = v;
+  }
+  __syncthreads();
+
+  const int32_t* table = pp.block_table + static_cast<size_t>(s) * pp.max_pages;
+  float m_w[RMAX], l_w[RMAX];
+  float4 acc[RMAX][LG];
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r) {
+    m_w[r] = -INFINITY;
+    l_w[r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < LG; ++i) acc[r][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int nchunks = (key_hi + 31) / 32;
+  for (int c = warp; c < nchunks; c += DEC_WARPS) {
+    const int j = c * 32 + lane;
+    const bool in = j < key_hi;
+    int page = in ? __ldg(table + j / pp.page_size) : -1;
+    const bool ok = in && page >= 0 && page < pp.num_pages;
+    const size_t krow = ok ? ((static_cast<size_t>(page) * pp.page_size + j % pp.page_size) * pp.Hkv + hk) * G : 0;
+    // scores of this lane's key against every row
+    float sc[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) sc[r] = 0.f;
+    if (ok) {
+#pragma unroll 8
+      for (int g = 0; g < G; ++g) {
+        const float4 kf = load4<DT>(kc, krow + g);
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) sc[r] = dot4(qs[r][g], kf, sc[r]);
+      }
+    }
+    float p[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      const bool vis = in && r < R && (!pp.causal || j <= pos[r]);
+      float x = vis ? sc[r] * pp.scale_log2 : -INFINITY;
+      float mx = x;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m_new = fmaxf(m_w[r], mx);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = fast_exp2(m_w[r] - m_use);
+      p[r] = fast_exp2(x - m_use);
+      float sum = p[r];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      l_w[r] = l_w[r] * alpha + sum;
+      m_w[r] = m_new;
+#pragma unroll
+      for (int i = 0; i < LG; ++i) {
+        acc[r][i].x *= alpha; acc[r][i].y *= alpha; acc[r][i].z *= alpha; acc[r][i].w *= alpha;
+      }
+    }
+    // P V: lanes over dimensions, VB keys per batch (loads first, then FMAs)
+    const int kmax = min(32, key_hi - c * 32);
+    for (int k0 = 0; k0 < kmax; k0 += VB) {
+      float4 vv[VB][LG];
+#pragma unroll
+      for (int b = 0; b < VB; ++b) {
+        const int k = k0 + b;
+        const int pg = __shfl_sync(0xffffffffu, page, k & 31);
+        const bool use = k < kmax && pg >= 0 && pg < pp.num_pages;  // warp-uniform
+        const int jk = c * 32 + k;
+        const size_t vrow = use ? ((static_cast<size_t>(pg) * pp.page_size + jk % pp.page_size) * pp.Hkv + hk) * G : 0;
+#pragma unroll
+        for (int i = 0; i < LG; ++i) {
+          const int g = lane + 32 * i;
+          vv[b][i] = (use && g < G) ? load4<DT>(vc, vrow + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < VB; ++b) {
+        const int k = (k0 + b) & 31;
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+          const float pk = __shfl_sync(0xffffffffu, p[r], k);  // 0 for a key past kmax (masked)
+#pragma unroll
+          for (int i = 0; i < LG; ++i) acc[r][i] = axpy4(pk, vv[b][i], acc[r][i]);
+        }
+      }
+    }
+  }
+  // combine the warps
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r) {
+    if (lane == 0) {
+      sm_m[warp][r] = m_w[r];
+      sm_l[warp][r] = l_w[r];
+    }
+#pragma unroll
+    for (int i = 0; i < LG; ++i)
+      if (lane + 32 * i < G) sm_acc[warp][r][lane + 32 * i] = acc[r][i];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < R * G; e += DEC_WARPS * 32) {
+    const int r = e / G, g = e - (e / G) * G;
+    float M = -INFINITY;
+#pragma unroll
+    for (int wv = 0; wv < DEC_WARPS; ++wv) M = fmaxf(M, sm_m[wv][r]);
+    float Ls = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int wv = 0; wv < DEC_WARPS; ++wv) {
+        const float f = fast_exp2(sm_m[wv][r] - M);  // 0 for a warp that saw no key
+        Ls = fmaf(f, sm_l[wv][r], Ls);
+        o = axpy4(f, sm_acc[wv][r][g], o);
+      }
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : __int_as_float(0x7fc00000);
+    const int t = q_lo + r / group, h = hk * group + r % group;
+    const size_t row = static_cast<size_t>(t) * pp.Hq + h;
+    store4<DT>(out, row * G + g, make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv));
+    if (lse && g == 0) lse[row] = Ls > 0.f ? (M + log2f(Ls)) * LN2 : -INFINITY;
+  }
+}
+
 template <int DT>
 static cudaError_t launch_dt(int D, const PagedParams& pp, const void* q, const void* k, const void* v,
                              void* out, float* lse, cudaStream_t st, int* unsupported) {
   const int group = pp.Hq / pp.Hkv;
+  if (static_cast<int64_t>(pp.max_queries) * group <= RMAX) {  // decode-shaped: a CTA per (sequence, kv head)
+    const dim3 grid(static_cast<unsigned>(pp.num_seqs) * pp.Hkv);
+    switch (D) {
+      case 16: paged_decode_kernel<16, DT><<<grid, DEC_WARPS * 32, 0, st>>>(q, k, v, out, lse, pp); break;
+      case 32: paged_decode_kernel<32, DT><<<grid, DEC_WARPS * 32, 0, st>>>(q, k, v, out, lse, pp); break;
+      case 64: paged_decode_kernel<64, DT><<<grid, DEC_WARPS * 32, 0, st>>>(q, k, v, out, lse, pp); break;
+      case 128: paged_decode_kernel<128, DT><<<grid, DEC_WARPS * 32, 0, st>>>(q, k, v, out, lse, pp); break;
+      default: *unsupported = 1; return cudaSuccess;
+    }
+    return cudaGetLastError();
+  }
   const int64_t ry = (static_cast<int64_t>(pp.max_queries) * group + ROWS - 1) / ROWS;
   const dim3 grid(static_cast<unsigned>(pp.num_seqs) * pp.Hkv, static_cast<unsigned>(ry > 0 ? ry : 1));
   switch (D) {
