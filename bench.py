@@ -37,6 +37,8 @@ METRIC = "attention fwd TFLOP/s and % of GB300 BF16 peak (causal, S=4096, D=128)
 KERNEL_NAME = "attn_fwd_tc_kernel"
 # key-range splits per workload (1 when absent): enough CTAs for 152 SMs
 SPLITS = {"bf16_gqa_chunk_32k": 4}
+# key-range splits of paged decode: ~1k keys per split for 1k-8k contexts
+PAGED_SPLITS = {"bf16_paged_decode": 8}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -429,11 +431,18 @@ def bench_paged(args):
     max_q = int(nq_s.max()) if len(nq_s) else 0
     out = torch.empty_like(t[0])
     stream = torch.cuda.current_stream(device)
+    pws = None
+    if not is_mla:
+        shp = attn.PagedShape(w.num_seqs, int(x["q_offsets"][-1]), w.Hq, w.Hkv, w.D, w.page_size,
+                              int(x["k_cache"].shape[0]), int(x["block_table"].shape[1]), max_q)
+        need = attn.paged_workspace_bytes(shp, PAGED_SPLITS.get(w.name, 1))
+        pws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
 
     def step():
         call = attn.paged_mla if is_mla else attn.paged_fwd
+        extra = {} if is_mla else {"num_splits": PAGED_SPLITS.get(w.name, 1), "workspace": pws}
         call(*t, ints["block_table"], ints["seq_lens"], ints["q_offsets"], positions=pos, causal=w.causal,
-             scale=x["scale"], max_queries=max_q, out=out, stream=stream)
+             scale=x["scale"], max_queries=max_q, out=out, stream=stream, **extra)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -499,6 +508,7 @@ def bench_paged(args):
         "config": {"workload": w.name, "num_seqs": w.num_seqs, **heads, "page_size": w.page_size, "ctx_range": list(w.ctx_range), "q_range": list(w.q_range),
                    "queries": int(x["q_offsets"][-1]), "keys": int(x["seq_lens"].sum()),
                    "parallelism": f"replicas x{world}", "flops_basis": "exact: per visible (query, key) pair and head",
+                   "num_splits": 1 if is_mla else PAGED_SPLITS.get(w.name, 1),
                    "l2": f"cache read {nbytes / 2**20:.0f} MiB per step"},
         "roofline": roof, "hbm_gbs_algorithmic": gbs, "e2e": None,
         "gpu_launches": args.steps, "clocks": clocks.summary(),

@@ -79,7 +79,10 @@ def load_library():
         lib.attn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_bwd_workspace_bytes.restype = ctypes.c_int
         lib.attn_paged_fwd.argtypes = [ctypes.POINTER(PagedShape), vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
-                                       ctypes.c_float, ctypes.c_int, vp, vp, vp]
+                                       ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp, vp, vp]
+        lib.attn_paged_workspace_bytes.argtypes = [ctypes.POINTER(PagedShape), ctypes.c_int,
+                                                   ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_paged_workspace_bytes.restype = ctypes.c_int
         lib.attn_paged_fwd.restype = ctypes.c_int
         lib.attn_paged_mla.argtypes = [ctypes.POINTER(MlaShape), vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                        ctypes.c_float, ctypes.c_int, vp, vp, vp]
@@ -322,9 +325,16 @@ def bwd(q, k, v, out, dout, lse, *, causal: bool = False, kv_lens=None, bias=Non
     return dq, dk, dv
 
 
+def paged_workspace_bytes(shape: PagedShape, num_splits: int) -> int:
+    """Workspace bytes attn_paged_fwd needs for ``shape`` and ``num_splits``."""
+    n = ctypes.c_size_t(0)
+    check(load_library().attn_paged_workspace_bytes(ctypes.byref(shape), int(num_splits), ctypes.byref(n)))
+    return n.value
+
+
 def paged_fwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, *, positions=None, causal: bool = True,
               scale: float | None = None, max_queries: int | None = None, return_lse: bool = False, out=None,
-              stream=None):
+              stream=None, num_splits: int = 1, workspace=None):
     """Attention of packed queries over a paged key/value cache (attn_paged_fwd).
 
     q [queries, Hq, D]; k_cache, v_cache [pages, page_size, Hkv, D] (same
@@ -332,6 +342,8 @@ def paged_fwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, *, position
     seq_lens int32 [num_seqs]; q_offsets int32 [num_seqs + 1]; positions
     int32 [queries] or None. ``max_queries`` bounds the queries of one
     sequence (computed from q_offsets, with a host sync, when None).
+    ``num_splits`` splits the keys of decode-shaped calls (workspace taken
+    from ``workspace``, a CUDA uint8 tensor, or allocated here).
     Returns out [queries, Hq, D] (and lse float32 [queries, Hq]).
     """
     import torch
@@ -369,10 +381,17 @@ def paged_fwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, *, position
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     shape = PagedShape(ns, nq, Hq, Hkv, D, P, pages, int(block_table.shape[1]), int(max_queries))
+    need = paged_workspace_bytes(shape, num_splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    elif need and (workspace.device != dev or workspace.numel() * workspace.element_size() < need):
+        raise AttnError(f"workspace must hold {need} bytes on q's device")
     ptr = lambda t: (t.data_ptr() or None) if t is not None else None
     check(load_library().attn_paged_fwd(ctypes.byref(shape), ptr(q), ptr(k_cache), ptr(v_cache), ptr(block_table),
                                         ptr(seq_lens), ptr(q_offsets), ptr(positions), int(bool(causal)),
-                                        float(scale), _dtype_code(q), ptr(out), ptr(lse), stream.cuda_stream or None))
+                                        float(scale), _dtype_code(q), int(num_splits),
+                                        ptr(workspace) if need else None, need, ptr(out), ptr(lse),
+                                        stream.cuda_stream or None))
     return (out, lse) if return_lse else out
 
 

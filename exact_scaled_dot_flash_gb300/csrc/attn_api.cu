@@ -467,10 +467,22 @@ int attn_bwd(const attn_shape_t* shape, const void* q, const void* k, const void
 // ---------------------------------------------------------------- paged cache
 extern "C" {
 
+int attn_paged_workspace_bytes(const attn_paged_shape_t* shape, int num_splits, size_t* bytes) {
+  if (!shape || !bytes) return ATTN_ERR_NULL;
+  const attn_paged_shape_t s = *shape;
+  if (s.num_queries < 0 || s.Hq <= 0 || s.Hkv <= 0 || s.D <= 0 || s.max_queries < 0) return ATTN_ERR_SHAPE;
+  if (num_splits < 1 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
+  const bool dec = attn::paged_is_decode(s.max_queries, s.Hq / s.Hkv);
+  attn_shape_t rows{1, 1, 1, s.num_queries * s.Hq, 0, s.D, 1, 1};
+  *bytes = (dec && num_splits > 1) ? static_cast<size_t>(split_layout(rows, num_splits).total) : 0;
+  return ATTN_OK;
+}
+
 int attn_paged_fwd(const attn_paged_shape_t* shape, const void* q, const void* k_cache,
                    const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
                    const int32_t* q_offsets, const int32_t* positions, int causal, float scale,
-                   attn_dtype_t dtype, void* out, float* lse, void* stream) {
+                   attn_dtype_t dtype, int num_splits, void* workspace, size_t workspace_bytes,
+                   void* out, float* lse, void* stream) {
   if (!shape) return ATTN_ERR_NULL;
   const attn_paged_shape_t s = *shape;
   if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
@@ -480,7 +492,12 @@ int attn_paged_fwd(const attn_paged_shape_t* shape, const void* q, const void* k
   if (causal != 0 && causal != 1) return ATTN_ERR_MASK;
   if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_SCALE;
   if (!(s.D == 16 || s.D == 32 || s.D == 64 || s.D == 128)) return ATTN_ERR_HEAD_DIM;
+  if (num_splits < 1 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
   const int64_t group = s.Hq / s.Hkv;
+  // splits apply to decode-shaped calls (the only kernel that splits)
+  const int splits = attn::paged_is_decode(s.max_queries, static_cast<int>(group)) ? num_splits : 1;
+  attn_shape_t rows_shape{1, 1, 1, s.num_queries * s.Hq, 0, s.D, 1, 1};
+  const SplitLayout lay = split_layout(rows_shape, splits);
   if (static_cast<int64_t>(s.num_seqs) * s.Hkv > 0x7fffffffLL ||
       (static_cast<int64_t>(s.max_queries) * group + 63) / 64 > 65535 ||
       static_cast<int64_t>(s.max_pages) * s.page_size > 0x7fffffffLL)
@@ -508,11 +525,22 @@ int attn_paged_fwd(const attn_paged_shape_t* shape, const void* q, const void* k
   for (const Buf& b : ins)
     if (overlaps(out, q_bytes, b.p, b.n) || overlaps(lse, lse_bytes, b.p, b.n)) return ATTN_ERR_OVERLAP;
   if (overlaps(out, q_bytes, lse, lse_bytes)) return ATTN_ERR_OVERLAP;
+  if (splits > 1) {
+    if (!workspace || workspace_bytes < static_cast<size_t>(lay.total)) return ATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+    for (const Buf& b : ins)
+      if (overlaps(workspace, lay.total, b.p, b.n)) return ATTN_ERR_OVERLAP;
+    if (overlaps(workspace, lay.total, out, q_bytes) || overlaps(workspace, lay.total, lse, lse_bytes))
+      return ATTN_ERR_OVERLAP;
+  }
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e);
   attn::PagedParams pp{};
+  pp.num_splits = splits;
+  pp.ws_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  pp.ws_ml = splits > 1 ? reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + lay.ml_offset) : nullptr;
   pp.num_seqs = s.num_seqs;
   pp.num_queries = s.num_queries;
   pp.Hq = s.Hq;
@@ -533,6 +561,17 @@ int attn_paged_fwd(const attn_paged_shape_t* shape, const void* q, const void* k
   e = attn::launch_paged_simt(s.D, static_cast<int>(dtype), pp, q, k_cache, v_cache, out, lse,
                               static_cast<cudaStream_t>(stream), &unsupported);
   if (unsupported) return ATTN_ERR_HEAD_DIM;
+  if (e == cudaSuccess && splits > 1) {  // merge the partials of rows r = query * Hq + head
+    attn::KernelParams mp{};
+    mp.B = 1;
+    mp.Hq = 1;
+    mp.Sq = s.num_queries * s.Hq;
+    mp.num_splits = splits;
+    mp.ws_o = pp.ws_o;
+    mp.ws_ml = pp.ws_ml;
+    mp.lse = lse;
+    e = attn::launch_split_merge(mp, s.D, static_cast<int>(dtype), out, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
 }
 

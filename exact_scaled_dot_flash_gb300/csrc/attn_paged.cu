@@ -141,15 +141,17 @@ __global__ void __launch_bounds__(THREADS) paged_fwd_kernel(const void* __restri
 }
 
 // Decode-shaped calls (at most RMAX rows = queries x group heads per
-// (sequence, kv head)): one CTA of 4 warps per (sequence, kv head). Each lane
+// (sequence, kv head)): one CTA of DEC_WARPS warps per (sequence, kv head,
+// split). Each lane
 // owns one key of a 32-key chunk and computes its scores against every row
 // (queries in shared memory, broadcast reads); each row keeps an online
 // softmax per warp (warp max and sum by shuffles); P V then runs with lanes
 // over dimensions, the probabilities shuffled out key by key and the value
 // rows read coalesced, VB rows per batch of independent loads. The warps take
-// interleaved chunks and are combined
-// through shared memory at the end. Bandwidth-bound: every key row is read
-// once for all the heads of its group.
+// interleaved chunks and are combined through shared memory at the end.
+// Bandwidth-bound: every key row is read once for all the heads of its group.
+// With num_splits > 1, CTA (., z) takes the z-th balanced run of 32-key
+// chunks and writes its unnormalised partial (m, l, O) for launch_split_merge.
 constexpr int RMAX = 8;
 constexpr int DEC_WARPS = 8;
 constexpr int VB = 8;  // value rows loaded together in P V
@@ -209,7 +211,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) paged_decode_kernel(const void
     for (int i = 0; i < LG; ++i) acc[r][i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const int nchunks = (key_hi + 31) / 32;
-  for (int c = warp; c < nchunks; c += DEC_WARPS) {
+  const int c_lo = static_cast<int>(static_cast<int64_t>(blockIdx.y) * nchunks / pp.num_splits);
+  const int c_hi = static_cast<int>(static_cast<int64_t>(blockIdx.y + 1) * nchunks / pp.num_splits);
+  for (int c = c_lo + warp; c < c_hi; c += DEC_WARPS) {
     const int j = c * 32 + lane;
     const bool in = j < key_hi;
     int page = in ? __ldg(table + j / pp.page_size) : -1;
@@ -305,9 +309,15 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) paged_decode_kernel(const void
         o = axpy4(f, sm_acc[wv][r][g], o);
       }
     }
-    const float inv = Ls > 0.f ? 1.f / Ls : __int_as_float(0x7fc00000);
     const int t = q_lo + r / group, h = hk * group + r % group;
     const size_t row = static_cast<size_t>(t) * pp.Hq + h;
+    if (pp.num_splits > 1) {  // partial of this split, relative to 2^M
+      const size_t rr = static_cast<size_t>(blockIdx.y) * pp.num_queries * pp.Hq + row;
+      reinterpret_cast<float4*>(pp.ws_o)[rr * G + g] = o;
+      if (g == 0) pp.ws_ml[rr] = make_float2(M, Ls);
+      continue;
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : __int_as_float(0x7fc00000);
     store4<DT>(out, row * G + g, make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv));
     if (lse && g == 0) lse[row] = Ls > 0.f ? (M + log2f(Ls)) * LN2 : -INFINITY;
   }
@@ -317,8 +327,8 @@ template <int DT>
 static cudaError_t launch_dt(int D, const PagedParams& pp, const void* q, const void* k, const void* v,
                              void* out, float* lse, cudaStream_t st, int* unsupported) {
   const int group = pp.Hq / pp.Hkv;
-  if (static_cast<int64_t>(pp.max_queries) * group <= RMAX) {  // decode-shaped: a CTA per (sequence, kv head)
-    const dim3 grid(static_cast<unsigned>(pp.num_seqs) * pp.Hkv);
+  if (paged_is_decode(pp.max_queries, group)) {  // a CTA per (sequence, kv head, split)
+    const dim3 grid(static_cast<unsigned>(pp.num_seqs) * pp.Hkv, static_cast<unsigned>(pp.num_splits));
     switch (D) {
       case 16: paged_decode_kernel<16, DT><<<grid, DEC_WARPS * 32, 0, st>>>(q, k, v, out, lse, pp); break;
       case 32: paged_decode_kernel<32, DT><<<grid, DEC_WARPS * 32, 0, st>>>(q, k, v, out, lse, pp); break;

@@ -87,7 +87,14 @@ struct PagedParams {
   float scale_log2;
   int* status;
   int device;
+  // decode-shaped calls only: key-range splits, each writing an unnormalised
+  // partial (rows r = query * Hq + head) that launch_split_merge combines
+  int num_splits;
+  float* ws_o;    // [num_splits, num_queries * Hq, D]
+  float2* ws_ml;  // [num_splits, num_queries * Hq] (m in log2 units, l)
 };
+// True when attn_paged_fwd takes the decode kernel (the only one that splits).
+inline bool paged_is_decode(int max_queries, int group) { return static_cast<long long>(max_queries) * group <= 8; }
 // MLA over a paged latent cache (PagedParams with Hq = heads, Hkv = 1).
 cudaError_t launch_mla_simt(int R, int Pd, int dtype, const PagedParams& pp, const void* q, const void* qp,
                             const void* lat, const void* kp, void* out, float* lse, cudaStream_t stream,

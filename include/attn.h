@@ -243,6 +243,14 @@ typedef struct {
  * sees no key is NaN (lse -inf). lse: NULL or float [num_queries, Hq] natural
  * log-sum-exp.
  *
+ * num_splits (1..ATTN_MAX_SPLITS) cuts the keys of every (sequence, kv head)
+ * of a decode-shaped call (max_queries * Hq/Hkv <= 8) into that many runs,
+ * one CTA each, merged afterwards from FP32 partial statistics (the split of
+ * attn_fwd_split); it needs a 16-byte-aligned workspace of
+ * attn_paged_workspace_bytes(shape, num_splits) bytes, disjoint from every
+ * other buffer; other calls ignore num_splits and the workspace. With splits,
+ * a query row outside every sequence range gets unspecified values.
+ *
  * All pointers are device pointers: q, k_cache, v_cache, out 16-byte aligned;
  * the int32 arrays and lse 4-byte aligned; out and lse disjoint from every
  * input. Page-table entries outside [0, num_pages) read as zero keys and
@@ -254,8 +262,14 @@ ATTN_API int attn_paged_fwd(const attn_paged_shape_t* shape,
                             const int32_t* block_table, const int32_t* seq_lens,
                             const int32_t* q_offsets, const int32_t* positions,
                             int causal, float scale, attn_dtype_t dtype,
+                            int num_splits, void* workspace, size_t workspace_bytes,
                             void* out, float* lse,
                             void* stream);
+
+/* attn_paged_workspace_bytes - workspace attn_paged_fwd needs for `shape` and
+ * `num_splits` (0 when the call does not split). Returns ATTN_OK,
+ * ATTN_ERR_NULL, ATTN_ERR_SHAPE or ATTN_ERR_SPLITS. */
+ATTN_API int attn_paged_workspace_bytes(const attn_paged_shape_t* shape, int num_splits, size_t* bytes);
 
 /* Shape of an MLA call: q [num_queries, H, R], qp [num_queries, H, Pd],
  * latent [num_pages, page_size, 1, R], kpos [num_pages, page_size, 1, Pd],

@@ -27,7 +27,7 @@ def _clean_status():
     assert attn.device_status(torch.cuda.current_device(), clear=True) == 0, "a kernel wait timed out"
 
 
-def run_paged(w, x):
+def run_paged(w, x, num_splits=1):
     import torch
     from exact_scaled_dot_flash_gb300 import attn
     q, k, v = (to_device(x[n], w.dtype) for n in ("q", "k_cache", "v_cache"))
@@ -35,13 +35,13 @@ def run_paged(w, x):
     pos = to_device(x["positions"], "i32") if x["positions"] is not None else None
     out = torch.full_like(q, 777.0)  # sentinel: a row the kernel skips cannot pass
     o, lse = attn.paged_fwd(q, k, v, ints["block_table"], ints["seq_lens"], ints["q_offsets"], positions=pos,
-                            causal=w.causal, scale=x["scale"], return_lse=True, out=out)
+                            causal=w.causal, scale=x["scale"], return_lse=True, out=out, num_splits=num_splits)
     return to_f64(o), lse.cpu().numpy().astype(np.float64)
 
 
-def check(w, x=None):
+def check(w, x=None, num_splits=1):
     x = x if x is not None else synth.make_paged_inputs(w)
-    got, lse = run_paged(w, x)
+    got, lse = run_paged(w, x, num_splits)
     ref, ref_lse = oracle.paged_attention(x["q"], x["k_cache"], x["v_cache"], x["block_table"], x["seq_lens"],
                                           x["q_offsets"], positions=x["positions"], causal=w.causal,
                                           scale=x["scale"], dtype=w.dtype, lse=True)
@@ -124,7 +124,7 @@ def test_paged_argument_errors():
         shape = shape or attn.PagedShape(1, 4, 2, 2, 64, 16, 3, 3, 4)
         return lib.attn_paged_fwd(ctypes.byref(shape), q.data_ptr(), kc.data_ptr(), kc.data_ptr(), tab.data_ptr(),
                                   lens.data_ptr(), offs.data_ptr(), None, causal, ctypes.c_float(scale),
-                                  attn.ATTN_BF16, o.data_ptr(), None, None)
+                                  attn.ATTN_BF16, 1, None, 0, o.data_ptr(), None, None)
     assert call() == 0
     torch.cuda.synchronize()
     assert call(shape=attn.PagedShape(1, 4, 3, 2, 64, 16, 3, 3, 4)) == -2   # Hq % Hkv
@@ -132,3 +132,25 @@ def test_paged_argument_errors():
     assert call(causal=2) == -7
     assert call(scale=0.0) == -6
     assert call(o=q) == -8                                                  # out overlaps q
+
+
+@pytest.mark.parametrize("splits", [2, 5, 32])
+def test_paged_decode_splits(splits):
+    # decode-shaped calls with the key range split and merged (every length
+    # case: fewer chunks than splits, a sequence without keys, explicit positions)
+    w = PW(f"paged_decode_split{splits}", "bf16", 7, 8, 2, 128, 32, (0, 2000), (1, 2), seed=30 + splits,
+           explicit_positions=True)
+    check(w, num_splits=splits)
+    w2 = PW(f"paged_decode_split{splits}_f32", "f32", 5, 4, 4, 64, 16, (1, 700), (1, 1), seed=40 + splits)
+    check(w2, num_splits=splits)
+
+
+def test_paged_split_workspace_errors():
+    from exact_scaled_dot_flash_gb300 import attn
+    decode = attn.PagedShape(4, 4, 8, 2, 128, 16, 10, 5, 1)   # 1 query x group 4 <= 8 rows: decode kernel
+    prefill = attn.PagedShape(4, 40, 8, 2, 128, 16, 10, 5, 10)
+    assert attn.paged_workspace_bytes(decode, 1) == 0
+    assert attn.paged_workspace_bytes(decode, 4) > 0
+    assert attn.paged_workspace_bytes(prefill, 4) == 0       # the prefill kernel does not split
+    with pytest.raises(attn.AttnError):
+        attn.paged_workspace_bytes(decode, 33)
