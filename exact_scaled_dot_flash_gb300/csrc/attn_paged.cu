@@ -223,12 +223,13 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) paged_decode_kernel(const void
     float sc[RMAX];
 #pragma unroll
     for (int r = 0; r < RMAX; ++r) sc[r] = 0.f;
-    if (ok) {
-#pragma unroll 8
-      for (int g = 0; g < G; ++g) {
-        const float4 kf = load4<DT>(kc, krow + g);
+    if (ok) {  // the lane's key row, 8 values per load
+#pragma unroll 4
+      for (int g2 = 0; g2 < G / 2; ++g2) {
+        float4 k0, k1;
+        simt::load8<DT>(kc, krow / 2 + g2, k0, k1);
 #pragma unroll
-        for (int r = 0; r < RMAX; ++r) sc[r] = dot4(qs[r][g], kf, sc[r]);
+        for (int r = 0; r < RMAX; ++r) sc[r] = dot4(qs[r][2 * g2 + 1], k1, dot4(qs[r][2 * g2], k0, sc[r]));
       }
     }
     float p[RMAX];

@@ -29,6 +29,32 @@ __device__ __forceinline__ float4 load4(const void* base, size_t idx4) {
   }
 }
 
+// 8 consecutive elements (float4 pair idx8 of the array) with one 16-byte
+// load for 16-bit types (two for F32).
+template <int DT>
+__device__ __forceinline__ void load8(const void* base, size_t idx8, float4& lo, float4& hi) {
+  if constexpr (DT == 0) {
+    lo = __ldg(reinterpret_cast<const float4*>(base) + 2 * idx8);
+    hi = __ldg(reinterpret_cast<const float4*>(base) + 2 * idx8 + 1);
+  } else {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(base) + idx8);
+    float2 a, b, c, d;
+    if constexpr (DT == 1) {
+      a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+      b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+      c = __half22float2(*reinterpret_cast<const __half2*>(&u.z));
+      d = __half22float2(*reinterpret_cast<const __half2*>(&u.w));
+    } else {
+      a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+      b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+      c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.z));
+      d = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.w));
+    }
+    lo = make_float4(a.x, a.y, b.x, b.y);
+    hi = make_float4(c.x, c.y, d.x, d.y);
+  }
+}
+
 template <int DT>
 __device__ __forceinline__ void store4(void* base, size_t idx4, float4 v) {
   if constexpr (DT == 0) {
