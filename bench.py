@@ -492,13 +492,25 @@ def bench_paged(args):
     mhz = (clocks.summary() or {}).get("sm_mhz") or 2070.0
     alu_peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
     tf = flops / (ms * 1e-3) / 1e12
-    hbm_bound = flops / nbytes < alu_peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
-    roof = ({"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
-             "frac": gbs / float(peaks["hbm_gbs"]), "peak_kind": f"{peak_kind} HBM copy"} if hbm_bound else
-            {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
-             "peak_kind": f"fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x {mhz:.0f} MHz"})
-    roof.update({"traffic": None, "kernel": "mla_fwd_kernel" if is_mla else "paged_fwd_kernel",
-                 "algorithmic_bytes": nbytes})
+    # the path the library takes: decode-shaped paged calls (<= 8 rows per
+    # sequence and kv head) stream the cache (HBM roofline); prefill-shaped
+    # F16/BF16 paged calls with D in {64, 128} run on the tensor cores; the
+    # rest (MLA) on the fp32 FMA pipes
+    decode = (not is_mla) and max_q * (w.Hq // w.Hkv) <= 8
+    tensor = (not is_mla) and not decode and w.dtype != "f32" and w.D in (64, 128)
+    if decode:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                "frac": gbs / float(peaks["hbm_gbs"]), "peak_kind": f"{peak_kind} HBM copy",
+                "kernel": "paged_decode_kernel"}
+    elif tensor:
+        pk = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": tf, "peak": pk, "unit": "TFLOP/s", "frac": tf / pk,
+                "peak_kind": f"{peak_kind} bf16 dense burst", "kernel": "paged_tc_kernel"}
+    else:
+        roof = {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
+                "peak_kind": f"fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x {mhz:.0f} MHz",
+                "kernel": "mla_fwd_kernel" if is_mla else "paged_fwd_kernel"}
+    roof.update({"traffic": None, "algorithmic_bytes": nbytes})
     heads = {"H": w.H, "R": w.R, "Pd": w.Pd} if is_mla else {"Hq": w.Hq, "Hkv": w.Hkv, "D": w.D}
     line = {
         "metric": f"{'MLA' if is_mla else 'paged attention'} TFLOP/s ({w.name})", "value": value, "unit": "TFLOP/s",
