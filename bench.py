@@ -38,7 +38,7 @@ KERNEL_NAME = "attn_fwd_tc_kernel"
 # key-range splits per workload (1 when absent): enough CTAs for 152 SMs
 SPLITS = {"bf16_gqa_chunk_32k": 4}
 # key-range splits of paged decode: ~1k keys per split for 1k-8k contexts
-PAGED_SPLITS = {"bf16_paged_decode": 8}
+PAGED_SPLITS = {"bf16_paged_decode": 8, "bf16_mla_decode": 4}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -431,18 +431,29 @@ def bench_paged(args):
     max_q = int(nq_s.max()) if len(nq_s) else 0
     out = torch.empty_like(t[0])
     stream = torch.cuda.current_stream(device)
-    pws = None
-    if not is_mla:
+    splits = args.splits if args.splits else PAGED_SPLITS.get(w.name, 1)
+    if is_mla:
+        shp = attn.MlaShape(w.num_seqs, int(x["q_offsets"][-1]), w.H, w.R, w.Pd, w.page_size,
+                            int(x["latent"].shape[0]), int(x["block_table"].shape[1]), max_q)
+        need = attn.mla_workspace_bytes(shp, splits)
+    else:
         shp = attn.PagedShape(w.num_seqs, int(x["q_offsets"][-1]), w.Hq, w.Hkv, w.D, w.page_size,
                               int(x["k_cache"].shape[0]), int(x["block_table"].shape[1]), max_q)
-        need = attn.paged_workspace_bytes(shp, PAGED_SPLITS.get(w.name, 1))
-        pws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+        need = attn.paged_workspace_bytes(shp, splits)
+    pws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    # the paths the library takes for this call (see attn_paged_fwd / attn_paged_mla)
+    decode = (not is_mla) and max_q * (w.Hq // w.Hkv) <= 8
+    if is_mla:
+        tensor = (w.dtype != "f32" and w.R in (256, 512) and w.Pd in (0, 64) and w.page_size % 8 == 0
+                  and (32 % w.page_size == 0 or w.page_size % 32 == 0))
+    else:
+        tensor = not decode and w.dtype != "f32" and w.D in (64, 128)
+    launches = 2 if need > 0 and (decode or (is_mla and tensor)) else 1
 
     def step():
         call = attn.paged_mla if is_mla else attn.paged_fwd
-        extra = {} if is_mla else {"num_splits": PAGED_SPLITS.get(w.name, 1), "workspace": pws}
         call(*t, ints["block_table"], ints["seq_lens"], ints["q_offsets"], positions=pos, causal=w.causal,
-             scale=x["scale"], max_queries=max_q, out=out, stream=stream, **extra)
+             scale=x["scale"], max_queries=max_q, out=out, stream=stream, num_splits=splits, workspace=pws)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -492,20 +503,21 @@ def bench_paged(args):
     mhz = (clocks.summary() or {}).get("sm_mhz") or 2070.0
     alu_peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
     tf = flops / (ms * 1e-3) / 1e12
-    # the path the library takes: decode-shaped paged calls (<= 8 rows per
-    # sequence and kv head) stream the cache (HBM roofline); prefill-shaped
-    # F16/BF16 paged calls with D in {64, 128} run on the tensor cores; the
-    # rest (MLA) on the fp32 FMA pipes
-    decode = (not is_mla) and max_q * (w.Hq // w.Hkv) <= 8
-    tensor = (not is_mla) and not decode and w.dtype != "f32" and w.D in (64, 128)
-    if decode:
+    # roofline of the path taken: decode-shaped paged calls (<= 8 rows per
+    # sequence and kv head) stream the cache (HBM); prefill-shaped F16/BF16
+    # paged calls with D in {64, 128} run on the tensor cores; tensor-core MLA
+    # is held to whichever of the tensor and HBM rooflines binds (the larger
+    # ideal time); the rest runs on the fp32 FMA pipes
+    mla_hbm = is_mla and tensor and nbytes / float(peaks["hbm_gbs"]) > flops / (float(peaks["bf16_tflops"]) * 1e3)
+    if decode or mla_hbm:
         roof = {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                 "frac": gbs / float(peaks["hbm_gbs"]), "peak_kind": f"{peak_kind} HBM copy",
-                "kernel": "paged_decode_kernel"}
+                "kernel": "mla_tc_kernel" if is_mla else "paged_decode_kernel"}
     elif tensor:
         pk = float(peaks["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": tf, "peak": pk, "unit": "TFLOP/s", "frac": tf / pk,
-                "peak_kind": f"{peak_kind} bf16 dense burst", "kernel": "paged_tc_kernel"}
+                "peak_kind": f"{peak_kind} bf16 dense burst",
+                "kernel": "mla_tc_kernel" if is_mla else "paged_tc_kernel"}
     else:
         roof = {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
                 "peak_kind": f"fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x {mhz:.0f} MHz",
@@ -520,10 +532,10 @@ def bench_paged(args):
         "config": {"workload": w.name, "num_seqs": w.num_seqs, **heads, "page_size": w.page_size, "ctx_range": list(w.ctx_range), "q_range": list(w.q_range),
                    "queries": int(x["q_offsets"][-1]), "keys": int(x["seq_lens"].sum()),
                    "parallelism": f"replicas x{world}", "flops_basis": "exact: per visible (query, key) pair and head",
-                   "num_splits": 1 if is_mla else PAGED_SPLITS.get(w.name, 1),
+                   "num_splits": splits if (decode or (is_mla and tensor)) else 1,
                    "l2": f"cache read {nbytes / 2**20:.0f} MiB per step"},
         "roofline": roof, "hbm_gbs_algorithmic": gbs, "e2e": None,
-        "gpu_launches": args.steps, "clocks": clocks.summary(),
+        "gpu_launches": args.steps * launches, "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
 

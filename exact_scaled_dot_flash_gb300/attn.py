@@ -85,8 +85,11 @@ def load_library():
         lib.attn_paged_workspace_bytes.restype = ctypes.c_int
         lib.attn_paged_fwd.restype = ctypes.c_int
         lib.attn_paged_mla.argtypes = [ctypes.POINTER(MlaShape), vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
-                                       ctypes.c_float, ctypes.c_int, vp, vp, vp]
+                                       ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp, vp, vp]
         lib.attn_paged_mla.restype = ctypes.c_int
+        lib.attn_paged_mla_workspace_bytes.argtypes = [ctypes.POINTER(MlaShape), ctypes.c_int,
+                                                       ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_paged_mla_workspace_bytes.restype = ctypes.c_int
         lib.attn_strerror.argtypes = [ctypes.c_int]
         lib.attn_strerror.restype = ctypes.c_char_p
         lib.attn_last_cuda_error.argtypes = []
@@ -395,14 +398,24 @@ def paged_fwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, *, position
     return (out, lse) if return_lse else out
 
 
+def mla_workspace_bytes(shape: MlaShape, num_splits: int) -> int:
+    """Workspace bytes attn_paged_mla needs for ``shape`` and ``num_splits``."""
+    n = ctypes.c_size_t(0)
+    check(load_library().attn_paged_mla_workspace_bytes(ctypes.byref(shape), int(num_splits), ctypes.byref(n)))
+    return n.value
+
+
 def paged_mla(q, qp, latent, kpos, block_table, seq_lens, q_offsets, *, positions=None, causal: bool = True,
-              scale: float, max_queries: int | None = None, return_lse: bool = False, out=None, stream=None):
+              scale: float, max_queries: int | None = None, return_lse: bool = False, out=None, stream=None,
+              num_splits: int = 1, workspace=None):
     """MLA with absorbed projections over a paged latent cache (attn_paged_mla).
 
     q [queries, H, R]; qp [queries, H, Pd]; latent [pages, page_size, 1, R];
     kpos [pages, page_size, 1, Pd]; metadata as for :func:`paged_fwd`;
-    ``scale`` is the original model's QK scale. Returns out [queries, H, R]
-    (and lse float32 [queries, H]).
+    ``scale`` is the original model's QK scale. ``num_splits`` splits the key
+    range of every 128-row block (workspace taken from ``workspace``, a CUDA
+    uint8 tensor, or allocated here). Returns out [queries, H, R] (and lse
+    float32 [queries, H]).
     """
     import torch
 
@@ -431,9 +444,15 @@ def paged_mla(q, qp, latent, kpos, block_table, seq_lens, q_offsets, *, position
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     shape = MlaShape(ns, nq, H, R, Pd, P, pages, int(block_table.shape[1]), int(max_queries))
+    need = mla_workspace_bytes(shape, num_splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    elif need and (workspace.device != dev or workspace.numel() * workspace.element_size() < need):
+        raise AttnError(f"workspace must hold {need} bytes on q's device")
     ptr = lambda t: (t.data_ptr() or None) if t is not None else None
     check(load_library().attn_paged_mla(ctypes.byref(shape), ptr(q), ptr(qp), ptr(latent), ptr(kpos),
                                         ptr(block_table), ptr(seq_lens), ptr(q_offsets), ptr(positions),
-                                        int(bool(causal)), float(scale), _dtype_code(q), ptr(out), ptr(lse),
+                                        int(bool(causal)), float(scale), _dtype_code(q), int(num_splits),
+                                        ptr(workspace) if need else None, need, ptr(out), ptr(lse),
                                         stream.cuda_stream or None))
     return (out, lse) if return_lse else out

@@ -596,10 +596,22 @@ int attn_paged_fwd(const attn_paged_shape_t* shape, const void* q, const void* k
 // ---------------------------------------------------------------- MLA
 extern "C" {
 
+int attn_paged_mla_workspace_bytes(const attn_mla_shape_t* shape, int num_splits, size_t* bytes) {
+  if (!shape || !bytes) return ATTN_ERR_NULL;
+  const attn_mla_shape_t s = *shape;
+  if (s.num_queries < 0 || s.H <= 0 || s.R <= 0 || static_cast<int64_t>(s.num_queries) * s.H > 0x7fffffffLL)
+    return ATTN_ERR_SHAPE;
+  if (num_splits < 1 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
+  attn_shape_t rows{1, 1, 1, s.num_queries * s.H, 0, s.R, 1, 1};
+  *bytes = num_splits > 1 ? static_cast<size_t>(split_layout(rows, num_splits).total) : 0;
+  return ATTN_OK;
+}
+
 int attn_paged_mla(const attn_mla_shape_t* shape, const void* q, const void* qp, const void* latent,
                    const void* kpos, const int32_t* block_table, const int32_t* seq_lens,
                    const int32_t* q_offsets, const int32_t* positions, int causal, float scale,
-                   attn_dtype_t dtype, void* out, float* lse, void* stream) {
+                   attn_dtype_t dtype, int num_splits, void* workspace, size_t workspace_bytes,
+                   void* out, float* lse, void* stream) {
   if (!shape) return ATTN_ERR_NULL;
   const attn_mla_shape_t s = *shape;
   if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
@@ -610,8 +622,10 @@ int attn_paged_mla(const attn_mla_shape_t* shape, const void* q, const void* qp,
   if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_SCALE;
   if (!(s.R == 128 || s.R == 256 || s.R == 512) || !(s.Pd == 0 || s.Pd == 16 || s.Pd == 32 || s.Pd == 64))
     return ATTN_ERR_HEAD_DIM;
+  if (num_splits < 1 || num_splits > ATTN_MAX_SPLITS) return ATTN_ERR_SPLITS;
   if ((static_cast<int64_t>(s.max_queries) * s.H + 7) / 8 > 65535 ||
-      static_cast<int64_t>(s.max_pages) * s.page_size > 0x7fffffffLL)
+      static_cast<int64_t>(s.max_pages) * s.page_size > 0x7fffffffLL ||
+      static_cast<int64_t>(s.num_queries) * s.H > 0x7fffffffLL)
     return ATTN_ERR_SHAPE;
   if (s.num_queries == 0 || s.num_seqs == 0) return ATTN_OK;
   if (!q || !out || !seq_lens || !q_offsets || (s.max_pages > 0 && !block_table) ||
@@ -638,11 +652,22 @@ int attn_paged_mla(const attn_mla_shape_t* shape, const void* q, const void* qp,
   for (const Buf& b : ins)
     if (overlaps(out, out_bytes, b.p, b.n) || overlaps(lse, lse_bytes, b.p, b.n)) return ATTN_ERR_OVERLAP;
   if (overlaps(out, out_bytes, lse, lse_bytes)) return ATTN_ERR_OVERLAP;
+  attn_shape_t rows_shape{1, 1, 1, s.num_queries * s.H, 0, s.R, 1, 1};
+  const SplitLayout lay = split_layout(rows_shape, num_splits);
+  if (num_splits > 1) {
+    if (!workspace || workspace_bytes < static_cast<size_t>(lay.total)) return ATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+    for (const Buf& b : ins)
+      if (overlaps(workspace, lay.total, b.p, b.n)) return ATTN_ERR_OVERLAP;
+    if (overlaps(workspace, lay.total, out, out_bytes) || overlaps(workspace, lay.total, lse, lse_bytes))
+      return ATTN_ERR_OVERLAP;
+  }
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e);
   attn::PagedParams pp{};
+  pp.num_splits = 1;
   pp.num_seqs = s.num_seqs;
   pp.num_queries = s.num_queries;
   pp.Hq = s.H;
@@ -659,9 +684,42 @@ int attn_paged_mla(const attn_mla_shape_t* shape, const void* q, const void* qp,
   pp.scale_log2 = scale * 1.4426950408889634f;
   pp.status = status_ptr(dev);
   pp.device = dev;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // F16/BF16 with R in {256, 512}, Pd in {0, 64} and a page size the 32-key
+  // tile gathers cover take the tensor cores (and the key-range splits)
+  const bool page_ok = s.page_size % 8 == 0 && (32 % s.page_size == 0 || s.page_size % 32 == 0);
+  if (dtype != ATTN_F32 && (s.R == 256 || s.R == 512) && (s.Pd == 0 || s.Pd == 64) && page_ok &&
+      s.num_pages > 0) {
+    attn::EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail_cuda(cudaErrorNotSupported);
+    pp.num_splits = num_splits;
+    pp.ws_o = num_splits > 1 ? static_cast<float*>(workspace) : nullptr;
+    pp.ws_ml = num_splits > 1 ? reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + lay.ml_offset)
+                              : nullptr;
+    const bool bf = dtype == ATTN_BF16;
+    using attn::mlatc::launch_mla_tc;
+#define ATTN_MLA_TC(R, PD)                                                                         \
+  (bf ? launch_mla_tc<R, PD, true>(enc, pp, q, qp, latent, kpos, out, lse, st)                     \
+      : launch_mla_tc<R, PD, false>(enc, pp, q, qp, latent, kpos, out, lse, st))
+    if (s.R == 512) e = s.Pd == 64 ? ATTN_MLA_TC(512, 64) : ATTN_MLA_TC(512, 0);
+    else e = s.Pd == 64 ? ATTN_MLA_TC(256, 64) : ATTN_MLA_TC(256, 0);
+#undef ATTN_MLA_TC
+    if (e == cudaSuccess && num_splits > 1) {  // merge the partials of rows r = query * H + head
+      attn::KernelParams mp{};
+      mp.B = 1;
+      mp.Hq = 1;
+      mp.Sq = s.num_queries * s.H;
+      mp.num_splits = num_splits;
+      mp.ws_o = pp.ws_o;
+      mp.ws_ml = pp.ws_ml;
+      mp.lse = lse;
+      e = attn::launch_split_merge(mp, s.R, static_cast<int>(dtype), out, st);
+    }
+    return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+  }
   int unsupported = 0;
-  e = attn::launch_mla_simt(s.R, s.Pd, static_cast<int>(dtype), pp, q, qp, latent, kpos, out, lse,
-                            static_cast<cudaStream_t>(stream), &unsupported);
+  e = attn::launch_mla_simt(s.R, s.Pd, static_cast<int>(dtype), pp, q, qp, latent, kpos, out, lse, st,
+                            &unsupported);
   if (unsupported) return ATTN_ERR_HEAD_DIM;
   return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
 }

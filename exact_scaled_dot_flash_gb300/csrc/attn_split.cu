@@ -86,6 +86,8 @@ cudaError_t launch_split_merge(const KernelParams& p, int D, int dtype, void* ou
     case 32: return split::launch_d<32>(p, dtype, out, stream);
     case 64: return split::launch_d<64>(p, dtype, out, stream);
     case 128: return split::launch_d<128>(p, dtype, out, stream);
+    case 256: return split::launch_d<256>(p, dtype, out, stream);
+    case 512: return split::launch_d<512>(p, dtype, out, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -87,10 +87,11 @@ struct PagedParams {
   float scale_log2;
   int* status;
   int device;
-  // decode-shaped calls only: key-range splits, each writing an unnormalised
-  // partial (rows r = query * Hq + head) that launch_split_merge combines
+  // decode-shaped paged calls and tensor-core MLA: key-range splits, each
+  // writing an unnormalised partial (rows r = query * Hq + head) that
+  // launch_split_merge combines
   int num_splits;
-  float* ws_o;    // [num_splits, num_queries * Hq, D]
+  float* ws_o;    // [num_splits, num_queries * Hq, D] (D = R for MLA)
   float2* ws_ml;  // [num_splits, num_queries * Hq] (m in log2 units, l)
 };
 namespace pagedtc {
@@ -103,6 +104,13 @@ cudaError_t launch_paged_tc(EncodeTiledFn enc, const PagedParams& pp, const void
 // True when attn_paged_fwd takes the decode kernel (the only one that splits).
 inline bool paged_is_decode(int max_queries, int group) { return static_cast<long long>(max_queries) * group <= 8; }
 // MLA over a paged latent cache (PagedParams with Hq = heads, Hkv = 1).
+namespace mlatc {
+// Tensor-core MLA (F16/BF16, R in {256, 512}, Pd in {0, 64}, page_size a
+// multiple of 8 dividing 32 or a multiple of 32); splits by pp.num_splits.
+template <int R, int PD, bool BF16>
+cudaError_t launch_mla_tc(EncodeTiledFn enc, const PagedParams& pp, const void* q, const void* qp, const void* lat,
+                          const void* kp, void* out, float* lse, cudaStream_t stream);
+}  // namespace mlatc
 cudaError_t launch_mla_simt(int R, int Pd, int dtype, const PagedParams& pp, const void* q, const void* qp,
                             const void* lat, const void* kp, void* out, float* lse, cudaStream_t stream,
                             int* unsupported);

@@ -295,16 +295,32 @@ typedef struct {
  * attn_paged_fwd, with one key/value head shared by all H heads.
  * Supported: R in {128, 256, 512}, Pd in {0, 16, 32, 64}; every dtype. q, qp,
  * latent, kpos, out 16-byte aligned device pointers (qp, kpos may be NULL when
- * Pd == 0); lse NULL or float [num_queries, H]. Asynchronous on `stream`;
- * returns ATTN_OK or a negative ATTN_ERR_* code. */
+ * Pd == 0); lse NULL or float [num_queries, H]; num_queries * H < 2^31.
+ *
+ * num_splits (1..ATTN_MAX_SPLITS) cuts the key tiles of every 128-row block of
+ * (query, head) rows into that many runs, one CTA each, merged afterwards
+ * from FP32 partial statistics (the split of attn_fwd_split). With
+ * num_splits > 1 a workspace of attn_paged_mla_workspace_bytes(shape,
+ * num_splits) bytes is required (16-byte aligned, disjoint from every other
+ * buffer); calls that run on the fp32 FMA kernel (F32, R = 128, Pd in
+ * {16, 32}, or page sizes that are not a multiple of 8 dividing 32 or a
+ * multiple of 32) ignore the splits. Asynchronous on `stream`; returns ATTN_OK
+ * or a negative ATTN_ERR_* code. */
 ATTN_API int attn_paged_mla(const attn_mla_shape_t* shape,
                             const void* q, const void* qp,
                             const void* latent, const void* kpos,
                             const int32_t* block_table, const int32_t* seq_lens,
                             const int32_t* q_offsets, const int32_t* positions,
                             int causal, float scale, attn_dtype_t dtype,
+                            int num_splits, void* workspace, size_t workspace_bytes,
                             void* out, float* lse,
                             void* stream);
+
+/* attn_paged_mla_workspace_bytes - workspace attn_paged_mla needs for `shape`
+ * and `num_splits`: 0 when num_splits == 1, else
+ * num_splits * num_queries * H * (4 R + 8) plus up to 255 bytes of padding.
+ * Returns ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_SHAPE or ATTN_ERR_SPLITS. */
+ATTN_API int attn_paged_mla_workspace_bytes(const attn_mla_shape_t* shape, int num_splits, size_t* bytes);
 
 /* Size of the device scratch array built into the library for
  * attn_fwd_split_noalloc (32 MiB per GPU that loads the library). */
