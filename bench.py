@@ -37,8 +37,9 @@ METRIC = "attention fwd TFLOP/s and % of GB300 BF16 peak (causal, S=4096, D=128)
 KERNEL_NAME = "attn_fwd_tc_kernel"
 # key-range splits per workload (1 when absent): enough CTAs for 152 SMs
 SPLITS = {"bf16_gqa_chunk_32k": 4}
-# key-range splits of paged decode: ~1k keys per split for 1k-8k contexts
-PAGED_SPLITS = {"bf16_paged_decode": 8, "bf16_mla_decode": 4}
+# key-range splits of the serving workloads (1 when absent): MLA decode has only
+# 64 x 2 CTAs of 128 rows without them; paged decode already has 512 CTAs
+PAGED_SPLITS = {"bf16_mla_decode": 4}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -447,7 +448,8 @@ def bench_paged(args):
         tensor = (w.dtype != "f32" and w.R in (256, 512) and w.Pd in (0, 64) and w.page_size % 8 == 0
                   and (32 % w.page_size == 0 or w.page_size % 32 == 0))
     else:
-        tensor = not decode and w.dtype != "f32" and w.D in (64, 128)
+        tensor = (w.dtype != "f32" and w.D in (64, 128) and w.page_size % 8 == 0
+                  and (128 % w.page_size == 0 or w.page_size % 128 == 0))
     launches = 2 if need > 0 and (decode or (is_mla and tensor)) else 1
 
     def step():
@@ -512,7 +514,7 @@ def bench_paged(args):
     if decode or mla_hbm:
         roof = {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                 "frac": gbs / float(peaks["hbm_gbs"]), "peak_kind": f"{peak_kind} HBM copy",
-                "kernel": "mla_tc_kernel" if is_mla else "paged_decode_kernel"}
+                "kernel": "mla_tc_kernel" if is_mla else ("paged_tc_kernel" if tensor else "paged_decode_kernel")}
     elif tensor:
         pk = float(peaks["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": tf, "peak": pk, "unit": "TFLOP/s", "frac": tf / pk,

@@ -558,11 +558,10 @@ int attn_paged_fwd(const attn_paged_shape_t* shape, const void* q, const void* k
   pp.status = status_ptr(dev);
   pp.device = dev;
   int unsupported = 0;
-  // prefill-shaped F16/BF16 calls with D in {64, 128} and a page size the
-  // tile gathers cover take the tensor cores
+  // F16/BF16 calls with D in {64, 128} and a page size the tile gathers
+  // cover take the tensor cores; the rest the fp32 FMA kernels
   const bool pow_ok = s.page_size % 8 == 0 && (128 % s.page_size == 0 || s.page_size % 128 == 0);
-  if (dtype != ATTN_F32 && (s.D == 64 || s.D == 128) && splits == 1 && pow_ok && s.num_pages > 0 &&
-      !attn::paged_is_decode(s.max_queries, static_cast<int>(group))) {
+  if (dtype != ATTN_F32 && (s.D == 64 || s.D == 128) && pow_ok && s.num_pages > 0) {
     attn::EncodeTiledFn enc = encode_fn();
     if (!enc) return fail_cuda(cudaErrorNotSupported);
     const bool bf = dtype == ATTN_BF16;
@@ -572,11 +571,11 @@ int attn_paged_fwd(const attn_paged_shape_t* shape, const void* q, const void* k
                            : launch_paged_tc<128, false>(enc, pp, q, k_cache, v_cache, out, lse, st);
     else e = bf ? launch_paged_tc<64, true>(enc, pp, q, k_cache, v_cache, out, lse, st)
                 : launch_paged_tc<64, false>(enc, pp, q, k_cache, v_cache, out, lse, st);
-    return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+  } else {
+    e = attn::launch_paged_simt(s.D, static_cast<int>(dtype), pp, q, k_cache, v_cache, out, lse,
+                                static_cast<cudaStream_t>(stream), &unsupported);
+    if (unsupported) return ATTN_ERR_HEAD_DIM;
   }
-  e = attn::launch_paged_simt(s.D, static_cast<int>(dtype), pp, q, k_cache, v_cache, out, lse,
-                              static_cast<cudaStream_t>(stream), &unsupported);
-  if (unsupported) return ATTN_ERR_HEAD_DIM;
   if (e == cudaSuccess && splits > 1) {  // merge the partials of rows r = query * Hq + head
     attn::KernelParams mp{};
     mp.B = 1;

@@ -1,24 +1,32 @@
 // attn_paged_tc.cuh - attention over a paged key/value cache with packed
 // variable-length queries on the tcgen05 tensor cores (F16/BF16, D in
-// {64, 128}): the prefill-shaped calls of attn_paged_fwd.
+// {64, 128}): attn_paged_fwd's prefill- and decode-shaped calls.
 //
 // Source: ruDNN user guide, section 9 (paged attention): physical pages
 // K, V [pages, page_size, Hkv, D] read through per-sequence page tables,
-// packed queries [queries, Hq, D], GQA, causal mask by absolute position.
+// packed queries [queries, Hq, D], GQA, causal mask by absolute position,
+// split key history merged from FP32 partial statistics.
 //
 // The pipeline is the dense forward's (attn_tc.cuh: 384 threads, two query
 // tiles of 128 rows per CTA sharing every K/V tile, S and P in tensor memory,
 // MMA order S_0 PV_1 S_1 PV_0, lazy rescale); what changes is the addressing:
-//  - a CTA is (sequence, query head, 256 consecutive queries of the sequence);
-//  - a Q tile is 128 consecutive packed queries of one head, loaded through a
-//    3-D view [queries, Hq, D] of q (box 64 x 1 x 128);
+//  - the rows of a CTA are (query, head) pairs of one sequence and one block
+//    of gp query heads that share a kv head (gp = Hq/Hkv when that divides
+//    128, else 1), packed as row = query * gp + head-in-block, so every K/V
+//    tile serves all the heads of a GQA group; a decode step (one query) is
+//    gp rows of a 128-row tile;
+//  - a CTA is (sequence, 256 packed rows, head block, key split);
+//  - a Q tile of 128 packed rows is one TMA box of a 4-D view
+//    [queries, Hq/gp, gp, D] of q (box 64 x gp x 1 x 128/gp);
 //  - a K/V tile of 128 keys is gathered page by page through a 4-D view
 //    [pages, page_size, Hkv, D] of the cache (box 64 x 1 x min(page_size, 128)
 //    x 1): one box per page inside the tile, at the page the table names; a
 //    page index outside the cache loads zeros (TMA fills out-of-range boxes);
 //  - row i of the CTA sees key j when j < seq_len and, causal, j <= its
 //    position (explicit, or the newest-token default);
-//  - rows are stored directly (their sequence's rows only) in the input dtype.
+//  - rows are stored directly (their sequence's rows only) in the input dtype;
+//    with num_splits > 1 the CTA covers a contiguous run of the key tiles and
+//    stores its unnormalised output and (m, l) for launch_split_merge.
 // Requires page_size a multiple of 8 that divides 128 or is a multiple of 128.
 #pragma once
 
@@ -66,45 +74,58 @@ struct Cfg {
 };
 
 struct PWork {
-  int s, h, hk, q_lo, nq, row0, L;
-  int n[NQ], nfull[NQ], nmax;
+  int s, hh, hk, sp, q_lo, nq, row0, L, j0;
+  int n[NQ], nfull[NQ], nmax;  // n, nmax: key tiles j0 .. j0+n-1 of this CTA's split
 };
 
-// blockIdx.x -> (sequence, 256-query block, head); empty when the block lies
-// past the sequence's queries.
-__device__ __forceinline__ PWork make_pwork(const PagedParams& pp, int qblocks) {
+// blockIdx.x -> (sequence, 256-row block, split, head block; the head block
+// fastest, so that the CTAs reading the same K/V tiles run side by side).
+// Empty when the row block lies past the sequence's rows.
+__device__ __forceinline__ PWork make_pwork(const PagedParams& pp, int qblocks, int gp) {
   PWork w;
-  const int item = static_cast<int>(blockIdx.x);
-  w.h = item % pp.Hq;
-  const int rest = item / pp.Hq;
-  const int qb = rest % qblocks;
-  w.s = rest / qblocks;
-  w.hk = w.h / (pp.Hq / pp.Hkv);
+  int item = static_cast<int>(blockIdx.x);
+  const int nhh = pp.Hq / gp;
+  w.hh = item % nhh;
+  item /= nhh;
+  w.sp = item % pp.num_splits;
+  item /= pp.num_splits;
+  const int qb = item % qblocks;
+  w.s = item / qblocks;
+  w.hk = (w.hh * gp) / (pp.Hq / pp.Hkv);
   w.q_lo = min(max(__ldg(pp.q_offsets + w.s), 0), pp.num_queries);
   const int q_hi = min(max(__ldg(pp.q_offsets + w.s + 1), w.q_lo), pp.num_queries);
   w.nq = q_hi - w.q_lo;
   w.row0 = qb * NQ * BM;
   w.L = min(max(__ldg(pp.seq_lens + w.s), 0), pp.max_pages * pp.page_size);
-  w.nmax = 0;
+  const int rows = w.nq * gp;
+  int ntot[NQ], nall = 0;
 #pragma unroll
   for (int t = 0; t < NQ; ++t) {
     const int r0 = w.row0 + t * BM;
-    w.n[t] = 0;
+    ntot[t] = 0;
     w.nfull[t] = 0;
-    if (r0 < w.nq) {
-      const int rlast = min(r0 + BM - 1, w.nq - 1);
+    if (r0 < rows) {
+      const int first_q = r0 / gp, last_q = min(w.nq - 1, (r0 + BM - 1) / gp);
       int hi = w.L, lo = w.L;
       if (pp.causal) {
         if (pp.positions) {
           lo = 0;  // arbitrary positions: every tile is masked element by element
         } else {
-          hi = min(hi, w.L - w.nq + rlast + 1);
-          lo = min(lo, w.L - w.nq + r0 + 1);
+          hi = min(hi, w.L - w.nq + last_q + 1);
+          lo = min(lo, w.L - w.nq + first_q + 1);
         }
       }
-      w.n[t] = hi > 0 ? (hi + BN - 1) / BN : 0;
+      ntot[t] = hi > 0 ? (hi + BN - 1) / BN : 0;
       w.nfull[t] = lo > 0 ? lo / BN : 0;
     }
+    nall = max(nall, ntot[t]);
+  }
+  w.j0 = static_cast<int>(static_cast<int64_t>(nall) * w.sp / pp.num_splits);
+  const int j1 = static_cast<int>(static_cast<int64_t>(nall) * (w.sp + 1) / pp.num_splits);
+  w.nmax = 0;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    w.n[t] = max(0, min(ntot[t], j1) - w.j0);
     w.nmax = max(w.nmax, w.n[t]);
   }
   return w;
@@ -114,7 +135,7 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     paged_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const PagedParams pp, void* out, float* lse,
-                    int qblocks) {
+                    int qblocks, int gp) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -123,8 +144,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8 * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const PWork w = make_pwork(pp, qblocks);
-  if (w.row0 >= w.nq) return;  // no query rows here (CTA-uniform); rows without keys still get NaN
+  const PWork w = make_pwork(pp, qblocks, gp);
+  if (w.row0 >= w.nq * gp) return;  // no rows here (CTA-uniform); rows without keys still get NaN
+  const bool partial = pp.num_splits > 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -163,15 +185,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (w.n[t] == 0) continue;
         mbar_arrive_expect_tx(bar(C::BAR_Q + t), C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(sb + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::BAR_Q + t), c * C::BOX_D, w.h,
-                      w.q_lo + w.row0 + t * BM);
+          tma_load_4d(sb + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::BAR_Q + t), c * C::BOX_D, 0,
+                      w.hh, w.q_lo + (w.row0 + t * BM) / gp);
       }
       const int32_t* table = pp.block_table + static_cast<size_t>(w.s) * pp.max_pages;
       const int box_rows = pp.page_size < BN ? pp.page_size : BN;
       const int boxes = BN / box_rows;
       int it = 0;
       bool ok = true;
-      for (int j = 0; j < w.nmax && ok; ++j) {
+      for (int jj = 0; jj < w.nmax && ok; ++jj) {
+        const int j = w.j0 + jj;  // key tile
         for (int kv = 0; kv < 2; ++kv, ++it) {
           const int st = it % C::STAGES;
           if (!mbar_wait(bar(C::BAR_EMPTY + st), ((it / C::STAGES) & 1) ^ 1)) { ok = false; break; }
@@ -262,8 +285,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     setmaxnreg_inc<REG_SOFTMAX>();
     const int t = warp >> 2;
     const int row = ((warp & 3) << 5) + lane;
-    const int rl = w.row0 + t * BM + row;  // row within the sequence's queries
-    const bool row_ok = rl < w.nq;
+    const int pr = w.row0 + t * BM + row;  // packed row: query * gp + head in block
+    const int tq = pr / gp;                // query within the sequence
+    const bool row_ok = tq < w.nq;
+    const int head = w.hh * gp + (pr - tq * gp);
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
     const uint32_t tS = tmem + lane_off + t * BN;
     const uint32_t tP = tS + C::COL_P;
@@ -271,7 +296,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int n_t = t ? w.n[1] : w.n[0];
     const int nfull_t = t ? w.nfull[1] : w.nfull[0];
     const float sc = pp.scale_log2;
-    const int pos = !row_ok ? -1 : (pp.positions ? __ldg(pp.positions + w.q_lo + rl) : w.L - w.nq + rl);
+    const int pos = !row_ok ? -1 : (pp.positions ? __ldg(pp.positions + w.q_lo + tq) : w.L - w.nq + tq);
     const int causal_lim = pp.causal ? pos : 0x7fffffff;
     const int key_lim = w.L;
     float m_run = -INFINITY, l_run = 0.f;
@@ -289,8 +314,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
       }
-      const int key0 = j * BN;
-      if (j >= nfull_t) {
+      const int key0 = (w.j0 + j) * BN;
+      if (w.j0 + j >= nfull_t) {
 #pragma unroll
         for (int i = 0; i < 128; ++i) {
           const int key = key0 + i;
@@ -364,36 +389,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (failed) {
       if (lane == 0) fail();
-    } else if (w.row0 + t * BM < w.nq) {
+    } else if (w.row0 + t * BM < w.nq * gp) {
       tc_fence_after();
       const bool live = have && l_run > 0.f;
-      const float inv = live ? 1.f / l_run : __int_as_float(0x7fc00000);
-      const size_t orow = static_cast<size_t>(w.q_lo + (row_ok ? rl : 0)) * pp.Hq + w.h;
-      uint8_t* dst = static_cast<uint8_t*>(out) + orow * D * 2;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
+      const size_t orow = static_cast<size_t>(w.q_lo + (row_ok ? tq : 0)) * pp.Hq + (row_ok ? head : 0);
+      if (partial) {  // unnormalised output of this key run and its (m, l)
+        const size_t prow = static_cast<size_t>(w.sp) * pp.num_queries * pp.Hq + orow;
+        float4* dst = reinterpret_cast<float4*>(pp.ws_o + prow * D);
         if (have) {
-          tmem_ld32(tO + 32 * c, o);
-          tmem_wait_ld();
-        } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
-        }
-        if (row_ok) {
-          uint32_t pk[16];
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
+            if (row_ok) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 x = fmul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
-                                   make_float2(inv, inv));
-            pk[i] = pack2<BF16>(x.x, x.y);
+              for (int u = 0; u < 8; ++u)
+                dst[c * 8 + u] = make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]),
+                                             __uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3]));
+            }
           }
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            reinterpret_cast<uint4*>(dst + c * 64)[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
+        if (row_ok) pp.ws_ml[prow] = make_float2(live ? m_run : -INFINITY, live ? l_run : 0.f);
+      } else {
+        const float inv = live ? 1.f / l_run : __int_as_float(0x7fc00000);
+        uint8_t* dst = static_cast<uint8_t*>(out) + orow * D * 2;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          if (have) {
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+          if (row_ok) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 x = fmul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
+                                     make_float2(inv, inv));
+              pk[i] = pack2<BF16>(x.x, x.y);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              reinterpret_cast<uint4*>(dst + c * 64)[u] =
+                  make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
+        }
+        if (row_ok && lse) lse[orow] = live ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
       }
-      if (row_ok && lse) lse[orow] = live ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
     }
   }
   tc_fence_before();
@@ -412,12 +458,16 @@ cudaError_t launch_paged_tc(EncodeTiledFn enc, const PagedParams& pp, const void
   const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   CUtensorMap tq, tk, tv;
-  {  // q viewed as [queries, Hq, D]
-    const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(pp.Hq),
-                                static_cast<cuuint64_t>(pp.num_queries)};
-    const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(pp.Hq) * D * 2};
-    const cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(BM)};
-    if (enc(&tq, dt, 3, const_cast<void*>(q), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  // gp query heads share each CTA's rows: the kv group when it divides 128
+  const int group = pp.Hq / pp.Hkv;
+  const int gp = BM % group == 0 ? group : 1;
+  {  // q viewed as [queries, Hq/gp, gp, D]
+    const cuuint64_t gdim[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(gp),
+                                static_cast<cuuint64_t>(pp.Hq / gp), static_cast<cuuint64_t>(pp.num_queries)};
+    const cuuint64_t gstride[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(gp) * D * 2,
+                                   static_cast<cuuint64_t>(pp.Hq) * D * 2};
+    const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(gp), 1u, static_cast<cuuint32_t>(BM / gp)};
+    if (enc(&tq, dt, 4, const_cast<void*>(q), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -443,11 +493,12 @@ cudaError_t launch_paged_tc(EncodeTiledFn enc, const PagedParams& pp, const void
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  const int qblocks = (pp.max_queries + NQ * BM - 1) / (NQ * BM);
-  const uint64_t ctas = static_cast<uint64_t>(pp.num_seqs) * qblocks * pp.Hq;
+  const int64_t qblocks = (static_cast<int64_t>(pp.max_queries) * gp + NQ * BM - 1) / (NQ * BM);
+  const int64_t ctas = static_cast<int64_t>(pp.num_seqs) * qblocks * (pp.Hq / gp) * pp.num_splits;
   if (ctas == 0) return cudaSuccess;
-  if (ctas > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(ctas), NUM_THREADS, smem, stream>>>(tq, tk, tv, pp, out, lse, qblocks);
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(ctas), NUM_THREADS, smem, stream>>>(tq, tk, tv, pp, out, lse,
+                                                                   static_cast<int>(qblocks), gp);
   return cudaGetLastError();
 }
 

@@ -95,13 +95,13 @@ struct PagedParams {
   float2* ws_ml;  // [num_splits, num_queries * Hq] (m in log2 units, l)
 };
 namespace pagedtc {
-// Tensor-core paged kernel (prefill-shaped calls, F16/BF16, D in {64, 128},
-// page_size a multiple of 8 dividing 128 or a multiple of 128).
+// Tensor-core paged kernel (F16/BF16, D in {64, 128}, page_size a multiple of
+// 8 dividing 128 or a multiple of 128); splits by pp.num_splits.
 template <int D, bool BF16>
 cudaError_t launch_paged_tc(EncodeTiledFn enc, const PagedParams& pp, const void* q, const void* k, const void* v,
                             void* out, float* lse, cudaStream_t stream);
 }  // namespace pagedtc
-// True when attn_paged_fwd takes the decode kernel (the only one that splits).
+// True for decode-shaped attn_paged_fwd calls (the only ones that split).
 inline bool paged_is_decode(int max_queries, int group) { return static_cast<long long>(max_queries) * group <= 8; }
 // MLA over a paged latent cache (PagedParams with Hq = heads, Hkv = 1).
 namespace mlatc {

@@ -243,7 +243,7 @@ typedef struct {
  * sees no key is NaN (lse -inf). lse: NULL or float [num_queries, Hq] natural
  * log-sum-exp.
  *
- * num_splits (1..ATTN_MAX_SPLITS) cuts the keys of every (sequence, kv head)
+ * num_splits (1..ATTN_MAX_SPLITS) cuts the keys of every sequence and head
  * of a decode-shaped call (max_queries * Hq/Hkv <= 8) into that many runs,
  * one CTA each, merged afterwards from FP32 partial statistics (the split of
  * attn_fwd_split); it needs a 16-byte-aligned workspace of

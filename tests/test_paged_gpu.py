@@ -67,6 +67,12 @@ CASES = [
     PW("paged_f32_d32_p8_positions", "f32", 5, 4, 1, 32, 8, (5, 300), (1, 60), seed=4, explicit_positions=True),
     PW("paged_bf16_d64_p256_noncausal", "bf16", 3, 6, 2, 64, 256, (200, 800), (10, 100), seed=5, causal=False),
     PW("paged_f16_d16_p1", "f16", 3, 2, 2, 16, 1, (1, 40), (1, 20), seed=6),
+    # tensor-core kernel, GQA heads packed into the rows: group 8 prefill with
+    # positions, group 6 (does not divide 128: one head per CTA), MQA group 32
+    PW("paged_bf16_d128_g8_positions", "bf16", 3, 32, 4, 128, 32, (60, 500), (20, 90), seed=9,
+       explicit_positions=True),
+    PW("paged_f16_d64_g6_prefill", "f16", 3, 12, 2, 64, 16, (40, 400), (5, 70), seed=10),
+    PW("paged_bf16_d64_mqa_g32", "bf16", 4, 32, 1, 64, 64, (1, 600), (1, 6), seed=11),
 ]
 
 
@@ -143,6 +149,12 @@ def test_paged_decode_splits(splits):
     check(w, num_splits=splits)
     w2 = PW(f"paged_decode_split{splits}_f32", "f32", 5, 4, 4, 64, 16, (1, 700), (1, 1), seed=40 + splits)
     check(w2, num_splits=splits)
+    # tensor-core decode: group 6 (one head per CTA) and group 8 with two queries
+    w3 = PW(f"paged_decode_split{splits}_g6", "f16", 4, 12, 2, 64, 128, (1, 1200), (1, 1), seed=60 + splits)
+    check(w3, num_splits=splits)
+    w4 = PW(f"paged_decode_split{splits}_g4q2", "bf16", 5, 16, 4, 128, 64, (2, 2500), (2, 2), seed=70 + splits,
+            causal=splits % 2 == 0)
+    check(w4, num_splits=splits)
 
 
 def test_paged_split_workspace_errors():
