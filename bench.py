@@ -146,7 +146,7 @@ def read_traffic(w):
     try:
         d = json.load(open(p))
         from exact_scaled_dot_flash_gb300 import build
-        if d.get("kernel_source_sha") != build.kernel_source_digest():
+        if d.get("kernel_source_sha") != build.kernel_source_digest(d.get("kernel_sources")):
             return None
         return d.get("dram_bytes_per_launch")
     except (OSError, ValueError, AttributeError):

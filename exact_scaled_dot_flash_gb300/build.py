@@ -46,7 +46,7 @@ def _headers():
 def _digest(paths, extra=()):
     h = hashlib.sha256()
     for p in paths:
-        h.update(p.encode())
+        h.update(os.path.basename(p).encode())  # not the directory: the same on every machine
         with open(p, "rb") as f:
             h.update(f.read())
     for e in extra:
@@ -54,9 +54,16 @@ def _digest(paths, extra=()):
     return h.hexdigest()
 
 
-def kernel_source_digest() -> str:
-    """Digest of every CUDA source and header: identifies the kernels a profile describes."""
-    return _digest(_sources() + _headers())[:16]
+def kernel_source_digest(names=None) -> str:
+    """Digest of the CUDA sources and headers a kernel is built from (file names
+    under csrc/ or include/; every source and header when None): identifies the
+    kernels a profile describes."""
+    if names is None:
+        paths = _sources() + _headers()
+    else:
+        paths = [os.path.join(CSRC, n) if os.path.exists(os.path.join(CSRC, n)) else os.path.join(INCLUDE, n)
+                 for n in sorted(names)]
+    return _digest(paths)[:16]
 
 
 def _compile(src, hdr_digest, verbose, extra_flags):
