@@ -38,8 +38,8 @@ KERNEL_NAME = "attn_fwd_tc_kernel"
 # key-range splits per workload (1 when absent): enough CTAs for 152 SMs
 SPLITS = {"bf16_gqa_chunk_32k": 4}
 # key-range splits of the serving workloads (1 when absent): MLA decode has only
-# 64 x 2 CTAs of 128 rows without them; paged decode already has 512 CTAs
-PAGED_SPLITS = {"bf16_mla_decode": 4}
+# 64 x 4 CTAs of 128 rows without them; paged decode already has 512 CTAs
+PAGED_SPLITS = {"bf16_mla_decode": 2}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -446,7 +446,7 @@ def bench_paged(args):
     decode = (not is_mla) and max_q * (w.Hq // w.Hkv) <= 8
     if is_mla:
         tensor = (w.dtype != "f32" and w.R in (256, 512) and w.Pd in (0, 64) and w.page_size % 8 == 0
-                  and (32 % w.page_size == 0 or w.page_size % 32 == 0))
+                  and (64 % w.page_size == 0 or w.page_size % 64 == 0))
     else:
         tensor = (w.dtype != "f32" and w.D in (64, 128) and w.page_size % 8 == 0
                   and (128 % w.page_size == 0 or w.page_size % 128 == 0))

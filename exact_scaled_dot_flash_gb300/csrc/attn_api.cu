@@ -684,9 +684,9 @@ int attn_paged_mla(const attn_mla_shape_t* shape, const void* q, const void* qp,
   pp.status = status_ptr(dev);
   pp.device = dev;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // F16/BF16 with R in {256, 512}, Pd in {0, 64} and a page size the 32-key
+  // F16/BF16 with R in {256, 512}, Pd in {0, 64} and a page size the 64-key
   // tile gathers cover take the tensor cores (and the key-range splits)
-  const bool page_ok = s.page_size % 8 == 0 && (32 % s.page_size == 0 || s.page_size % 32 == 0);
+  const bool page_ok = s.page_size % 8 == 0 && (64 % s.page_size == 0 || s.page_size % 64 == 0);
   if (dtype != ATTN_F32 && (s.R == 256 || s.R == 512) && (s.Pd == 0 || s.Pd == 64) && page_ok &&
       s.num_pages > 0) {
     attn::EncodeTiledFn enc = encode_fn();

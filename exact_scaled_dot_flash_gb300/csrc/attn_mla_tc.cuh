@@ -11,31 +11,33 @@
 // Shape of the work: the rows of a sequence are its (query, head) pairs,
 // row = query * H + head, so a decode step with H = 128 heads is one 128-row
 // tile. A key row [c_j | kp_j] is R + Pd wide (576 for R = 512, Pd = 64) and
-// the output is R wide, which is more than tensor memory holds next to the
-// scores (128 lanes x 512 fp32 columns). So each 128-row block is run by R/256
-// CTAs, one per 256-column slice of the output; every CTA computes the full
-// scores S = [q | qp] [c | kp]^T of its rows (the same MMAs, so the same P, in
-// each CTA), and its own slice of P . c.
+// the output R wide. Each 128-row block is run by R/128 CTAs, one per
+// 128-column slice of the output: every CTA computes the full scores
+// S = [q | qp] [c | kp]^T of its rows (the same MMAs, so the same P, in each
+// CTA) and its own slice of P . c. With only 128 output columns the whole
+// query fits in tensor memory next to the scores, so shared memory holds
+// nothing but a ring of 64-key tiles, and the score MMAs are 64 keys wide: a
+// 128 x N x 16 MMA costs about the same for N = 16..64, so the width halves
+// the score cost per key against 32-key tiles.
 //
-// Tensor memory (512 columns): two S/P buffers of BN = 32 columns, then the
-// first query chunks (64 dims = 32 packed columns each, up to six), then the
-// 256-column output slice. The remaining query chunks stay in shared memory
-// (three for R = 512, Pd = 64), which leaves room for a ring of 32-key tiles.
-// The S MMA reads a query chunk from tensor memory (A operand) or shared
-// memory, and the key chunk from the ring; P . V reads P from tensor memory
-// and the latent columns of the same ring tile as V (the values are the latent
-// rows, so no separate value load exists).
+// Tensor memory (512 columns): the query chunks (64 dims = 32 packed 16-bit
+// columns each, at most nine), S (64 fp32 columns), P (32 packed columns), the
+// 128-column output slice. The S MMA reads its A operand (the query) from
+// tensor memory and the key chunk from the ring; P . V reads P from tensor
+// memory and this slice's two latent chunks of the same ring tile as V (the
+// values are the latent rows, so no separate value load exists).
 //
-// Warps: 0-3 softmax (one row per thread: tensor-memory loads of 32 scores,
-// masks, online softmax with a lazy rescale of O), 4 TMA producer (query
-// chunks once; key tiles gathered page by page through 3-D views
+// Warps: 0-3 softmax (one row per thread: loads the 64 scores, frees S for the
+// next tile's MMA, masks, online softmax, waits for the previous P . V before
+// writing P and, rarely, rescaling O), 4 TMA producer (the query once through
+// ring stages 1.., then key tiles gathered page by page through 3-D views
 // [pages, page_size, R] and [pages, page_size, Pd] of the caches; an invalid
 // page id loads zeros), 5 MMA issuer, order S_0 S_1 PV_0 S_2 PV_1 ...
 //
 // Key-range splits: the CTA's key tiles are cut into num_splits balanced runs;
 // with more than one run each CTA writes its unnormalised partial output and
 // (m, l) and launch_split_merge combines them (the split of attn_fwd_split).
-// Requires page_size a multiple of 8 that divides 32 or is a multiple of 32.
+// Requires page_size a multiple of 8 that divides 64 or is a multiple of 64.
 #pragma once
 
 #include <atomic>
@@ -47,15 +49,16 @@ namespace attn {
 namespace mlatc {
 
 constexpr int BM = 128;           // (query, head) rows per CTA
-constexpr int BN = 32;            // keys per tile
-constexpr int OC = 256;           // output columns per CTA
+constexpr int BN = 64;            // keys per tile
+constexpr int OC = 128;           // output columns per CTA
 constexpr int NUM_THREADS = 192;  // warps 0-3 softmax, 4 TMA, 5 MMA
 constexpr int WARP_TMA = 4;
 constexpr int WARP_MMA = 5;
 constexpr int TMEM_COLS = 512;
-constexpr int COL_S = 0;          // S/P buffers: columns [0, 2 BN)
-constexpr int COL_Q = 2 * BN;     // query chunks held in tensor memory
-constexpr int COL_O = 256;        // output slice: columns [256, 512)
+constexpr int COL_Q = 0;          // query chunks: columns [0, 32 NCH), NCH <= 9
+constexpr int COL_S = 288;        // S: 64 fp32 columns
+constexpr int COL_P = 352;        // P: 64 keys as 32 packed columns
+constexpr int COL_O = 384;        // output slice: columns [384, 512)
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -67,29 +70,24 @@ struct Cfg {
   static constexpr int NH = R / OC;          // CTAs per row block (output slices)
   static constexpr int NCH = (R + PD) / 64;  // 64-wide chunks of a key row
   static constexpr int NCH_LAT = R / 64;     // ... of which latent
-  static constexpr int NQT_MAX = (COL_O - COL_Q) / 32;
-  static constexpr int NQT = NCH < NQT_MAX ? NCH : NQT_MAX;  // query chunks in tensor memory
-  static constexpr int NQS = NCH - NQT;                      // query chunks in shared memory
   static constexpr int QCH_BYTES = BM * 128;
   static constexpr int KCH_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = NCH * KCH_BYTES;
-  static constexpr int OFF_QS = 0;
-  static constexpr int OFF_RING = NQS * QCH_BYTES;
   static constexpr int RESERVE = 1024 + 256;  // base alignment + barriers
-  static constexpr int ST_FIT = (SMEM_LIMIT - RESERVE - OFF_RING) / STAGE_BYTES;
-  static constexpr int STAGES = ST_FIT > 8 ? 8 : ST_FIT;
-  // the tensor-memory-bound query chunks pass through ring stages 1.. first
-  static constexpr int OFF_STAGING = OFF_RING + STAGE_BYTES;
+  static constexpr int ST_FIT = (SMEM_LIMIT - RESERVE) / STAGE_BYTES;
+  static constexpr int STAGES = ST_FIT > 6 ? 6 : ST_FIT;
+  // the query passes through ring stages 1.. on its way to tensor memory
+  static constexpr int OFF_STAGING = STAGE_BYTES;
   static_assert(STAGES >= 3, "ring too small");
-  static_assert(OFF_STAGING + NQT * QCH_BYTES <= OFF_RING + STAGES * STAGE_BYTES, "staging overflows the ring");
-  static constexpr int OFF_BAR = OFF_RING + STAGES * STAGE_BYTES;
-  static constexpr int BAR_FULL = 0, BAR_EMPTY = STAGES, BAR_Q = 2 * STAGES, BAR_QST = BAR_Q + 1,
-                       BAR_QT = BAR_Q + 2, BAR_S = BAR_Q + 3, BAR_P = BAR_S + 2, BAR_PV = BAR_P + 2,
-                       BAR_DONE = BAR_PV + 1, NUM_BARS = BAR_DONE + 1;
+  static_assert(OFF_STAGING + NCH * QCH_BYTES <= STAGES * STAGE_BYTES, "staging overflows the ring");
+  static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
+  static constexpr int BAR_FULL = 0, BAR_EMPTY = STAGES, BAR_QST = 2 * STAGES, BAR_QT = BAR_QST + 1,
+                       BAR_S = BAR_QST + 2, BAR_SFREE = BAR_S + 1, BAR_P = BAR_S + 2, BAR_PV = BAR_S + 3,
+                       BAR_DONE = BAR_S + 4, NUM_BARS = BAR_DONE + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
-  static_assert(COL_Q + NQT * 32 <= COL_O, "tensor memory");
+  static_assert(COL_Q + NCH * 32 <= COL_S && COL_O + OC <= TMEM_COLS, "tensor memory");
 };
 
 struct MWork {
@@ -179,13 +177,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(C::BAR_FULL + s), 1);
       mbar_init(bar(C::BAR_EMPTY + s), 1);
     }
-    mbar_init(bar(C::BAR_Q), 1);
     mbar_init(bar(C::BAR_QST), 1);
     mbar_init(bar(C::BAR_QT), BM);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(C::BAR_S + b), 1);
-      mbar_init(bar(C::BAR_P + b), BM);
-    }
+    mbar_init(bar(C::BAR_S), 1);
+    mbar_init(bar(C::BAR_SFREE), BM);
+    mbar_init(bar(C::BAR_P), BM);
     mbar_init(bar(C::BAR_PV), 1);
     mbar_init(bar(C::BAR_DONE), 1);
     mbar_init_fence();
@@ -213,16 +209,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tm_kp);
       }
       const int gy = static_cast<int>(grow0);
-      auto load_q = [&](uint32_t dst, int c, uint32_t b) {
-        if (c < C::NCH_LAT) tma_load_2d(dst, &tm_q, b, c * 64, gy);
-        else tma_load_2d(dst, &tm_qp, b, (c - C::NCH_LAT) * 64, gy);
-      };
-      mbar_arrive_expect_tx(bar(C::BAR_QST), C::NQT * C::QCH_BYTES);
-      for (int c = 0; c < C::NQT; ++c) load_q(sb + C::OFF_STAGING + c * C::QCH_BYTES, c, bar(C::BAR_QST));
-      if constexpr (C::NQS > 0) {
-        mbar_arrive_expect_tx(bar(C::BAR_Q), C::NQS * C::QCH_BYTES);
-        for (int c = C::NQT; c < C::NCH; ++c)
-          load_q(sb + C::OFF_QS + (c - C::NQT) * C::QCH_BYTES, c, bar(C::BAR_Q));
+      mbar_arrive_expect_tx(bar(C::BAR_QST), C::NCH * C::QCH_BYTES);
+      for (int c = 0; c < C::NCH; ++c) {
+        const uint32_t dst = sb + C::OFF_STAGING + c * C::QCH_BYTES;
+        if (c < C::NCH_LAT) tma_load_2d(dst, &tm_q, bar(C::BAR_QST), c * 64, gy);
+        else tma_load_2d(dst, &tm_qp, bar(C::BAR_QST), (c - C::NCH_LAT) * 64, gy);
       }
       const int32_t* table = pp.block_table + static_cast<size_t>(w.s) * pp.max_pages;
       const int P = pp.page_size;
@@ -232,11 +223,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int issued = 0;
       for (int i = 0; i < n && ok; ++i, ++issued) {
         const int st = i % C::STAGES;
-        // stages 1.. hold the staged query chunks until they are in tensor memory
+        // stages 1.. hold the staged query until it is in tensor memory
         if (i == 1 && !mbar_wait(bar(C::BAR_QT), 0)) { ok = false; break; }
         if (!mbar_wait(bar(C::BAR_EMPTY + st), ((i / C::STAGES) & 1) ^ 1)) { ok = false; break; }
         mbar_arrive_expect_tx(bar(C::BAR_FULL + st), C::STAGE_BYTES);
-        const uint32_t base = sb + C::OFF_RING + st * C::STAGE_BYTES;
+        const uint32_t base = sb + st * C::STAGE_BYTES;
         for (int b = 0; b < boxes; ++b) {
           const int key = (w.t0 + i) * BN + b * box_rows;
           const int pidx = key / P;
@@ -256,7 +247,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait(bar(C::BAR_FULL + st), (fills - 1) & 1)) fail();
       }
       if (!mbar_wait(bar(C::BAR_QST), 0)) fail();
-      if (C::NQS > 0 && !mbar_wait(bar(C::BAR_Q), 0)) fail();
     }
     __syncwarp();
   } else if (warp == WARP_MMA) {
@@ -267,41 +257,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr int ST = C::STAGES;
       constexpr uint32_t STAGE16 = C::STAGE_BYTES >> 4;
       constexpr uint32_t KCH16 = C::KCH_BYTES >> 4;
-      constexpr uint32_t QCH16 = C::QCH_BYTES >> 4;
       constexpr uint32_t VSTEP16 = (16 * 128) >> 4;
       bool ok = mbar_wait(bar(C::BAR_QT), 0);
-      if (C::NQS > 0 && ok) ok = mbar_wait(bar(C::BAR_Q), 0);
       tc_fence_after();
-      const uint64_t dqs = smem_desc(sb + C::OFF_QS, 16, 1024, 2u);
-      const uint64_t dk = smem_desc(sb + C::OFF_RING, 16, 1024, 2u);
-      const uint64_t dv = smem_desc(sb + C::OFF_RING + w.h * (OC / 64) * C::KCH_BYTES, C::KCH_BYTES, 1024, 2u);
+      const uint64_t dk = smem_desc(sb, 16, 1024, 2u);
+      const uint64_t dv = smem_desc(sb + w.h * (OC / 64) * C::KCH_BYTES, C::KCH_BYTES, 1024, 2u);
       for (int i = 0; i <= n && ok; ++i) {
         if (i < n) {
           const int st = i % ST;
           if (!mbar_wait(bar(C::BAR_FULL + st), (i / ST) & 1)) { ok = false; break; }
+          // S is single-buffered: the softmax must have read S(i-1)
+          if (i > 0 && !mbar_wait(bar(C::BAR_SFREE), (i - 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d = tmem + COL_S + (i & 1) * BN;
           const uint64_t b0 = dk + st * STAGE16;
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bd = b0 + c * KCH16 + kk * 2;
-              if (c < C::NQT) umma_ts(d, tmem + COL_Q + c * 32 + kk * 8, bd, idesc_s, (c | kk) ? 1u : 0u);
-              else umma_ss(d, dqs + (c - C::NQT) * QCH16 + kk * 2, bd, idesc_s, 1u);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+              umma_ts(tmem + COL_S, tmem + COL_Q + c * 32 + kk * 8, b0 + c * KCH16 + kk * 2, idesc_s,
+                      (c | kk) ? 1u : 0u);
           }
-          umma_commit(bar(C::BAR_S + (i & 1)));
+          umma_commit(bar(C::BAR_S));
         }
         if (i >= 1) {
           const int j = i - 1;
-          if (!mbar_wait(bar(C::BAR_P + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+          if (!mbar_wait(bar(C::BAR_P), j & 1)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a = tmem + COL_S + (j & 1) * BN;
           const uint64_t b0 = dv + (j % ST) * STAGE16;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            umma_ts(tmem + COL_O, a + kk * 8, b0 + kk * VSTEP16, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_ts(tmem + COL_O, tmem + COL_P + kk * 8, b0 + kk * VSTEP16, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(C::BAR_PV));
           umma_commit(bar(C::BAR_EMPTY + j % ST));
         }
@@ -318,6 +303,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int64_t grow = grow0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tQ = tmem + lane_off + COL_Q;
+    const uint32_t tS = tmem + lane_off + COL_S;
+    const uint32_t tP = tmem + lane_off + COL_P;
     const uint32_t tO = tmem + lane_off + COL_O;
     const int tq = (w.row0 + r) / H;
     const int pos = !row_ok ? -1 : (pp.positions ? __ldg(pp.positions + w.q_lo + tq) : w.L - w.nq + tq);
@@ -325,14 +312,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int key_lim = w.L;
     const float sc = pp.scale_log2;
     bool failed = false;
-    // query chunks: staged shared memory (128-byte swizzled rows) -> tensor memory
+    // the query: staged shared memory (128-byte swizzled rows) -> tensor memory
     {
       const bool ok = mbar_wait(bar(C::BAR_QST), 0);
       if (__any_sync(0xffffffffu, !ok)) failed = true;
       if (!failed) {
         const uint8_t* row = smem + C::OFF_STAGING + r * 128;
 #pragma unroll 1
-        for (int c = 0; c < C::NQT; ++c) {
+        for (int c = 0; c < C::NCH; ++c) {
           uint32_t wd[32];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -351,19 +338,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     float m_run = -INFINITY, l_run = 0.f;
     for (int i = 0; i < n && !failed; ++i) {
-      const int b = i & 1;
-      const bool ok = mbar_wait(bar(C::BAR_S + b), (i >> 1) & 1);
+      const bool ok = mbar_wait(bar(C::BAR_S), i & 1);
       if (__any_sync(0xffffffffu, !ok)) { failed = true; break; }
       tc_fence_after();
-      const uint32_t tS = tmem + lane_off + COL_S + b * BN;
       float s[BN];
       {
-        uint32_t sr[32];
-        tmem_ld32(tS, sr);
+        uint32_t sr[2][32];
+        tmem_ld32(tS, sr[0]);
+        tmem_ld32(tS + 32, sr[1]);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < BN; ++k) s[k] = __uint_as_float(sr[k]);
+        for (int k = 0; k < BN; ++k) s[k] = __uint_as_float(sr[k >> 5][k & 31]);
       }
+      tc_fence_before();
+      mbar_arrive(bar(C::BAR_SFREE));  // the next tile's scores may overwrite S
       const int tile = w.t0 + i;
       if (tile >= w.nfull) {
         const int key0 = tile * BN;
@@ -375,11 +363,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       float c0 = fmax3(s[0], s[1], s[2]), c1 = fmax3(s[3], s[4], s[5]);
 #pragma unroll
-      for (int k = 6; k < 30; k += 4) {
+      for (int k = 6; k < 62; k += 4) {
         c0 = fmax3(c0, s[k], s[k + 1]);
         c1 = fmax3(c1, s[k + 2], s[k + 3]);
       }
-      const float m_tile = fmax3(c0, c1, fmaxf(s[30], s[31])) * sc;
+      const float m_tile = fmax3(c0, c1, fmaxf(s[62], s[63])) * sc;
       const bool need = m_tile > m_run + RESCALE_LOG2;
       float alpha = 1.f;
       if (need) {
@@ -389,9 +377,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
       float2 sum_a = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
-      uint32_t pk[16];
+      uint32_t pk[32];
 #pragma unroll
-      for (int k = 0; k < 16; k += 2) {
+      for (int k = 0; k < 32; k += 2) {
         const float2 xa = ffma2(make_float2(s[2 * k], s[2 * k + 1]), make_float2(sc, sc), make_float2(neg_m, neg_m));
         const float2 xb =
             ffma2(make_float2(s[2 * k + 2], s[2 * k + 3]), make_float2(sc, sc), make_float2(neg_m, neg_m));
@@ -402,32 +390,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         pk[k] = pack2<BF16>(pa.x, pa.y);
         pk[k + 1] = pack2<BF16>(pb.x, pb.y);
       }
-      tmem_st16(tS, pk);
       l_run += (sum_a.x + sum_a.y) + (sum_b.x + sum_b.y);
-      if (i > 0 && __any_sync(0xffffffffu, need)) {
-        // O holds the earlier tiles relative to the old maximum: rescale it
-        // once their last P . V (issued before this tile's) has finished
+      // P is single-buffered and O is read by P . V: wait for the previous one
+      if (i > 0) {
         const bool pv = mbar_wait(bar(C::BAR_PV), (i - 1) & 1);
         if (__any_sync(0xffffffffu, !pv)) { failed = true; break; }
         tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {  // O holds earlier tiles relative to the old maximum
 #pragma unroll 1
-        for (int c = 0; c < OC / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * c, o);
-          tmem_wait_ld();
+          for (int c = 0; c < OC / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            const float2 x = fmul2(make_float2(__uint_as_float(o[k]), __uint_as_float(o[k + 1])),
-                                   make_float2(alpha, alpha));
-            o[k] = __float_as_uint(x.x);
-            o[k + 1] = __float_as_uint(x.y);
+            for (int k = 0; k < 32; k += 2) {
+              const float2 x = fmul2(make_float2(__uint_as_float(o[k]), __uint_as_float(o[k + 1])),
+                                     make_float2(alpha, alpha));
+              o[k] = __float_as_uint(x.x);
+              o[k + 1] = __float_as_uint(x.y);
+            }
+            tmem_st32(tO + 32 * c, o);
           }
-          tmem_st32(tO + 32 * c, o);
         }
       }
+      tmem_st32(tP, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(C::BAR_P + b));
+      mbar_arrive(bar(C::BAR_P));
     }
     // ---------------------------------------------------------------- epilogue
     if (!failed) {

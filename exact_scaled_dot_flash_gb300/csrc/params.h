@@ -106,7 +106,7 @@ inline bool paged_is_decode(int max_queries, int group) { return static_cast<lon
 // MLA over a paged latent cache (PagedParams with Hq = heads, Hkv = 1).
 namespace mlatc {
 // Tensor-core MLA (F16/BF16, R in {256, 512}, Pd in {0, 64}, page_size a
-// multiple of 8 dividing 32 or a multiple of 32); splits by pp.num_splits.
+// multiple of 8 dividing 64 or a multiple of 64); splits by pp.num_splits.
 template <int R, int PD, bool BF16>
 cudaError_t launch_mla_tc(EncodeTiledFn enc, const PagedParams& pp, const void* q, const void* qp, const void* lat,
                           const void* kp, void* out, float* lse, cudaStream_t stream);

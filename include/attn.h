@@ -303,8 +303,8 @@ typedef struct {
  * num_splits > 1 a workspace of attn_paged_mla_workspace_bytes(shape,
  * num_splits) bytes is required (16-byte aligned, disjoint from every other
  * buffer); calls that run on the fp32 FMA kernel (F32, R = 128, Pd in
- * {16, 32}, or page sizes that are not a multiple of 8 dividing 32 or a
- * multiple of 32) ignore the splits. Asynchronous on `stream`; returns ATTN_OK
+ * {16, 32}, or page sizes that are not a multiple of 8 dividing 64 or a
+ * multiple of 64) ignore the splits. Asynchronous on `stream`; returns ATTN_OK
  * or a negative ATTN_ERR_* code. */
 ATTN_API int attn_paged_mla(const attn_mla_shape_t* shape,
                             const void* q, const void* qp,

@@ -75,8 +75,9 @@ def test_mla_matches_oracle(w):
 
 
 # Tensor-core kernel (F16/BF16, R in {256, 512}, Pd in {0, 64}, page sizes
-# 8, 16 or multiples of 32): 128-row blocks of (query, head) rows, one CTA per
-# 256-column output slice, 32-key tiles; several tiles and a ragged last tile.
+# 8, 16, 32 or multiples of 64): 128-row blocks of (query, head) rows, one CTA
+# per 128-column output slice, 64-key tiles; several tiles and a ragged last
+# tile.
 TC_CASES = [
     MW("mla_tc_bf16_r512_p64_h128_decode", "bf16", 5, 128, 512, 64, 64, (1, 700), (1, 1), seed=11),
     MW("mla_tc_bf16_r512_p64_h16_p8", "bf16", 4, 16, 512, 64, 8, (30, 400), (1, 3), seed=12),
@@ -84,7 +85,7 @@ TC_CASES = [
     MW("mla_tc_bf16_r256_p64_p16_positions", "bf16", 4, 8, 256, 64, 16, (1, 300), (1, 40), seed=14,
        explicit_positions=True),
     MW("mla_tc_f16_r256_p0_p128_noncausal", "f16", 3, 32, 256, 0, 128, (40, 600), (1, 9), seed=15, causal=False),
-    MW("mla_tc_bf16_r512_p64_prefill_p96", "bf16", 2, 8, 512, 64, 96, (150, 420), (40, 150), seed=16),
+    MW("mla_tc_bf16_r512_p64_prefill_p192", "bf16", 2, 8, 512, 64, 192, (150, 420), (40, 150), seed=16),
 ]
 
 
@@ -121,9 +122,12 @@ def test_mla_tensor_core_edges():
 
 
 def test_mla_splits_ignored_on_fma_path():
-    # the fp32 FMA kernel (here F32) takes the workspace but does not split
+    # the fp32 FMA kernel (here F32, and a page size of 96) takes the workspace
+    # but does not split
     w = MW("mla_f32_split", "f32", 3, 4, 128, 16, 8, (1, 120), (1, 4), seed=62)
     check(w, num_splits=4)
+    w2 = MW("mla_bf16_p96_split", "bf16", 2, 8, 512, 64, 96, (150, 420), (1, 3), seed=63)
+    check(w2, num_splits=3)
 
 
 def test_mla_workspace_errors():
