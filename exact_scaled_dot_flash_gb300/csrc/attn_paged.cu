@@ -1,5 +1,7 @@
 // attn_paged.cu - attention over a paged key/value cache with packed
-// variable-length queries, fp32 FMA arithmetic for every dtype.
+// variable-length queries, fp32 FMA arithmetic: the calls the tensor-core
+// kernel (attn_paged_tc.cuh) does not take (F32, D in {16, 32}, page sizes
+// its tile gathers do not cover).
 //
 // Source: ruDNN user guide, section 9 (paged attention): the kernel reads the
 // physical cache pages directly (K and V [pages, page_size, Hkv, D]) through

@@ -216,10 +216,14 @@ ATTN_API int attn_bwd_workspace_bytes(const attn_shape_t* shape, size_t* bytes);
  *   q, out  [num_queries, Hq, D]           packed queries, sequence by sequence
  *   k_cache, v_cache [num_pages, page_size, Hkv, D]   physical pages
  *   block_table [num_seqs, max_pages] int32   physical page of key block b of sequence s
- *   max_queries: an upper bound on the queries of one sequence (sizes the grid
- *   and picks the kernel: at most 8 rows of queries x (Hq/Hkv) heads per
- *   sequence and kv head take the decode kernel). Rows beyond a bound that is
- *   too small are not written. */
+ *   max_queries: an upper bound on the queries of one sequence (sizes the grid;
+ *   a call with at most 8 rows of queries x (Hq/Hkv) heads per sequence and kv
+ *   head is decode-shaped, the only shape that splits). Rows beyond a bound
+ *   that is too small are not written.
+ * F16/BF16 calls with D in {64, 128} and a page size that is a multiple of 8
+ * dividing 128 or a multiple of 128 run on the tensor cores, the query heads
+ * of a GQA group packed into the rows of one tile; the rest on fp32 FMA
+ * kernels. */
 typedef struct {
   int32_t num_seqs, num_queries, Hq, Hkv, D;
   int32_t page_size, num_pages, max_pages, max_queries;
