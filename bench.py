@@ -355,7 +355,9 @@ def bench_gpu(args):
         d2h = oh.numel() * oh.element_size()
         e2e = {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
-               "path": "attn.fwd on pinned host tensors: H2D copies, attn_fwd, D2H copy, sync"}
+               "path": ("attn.fwd on pinned host tensors -> attn_fwd_host: chunked H2D copies, attn_fwd per "
+                        "chunk and D2H copies overlapped on three streams, sync") if splits == 1 else
+                       "attn.fwd_split on device copies made inside the step: H2D, attn_fwd_split, D2H, sync"}
 
     if rank != 0:
         return

@@ -90,6 +90,12 @@ def load_library():
         lib.attn_paged_mla_workspace_bytes.argtypes = [ctypes.POINTER(MlaShape), ctypes.c_int,
                                                        ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_paged_mla_workspace_bytes.restype = ctypes.c_int
+        lib.attn_fwd_host.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, ctypes.c_int, vp, vp, ctypes.c_float,
+                                      ctypes.c_int, vp, ctypes.c_size_t, vp, vp]
+        lib.attn_fwd_host.restype = ctypes.c_int
+        lib.attn_fwd_host_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.c_int, ctypes.c_int,
+                                                      ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_fwd_host_workspace_bytes.restype = ctypes.c_int
         lib.attn_strerror.argtypes = [ctypes.c_int]
         lib.attn_strerror.restype = ctypes.c_char_p
         lib.attn_last_cuda_error.argtypes = []
@@ -172,9 +178,10 @@ def fwd(q, k, v, *, causal: bool = False, kv_lens=None, bias=None, scale: float 
     taken from ``workspace`` (a CUDA uint8 tensor) or allocated here.
     return_lse: also return the float32 [B,Hq,Sq] row log-sum-exp.
     Tensors on a CUDA device run on ``stream`` (default: the current stream)
-    and the result is returned without synchronising. Host tensors are copied
-    to the current CUDA device, computed there, and the result is copied back
-    (synchronising); pinned host memory makes the copies asynchronous DMA.
+    and the result is returned without synchronising. Host tensors run through
+    attn_fwd_host on the current CUDA device (chunked uploads, kernels and
+    downloads overlapped; synchronising); pinned host memory makes the copies
+    asynchronous DMA.
     """
     import torch
 
@@ -239,20 +246,62 @@ def fwd(q, k, v, *, causal: bool = False, kv_lens=None, bias=None, scale: float 
     return (out, lse) if return_lse else out
 
 
-def _fwd_host(q, k, v, *, causal, kv_lens, bias, scale, out):
-    """Host tensors in, host tensor out: H2D copies, the GPU kernel, a D2H copy."""
+def host_workspace_bytes(shape: Shape, dtype_code: int, with_bias: bool) -> int:
+    """Device workspace attn_fwd_host needs for ``shape``."""
+    n = ctypes.c_size_t(0)
+    check(load_library().attn_fwd_host_workspace_bytes(ctypes.byref(shape), int(dtype_code), int(bool(with_bias)),
+                                                      ctypes.byref(n)))
+    return n.value
+
+
+def _fwd_host(q, k, v, *, causal, kv_lens, bias, scale, out, workspace=None):
+    """Host tensors in, host tensor out (attn_fwd_host): chunked uploads, the
+    kernel per chunk and downloads overlapped on three streams; synchronises."""
     import torch
 
-    dev = torch.device("cuda", torch.cuda.current_device())
-
-    def up(t):
-        return None if t is None else t.to(dev, non_blocking=True)
-
-    o_dev = fwd(up(q), up(k), up(v), causal=causal, kv_lens=up(kv_lens), bias=up(bias), scale=scale)
+    for name, t in (("k", k), ("v", v), ("kv_lens", kv_lens), ("bias", bias), ("out", out)):
+        if t is not None and t.device.type != "cpu":
+            raise AttnError(f"{name} must be a host tensor like q")
+    for name, t in (("k", k), ("v", v)):
+        if t.dtype != q.dtype:
+            raise AttnError(f"{name} dtype {t.dtype} differs from q dtype {q.dtype}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dim() != 4 or not t.is_contiguous():
+            raise AttnError(f"{name} must be a contiguous 4-D [B, H, S, D] tensor")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    if tuple(k.shape) != (B, Hkv, Sk, D) or tuple(v.shape) != tuple(k.shape):
+        raise AttnError("k and v must be [B, Hkv, Sk, D] matching q")
+    mask = MASK_CAUSAL if causal else MASK_NONE
+    if kv_lens is not None:
+        if kv_lens.dtype != torch.int32 or tuple(kv_lens.shape) != (B,) or not kv_lens.is_contiguous():
+            raise AttnError("kv_lens must be a contiguous int32 [B] host tensor")
+        mask |= MASK_KEY_PADDING
+    bb = bh = 1
+    if bias is not None:
+        if bias.dtype != torch.float32 or bias.dim() != 4 or not bias.is_contiguous() or \
+                tuple(bias.shape[2:]) != (Sq, Sk):
+            raise AttnError("bias must be a contiguous float32 [bias_b, bias_h, Sq, Sk] host tensor")
+        bb, bh = int(bias.shape[0]), int(bias.shape[1])
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
-    out.copy_(o_dev, non_blocking=True)
-    torch.cuda.current_stream(dev).synchronize()
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise AttnError("out must be a contiguous host tensor like q")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    shape = Shape(B, Hq, Hkv, Sq, Sk, D, bb, bh)
+    need = host_workspace_bytes(shape, _dtype_code(q), bias is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    elif workspace.device != dev or workspace.numel() * workspace.element_size() < need:
+        raise AttnError(f"workspace must hold {need} bytes on the current device")
+    stream = torch.cuda.current_stream(dev)
+    ptr = lambda t: (t.data_ptr() or None) if t is not None else None
+    check(load_library().attn_fwd_host(ctypes.byref(shape), ptr(q), ptr(k), ptr(v), mask, ptr(kv_lens), ptr(bias),
+                                       ctypes.c_float(scale), _dtype_code(q), ptr(workspace) if need else None, need,
+                                       ptr(out), stream.cuda_stream or None))
+    stream.synchronize()
     return out
 
 

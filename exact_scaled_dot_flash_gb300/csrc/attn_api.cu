@@ -63,6 +63,12 @@ int fail_cuda(cudaError_t e) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+int attn::record_cuda_error(cudaError_t e) { return fail_cuda(e); }
+
+namespace {
+
 bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
   if (!a || !b || na <= 0 || nb <= 0) return false;
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
@@ -114,7 +120,7 @@ const char* attn_strerror(int code) {
     case ATTN_ERR_CUDA: return "CUDA call failed";
     case ATTN_ERR_TIMEOUT: return "a kernel wait timed out";
     case ATTN_ERR_SPLITS: return "num_splits must be in [1, 32]";
-    case ATTN_ERR_WORKSPACE: return "split workspace is NULL or smaller than attn_split_workspace_bytes";
+    case ATTN_ERR_WORKSPACE: return "workspace is NULL or smaller than its *_workspace_bytes query";
     case ATTN_ERR_SCRATCH:
       return "problem needs more split scratch than ATTN_NOALLOC_SCRATCH_BYTES (use fewer splits or a workspace)";
     default: return "unknown status code";

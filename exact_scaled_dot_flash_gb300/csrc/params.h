@@ -129,5 +129,7 @@ cudaError_t launch_split_merge(const KernelParams& p, int D, int dtype, void* ou
                                cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(int* status, unsigned long long limit_ns,
                                       cudaStream_t stream);
+// Records a failed CUDA call for attn_last_cuda_error(); returns ATTN_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
 
 }  // namespace attn

@@ -386,6 +386,44 @@ ATTN_API int attn_last_cuda_error(void);
  * Returns ATTN_OK, ATTN_ERR_NULL or ATTN_ERR_CUDA. */
 ATTN_API int attn_device_status(int device, int* flags, int clear);
 
+/* attn_fwd_host - attn_fwd on tensors in HOST memory: q, k, v, kv_lens, bias
+ * and out are host pointers with attn_fwd's layouts and rules; the result is
+ * identical to attn_fwd on device copies of the same inputs. (The pages have
+ * no counterpart; this is the library's executor for host-resident tensors.)
+ *
+ * The problem is cut into chunks of whole (batch, kv head) units (about 8 in
+ * all); two chunk slots live in `workspace` (device memory of at least
+ * attn_fwd_host_workspace_bytes(shape, dtype, bias != NULL) bytes, 16-byte
+ * aligned, owned by the caller). The upload of chunk c+1 (a library copy
+ * stream), the attention of chunk c (on `stream`) and the download of chunk
+ * c-1 (a second library copy stream) run at the same time; `stream` is
+ * ordered after every copy when the call returns, so `out` is complete, and
+ * the inputs may be released, once `stream` has completed. Pinned (page-locked)
+ * host buffers make the copies asynchronous DMA; pageable ones work but the
+ * copies then block the calling thread.
+ *
+ * Calls on one device are enqueued one at a time (a per-device lock); calls in
+ * flight at once need separate workspaces. Allocates no device memory; creates
+ * two streams and seven events per device on first use, kept until the
+ * process exits. Returns ATTN_OK or a negative ATTN_ERR_* code (argument
+ * errors before anything is enqueued; ATTN_ERR_WORKSPACE for a missing or
+ * small workspace). */
+ATTN_API int attn_fwd_host(const attn_shape_t* shape,
+                           const void* q, const void* k, const void* v,
+                           int mask_kind, const int32_t* kv_lens,
+                           const float* bias,
+                           float scale, attn_dtype_t dtype,
+                           void* workspace, size_t workspace_bytes,
+                           void* out,
+                           void* stream);
+
+/* attn_fwd_host_workspace_bytes - device workspace attn_fwd_host needs for
+ * `shape`, `dtype` and whether a bias is passed (0 when B or Sq is 0): the
+ * kv_lens array and two slots for the largest chunk's Q, K, V, O and bias.
+ * Returns ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_DTYPE or ATTN_ERR_SHAPE. */
+ATTN_API int attn_fwd_host_workspace_bytes(const attn_shape_t* shape, attn_dtype_t dtype, int with_bias,
+                                           size_t* bytes);
+
 /* attn_selftest_wait_timeout - failure-path self-test (the pages have no
  * counterpart; it checks this library's own error reporting). Launches, on
  * `stream`, a one-thread kernel that waits on an mbarrier phase nothing

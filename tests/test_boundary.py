@@ -206,3 +206,59 @@ def test_library_exports_only_the_c_abi(lib):
     names = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
     names = {n for n in names if not n.startswith("_")}  # linker-provided markers
     assert names == set(declared_functions())
+
+
+def _host_ws(lib, shape, dtype=A.ATTN_BF16, bias=False):
+    n = ctypes.c_size_t(0)
+    rc = lib.attn_fwd_host_workspace_bytes(ctypes.byref(shape), dtype, int(bias), ctypes.byref(n))
+    return rc, n.value
+
+
+def test_host_workspace_holds_two_chunk_slots(lib):
+    # headline-sized problem: 4 batches x 32 kv heads in 8 chunks of 16 heads
+    rc, n = _host_ws(lib, _shape(B=4, Hq=32, Hkv=32, Sq=4096, Sk=4096, D=128))
+    assert rc == 0
+    chunk = 16 * 4096 * 128 * 2                       # Q, K, V or O of one chunk
+    assert 2 * 4 * chunk <= n <= 2 * 4 * chunk + 4096   # two slots of Q, K, V, O (+ padding)
+    # a per-head bias adds one bias slice per slot; a broadcast bias one row block
+    rc, nb = _host_ws(lib, _shape(B=4, Hq=32, Hkv=32, Sq=512, Sk=512, D=64, bb=1, bh=32), bias=True)
+    rc0, n0 = _host_ws(lib, _shape(B=4, Hq=32, Hkv=32, Sq=512, Sk=512, D=64))
+    assert rc == rc0 == 0 and nb - n0 >= 2 * 16 * 512 * 512 * 4
+    rc, n1 = _host_ws(lib, _shape(B=4, Hq=32, Hkv=32, Sq=512, Sk=512, D=64, bb=4, bh=1), bias=True)
+    assert rc == 0 and 2 * 512 * 512 * 4 <= n1 - n0 < 2 * 16 * 512 * 512 * 4
+    # GQA: a chunk carries whole groups of query heads
+    rc, ng = _host_ws(lib, _shape(B=1, Hq=32, Hkv=8, Sq=256, Sk=1024, D=128))
+    assert rc == 0 and ng >= 2 * (2 * 4 * 256 * 128 * 2 + 2 * 1024 * 128 * 2)
+    # F32 doubles the element size
+    rc, nf = _host_ws(lib, _shape(B=2, Hq=4, Hkv=4, Sq=64, Sk=64, D=64), dtype=A.ATTN_F32)
+    rc2, nh = _host_ws(lib, _shape(B=2, Hq=4, Hkv=4, Sq=64, Sk=64, D=64), dtype=A.ATTN_F16)
+    assert rc == rc2 == 0 and nf > nh
+
+
+def test_host_workspace_errors_and_empty(lib):
+    assert _host_ws(lib, _shape(B=0))[1] == 0 and _host_ws(lib, _shape(B=0))[0] == 0
+    assert _host_ws(lib, _shape(Sq=0)) == (0, 0)
+    assert _host_ws(lib, _shape(Hq=3, Hkv=2))[0] == codes["ATTN_ERR_SHAPE"]
+    assert _host_ws(lib, _shape(B=2, bb=3), bias=True)[0] == codes["ATTN_ERR_SHAPE"]
+    assert _host_ws(lib, _shape(), dtype=7)[0] == codes["ATTN_ERR_DTYPE"]
+    n = ctypes.c_size_t(0)
+    assert lib.attn_fwd_host_workspace_bytes(None, 0, 0, ctypes.byref(n)) == codes["ATTN_ERR_NULL"]
+
+
+def test_host_call_argument_errors(lib):
+    # rejected before any CUDA call (host pointers never dereferenced)
+    s = _shape(B=2, Hq=2, Hkv=2, Sq=8, Sk=8, D=64)
+    rc, need = _host_ws(lib, s)
+
+    def call(shape=s, ws=FAKE, nbytes=need, out=FAKE * 8, scale=0.125, dtype=A.ATTN_BF16, mask=0):
+        return lib.attn_fwd_host(ctypes.byref(shape), FAKE, FAKE * 2, FAKE * 3, mask, None, None,
+                                 ctypes.c_float(scale), dtype, ws, nbytes, out, None)
+    assert call(ws=None) == codes["ATTN_ERR_WORKSPACE"]
+    assert call(nbytes=need - 1) == codes["ATTN_ERR_WORKSPACE"]
+    assert call(ws=FAKE + 4) == codes["ATTN_ERR_ALIGN"]
+    assert call(out=FAKE) == codes["ATTN_ERR_OVERLAP"]
+    assert call(scale=-1.0) == codes["ATTN_ERR_SCALE"]
+    assert call(mask=A.MASK_KEY_PADDING) == codes["ATTN_ERR_MASK"]
+    assert call(shape=_shape(B=2, D=48)) == codes["ATTN_ERR_HEAD_DIM"]
+    assert call(out=None) == codes["ATTN_ERR_NULL"]
+    assert call(shape=_shape(B=0)) == 0
