@@ -183,38 +183,43 @@ def bench_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    w = synth.WORKLOADS[WORKLOAD]
+    w = synth.WORKLOADS[args.workload]
     x = synth.make_inputs(w)
     wid = oracle.prepare(x["q"], x["k"], x["v"], kv_lens=x["kv_lens"], bias=x["bias"], dtype=w.dtype)
-    # per step: the last `nrows` query rows of head (0, 0) -- the heaviest causal rows
-    rows_all = np.array([(0, 0, i) for i in range(w.Sq)], dtype=np.int64)
+    threads = args.threads if args.threads > 0 else os.cpu_count()
+    # per step: the last `nrows` query rows of every head of batch 0 in turn
+    # (for causal workloads the last rows are the heaviest)
+    rows_all = np.array([(0, h, i) for h in range(w.Hq) for i in range(w.Sq)], dtype=np.int64)
+    L0 = min(max(int(x["kv_lens"][0]), 0), w.Sk) if x["kv_lens"] is not None else w.Sk
 
-    def flops_of(rows):
-        return float(sum(4.0 * (r[2] + 1) * w.D for r in rows))  # causal: row i sees i+1 keys
+    def flops_of(rows):  # exact: 4 D FLOP per visible (query, key) pair
+        vis = [min(L0, int(r[2]) + w.Sk - w.Sq + 1) if w.causal else L0 for r in rows]
+        return float(sum(4.0 * max(n, 0) * w.D for n in vis))
 
     probe = rows_all[-64:]
     t0 = time.perf_counter()
-    oracle.attention_rows(None, None, None, probe, mask=w.mask, scale=x["scale"], widened=wid)
+    oracle.attention_rows(None, None, None, probe, mask=w.mask, scale=x["scale"], widened=wid, threads=threads)
     tp = max(time.perf_counter() - t0, 1e-4)
     budget = 90.0 / max(1, args.steps + args.warmup)
-    nrows = int(max(16, min(w.Sq, 64 * budget / tp)))
+    nrows = int(max(16, min(len(rows_all), 64 * budget / tp)))
     rows = rows_all[-nrows:]
     for _ in range(args.warmup):
-        oracle.attention_rows(None, None, None, rows, mask=w.mask, scale=x["scale"], widened=wid)
+        oracle.attention_rows(None, None, None, rows, mask=w.mask, scale=x["scale"], widened=wid, threads=threads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.attention_rows(None, None, None, rows, mask=w.mask, scale=x["scale"], widened=wid)
+        oracle.attention_rows(None, None, None, rows, mask=w.mask, scale=x["scale"], widened=wid, threads=threads)
     dt = time.perf_counter() - t0
     value = flops_of(rows) * args.steps / dt / 1e12
-    sample = (f"the last {nrows} query rows of head (0,0) of {w.name} per step (all their visible "
-              f"keys), float64 oracle on {os.cpu_count()} threads")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+    sample = (f"the last {nrows} query rows of batch 0 of {w.name} per step (all their visible "
+              f"keys), float64 oracle on {threads} threads")
+    metric = METRIC if w.name == WORKLOAD else f"attention fwd TFLOP/s ({w.name})"
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
-                       "D": w.D, "causal": True},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                       "D": w.D, "causal": w.causal},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -263,8 +268,9 @@ def bench_gpu(args):
         ws = torch.empty(attn.split_workspace_bytes(shp, splits), dtype=torch.uint8, device=device)
 
     def step():
-        attn.fwd(q, k, v, causal=causal, kv_lens=lens, bias=bias, scale=scale, out=out, stream=stream,
-                 num_splits=splits, workspace=ws)
+        # the current stream: the bench's own, or the capture stream of a CUDA graph
+        attn.fwd(q, k, v, causal=causal, kv_lens=lens, bias=bias, scale=scale, out=out,
+                 stream=torch.cuda.current_stream(device), num_splits=splits, workspace=ws)
 
     bwd_bufs = None
     if args.pass_ == "bwd":
@@ -293,18 +299,43 @@ def bench_gpu(args):
     attn.device_status(device.index, clear=True)
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    graph = None
+    if args.graph:  # the K steps captured once, replayed as one graph launch
+        if args.pass_ != "fwd" or args.l2_flush:
+            raise SystemExit("--graph times the forward without --l2-flush")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(args.steps):
+                step()
+        torch.cuda.synchronize()
+        graph.replay()  # one untimed replay
+        torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device) if args.l2_flush else None
+    per_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)] if args.l2_flush else None
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     smi_id = vis.split(",")[device.index] if vis else str(device.index)
     with ClockSampler(smi_id) as clocks:
         barrier()
         torch.cuda.synchronize()
-        start.record(stream)
-        for _ in range(args.steps):
-            step()
-        end.record(stream)
+        if per_step:  # each step timed alone, 256 MiB written between steps to evict L2
+            for s_ev, e_ev in per_step:
+                flush.zero_()
+                s_ev.record(stream)
+                step()
+                e_ev.record(stream)
+        else:
+            start.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                for _ in range(args.steps):
+                    step()
+            end.record(stream)
         torch.cuda.synchronize()
         barrier()
-    elapsed_ms = start.elapsed_time(end)
+    elapsed_ms = (sum(s_ev.elapsed_time(e_ev) for s_ev, e_ev in per_step) if per_step
+                  else start.elapsed_time(end))
     status = attn.device_status(device.index, clear=True)
     if status:
         raise RuntimeError(f"kernel status flags {status:#x} during the timed region")
@@ -375,9 +406,12 @@ def bench_gpu(args):
                    "causal": w.causal, "key_padding": bool(w.mask & synth.MASK_KEY_PADDING),
                    "bias": [w.bias_b, w.bias_h] if w.bias else None, "parallelism": f"replicas x{world}",
                    "num_splits": splits, "flops_basis": flops_basis,
-                   "l2": (f"inputs larger than L2: {w.io_bytes() / 2**20:.0f} MiB per step vs 129 MB L2, no flush"
+                   "l2": ("L2 flushed: 256 MiB written between timed steps, each step timed alone"
+                          if args.l2_flush else
+                          f"inputs larger than L2: {w.io_bytes() / 2**20:.0f} MiB per step vs 129 MB L2, no flush"
                           if w.io_bytes() > 129e6 else
-                          f"working set {w.io_bytes() / 2**20:.1f} MiB fits in L2 (L2-hot steps)")},
+                          f"working set {w.io_bytes() / 2**20:.1f} MiB fits in L2 (L2-hot steps)"),
+                   "launch": "CUDA graph of the K steps, one replay" if graph is not None else "eager"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_kind": f"{peak_kind} bf16 dense burst",
@@ -558,6 +592,12 @@ def main():
                     help="time the forward (default) or the backward (attn_bwd) of the workload")
     ap.add_argument("--splits", type=int, default=0,
                     help="key-range splits (attn_fwd_split); 0 = the workload's default")
+    ap.add_argument("--threads", type=int, default=0,
+                    help="host threads of the reference arm's oracle (0 = all cores)")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the K forward steps in a CUDA graph and time one replay")
+    ap.add_argument("--l2-flush", action="store_true",
+                    help="write 256 MiB between steps and time each step alone (L2-cold inputs)")
     args = ap.parse_args()
     paged = args.workload in synth.PAGED_WORKLOADS or args.workload in synth.MLA_WORKLOADS
     if args.impl == "reference" and paged:
