@@ -58,6 +58,23 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's ``value`` (a replicated job takes as long as
+    its slowest rank); ``value`` itself outside a multi-rank process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(work_per_rank: float, max_seconds: float, world: int) -> float:
+    """Whole-job throughput of ``world`` replicas that each do ``work_per_rank``."""
+    return world * work_per_rank / max_seconds
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -339,16 +356,12 @@ def bench_gpu(args):
     status = attn.device_status(device.index, clear=True)
     if status:
         raise RuntimeError(f"kernel status flags {status:#x} during the timed region")
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, device)
     ms = elapsed_ms / args.steps
     flops, flops_basis = step_flops(w)
     if args.pass_ == "bwd":  # nominal backward work: 2.5x the forward's (5 matmuls for 2)
         flops, flops_basis = 2.5 * flops, "2.5 x forward (" + flops_basis + ")"
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = replica_throughput(flops, ms * 1e-3, world) / 1e12
 
     # end to end through the public API with host buffers (pinned), copies inside
     e2e = None
@@ -377,14 +390,10 @@ def bench_gpu(args):
             e2e_step()
         torch.cuda.synchronize()
         e2e_s = (time.perf_counter() - t0) / e2e_steps
-        if world > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([e2e_s], device=device)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_s = float(tt.item())
+        e2e_s = max_over_ranks(e2e_s, device)
         h2d = sum(a.numel() * a.element_size() for a in hosts if a is not None)
         d2h = oh.numel() * oh.element_size()
-        e2e = {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": replica_throughput(flops, e2e_s, world) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
                "path": ("attn.fwd on pinned host tensors -> attn_fwd_host: chunked H2D copies, attn_fwd per "
                         "chunk and D2H copies overlapped on three streams, sync") if splits == 1 else
@@ -512,11 +521,7 @@ def bench_paged(args):
     elapsed_ms = start.elapsed_time(end)
     if attn.device_status(device.index, clear=True):
         raise RuntimeError("kernel status flags set during the timed region")
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, device)
     ms = elapsed_ms / args.steps
     # exact work: 4*D FLOP per visible (query, key) pair and query head
     pairs = 0
@@ -533,7 +538,7 @@ def bench_paged(args):
     else:
         flops = 4.0 * w.D * w.Hq * pairs
         nbytes = (2 * nkt * w.Hkv * w.D + 2 * nqt * w.Hq * w.D) * es
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = replica_throughput(flops, ms * 1e-3, world) / 1e12
     if rank != 0:
         return
     peaks, peak_kind = load_peaks()
