@@ -117,6 +117,23 @@ __device__ __forceinline__ void tmem_st_packed64(uint32_t taddr, const float* x)
 }
 
 // Store D/2 fp32 values (one thread's half row) to global memory in 16-bit.
+// Linear CTA index -> (tile rank, head) over a grid of (tiles, heads): heads
+// are taken HEAD_GROUP at a time, and inside a group the tiles of all its heads
+// are interleaved by rank, rank 0 first. The kernels map rank 0 to their
+// heaviest causal tile, so the longest CTAs start first across the whole grid
+// while the tiles a group's CTAs share stay in L2.
+constexpr int HEAD_GROUP = 16;
+__device__ __forceinline__ void cta_order(int& rank, int& head) {
+  const int ntiles = static_cast<int>(gridDim.x), nheads = static_cast<int>(gridDim.y);
+  const int lin = static_cast<int>(blockIdx.y) * ntiles + static_cast<int>(blockIdx.x);
+  const int per_group = ntiles * HEAD_GROUP;
+  const int g = lin / per_group;
+  const int within = lin - g * per_group;
+  const int hg = min(HEAD_GROUP, nheads - g * HEAD_GROUP);
+  rank = within / hg;
+  head = g * HEAD_GROUP + (within - rank * hg);
+}
+
 template <bool BF16, int N>
 __device__ __forceinline__ void store_row16(void* dst, const float* x, float mul) {
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -143,8 +160,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work: 128 keys of one (b, kv head); every query tile that sees them
-  const int kb = blockIdx.x;
-  const int bhk = blockIdx.y;
+  // (causal: the first key blocks see the most query tiles, so they start first)
+  int kb, bhk;
+  cta_order(kb, bhk);
   const int b = bhk / p.Hkv, hk = bhk - b * p.Hkv;
   const int key0 = kb * BR;
   int lim = p.Sk;
@@ -428,8 +446,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   // ---- work: 128 query rows of one (b, query head); the key tiles they see
   // causal: the last query tiles see the most keys, so they start first
-  const int qt = p.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int bh = blockIdx.y;
+  int rank, bh;
+  cta_order(rank, bh);
+  const int qt = p.causal ? static_cast<int>(gridDim.x) - 1 - rank : rank;
   const int b = bh / p.Hq, hq = bh - b * p.Hq;
   const int bhk = b * p.Hkv + hq / p.group;
   const int q0 = qt * BR;
