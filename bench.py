@@ -37,9 +37,10 @@ METRIC = "attention fwd TFLOP/s and % of GB300 BF16 peak (causal, S=4096, D=128)
 KERNEL_NAME = "attn_fwd_tc_kernel"
 # key-range splits per workload (1 when absent): enough CTAs for 152 SMs
 SPLITS = {"bf16_gqa_chunk_32k": 4}
-# key-range splits of the serving workloads (1 when absent): MLA decode has only
-# 64 x 4 CTAs of 128 rows without them; paged decode already has 512 CTAs
-PAGED_SPLITS = {"bf16_mla_decode": 2}
+# key-range splits of the serving workloads (1 when absent): with the decode
+# kernels' longest-sequence-first order neither decode workload gains from splits
+# (MLA decode: 218 us unsplit, 232 us with 2, 257 us with 4)
+PAGED_SPLITS = {}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

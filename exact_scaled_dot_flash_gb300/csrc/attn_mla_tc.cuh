@@ -44,6 +44,7 @@
 
 #include "params.h"
 #include "ptx.cuh"
+#include "seq_order.cuh"
 
 namespace attn {
 namespace mlatc {
@@ -95,8 +96,9 @@ struct MWork {
 };
 
 // blockIdx.x -> (sequence, 128-row block, split, output slice); the slice is
-// fastest so that the CTAs sharing key tiles run side by side.
-template <int NH>
+// fastest so that the CTAs sharing key tiles run side by side. LPT: the
+// sequences longest first, for calls with one row block per sequence (decode).
+template <int NH, bool LPT>
 __device__ __forceinline__ MWork make_mwork(const PagedParams& pp, int rblocks) {
   MWork w;
   int item = static_cast<int>(blockIdx.x);
@@ -105,7 +107,8 @@ __device__ __forceinline__ MWork make_mwork(const PagedParams& pp, int rblocks) 
   w.sp = item % pp.num_splits;
   item /= pp.num_splits;
   const int rb = item % rblocks;
-  w.s = item / rblocks;
+  if constexpr (LPT) w.s = seq_by_rank(pp, item / rblocks);  // longest sequences first
+  else w.s = item / rblocks;
   const int H = pp.Hq;
   w.q_lo = min(max(__ldg(pp.q_offsets + w.s), 0), pp.num_queries);
   const int q_hi = min(max(__ldg(pp.q_offsets + w.s + 1), w.q_lo), pp.num_queries);
@@ -131,7 +134,7 @@ __device__ __forceinline__ MWork make_mwork(const PagedParams& pp, int rblocks) 
   return w;
 }
 
-template <int R, int PD, bool BF16>
+template <int R, int PD, bool BF16, bool LPT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
                   const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_kp,
@@ -145,7 +148,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = pp.Hq;
-  const MWork w = make_mwork<C::NH>(pp, rblocks);
+  const MWork w = make_mwork<C::NH, LPT>(pp, rblocks);
   const int rows_seq = w.nq * H;
   if (w.row0 >= rows_seq) return;  // no rows here (CTA-uniform)
   const int64_t rows_total = static_cast<int64_t>(pp.num_queries) * H;
@@ -509,16 +512,17 @@ cudaError_t launch_mla_tc(EncodeTiledFn enc, const PagedParams& pp, const void* 
     tqp = tq;  // unused
     tkp = tlat;
   }
-  auto kern = mla_tc_kernel<R, PD, BF16>;
+  const int64_t rblocks = (static_cast<int64_t>(pp.max_queries) * pp.Hq + BM - 1) / BM;
+  const bool lpt = rblocks == 1;
+  auto kern = lpt ? mla_tc_kernel<R, PD, BF16, true> : mla_tc_kernel<R, PD, BF16, false>;
   constexpr int smem = C::SMEM_BYTES;
-  static std::atomic<unsigned long long> configured{0};
+  static std::atomic<unsigned long long> configured[2] = {{0}, {0}};
   const unsigned long long bit = pp.device >= 0 && pp.device < 64 ? 1ull << pp.device : 0ull;
-  if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+  if (!bit || !(configured[lpt].load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
+    configured[lpt].fetch_or(bit, std::memory_order_acq_rel);
   }
-  const int64_t rblocks = (static_cast<int64_t>(pp.max_queries) * pp.Hq + BM - 1) / BM;
   const int64_t ctas = static_cast<int64_t>(pp.num_seqs) * rblocks * pp.num_splits * C::NH;
   if (ctas == 0) return cudaSuccess;
   if (ctas > 0x7fffffffLL || rblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
