@@ -11,8 +11,9 @@ The arithmetic lives in ``attn_ref.c`` (plain C, float64, threaded over
 heads); this module widens the stored inputs exactly to float64, compiles the
 C file on first use (gcc) and calls it through ctypes.
 
-Every function is pinned by ``tests/test_oracle_pins.py`` (forward, LSE) and
-``tests/test_oracle_bwd_pins.py`` (backward) against closed forms, invariants,
+Every function is pinned by ``tests/test_oracle_pins.py`` (forward, LSE),
+``tests/test_oracle_bwd_pins.py`` (backward), the paged and MLA pins and
+``tests/test_oracle_paged_bwd_pins.py`` (paged and MLA backward) against closed forms, invariants,
 a 50-digit brute force of the pages' raw-exp kernel, finite differences of the
 forward, and textbook reductions; none is "parity unpinned".
 """
@@ -78,6 +79,12 @@ def _load():
             lib.oracle_paged_mla.argtypes = [i64, i64, i64, i64, i64, i64, dp, dp, dp, dp, ip, ip, ip, ip,
                                              ctypes.c_int, ctypes.c_double, dp, dp]
             lib.oracle_paged_mla.restype = ctypes.c_int
+            lib.oracle_paged_attention_bwd.argtypes = [i64] * 8 + [dp, dp, dp, ip, ip, ip, ip, ctypes.c_int,
+                                                                   ctypes.c_double, dp, dp, dp, dp]
+            lib.oracle_paged_attention_bwd.restype = ctypes.c_int
+            lib.oracle_paged_mla_bwd.argtypes = [i64] * 8 + [dp, dp, dp, dp, ip, ip, ip, ip, ctypes.c_int,
+                                                             ctypes.c_double, dp, dp, dp, dp, dp]
+            lib.oracle_paged_mla_bwd.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -273,6 +280,76 @@ def paged_mla(q, qp, latent, kpos, block_table, seq_lens, q_offsets, *, position
     if rc != 0:
         raise ValueError(f"oracle_paged_mla rejected its arguments (rc={rc})")
     return (out, ls) if lse else out
+
+
+def _paged_meta(block_table, seq_lens, q_offsets, positions, nq):
+    tab = np.ascontiguousarray(block_table, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    offs = np.ascontiguousarray(q_offsets, dtype=np.int32)
+    ns = lens.shape[0]
+    if tab.ndim != 2 or tab.shape[0] != ns or offs.shape != (ns + 1,) or offs[-1] != nq:
+        raise ValueError("block_table [num_seqs, max_pages], q_offsets [num_seqs + 1] ending at queries")
+    pos = None if positions is None else np.ascontiguousarray(positions, dtype=np.int32)
+    return tab, lens, offs, pos
+
+
+def paged_attention_bwd(q, k_cache, v_cache, dout, block_table, seq_lens, q_offsets, *, positions=None,
+                        causal: bool = True, scale: float, dtype: str | None = None):
+    """Float64 gradients of :func:`paged_attention` for dL/dO = ``dout``.
+
+    Returns dq [queries, Hq, D] and dk, dv in the cache's shape [pages,
+    page_size, Hkv, D]: a page read by several sequences (or blocks) gets the
+    sum of every read's contribution, a page nobody reads gets zero.
+    """
+    lib = _load()
+    w = (lambda a: widen(a, dtype)) if dtype else (lambda a: np.ascontiguousarray(a, dtype=np.float64))
+    q64, k64, v64, g64 = w(q), w(k_cache), w(v_cache), w(dout)
+    nq, Hq, D = q64.shape
+    pages, P, Hkv, Dk = k64.shape
+    if Dk != D or v64.shape != k64.shape or g64.shape != q64.shape:
+        raise ValueError("k_cache, v_cache [pages, page_size, Hkv, D]; dout like q")
+    tab, lens, offs, pos = _paged_meta(block_table, seq_lens, q_offsets, positions, nq)
+    dq = np.empty_like(q64)
+    dk = np.empty_like(k64)
+    dv = np.empty_like(v64)
+    ip = ctypes.POINTER(ctypes.c_int32)
+    rc = lib.oracle_paged_attention_bwd(lens.shape[0], Hq, Hkv, D, P, tab.shape[1], pages, nq, _dptr(q64),
+                                        _dptr(k64), _dptr(v64), tab.ctypes.data_as(ip), lens.ctypes.data_as(ip),
+                                        offs.ctypes.data_as(ip), pos.ctypes.data_as(ip) if pos is not None else None,
+                                        int(bool(causal)), float(scale), _dptr(g64), _dptr(dq), _dptr(dk), _dptr(dv))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_attention_bwd rejected its arguments (rc={rc})")
+    return dq, dk, dv
+
+
+def paged_mla_bwd(q, qp, latent, kpos, dout, block_table, seq_lens, q_offsets, *, positions=None,
+                  causal: bool = True, scale: float, dtype: str | None = None):
+    """Float64 gradients of :func:`paged_mla` for dL/dO = ``dout`` [queries, H, R].
+
+    Returns dq [queries, H, R], dqp [queries, H, P], and the cache-shaped
+    dlatent [pages, page_size, 1, R] (key and value contributions summed) and
+    dkpos [pages, page_size, 1, P].
+    """
+    lib = _load()
+    w = (lambda a: widen(a, dtype)) if dtype else (lambda a: np.ascontiguousarray(a, dtype=np.float64))
+    q64, qp64, lat64, kp64, g64 = w(q), w(qp), w(latent), w(kpos), w(dout)
+    nq, H, R = q64.shape
+    pages, P, one, R2 = lat64.shape
+    Pd = qp64.shape[2]
+    if (one != 1 or R2 != R or kp64.shape != (pages, P, 1, Pd) or qp64.shape[:2] != (nq, H)
+            or g64.shape != q64.shape):
+        raise ValueError("latent [pages, page_size, 1, R], kpos [pages, page_size, 1, P], qp [queries, H, P]")
+    tab, lens, offs, pos = _paged_meta(block_table, seq_lens, q_offsets, positions, nq)
+    dq, dqp, dlat, dkp = (np.empty_like(a) for a in (q64, qp64, lat64, kp64))
+    ip = ctypes.POINTER(ctypes.c_int32)
+    rc = lib.oracle_paged_mla_bwd(lens.shape[0], H, R, Pd, P, tab.shape[1], pages, nq, _dptr(q64), _dptr(qp64),
+                                  _dptr(lat64), _dptr(kp64), tab.ctypes.data_as(ip), lens.ctypes.data_as(ip),
+                                  offs.ctypes.data_as(ip), pos.ctypes.data_as(ip) if pos is not None else None,
+                                  int(bool(causal)), float(scale), _dptr(g64), _dptr(dq), _dptr(dqp), _dptr(dlat),
+                                  _dptr(dkp))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_mla_bwd rejected its arguments (rc={rc})")
+    return dq, dqp, dlat, dkp
 
 
 def prepare(q, k, v, *, kv_lens=None, bias=None, dtype: str | None = None):

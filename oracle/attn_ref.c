@@ -558,3 +558,199 @@ int oracle_paged_mla(int64_t num_seqs, int64_t H, int64_t R, int64_t Pd, int64_t
   free(sc);
   return 0;
 }
+
+/*
+ * Backward of the paged-cache attention and of paged MLA, in float64.
+ *
+ * Source: ruDNN user guide, section 11 (backward of paged attention and
+ * ordered history gradients): the paged backward returns dq for the packed
+ * queries and dk, dv in the shape of the physical caches (the "history"
+ * gradients); the MLA backward returns dq, dqp and the cache-shaped dlatent,
+ * dkp, where dlatent holds both the key and the value contribution of each
+ * latent row. Per query row the chain rule is that of oracle_attention_bwd
+ * above (w = softmax weights, dw_j = dout . v_j, ds_j = w_j (dw_j - sum_k w_k
+ * dw_k)), with key j of sequence s at row j % page_size of page
+ * table[s][j / page_size], and for MLA s_j = scale (q . c_j + qp . kp_j),
+ * v_j = c_j.
+ *
+ * Readings where the pages are silent: a physical page read by several
+ * sequences (a shared prefix), or by one sequence at several logical blocks,
+ * receives the sum of the contributions of every read; a page that no query
+ * reads gets zero gradients; a query row with no visible key contributes
+ * nothing and gets dq = 0; query rows outside every sequence's range get 0.
+ */
+static int paged_check(int64_t num_seqs, int64_t page_size, int64_t max_pages, int64_t num_pages,
+                       int64_t num_queries, const int32_t* table, const int32_t* seq_len,
+                       const int32_t* q_off, int64_t* cap) {
+  *cap = 1;
+  for (int64_t s = 0; s < num_seqs; ++s) {
+    const int64_t L = seq_len[s];
+    if (L < 0 || L > max_pages * page_size) return -1;
+    if (q_off[s] < 0 || q_off[s + 1] < q_off[s] || q_off[s + 1] > num_queries) return -1;
+    for (int64_t b = 0; b < (L + page_size - 1) / page_size; ++b) {
+      const int32_t pg = table[s * max_pages + b];
+      if (pg < 0 || pg >= num_pages) return -1;
+    }
+    if (L > *cap) *cap = L;
+  }
+  return 0;
+}
+
+int oracle_paged_attention_bwd(int64_t num_seqs, int64_t Hq, int64_t Hkv, int64_t D, int64_t page_size,
+                               int64_t max_pages, int64_t num_pages, int64_t num_queries, const double* q,
+                               const double* kc, const double* vc, const int32_t* table,
+                               const int32_t* seq_len, const int32_t* q_off, const int32_t* positions,
+                               int causal, double scale, const double* dout, double* dq, double* dk,
+                               double* dv) {
+  if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || page_size <= 0 || max_pages < 0 ||
+      num_pages < 0 || num_queries < 0)
+    return -1;
+  int64_t cap;
+  if (paged_check(num_seqs, page_size, max_pages, num_pages, num_queries, table, seq_len, q_off, &cap))
+    return -1;
+  const int64_t group = Hq / Hkv;
+  for (int64_t x = 0; x < num_queries * Hq * D; ++x) dq[x] = 0.0;
+  for (int64_t x = 0; x < num_pages * page_size * Hkv * D; ++x) dk[x] = dv[x] = 0.0;
+  double* w = (double*)malloc(sizeof(double) * (size_t)cap);
+  double* dw = (double*)malloc(sizeof(double) * (size_t)cap);
+  if (!w || !dw) {
+    free(w);
+    free(dw);
+    return -2;
+  }
+  for (int64_t s = 0; s < num_seqs; ++s) {
+    const int64_t L = seq_len[s];
+    const int64_t n = q_off[s + 1] - q_off[s];
+    for (int64_t t = q_off[s]; t < q_off[s + 1]; ++t) {
+      const int64_t p_t = positions ? positions[t] : L - n + (t - q_off[s]);
+      for (int64_t h = 0; h < Hq; ++h) {
+        const int64_t hk = h / group;
+        const double* qi = q + (t * Hq + h) * D;
+        const double* gi = dout + (t * Hq + h) * D;
+        double* dqi = dq + (t * Hq + h) * D;
+        /* the forward's weights of this row */
+        double m = -INFINITY;
+        for (int64_t j = 0; j < L; ++j) {
+          w[j] = -INFINITY;
+          if (!causal || j <= p_t) {
+            const int64_t row = (table[s * max_pages + j / page_size] * page_size + j % page_size) * Hkv + hk;
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d) acc += qi[d] * kc[row * D + d];
+            w[j] = scale * acc;
+          }
+          if (w[j] > m) m = w[j];
+        }
+        if (m == -INFINITY) continue; /* no visible key: no contribution */
+        double l = 0.0;
+        for (int64_t j = 0; j < L; ++j) {
+          w[j] = exp(w[j] - m);
+          l += w[j];
+        }
+        double wdw = 0.0;
+        for (int64_t j = 0; j < L; ++j) {
+          w[j] /= l;
+          dw[j] = 0.0;
+          if (w[j] == 0.0) continue;
+          const int64_t row = (table[s * max_pages + j / page_size] * page_size + j % page_size) * Hkv + hk;
+          for (int64_t d = 0; d < D; ++d) dw[j] += gi[d] * vc[row * D + d];
+          wdw += w[j] * dw[j];
+        }
+        for (int64_t j = 0; j < L; ++j) {
+          if (w[j] == 0.0) continue; /* masked, or exp underflow: zero weight, zero terms */
+          const int64_t row = (table[s * max_pages + j / page_size] * page_size + j % page_size) * Hkv + hk;
+          const double dsj = w[j] * (dw[j] - wdw);
+          for (int64_t d = 0; d < D; ++d) {
+            dqi[d] += scale * dsj * kc[row * D + d];
+            dk[row * D + d] += scale * dsj * qi[d];
+            dv[row * D + d] += w[j] * gi[d];
+          }
+        }
+      }
+    }
+  }
+  free(w);
+  free(dw);
+  return 0;
+}
+
+int oracle_paged_mla_bwd(int64_t num_seqs, int64_t H, int64_t R, int64_t Pd, int64_t page_size,
+                         int64_t max_pages, int64_t num_pages, int64_t num_queries, const double* q,
+                         const double* qp, const double* lat, const double* kp, const int32_t* table,
+                         const int32_t* seq_len, const int32_t* q_off, const int32_t* positions, int causal,
+                         double scale, const double* dout, double* dq, double* dqp, double* dlat,
+                         double* dkp) {
+  if (num_seqs < 0 || H <= 0 || R <= 0 || Pd < 0 || page_size <= 0 || max_pages < 0 || num_pages < 0 ||
+      num_queries < 0)
+    return -1;
+  int64_t cap;
+  if (paged_check(num_seqs, page_size, max_pages, num_pages, num_queries, table, seq_len, q_off, &cap))
+    return -1;
+  for (int64_t x = 0; x < num_queries * H * R; ++x) dq[x] = 0.0;
+  for (int64_t x = 0; x < num_queries * H * Pd; ++x) dqp[x] = 0.0;
+  for (int64_t x = 0; x < num_pages * page_size * R; ++x) dlat[x] = 0.0;
+  for (int64_t x = 0; x < num_pages * page_size * Pd; ++x) dkp[x] = 0.0;
+  double* w = (double*)malloc(sizeof(double) * (size_t)cap);
+  double* dw = (double*)malloc(sizeof(double) * (size_t)cap);
+  if (!w || !dw) {
+    free(w);
+    free(dw);
+    return -2;
+  }
+  for (int64_t s = 0; s < num_seqs; ++s) {
+    const int64_t L = seq_len[s];
+    const int64_t n = q_off[s + 1] - q_off[s];
+    for (int64_t t = q_off[s]; t < q_off[s + 1]; ++t) {
+      const int64_t p_t = positions ? positions[t] : L - n + (t - q_off[s]);
+      for (int64_t h = 0; h < H; ++h) {
+        const double* qi = q + (t * H + h) * R;
+        const double* qpt = qp + (t * H + h) * Pd;
+        const double* gi = dout + (t * H + h) * R;
+        double* dqi = dq + (t * H + h) * R;
+        double* dqpi = dqp + (t * H + h) * Pd;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < L; ++j) {
+          w[j] = -INFINITY;
+          if (!causal || j <= p_t) {
+            const int64_t row = table[s * max_pages + j / page_size] * page_size + j % page_size;
+            double acc = 0.0;
+            for (int64_t d = 0; d < R; ++d) acc += qi[d] * lat[row * R + d];
+            for (int64_t d = 0; d < Pd; ++d) acc += qpt[d] * kp[row * Pd + d];
+            w[j] = scale * acc;
+          }
+          if (w[j] > m) m = w[j];
+        }
+        if (m == -INFINITY) continue;
+        double l = 0.0;
+        for (int64_t j = 0; j < L; ++j) {
+          w[j] = exp(w[j] - m);
+          l += w[j];
+        }
+        double wdw = 0.0;
+        for (int64_t j = 0; j < L; ++j) {
+          w[j] /= l;
+          dw[j] = 0.0;
+          if (w[j] == 0.0) continue;
+          const int64_t row = table[s * max_pages + j / page_size] * page_size + j % page_size;
+          for (int64_t d = 0; d < R; ++d) dw[j] += gi[d] * lat[row * R + d];
+          wdw += w[j] * dw[j];
+        }
+        for (int64_t j = 0; j < L; ++j) {
+          if (w[j] == 0.0) continue;
+          const int64_t row = table[s * max_pages + j / page_size] * page_size + j % page_size;
+          const double dsj = w[j] * (dw[j] - wdw);
+          for (int64_t d = 0; d < R; ++d) {
+            dqi[d] += scale * dsj * lat[row * R + d];
+            dlat[row * R + d] += scale * dsj * qi[d] + w[j] * gi[d]; /* key and value parts */
+          }
+          for (int64_t d = 0; d < Pd; ++d) {
+            dqpi[d] += scale * dsj * kp[row * Pd + d];
+            dkp[row * Pd + d] += scale * dsj * qpt[d];
+          }
+        }
+      }
+    }
+  }
+  free(w);
+  free(dw);
+  return 0;
+}

@@ -81,6 +81,29 @@ MUTANTS_MLA = {
 }
 
 
+# Mistakes in the paged and MLA backward, caught by the paged backward pins.
+MUTANTS_PBWD = {
+    "pbwd_no_row_term": ("const double dsj = w[j] * (dw[j] - wdw);\n          for (int64_t d = 0; d < D; ++d) {",
+                         "const double dsj = w[j] * dw[j];\n          for (int64_t d = 0; d < D; ++d) {"),
+    "pbwd_dv_uses_ds": ("dv[row * D + d] += w[j] * gi[d];", "dv[row * D + d] += dsj * gi[d];"),
+    "pbwd_dk_unscaled": ("dk[row * D + d] += scale * dsj * qi[d];", "dk[row * D + d] += dsj * qi[d];"),
+    "pbwd_dk_overwrites": ("dk[row * D + d] += scale * dsj * qi[d];", "dk[row * D + d] = scale * dsj * qi[d];"),
+    "mla_bwd_no_value_part": ("dlat[row * R + d] += scale * dsj * qi[d] + w[j] * gi[d];",
+                              "dlat[row * R + d] += scale * dsj * qi[d];"),
+    "mla_bwd_dkp_uses_q": ("dkp[row * Pd + d] += scale * dsj * qpt[d];", "dkp[row * Pd + d] += scale * dsj * qi[d];"),
+    "mla_bwd_dqp_from_latent": ("dqpi[d] += scale * dsj * kp[row * Pd + d];",
+                                "dqpi[d] += scale * dsj * lat[row * R + d];"),
+}
+
+
+def _pbwd_pins():
+    from tests import test_oracle_paged_bwd_pins as pb
+    yield lambda: pb.test_paged_bwd_matches_finite_differences(True, None)
+    yield pb.test_shared_page_gradient_is_the_sum_over_private_copies
+    yield lambda: pb.test_mla_bwd_is_paged_bwd_over_concatenated_keys(True, 2)
+    yield pb.test_mla_bwd_matches_finite_differences
+
+
 def _mla_pins():
     yield mpins.test_mla_single_key_returns_its_latent_row
     for causal in (True, False):
@@ -120,9 +143,10 @@ def _pins():
                 yield lambda m=mask, b=bshape, s=sq_sk: pins.test_brute_force_tiny(m, b, s)
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS) + sorted(MUTANTS_BWD) + sorted(MUTANTS_PAGED) + sorted(MUTANTS_MLA))
+@pytest.mark.parametrize("name", sorted(MUTANTS) + sorted(MUTANTS_BWD) + sorted(MUTANTS_PAGED) + sorted(MUTANTS_MLA)
+                         + sorted(MUTANTS_PBWD))
 def test_pins_catch_mutant(name, tmp_path, monkeypatch):
-    old, new = {**MUTANTS, **MUTANTS_BWD, **MUTANTS_PAGED, **MUTANTS_MLA}[name]
+    old, new = {**MUTANTS, **MUTANTS_BWD, **MUTANTS_PAGED, **MUTANTS_MLA, **MUTANTS_PBWD}[name]
     src = open(SRC).read()
     assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
     mut = tmp_path / "attn_mut.c"
@@ -144,10 +168,13 @@ def test_pins_catch_mutant(name, tmp_path, monkeypatch):
     lib.oracle_paged_attention.restype = ctypes.c_int
     lib.oracle_paged_mla.argtypes = real.oracle_paged_mla.argtypes
     lib.oracle_paged_mla.restype = ctypes.c_int
+    for fn in ("oracle_paged_attention_bwd", "oracle_paged_mla_bwd"):
+        getattr(lib, fn).argtypes = getattr(real, fn).argtypes
+        getattr(lib, fn).restype = ctypes.c_int
     monkeypatch.setattr(oracle, "_lib", lib)
     caught = []
     pins_for = (_pins if name in MUTANTS else _bwd_pins if name in MUTANTS_BWD
-                else _paged_pins if name in MUTANTS_PAGED else _mla_pins)
+                else _paged_pins if name in MUTANTS_PAGED else _mla_pins if name in MUTANTS_MLA else _pbwd_pins)
     for pin in pins_for():
         try:
             pin()
