@@ -90,6 +90,18 @@ def load_library():
         lib.attn_paged_mla_workspace_bytes.argtypes = [ctypes.POINTER(MlaShape), ctypes.c_int,
                                                        ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_paged_mla_workspace_bytes.restype = ctypes.c_int
+        lib.attn_paged_bwd.argtypes = [ctypes.POINTER(PagedShape), vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                       ctypes.c_float, ctypes.c_int, vp, vp, vp, vp, ctypes.c_size_t, vp, vp, vp, vp]
+        lib.attn_paged_bwd.restype = ctypes.c_int
+        lib.attn_paged_bwd_workspace_bytes.argtypes = [ctypes.POINTER(PagedShape), ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_paged_bwd_workspace_bytes.restype = ctypes.c_int
+        lib.attn_paged_mla_bwd.argtypes = [ctypes.POINTER(MlaShape), vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                           ctypes.c_float, ctypes.c_int, vp, vp, vp, vp, ctypes.c_size_t, vp, vp,
+                                           vp, vp, vp]
+        lib.attn_paged_mla_bwd.restype = ctypes.c_int
+        lib.attn_paged_mla_bwd_workspace_bytes.argtypes = [ctypes.POINTER(MlaShape),
+                                                           ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_paged_mla_bwd_workspace_bytes.restype = ctypes.c_int
         lib.attn_fwd_host.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, ctypes.c_int, vp, vp, ctypes.c_float,
                                       ctypes.c_int, vp, ctypes.c_size_t, vp, vp]
         lib.attn_fwd_host.restype = ctypes.c_int
@@ -505,3 +517,118 @@ def paged_mla(q, qp, latent, kpos, block_table, seq_lens, q_offsets, *, position
                                         ptr(workspace) if need else None, need, ptr(out), ptr(lse),
                                         stream.cuda_stream or None))
     return (out, lse) if return_lse else out
+
+
+def paged_bwd_workspace_bytes(shape: PagedShape) -> int:
+    """Workspace bytes attn_paged_bwd needs for ``shape``."""
+    n = ctypes.c_size_t(0)
+    check(load_library().attn_paged_bwd_workspace_bytes(ctypes.byref(shape), ctypes.byref(n)))
+    return n.value
+
+
+def _workspace(need, workspace, dev):
+    import torch
+    if workspace is None:
+        return torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if workspace.device != dev or workspace.numel() * workspace.element_size() < need:
+        raise AttnError(f"workspace must hold {need} bytes on q's device")
+    return workspace
+
+
+def paged_bwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, dout, *, out=None, lse=None, positions=None,
+              causal: bool = True, scale: float | None = None, max_queries: int | None = None,
+              grads=("dq", "dk", "dv"), workspace=None, stream=None):
+    """Gradients of :func:`paged_fwd` for dL/dO = ``dout`` (attn_paged_bwd, ordered).
+
+    Arguments as for :func:`paged_fwd`; ``out`` and ``lse`` are the forward's
+    output and float32 [queries, Hq] log-sum-exp (when either is None the
+    forward runs here first to recompute them). ``grads`` names the gradients
+    wanted. Returns (dq [queries, Hq, D], dk, dv [pages, page_size, Hkv, D]),
+    None in place of a gradient not asked for.
+    """
+    import torch
+
+    dev = q.device
+    if dout.device != dev or dout.dtype != q.dtype or tuple(dout.shape) != tuple(q.shape) or not dout.is_contiguous():
+        raise AttnError("dout must be a contiguous tensor like q")
+    nq, Hq, D = q.shape
+    pages, P, Hkv, _ = k_cache.shape
+    ns = int(seq_lens.shape[0])
+    if max_queries is None:
+        max_queries = int((q_offsets[1:] - q_offsets[:-1]).max().item()) if ns else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None or lse is None:
+        out, lse = paged_fwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, positions=positions,
+                             causal=causal, scale=scale, max_queries=max_queries, return_lse=True, stream=stream)
+    if out.device != dev or out.dtype != q.dtype or tuple(out.shape) != tuple(q.shape) or not out.is_contiguous():
+        raise AttnError("out must be a contiguous tensor like q")
+    if lse.device != dev or lse.dtype != torch.float32 or tuple(lse.shape) != (nq, Hq) or not lse.is_contiguous():
+        raise AttnError("lse must be a contiguous float32 [queries, Hq] tensor on q's device")
+    shape = PagedShape(ns, nq, Hq, Hkv, D, P, pages, int(block_table.shape[1]), int(max_queries))
+    need = paged_bwd_workspace_bytes(shape)
+    workspace = _workspace(need, workspace, dev)
+    dq = torch.empty_like(q) if "dq" in grads else None
+    dk = torch.empty_like(k_cache) if "dk" in grads else None
+    dv = torch.empty_like(v_cache) if "dv" in grads else None
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    ptr = lambda t: (t.data_ptr() or None) if t is not None else None
+    check(load_library().attn_paged_bwd(ctypes.byref(shape), ptr(q), ptr(k_cache), ptr(v_cache), ptr(block_table),
+                                        ptr(seq_lens), ptr(q_offsets), ptr(positions), int(bool(causal)),
+                                        float(scale), _dtype_code(q), ptr(out), ptr(dout), ptr(lse),
+                                        ptr(workspace), need, ptr(dq), ptr(dk), ptr(dv), stream.cuda_stream or None))
+    return dq, dk, dv
+
+
+def mla_bwd_workspace_bytes(shape: MlaShape) -> int:
+    """Workspace bytes attn_paged_mla_bwd needs for ``shape``."""
+    n = ctypes.c_size_t(0)
+    check(load_library().attn_paged_mla_bwd_workspace_bytes(ctypes.byref(shape), ctypes.byref(n)))
+    return n.value
+
+
+def paged_mla_bwd(q, qp, latent, kpos, block_table, seq_lens, q_offsets, dout, *, out=None, lse=None,
+                  positions=None, causal: bool = True, scale: float, max_queries: int | None = None,
+                  grads=("dq", "dqp", "dlatent", "dkpos"), workspace=None, stream=None):
+    """Gradients of :func:`paged_mla` for dL/dO = ``dout`` (attn_paged_mla_bwd, ordered).
+
+    Returns (dq [queries, H, R], dqp [queries, H, Pd], dlatent [pages,
+    page_size, 1, R] with its key and value parts, dkpos [pages, page_size, 1,
+    Pd]), None in place of a gradient not asked for (or of dqp, dkpos when
+    Pd == 0). ``out``/``lse`` as for :func:`paged_bwd`.
+    """
+    import torch
+
+    dev = q.device
+    if dout.device != dev or dout.dtype != q.dtype or tuple(dout.shape) != tuple(q.shape) or not dout.is_contiguous():
+        raise AttnError("dout must be a contiguous tensor like q")
+    nq, H, R = q.shape
+    pages, P = int(latent.shape[0]), int(latent.shape[1])
+    Pd = int(qp.shape[2])
+    ns = int(seq_lens.shape[0])
+    if max_queries is None:
+        max_queries = int((q_offsets[1:] - q_offsets[:-1]).max().item()) if ns else 0
+    if out is None or lse is None:
+        out, lse = paged_mla(q, qp, latent, kpos, block_table, seq_lens, q_offsets, positions=positions,
+                             causal=causal, scale=scale, max_queries=max_queries, return_lse=True, stream=stream)
+    if out.device != dev or out.dtype != q.dtype or tuple(out.shape) != tuple(q.shape) or not out.is_contiguous():
+        raise AttnError("out must be a contiguous tensor like q")
+    if lse.device != dev or lse.dtype != torch.float32 or tuple(lse.shape) != (nq, H) or not lse.is_contiguous():
+        raise AttnError("lse must be a contiguous float32 [queries, H] tensor on q's device")
+    shape = MlaShape(ns, nq, H, R, Pd, P, pages, int(block_table.shape[1]), int(max_queries))
+    need = mla_bwd_workspace_bytes(shape)
+    workspace = _workspace(need, workspace, dev)
+    dq = torch.empty_like(q) if "dq" in grads else None
+    dqp = torch.empty_like(qp) if "dqp" in grads and Pd else None
+    dlat = torch.empty_like(latent) if "dlatent" in grads else None
+    dkp = torch.empty_like(kpos) if "dkpos" in grads and Pd else None
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    ptr = lambda t: (t.data_ptr() or None) if t is not None else None
+    check(load_library().attn_paged_mla_bwd(ctypes.byref(shape), ptr(q), ptr(qp), ptr(latent), ptr(kpos),
+                                            ptr(block_table), ptr(seq_lens), ptr(q_offsets), ptr(positions),
+                                            int(bool(causal)), float(scale), _dtype_code(q), ptr(out), ptr(dout),
+                                            ptr(lse), ptr(workspace), need, ptr(dq), ptr(dqp), ptr(dlat), ptr(dkp),
+                                            stream.cuda_stream or None))
+    return dq, dqp, dlat, dkp

@@ -9,9 +9,11 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <initializer_list>
 #include <mutex>
 
 #include "attn.h"
+#include "paged_bwd.h"
 #include "params.h"
 
 namespace {
@@ -726,6 +728,225 @@ int attn_paged_mla(const attn_mla_shape_t* shape, const void* q, const void* qp,
   e = attn::launch_mla_simt(s.R, s.Pd, static_cast<int>(dtype), pp, q, qp, latent, kpos, out, lse, st,
                             &unsupported);
   if (unsupported) return ATTN_ERR_HEAD_DIM;
+  return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- paged backward
+namespace {
+
+// Grid limits and required pointers shared by both paged backward calls;
+// `rows_per_cta` is the query-major kernel's (query, head) rows per CTA.
+int check_paged_bwd_shape(int num_seqs, int num_queries, int heads, int Hkv, int page_size, int num_pages,
+                          int max_pages, int max_queries, int rows_per_cta) {
+  if (num_seqs < 0 || num_queries < 0 || heads <= 0 || Hkv <= 0 || heads % Hkv != 0 || page_size <= 0 ||
+      num_pages < 0 || max_pages < 0 || max_queries < 0)
+    return ATTN_ERR_SHAPE;
+  const int64_t group = heads / Hkv;
+  if (static_cast<int64_t>(num_seqs) * Hkv > 0x7fffffffLL || static_cast<int64_t>(num_pages) * Hkv > 0x7fffffffLL ||
+      (static_cast<int64_t>(max_queries) * group + rows_per_cta - 1) / rows_per_cta > 65535 ||
+      (static_cast<int64_t>(page_size) + rows_per_cta - 1) / rows_per_cta > 65535 ||
+      static_cast<int64_t>(max_pages) * page_size > 0x7fffffffLL ||
+      static_cast<int64_t>(num_seqs) * max_pages > 0x7fffffffLL)
+    return ATTN_ERR_SHAPE;
+  return ATTN_OK;
+}
+
+attn::pbwd::Layout paged_bwd_layout(int num_seqs, int num_queries, int heads, int num_pages, int max_pages) {
+  return attn::pbwd::layout(static_cast<int64_t>(num_queries) * heads, num_pages,
+                            static_cast<int64_t>(num_seqs) * max_pages);
+}
+
+attn::PagedParams paged_bwd_params(int dev, int num_seqs, int num_queries, int heads, int Hkv, int page_size,
+                                   int num_pages, int max_pages, int max_queries, const int32_t* block_table,
+                                   const int32_t* seq_lens, const int32_t* q_offsets, const int32_t* positions,
+                                   int causal, float scale) {
+  attn::PagedParams pp{};
+  pp.num_splits = 1;
+  pp.num_seqs = num_seqs;
+  pp.num_queries = num_queries;
+  pp.Hq = heads;
+  pp.Hkv = Hkv;
+  pp.page_size = page_size;
+  pp.num_pages = num_pages;
+  pp.max_pages = max_pages;
+  pp.max_queries = max_queries;
+  pp.block_table = block_table;
+  pp.seq_lens = seq_lens;
+  pp.q_offsets = q_offsets;
+  pp.positions = positions;
+  pp.causal = causal;
+  pp.scale_log2 = scale * 1.4426950408889634f;
+  pp.status = status_ptr(dev);
+  pp.device = dev;
+  return pp;
+}
+
+struct Buf { const void* p; int64_t n; };
+
+// Every written buffer is disjoint from every read buffer and from the others.
+bool any_overlap(const Buf* outs, int n_out, const Buf* ins, int n_in) {
+  for (int a = 0; a < n_out; ++a) {
+    for (int i = 0; i < n_in; ++i)
+      if (overlaps(outs[a].p, outs[a].n, ins[i].p, ins[i].n)) return true;
+    for (int c = a + 1; c < n_out; ++c)
+      if (overlaps(outs[a].p, outs[a].n, outs[c].p, outs[c].n)) return true;
+  }
+  return false;
+}
+
+bool misaligned4(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return true;
+  return false;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_paged_bwd_workspace_bytes(const attn_paged_shape_t* shape, size_t* bytes) {
+  if (!shape || !bytes) return ATTN_ERR_NULL;
+  const attn_paged_shape_t s = *shape;
+  if (s.num_seqs < 0 || s.num_queries < 0 || s.Hq <= 0 || s.num_pages < 0 || s.max_pages < 0)
+    return ATTN_ERR_SHAPE;
+  *bytes = static_cast<size_t>(paged_bwd_layout(s.num_seqs, s.num_queries, s.Hq, s.num_pages, s.max_pages).total);
+  return ATTN_OK;
+}
+
+int attn_paged_bwd(const attn_paged_shape_t* shape, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_offsets,
+                   const int32_t* positions, int causal, float scale, attn_dtype_t dtype, const void* out,
+                   const void* dout, const float* lse, void* workspace, size_t workspace_bytes, void* dq,
+                   void* dk_cache, void* dv_cache, void* stream) {
+  if (!shape) return ATTN_ERR_NULL;
+  const attn_paged_shape_t s = *shape;
+  if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+  int rc = check_paged_bwd_shape(s.num_seqs, s.num_queries, s.Hq, s.Hkv, s.page_size, s.num_pages, s.max_pages,
+                                 s.max_queries, 64);
+  if (rc != ATTN_OK) return rc;
+  if (s.D <= 0) return ATTN_ERR_SHAPE;
+  if (causal != 0 && causal != 1) return ATTN_ERR_MASK;
+  if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_SCALE;
+  if (!(s.D == 16 || s.D == 32 || s.D == 64 || s.D == 128)) return ATTN_ERR_HEAD_DIM;
+  const bool work = s.num_queries > 0 && s.num_seqs > 0 && (dq || dk_cache || dv_cache);
+  if (work && (!q || !out || !dout || !lse || !seq_lens || !q_offsets || (s.max_pages > 0 && !block_table) ||
+               (s.num_pages > 0 && (!k_cache || !v_cache))))
+    return ATTN_ERR_NULL;
+  for (const void* p16 : {q, k_cache, v_cache, out, dout, static_cast<const void*>(dq),
+                          static_cast<const void*>(dk_cache), static_cast<const void*>(dv_cache)})
+    if (p16 && !aligned16(p16)) return ATTN_ERR_ALIGN;
+  if (misaligned4({block_table, seq_lens, q_offsets, positions, lse})) return ATTN_ERR_ALIGN;
+  const int es = elem_size(dtype);
+  const int64_t q_bytes = static_cast<int64_t>(s.num_queries) * s.Hq * s.D * es;
+  const int64_t kv_bytes = static_cast<int64_t>(s.num_pages) * s.page_size * s.Hkv * s.D * es;
+  const attn::pbwd::Layout lay = paged_bwd_layout(s.num_seqs, s.num_queries, s.Hq, s.num_pages, s.max_pages);
+  if (work) {
+    if (!workspace || workspace_bytes < static_cast<size_t>(lay.total)) return ATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  }
+  const Buf ins[] = {{q, q_bytes}, {k_cache, kv_bytes}, {v_cache, kv_bytes}, {out, q_bytes}, {dout, q_bytes},
+                     {lse, static_cast<int64_t>(s.num_queries) * s.Hq * 4},
+                     {block_table, static_cast<int64_t>(s.num_seqs) * s.max_pages * 4},
+                     {seq_lens, static_cast<int64_t>(s.num_seqs) * 4},
+                     {q_offsets, static_cast<int64_t>(s.num_seqs + 1) * 4},
+                     {positions, positions ? static_cast<int64_t>(s.num_queries) * 4 : 0}};
+  const Buf outs[] = {{dq, q_bytes}, {dk_cache, kv_bytes}, {dv_cache, kv_bytes},
+                      {work ? workspace : nullptr, lay.total}};
+  if (any_overlap(outs, 4, ins, 10)) return ATTN_ERR_OVERLAP;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (!work) {  // no query: the cache gradients are zero
+    if (dk_cache && kv_bytes) e = cudaMemsetAsync(dk_cache, 0, static_cast<size_t>(kv_bytes), st);
+    if (e == cudaSuccess && dv_cache && kv_bytes) e = cudaMemsetAsync(dv_cache, 0, static_cast<size_t>(kv_bytes), st);
+    return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+  }
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return fail_cuda(e);
+  const attn::PagedParams pp =
+      paged_bwd_params(dev, s.num_seqs, s.num_queries, s.Hq, s.Hkv, s.page_size, s.num_pages, s.max_pages,
+                       s.max_queries, block_table, seq_lens, q_offsets, positions, causal, scale);
+  const attn::pbwd::Buffers b = attn::pbwd::carve(workspace, lay);
+  e = attn::pbwd::launch_preprocess(static_cast<int>(dtype), s.D, out, dout, lse, b,
+                                    static_cast<int64_t>(s.num_queries) * s.Hq, st);
+  if (e == cudaSuccess && (dk_cache || dv_cache)) e = attn::pbwd::launch_page_index(pp, b, st);
+  if (e == cudaSuccess)
+    e = attn::pbwd::launch_paged_bwd(s.D, static_cast<int>(dtype), pp, q, k_cache, v_cache, dout, b, dq, dk_cache,
+                                     dv_cache, scale, st);
+  return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+}
+
+int attn_paged_mla_bwd_workspace_bytes(const attn_mla_shape_t* shape, size_t* bytes) {
+  if (!shape || !bytes) return ATTN_ERR_NULL;
+  const attn_mla_shape_t s = *shape;
+  if (s.num_seqs < 0 || s.num_queries < 0 || s.H <= 0 || s.num_pages < 0 || s.max_pages < 0) return ATTN_ERR_SHAPE;
+  *bytes = static_cast<size_t>(paged_bwd_layout(s.num_seqs, s.num_queries, s.H, s.num_pages, s.max_pages).total);
+  return ATTN_OK;
+}
+
+int attn_paged_mla_bwd(const attn_mla_shape_t* shape, const void* q, const void* qp, const void* latent,
+                       const void* kpos, const int32_t* block_table, const int32_t* seq_lens,
+                       const int32_t* q_offsets, const int32_t* positions, int causal, float scale,
+                       attn_dtype_t dtype, const void* out, const void* dout, const float* lse, void* workspace,
+                       size_t workspace_bytes, void* dq, void* dqp, void* dlatent, void* dkpos, void* stream) {
+  if (!shape) return ATTN_ERR_NULL;
+  const attn_mla_shape_t s = *shape;
+  if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+  if (s.R <= 0 || s.Pd < 0) return ATTN_ERR_SHAPE;
+  if (!(s.R == 128 || s.R == 256 || s.R == 512) || !(s.Pd == 0 || s.Pd == 16 || s.Pd == 32 || s.Pd == 64))
+    return ATTN_ERR_HEAD_DIM;
+  int rc = check_paged_bwd_shape(s.num_seqs, s.num_queries, s.H, 1, s.page_size, s.num_pages, s.max_pages,
+                                 s.max_queries, 8192 / s.R);
+  if (rc != ATTN_OK) return rc;
+  if (causal != 0 && causal != 1) return ATTN_ERR_MASK;
+  if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_SCALE;
+  if (s.Pd == 0) dqp = dkpos = nullptr;  // nothing to compute
+  const bool work = s.num_queries > 0 && s.num_seqs > 0 && (dq || dqp || dlatent || dkpos);
+  if (work && (!q || !out || !dout || !lse || !seq_lens || !q_offsets || (s.max_pages > 0 && !block_table) ||
+               (s.num_pages > 0 && !latent) || (s.Pd > 0 && (!qp || (s.num_pages > 0 && !kpos)))))
+    return ATTN_ERR_NULL;
+  for (const void* p16 : {q, qp, latent, kpos, out, dout, static_cast<const void*>(dq), static_cast<const void*>(dqp),
+                          static_cast<const void*>(dlatent), static_cast<const void*>(dkpos)})
+    if (p16 && !aligned16(p16)) return ATTN_ERR_ALIGN;
+  if (misaligned4({block_table, seq_lens, q_offsets, positions, lse})) return ATTN_ERR_ALIGN;
+  const int es = elem_size(dtype);
+  const int64_t rows = static_cast<int64_t>(s.num_queries) * s.H;
+  const int64_t tok = static_cast<int64_t>(s.num_pages) * s.page_size;
+  const attn::pbwd::Layout lay = paged_bwd_layout(s.num_seqs, s.num_queries, s.H, s.num_pages, s.max_pages);
+  if (work) {
+    if (!workspace || workspace_bytes < static_cast<size_t>(lay.total)) return ATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  }
+  const Buf ins[] = {{q, rows * s.R * es}, {qp, rows * s.Pd * es}, {latent, tok * s.R * es},
+                     {kpos, tok * s.Pd * es}, {out, rows * s.R * es}, {dout, rows * s.R * es}, {lse, rows * 4},
+                     {block_table, static_cast<int64_t>(s.num_seqs) * s.max_pages * 4},
+                     {seq_lens, static_cast<int64_t>(s.num_seqs) * 4},
+                     {q_offsets, static_cast<int64_t>(s.num_seqs + 1) * 4},
+                     {positions, positions ? static_cast<int64_t>(s.num_queries) * 4 : 0}};
+  const Buf outs[] = {{dq, rows * s.R * es}, {dqp, rows * s.Pd * es}, {dlatent, tok * s.R * es},
+                      {dkpos, tok * s.Pd * es}, {work ? workspace : nullptr, lay.total}};
+  if (any_overlap(outs, 5, ins, 11)) return ATTN_ERR_OVERLAP;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (!work) {
+    if (dlatent && tok) e = cudaMemsetAsync(dlatent, 0, static_cast<size_t>(tok * s.R * es), st);
+    if (e == cudaSuccess && dkpos && tok) e = cudaMemsetAsync(dkpos, 0, static_cast<size_t>(tok * s.Pd * es), st);
+    return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+  }
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return fail_cuda(e);
+  const attn::PagedParams pp =
+      paged_bwd_params(dev, s.num_seqs, s.num_queries, s.H, 1, s.page_size, s.num_pages, s.max_pages,
+                       s.max_queries, block_table, seq_lens, q_offsets, positions, causal, scale);
+  const attn::pbwd::Buffers b = attn::pbwd::carve(workspace, lay);
+  e = attn::pbwd::launch_preprocess(static_cast<int>(dtype), s.R, out, dout, lse, b, rows, st);
+  if (e == cudaSuccess && (dlatent || dkpos)) e = attn::pbwd::launch_page_index(pp, b, st);
+  if (e == cudaSuccess)
+    e = attn::pbwd::launch_mla_bwd(s.R, s.Pd, static_cast<int>(dtype), pp, q, qp, latent, kpos, dout, b, dq, dqp,
+                                   dlatent, dkpos, scale, st);
   return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
 }
 

@@ -1,0 +1,374 @@
+// paged_bwd.cuh - kernels of the backward over a paged cache (paged attention
+// and paged MLA), fp32 FMA arithmetic for every dtype, ordered: no atomics
+// in any gradient, one fixed summation order, so repeated calls return the
+// same bits.
+//
+// Source: ruDNN user guide, section 11 (backward of paged attention and
+// ordered history gradients): dq for the packed queries and dk, dv in the
+// shape of the physical caches, the probabilities recomputed from the forward's
+// statistics; an ordered variant reduces the history (cache) gradients
+// without atomics, using a workspace that holds row statistics and a reverse
+// index from physical pages to the table entries that read them. For MLA the
+// latent gradient holds both its key and its value contribution.
+//
+// With the forward's lse_i and D_i = dout_i . out_i, for every visible (i, j):
+//   p_ij = exp(s_ij - lse_i),  dp_ij = dout_i . v_j,  ds_ij = p_ij (dp_ij - D_i)
+//   dq_i = scale sum_j ds_ij k_j,  dk_j = scale sum_i ds_ij q_i,  dv_j = sum_i p_ij dout_i
+// paged attention: s_ij = scale q_i . k_j, v_j its own cache;
+// MLA:             s_ij = scale (q_i . c_j + qp_i . kp_j), k_j = v_j = c_j, so
+//                  dc_j = sum_i (p_ij dout_i + scale ds_ij q_i), dkp_j = scale
+//                  sum_i ds_ij qp_i, dqp_i = scale sum_j ds_ij kp_j.
+//
+// Two kernels after the preprocess and the page index:
+//  - key-major (dkdv_kernel): a CTA owns up to ROWS key slots of one physical
+//    page and key/value head, keeps their rows in registers, and walks the
+//    table entries that read the page (ascending), and for each the (query,
+//    head) rows of that sequence (ascending) staged through shared memory;
+//    slots of a page nobody reads are written as zeros;
+//  - query-major (dq_kernel): a CTA owns ROWS (query, head) rows of one
+//    sequence and key/value head and streams the sequence's keys, gathered
+//    through the page table, through shared memory.
+// TPK threads share a row (or key), each owning DK/TPK elements; the dot
+// products are reduced with log2(TPK) xor shuffles.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "paged_bwd.h"
+#include "params.h"
+#include "ptx.cuh"
+#include "simt.cuh"
+
+namespace attn {
+namespace pbwd {
+
+using simt::axpy4;
+using simt::dot4;
+using simt::load4;
+using simt::store4;
+
+constexpr int THREADS = 256;
+
+// DK: width of q, k, v, dout (D, or the latent rank R); PD: positional width
+// (MLA only); TPK: threads per row or key.
+template <int DK, int PD, int TPK>
+struct Cfg {
+  static constexpr int G = DK / 4, PG = PD / 4;
+  static constexpr int GPT = G / TPK;                // float4 groups of a main vector per thread
+  static constexpr int PPT = (PG + TPK - 1) / TPK;   // positional groups per thread (some idle)
+  static constexpr int ROWS = THREADS / TPK;         // keys (key-major) or rows (query-major) per CTA
+  static constexpr int RT = DK <= 128 ? 32 : 16;     // rows or keys per shared-memory tile
+  static_assert(G % TPK == 0 && GPT >= 1, "DK must split evenly over TPK threads");
+  static constexpr size_t dkdv_smem(bool) { return static_cast<size_t>(RT) * (2 * G + PG) * 16 + RT * 12; }
+  static constexpr size_t dq_smem(bool mla) { return static_cast<size_t>(RT) * ((mla ? 1 : 2) * G + PG) * 16; }
+};
+
+template <int TPK>
+__device__ __forceinline__ float quad_sum(float x) {
+#pragma unroll
+  for (int o = 1; o < TPK; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__device__ __forceinline__ int keys_of(const PagedParams& pp, int s) {
+  const int64_t cap = static_cast<int64_t>(pp.max_pages) * pp.page_size;
+  const int L = __ldg(pp.seq_lens + s);
+  return L < 0 ? 0 : (L > cap ? static_cast<int>(cap) : L);
+}
+
+__device__ __forceinline__ int clamp_off(const PagedParams& pp, int s) {
+  const int o = __ldg(pp.q_offsets + s);
+  return o < 0 ? 0 : (o > pp.num_queries ? pp.num_queries : o);
+}
+
+// The query rows of sequence s: [q0, q0 + n).
+__device__ __forceinline__ void rows_of(const PagedParams& pp, int s, int& q0, int& n) {
+  q0 = clamp_off(pp, s);
+  const int q1 = clamp_off(pp, s + 1);
+  n = q1 > q0 ? q1 - q0 : 0;
+}
+
+__device__ __forceinline__ int position_of(const PagedParams& pp, int row, int q0, int n, int L) {
+  return pp.positions ? __ldg(pp.positions + row) : L - n + (row - q0);
+}
+
+template <int DK, int PD, int TPK, int DT, bool MLA>
+__global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ q, const void* __restrict__ qp,
+                                                       const void* __restrict__ k, const void* __restrict__ kp,
+                                                       const void* __restrict__ v, const void* __restrict__ dout,
+                                                       const Buffers b, void* __restrict__ dk,
+                                                       void* __restrict__ dkp, void* __restrict__ dv,
+                                                       const PagedParams pp, float scale, int kpc) {
+  using C = Cfg<DK, PD, TPK>;
+  constexpr int G = C::G, PG = C::PG, GPT = C::GPT, PPT = C::PPT, RT = C::RT;
+  extern __shared__ float4 smem[];
+  float4* qs = smem;             // [RT][G]
+  float4* gs = qs + RT * G;      // [RT][G]
+  float4* qps = gs + RT * G;     // [RT][PG]
+  float* ls = reinterpret_cast<float*>(qps + RT * PG);
+  float* dss = ls + RT;
+  int* ps = reinterpret_cast<int*>(dss + RT);
+
+  const int tid = threadIdx.x, part = tid % TPK, kl = tid / TPK;
+  const int page = blockIdx.x / pp.Hkv, hk = blockIdx.x - page * pp.Hkv;
+  const int group = pp.Hq / pp.Hkv;
+  const int P = pp.page_size;
+  const int t0 = blockIdx.y * kpc;
+  const int t = t0 + kl;
+  const bool key_ok = kl < kpc && t < P;
+  const size_t slot = static_cast<size_t>(page) * P + (key_ok ? t : 0);
+  const size_t krow = (slot * pp.Hkv + hk) * G;
+
+  float4 kr[GPT], vr[GPT], dka[GPT], dva[GPT], kpr[PPT > 0 ? PPT : 1], dkpa[PPT > 0 ? PPT : 1];
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < GPT; ++c) {
+    kr[c] = key_ok ? load4<DT>(k, krow + part + TPK * c) : z;
+    if constexpr (!MLA) vr[c] = key_ok ? load4<DT>(v, krow + part + TPK * c) : z;
+    dka[c] = dva[c] = z;
+  }
+#pragma unroll
+  for (int c = 0; c < PPT; ++c) {
+    const int gi = part + TPK * c;
+    kpr[c] = (key_ok && gi < PG) ? load4<DT>(kp, slot * PG + gi) : z;
+    dkpa[c] = z;
+  }
+
+  const int r_lo = __ldg(b.offsets + page), r_hi = __ldg(b.offsets + page + 1);
+  for (int ri = r_lo; ri < r_hi; ++ri) {
+    const int code = __ldg(b.refs + ri);
+    const int s = code / pp.max_pages, blk = code - s * pp.max_pages;
+    const int L = keys_of(pp, s);
+    const int kmin = blk * P + t0;  // first key position of this CTA in sequence s
+    if (kmin >= L) continue;
+    int q0, n;
+    rows_of(pp, s, q0, n);
+    const int kpos = blk * P + t;
+    const bool key_vis = key_ok && kpos < L;
+    const int npairs = n * group;
+    int e_lo = 0;  // rows before e_lo see none of these keys (default positions only)
+    if (pp.causal && !pp.positions) e_lo = max(0, kmin - (L - n)) * group;
+    for (int e0 = e_lo; e0 < npairs; e0 += RT) {
+      __syncthreads();
+      for (int idx = tid; idx < RT * (2 * G + PG); idx += blockDim.x) {
+        const int r = idx / (2 * G + PG), c = idx - r * (2 * G + PG);
+        const int e = e0 + r;
+        const bool in = e < npairs;
+        const int qi = in ? e / group : 0;
+        const size_t rr = static_cast<size_t>(q0 + qi) * pp.Hq + hk * group + (in ? e - qi * group : 0);
+        if (c < G) qs[r * G + c] = in ? load4<DT>(q, rr * G + c) : z;
+        else if (c < 2 * G) gs[r * G + c - G] = in ? load4<DT>(dout, rr * G + c - G) : z;
+        else qps[r * PG + c - 2 * G] = in ? load4<DT>(qp, rr * PG + c - 2 * G) : z;
+      }
+      if (tid < RT) {
+        const int e = e0 + tid;
+        const bool in = e < npairs;
+        const int qi = in ? e / group : 0;
+        const size_t rr = static_cast<size_t>(q0 + qi) * pp.Hq + hk * group + (in ? e - qi * group : 0);
+        const float l2 = in ? b.lse2[rr] : -INFINITY;
+        ls[tid] = l2;
+        dss[tid] = l2 != -INFINITY ? b.dsum[rr] : 0.f;
+        ps[tid] = in ? position_of(pp, q0 + qi, q0, n, L) : -1;
+      }
+      __syncthreads();
+#pragma unroll 2
+      for (int r = 0; r < RT; ++r) {
+        float sd = 0.f, pd = 0.f;
+#pragma unroll
+        for (int c = 0; c < GPT; ++c) {
+          sd = dot4(qs[r * G + part + TPK * c], kr[c], sd);
+          pd = dot4(gs[r * G + part + TPK * c], MLA ? kr[c] : vr[c], pd);
+        }
+#pragma unroll
+        for (int c = 0; c < PPT; ++c)
+          if (part + TPK * c < PG) sd = dot4(qps[r * PG + part + TPK * c], kpr[c], sd);
+        sd = quad_sum<TPK>(sd);
+        pd = quad_sum<TPK>(pd);
+        const float l2 = ls[r];
+        const bool vis = key_vis && l2 != -INFINITY && (!pp.causal || kpos <= ps[r]);
+        const float pr = vis ? fast_exp2(sd * pp.scale_log2 - l2) : 0.f;
+        const float ds = vis ? pr * (pd - dss[r]) : 0.f;
+#pragma unroll
+        for (int c = 0; c < GPT; ++c) {
+          if constexpr (MLA) {
+            dka[c] = axpy4(pr, gs[r * G + part + TPK * c], dka[c]);
+            dka[c] = axpy4(ds * scale, qs[r * G + part + TPK * c], dka[c]);
+          } else {
+            dva[c] = axpy4(pr, gs[r * G + part + TPK * c], dva[c]);
+            dka[c] = axpy4(ds, qs[r * G + part + TPK * c], dka[c]);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < PPT; ++c)
+          if (part + TPK * c < PG) dkpa[c] = axpy4(ds, qps[r * PG + part + TPK * c], dkpa[c]);
+      }
+    }
+  }
+  if (!key_ok) return;
+#pragma unroll
+  for (int c = 0; c < GPT; ++c) {
+    const float4 a = dka[c];
+    if constexpr (MLA) {
+      if (dk) store4<DT>(dk, krow + part + TPK * c, a);
+    } else {
+      if (dk) store4<DT>(dk, krow + part + TPK * c, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
+      if (dv) store4<DT>(dv, krow + part + TPK * c, dva[c]);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < PPT; ++c) {
+    const int gi = part + TPK * c;
+    const float4 a = dkpa[c];
+    if (dkp && gi < PG)
+      store4<DT>(dkp, slot * PG + gi, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
+  }
+}
+
+template <int DK, int PD, int TPK, int DT, bool MLA>
+__global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q, const void* __restrict__ qp,
+                                                     const void* __restrict__ k, const void* __restrict__ kp,
+                                                     const void* __restrict__ v, const void* __restrict__ dout,
+                                                     const Buffers b, void* __restrict__ dq,
+                                                     void* __restrict__ dqp, const PagedParams pp, float scale) {
+  using C = Cfg<DK, PD, TPK>;
+  constexpr int G = C::G, PG = C::PG, GPT = C::GPT, PPT = C::PPT, RT = C::RT, ROWS = C::ROWS;
+  constexpr int VG = MLA ? 0 : G;  // value groups staged (MLA reuses the latent)
+  extern __shared__ float4 smem[];
+  float4* ks = smem;           // [RT][G]
+  float4* vs = ks + RT * G;    // [RT][VG]
+  float4* kps = vs + RT * VG;  // [RT][PG]
+  __shared__ int hi_s;
+
+  const int tid = threadIdx.x, part = tid % TPK, rl = tid / TPK;
+  const int s = blockIdx.x / pp.Hkv, hk = blockIdx.x - s * pp.Hkv;
+  const int group = pp.Hq / pp.Hkv;
+  const int P = pp.page_size;
+  int q0, n;
+  rows_of(pp, s, q0, n);
+  const int npairs = n * group;
+  const int e = blockIdx.y * ROWS + rl;
+  if (blockIdx.y * ROWS >= npairs) return;  // uniform over the CTA
+  const int L = keys_of(pp, s);
+  const bool row_ok = e < npairs;
+  const int qi = row_ok ? e / group : 0;
+  const size_t rr = static_cast<size_t>(q0 + qi) * pp.Hq + hk * group + (row_ok ? e - qi * group : 0);
+
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 qr[GPT], gr[GPT], acc[GPT], qpr[PPT > 0 ? PPT : 1], accp[PPT > 0 ? PPT : 1];
+#pragma unroll
+  for (int c = 0; c < GPT; ++c) {
+    qr[c] = row_ok ? load4<DT>(q, rr * G + part + TPK * c) : z;
+    gr[c] = row_ok ? load4<DT>(dout, rr * G + part + TPK * c) : z;
+    acc[c] = z;
+  }
+#pragma unroll
+  for (int c = 0; c < PPT; ++c) {
+    const int gi = part + TPK * c;
+    qpr[c] = (row_ok && gi < PG) ? load4<DT>(qp, rr * PG + gi) : z;
+    accp[c] = z;
+  }
+  const float l2 = row_ok ? b.lse2[rr] : -INFINITY;
+  const bool live = l2 != -INFINITY;
+  const float dsi = live ? b.dsum[rr] : 0.f;
+  const int pos = row_ok ? position_of(pp, q0 + qi, q0, n, L) : -1;
+  // keys past every row's causal limit are not visited
+  if (tid == 0) hi_s = 0;
+  __syncthreads();
+  if (live && part == 0) atomicMax(&hi_s, pp.causal ? min(L, max(pos + 1, 0)) : L);
+  __syncthreads();
+  const int hi = hi_s;
+
+  for (int key0 = 0; key0 < hi; key0 += RT) {
+    __syncthreads();
+    for (int idx = tid; idx < RT * (G + VG + PG); idx += blockDim.x) {
+      const int r = idx / (G + VG + PG), c = idx - r * (G + VG + PG);
+      const int j = key0 + r;
+      int pg = -1;
+      if (j < hi) pg = __ldg(pp.block_table + static_cast<size_t>(s) * pp.max_pages + j / P);
+      const bool ok = pg >= 0 && pg < pp.num_pages;  // entries outside the cache read as zero keys
+      const size_t sl = ok ? static_cast<size_t>(pg) * P + j % P : 0;
+      if (c < G) ks[r * G + c] = ok ? load4<DT>(k, (sl * pp.Hkv + hk) * G + c) : z;
+      else if (c < G + VG) vs[r * VG + c - G] = ok ? load4<DT>(v, (sl * pp.Hkv + hk) * G + c - G) : z;
+      else kps[r * PG + c - G - VG] = ok ? load4<DT>(kp, sl * PG + c - G - VG) : z;
+    }
+    __syncthreads();
+#pragma unroll 2
+    for (int c2 = 0; c2 < RT; ++c2) {
+      const int j = key0 + c2;
+      float sd = 0.f, pd = 0.f;
+#pragma unroll
+      for (int c = 0; c < GPT; ++c) {
+        sd = dot4(qr[c], ks[c2 * G + part + TPK * c], sd);
+        pd = dot4(gr[c], MLA ? ks[c2 * G + part + TPK * c] : vs[c2 * VG + part + TPK * c], pd);
+      }
+#pragma unroll
+      for (int c = 0; c < PPT; ++c)
+        if (part + TPK * c < PG) sd = dot4(qpr[c], kps[c2 * PG + part + TPK * c], sd);
+      sd = quad_sum<TPK>(sd);
+      pd = quad_sum<TPK>(pd);
+      const bool vis = live && j < L && (!pp.causal || j <= pos);
+      const float pr = vis ? fast_exp2(sd * pp.scale_log2 - l2) : 0.f;
+      const float ds = vis ? pr * (pd - dsi) : 0.f;
+#pragma unroll
+      for (int c = 0; c < GPT; ++c) acc[c] = axpy4(ds, ks[c2 * G + part + TPK * c], acc[c]);
+#pragma unroll
+      for (int c = 0; c < PPT; ++c)
+        if (part + TPK * c < PG) accp[c] = axpy4(ds, kps[c2 * PG + part + TPK * c], accp[c]);
+    }
+  }
+  if (!row_ok) return;
+#pragma unroll
+  for (int c = 0; c < GPT; ++c) {
+    const float4 a = acc[c];
+    if (dq) store4<DT>(dq, rr * G + part + TPK * c, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
+  }
+#pragma unroll
+  for (int c = 0; c < PPT; ++c) {
+    const int gi = part + TPK * c;
+    const float4 a = accp[c];
+    if (dqp && gi < PG)
+      store4<DT>(dqp, rr * PG + gi, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
+  }
+}
+
+// Launch both kernels of one instance (either may be skipped by passing no
+// outputs for it).
+template <int DK, int PD, int TPK, int DT, bool MLA>
+cudaError_t launch_instance(const PagedParams& pp, const void* q, const void* qp, const void* k, const void* kp,
+                            const void* v, const void* dout, const Buffers& b, void* dq, void* dqp, void* dk,
+                            void* dkp, void* dv, float scale, cudaStream_t st) {
+  using C = Cfg<DK, PD, TPK>;
+  const int group = pp.Hq / pp.Hkv;
+  if (dk || dkp || dv) {
+    // keys per CTA: the page's slots, rounded up so that a CTA is whole warps
+    const int unit = 32 / TPK;
+    const int kpc = pp.page_size >= C::ROWS ? C::ROWS : (pp.page_size + unit - 1) / unit * unit;
+    const dim3 grid(static_cast<unsigned>(pp.num_pages) * pp.Hkv,
+                    static_cast<unsigned>((pp.page_size + kpc - 1) / kpc));
+    const size_t smem = C::dkdv_smem(MLA);
+    auto kern = dkdv_kernel<DK, PD, TPK, DT, MLA>;
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    if (grid.x > 0) kern<<<grid, kpc * TPK, smem, st>>>(q, qp, k, kp, v, dout, b, dk, dkp, dv, pp, scale, kpc);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (dq || dqp) {
+    const int64_t blocks = (static_cast<int64_t>(pp.max_queries) * group + C::ROWS - 1) / C::ROWS;
+    const dim3 grid(static_cast<unsigned>(pp.num_seqs) * pp.Hkv, static_cast<unsigned>(blocks));
+    const size_t smem = C::dq_smem(MLA);
+    auto kern = dq_kernel<DK, PD, TPK, DT, MLA>;
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    if (grid.x > 0 && grid.y > 0) kern<<<grid, THREADS, smem, st>>>(q, qp, k, kp, v, dout, b, dq, dqp, pp, scale);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pbwd
+}  // namespace attn

@@ -326,6 +326,88 @@ ATTN_API int attn_paged_mla(const attn_mla_shape_t* shape,
  * Returns ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_SHAPE or ATTN_ERR_SPLITS. */
 ATTN_API int attn_paged_mla_workspace_bytes(const attn_mla_shape_t* shape, int num_splits, size_t* bytes);
 
+/* attn_paged_bwd - gradients of attn_paged_fwd for a loss whose gradient with
+ * respect to its output is `dout`: dq for the packed queries and the history
+ * gradients dk_cache, dv_cache in the shape of the physical caches.
+ * Asynchronous on `stream`.
+ *
+ * Source: ruDNN user guide, section 11 (backward of paged attention and
+ * ordered history gradients): the backward returns dq, dk, dv, recomputes the
+ * probabilities instead of storing the score matrix, may skip any gradient
+ * the caller does not want, and has an ordered variant that reduces the cache
+ * gradients without atomics through a workspace holding row statistics and a
+ * reverse page index. This call is that ordered variant: every gradient is
+ * summed in one fixed order (the readers of a page by ascending (sequence,
+ * block), their query rows and heads ascending), so repeated calls give
+ * identical bits. Per visible (query row i, key j), with the forward's lse_i:
+ *   p_ij = exp(scale q_i.k_j - lse_i),  dp_ij = dout_i . v_j,
+ *   D_i = dout_i . out_i,  ds_ij = p_ij (dp_ij - D_i),
+ *   dq_i = scale sum_j ds_ij k_j,  dk_j = scale sum_i ds_ij q_i,  dv_j = sum_i p_ij dout_i.
+ * A physical page read by several sequences (a shared prefix), or by one
+ * sequence at several blocks, receives the sum of every read; a page that no
+ * sequence with queries reads gets zeros. A row with no visible key (lse
+ * -inf) contributes nothing and gets dq = 0.
+ *
+ * shape, q, k_cache, v_cache, block_table, seq_lens, q_offsets, positions,
+ *   causal, scale, dtype: exactly as given to attn_paged_fwd (same metadata
+ *   rules; page-table entries outside [0, num_pages) read as zero keys and
+ *   receive nothing).
+ * out, dout: the forward output and dL/dO, [num_queries, Hq, D] in dtype.
+ * lse: the forward's float [num_queries, Hq] natural log-sum-exp.
+ * workspace: at least attn_paged_bwd_workspace_bytes(shape) bytes, 16-byte
+ *   aligned, caller-owned, disjoint from every other buffer.
+ * dq [num_queries, Hq, D], dk_cache, dv_cache [num_pages, page_size, Hkv, D]:
+ *   outputs in dtype, 16-byte aligned device pointers; each may be NULL (not
+ *   computed). dk_cache and dv_cache are written entirely; dq rows outside
+ *   every sequence's range (or beyond max_queries) are not written.
+ * D in {16, 32, 64, 128}, every dtype (fp32 FMA arithmetic). Returns ATTN_OK or
+ * a negative ATTN_ERR_* code (validation before any launch). */
+ATTN_API int attn_paged_bwd(const attn_paged_shape_t* shape,
+                            const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_table, const int32_t* seq_lens,
+                            const int32_t* q_offsets, const int32_t* positions,
+                            int causal, float scale, attn_dtype_t dtype,
+                            const void* out, const void* dout, const float* lse,
+                            void* workspace, size_t workspace_bytes,
+                            void* dq, void* dk_cache, void* dv_cache,
+                            void* stream);
+
+/* attn_paged_bwd_workspace_bytes - workspace attn_paged_bwd needs: two float
+ * arrays of num_queries * Hq (row statistics), num_pages + num_pages + 1 ints
+ * (reverse index counts and offsets) and num_seqs * max_pages ints (the index),
+ * each rounded up to 256 bytes. Returns ATTN_OK, ATTN_ERR_NULL or ATTN_ERR_SHAPE. */
+ATTN_API int attn_paged_bwd_workspace_bytes(const attn_paged_shape_t* shape, size_t* bytes);
+
+/* attn_paged_mla_bwd - gradients of attn_paged_mla: dq [num_queries, H, R],
+ * dqp [num_queries, H, Pd], and the cache-shaped dlatent [num_pages,
+ * page_size, 1, R] and dkpos [num_pages, page_size, 1, Pd].
+ *
+ * Source: ruDNN user guide, section 11: the MLA backward returns dq, dqp,
+ * dlatent and dkp, dlatent holding both the key and the value contribution of
+ * each latent row. With s_ij = scale (q_i . c_j + qp_i . kp_j) and v_j = c_j:
+ *   dc_j = sum_i (p_ij dout_i + scale ds_ij q_i),  dkp_j = scale sum_i ds_ij qp_i,
+ *   dq_i = scale sum_j ds_ij c_j,  dqp_i = scale sum_j ds_ij kp_j.
+ * Everything else (ordered summation, shared pages, skipped outputs, the
+ * workspace of attn_paged_mla_bwd_workspace_bytes, edge cases) is as for
+ * attn_paged_bwd with one latent head shared by all H heads. R in {128, 256,
+ * 512}, Pd in {0, 16, 32, 64}, every dtype (fp32 FMA arithmetic); with Pd == 0,
+ * qp, kpos, dqp and dkpos are ignored. */
+ATTN_API int attn_paged_mla_bwd(const attn_mla_shape_t* shape,
+                                const void* q, const void* qp,
+                                const void* latent, const void* kpos,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                const int32_t* q_offsets, const int32_t* positions,
+                                int causal, float scale, attn_dtype_t dtype,
+                                const void* out, const void* dout, const float* lse,
+                                void* workspace, size_t workspace_bytes,
+                                void* dq, void* dqp, void* dlatent, void* dkpos,
+                                void* stream);
+
+/* attn_paged_mla_bwd_workspace_bytes - workspace attn_paged_mla_bwd needs (the
+ * layout of attn_paged_bwd_workspace_bytes with Hq = H). Returns ATTN_OK,
+ * ATTN_ERR_NULL or ATTN_ERR_SHAPE. */
+ATTN_API int attn_paged_mla_bwd_workspace_bytes(const attn_mla_shape_t* shape, size_t* bytes);
+
 /* Size of the device scratch array built into the library for
  * attn_fwd_split_noalloc (32 MiB per GPU that loads the library). */
 #define ATTN_NOALLOC_SCRATCH_BYTES (32u << 20)

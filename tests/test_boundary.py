@@ -262,3 +262,67 @@ def test_host_call_argument_errors(lib):
     assert call(shape=_shape(B=2, D=48)) == codes["ATTN_ERR_HEAD_DIM"]
     assert call(out=None) == codes["ATTN_ERR_NULL"]
     assert call(shape=_shape(B=0)) == 0
+
+
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_paged_bwd_workspace_layout(lib):
+    # row statistics (2 x rows floats), page counts, page offsets, the index
+    s = A.PagedShape(3, 10, 4, 2, 64, 16, 7, 5, 4)
+    n = ctypes.c_size_t(0)
+    assert lib.attn_paged_bwd_workspace_bytes(ctypes.byref(s), ctypes.byref(n)) == 0
+    assert n.value == 2 * _r256(40 * 4) + _r256(7 * 4) + _r256(8 * 4) + _r256(15 * 4)
+    m = A.MlaShape(3, 10, 16, 512, 64, 64, 700, 50, 4)
+    assert lib.attn_paged_mla_bwd_workspace_bytes(ctypes.byref(m), ctypes.byref(n)) == 0
+    assert n.value == 2 * _r256(160 * 4) + _r256(700 * 4) + _r256(701 * 4) + _r256(150 * 4)
+    assert lib.attn_paged_bwd_workspace_bytes(None, ctypes.byref(n)) == codes["ATTN_ERR_NULL"]
+    bad = A.PagedShape(3, -1, 4, 2, 64, 16, 7, 5, 4)
+    assert lib.attn_paged_bwd_workspace_bytes(ctypes.byref(bad), ctypes.byref(n)) == codes["ATTN_ERR_SHAPE"]
+
+
+def _paged_bwd_call(lib, shape, ws=FAKE * 40, nbytes=1 << 20, dq=FAKE * 30, dk=FAKE * 31, dv=FAKE * 32,
+                    dtype=A.ATTN_BF16, causal=1, scale=0.125, lse=FAKE * 12, table=FAKE * 20):
+    # q, k, v, out, dout at FAKE x 1..5; metadata at FAKE x 20..23 (never dereferenced)
+    return lib.attn_paged_bwd(ctypes.byref(shape), FAKE, FAKE * 2, FAKE * 3, table or None, FAKE * 21, FAKE * 22,
+                              None, causal, ctypes.c_float(scale), dtype, FAKE * 4, FAKE * 5, lse or None,
+                              ws or None, nbytes, dq or None, dk or None, dv or None, None)
+
+
+def test_paged_bwd_argument_errors(lib):
+    s = A.PagedShape(2, 4, 2, 2, 64, 16, 3, 2, 2)
+    n = ctypes.c_size_t(0)
+    lib.attn_paged_bwd_workspace_bytes(ctypes.byref(s), ctypes.byref(n))
+    need = n.value
+    assert _paged_bwd_call(lib, s, ws=0) == codes["ATTN_ERR_WORKSPACE"]
+    assert _paged_bwd_call(lib, s, nbytes=need - 1) == codes["ATTN_ERR_WORKSPACE"]
+    assert _paged_bwd_call(lib, s, ws=FAKE * 40 + 4) == codes["ATTN_ERR_ALIGN"]
+    assert _paged_bwd_call(lib, s, dq=FAKE * 4) == codes["ATTN_ERR_OVERLAP"]        # dq on out
+    assert _paged_bwd_call(lib, s, dk=FAKE * 30) == codes["ATTN_ERR_OVERLAP"]       # dk on dq
+    assert _paged_bwd_call(lib, s, ws=FAKE * 32) == codes["ATTN_ERR_OVERLAP"]       # workspace on dv
+    assert _paged_bwd_call(lib, s, lse=0) == codes["ATTN_ERR_NULL"]
+    assert _paged_bwd_call(lib, s, table=0) == codes["ATTN_ERR_NULL"]
+    assert _paged_bwd_call(lib, s, dtype=9) == codes["ATTN_ERR_DTYPE"]
+    assert _paged_bwd_call(lib, s, causal=2) == codes["ATTN_ERR_MASK"]
+    assert _paged_bwd_call(lib, s, scale=float("inf")) == codes["ATTN_ERR_SCALE"]
+    assert _paged_bwd_call(lib, A.PagedShape(2, 4, 2, 2, 96, 16, 3, 2, 2)) == codes["ATTN_ERR_HEAD_DIM"]
+    assert _paged_bwd_call(lib, A.PagedShape(2, 4, 3, 2, 64, 16, 3, 2, 2)) == codes["ATTN_ERR_SHAPE"]
+    # nothing asked for: validated, then a no-op (no workspace needed)
+    assert _paged_bwd_call(lib, s, ws=0, dq=0, dk=0, dv=0) == codes["ATTN_OK"]
+
+
+def test_paged_mla_bwd_argument_errors(lib):
+    m = A.MlaShape(2, 4, 8, 256, 64, 16, 3, 2, 2)
+
+    def call(shape=m, ws=FAKE * 40, nbytes=1 << 20, dqp=FAKE * 33, qp=FAKE * 6, dtype=A.ATTN_BF16):
+        return lib.attn_paged_mla_bwd(ctypes.byref(shape), FAKE, qp or None, FAKE * 2, FAKE * 3, FAKE * 20,
+                                      FAKE * 21, FAKE * 22, None, 1, ctypes.c_float(0.1), dtype, FAKE * 4, FAKE * 5,
+                                      FAKE * 12, ws or None, nbytes, FAKE * 30, dqp or None, FAKE * 31, FAKE * 32,
+                                      None)
+    assert call(ws=0) == codes["ATTN_ERR_WORKSPACE"]
+    assert call(qp=0) == codes["ATTN_ERR_NULL"]
+    assert call(dqp=FAKE * 6) == codes["ATTN_ERR_OVERLAP"]
+    assert call(shape=A.MlaShape(2, 4, 8, 192, 64, 16, 3, 2, 2)) == codes["ATTN_ERR_HEAD_DIM"]
+    assert call(shape=A.MlaShape(2, 4, 8, 256, 48, 16, 3, 2, 2)) == codes["ATTN_ERR_HEAD_DIM"]
+    assert call(dtype=5) == codes["ATTN_ERR_DTYPE"]
