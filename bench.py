@@ -497,8 +497,23 @@ def bench_paged(args):
         tensor = (w.dtype != "f32" and w.D in (64, 128) and w.page_size % 8 == 0
                   and (128 % w.page_size == 0 or w.page_size % 128 == 0))
     launches = 2 if need > 0 and (decode or (is_mla and tensor)) else 1
+    bwd = args.pass_ == "bwd"
+    if bwd:  # the forward's output and statistics once, untimed; a random dL/dO
+        call = attn.paged_mla if is_mla else attn.paged_fwd
+        fo, flse = call(*t, ints["block_table"], ints["seq_lens"], ints["q_offsets"], positions=pos,
+                        causal=w.causal, scale=x["scale"], max_queries=max_q, return_lse=True)
+        g = make_device_tensor(synth.to_storage(synth.normal_f32(w.seed, 9, x["q"].shape), w.dtype), w.dtype, device)
+        need = attn.mla_bwd_workspace_bytes(shp) if is_mla else attn.paged_bwd_workspace_bytes(shp)
+        pws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+        # preprocess, page-index count / scan / fill / sort, key-major and query-major kernels
+        launches = 7
 
     def step():
+        if bwd:
+            call = attn.paged_mla_bwd if is_mla else attn.paged_bwd
+            call(*t, ints["block_table"], ints["seq_lens"], ints["q_offsets"], g, out=fo, lse=flse, positions=pos,
+                 causal=w.causal, scale=x["scale"], max_queries=max_q, workspace=pws, stream=stream)
+            return
         call = attn.paged_mla if is_mla else attn.paged_fwd
         call(*t, ints["block_table"], ints["seq_lens"], ints["q_offsets"], positions=pos, causal=w.causal,
              scale=x["scale"], max_queries=max_q, out=out, stream=stream, num_splits=splits, workspace=pws)
@@ -539,6 +554,10 @@ def bench_paged(args):
     else:
         flops = 4.0 * w.D * w.Hq * pairs
         nbytes = (2 * nkt * w.Hkv * w.D + 2 * nqt * w.Hq * w.D) * es
+    flops_basis = "exact: per visible (query, key) pair and head"
+    if bwd:  # nominal backward work: 2.5x the forward's (5 matmuls for 2)
+        flops, flops_basis = 2.5 * flops, "2.5 x forward (" + flops_basis + ")"
+        nbytes *= 2  # inputs and out/dout read, gradients written: twice the forward's bytes
     value = replica_throughput(flops, ms * 1e-3, world) / 1e12
     if rank != 0:
         return
@@ -553,7 +572,11 @@ def bench_paged(args):
     # is held to whichever of the tensor and HBM rooflines binds (the larger
     # ideal time); the rest runs on the fp32 FMA pipes
     mla_hbm = is_mla and tensor and nbytes / float(peaks["hbm_gbs"]) > flops / (float(peaks["bf16_tflops"]) * 1e3)
-    if decode or mla_hbm:
+    if bwd:  # the backward over a paged cache runs on the fp32 FMA pipes
+        roof = {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
+                "peak_kind": f"fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x {mhz:.0f} MHz",
+                "kernel": "dkdv_kernel + dq_kernel (paged backward, whole call)"}
+    elif decode or mla_hbm:
         roof = {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                 "frac": gbs / float(peaks["hbm_gbs"]), "peak_kind": f"{peak_kind} HBM copy",
                 "kernel": "mla_tc_kernel" if is_mla else ("paged_tc_kernel" if tensor else "paged_decode_kernel")}
@@ -569,14 +592,15 @@ def bench_paged(args):
     roof.update({"traffic": None, "algorithmic_bytes": nbytes})
     heads = {"H": w.H, "R": w.R, "Pd": w.Pd} if is_mla else {"Hq": w.Hq, "Hkv": w.Hkv, "D": w.D}
     line = {
-        "metric": f"{'MLA' if is_mla else 'paged attention'} TFLOP/s ({w.name})", "value": value, "unit": "TFLOP/s",
+        "metric": f"{'MLA' if is_mla else 'paged attention'}{' bwd' if bwd else ''} TFLOP/s ({w.name})",
+        "value": value, "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "num_seqs": w.num_seqs, **heads, "page_size": w.page_size, "ctx_range": list(w.ctx_range), "q_range": list(w.q_range),
                    "queries": int(x["q_offsets"][-1]), "keys": int(x["seq_lens"].sum()),
-                   "parallelism": f"replicas x{world}", "flops_basis": "exact: per visible (query, key) pair and head",
-                   "num_splits": splits if (decode or (is_mla and tensor)) else 1,
+                   "parallelism": f"replicas x{world}", "flops_basis": flops_basis,
+                   "num_splits": splits if (decode or (is_mla and tensor)) and not bwd else 1,
                    "l2": f"cache read {nbytes / 2**20:.0f} MiB per step"},
         "roofline": roof, "hbm_gbs_algorithmic": gbs, "e2e": None,
         "gpu_launches": args.steps * launches, "clocks": clocks.summary(),
@@ -595,7 +619,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=sorted(synth.WORKLOADS) + sorted(synth.PAGED_WORKLOADS) + sorted(synth.MLA_WORKLOADS))
     ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"],
-                    help="time the forward (default) or the backward (attn_bwd) of the workload")
+                    help="time the forward (default) or the backward (attn_bwd, attn_paged_bwd, "
+                         "attn_paged_mla_bwd) of the workload")
     ap.add_argument("--splits", type=int, default=0,
                     help="key-range splits (attn_fwd_split); 0 = the workload's default")
     ap.add_argument("--threads", type=int, default=0,

@@ -872,6 +872,25 @@ int attn_paged_bwd(const attn_paged_shape_t* shape, const void* q, const void* k
   e = attn::pbwd::launch_preprocess(static_cast<int>(dtype), s.D, out, dout, lse, b,
                                     static_cast<int64_t>(s.num_queries) * s.Hq, st);
   if (e == cudaSuccess && (dk_cache || dv_cache)) e = attn::pbwd::launch_page_index(pp, b, st);
+  // F16/BF16 with D in {64, 128} and a page size the 128-key tile gathers
+  // cover take the tensor cores; the pages that do not have exactly one reader
+  // then go through the fp32 FMA key-major kernel
+  const bool page_ok = s.page_size % 8 == 0 && (128 % s.page_size == 0 || s.page_size % 128 == 0);
+  if (e == cudaSuccess && dtype != ATTN_F32 && (s.D == 64 || s.D == 128) && page_ok && s.num_pages > 0) {
+    attn::EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail_cuda(cudaErrorNotSupported);
+    const attn::pbwd::TcArgs ta{b.lse2, b.dsum, b.offsets, dq, dk_cache, dv_cache, scale};
+    const bool bf = dtype == ATTN_BF16;
+    using attn::pbwd::launch_paged_bwd_tc;
+    if (s.D == 128) e = bf ? launch_paged_bwd_tc<128, true>(enc, pp, q, k_cache, v_cache, dout, ta, st)
+                           : launch_paged_bwd_tc<128, false>(enc, pp, q, k_cache, v_cache, dout, ta, st);
+    else e = bf ? launch_paged_bwd_tc<64, true>(enc, pp, q, k_cache, v_cache, dout, ta, st)
+                : launch_paged_bwd_tc<64, false>(enc, pp, q, k_cache, v_cache, dout, ta, st);
+    if (e == cudaSuccess && (dk_cache || dv_cache))
+      e = attn::pbwd::launch_paged_dkdv_shared(s.D, static_cast<int>(dtype), pp, q, k_cache, v_cache, dout, b,
+                                               dk_cache, dv_cache, scale, st);
+    return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+  }
   if (e == cudaSuccess)
     e = attn::pbwd::launch_paged_bwd(s.D, static_cast<int>(dtype), pp, q, k_cache, v_cache, dout, b, dq, dk_cache,
                                      dv_cache, scale, st);

@@ -199,5 +199,19 @@ cudaError_t launch_paged_bwd(int D, int dtype, const PagedParams& pp, const void
 #undef ATTN_PBWD
 }
 
+cudaError_t launch_paged_dkdv_shared(int D, int dtype, const PagedParams& pp, const void* q, const void* k,
+                                     const void* v, const void* dout, const Buffers& b, void* dk, void* dv,
+                                     float scale, cudaStream_t st) {
+#define ATTN_PBWD(DD, TT)                                                                                   \
+  launch_instance<DD, 0, 4, TT, false>(pp, q, nullptr, k, nullptr, v, dout, b, nullptr, nullptr, dk, nullptr, dv, \
+                                       scale, st, true)
+  switch (D) {
+    case 64: return dtype == 1 ? ATTN_PBWD(64, 1) : ATTN_PBWD(64, 2);
+    case 128: return dtype == 1 ? ATTN_PBWD(128, 1) : ATTN_PBWD(128, 2);
+    default: return cudaErrorInvalidValue;
+  }
+#undef ATTN_PBWD
+}
+
 }  // namespace pbwd
 }  // namespace attn

@@ -1,0 +1,659 @@
+// attn_paged_bwd_tc.cuh - the backward over a paged cache on the tcgen05
+// tensor cores (F16/BF16, D in {64, 128}, page_size a multiple of 8 that
+// divides 128 or a multiple of 128).
+//
+// Source: ruDNN user guide, section 11 (backward of paged attention): dq for
+// the packed queries and the history gradients dk, dv in the cache's shape,
+// the probabilities recomputed from the forward's statistics; ordered, no
+// atomics.
+//
+// The two kernels are the dense backward's (attn_bwd_tc.cuh: 384 threads, 8
+// elementwise warps, a TMA producer, an MMA issuer; the same MMA order, TMEM
+// map and packing) with paged addressing:
+//  - rows and columns of the query side are (query, head) pairs of one
+//    sequence and of a block of gp query heads sharing a kv head (gp = Hq/Hkv
+//    when it divides 128, else 1), packed query-major: pair = query * gp +
+//    head-in-block; a tile of 128 pairs is one TMA box of the 4-D view
+//    [queries, Hq/gp, gp, D] (the paged forward's view), so a decode step's
+//    gp heads share one tile;
+//  - a K/V tile of 128 keys of a sequence is gathered page by page through
+//    the 4-D view [pages, page_size, Hkv, D] of the cache (boxes of
+//    min(page_size, 128) rows; a page id outside the cache loads zeros);
+//  - pair p sees key j when p's query exists in the sequence, j < seq_len and,
+//    causal, j <= its position (explicit, or the newest-token default);
+//  - paged_dkdv_tc_kernel: CTA = (sequence, 128-key block, kv head), K and V
+//    resident, the (Q, dO) tiles of every head block of the group streamed.
+//    Its key rows are stored straight into the cache gradients only for the
+//    physical pages with exactly one reader (the reverse index's count); pages
+//    read by several sequences (or blocks), or by none, are left to the fp32
+//    FMA key-major kernel, which sums their readers in the index order;
+//  - paged_dq_tc_kernel: CTA = (sequence, head block, 128 pairs), Q and dO
+//    resident, the sequence's K/V tiles streamed; the rows of its sequence
+//    are stored directly.
+#pragma once
+
+#include <atomic>
+
+#include "attn_bwd_tc.cuh"
+#include "paged_bwd.h"
+#include "params.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace pbwd {
+namespace tc {
+
+using bwdtc::BR;
+using bwdtc::Cfg;
+using bwdtc::DqCfg;
+using bwdtc::NUM_THREADS;
+using bwdtc::REG_EW;
+using bwdtc::REG_OTHER;
+using bwdtc::TMEM_COLS;
+using bwdtc::WARP_MMA;
+using bwdtc::WARP_TMA;
+using bwdtc::kstep16;
+using bwdtc::store_row16;
+using bwdtc::tmem_a_kstep;
+using bwdtc::tmem_ld64;
+using bwdtc::tmem_st_packed64;
+
+__device__ __forceinline__ int seq_keys(const PagedParams& pp, int s) {
+  const int64_t cap = static_cast<int64_t>(pp.max_pages) * pp.page_size;
+  const int L = __ldg(pp.seq_lens + s);
+  return L < 0 ? 0 : (L > cap ? static_cast<int>(cap) : L);
+}
+
+__device__ __forceinline__ void seq_rows(const PagedParams& pp, int s, int& q0, int& n) {
+  int a = __ldg(pp.q_offsets + s), b = __ldg(pp.q_offsets + s + 1);
+  a = a < 0 ? 0 : (a > pp.num_queries ? pp.num_queries : a);
+  b = b < 0 ? 0 : (b > pp.num_queries ? pp.num_queries : b);
+  q0 = a;
+  n = b > a ? b - a : 0;
+}
+
+// Load the 128 keys [key0, key0 + 128) of a sequence's page table into a
+// swizzled tile (one box per page, or one box inside a page of >= 128 keys).
+template <int D>
+__device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap* m, uint32_t bar, const int32_t* table,
+                                             const PagedParams& pp, int key0, int hk) {
+  using C = Cfg<D>;
+  const int box_rows = pp.page_size < BR ? pp.page_size : BR;
+  const int boxes = BR / box_rows;
+  for (int i = 0; i < boxes; ++i) {
+    const int key = key0 + i * box_rows;
+    const int pidx = key / pp.page_size;
+    const int page = pidx < pp.max_pages ? __ldg(table + pidx) : -1;  // -1: a zero-filled box
+    for (int c = 0; c < C::NCHUNK; ++c)
+      tma_load_4d(dst + c * C::CHUNK_BYTES + i * box_rows * 128, m, bar, c * C::BOX_D, hk, key % pp.page_size,
+                  page);
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    paged_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         const PagedParams pp, const TcArgs a, int kblocks, int gp) {
+  using C = Cfg<D>;
+  // ---- work: key block kb of sequence s, kv head hk
+  const int lin = static_cast<int>(blockIdx.x);
+  const int kb = lin % kblocks;
+  const int rest = lin / kblocks;
+  const int hk = rest % pp.Hkv, s = rest / pp.Hkv;
+  const int L = seq_keys(pp, s);
+  int q0, n;
+  seq_rows(pp, s, q0, n);
+  const int P = pp.page_size;
+  const int used = (L + P - 1) / P;  // pages the sequence reads
+  const int key0 = kb * BR;
+  if (n == 0 || key0 >= used * P) return;  // not a block of this sequence's pages (uniform)
+  const int group = pp.Hq / pp.Hkv;
+  const int hblocks = group / gp;
+  const int ptiles = (n * gp + BR - 1) / BR;  // tiles of 128 (query, head) pairs per head block
+  const int diag = L - n;                      // default positions: query qi sits at diag + qi
+  const bool dflt = pp.positions == nullptr;
+  const int t_lo = (pp.causal && dflt) ? (max(0, key0 - diag) * gp) / BR : 0;
+  const int per_hb = key0 < L ? max(0, ptiles - t_lo) : 0;
+  const int N = per_hb * hblocks;
+  const int32_t* table = pp.block_table + static_cast<size_t>(s) * pp.max_pages;
+
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < C::STAGES; ++st) {
+      mbar_init(bar(C::BAR_FULL + st), 1);
+      mbar_init(bar(C::BAR_EMPTY + st), 1);
+    }
+    mbar_init(bar(C::BAR_RES), 1);
+    mbar_init(bar(C::BAR_S), 1);
+    mbar_init(bar(C::BAR_S + 1), 1);
+    mbar_init(bar(C::BAR_DP), 1);
+    mbar_init(bar(C::BAR_P), 256);
+    mbar_init(bar(C::BAR_DS), 256);
+    mbar_init(bar(C::BAR_DONE), 1);
+    mbar_init_fence();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto fail = [&]() {
+    if (pp.status) atomicOr(pp.status, STATUS_TIMEOUT);
+  };
+
+  if (warp >= 8) {
+    setmaxnreg_dec<REG_OTHER>();
+    if (warp == WARP_TMA && lane == 0 && N > 0) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(bar(C::BAR_RES), 2 * C::TILE_BYTES);
+      load_kv_tile<D>(sb, &tm_k, bar(C::BAR_RES), table, pp, key0, hk);
+      load_kv_tile<D>(sb + C::TILE_BYTES, &tm_v, bar(C::BAR_RES), table, pp, key0, hk);
+      int it = 0;
+      for (; it < N; ++it) {
+        const int st = it % C::STAGES;
+        if (!mbar_wait(bar(C::BAR_EMPTY + st), ((it / C::STAGES) & 1) ^ 1)) { fail(); break; }
+        const int hb = it / per_hb, t = t_lo + (it - hb * per_hb);
+        const int hh = hk * hblocks + hb;  // head block in [0, Hq / gp)
+        const int qs = q0 + t * (BR / gp);
+        const uint32_t dst = sb + C::OFF_RING + st * 2 * C::TILE_BYTES;
+        mbar_arrive_expect_tx(bar(C::BAR_FULL + st), 2 * C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          tma_load_4d(dst + c * C::CHUNK_BYTES, &tm_q, bar(C::BAR_FULL + st), c * C::BOX_D, 0, hh, qs);
+          tma_load_4d(dst + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_do, bar(C::BAR_FULL + st), c * C::BOX_D, 0, hh,
+                      qs);
+        }
+      }
+      for (int st = 0; st < C::STAGES && st < it; ++st) {
+        const int fills = (it - st + C::STAGES - 1) / C::STAGES;
+        if (!mbar_wait(bar(C::BAR_FULL + st), (fills - 1) & 1)) fail();
+      }
+      if (!mbar_wait(bar(C::BAR_RES), 0)) fail();
+    } else if (warp == WARP_MMA && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer (the dense kernel's)
+      constexpr uint32_t idesc_s = make_idesc_f16(BF16, BR, BR, false);
+      constexpr uint32_t idesc_o = make_idesc_f16(BF16, BR, D, true);
+      constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
+      constexpr uint32_t RSTEP16 = (16 * 128) >> 4;
+      const uint64_t dk_a = smem_desc(sb, 16, C::SBO, C::LAYOUT);
+      const uint64_t dv_a = smem_desc(sb + C::TILE_BYTES, 16, C::SBO, C::LAYOUT);
+      const uint64_t ring_k = smem_desc(sb + C::OFF_RING, 16, C::SBO, C::LAYOUT);
+      const uint64_t ring_mn = smem_desc(sb + C::OFF_RING, C::CHUNK_BYTES, C::SBO, C::LAYOUT);
+      bool ok = true;
+      auto issue_s = [&](int it) {
+        const int st = it % C::STAGES;
+        if (!mbar_wait(bar(C::BAR_FULL + st), (it / C::STAGES) & 1)) return false;
+        tc_fence_after();
+        const uint64_t q = ring_k + st * 2 * TILE16;
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_D; ++k)
+          umma_ss(tmem + 0, dk_a + kstep16<D>(k), q + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
+        umma_commit(bar(C::BAR_S));
+        return true;
+      };
+      auto issue_dp = [&](int it) {
+        const int st = it % C::STAGES;
+        const uint64_t g = ring_k + st * 2 * TILE16 + TILE16;
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_D; ++k)
+          umma_ss(tmem + BR, dv_a + kstep16<D>(k), g + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
+        umma_commit(bar(C::BAR_DP));
+      };
+      if (N > 0) {
+        if (!mbar_wait(bar(C::BAR_RES), 0)) ok = false;
+        tc_fence_after();
+        if (ok && !issue_s(0)) ok = false;
+        if (ok) issue_dp(0);
+        for (int it = 0; it < N && ok; ++it) {
+          const int st = it % C::STAGES;
+          if (!mbar_wait(bar(C::BAR_P), it & 1)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const uint64_t g = ring_mn + st * 2 * TILE16 + TILE16;
+#pragma unroll
+            for (int k = 0; k < C::KSTEPS_R; ++k)
+              umma_ts(tmem + 256, tmem + tmem_a_kstep(k), g + k * RSTEP16, idesc_o, (it > 0 || k > 0) ? 1u : 0u);
+          }
+          if (it + 1 < N && !issue_s(it + 1)) { ok = false; break; }
+          if (!mbar_wait(bar(C::BAR_DS), it & 1)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const uint64_t q = ring_mn + st * 2 * TILE16;
+#pragma unroll
+            for (int k = 0; k < C::KSTEPS_R; ++k)
+              umma_ts(tmem + 256 + D, tmem + BR + tmem_a_kstep(k), q + k * RSTEP16, idesc_o,
+                      (it > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit(bar(C::BAR_EMPTY + st));
+          if (it + 1 < N) issue_dp(it + 1);
+        }
+      }
+      if (!ok) fail();
+      umma_commit(bar(C::BAR_DONE));
+      if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- elementwise
+    setmaxnreg_inc<REG_EW>();
+    const int half = warp >> 2;                // pair columns [64 half, +64) of the tile
+    const int row = ((warp & 3) << 5) + lane;  // key row = TMEM lane
+    const int key = key0 + row;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    const uint32_t tS = tmem + lane_off, tDP = tS + BR;
+    const float sc = pp.scale_log2;
+    const bool key_vis = key < L;
+    bool failed = false;
+    for (int it = 0; it < N; ++it) {
+      const int hb = it / per_hb, t = t_lo + (it - hb * per_hb);
+      // statistics and position of pair columns lane and lane + 32 of this warpgroup's 64
+      float l2v[2], dsv[2];
+      int posv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int pair = t * BR + 64 * half + 32 * u + lane;
+        const int qi = pair / gp;
+        const int hq = hk * group + hb * gp + (pair - qi * gp);
+        const bool in = qi < n;
+        const size_t ri = static_cast<size_t>(q0 + qi) * pp.Hq + hq;
+        l2v[u] = in ? __ldg(a.lse2 + ri) : -INFINITY;
+        dsv[u] = in ? __ldg(a.dsum + ri) : 0.f;
+        posv[u] = in ? (dflt ? diag + qi : __ldg(pp.positions + q0 + qi)) : -1;
+      }
+      float x[64];
+      const bool ok = mbar_wait(bar(C::BAR_S), it & 1);
+      if (__any_sync(0xffffffffu, !ok)) { failed = true; break; }
+      tc_fence_after();
+      tmem_ld64<BF16>(tS + 64 * half, x);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float l2 = __shfl_sync(0xffffffffu, c < 32 ? l2v[0] : l2v[1], c & 31);
+        const int pos = __shfl_sync(0xffffffffu, c < 32 ? posv[0] : posv[1], c & 31);
+        const bool vis = key_vis && (!pp.causal || key <= pos) && l2 != -INFINITY;
+        x[c] = vis ? fast_exp2(x[c] * sc - l2) : 0.f;
+      }
+      tmem_st_packed64<BF16>(tS + 64 * half, x);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::BAR_P));
+      const bool ok2 = mbar_wait(bar(C::BAR_DP), it & 1);
+      if (__any_sync(0xffffffffu, !ok2)) { failed = true; break; }
+      tc_fence_after();
+      float dp[64];
+      tmem_ld64<BF16>(tDP + 64 * half, dp);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float dsi = __shfl_sync(0xffffffffu, c < 32 ? dsv[0] : dsv[1], c & 31);
+        dp[c] = x[c] * (dp[c] - dsi);
+      }
+      tmem_st_packed64<BF16>(tDP + 64 * half, dp);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::BAR_DS));
+    }
+    // ---------------------------------------------------------------- epilogue
+    // warpgroup 0 writes dK (scaled), warpgroup 1 dV; a key row goes to its
+    // physical slot when its page has exactly one reader
+    if (failed) {
+      if (lane == 0) fail();
+    } else {
+      bool ok = true;
+      if (N > 0) {
+        ok = mbar_wait(bar(C::BAR_DONE), 0);
+        if (__any_sync(0xffffffffu, !ok)) { ok = false; if (lane == 0) fail(); }
+      }
+      const int pidx = key / P;
+      int page = pidx < used ? __ldg(table + pidx) : -1;
+      if (page >= pp.num_pages || (page >= 0 && __ldg(a.offsets + page + 1) - __ldg(a.offsets + page) != 1))
+        page = -1;
+      void* dst = half == 0 ? a.dk : a.dv;
+      if (ok) {
+        tc_fence_after();
+        const uint32_t src = tmem + lane_off + 256 + (half == 0 ? D : 0);
+        const float mul = half == 0 ? a.scale : 1.f;
+        uint8_t* rowp = static_cast<uint8_t*>(dst) +
+                        ((static_cast<size_t>(page < 0 ? 0 : page) * P + key % P) * pp.Hkv + hk) * D * 2;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float v[32];
+          if (N > 0) {
+            uint32_t r[32];
+            tmem_ld32(src + 32 * c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0.f;
+          }
+          if (page >= 0 && dst) store_row16<BF16, 32>(rowp + c * 64, v, mul);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    paged_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const PagedParams pp, const TcArgs a, int qtiles, int gp) {
+  using C = Cfg<D>;
+  using Q = DqCfg<D>;
+  // ---- work: 128 (query, head) pairs of head block hh of sequence s
+  const int lin = static_cast<int>(blockIdx.x);
+  const int t = lin % qtiles;
+  const int rest = lin / qtiles;
+  const int nhb = pp.Hq / gp;
+  const int hh = rest % nhb, s = rest / nhb;
+  int q0, n;
+  seq_rows(pp, s, q0, n);
+  if (t * BR >= n * gp) return;  // uniform
+  const int L = seq_keys(pp, s);
+  const int group = pp.Hq / pp.Hkv;
+  const int hk = hh * gp / group;
+  const int diag = L - n;
+  const bool dflt = pp.positions == nullptr;
+  int hi = L;  // keys past every row's causal limit are not visited (default positions)
+  if (pp.causal && dflt) hi = min(hi, max(0, diag + min(n - 1, ((t + 1) * BR - 1) / gp) + 1));
+  const int N = hi > 0 ? (hi + BR - 1) / BR : 0;
+  const int32_t* table = pp.block_table + static_cast<size_t>(s) * pp.max_pages;
+
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + Q::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Q::OFF_MISC);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < Q::KST; ++st) {
+      mbar_init(bar(Q::BAR_KFULL + st), 1);
+      mbar_init(bar(Q::BAR_KEMPTY + st), 1);
+    }
+    for (int st = 0; st < Q::VST; ++st) {
+      mbar_init(bar(Q::BAR_VFULL + st), 1);
+      mbar_init(bar(Q::BAR_VEMPTY + st), 1);
+    }
+    mbar_init(bar(Q::BAR_RES), 1);
+    mbar_init(bar(Q::BAR_S), 1);
+    mbar_init(bar(Q::BAR_S + 1), 1);
+    mbar_init(bar(Q::BAR_DP), 1);
+    mbar_init(bar(Q::BAR_DS), 256);
+    mbar_init(bar(Q::BAR_DONE), 1);
+    mbar_init_fence();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto fail = [&]() {
+    if (pp.status) atomicOr(pp.status, STATUS_TIMEOUT);
+  };
+
+  if (warp >= 8) {
+    setmaxnreg_dec<REG_OTHER>();
+    if (warp == WARP_TMA && lane == 0 && N > 0) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const int qs = q0 + t * (BR / gp);
+      mbar_arrive_expect_tx(bar(Q::BAR_RES), 2 * C::TILE_BYTES);
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        tma_load_4d(sb + c * C::CHUNK_BYTES, &tm_q, bar(Q::BAR_RES), c * C::BOX_D, 0, hh, qs);
+        tma_load_4d(sb + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_do, bar(Q::BAR_RES), c * C::BOX_D, 0, hh, qs);
+      }
+      int nk = 0, nv = 0;
+      bool ok = true;
+      for (int j = 0; j < N && ok; ++j) {
+        const int ks = j % Q::KST, vs = j % Q::VST;
+        if (!mbar_wait(bar(Q::BAR_KEMPTY + ks), ((j / Q::KST) & 1) ^ 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(Q::BAR_KFULL + ks), C::TILE_BYTES);
+        load_kv_tile<D>(sb + Q::OFF_K + ks * C::TILE_BYTES, &tm_k, bar(Q::BAR_KFULL + ks), table, pp, j * BR, hk);
+        ++nk;
+        if (!mbar_wait(bar(Q::BAR_VEMPTY + vs), ((j / Q::VST) & 1) ^ 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(Q::BAR_VFULL + vs), C::TILE_BYTES);
+        load_kv_tile<D>(sb + Q::OFF_V + vs * C::TILE_BYTES, &tm_v, bar(Q::BAR_VFULL + vs), table, pp, j * BR, hk);
+        ++nv;
+      }
+      if (!ok) fail();
+      for (int st = 0; st < Q::KST && st < nk; ++st)
+        if (!mbar_wait(bar(Q::BAR_KFULL + st), (((nk - st + Q::KST - 1) / Q::KST) - 1) & 1)) fail();
+      for (int st = 0; st < Q::VST && st < nv; ++st)
+        if (!mbar_wait(bar(Q::BAR_VFULL + st), (((nv - st + Q::VST - 1) / Q::VST) - 1) & 1)) fail();
+      if (!mbar_wait(bar(Q::BAR_RES), 0)) fail();
+    } else if (warp == WARP_MMA && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer (the dense kernel's)
+      constexpr uint32_t idesc_s = make_idesc_f16(BF16, BR, BR, false);
+      constexpr uint32_t idesc_o = make_idesc_f16(BF16, BR, D, true);
+      constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
+      constexpr uint32_t RSTEP16 = (16 * 128) >> 4;
+      const uint64_t q_a = smem_desc(sb, 16, C::SBO, C::LAYOUT);
+      const uint64_t do_a = smem_desc(sb + C::TILE_BYTES, 16, C::SBO, C::LAYOUT);
+      const uint64_t k_b = smem_desc(sb + Q::OFF_K, 16, C::SBO, C::LAYOUT);
+      const uint64_t k_mn = smem_desc(sb + Q::OFF_K, C::CHUNK_BYTES, C::SBO, C::LAYOUT);
+      const uint64_t v_b = smem_desc(sb + Q::OFF_V, 16, C::SBO, C::LAYOUT);
+      bool ok = true;
+      auto issue_s = [&](int j) {
+        const int ks = j % Q::KST;
+        if (!mbar_wait(bar(Q::BAR_KFULL + ks), (j / Q::KST) & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_D; ++k)
+          umma_ss(tmem + BR * (j & 1), q_a + kstep16<D>(k), k_b + ks * TILE16 + kstep16<D>(k), idesc_s,
+                  k > 0 ? 1u : 0u);
+        umma_commit(bar(Q::BAR_S + (j & 1)));
+        return true;
+      };
+      auto issue_dp = [&](int j) {
+        const int vs = j % Q::VST;
+        if (!mbar_wait(bar(Q::BAR_VFULL + vs), (j / Q::VST) & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_D; ++k)
+          umma_ss(tmem + 2 * BR, do_a + kstep16<D>(k), v_b + vs * TILE16 + kstep16<D>(k), idesc_s,
+                  k > 0 ? 1u : 0u);
+        umma_commit(bar(Q::BAR_DP));
+        umma_commit(bar(Q::BAR_VEMPTY + vs));
+        return true;
+      };
+      if (N > 0) {
+        if (!mbar_wait(bar(Q::BAR_RES), 0)) ok = false;
+        tc_fence_after();
+        if (ok && !issue_s(0)) ok = false;
+        if (ok && !issue_dp(0)) ok = false;
+        if (ok && N > 1 && !issue_s(1)) ok = false;
+        for (int j = 0; j < N && ok; ++j) {
+          if (!mbar_wait(bar(Q::BAR_DS), j & 1)) { ok = false; break; }
+          tc_fence_after();
+          const int ks = j % Q::KST;
+#pragma unroll
+          for (int k = 0; k < C::KSTEPS_R; ++k)
+            umma_ts(tmem + 3 * BR, tmem + 2 * BR + tmem_a_kstep(k), k_mn + ks * TILE16 + k * RSTEP16, idesc_o,
+                    (j > 0 || k > 0) ? 1u : 0u);
+          umma_commit(bar(Q::BAR_KEMPTY + ks));
+          if (j + 1 < N && !issue_dp(j + 1)) { ok = false; break; }
+          if (j + 2 < N && !issue_s(j + 2)) { ok = false; break; }
+        }
+      }
+      if (!ok) fail();
+      umma_commit(bar(Q::BAR_DONE));
+      if (!mbar_wait(bar(Q::BAR_DONE), 0)) fail();
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- elementwise
+    setmaxnreg_inc<REG_EW>();
+    const int half = warp >> 2;                // key columns [64 half, +64)
+    const int row = ((warp & 3) << 5) + lane;  // pair row = TMEM lane
+    const int pair = t * BR + row;
+    const int qi = pair / gp;
+    const int hq = hh * gp + (pair - qi * gp);
+    const bool row_ok = qi < n;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    const size_t ri = static_cast<size_t>(q0 + (row_ok ? qi : 0)) * pp.Hq + hq;
+    const float l2 = row_ok ? __ldg(a.lse2 + ri) : -INFINITY;
+    const bool live = l2 != -INFINITY;
+    const float dsi = live ? __ldg(a.dsum + ri) : 0.f;
+    const int pos = row_ok ? (dflt ? diag + qi : __ldg(pp.positions + q0 + qi)) : -1;
+    const int causal_lim = pp.causal ? pos : 0x7fffffff;
+    const float sc = pp.scale_log2;
+    bool failed = false;
+    for (int j = 0; j < N; ++j) {
+      float x[64];
+      const bool ok = mbar_wait(bar(Q::BAR_S + (j & 1)), (j >> 1) & 1);
+      if (__any_sync(0xffffffffu, !ok)) { failed = true; break; }
+      tc_fence_after();
+      tmem_ld64<BF16>(tmem + lane_off + BR * (j & 1) + 64 * half, x);
+      const int kc0 = j * BR + 64 * half;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const int key = kc0 + c;
+        const bool vis = live && key < L && key <= causal_lim;
+        x[c] = vis ? fast_exp2(x[c] * sc - l2) : 0.f;
+      }
+      const bool ok2 = mbar_wait(bar(Q::BAR_DP), j & 1);
+      if (__any_sync(0xffffffffu, !ok2)) { failed = true; break; }
+      tc_fence_after();
+      float dp[64];
+      tmem_ld64<BF16>(tmem + lane_off + 2 * BR + 64 * half, dp);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) dp[c] = x[c] * (dp[c] - dsi);
+      tmem_st_packed64<BF16>(tmem + lane_off + 2 * BR + 64 * half, dp);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(Q::BAR_DS));
+    }
+    // ---------------------------------------------------------------- epilogue
+    if (failed) {
+      if (lane == 0) fail();
+    } else {
+      bool ok = true;
+      if (N > 0) {
+        ok = mbar_wait(bar(Q::BAR_DONE), 0);
+        if (__any_sync(0xffffffffu, !ok)) { ok = false; if (lane == 0) fail(); }
+      }
+      if (ok) {
+        tc_fence_after();
+        uint8_t* rowp = static_cast<uint8_t*>(a.dq) + (ri * D + half * (D / 2)) * 2;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          float v[32];
+          if (N > 0) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + 3 * BR + half * (D / 2) + 32 * c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0.f;
+          }
+          if (row_ok) store_row16<BF16, 32>(rowp + c * 64, v, a.scale);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace tc
+
+template <int D, bool BF16>
+cudaError_t launch_paged_bwd_tc(EncodeTiledFn enc, const PagedParams& pp, const void* q, const void* k,
+                                const void* v, const void* dout, const TcArgs& a, cudaStream_t st) {
+  using namespace tc;
+  const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  const int group = pp.Hq / pp.Hkv;
+  const int gp = BR % group == 0 ? group : 1;
+  CUtensorMap tq, tdo, tk, tv;
+  {  // q, dout viewed as [queries, Hq/gp, gp, D]; boxes of 128 (query, head) pairs
+    const cuuint64_t gdim[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(gp),
+                                static_cast<cuuint64_t>(pp.Hq / gp), static_cast<cuuint64_t>(pp.num_queries)};
+    const cuuint64_t gstride[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(gp) * D * 2,
+                                   static_cast<cuuint64_t>(pp.Hq) * D * 2};
+    const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(gp), 1u, static_cast<cuuint32_t>(BR / gp)};
+    for (int i = 0; i < 2; ++i)
+      if (enc(i == 0 ? &tq : &tdo, dt, 4, const_cast<void*>(i == 0 ? q : dout), gdim, gstride, box, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+  }
+  {  // k, v viewed as [pages, page_size, Hkv, D]
+    const cuuint64_t gdim[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(pp.Hkv),
+                                static_cast<cuuint64_t>(pp.page_size), static_cast<cuuint64_t>(pp.num_pages)};
+    const cuuint64_t gstride[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(pp.Hkv) * D * 2,
+                                   static_cast<cuuint64_t>(pp.page_size) * pp.Hkv * D * 2};
+    const cuuint32_t box[4] = {64u, 1u, static_cast<cuuint32_t>(pp.page_size < BR ? pp.page_size : BR), 1u};
+    for (int i = 0; i < 2; ++i)
+      if (enc(i == 0 ? &tk : &tv, dt, 4, const_cast<void*>(i == 0 ? k : v), gdim, gstride, box, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+  }
+  auto kv = paged_dkdv_tc_kernel<D, BF16>;
+  auto kq = paged_dq_tc_kernel<D, BF16>;
+  constexpr int smem_kv = Cfg<D>::SMEM_BYTES;
+  constexpr int smem_q = DqCfg<D>::SMEM_BYTES;
+  static std::atomic<unsigned long long> configured{0};
+  const unsigned long long bit = pp.device >= 0 && pp.device < 64 ? 1ull << pp.device : 0ull;
+  if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  if (a.dk || a.dv) {
+    const int64_t kblocks = (static_cast<int64_t>(pp.max_pages) * pp.page_size + BR - 1) / BR;
+    const int64_t ctas = static_cast<int64_t>(pp.num_seqs) * pp.Hkv * kblocks;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (ctas > 0)
+      kv<<<static_cast<unsigned>(ctas), NUM_THREADS, smem_kv, st>>>(tq, tdo, tk, tv, pp, a,
+                                                                    static_cast<int>(kblocks), gp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (a.dq) {
+    const int64_t qtiles = (static_cast<int64_t>(pp.max_queries) * gp + BR - 1) / BR;
+    const int64_t ctas = static_cast<int64_t>(pp.num_seqs) * (pp.Hq / gp) * qtiles;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (ctas > 0)
+      kq<<<static_cast<unsigned>(ctas), NUM_THREADS, smem_q, st>>>(tq, tdo, tk, tv, pp, a,
+                                                                   static_cast<int>(qtiles), gp);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pbwd
+}  // namespace attn

@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
                                                        const void* __restrict__ v, const void* __restrict__ dout,
                                                        const Buffers b, void* __restrict__ dk,
                                                        void* __restrict__ dkp, void* __restrict__ dv,
-                                                       const PagedParams pp, float scale, int kpc) {
+                                                       const PagedParams pp, float scale, int kpc,
+                                                       int skip_single) {
   using C = Cfg<DK, PD, TPK>;
   constexpr int G = C::G, PG = C::PG, GPT = C::GPT, PPT = C::PPT, RT = C::RT;
   extern __shared__ float4 smem[];
@@ -136,6 +137,7 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
   }
 
   const int r_lo = __ldg(b.offsets + page), r_hi = __ldg(b.offsets + page + 1);
+  if (skip_single && r_hi - r_lo == 1) return;  // the tensor-core kernel writes pages with one reader
   for (int ri = r_lo; ri < r_hi; ++ri) {
     const int code = __ldg(b.refs + ri);
     const int s = code / pp.max_pages, blk = code - s * pp.max_pages;
@@ -172,8 +174,9 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
         ps[tid] = in ? position_of(pp, q0 + qi, q0, n, L) : -1;
       }
       __syncthreads();
+      const int rows_here = min(RT, npairs - e0);  // rows past the sequence's last are not visited
 #pragma unroll 2
-      for (int r = 0; r < RT; ++r) {
+      for (int r = 0; r < rows_here; ++r) {
         float sd = 0.f, pd = 0.f;
 #pragma unroll
         for (int c = 0; c < GPT; ++c) {
@@ -337,7 +340,7 @@ __global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q,
 template <int DK, int PD, int TPK, int DT, bool MLA>
 cudaError_t launch_instance(const PagedParams& pp, const void* q, const void* qp, const void* k, const void* kp,
                             const void* v, const void* dout, const Buffers& b, void* dq, void* dqp, void* dk,
-                            void* dkp, void* dv, float scale, cudaStream_t st) {
+                            void* dkp, void* dv, float scale, cudaStream_t st, bool skip_single = false) {
   using C = Cfg<DK, PD, TPK>;
   const int group = pp.Hq / pp.Hkv;
   if (dk || dkp || dv) {
@@ -352,7 +355,8 @@ cudaError_t launch_instance(const PagedParams& pp, const void* q, const void* qp
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       if (e != cudaSuccess) return e;
     }
-    if (grid.x > 0) kern<<<grid, kpc * TPK, smem, st>>>(q, qp, k, kp, v, dout, b, dk, dkp, dv, pp, scale, kpc);
+    if (grid.x > 0) kern<<<grid, kpc * TPK, smem, st>>>(q, qp, k, kp, v, dout, b, dk, dkp, dv, pp, scale, kpc,
+                                                      skip_single ? 1 : 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

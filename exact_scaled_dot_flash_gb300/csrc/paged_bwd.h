@@ -42,6 +42,29 @@ cudaError_t launch_paged_bwd(int D, int dtype, const PagedParams& pp, const void
                              const void* v, const void* dout, const Buffers& b, void* dq, void* dk, void* dv,
                              float scale, cudaStream_t st);
 
+// Key-major pass of the fp32 FMA kernels over the pages whose reader count
+// is not one (no reader: zeros; shared: every reader in order), after the
+// tensor-core pass has written the pages with exactly one reader.
+cudaError_t launch_paged_dkdv_shared(int D, int dtype, const PagedParams& pp, const void* q, const void* k,
+                                     const void* v, const void* dout, const Buffers& b, void* dk, void* dv,
+                                     float scale, cudaStream_t st);
+
+// Tensor-core paged backward (F16/BF16, D in {64, 128}, page_size a multiple
+// of 8 dividing 128 or a multiple of 128): dq for every row, and dk/dv for the
+// pages with exactly one reader (when dk or dv is given).
+struct TcArgs {
+  const float* lse2;
+  const float* dsum;
+  const int* offsets;  // the reverse index's per-page offsets (reader counts)
+  void* dq;
+  void* dk;
+  void* dv;
+  float scale;
+};
+template <int D, bool BF16>
+cudaError_t launch_paged_bwd_tc(EncodeTiledFn enc, const PagedParams& pp, const void* q, const void* k,
+                                const void* v, const void* dout, const TcArgs& a, cudaStream_t st);
+
 // Paged MLA (Hq = heads, Hkv = 1): dq [nq, H, R], dqp [nq, H, Pd], dlatent
 // [pages, page_size, R], dkpos [pages, page_size, Pd]; outputs may be nullptr.
 // R in {128, 256, 512}, Pd in {0, 16, 32, 64}.

@@ -1,5 +1,8 @@
 """GPU parity of the backward over a paged cache (attn_paged_bwd and
-attn_paged_mla_bwd) against the float64 oracle.
+attn_paged_mla_bwd) against the float64 oracle. F16/BF16 cases with D in
+{64, 128} and page sizes of 8..256 take the tensor-core kernels (with the fp32
+FMA key-major kernel for shared and unread pages); the others the fp32 FMA
+kernels throughout.
 
 The pipeline is the user's: the CUDA paged forward with its log-sum-exp, then
 the CUDA backward on (inputs, out, dout, lse); the oracle computes every
@@ -93,6 +96,9 @@ PAGED_CASES = [
     PW("pbwd_bf16_d128_decode_p16", "bf16", 8, 16, 4, 128, 16, (100, 1500), (1, 1), seed=6),
     PW("pbwd_f16_d128_prefill_p8_pos", "f16", 3, 4, 2, 128, 8, (100, 300), (50, 300), seed=7,
        explicit_positions=True),
+    # a group of 6 (does not divide 128): one head per tile on the tensor cores
+    PW("pbwd_bf16_d64_g6_p32", "bf16", 3, 12, 2, 64, 32, (100, 400), (1, 150), seed=8),
+    PW("pbwd_f16_d64_p128_full", "f16", 3, 4, 2, 64, 128, (200, 700), (1, 200), seed=9, causal=False),
 ]
 
 

@@ -121,3 +121,84 @@ def test_mla_workload_full_size_sampled(name):
                                     sub["seq_lens"], sub["q_offsets"], positions=sub["positions"], causal=w.causal,
                                     scale=x["scale"], dtype=w.dtype, lse=True)
     check_rows(got[rows], got_lse[rows], ref, ref_lse, w.dtype, name)
+
+
+def compact_all_rows(x, seqs, caches, P):
+    """The sub-problem of sequences ``seqs`` with all their queries (so the
+    default positions stay the same): (sub-problem, query rows of the full
+    problem in order, physical pages of the full problem in the order of the
+    sub-problem's cache)."""
+    table, lens, offs = x["block_table"], x["seq_lens"], x["q_offsets"]
+    pages = []
+    for s in seqs:
+        pages += [int(p) for p in table[s, :(int(lens[s]) + P - 1) // P]]
+    remap = {p: i for i, p in enumerate(pages)}
+    sub = {c: np.ascontiguousarray(x[c][np.array(pages, dtype=np.int64)]) for c in caches}
+    width = max(1, max((int(lens[s]) + P - 1) // P for s in seqs))
+    sub["block_table"] = np.full((len(seqs), width), -1, dtype=np.int32)
+    rows, sub_offs = [], [0]
+    for i, s in enumerate(seqs):
+        used = (int(lens[s]) + P - 1) // P
+        sub["block_table"][i, :used] = [remap[int(p)] for p in table[s, :used]]
+        rows += list(range(int(offs[s]), int(offs[s + 1])))
+        sub_offs.append(len(rows))
+    sub["seq_lens"] = lens[np.array(seqs)].astype(np.int32)
+    sub["q_offsets"] = np.array(sub_offs, dtype=np.int32)
+    sub["positions"] = None if x["positions"] is None else x["positions"][np.array(rows)]
+    return sub, np.array(rows), np.array(pages)
+
+
+def cheapest(x, n):
+    """The n sequences (with queries) of least oracle work (keys x queries)."""
+    cost = x["seq_lens"].astype(np.int64) * np.diff(x["q_offsets"])
+    order = [int(s) for s in np.argsort(cost, kind="stable") if np.diff(x["q_offsets"])[s] > 0]
+    return order[:n]
+
+
+def check_grads(got, ref, dtype, name):
+    for gname, a, b in zip(name[1], got, ref):
+        err = float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-300))
+        assert err <= TOL[dtype], f"{name[0]} {gname}: rel err {err:.3e}"
+
+
+def test_paged_prefill_backward_full_size_sampled():
+    # the full-size call; no page is shared, so a page's gradients come from its
+    # own sequence alone and the compact sub-problem reproduces them
+    import torch
+    from exact_scaled_dot_flash_gb300 import attn
+    w = synth.PAGED_WORKLOADS["bf16_paged_prefill"]
+    x = synth.make_paged_inputs(w)
+    q, kc, vc = (to_device(x[n], w.dtype) for n in ("q", "k_cache", "v_cache"))
+    ints = {n: to_device(x[n], "i32") for n in ("block_table", "seq_lens", "q_offsets")}
+    g = synth.to_storage(synth.normal_f32(w.seed, 9, x["q"].shape), w.dtype)
+    dq, dk, dv = attn.paged_bwd(q, kc, vc, ints["block_table"], ints["seq_lens"], ints["q_offsets"],
+                                to_device(g, w.dtype), causal=w.causal, scale=x["scale"])
+    torch.cuda.synchronize()
+    seqs = cheapest(x, 2)
+    sub, rows, pages = compact_all_rows(x, seqs, ("k_cache", "v_cache"), w.page_size)
+    ref = oracle.paged_attention_bwd(x["q"][rows], sub["k_cache"], sub["v_cache"], g[rows], sub["block_table"],
+                                     sub["seq_lens"], sub["q_offsets"], positions=sub["positions"],
+                                     causal=w.causal, scale=x["scale"], dtype=w.dtype)
+    got = (to_f64(dq)[rows], to_f64(dk)[pages], to_f64(dv)[pages])
+    check_grads(got, ref, w.dtype, (w.name, ("dq", "dk", "dv")))
+
+
+def test_mla_decode_backward_full_size_sampled():
+    import torch
+    from exact_scaled_dot_flash_gb300 import attn
+    w = synth.MLA_WORKLOADS["bf16_mla_decode"]
+    x = synth.make_mla_inputs(w)
+    q, qp, lat, kp = (to_device(x[n], w.dtype) for n in ("q", "qp", "latent", "kpos"))
+    ints = {n: to_device(x[n], "i32") for n in ("block_table", "seq_lens", "q_offsets")}
+    g = synth.to_storage(synth.normal_f32(w.seed, 9, x["q"].shape), w.dtype)
+    grads = attn.paged_mla_bwd(q, qp, lat, kp, ints["block_table"], ints["seq_lens"], ints["q_offsets"],
+                               to_device(g, w.dtype), causal=w.causal, scale=x["scale"])
+    torch.cuda.synchronize()
+    seqs = cheapest(x, 3)
+    sub, rows, pages = compact_all_rows(x, seqs, ("latent", "kpos"), w.page_size)
+    ref = oracle.paged_mla_bwd(x["q"][rows], x["qp"][rows], sub["latent"], sub["kpos"], g[rows],
+                               sub["block_table"], sub["seq_lens"], sub["q_offsets"], positions=sub["positions"],
+                               causal=w.causal, scale=x["scale"], dtype=w.dtype)
+    dq, dqp, dlat, dkp = (to_f64(t) for t in grads)
+    got = (dq[rows], dqp[rows], dlat[pages], dkp[pages])
+    check_grads(got, ref, w.dtype, (w.name, ("dq", "dqp", "dlatent", "dkpos")))
