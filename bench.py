@@ -506,7 +506,8 @@ def bench_paged(args):
         need = attn.mla_bwd_workspace_bytes(shp) if is_mla else attn.paged_bwd_workspace_bytes(shp)
         pws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
         # preprocess, page-index count / scan / fill / sort, key-major and query-major kernels
-        launches = 7
+        # (tensor-core paths add the FMA key-major pass over shared pages)
+        launches = 8 if (not is_mla and tensor) else 7
 
     def step():
         if bwd:
@@ -572,7 +573,18 @@ def bench_paged(args):
     # is held to whichever of the tensor and HBM rooflines binds (the larger
     # ideal time); the rest runs on the fp32 FMA pipes
     mla_hbm = is_mla and tensor and nbytes / float(peaks["hbm_gbs"]) > flops / (float(peaks["bf16_tflops"]) * 1e3)
-    if bwd:  # the backward over a paged cache runs on the fp32 FMA pipes
+    # the paged backward: tensor cores for F16/BF16 paged attention with D in
+    # {64, 128} (HBM-bound when decode-shaped), the fp32 FMA kernels otherwise
+    bwd_tc = bwd and not is_mla and tensor
+    tc_names = "paged_dkdv_tc_kernel + paged_dq_tc_kernel (+ FMA pass over shared pages), whole call"
+    if bwd and bwd_tc and decode:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                "frac": gbs / float(peaks["hbm_gbs"]), "peak_kind": f"{peak_kind} HBM copy", "kernel": tc_names}
+    elif bwd_tc:
+        pk = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": tf, "peak": pk, "unit": "TFLOP/s", "frac": tf / pk,
+                "peak_kind": f"{peak_kind} bf16 dense burst", "kernel": tc_names}
+    elif bwd:
         roof = {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
                 "peak_kind": f"fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x {mhz:.0f} MHz",
                 "kernel": "dkdv_kernel + dq_kernel (paged backward, whole call)"}

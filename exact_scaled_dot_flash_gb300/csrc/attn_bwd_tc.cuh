@@ -77,7 +77,13 @@ struct Cfg {
   static constexpr int OFF_BAR = OFF_RING + STAGES * 2 * TILE_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 8;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  // per elementwise warp, the current query tile's column statistics (lse2, D,
+  // visibility limit) of the paged key-major kernel, read with broadcast loads
+  // (the dense kernel shuffles them: staging them measured no faster there)
+  static constexpr int OFF_STATS = (OFF_MISC + 16 + 15) / 16 * 16;
+  static constexpr int STATS_PER_WARP = 3 * 64;  // floats
+  static constexpr int SMEM_BYTES = OFF_STATS + 8 * STATS_PER_WARP * 4 + 1024;
+  static_assert(SMEM_BYTES <= 232448, "key-major kernel shared memory");
   static constexpr int BAR_FULL = 0, BAR_EMPTY = STAGES;
   static constexpr int BAR_RES = 2 * STAGES;            // resident tiles loaded
   static constexpr int BAR_S = BAR_RES + 1;             // 2 (dq kernel double-buffers S)

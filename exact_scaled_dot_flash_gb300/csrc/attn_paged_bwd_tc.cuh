@@ -254,35 +254,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
     const uint32_t tS = tmem + lane_off, tDP = tS + BR;
     const float sc = pp.scale_log2;
-    const bool key_vis = key < L;
+    // this warp's copy of the tile's column statistics
+    float* st_l2 = reinterpret_cast<float*>(smem + C::OFF_STATS) + warp * C::STATS_PER_WARP;
+    float* st_ds = st_l2 + 64;
+    int* st_lim = reinterpret_cast<int*>(st_l2 + 128);
+    // keys past the sequence see nothing: their limit test always fails
+    const int kcmp = key < L ? key : 0x7fffffff;
     bool failed = false;
     for (int it = 0; it < N; ++it) {
       const int hb = it / per_hb, t = t_lo + (it - hb * per_hb);
-      // statistics and position of pair columns lane and lane + 32 of this warpgroup's 64
-      float l2v[2], dsv[2];
-      int posv[2];
+      // pair columns lane and lane + 32 of this warpgroup's 64: lse2, D and the
+      // largest visible key (-1 for a pair with no query or no visible key)
+      __syncwarp();
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int pair = t * BR + 64 * half + 32 * u + lane;
         const int qi = pair / gp;
         const int hq = hk * group + hb * gp + (pair - qi * gp);
         const bool in = qi < n;
-        const size_t ri = static_cast<size_t>(q0 + qi) * pp.Hq + hq;
-        l2v[u] = in ? __ldg(a.lse2 + ri) : -INFINITY;
-        dsv[u] = in ? __ldg(a.dsum + ri) : 0.f;
-        posv[u] = in ? (dflt ? diag + qi : __ldg(pp.positions + q0 + qi)) : -1;
+        const size_t ri = static_cast<size_t>(q0 + (in ? qi : 0)) * pp.Hq + hq;
+        const float l2 = in ? __ldg(a.lse2 + ri) : -INFINITY;
+        const bool live = l2 != -INFINITY;
+        int lim = 0x7ffffffe;
+        if (pp.causal && live) lim = dflt ? diag + qi : min(__ldg(pp.positions + q0 + qi), 0x7ffffffe);
+        st_l2[32 * u + lane] = live ? l2 : 0.f;
+        st_ds[32 * u + lane] = live ? __ldg(a.dsum + ri) : 0.f;
+        st_lim[32 * u + lane] = live ? lim : -1;
       }
+      __syncwarp();
       float x[64];
       const bool ok = mbar_wait(bar(C::BAR_S), it & 1);
       if (__any_sync(0xffffffffu, !ok)) { failed = true; break; }
       tc_fence_after();
       tmem_ld64<BF16>(tS + 64 * half, x);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float l2 = __shfl_sync(0xffffffffu, c < 32 ? l2v[0] : l2v[1], c & 31);
-        const int pos = __shfl_sync(0xffffffffu, c < 32 ? posv[0] : posv[1], c & 31);
-        const bool vis = key_vis && (!pp.causal || key <= pos) && l2 != -INFINITY;
-        x[c] = vis ? fast_exp2(x[c] * sc - l2) : 0.f;
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = reinterpret_cast<const float4*>(st_l2)[c4];
+        const int4 m4 = reinterpret_cast<const int4*>(st_lim)[c4];
+        x[4 * c4 + 0] = kcmp <= m4.x ? fast_exp2(x[4 * c4 + 0] * sc - l4.x) : 0.f;
+        x[4 * c4 + 1] = kcmp <= m4.y ? fast_exp2(x[4 * c4 + 1] * sc - l4.y) : 0.f;
+        x[4 * c4 + 2] = kcmp <= m4.z ? fast_exp2(x[4 * c4 + 2] * sc - l4.z) : 0.f;
+        x[4 * c4 + 3] = kcmp <= m4.w ? fast_exp2(x[4 * c4 + 3] * sc - l4.w) : 0.f;
       }
       tmem_st_packed64<BF16>(tS + 64 * half, x);
       tmem_wait_st();
@@ -294,9 +306,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float dp[64];
       tmem_ld64<BF16>(tDP + 64 * half, dp);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float dsi = __shfl_sync(0xffffffffu, c < 32 ? dsv[0] : dsv[1], c & 31);
-        dp[c] = x[c] * (dp[c] - dsi);
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 d4 = reinterpret_cast<const float4*>(st_ds)[c4];
+        dp[4 * c4 + 0] = x[4 * c4 + 0] * (dp[4 * c4 + 0] - d4.x);
+        dp[4 * c4 + 1] = x[4 * c4 + 1] * (dp[4 * c4 + 1] - d4.y);
+        dp[4 * c4 + 2] = x[4 * c4 + 2] * (dp[4 * c4 + 2] - d4.z);
+        dp[4 * c4 + 3] = x[4 * c4 + 3] * (dp[4 * c4 + 3] - d4.w);
       }
       tmem_st_packed64<BF16>(tDP + 64 * half, dp);
       tmem_wait_st();

@@ -121,6 +121,9 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
   const size_t slot = static_cast<size_t>(page) * P + (key_ok ? t : 0);
   const size_t krow = (slot * pp.Hkv + hk) * G;
 
+  const int r_lo = __ldg(b.offsets + page), r_hi = __ldg(b.offsets + page + 1);
+  if (skip_single && r_hi - r_lo == 1) return;  // the tensor-core kernel writes pages with one reader
+
   float4 kr[GPT], vr[GPT], dka[GPT], dva[GPT], kpr[PPT > 0 ? PPT : 1], dkpa[PPT > 0 ? PPT : 1];
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -136,8 +139,6 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
     dkpa[c] = z;
   }
 
-  const int r_lo = __ldg(b.offsets + page), r_hi = __ldg(b.offsets + page + 1);
-  if (skip_single && r_hi - r_lo == 1) return;  // the tensor-core kernel writes pages with one reader
   for (int ri = r_lo; ri < r_hi; ++ri) {
     const int code = __ldg(b.refs + ri);
     const int s = code / pp.max_pages, blk = code - s * pp.max_pages;
