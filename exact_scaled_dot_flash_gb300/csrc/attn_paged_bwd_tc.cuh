@@ -260,12 +260,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int* st_lim = reinterpret_cast<int*>(st_l2 + 128);
     // keys past the sequence see nothing: their limit test always fails
     const int kcmp = key < L ? key : 0x7fffffff;
-    bool failed = false;
-    for (int it = 0; it < N; ++it) {
+    // pair columns lane and lane + 32 of this warpgroup's 64 of tile `it`:
+    // lse2, D and the largest visible key (-1 for a pair with no query or no
+    // visible key); loaded one tile ahead so their latency hides behind a tile
+    float l2v[2], dsv[2];
+    int limv[2];
+    auto load_stats = [&](int it) {
       const int hb = it / per_hb, t = t_lo + (it - hb * per_hb);
-      // pair columns lane and lane + 32 of this warpgroup's 64: lse2, D and the
-      // largest visible key (-1 for a pair with no query or no visible key)
-      __syncwarp();
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int pair = t * BR + 64 * half + 32 * u + lane;
@@ -273,14 +274,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int hq = hk * group + hb * gp + (pair - qi * gp);
         const bool in = qi < n;
         const size_t ri = static_cast<size_t>(q0 + (in ? qi : 0)) * pp.Hq + hq;
-        const float l2 = in ? __ldg(a.lse2 + ri) : -INFINITY;
-        const bool live = l2 != -INFINITY;
-        int lim = 0x7ffffffe;
-        if (pp.causal && live) lim = dflt ? diag + qi : min(__ldg(pp.positions + q0 + qi), 0x7ffffffe);
-        st_l2[32 * u + lane] = live ? l2 : 0.f;
-        st_ds[32 * u + lane] = live ? __ldg(a.dsum + ri) : 0.f;
-        st_lim[32 * u + lane] = live ? lim : -1;
+        l2v[u] = in ? __ldg(a.lse2 + ri) : -INFINITY;
+        dsv[u] = in ? __ldg(a.dsum + ri) : 0.f;
+        limv[u] = 0x7ffffffe;
+        if (pp.causal) limv[u] = dflt ? diag + qi : (in ? min(__ldg(pp.positions + q0 + qi), 0x7ffffffe) : -1);
       }
+    };
+    if (N > 0) load_stats(0);
+    bool failed = false;
+    for (int it = 0; it < N; ++it) {
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const bool live = l2v[u] != -INFINITY;
+        st_l2[32 * u + lane] = live ? l2v[u] : 0.f;
+        st_ds[32 * u + lane] = live ? dsv[u] : 0.f;
+        st_lim[32 * u + lane] = live ? limv[u] : -1;
+      }
+      if (it + 1 < N) load_stats(it + 1);
       __syncwarp();
       float x[64];
       const bool ok = mbar_wait(bar(C::BAR_S), it & 1);
