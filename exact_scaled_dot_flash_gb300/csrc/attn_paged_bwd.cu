@@ -25,19 +25,25 @@ constexpr float LOG2E = 1.4426950408889634f;
 int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
 // D_i = dout_i . out_i (0 for a row with no visible key) and lse_i * log2(e);
-// one warp per row of `width` elements.
+// 2^tpr_log2 threads per row of groups8 x 8 elements, 16-byte loads.
 template <int DT>
 __global__ void __launch_bounds__(256) preprocess_kernel(const void* out, const void* dout, const float* lse,
-                                                         float* dsum, float* lse2, int64_t rows, int groups) {
-  const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
+                                                         float* dsum, float* lse2, int64_t rows, int groups8,
+                                                         int tpr_log2) {
+  const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> tpr_log2;
+  const int tpr = 1 << tpr_log2;
+  const int sub = threadIdx.x & (tpr - 1);
   float acc = 0.f;
-  for (int g = lane; g < groups; g += 32)
-    acc = simt::dot4(simt::load4<DT>(out, r * groups + g), simt::load4<DT>(dout, r * groups + g), acc);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
+  if (r < rows) {
+    for (int g = sub; g < groups8; g += tpr) {
+      float4 a0, a1, b0, b1;
+      simt::load8<DT>(out, r * groups8 + g, a0, a1);
+      simt::load8<DT>(dout, r * groups8 + g, b0, b1);
+      acc = simt::dot4(a1, b1, simt::dot4(a0, b0, acc));
+    }
+  }
+  for (int o = tpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (r < rows && sub == 0) {
     const float l = lse[r];
     dsum[r] = l == -INFINITY ? 0.f : acc;
     lse2[r] = l * LOG2E;
@@ -119,11 +125,13 @@ __global__ void fill_kernel(const PagedParams pp, int* count, const int* offsets
 }
 
 // Insertion sort of every page's segment (segments are short: one entry per
-// sequence or block that reads the page).
-__global__ void sort_kernel(const int* offsets, int* refs, int pages) {
+// sequence or block that reads the page); pages whose reader count is not one
+// join the list (in any order: each is computed on its own).
+__global__ void sort_kernel(const int* offsets, int* refs, int* list, int pages) {
   const int p = blockIdx.x * blockDim.x + threadIdx.x;
   if (p >= pages) return;
   const int lo = offsets[p], hi = offsets[p + 1];
+  if (hi - lo != 1) list[1 + atomicAdd(list, 1)] = p;
   for (int i = lo + 1; i < hi; ++i) {
     const int x = refs[i];
     int j = i - 1;
@@ -144,7 +152,8 @@ Layout layout(int64_t rows, int64_t num_pages, int64_t table_entries) {
   l.count = l.lse2 + round256(rows * 4);
   l.offsets = l.count + round256(num_pages * 4);
   l.refs = l.offsets + round256((num_pages + 1) * 4);
-  l.total = l.refs + round256(table_entries * 4);
+  l.list = l.refs + round256(table_entries * 4);
+  l.total = l.list + round256((num_pages + 1) * 4);
   return l;
 }
 
@@ -152,32 +161,39 @@ Buffers carve(void* workspace, const Layout& lay) {
   uint8_t* w = static_cast<uint8_t*>(workspace);
   return Buffers{reinterpret_cast<float*>(w + lay.dsum), reinterpret_cast<float*>(w + lay.lse2),
                  reinterpret_cast<int*>(w + lay.count), reinterpret_cast<int*>(w + lay.offsets),
-                 reinterpret_cast<int*>(w + lay.refs)};
+                 reinterpret_cast<int*>(w + lay.refs), reinterpret_cast<int*>(w + lay.list)};
 }
 
 cudaError_t launch_preprocess(int dtype, int width, const void* out, const void* dout, const float* lse,
                               const Buffers& b, int64_t rows, cudaStream_t st) {
-  const int64_t blocks = (rows * 32 + 255) / 256;
+  const int groups8 = width / 8;  // widths are multiples of 16
+  int tpr_log2 = 0;
+  while ((2 << tpr_log2) <= groups8 && (2 << tpr_log2) <= 32) ++tpr_log2;
+  const int64_t blocks = ((rows << tpr_log2) + 255) / 256;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const unsigned nb = static_cast<unsigned>(blocks);
-  const int groups = width / 4;
-  if (dtype == 0) preprocess_kernel<0><<<nb, 256, 0, st>>>(out, dout, lse, b.dsum, b.lse2, rows, groups);
-  else if (dtype == 1) preprocess_kernel<1><<<nb, 256, 0, st>>>(out, dout, lse, b.dsum, b.lse2, rows, groups);
-  else preprocess_kernel<2><<<nb, 256, 0, st>>>(out, dout, lse, b.dsum, b.lse2, rows, groups);
+  if (dtype == 0)
+    preprocess_kernel<0><<<nb, 256, 0, st>>>(out, dout, lse, b.dsum, b.lse2, rows, groups8, tpr_log2);
+  else if (dtype == 1)
+    preprocess_kernel<1><<<nb, 256, 0, st>>>(out, dout, lse, b.dsum, b.lse2, rows, groups8, tpr_log2);
+  else
+    preprocess_kernel<2><<<nb, 256, 0, st>>>(out, dout, lse, b.dsum, b.lse2, rows, groups8, tpr_log2);
   return cudaGetLastError();
 }
 
 cudaError_t launch_page_index(const PagedParams& pp, const Buffers& b, cudaStream_t st) {
   if (pp.num_pages <= 0) return cudaSuccess;
   cudaError_t e = cudaMemsetAsync(b.count, 0, static_cast<size_t>(pp.num_pages) * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(b.list, 0, 4, st);
   if (e != cudaSuccess) return e;
   const int64_t entries = static_cast<int64_t>(pp.num_seqs) * pp.max_pages;
   const unsigned eb = static_cast<unsigned>((entries + 255) / 256);
   if (eb > 0) count_kernel<<<eb, 256, 0, st>>>(pp, b.count);
   scan_kernel<<<1, 1024, 0, st>>>(b.count, b.offsets, pp.num_pages);
   if (eb > 0) fill_kernel<<<eb, 256, 0, st>>>(pp, b.count, b.offsets, b.refs);
-  sort_kernel<<<static_cast<unsigned>((pp.num_pages + 255) / 256), 256, 0, st>>>(b.offsets, b.refs, pp.num_pages);
+  sort_kernel<<<static_cast<unsigned>((pp.num_pages + 255) / 256), 256, 0, st>>>(b.offsets, b.refs, b.list,
+                                                                                  pp.num_pages);
   return cudaGetLastError();
 }
 

@@ -35,6 +35,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "paged_bwd.h"
 #include "params.h"
 #include "ptx.cuh"
@@ -93,14 +95,14 @@ __device__ __forceinline__ int position_of(const PagedParams& pp, int row, int q
   return pp.positions ? __ldg(pp.positions + row) : L - n + (row - q0);
 }
 
+// The key slots [blockIdx.y * kpc, +kpc) of one physical page and kv head.
 template <int DK, int PD, int TPK, int DT, bool MLA>
-__global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ q, const void* __restrict__ qp,
-                                                       const void* __restrict__ k, const void* __restrict__ kp,
-                                                       const void* __restrict__ v, const void* __restrict__ dout,
-                                                       const Buffers b, void* __restrict__ dk,
-                                                       void* __restrict__ dkp, void* __restrict__ dv,
-                                                       const PagedParams pp, float scale, int kpc,
-                                                       int skip_single) {
+__device__ __forceinline__ void dkdv_page(const void* __restrict__ q, const void* __restrict__ qp,
+                                          const void* __restrict__ k, const void* __restrict__ kp,
+                                          const void* __restrict__ v, const void* __restrict__ dout,
+                                          const Buffers& b, void* __restrict__ dk, void* __restrict__ dkp,
+                                          void* __restrict__ dv, const PagedParams& pp, float scale, int kpc,
+                                          int page, int hk) {
   using C = Cfg<DK, PD, TPK>;
   constexpr int G = C::G, PG = C::PG, GPT = C::GPT, PPT = C::PPT, RT = C::RT;
   extern __shared__ float4 smem[];
@@ -112,7 +114,6 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
   int* ps = reinterpret_cast<int*>(dss + RT);
 
   const int tid = threadIdx.x, part = tid % TPK, kl = tid / TPK;
-  const int page = blockIdx.x / pp.Hkv, hk = blockIdx.x - page * pp.Hkv;
   const int group = pp.Hq / pp.Hkv;
   const int P = pp.page_size;
   const int t0 = blockIdx.y * kpc;
@@ -122,7 +123,6 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
   const size_t krow = (slot * pp.Hkv + hk) * G;
 
   const int r_lo = __ldg(b.offsets + page), r_hi = __ldg(b.offsets + page + 1);
-  if (skip_single && r_hi - r_lo == 1) return;  // the tensor-core kernel writes pages with one reader
 
   float4 kr[GPT], vr[GPT], dka[GPT], dva[GPT], kpr[PPT > 0 ? PPT : 1], dkpa[PPT > 0 ? PPT : 1];
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -226,6 +226,29 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
     const float4 a = dkpa[c];
     if (dkp && gi < PG)
       store4<DT>(dkp, slot * PG + gi, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
+  }
+}
+
+// Every page (one CTA per page and kv head), or, with `listed`, the pages of
+// the index's list of pages whose reader count is not one (after the
+// tensor-core kernel has written the others), the CTAs striding over it.
+template <int DK, int PD, int TPK, int DT, bool MLA>
+__global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ q, const void* __restrict__ qp,
+                                                       const void* __restrict__ k, const void* __restrict__ kp,
+                                                       const void* __restrict__ v, const void* __restrict__ dout,
+                                                       const Buffers b, void* __restrict__ dk,
+                                                       void* __restrict__ dkp, void* __restrict__ dv,
+                                                       const PagedParams pp, float scale, int kpc, int listed) {
+  const int unit = blockIdx.x / pp.Hkv, hk = blockIdx.x - unit * pp.Hkv;
+  if (!listed) {
+    dkdv_page<DK, PD, TPK, DT, MLA>(q, qp, k, kp, v, dout, b, dk, dkp, dv, pp, scale, kpc, unit, hk);
+    return;
+  }
+  const int n = *b.list;  // uniform over the CTA
+  const int stride = gridDim.x / pp.Hkv;
+  for (int li = unit; li < n; li += stride) {
+    __syncthreads();  // the previous page's shared-memory rows are no longer read
+    dkdv_page<DK, PD, TPK, DT, MLA>(q, qp, k, kp, v, dout, b, dk, dkp, dv, pp, scale, kpc, b.list[1 + li], hk);
   }
 }
 
@@ -345,11 +368,12 @@ cudaError_t launch_instance(const PagedParams& pp, const void* q, const void* qp
   using C = Cfg<DK, PD, TPK>;
   const int group = pp.Hq / pp.Hkv;
   if (dk || dkp || dv) {
-    // keys per CTA: the page's slots, rounded up so that a CTA is whole warps
+    // keys per CTA: the page's slots, rounded up so that a CTA is whole warps;
+    // over the listed pages, at most 1024 page slots of CTAs stride the list
     const int unit = 32 / TPK;
     const int kpc = pp.page_size >= C::ROWS ? C::ROWS : (pp.page_size + unit - 1) / unit * unit;
-    const dim3 grid(static_cast<unsigned>(pp.num_pages) * pp.Hkv,
-                    static_cast<unsigned>((pp.page_size + kpc - 1) / kpc));
+    const unsigned units = static_cast<unsigned>(skip_single ? std::min(pp.num_pages, 1024) : pp.num_pages);
+    const dim3 grid(units * pp.Hkv, static_cast<unsigned>((pp.page_size + kpc - 1) / kpc));
     const size_t smem = C::dkdv_smem(MLA);
     auto kern = dkdv_kernel<DK, PD, TPK, DT, MLA>;
     if (smem > 48 * 1024) {

@@ -13,9 +13,10 @@ namespace pbwd {
 // Device scratch of one backward call, carved from the caller's workspace:
 // per-row D_i and lse_i (log2 units), then the reverse page index (per
 // physical page its count, its offset into refs, and refs: the table entries
-// s * max_pages + b that read it, ascending).
+// s * max_pages + b that read it, ascending), then the list of the pages whose
+// reader count is not one (list[0] = their number, list[1..] the pages).
 struct Layout {
-  int64_t dsum, lse2, count, offsets, refs, total;  // byte offsets, total size
+  int64_t dsum, lse2, count, offsets, refs, list, total;  // byte offsets, total size
 };
 Layout layout(int64_t rows, int64_t num_pages, int64_t table_entries);
 
@@ -25,6 +26,7 @@ struct Buffers {
   int* count;
   int* offsets;
   int* refs;
+  int* list;
 };
 Buffers carve(void* workspace, const Layout& lay);
 

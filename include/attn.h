@@ -374,8 +374,9 @@ ATTN_API int attn_paged_bwd(const attn_paged_shape_t* shape,
 
 /* attn_paged_bwd_workspace_bytes - workspace attn_paged_bwd needs: two float
  * arrays of num_queries * Hq (row statistics), num_pages + num_pages + 1 ints
- * (reverse index counts and offsets) and num_seqs * max_pages ints (the index),
- * each rounded up to 256 bytes. Returns ATTN_OK, ATTN_ERR_NULL or ATTN_ERR_SHAPE. */
+ * (reverse index counts and offsets), num_seqs * max_pages ints (the index)
+ * and num_pages + 1 ints (the pages that do not have exactly one reader), each
+ * rounded up to 256 bytes. Returns ATTN_OK, ATTN_ERR_NULL or ATTN_ERR_SHAPE. */
 ATTN_API int attn_paged_bwd_workspace_bytes(const attn_paged_shape_t* shape, size_t* bytes);
 
 /* attn_paged_mla_bwd - gradients of attn_paged_mla: dq [num_queries, H, R],

@@ -269,14 +269,15 @@ def _r256(x):
 
 
 def test_paged_bwd_workspace_layout(lib):
-    # row statistics (2 x rows floats), page counts, page offsets, the index
+    # row statistics (2 x rows floats), page counts, page offsets, the index,
+    # the list of pages without exactly one reader
     s = A.PagedShape(3, 10, 4, 2, 64, 16, 7, 5, 4)
     n = ctypes.c_size_t(0)
     assert lib.attn_paged_bwd_workspace_bytes(ctypes.byref(s), ctypes.byref(n)) == 0
-    assert n.value == 2 * _r256(40 * 4) + _r256(7 * 4) + _r256(8 * 4) + _r256(15 * 4)
+    assert n.value == 2 * _r256(40 * 4) + _r256(7 * 4) + _r256(8 * 4) + _r256(15 * 4) + _r256(8 * 4)
     m = A.MlaShape(3, 10, 16, 512, 64, 64, 700, 50, 4)
     assert lib.attn_paged_mla_bwd_workspace_bytes(ctypes.byref(m), ctypes.byref(n)) == 0
-    assert n.value == 2 * _r256(160 * 4) + _r256(700 * 4) + _r256(701 * 4) + _r256(150 * 4)
+    assert n.value == 2 * _r256(160 * 4) + _r256(700 * 4) + _r256(701 * 4) + _r256(150 * 4) + _r256(701 * 4)
     assert lib.attn_paged_bwd_workspace_bytes(None, ctypes.byref(n)) == codes["ATTN_ERR_NULL"]
     bad = A.PagedShape(3, -1, 4, 2, 64, 16, 7, 5, 4)
     assert lib.attn_paged_bwd_workspace_bytes(ctypes.byref(bad), ctypes.byref(n)) == codes["ATTN_ERR_SHAPE"]
