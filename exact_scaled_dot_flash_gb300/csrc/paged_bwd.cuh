@@ -369,10 +369,10 @@ cudaError_t launch_instance(const PagedParams& pp, const void* q, const void* qp
   const int group = pp.Hq / pp.Hkv;
   if (dk || dkp || dv) {
     // keys per CTA: the page's slots, rounded up so that a CTA is whole warps;
-    // over the listed pages, at most 1024 page slots of CTAs stride the list
+    // over the listed pages (usually few), 128 page slots of CTAs stride the list
     const int unit = 32 / TPK;
     const int kpc = pp.page_size >= C::ROWS ? C::ROWS : (pp.page_size + unit - 1) / unit * unit;
-    const unsigned units = static_cast<unsigned>(skip_single ? std::min(pp.num_pages, 1024) : pp.num_pages);
+    const unsigned units = static_cast<unsigned>(skip_single ? std::min(pp.num_pages, 128) : pp.num_pages);
     const dim3 grid(units * pp.Hkv, static_cast<unsigned>((pp.page_size + kpc - 1) / kpc));
     const size_t smem = C::dkdv_smem(MLA);
     auto kern = dkdv_kernel<DK, PD, TPK, DT, MLA>;
