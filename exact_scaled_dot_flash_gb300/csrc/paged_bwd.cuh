@@ -36,6 +36,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "paged_bwd.h"
 #include "params.h"
@@ -359,6 +360,18 @@ __global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q,
   }
 }
 
+// Opts a kernel into `smem` bytes of dynamic shared memory when that is above
+// the default 48 KB, once per device (`done`: the kernel's own device mask).
+template <typename Kernel>
+cudaError_t allow_smem(Kernel kern, size_t smem, int device, std::atomic<unsigned long long>& done) {
+  if (smem <= 48 * 1024) return cudaSuccess;
+  const unsigned long long bit = device >= 0 && device < 64 ? 1ull << device : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 // Launch both kernels of one instance (either may be skipped by passing no
 // outputs for it).
 template <int DK, int PD, int TPK, int DT, bool MLA>
@@ -366,6 +379,7 @@ cudaError_t launch_instance(const PagedParams& pp, const void* q, const void* qp
                             const void* v, const void* dout, const Buffers& b, void* dq, void* dqp, void* dk,
                             void* dkp, void* dv, float scale, cudaStream_t st, bool skip_single = false) {
   using C = Cfg<DK, PD, TPK>;
+  static std::atomic<unsigned long long> smem_done[2] = {{0}, {0}};  // this instance's two kernels
   const int group = pp.Hq / pp.Hkv;
   if (dk || dkp || dv) {
     // keys per CTA: the page's slots, rounded up so that a CTA is whole warps;
@@ -376,13 +390,11 @@ cudaError_t launch_instance(const PagedParams& pp, const void* q, const void* qp
     const dim3 grid(units * pp.Hkv, static_cast<unsigned>((pp.page_size + kpc - 1) / kpc));
     const size_t smem = C::dkdv_smem(MLA);
     auto kern = dkdv_kernel<DK, PD, TPK, DT, MLA>;
-    if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
-    }
+    cudaError_t e = allow_smem(kern, smem, pp.device, smem_done[0]);
+    if (e != cudaSuccess) return e;
     if (grid.x > 0) kern<<<grid, kpc * TPK, smem, st>>>(q, qp, k, kp, v, dout, b, dk, dkp, dv, pp, scale, kpc,
                                                       skip_single ? 1 : 0);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (dq || dqp) {
@@ -390,10 +402,8 @@ cudaError_t launch_instance(const PagedParams& pp, const void* q, const void* qp
     const dim3 grid(static_cast<unsigned>(pp.num_seqs) * pp.Hkv, static_cast<unsigned>(blocks));
     const size_t smem = C::dq_smem(MLA);
     auto kern = dq_kernel<DK, PD, TPK, DT, MLA>;
-    if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
-    }
+    cudaError_t e = allow_smem(kern, smem, pp.device, smem_done[1]);
+    if (e != cudaSuccess) return e;
     if (grid.x > 0 && grid.y > 0) kern<<<grid, THREADS, smem, st>>>(q, qp, k, kp, v, dout, b, dq, dqp, pp, scale);
   }
   return cudaGetLastError();

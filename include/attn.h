@@ -360,8 +360,12 @@ ATTN_API int attn_paged_mla_workspace_bytes(const attn_mla_shape_t* shape, int n
  *   outputs in dtype, 16-byte aligned device pointers; each may be NULL (not
  *   computed). dk_cache and dv_cache are written entirely; dq rows outside
  *   every sequence's range (or beyond max_queries) are not written.
- * D in {16, 32, 64, 128}, every dtype (fp32 FMA arithmetic). Returns ATTN_OK or
- * a negative ATTN_ERR_* code (validation before any launch). */
+ * D in {16, 32, 64, 128}, every dtype. F16/BF16 calls with D in {64, 128} and a
+ * page size that is a multiple of 8 dividing 128 or a multiple of 128 run on
+ * the tensor cores (pages with exactly one reader written by them, the others
+ * by an fp32 FMA pass over those pages); the rest on fp32 FMA kernels.
+ * Returns ATTN_OK or a negative ATTN_ERR_* code (validation before any
+ * launch). */
 ATTN_API int attn_paged_bwd(const attn_paged_shape_t* shape,
                             const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_table, const int32_t* seq_lens,
