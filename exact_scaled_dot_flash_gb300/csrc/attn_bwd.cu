@@ -15,7 +15,8 @@
 // GQA: dk, dv of a key/value head sum over its query heads. Rows with
 // lse = -inf (no visible key) contribute nothing and get dq = 0.
 //
-// Three kernels: a per-row preprocess (D_i and lse in log2 units), a
+// Three kernels: a per-row preprocess (D_i and lse in log2 units; the paged
+// backward's row-statistics kernel), a
 // key-major kernel for dk, dv (each CTA owns 64 keys of one (b, kv head) and
 // walks every query row of the group that can see them), and a query-major
 // kernel for dq (64 rows per CTA, keys streamed through shared memory).
@@ -24,6 +25,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "paged_bwd.h"
 #include "params.h"
 #include "ptx.cuh"
 #include "simt.cuh"
@@ -40,25 +42,6 @@ constexpr int ROWS = 64;     // keys (dk/dv kernel) or query rows (dq kernel) pe
 constexpr int THREADS = 256;
 constexpr int RT = 32;       // query rows (or keys) per shared-memory tile
 constexpr float LOG2E = 1.4426950408889634f;
-
-// D_i = dout_i . o_i and lse_i * log2(e), one warp per row.
-template <int D, int DT>
-__global__ void __launch_bounds__(256) preprocess_kernel(const void* out, const void* dout,
-                                                         const float* lse, float* dsum,
-                                                         float* lse2, int64_t rows) {
-  const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
-  float acc = 0.f;
-  for (int g = lane; g < D / 4; g += 32)
-    acc = dot4(load4<DT>(out, r * (D / 4) + g), load4<DT>(dout, r * (D / 4) + g), acc);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
-    dsum[r] = acc;
-    lse2[r] = lse[r] * LOG2E;  // -inf stays -inf
-  }
-}
 
 // dk, dv: CTA = 64 keys of one (b, kv head); all query heads of its group.
 template <int D, int DT, bool BIAS>
@@ -262,10 +245,7 @@ static cudaError_t launch_d(const KernelParams& p, const void* q, const void* k,
                             float* lse2, void* dq, void* dk, void* dv, float scale,
                             cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Sq;
-  const int64_t pre_blocks = (rows * 32 + 255) / 256;
-  if (pre_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  preprocess_kernel<D, DT><<<static_cast<unsigned>(pre_blocks), 256, 0, st>>>(out, dout, lse, dsum, lse2, rows);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_bwd_preprocess(D, DT, out, dout, lse, dsum, lse2, rows, st);
   if (e != cudaSuccess) return e;
   const dim3 g_kv(static_cast<unsigned>(p.B) * p.Hkv, static_cast<unsigned>((p.Sk + ROWS - 1) / ROWS));
   const dim3 g_q(static_cast<unsigned>(p.B) * p.Hq, static_cast<unsigned>((p.Sq + ROWS - 1) / ROWS));
@@ -295,25 +275,14 @@ static cudaError_t launch_dt(int D, const KernelParams& p, const void* q, const 
 
 }  // namespace bwd
 
+// D_i = dout_i . o_i and lse_i in log2 units (the paged backward's row
+// statistics kernel: rows of D elements, 16-byte loads, D_i = 0 for a row
+// with no visible key).
 cudaError_t launch_bwd_preprocess(int D, int dtype, const void* out, const void* dout, const float* lse,
                                   float* dsum, float* lse2, int64_t rows, cudaStream_t st) {
-  const int64_t blocks = (rows * 32 + 255) / 256;
-  if (blocks <= 0) return cudaSuccess;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const unsigned nb = static_cast<unsigned>(blocks);
-#define ATTN_PRE(DD, TT) bwd::preprocess_kernel<DD, TT><<<nb, 256, 0, st>>>(out, dout, lse, dsum, lse2, rows)
-#define ATTN_PRE_D(DD) \
-  case DD: if (dtype == 0) ATTN_PRE(DD, 0); else if (dtype == 1) ATTN_PRE(DD, 1); else ATTN_PRE(DD, 2); break;
-  switch (D) {
-    ATTN_PRE_D(16)
-    ATTN_PRE_D(32)
-    ATTN_PRE_D(64)
-    ATTN_PRE_D(128)
-    default: return cudaErrorInvalidValue;
-  }
-#undef ATTN_PRE_D
-#undef ATTN_PRE
-  return cudaGetLastError();
+  if (!(D == 16 || D == 32 || D == 64 || D == 128)) return cudaErrorInvalidValue;
+  const pbwd::Buffers b{dsum, lse2, nullptr, nullptr, nullptr, nullptr};
+  return pbwd::launch_preprocess(dtype, D, out, dout, lse, b, rows, st);
 }
 
 cudaError_t launch_bwd_simt(int D, int dtype, const KernelParams& p, const void* q, const void* k,
