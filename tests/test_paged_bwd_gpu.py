@@ -223,3 +223,27 @@ def test_mla_bwd_shared_prefix_and_determinism():
     torch.cuda.synchronize()
     for t, u in zip(a, b):
         assert torch.equal(t.view(torch.int16), u.view(torch.int16))
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64)])
+def test_paged_bwd_invalid_page_entry_reads_zeros(dtype, D):
+    # a table entry outside the cache inside a sequence's range reads as zero
+    # keys and values (as in the forward) and receives nothing: the same as a
+    # valid page of zeros, whose own gradient is simply not kept
+    import torch
+    w = PW(f"pbwd_invalid_{dtype}", dtype, 3, 8, 2, D, 16, (40, 120), (2, 9), seed=31, spare_pages=2)
+    x = synth.make_paged_inputs(w)
+    pages = x["k_cache"].shape[0]
+    zero = np.zeros_like(x["k_cache"][:1])
+    x_zero = {**x, "k_cache": np.concatenate([x["k_cache"], zero]), "v_cache": np.concatenate([x["v_cache"], zero])}
+    t_zero = x["block_table"].copy()
+    t_bad = x["block_table"].copy()
+    t_zero[0, 1] = pages       # the appended zero page
+    t_bad[0, 1] = pages + 50   # outside the cache
+    g = dout_like(w.seed, x["q"], w.dtype)
+    a = run_paged(w, {**x_zero, "block_table": t_zero}, g)
+    b = run_paged(w, {**x, "block_table": t_bad}, g)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_f64(b[0]), to_f64(a[0]))
+    for i in (1, 2):
+        np.testing.assert_array_equal(to_f64(b[i]), to_f64(a[i])[:pages])
