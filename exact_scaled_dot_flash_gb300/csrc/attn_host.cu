@@ -33,8 +33,7 @@ constexpr int kTargetChunks = 8;  // enough chunks to overlap; 16 measured no be
 int64_t up256(int64_t x) { return (x + 255) / 256 * 256; }
 
 struct HostPlan {
-  int nh = 0;     // kv heads per chunk (the last chunk of a batch index may have fewer)
-  int per_b = 0;  // chunks per batch index
+  int nh = 0;  // kv heads of the largest chunk
   int64_t q_bytes = 0, kv_bytes = 0, bias_bytes = 0;  // of the largest chunk
   int64_t off_q = 0, off_k = 0, off_v = 0, off_o = 0, off_bias = 0;  // within a slot
   int64_t off_lens = 0, off_slot[2] = {0, 0}, slot_bytes = 0, total = 0;
@@ -48,7 +47,6 @@ HostPlan make_plan(const attn_shape_t& s, int es, bool bias) {
   int want = (kTargetChunks + s.B - 1) / s.B;
   want = want < 1 ? 1 : (want > s.Hkv ? s.Hkv : want);
   p.nh = (s.Hkv + want - 1) / want;
-  p.per_b = (s.Hkv + p.nh - 1) / p.nh;
   p.q_bytes = static_cast<int64_t>(p.nh) * g * s.Sq * s.D * es;
   p.kv_bytes = static_cast<int64_t>(p.nh) * s.Sk * s.D * es;
   p.bias_bytes = bias ? static_cast<int64_t>(s.bias_h == 1 ? 1 : p.nh * g) * s.Sq * s.Sk * 4 : 0;
@@ -172,9 +170,13 @@ int attn_fwd_host(const attn_shape_t* shape, const void* q, const void* k, const
   if (e == cudaSuccess && d_lens) e = cp(d_lens, kv_lens, static_cast<int64_t>(s.B) * 4, cudaMemcpyHostToDevice, x.up);
   int c = 0;
   for (int b = 0; b < s.B && e == cudaSuccess && rc == ATTN_OK; ++b) {
-    for (int j = 0; j < p.per_b && e == cudaSuccess && rc == ATTN_OK; ++j, ++c) {
-      const int h0 = j * p.nh;
-      const int nh = (h0 + p.nh <= s.Hkv) ? p.nh : s.Hkv - h0;
+    // chunks of p.nh kv heads; in the last batch index they taper (p.nh, p.nh/2,
+    // then p.nh/4 each) so that the compute and download left after the last
+    // upload are short
+    int step = p.nh;
+    for (int h0 = 0; h0 < s.Hkv && e == cudaSuccess && rc == ATTN_OK; h0 += step, ++c) {
+      if (b == s.B - 1 && h0 > 0) step = step / 2 > (p.nh + 3) / 4 ? step / 2 : (p.nh + 3) / 4;
+      const int nh = (h0 + step <= s.Hkv) ? step : s.Hkv - h0;
       const int sl = c & 1;
       uint8_t* slot = ws + p.off_slot[sl];
       const int64_t qoff = (static_cast<int64_t>(b) * s.Hq + static_cast<int64_t>(h0) * g) * row_q;
