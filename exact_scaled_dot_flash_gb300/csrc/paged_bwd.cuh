@@ -24,7 +24,9 @@
 //    page and key/value head, keeps their rows in registers, and walks the
 //    table entries that read the page (ascending), and for each the (query,
 //    head) rows of that sequence (ascending) staged through shared memory;
-//    slots of a page nobody reads are written as zeros;
+//    slots of a page nobody reads are written as zeros. After the tensor-core
+//    kernels it runs only over the index's list of pages whose reader count is
+//    not one, its CTAs striding over the list;
 //  - query-major (dq_kernel): a CTA owns ROWS (query, head) rows of one
 //    sequence and key/value head and streams the sequence's keys, gathered
 //    through the page table, through shared memory.
