@@ -155,43 +155,93 @@ __device__ __forceinline__ void dkdv_page(const void* __restrict__ q, const void
     const int npairs = n * group;
     int e_lo = 0;  // rows before e_lo see none of these keys (default positions only)
     if (pp.causal && !pp.positions) e_lo = max(0, kmin - (L - n)) * group;
-    for (int e0 = e_lo; e0 < npairs; e0 += RT) {
-      __syncthreads();
-      for (int idx = tid; idx < RT * (2 * G + PG); idx += blockDim.x) {
-        const int r = idx / (2 * G + PG), c = idx - r * (2 * G + PG);
-        const int e = e0 + r;
-        const bool in = e < npairs;
-        const int qi = in ? e / group : 0;
-        const size_t rr = static_cast<size_t>(q0 + qi) * pp.Hq + hk * group + (in ? e - qi * group : 0);
-        if (c < G) qs[r * G + c] = in ? load4<DT>(q, rr * G + c) : z;
-        else if (c < 2 * G) gs[r * G + c - G] = in ? load4<DT>(dout, rr * G + c - G) : z;
-        else qps[r * PG + c - 2 * G] = in ? load4<DT>(qp, rr * PG + c - 2 * G) : z;
+    // the (query, head) rows of tile e0 of this sequence: element idx of the
+    // tile is column c of row r (q, then dout, then qp); row r's statistics
+    auto row_of = [&](int e, size_t& rr) {
+      const bool in = e < npairs;
+      const int qi = in ? e / group : 0;
+      rr = static_cast<size_t>(q0 + qi) * pp.Hq + hk * group + (in ? e - qi * group : 0);
+      return in;
+    };
+    auto element = [&](int e0, int idx) {
+      const int r = idx / (2 * G + PG), c = idx - r * (2 * G + PG);
+      size_t rr;
+      if (!row_of(e0 + r, rr)) return z;
+      return c < G ? load4<DT>(q, rr * G + c)
+                   : (c < 2 * G ? load4<DT>(dout, rr * G + c - G) : load4<DT>(qp, rr * PG + c - 2 * G));
+    };
+    auto put = [&](int idx, float4 v) {
+      const int r = idx / (2 * G + PG), c = idx - r * (2 * G + PG);
+      if (c < G) qs[r * G + c] = v;
+      else if (c < 2 * G) gs[r * G + c - G] = v;
+      else qps[r * PG + c - 2 * G] = v;
+    };
+    // full 256-thread CTAs load the next tile into registers while computing
+    // this one (its latency would otherwise be paid once per tile)
+    constexpr int TOT = RT * (2 * G + PG);
+    constexpr int NPT = (TOT + THREADS - 1) / THREADS;
+    const bool pf = blockDim.x == THREADS;
+    float4 pre[NPT];
+    float pre_l2 = -INFINITY, pre_ds = 0.f;
+    int pre_pos = -1;
+    auto fetch = [&](int e0) {
+#pragma unroll
+      for (int k = 0; k < NPT; ++k) {
+        const int idx = tid + k * THREADS;
+        pre[k] = idx < TOT ? element(e0, idx) : z;
       }
       if (tid < RT) {
-        const int e = e0 + tid;
-        const bool in = e < npairs;
-        const int qi = in ? e / group : 0;
-        const size_t rr = static_cast<size_t>(q0 + qi) * pp.Hq + hk * group + (in ? e - qi * group : 0);
-        const float l2 = in ? b.lse2[rr] : -INFINITY;
-        ls[tid] = l2;
-        dss[tid] = l2 != -INFINITY ? b.dsum[rr] : 0.f;
-        ps[tid] = in ? position_of(pp, q0 + qi, q0, n, L) : -1;
+        size_t rr;
+        const bool in = row_of(e0 + tid, rr);
+        pre_l2 = in ? b.lse2[rr] : -INFINITY;
+        pre_ds = in ? b.dsum[rr] : 0.f;
+        pre_pos = in ? position_of(pp, static_cast<int>(rr / pp.Hq), q0, n, L) : -1;
+      }
+    };
+    if (pf && e_lo < npairs) fetch(e_lo);
+    for (int e0 = e_lo; e0 < npairs; e0 += RT) {
+      __syncthreads();
+      if (pf) {
+#pragma unroll
+        for (int k = 0; k < NPT; ++k)
+          if (tid + k * THREADS < TOT) put(tid + k * THREADS, pre[k]);
+      } else {
+        for (int idx = tid; idx < TOT; idx += blockDim.x) put(idx, element(e0, idx));
+        if (tid < RT) {
+          size_t rr;
+          const bool in = row_of(e0 + tid, rr);
+          pre_l2 = in ? b.lse2[rr] : -INFINITY;
+          pre_ds = in ? b.dsum[rr] : 0.f;
+          pre_pos = in ? position_of(pp, static_cast<int>(rr / pp.Hq), q0, n, L) : -1;
+        }
+      }
+      if (tid < RT) {
+        ls[tid] = pre_l2;
+        dss[tid] = pre_l2 != -INFINITY ? pre_ds : 0.f;
+        ps[tid] = pre_pos;
       }
       __syncthreads();
+      if (pf && e0 + RT < npairs) fetch(e0 + RT);
       const int rows_here = min(RT, npairs - e0);  // rows past the sequence's last are not visited
 #pragma unroll 2
       for (int r = 0; r < rows_here; ++r) {
-        float sd = 0.f, pd = 0.f;
+        // two independent partial sums per dot product (shorter FMA chains)
+        float sa = 0.f, sb = 0.f, pa = 0.f, pb = 0.f;
 #pragma unroll
         for (int c = 0; c < GPT; ++c) {
-          sd = dot4(qs[r * G + part + TPK * c], kr[c], sd);
-          pd = dot4(gs[r * G + part + TPK * c], MLA ? kr[c] : vr[c], pd);
+          if (c & 1) {
+            sb = dot4(qs[r * G + part + TPK * c], kr[c], sb);
+            pb = dot4(gs[r * G + part + TPK * c], MLA ? kr[c] : vr[c], pb);
+          } else {
+            sa = dot4(qs[r * G + part + TPK * c], kr[c], sa);
+            pa = dot4(gs[r * G + part + TPK * c], MLA ? kr[c] : vr[c], pa);
+          }
         }
 #pragma unroll
         for (int c = 0; c < PPT; ++c)
-          if (part + TPK * c < PG) sd = dot4(qps[r * PG + part + TPK * c], kpr[c], sd);
-        sd = quad_sum<TPK>(sd);
-        pd = quad_sum<TPK>(pd);
+          if (part + TPK * c < PG) sb = dot4(qps[r * PG + part + TPK * c], kpr[c], sb);
+        const float sd = quad_sum<TPK>(sa + sb);
+        const float pd = quad_sum<TPK>(pa + pb);
         const float l2 = ls[r];
         const bool vis = key_vis && l2 != -INFINITY && (!pp.causal || kpos <= ps[r]);
         const float pr = vis ? fast_exp2(sd * pp.scale_log2 - l2) : 0.f;
@@ -309,34 +359,68 @@ __global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q,
   __syncthreads();
   const int hi = hi_s;
 
-  for (int key0 = 0; key0 < hi; key0 += RT) {
-    __syncthreads();
-    for (int idx = tid; idx < RT * (G + VG + PG); idx += blockDim.x) {
+  // the key tile at key0, gathered through the page table into registers one
+  // tile ahead (its load latency hides behind the current tile), then stored
+  // to shared memory: element idx is column c of key row r (k, then v, then kp)
+  constexpr int TOT = RT * (G + VG + PG);
+  constexpr int NPT = (TOT + THREADS - 1) / THREADS;
+  float4 pre[NPT];
+  auto fetch = [&](int key0) {
+#pragma unroll
+    for (int u = 0; u < NPT; ++u) {
+      const int idx = tid + u * THREADS;
       const int r = idx / (G + VG + PG), c = idx - r * (G + VG + PG);
       const int j = key0 + r;
       int pg = -1;
-      if (j < hi) pg = __ldg(pp.block_table + static_cast<size_t>(s) * pp.max_pages + j / P);
+      if (idx < TOT && j < hi) pg = __ldg(pp.block_table + static_cast<size_t>(s) * pp.max_pages + j / P);
       const bool ok = pg >= 0 && pg < pp.num_pages;  // entries outside the cache read as zero keys
       const size_t sl = ok ? static_cast<size_t>(pg) * P + j % P : 0;
-      if (c < G) ks[r * G + c] = ok ? load4<DT>(k, (sl * pp.Hkv + hk) * G + c) : z;
-      else if (c < G + VG) vs[r * VG + c - G] = ok ? load4<DT>(v, (sl * pp.Hkv + hk) * G + c - G) : z;
-      else kps[r * PG + c - G - VG] = ok ? load4<DT>(kp, sl * PG + c - G - VG) : z;
+      float4 x = z;
+      if (ok) {
+        if (c < G) x = load4<DT>(k, (sl * pp.Hkv + hk) * G + c);
+        else if (c < G + VG) x = load4<DT>(v, (sl * pp.Hkv + hk) * G + c - G);
+        else x = load4<DT>(kp, sl * PG + c - G - VG);
+      }
+      pre[u] = x;
+    }
+  };
+  if (hi > 0) fetch(0);
+  for (int key0 = 0; key0 < hi; key0 += RT) {
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < NPT; ++u) {
+      const int idx = tid + u * THREADS;
+      if (idx < TOT) {
+        const int r = idx / (G + VG + PG), c = idx - r * (G + VG + PG);
+        if (c < G) ks[r * G + c] = pre[u];
+        else if (c < G + VG) vs[r * VG + c - G] = pre[u];
+        else kps[r * PG + c - G - VG] = pre[u];
+      }
     }
     __syncthreads();
+    if (key0 + RT < hi) fetch(key0 + RT);
 #pragma unroll 2
     for (int c2 = 0; c2 < RT; ++c2) {
       const int j = key0 + c2;
-      float sd = 0.f, pd = 0.f;
+      // two independent partial sums per dot product (shorter FMA chains)
+      float sa = 0.f, sb = 0.f, pa = 0.f, pb = 0.f;
 #pragma unroll
       for (int c = 0; c < GPT; ++c) {
-        sd = dot4(qr[c], ks[c2 * G + part + TPK * c], sd);
-        pd = dot4(gr[c], MLA ? ks[c2 * G + part + TPK * c] : vs[c2 * VG + part + TPK * c], pd);
+        const float4 kv = ks[c2 * G + part + TPK * c];
+        const float4 vv = MLA ? kv : vs[c2 * VG + part + TPK * c];
+        if (c & 1) {
+          sb = dot4(qr[c], kv, sb);
+          pb = dot4(gr[c], vv, pb);
+        } else {
+          sa = dot4(qr[c], kv, sa);
+          pa = dot4(gr[c], vv, pa);
+        }
       }
 #pragma unroll
       for (int c = 0; c < PPT; ++c)
-        if (part + TPK * c < PG) sd = dot4(qpr[c], kps[c2 * PG + part + TPK * c], sd);
-      sd = quad_sum<TPK>(sd);
-      pd = quad_sum<TPK>(pd);
+        if (part + TPK * c < PG) sb = dot4(qpr[c], kps[c2 * PG + part + TPK * c], sb);
+      const float sd = quad_sum<TPK>(sa + sb);
+      const float pd = quad_sum<TPK>(pa + pb);
       const bool vis = live && j < L && (!pp.causal || j <= pos);
       const float pr = vis ? fast_exp2(sd * pp.scale_log2 - l2) : 0.f;
       const float ds = vis ? pr * (pd - dsi) : 0.f;
