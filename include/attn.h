@@ -1,6 +1,10 @@
 /*
- * attn.h - C ABI of the exact scaled-dot-product attention forward library
- * (libattn.so) for GB300 / sm_103a.
+ * attn.h - C ABI of the exact scaled-dot-product attention library
+ * (libattn.so) for GB300 / sm_103a: the dense forward (attn_fwd, with key
+ * splits and the log-sum-exp in attn_fwd_split, on host buffers in
+ * attn_fwd_host), its backward (attn_bwd), attention and MLA over a paged
+ * cache (attn_paged_fwd, attn_paged_mla) and their backward (attn_paged_bwd,
+ * attn_paged_mla_bwd). Each entry below states its own definition and source.
  *
  * The operation, per batch b, query head hq and query row i:
  *
