@@ -262,6 +262,51 @@ def step_flops(w):
     return 4.0 * w.B * w.Hq * w.D * pairs, "exact: 4*D per visible (query, key) pair"
 
 
+def measure_f16_peak(device, n=8192, reps=10):
+    """Dense F16 tensor throughput on this GPU: torch.matmul of two n x n f16
+    matrices (2 n^3 FLOP), best of ``reps`` timed with CUDA events. Serves as
+    the roofline denominator of F16 workloads (the BF16 one is the driver's
+    measurement in MEASURED_PEAKS.json)."""
+    import torch
+    a = torch.randn(n, n, device=device, dtype=torch.float16)
+    b = torch.randn(n, n, device=device, dtype=torch.float16)
+    c = torch.empty(n, n, device=device, dtype=torch.float16)
+    for _ in range(3):
+        torch.matmul(a, b, out=c)
+    best = float("inf")
+    for _ in range(reps):
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_ev.record()
+        torch.matmul(a, b, out=c)
+        e_ev.record()
+        torch.cuda.synchronize()
+        best = min(best, s_ev.elapsed_time(e_ev))
+    del a, b, c
+    return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+
+
+def padding_ideal(w, x, peak_tflops, hbm_gbs):
+    """Exact work of a key-padding workload: 4*D FLOP per visible (query, key)
+    pair, and the bytes needed once (Q, O, the valid K/V rows, the bias once,
+    kv_lens); the ideal time is the larger of FLOP/peak and bytes/bandwidth."""
+    import numpy as np
+    es = {"f32": 4, "f16": 2, "bf16": 2}[w.dtype]
+    L = np.clip(np.asarray(x["kv_lens"], dtype=np.int64), 0, w.Sk)
+    if w.causal:
+        i = np.arange(w.Sq, dtype=np.int64)
+        vis = np.minimum(L[:, None], np.clip(i[None, :] + (w.Sk - w.Sq) + 1, 0, w.Sk)).sum()
+    else:
+        vis = int(L.sum()) * w.Sq
+    flops = 4.0 * w.D * w.Hq * float(vis)
+    nbytes = 2 * w.B * w.Hq * w.Sq * w.D * es + 2 * int(L.sum()) * w.Hkv * w.D * es + 4 * w.B
+    if w.bias:
+        nbytes += w.bias_b * w.bias_h * w.Sq * w.Sk * 4
+    t_flop = flops / (peak_tflops * 1e12)
+    t_mem = nbytes / (hbm_gbs * 1e9)
+    return {"exact_flops": flops, "algorithmic_bytes": nbytes, "ideal_us": max(t_flop, t_mem) * 1e6,
+            "bound_of_ideal": "tensor" if t_flop >= t_mem else "hbm"}
+
+
 def bench_gpu(args):
     import torch
     from exact_scaled_dot_flash_gb300 import attn
@@ -412,6 +457,10 @@ def bench_gpu(args):
         return
     peaks, peak_kind = load_peaks()
     peak = float(peaks["bf16_tflops"])
+    peak_desc = f"{peak_kind} bf16 dense burst"
+    if w.dtype == "f16":  # F16 runs against an F16 peak measured in this run
+        peak = measure_f16_peak(device)
+        peak_desc = "f16 dense burst measured in this run (torch.matmul f16 8192^3, best of 10)"
     achieved = flops / (ms * 1e-3) / 1e12
     traffic = read_traffic(w)
     hbm_gbs = w.io_bytes() / (ms * 1e-3) / 1e9
@@ -432,7 +481,7 @@ def bench_gpu(args):
                    "launch": "CUDA graph of the K steps, one replay" if graph is not None else "eager"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_kind": f"{peak_kind} bf16 dense burst",
+                     "peak_kind": peak_desc,
                      "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
                      "kernel": KERNEL_NAME if w.dtype != "f32" else "attn_fwd_f32_kernel",
                      "hbm_gbs_algorithmic": hbm_gbs,
@@ -441,6 +490,10 @@ def bench_gpu(args):
         "gpu_launches": args.steps * (3 if args.pass_ == "bwd" else (2 if splits > 1 else 1)),
         "clocks": clocks.summary(),
     }
+    if w.mask & synth.MASK_KEY_PADDING and args.pass_ == "fwd":
+        ideal = padding_ideal(w, x, peak, float(peaks["hbm_gbs"]))
+        ideal["frac_of_ideal"] = ideal["ideal_us"] / (ms * 1e3)
+        line["roofline"]["padding"] = ideal
     if args.pass_ == "bwd" and w.dtype != "f32" and w.D in (64, 128):
         line["roofline"].update({"kernel": "dkdv_tc_kernel + dq_tc_kernel", "traffic": None})
     elif args.pass_ == "bwd":
