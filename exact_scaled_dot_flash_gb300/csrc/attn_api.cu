@@ -26,11 +26,22 @@ thread_local int g_last_cuda_error = 0;
 // Sticky per-device status word that kernels OR STATUS_* bits into.
 __device__ int g_status_word;
 
+// The status word's device address, per device and per CUDA context: after a
+// device or primary-context reset the module is loaded again and the address
+// may move, so a cached address is used only while the context it was looked
+// up in is still the current one.
 struct DeviceState {
-  std::once_flag once;
+  std::mutex mu;
+  unsigned long long ctx_id = 0;
   int* status = nullptr;
 };
 DeviceState g_devices[kMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+std::once_flag g_ctx_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
 
 std::once_flag g_encode_once;
 attn::EncodeTiledFn g_encode = nullptr;
@@ -47,14 +58,50 @@ attn::EncodeTiledFn encode_fn() {
   return g_encode;
 }
 
-// Device address of g_status_word on the current device (looked up once).
+}  // namespace
+
+// Unique id of the calling thread's current CUDA context (0 when there is
+// none yet, or the driver cannot tell).
+unsigned long long attn::current_context_id() {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(fn);
+  });
+  if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+namespace {
+
+// Device address of g_status_word on the current device `dev`, looked up
+// again whenever the current context differs from the one the cached address
+// came from; a failed lookup is not cached (the next call retries).
 int* status_ptr(int dev) {
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
   DeviceState& st = g_devices[dev];
-  std::call_once(st.once, [&st] {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) st.status = static_cast<int*>(p);
-  });
+  unsigned long long id = attn::current_context_id();
+  std::lock_guard<std::mutex> lock(st.mu);
+  if (st.status != nullptr && id != 0 && st.ctx_id == id) return st.status;
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = static_cast<int>(e);
+    return nullptr;
+  }
+  if (id == 0) id = attn::current_context_id();  // the lookup may have made the context current
+  st.status = static_cast<int*>(p);
+  st.ctx_id = id;
   return st.status;
 }
 

@@ -21,30 +21,42 @@ constexpr int kMaxDevices = 64;
 
 // The scratch of every attn_fwd_split_noalloc call on a device. The split
 // kernel writes every partial (O, m, l) the merge kernel reads before it is
-// read, so stale contents from an earlier call never leak into a result and
-// nothing has to be cleared between calls.
+// read, so nothing has to be cleared between calls; a split CTA whose bounded
+// wait expired writes (m = +inf, l = NaN) for its rows, which the merge turns
+// into NaN rows, so another call's partials never pass as a result.
 static __device__ __align__(256) unsigned char g_split_scratch[kScratchBytes];
 
+// In host code g_split_scratch names a host-side shadow, not device memory:
+// the device address comes from cudaGetSymbolAddress, called while the device
+// is current. It is cached per device together with the id of the CUDA
+// context it was looked up in; a later call in another context (after a
+// device or primary-context reset, which reloads the module and may move the
+// array) looks it up again. A failed lookup is not cached: the next call
+// retries, and the error is recorded for attn_last_cuda_error().
 struct ScratchState {
-  std::once_flag once;
+  std::mutex mu;
+  unsigned long long ctx_id = 0;
   void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
 };
 ScratchState g_scratch[kMaxDevices];
 
-// In host code g_split_scratch names a host-side shadow, not device memory:
-// the device address comes from cudaGetSymbolAddress, once per device, while
-// that device is current.
 int scratch_ptr(int dev, void** out) {
-  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return attn::record_cuda_error(cudaErrorInvalidDevice);
   ScratchState& st = g_scratch[dev];
-  std::call_once(st.once, [&st] {
-    void* p = nullptr;
-    st.err = cudaGetSymbolAddress(&p, g_split_scratch);
-    if (st.err == cudaSuccess) st.ptr = p;
-  });
-  if (st.err != cudaSuccess || st.ptr == nullptr) return ATTN_ERR_CUDA;
-  *out = st.ptr;
+  unsigned long long id = attn::current_context_id();
+  std::lock_guard<std::mutex> lock(st.mu);
+  if (st.ptr != nullptr && id != 0 && st.ctx_id == id) {
+    *out = st.ptr;
+    return ATTN_OK;
+  }
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_split_scratch);
+  if (e != cudaSuccess || p == nullptr)
+    return attn::record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+  if (id == 0) id = attn::current_context_id();  // the lookup may have made the context current
+  st.ptr = p;
+  st.ctx_id = id;
+  *out = p;
   return ATTN_OK;
 }
 
@@ -63,8 +75,8 @@ extern "C" int attn_fwd_split_noalloc(const attn_shape_t* shape, const void* q, 
     return attn_fwd_split(shape, q, k, v, mask_kind, kv_lens, bias, scale, dtype, num_splits,
                           nullptr, 0, out, lse, stream);
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return attn::record_cuda_error(e);
   void* ws = nullptr;
   const int sr = scratch_ptr(dev, &ws);
   if (sr != ATTN_OK) return sr;

@@ -8,7 +8,8 @@
 // score). With M = max_s m_s and w_s = 2^(m_s - M) (0 for an empty part):
 //   O = sum_s w_s O_s / sum_s w_s l_s,   lse = (M + log2 sum_s w_s l_s) ln 2,
 // which is the softmax over the union of the parts. A row whose parts are all
-// empty has no visible key: O is NaN and lse is -inf.
+// empty has no visible key: O is NaN and lse is -inf. A part whose kernel gave
+// up on a bounded wait stores m = +inf, l = NaN, which makes O and lse NaN.
 #include "params.h"
 #include "ptx.cuh"
 
@@ -55,7 +56,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const KernelParams p, void* 
     reinterpret_cast<uint2*>(out)[r * G + g] =
         make_uint2(pack2<BF16>(acc.x, acc.y), pack2<BF16>(acc.z, acc.w));
   }
-  if (g == 0 && p.lse != nullptr) p.lse[r] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
+  // L is NaN only when a part reported a failed kernel wait (m = +inf, l = NaN)
+  if (g == 0 && p.lse != nullptr)
+    p.lse[r] = L > 0.f ? (M + log2f(L)) * LN2 : (L == 0.f ? -INFINITY : __int_as_float(0x7fc00000));
 }
 
 __global__ void fill_kernel(float* out, int64_t count, float value) {

@@ -587,13 +587,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool ok = mbar_wait(bar(C::BAR_O + t), 0);
         if (__any_sync(0xffffffffu, !ok)) failed = true;
       }
+      const size_t rr =
+          (static_cast<size_t>(blockIdx.x % p.num_splits) * p.B * p.Hq + w.bh) * p.Sq +
+          static_cast<size_t>(row_g);
       if (failed) {
         if (lane == 0) fail();
+        // m = +inf, l = NaN: the merge makes the row NaN whatever the other
+        // parts (or an earlier call's scratch) hold
+        if (row_g < p.Sq) p.ws_ml[rr] = make_float2(INFINITY, __int_as_float(0x7fc00000));
       } else {
         tc_fence_after();
-        const size_t rr =
-            (static_cast<size_t>(blockIdx.x % p.num_splits) * p.B * p.Hq + w.bh) * p.Sq +
-            static_cast<size_t>(row_g);
         float4* wrow = reinterpret_cast<float4*>(p.ws_o + rr * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {

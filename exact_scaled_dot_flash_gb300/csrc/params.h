@@ -131,5 +131,9 @@ cudaError_t launch_wait_timeout_probe(int* status, unsigned long long limit_ns,
                                       cudaStream_t stream);
 // Records a failed CUDA call for attn_last_cuda_error(); returns ATTN_ERR_CUDA.
 int record_cuda_error(cudaError_t e);
+// Unique id of the calling thread's current CUDA context, 0 if there is none.
+// Caches of device addresses are keyed on it: a device reset reloads the
+// module and may move every __device__ variable.
+unsigned long long current_context_id();
 
 }  // namespace attn

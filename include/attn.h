@@ -451,10 +451,19 @@ ATTN_API int attn_paged_mla_bwd_workspace_bytes(const attn_mla_shape_t* shape, s
  *
  * Set-up: the first call with num_splits > 1 on a device looks up the
  * array's device address (cudaGetSymbolAddress, with that device current)
- * and caches it; make that first call before any stream capture begins.
+ * and caches it with the id of the current CUDA context; make that first
+ * call before any stream capture begins. A call made in another context
+ * than the cached one (after cudaDeviceReset or a primary-context reset,
+ * which reload the library's device module and may move the array) looks
+ * the address up again, as does every call after a failed lookup.
  *
- * Returns ATTN_OK, ATTN_ERR_SCRATCH, ATTN_ERR_CUDA if the set-up fails, or
- * any code of attn_fwd_split. */
+ * A split CTA whose bounded wait expired (a nonzero attn_device_status
+ * word) writes partials that make its rows NaN in out (and
+ * their lse NaN), so a failed call never returns another call's partials.
+ *
+ * Returns ATTN_OK, ATTN_ERR_SCRATCH, ATTN_ERR_CUDA if the set-up fails (the
+ * CUDA error code is then in attn_last_cuda_error), or any code of
+ * attn_fwd_split. */
 ATTN_API int attn_fwd_split_noalloc(const attn_shape_t* shape,
                                     const void* q, const void* k, const void* v,
                                     int mask_kind, const int32_t* kv_lens,
