@@ -8,6 +8,7 @@ raises; there is no CPU fallback.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -51,75 +52,99 @@ def library_path() -> str:
     return os.path.join(_HERE, _LIBNAME)
 
 
+def checked_library_path() -> str:
+    """Path of the bounds-checked build (``build.build(checked=True)``)."""
+    return os.path.join(_HERE, "libattn_checked.so")
+
+
 def load_library():
     """Open libattn.so once; raise AttnError if it has not been built."""
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        path = library_path()
-        if not os.path.exists(path):
-            raise AttnError(f"{path} is missing: build the CUDA library first "
-                            "(python -c 'import __graft_entry__ as g; g.build()')")
-        lib = ctypes.CDLL(path)
-        vp = ctypes.c_void_p
-        lib.attn_fwd.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, ctypes.c_int, vp, vp,
-                                 ctypes.c_float, ctypes.c_int, vp, vp]
-        lib.attn_fwd.restype = ctypes.c_int
-        lib.attn_fwd_split.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, ctypes.c_int, vp, vp,
-                                       ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t,
+        if _lib is None:
+            _lib = _open(library_path())
+        return _lib
+
+
+@contextlib.contextmanager
+def use_library(path):
+    """Route every call of this module through the library build at ``path``
+    (for example the bounds-checked libattn_checked.so) while the block runs;
+    its device status word is then the one :func:`device_status` reads."""
+    global _lib
+    lib = _open(path)
+    with _lock:
+        prev, _lib = _lib, lib
+    try:
+        yield lib
+    finally:
+        with _lock:
+            _lib = prev
+
+
+def _open(path):
+    """Open a build of the library and declare its C signatures."""
+    if not os.path.exists(path):
+        raise AttnError(f"{path} is missing: build the CUDA library first "
+                        "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp = ctypes.c_void_p
+    lib.attn_fwd.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, ctypes.c_int, vp, vp,
+                             ctypes.c_float, ctypes.c_int, vp, vp]
+    lib.attn_fwd.restype = ctypes.c_int
+    lib.attn_fwd_split.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, ctypes.c_int, vp, vp,
+                                   ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t,
+                                   vp, vp, vp]
+    lib.attn_fwd_split.restype = ctypes.c_int
+    lib.attn_split_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.c_int,
+                                               ctypes.POINTER(ctypes.c_size_t)]
+    lib.attn_split_workspace_bytes.restype = ctypes.c_int
+    lib.attn_bwd.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp,
+                             ctypes.c_float, ctypes.c_int, vp, ctypes.c_size_t, vp, vp, vp, vp]
+    lib.attn_bwd.restype = ctypes.c_int
+    lib.attn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(ctypes.c_size_t)]
+    lib.attn_bwd_workspace_bytes.restype = ctypes.c_int
+    lib.attn_paged_fwd.argtypes = [ctypes.POINTER(PagedShape), vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                   ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp, vp, vp]
+    lib.attn_paged_workspace_bytes.argtypes = [ctypes.POINTER(PagedShape), ctypes.c_int,
+                                               ctypes.POINTER(ctypes.c_size_t)]
+    lib.attn_paged_workspace_bytes.restype = ctypes.c_int
+    lib.attn_paged_fwd.restype = ctypes.c_int
+    lib.attn_paged_mla.argtypes = [ctypes.POINTER(MlaShape), vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                   ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp, vp, vp]
+    lib.attn_paged_mla.restype = ctypes.c_int
+    lib.attn_paged_mla_workspace_bytes.argtypes = [ctypes.POINTER(MlaShape), ctypes.c_int,
+                                                   ctypes.POINTER(ctypes.c_size_t)]
+    lib.attn_paged_mla_workspace_bytes.restype = ctypes.c_int
+    lib.attn_paged_bwd.argtypes = [ctypes.POINTER(PagedShape), vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                   ctypes.c_float, ctypes.c_int, vp, vp, vp, vp, ctypes.c_size_t, vp, vp, vp, vp]
+    lib.attn_paged_bwd.restype = ctypes.c_int
+    lib.attn_paged_bwd_workspace_bytes.argtypes = [ctypes.POINTER(PagedShape), ctypes.POINTER(ctypes.c_size_t)]
+    lib.attn_paged_bwd_workspace_bytes.restype = ctypes.c_int
+    lib.attn_paged_mla_bwd.argtypes = [ctypes.POINTER(MlaShape), vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                       ctypes.c_float, ctypes.c_int, vp, vp, vp, vp, ctypes.c_size_t, vp, vp,
                                        vp, vp, vp]
-        lib.attn_fwd_split.restype = ctypes.c_int
-        lib.attn_split_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.c_int,
-                                                   ctypes.POINTER(ctypes.c_size_t)]
-        lib.attn_split_workspace_bytes.restype = ctypes.c_int
-        lib.attn_bwd.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp,
-                                 ctypes.c_float, ctypes.c_int, vp, ctypes.c_size_t, vp, vp, vp, vp]
-        lib.attn_bwd.restype = ctypes.c_int
-        lib.attn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(ctypes.c_size_t)]
-        lib.attn_bwd_workspace_bytes.restype = ctypes.c_int
-        lib.attn_paged_fwd.argtypes = [ctypes.POINTER(PagedShape), vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
-                                       ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp, vp, vp]
-        lib.attn_paged_workspace_bytes.argtypes = [ctypes.POINTER(PagedShape), ctypes.c_int,
-                                                   ctypes.POINTER(ctypes.c_size_t)]
-        lib.attn_paged_workspace_bytes.restype = ctypes.c_int
-        lib.attn_paged_fwd.restype = ctypes.c_int
-        lib.attn_paged_mla.argtypes = [ctypes.POINTER(MlaShape), vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
-                                       ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp, vp, vp]
-        lib.attn_paged_mla.restype = ctypes.c_int
-        lib.attn_paged_mla_workspace_bytes.argtypes = [ctypes.POINTER(MlaShape), ctypes.c_int,
+    lib.attn_paged_mla_bwd.restype = ctypes.c_int
+    lib.attn_paged_mla_bwd_workspace_bytes.argtypes = [ctypes.POINTER(MlaShape),
                                                        ctypes.POINTER(ctypes.c_size_t)]
-        lib.attn_paged_mla_workspace_bytes.restype = ctypes.c_int
-        lib.attn_paged_bwd.argtypes = [ctypes.POINTER(PagedShape), vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
-                                       ctypes.c_float, ctypes.c_int, vp, vp, vp, vp, ctypes.c_size_t, vp, vp, vp, vp]
-        lib.attn_paged_bwd.restype = ctypes.c_int
-        lib.attn_paged_bwd_workspace_bytes.argtypes = [ctypes.POINTER(PagedShape), ctypes.POINTER(ctypes.c_size_t)]
-        lib.attn_paged_bwd_workspace_bytes.restype = ctypes.c_int
-        lib.attn_paged_mla_bwd.argtypes = [ctypes.POINTER(MlaShape), vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
-                                           ctypes.c_float, ctypes.c_int, vp, vp, vp, vp, ctypes.c_size_t, vp, vp,
-                                           vp, vp, vp]
-        lib.attn_paged_mla_bwd.restype = ctypes.c_int
-        lib.attn_paged_mla_bwd_workspace_bytes.argtypes = [ctypes.POINTER(MlaShape),
-                                                           ctypes.POINTER(ctypes.c_size_t)]
-        lib.attn_paged_mla_bwd_workspace_bytes.restype = ctypes.c_int
-        lib.attn_fwd_host.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, ctypes.c_int, vp, vp, ctypes.c_float,
-                                      ctypes.c_int, vp, ctypes.c_size_t, vp, vp]
-        lib.attn_fwd_host.restype = ctypes.c_int
-        lib.attn_fwd_host_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.c_int, ctypes.c_int,
-                                                      ctypes.POINTER(ctypes.c_size_t)]
-        lib.attn_fwd_host_workspace_bytes.restype = ctypes.c_int
-        lib.attn_strerror.argtypes = [ctypes.c_int]
-        lib.attn_strerror.restype = ctypes.c_char_p
-        lib.attn_last_cuda_error.argtypes = []
-        lib.attn_last_cuda_error.restype = ctypes.c_int
-        lib.attn_device_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int]
-        lib.attn_device_status.restype = ctypes.c_int
-        lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, ctypes.c_void_p]
-        lib.attn_selftest_wait_timeout.restype = ctypes.c_int
-        lib.attn_version.argtypes = []
-        lib.attn_version.restype = ctypes.c_int
-        _lib = lib
-        return lib
+    lib.attn_paged_mla_bwd_workspace_bytes.restype = ctypes.c_int
+    lib.attn_fwd_host.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, ctypes.c_int, vp, vp, ctypes.c_float,
+                                  ctypes.c_int, vp, ctypes.c_size_t, vp, vp]
+    lib.attn_fwd_host.restype = ctypes.c_int
+    lib.attn_fwd_host_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.c_int, ctypes.c_int,
+                                                  ctypes.POINTER(ctypes.c_size_t)]
+    lib.attn_fwd_host_workspace_bytes.restype = ctypes.c_int
+    lib.attn_strerror.argtypes = [ctypes.c_int]
+    lib.attn_strerror.restype = ctypes.c_char_p
+    lib.attn_last_cuda_error.argtypes = []
+    lib.attn_last_cuda_error.restype = ctypes.c_int
+    lib.attn_device_status.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int]
+    lib.attn_device_status.restype = ctypes.c_int
+    lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, ctypes.c_void_p]
+    lib.attn_selftest_wait_timeout.restype = ctypes.c_int
+    lib.attn_version.argtypes = []
+    lib.attn_version.restype = ctypes.c_int
+    return lib
 
 
 def strerror(code: int) -> str:
@@ -179,7 +204,7 @@ def split_workspace_bytes(shape: Shape, num_splits: int) -> int:
 
 
 def fwd(q, k, v, *, causal: bool = False, kv_lens=None, bias=None, scale: float | None = None,
-        out=None, stream=None, num_splits: int = 1, return_lse: bool = False, workspace=None):
+        out=None, stream=None, num_splits: int = 1, return_lse: bool = False, workspace=None, lse_out=None):
     """O = softmax(Q K^T * scale + mask + bias) V on the GPU.
 
     q: [B,Hq,Sq,D]; k, v: [B,Hkv,Sk,D]; float32, float16 or bfloat16, contiguous.
@@ -188,7 +213,8 @@ def fwd(q, k, v, *, causal: bool = False, kv_lens=None, bias=None, scale: float 
     scale: defaults to 1/sqrt(D).
     num_splits: 1..32 key-range splits (attn_fwd_split); the fp32 workspace is
     taken from ``workspace`` (a CUDA uint8 tensor) or allocated here.
-    return_lse: also return the float32 [B,Hq,Sq] row log-sum-exp.
+    return_lse: also return the float32 [B,Hq,Sq] row log-sum-exp (written
+    into ``lse_out`` when given).
     Tensors on a CUDA device run on ``stream`` (default: the current stream)
     and the result is returned without synchronising. Host tensors run through
     attn_fwd_host on the current CUDA device (chunked uploads, kernels and
@@ -246,7 +272,7 @@ def fwd(q, k, v, *, causal: bool = False, kv_lens=None, bias=None, scale: float 
         call(shape, q.data_ptr(), k.data_ptr(), v.data_ptr(), mask, kv_ptr, b_ptr, scale,
              _dtype_code(q), out.data_ptr(), stream.cuda_stream)
         return out
-    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=dev) if return_lse else None
+    lse = _lse_buffer(lse_out, (B, Hq, Sq), dev) if return_lse else None
     need = split_workspace_bytes(shape, num_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
@@ -389,6 +415,26 @@ def bwd(q, k, v, out, dout, lse, *, causal: bool = False, kv_lens=None, bias=Non
     return dq, dk, dv
 
 
+def _lse_buffer(lse_out, shape, dev):
+    import torch
+    if lse_out is None:
+        return torch.empty(shape, dtype=torch.float32, device=dev)
+    if (tuple(lse_out.shape) != tuple(shape) or lse_out.dtype != torch.float32 or lse_out.device != dev
+            or not lse_out.is_contiguous()):
+        raise AttnError(f"lse_out must be a contiguous float32 {list(shape)} tensor on q's device")
+    return lse_out
+
+
+def _grad_buffer(name, given, like):
+    import torch
+    if given is None:
+        return torch.empty_like(like)
+    if (given.shape != like.shape or given.dtype != like.dtype or given.device != like.device
+            or not given.is_contiguous()):
+        raise AttnError(f"{name} must be a contiguous tensor shaped like its input")
+    return given
+
+
 def paged_workspace_bytes(shape: PagedShape, num_splits: int) -> int:
     """Workspace bytes attn_paged_fwd needs for ``shape`` and ``num_splits``."""
     n = ctypes.c_size_t(0)
@@ -398,7 +444,7 @@ def paged_workspace_bytes(shape: PagedShape, num_splits: int) -> int:
 
 def paged_fwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, *, positions=None, causal: bool = True,
               scale: float | None = None, max_queries: int | None = None, return_lse: bool = False, out=None,
-              stream=None, num_splits: int = 1, workspace=None):
+              stream=None, num_splits: int = 1, workspace=None, lse_out=None):
     """Attention of packed queries over a paged key/value cache (attn_paged_fwd).
 
     q [queries, Hq, D]; k_cache, v_cache [pages, page_size, Hkv, D] (same
@@ -408,7 +454,8 @@ def paged_fwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, *, position
     sequence (computed from q_offsets, with a host sync, when None).
     ``num_splits`` splits the keys of decode-shaped calls (workspace taken
     from ``workspace``, a CUDA uint8 tensor, or allocated here).
-    Returns out [queries, Hq, D] (and lse float32 [queries, Hq]).
+    Returns out [queries, Hq, D] (and lse float32 [queries, Hq], written into
+    ``lse_out`` when given).
     """
     import torch
 
@@ -441,7 +488,7 @@ def paged_fwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, *, position
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
-    lse = torch.empty((nq, Hq), dtype=torch.float32, device=dev) if return_lse else None
+    lse = _lse_buffer(lse_out, (nq, Hq), dev) if return_lse else None
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     shape = PagedShape(ns, nq, Hq, Hkv, D, P, pages, int(block_table.shape[1]), int(max_queries))
@@ -468,7 +515,7 @@ def mla_workspace_bytes(shape: MlaShape, num_splits: int) -> int:
 
 def paged_mla(q, qp, latent, kpos, block_table, seq_lens, q_offsets, *, positions=None, causal: bool = True,
               scale: float, max_queries: int | None = None, return_lse: bool = False, out=None, stream=None,
-              num_splits: int = 1, workspace=None):
+              num_splits: int = 1, workspace=None, lse_out=None):
     """MLA with absorbed projections over a paged latent cache (attn_paged_mla).
 
     q [queries, H, R]; qp [queries, H, Pd]; latent [pages, page_size, 1, R];
@@ -476,7 +523,7 @@ def paged_mla(q, qp, latent, kpos, block_table, seq_lens, q_offsets, *, position
     ``scale`` is the original model's QK scale. ``num_splits`` splits the key
     range of every 128-row block (workspace taken from ``workspace``, a CUDA
     uint8 tensor, or allocated here). Returns out [queries, H, R] (and lse
-    float32 [queries, H]).
+    float32 [queries, H], written into ``lse_out`` when given).
     """
     import torch
 
@@ -501,7 +548,7 @@ def paged_mla(q, qp, latent, kpos, block_table, seq_lens, q_offsets, *, position
         max_queries = int((q_offsets[1:] - q_offsets[:-1]).max().item()) if ns else 0
     if out is None:
         out = torch.empty_like(q)
-    lse = torch.empty((nq, H), dtype=torch.float32, device=dev) if return_lse else None
+    lse = _lse_buffer(lse_out, (nq, H), dev) if return_lse else None
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     shape = MlaShape(ns, nq, H, R, Pd, P, pages, int(block_table.shape[1]), int(max_queries))
@@ -537,14 +584,15 @@ def _workspace(need, workspace, dev):
 
 def paged_bwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, dout, *, out=None, lse=None, positions=None,
               causal: bool = True, scale: float | None = None, max_queries: int | None = None,
-              grads=("dq", "dk", "dv"), workspace=None, stream=None):
+              grads=("dq", "dk", "dv"), workspace=None, stream=None, dq=None, dk=None, dv=None):
     """Gradients of :func:`paged_fwd` for dL/dO = ``dout`` (attn_paged_bwd, ordered).
 
     Arguments as for :func:`paged_fwd`; ``out`` and ``lse`` are the forward's
     output and float32 [queries, Hq] log-sum-exp (when either is None the
     forward runs here first to recompute them). ``grads`` names the gradients
-    wanted. Returns (dq [queries, Hq, D], dk, dv [pages, page_size, Hkv, D]),
-    None in place of a gradient not asked for.
+    wanted; ``dq``/``dk``/``dv`` receive them when given. Returns (dq
+    [queries, Hq, D], dk, dv [pages, page_size, Hkv, D]), None in place of a
+    gradient not asked for.
     """
     import torch
 
@@ -568,9 +616,9 @@ def paged_bwd(q, k_cache, v_cache, block_table, seq_lens, q_offsets, dout, *, ou
     shape = PagedShape(ns, nq, Hq, Hkv, D, P, pages, int(block_table.shape[1]), int(max_queries))
     need = paged_bwd_workspace_bytes(shape)
     workspace = _workspace(need, workspace, dev)
-    dq = torch.empty_like(q) if "dq" in grads else None
-    dk = torch.empty_like(k_cache) if "dk" in grads else None
-    dv = torch.empty_like(v_cache) if "dv" in grads else None
+    dq = _grad_buffer("dq", dq, q) if "dq" in grads else None
+    dk = _grad_buffer("dk", dk, k_cache) if "dk" in grads else None
+    dv = _grad_buffer("dv", dv, v_cache) if "dv" in grads else None
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     ptr = lambda t: (t.data_ptr() or None) if t is not None else None
@@ -590,13 +638,15 @@ def mla_bwd_workspace_bytes(shape: MlaShape) -> int:
 
 def paged_mla_bwd(q, qp, latent, kpos, block_table, seq_lens, q_offsets, dout, *, out=None, lse=None,
                   positions=None, causal: bool = True, scale: float, max_queries: int | None = None,
-                  grads=("dq", "dqp", "dlatent", "dkpos"), workspace=None, stream=None):
+                  grads=("dq", "dqp", "dlatent", "dkpos"), workspace=None, stream=None, dq=None, dqp=None,
+                  dlatent=None, dkpos=None):
     """Gradients of :func:`paged_mla` for dL/dO = ``dout`` (attn_paged_mla_bwd, ordered).
 
     Returns (dq [queries, H, R], dqp [queries, H, Pd], dlatent [pages,
     page_size, 1, R] with its key and value parts, dkpos [pages, page_size, 1,
     Pd]), None in place of a gradient not asked for (or of dqp, dkpos when
-    Pd == 0). ``out``/``lse`` as for :func:`paged_bwd`.
+    Pd == 0); the given ``dq``/``dqp``/``dlatent``/``dkpos`` tensors receive
+    them. ``out``/``lse`` as for :func:`paged_bwd`.
     """
     import torch
 
@@ -619,10 +669,10 @@ def paged_mla_bwd(q, qp, latent, kpos, block_table, seq_lens, q_offsets, dout, *
     shape = MlaShape(ns, nq, H, R, Pd, P, pages, int(block_table.shape[1]), int(max_queries))
     need = mla_bwd_workspace_bytes(shape)
     workspace = _workspace(need, workspace, dev)
-    dq = torch.empty_like(q) if "dq" in grads else None
-    dqp = torch.empty_like(qp) if "dqp" in grads and Pd else None
-    dlat = torch.empty_like(latent) if "dlatent" in grads else None
-    dkp = torch.empty_like(kpos) if "dkpos" in grads and Pd else None
+    dq = _grad_buffer("dq", dq, q) if "dq" in grads else None
+    dqp = _grad_buffer("dqp", dqp, qp) if "dqp" in grads and Pd else None
+    dlat = _grad_buffer("dlatent", dlatent, latent) if "dlatent" in grads else None
+    dkp = _grad_buffer("dkpos", dkpos, kpos) if "dkpos" in grads and Pd else None
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     ptr = lambda t: (t.data_ptr() or None) if t is not None else None

@@ -5,6 +5,13 @@ under ``_build/``; the objects link into ``libattn.so`` next to this file
 with the CUDA runtime linked statically, so the library loads into any
 process (PyTorch's or a plain C program) without a torch ABI dependency.
 Run ``python -m exact_scaled_dot_flash_gb300.build`` or call :func:`build`.
+
+``build(checked=True)`` (``python -m exact_scaled_dot_flash_gb300.build
+--checked``) makes the bounds-checked variant ``libattn_checked.so`` from the
+same sources with ``-DATTN_CHECKED`` (objects under ``_build_checked/``): its
+paged, MLA, split and backward kernels test every computed global and
+shared-memory index and record a violation in the device status word
+(ATTN_STATUS_BOUNDS) instead of making the access.
 """
 from __future__ import annotations
 
@@ -22,6 +29,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
+CHECKED_OUT_DIR = os.path.join(PKG, "_build_checked")
+CHECKED_LIB = os.path.join(PKG, "libattn_checked.so")
+CHECKED_FLAGS = ("-DATTN_CHECKED",)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr",
               "-I", INCLUDE, "-I", CSRC]
@@ -66,8 +76,8 @@ def kernel_source_digest(names=None) -> str:
     return _digest(paths)[:16]
 
 
-def _compile(src, hdr_digest, verbose, extra_flags):
-    obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+def _compile(src, hdr_digest, verbose, extra_flags, out_dir=OUT_DIR):
+    obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
     stamp = obj + ".sha"
     key = _digest([src], (hdr_digest, *NVCC_FLAGS, *extra_flags))
     if os.path.exists(obj) and os.path.exists(stamp) and open(stamp).read() == key:
@@ -83,32 +93,35 @@ def _compile(src, hdr_digest, verbose, extra_flags):
     return obj, r.stdout + r.stderr
 
 
-def build(verbose: bool = False, jobs: int | None = None, extra_flags=()) -> str:
-    """Compile every CUDA translation unit for sm_103a and link libattn.so."""
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(verbose: bool = False, jobs: int | None = None, extra_flags=(), checked: bool = False) -> str:
+    """Compile every CUDA translation unit for sm_103a and link libattn.so
+    (with ``checked``, the bounds-checked libattn_checked.so)."""
+    out_dir, lib = (CHECKED_OUT_DIR, CHECKED_LIB) if checked else (OUT_DIR, LIB)
+    if checked:
+        extra_flags = tuple(extra_flags) + CHECKED_FLAGS
+    os.makedirs(out_dir, exist_ok=True)
     srcs = _sources()
     hdr = _digest(_headers())
     jobs = jobs or min(len(srcs), os.cpu_count() or 4)
     logs = []
     with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
-        futs = [ex.submit(_compile, s, hdr, verbose, tuple(extra_flags)) for s in srcs]
+        futs = [ex.submit(_compile, s, hdr, verbose, tuple(extra_flags), out_dir) for s in srcs]
         objs = []
         for f in futs:
             o, log = f.result()
             objs.append(o)
             if log:
                 logs.append(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
         sys.stdout.write("".join(logs))
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    build(verbose="-v" in sys.argv)
-    print(LIB)
+    print(build(verbose="-v" in sys.argv, checked="--checked" in sys.argv))

@@ -497,7 +497,8 @@ int attn_bwd(const attn_shape_t* shape, const void* q, const void* k, const void
   if (tc) {
     attn::EncodeTiledFn enc = encode_fn();
     if (!enc) return fail_cuda(cudaErrorNotSupported);
-    e = attn::launch_bwd_preprocess(s.D, static_cast<int>(dtype), out, dout, lse, dsum, lse2, bhq * s.Sq, st);
+    e = attn::launch_bwd_preprocess(s.D, static_cast<int>(dtype), out, dout, lse, dsum, lse2, bhq * s.Sq, st,
+                                    p.status);
     if (e != cudaSuccess) return fail_cuda(e);
     attn::BwdArgs a{lse2, dsum, dq, dk, dv, scale};
     const bool bf = dtype == ATTN_BF16;
@@ -917,7 +918,7 @@ int attn_paged_bwd(const attn_paged_shape_t* shape, const void* q, const void* k
                        s.max_queries, block_table, seq_lens, q_offsets, positions, causal, scale);
   const attn::pbwd::Buffers b = attn::pbwd::carve(workspace, lay);
   e = attn::pbwd::launch_preprocess(static_cast<int>(dtype), s.D, out, dout, lse, b,
-                                    static_cast<int64_t>(s.num_queries) * s.Hq, st);
+                                    static_cast<int64_t>(s.num_queries) * s.Hq, st, pp.status);
   if (e == cudaSuccess && (dk_cache || dv_cache)) e = attn::pbwd::launch_page_index(pp, b, st);
   // F16/BF16 with D in {64, 128} and a page size the 128-key tile gathers
   // cover take the tensor cores; the pages that do not have exactly one reader
@@ -1008,8 +1009,23 @@ int attn_paged_mla_bwd(const attn_mla_shape_t* shape, const void* q, const void*
       paged_bwd_params(dev, s.num_seqs, s.num_queries, s.H, 1, s.page_size, s.num_pages, s.max_pages,
                        s.max_queries, block_table, seq_lens, q_offsets, positions, causal, scale);
   const attn::pbwd::Buffers b = attn::pbwd::carve(workspace, lay);
-  e = attn::pbwd::launch_preprocess(static_cast<int>(dtype), s.R, out, dout, lse, b, rows, st);
+  e = attn::pbwd::launch_preprocess(static_cast<int>(dtype), s.R, out, dout, lse, b, rows, st, pp.status);
   if (e == cudaSuccess && (dlatent || dkpos)) e = attn::pbwd::launch_page_index(pp, b, st);
+  // F16/BF16 with R in {256, 512}, Pd in {0, 64} and a page size the 128-key
+  // gathers cover take the tensor cores; the pages that do not have exactly
+  // one reader then go through the fp32 FMA key-major kernel
+  const bool page_ok = s.page_size % 8 == 0 && (128 % s.page_size == 0 || s.page_size % 128 == 0);
+  if (e == cudaSuccess && dtype != ATTN_F32 && (s.R == 256 || s.R == 512) && (s.Pd == 0 || s.Pd == 64) &&
+      page_ok && s.num_pages > 0) {
+    attn::EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail_cuda(cudaErrorNotSupported);
+    e = attn::pbwd::launch_mla_bwd_tc(enc, s.R, s.Pd, dtype == ATTN_BF16, pp, q, qp, latent, kpos, dout, b, dq, dqp,
+                                      dlatent, dkpos, scale, st);
+    if (e == cudaSuccess && (dlatent || dkpos))
+      e = attn::pbwd::launch_mla_dkdv_shared(s.R, s.Pd, static_cast<int>(dtype), pp, q, qp, latent, kpos, dout, b,
+                                             dlatent, dkpos, scale, st);
+    return e == cudaSuccess ? ATTN_OK : fail_cuda(e);
+  }
   if (e == cudaSuccess)
     e = attn::pbwd::launch_mla_bwd(s.R, s.Pd, static_cast<int>(dtype), pp, q, qp, latent, kpos, dout, b, dq, dqp,
                                    dlatent, dkpos, scale, st);

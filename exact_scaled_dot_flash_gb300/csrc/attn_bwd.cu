@@ -71,13 +71,18 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
     lim = L < 0 ? 0 : (L > p.Sk ? p.Sk : L);
   }
   const int diag = p.Sk - p.Sq;
+  // extents (float4 groups, rows, elements) for the bounds-checked build
+  int* const st = p.status;
+  const size_t nq4 = static_cast<size_t>(p.B) * p.Hq * p.Sq * G, nk4 = static_cast<size_t>(p.B) * p.Hkv * p.Sk * G;
+  const int64_t nrows = static_cast<int64_t>(p.B) * p.Hq * p.Sq;
+  const int64_t nbias = static_cast<int64_t>(p.bias_b) * p.bias_h * p.Sq * p.Sk;
 
   float4 kr[GPT], vr[GPT], dka[GPT], dva[GPT];
   const size_t kvrow = (static_cast<size_t>(bhk) * p.Sk + (key_ok ? key : 0)) * G;
 #pragma unroll
   for (int i = 0; i < GPT; ++i) {
-    kr[i] = key_ok ? load4<DT>(k, kvrow + part + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    vr[i] = key_ok ? load4<DT>(v, kvrow + part + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    kr[i] = key_ok ? load4<DT>(k, kvrow + part + 4 * i, nk4, st) : make_float4(0.f, 0.f, 0.f, 0.f);
+    vr[i] = key_ok ? load4<DT>(v, kvrow + part + 4 * i, nk4, st) : make_float4(0.f, 0.f, 0.f, 0.f);
     dka[i] = dva[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   // query rows that can see some key of this CTA (causal: i >= key0 - diag)
@@ -98,11 +103,11 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
         const int r = e / G, c = e - (e / G) * G;
         const bool in = r0 + r < p.Sq;
         const size_t idx = (bh * p.Sq + (in ? r0 + r : 0)) * G + c;
-        qs[r][c] = in ? load4<DT>(q, idx) : make_float4(0.f, 0.f, 0.f, 0.f);
-        gs[r][c] = in ? load4<DT>(dout, idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+        qs[r][c] = in ? load4<DT>(q, idx, nq4, st) : make_float4(0.f, 0.f, 0.f, 0.f);
+        gs[r][c] = in ? load4<DT>(dout, idx, nq4, st) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       if (tid < RT) {
-        const bool in = r0 + tid < p.Sq;
+        const bool in = r0 + tid < p.Sq && in_bounds(st, static_cast<int64_t>(bh * p.Sq + r0 + tid), nrows);
         ls[tid] = in ? lse2[bh * p.Sq + r0 + tid] : -INFINITY;
         dss[tid] = in ? dsum[bh * p.Sq + r0 + tid] : 0.f;
       }
@@ -124,7 +129,8 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
         const bool vis = key_ok && i < p.Sq && key < lim && (!p.causal || key <= i + diag) && l2 != -INFINITY;
         float x = sd * p.scale_log2 - l2;
         if constexpr (BIAS) {
-          if (vis) x = fmaf(__ldg(brow0 + static_cast<size_t>(i) * p.Sk + key), LOG2E, x);
+          const int64_t bi = (brow0 - p.bias) + static_cast<int64_t>(i) * p.Sk + key;
+          if (vis && in_bounds(st, bi, nbias)) x = fmaf(__ldg(p.bias + bi), LOG2E, x);
         }
         const float pr = vis ? fast_exp2(x) : 0.f;
         const float ds = pr * (pd - dss[r]);
@@ -140,8 +146,8 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
 #pragma unroll
   for (int c = 0; c < GPT; ++c) {
     const float4 a = dka[c];
-    store4<DT>(dk, kvrow + part + 4 * c, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
-    store4<DT>(dv, kvrow + part + 4 * c, dva[c]);
+    store4<DT>(dk, kvrow + part + 4 * c, nk4, st, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
+    store4<DT>(dv, kvrow + part + 4 * c, nk4, st, dva[c]);
   }
 }
 
@@ -175,17 +181,23 @@ __global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q,
   const int diag = p.Sk - p.Sq;
   int hi = lim;
   if (p.causal) hi = min(hi, min(q0 + ROWS - 1, p.Sq - 1) + diag + 1);
+  // extents (float4 groups, rows, elements) for the bounds-checked build
+  int* const st = p.status;
+  const size_t nq4 = static_cast<size_t>(p.B) * p.Hq * p.Sq * G, nk4 = static_cast<size_t>(p.B) * p.Hkv * p.Sk * G;
+  const int64_t nrows = static_cast<int64_t>(p.B) * p.Hq * p.Sq;
+  const int64_t nbias = static_cast<int64_t>(p.bias_b) * p.bias_h * p.Sq * p.Sk;
 
   const size_t qrow = (static_cast<size_t>(bh) * p.Sq + (row_ok ? i : 0)) * G;
   float4 qr[GPT], gr[GPT], acc[GPT];
 #pragma unroll
   for (int c = 0; c < GPT; ++c) {
-    qr[c] = row_ok ? load4<DT>(q, qrow + part + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
-    gr[c] = row_ok ? load4<DT>(dout, qrow + part + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    qr[c] = row_ok ? load4<DT>(q, qrow + part + 4 * c, nq4, st) : make_float4(0.f, 0.f, 0.f, 0.f);
+    gr[c] = row_ok ? load4<DT>(dout, qrow + part + 4 * c, nq4, st) : make_float4(0.f, 0.f, 0.f, 0.f);
     acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  const float l2 = row_ok ? lse2[static_cast<size_t>(bh) * p.Sq + i] : -INFINITY;
-  const float dsi = row_ok ? dsum[static_cast<size_t>(bh) * p.Sq + i] : 0.f;
+  const bool stat_ok = row_ok && in_bounds(st, static_cast<int64_t>(bh) * p.Sq + i, nrows);
+  const float l2 = stat_ok ? lse2[static_cast<size_t>(bh) * p.Sq + i] : -INFINITY;
+  const float dsi = stat_ok ? dsum[static_cast<size_t>(bh) * p.Sq + i] : 0.f;
   const float* brow = nullptr;
   if constexpr (BIAS) {
     if (row_ok) {
@@ -203,8 +215,8 @@ __global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q,
       const int r = e / G, c = e - (e / G) * G;
       const bool in = key0 + r < hi;
       const size_t idx = (static_cast<size_t>(bhk) * p.Sk + (in ? key0 + r : 0)) * G + c;
-      ks[r][c] = in ? load4<DT>(k, idx) : make_float4(0.f, 0.f, 0.f, 0.f);
-      vs[r][c] = in ? load4<DT>(v, idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+      ks[r][c] = in ? load4<DT>(k, idx, nk4, st) : make_float4(0.f, 0.f, 0.f, 0.f);
+      vs[r][c] = in ? load4<DT>(v, idx, nk4, st) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
 #pragma unroll 2
@@ -223,7 +235,7 @@ __global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q,
       const bool vis = live && key < lim && key <= causal_lim;
       float x = sd * p.scale_log2 - l2;
       if constexpr (BIAS) {
-        if (vis) x = fmaf(__ldg(brow + key), LOG2E, x);
+        if (vis && in_bounds(st, (brow - p.bias) + key, nbias)) x = fmaf(__ldg(brow + key), LOG2E, x);
       }
       const float pr = vis ? fast_exp2(x) : 0.f;
       const float ds = pr * (pd - dsi);
@@ -235,7 +247,7 @@ __global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q,
 #pragma unroll
   for (int c = 0; c < GPT; ++c) {
     const float4 a = acc[c];
-    store4<DT>(dq, qrow + part + 4 * c, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
+    store4<DT>(dq, qrow + part + 4 * c, nq4, st, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
   }
 }
 
@@ -245,7 +257,7 @@ static cudaError_t launch_d(const KernelParams& p, const void* q, const void* k,
                             float* lse2, void* dq, void* dk, void* dv, float scale,
                             cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Sq;
-  cudaError_t e = launch_bwd_preprocess(D, DT, out, dout, lse, dsum, lse2, rows, st);
+  cudaError_t e = launch_bwd_preprocess(D, DT, out, dout, lse, dsum, lse2, rows, st, p.status);
   if (e != cudaSuccess) return e;
   const dim3 g_kv(static_cast<unsigned>(p.B) * p.Hkv, static_cast<unsigned>((p.Sk + ROWS - 1) / ROWS));
   const dim3 g_q(static_cast<unsigned>(p.B) * p.Hq, static_cast<unsigned>((p.Sq + ROWS - 1) / ROWS));
@@ -279,10 +291,10 @@ static cudaError_t launch_dt(int D, const KernelParams& p, const void* q, const 
 // statistics kernel: rows of D elements, 16-byte loads, D_i = 0 for a row
 // with no visible key).
 cudaError_t launch_bwd_preprocess(int D, int dtype, const void* out, const void* dout, const float* lse,
-                                  float* dsum, float* lse2, int64_t rows, cudaStream_t st) {
+                                  float* dsum, float* lse2, int64_t rows, cudaStream_t st, int* status) {
   if (!(D == 16 || D == 32 || D == 64 || D == 128)) return cudaErrorInvalidValue;
   const pbwd::Buffers b{dsum, lse2, nullptr, nullptr, nullptr, nullptr};
-  return pbwd::launch_preprocess(dtype, D, out, dout, lse, b, rows, st);
+  return pbwd::launch_preprocess(dtype, D, out, dout, lse, b, rows, st, status);
 }
 
 cudaError_t launch_bwd_simt(int D, int dtype, const KernelParams& p, const void* q, const void* k,

@@ -329,10 +329,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // lse2 and D of this warpgroup's 64 query rows: lane l holds rows l and
       // l + 32 (coalesced loads, issued before the wait), shuffled out below
       const int ia = i0 + lane, ib = i0 + 32 + lane;
-      const float l2a = ia < p.Sq ? __ldg(a.lse2 + bhq * p.Sq + ia) : -INFINITY;
-      const float l2b = ib < p.Sq ? __ldg(a.lse2 + bhq * p.Sq + ib) : -INFINITY;
-      const float dsa = ia < p.Sq ? __ldg(a.dsum + bhq * p.Sq + ia) : 0.f;
-      const float dsb = ib < p.Sq ? __ldg(a.dsum + bhq * p.Sq + ib) : 0.f;
+      const int64_t nrows = static_cast<int64_t>(p.B) * p.Hq * p.Sq;  // extents for the checked build
+      const bool oka = ia < p.Sq && in_bounds(p.status, static_cast<int64_t>(bhq) * p.Sq + ia, nrows);
+      const bool okb = ib < p.Sq && in_bounds(p.status, static_cast<int64_t>(bhq) * p.Sq + ib, nrows);
+      const float l2a = oka ? __ldg(a.lse2 + bhq * p.Sq + ia) : -INFINITY;
+      const float l2b = okb ? __ldg(a.lse2 + bhq * p.Sq + ib) : -INFINITY;
+      const float dsa = oka ? __ldg(a.dsum + bhq * p.Sq + ia) : 0.f;
+      const float dsb = okb ? __ldg(a.dsum + bhq * p.Sq + ib) : 0.f;
       float x[64];
       const bool ok = mbar_wait(bar(C::BAR_S), it & 1);
       if (__any_sync(0xffffffffu, !ok)) { failed = true; break; }
@@ -346,7 +349,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool vis = key_vis && (!p.causal || key <= i + diag) && l2 != -INFINITY;
         float s2 = x[c] * sc - l2;
         if constexpr (BIAS) {
-          if (vis) s2 = fmaf(__ldg(bcol + static_cast<size_t>(i) * p.Sk), LOG2E, s2);
+          const int64_t bi = (bcol - p.bias) + static_cast<int64_t>(i) * p.Sk;
+          if (vis && in_bounds(p.status, bi, static_cast<int64_t>(p.bias_b) * p.bias_h * p.Sq * p.Sk))
+            s2 = fmaf(__ldg(p.bias + bi), LOG2E, s2);
         }
         x[c] = vis ? fast_exp2(s2) : 0.f;
       }
@@ -385,6 +390,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         void* dst = half == 0 ? a.dk : a.dv;
         const float mul = half == 0 ? a.scale : 1.f;
         uint8_t* rowp = static_cast<uint8_t*>(dst) + (static_cast<size_t>(bhk) * p.Sk + key) * D * 2;
+        const bool row_in = key < p.Sk && range_in_bounds(p.status, (static_cast<int64_t>(bhk) * p.Sk + key) * D, D,
+                                                          static_cast<int64_t>(p.B) * p.Hkv * p.Sk * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float v[32];
@@ -398,7 +405,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = 0.f;
           }
-          if (key < p.Sk) store_row16<BF16, 32>(rowp + c * 64, v, mul);
+          if (row_in) store_row16<BF16, 32>(rowp + c * 64, v, mul);
         }
       }
     }
@@ -601,8 +608,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const bool row_ok = i < p.Sq;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
     const size_t ri = static_cast<size_t>(bh) * p.Sq + i;
-    const float l2 = row_ok ? __ldg(a.lse2 + ri) : -INFINITY;
-    const float dsi = row_ok ? __ldg(a.dsum + ri) : 0.f;
+    const int64_t nrows = static_cast<int64_t>(p.B) * p.Hq * p.Sq;  // extent for the checked build
+    const bool stat_ok = row_ok && in_bounds(p.status, static_cast<int64_t>(ri), nrows);
+    const float l2 = stat_ok ? __ldg(a.lse2 + ri) : -INFINITY;
+    const float dsi = stat_ok ? __ldg(a.dsum + ri) : 0.f;
     const bool live = row_ok && l2 != -INFINITY;
     const int causal_lim = p.causal ? i + diag : 0x7fffffff;
     const float sc = p.scale_log2;
@@ -628,7 +637,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool vis = live && key < lim && key <= causal_lim;
         float s2 = x[c] * sc - l2;
         if constexpr (BIAS) {
-          if (vis) s2 = fmaf(__ldg(brow + key), LOG2E, s2);
+          if (vis && in_bounds(p.status, (brow - p.bias) + key,
+                               static_cast<int64_t>(p.bias_b) * p.bias_h * p.Sq * p.Sk))
+            s2 = fmaf(__ldg(brow + key), LOG2E, s2);
         }
         x[c] = vis ? fast_exp2(s2) : 0.f;
       }
@@ -656,6 +667,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (ok) {
         tc_fence_after();
         uint8_t* rowp = static_cast<uint8_t*>(a.dq) + (ri * D + half * (D / 2)) * 2;
+        const bool row_in = row_ok && range_in_bounds(p.status, static_cast<int64_t>(ri) * D + half * (D / 2), D / 2,
+                                                      nrows * D);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           float v[32];
@@ -669,7 +682,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = 0.f;
           }
-          if (row_ok) store_row16<BF16, 32>(rowp + c * 64, v, a.scale);
+          if (row_in) store_row16<BF16, 32>(rowp + c * 64, v, a.scale);
         }
       }
     }

@@ -144,15 +144,18 @@ __global__ void __launch_bounds__(THREADS)
     }
   }
   if (!row_ok) return;
+  const int64_t nrows = static_cast<int64_t>(p.B) * p.Hq * p.Sq;  // extent for the checked build
   if (p.num_splits > 1) {
     // partial result: accumulator relative to 2^m_run, and (m_run, l_run)
     const size_t r = (static_cast<size_t>(blockIdx.z) * p.B * p.Hq + bh) * p.Sq + row_g;
+    if (!in_bounds(p.status, static_cast<int64_t>(r), p.num_splits * nrows)) return;
     float4* wrow = reinterpret_cast<float4*>(p.ws_o + r * D);
 #pragma unroll
     for (int i = 0; i < GPT; ++i) wrow[part + 4 * i] = acc[i];
     if (part == 0) p.ws_ml[r] = make_float2(m_run, l_run);
     return;
   }
+  if (!in_bounds(p.status, static_cast<int64_t>(bh) * p.Sq + row_g, nrows)) return;
   if (p.lse != nullptr && part == 0)
     p.lse[static_cast<size_t>(bh) * p.Sq + row_g] =
         l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;

@@ -65,7 +65,12 @@ __global__ void __launch_bounds__(THREADS) mla_fwd_kernel(const void* __restrict
   const bool row_ok = tq < nq;
   const int t = q_lo + (row_ok ? tq : 0);
   const int L = min(max(__ldg(pp.seq_lens + s), 0), pp.max_pages * pp.page_size);
-  const int pos = pp.positions ? __ldg(pp.positions + t) : L - nq + tq;
+  // extents (float4 groups, rows, entries) for the bounds-checked build
+  int* const st = pp.status;
+  const int64_t nrows = static_cast<int64_t>(pp.num_queries) * H;
+  const size_t ntok = static_cast<size_t>(pp.num_pages) * pp.page_size;
+  const int64_t ntab = static_cast<int64_t>(pp.num_seqs) * pp.max_pages;
+  const int pos = pp.positions ? (in_bounds(st, t, pp.num_queries) ? __ldg(pp.positions + t) : -1) : L - nq + tq;
   const int key_hi_row = pp.causal ? min(L, pos + 1) : L;
   int key_hi = L;
   if (pp.causal && !pp.positions) {
@@ -77,14 +82,14 @@ __global__ void __launch_bounds__(THREADS) mla_fwd_kernel(const void* __restrict
   float4 qr[GRT], acc[GRT];
 #pragma unroll
   for (int i = 0; i < GRT; ++i) {
-    qr[i] = row_ok ? load4<DT>(q, row * GR + part + TPR * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    qr[i] = row_ok ? load4<DT>(q, row * GR + part + TPR * i, nrows * GR, st) : make_float4(0.f, 0.f, 0.f, 0.f);
     acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float4 qpr[GPT > 0 ? GPT : 1];
 #pragma unroll
   for (int i = 0; i < GPT; ++i) {
     const int g = part + TPR * i;
-    qpr[i] = (row_ok && g < GP) ? load4<DT>(qp, row * GP + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+    qpr[i] = (row_ok && g < GP) ? load4<DT>(qp, row * GP + g, nrows * GP, st) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const int32_t* table = pp.block_table + static_cast<size_t>(s) * pp.max_pages;
   float m_run = -INFINITY, l_run = 0.f;
@@ -94,15 +99,18 @@ __global__ void __launch_bounds__(THREADS) mla_fwd_kernel(const void* __restrict
       const int kr = e / (GR + GP), c = e - kr * (GR + GP);
       const int j = key0 + kr;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (j < key_hi) {
+      if (j < key_hi && in_bounds(st, static_cast<int64_t>(s) * pp.max_pages + j / pp.page_size, ntab)) {
         const int page = __ldg(table + j / pp.page_size);
         if (page >= 0 && page < pp.num_pages) {
           const size_t tok = static_cast<size_t>(page) * pp.page_size + j % pp.page_size;
-          v = c < GR ? load4<DT>(lat, tok * GR + c) : load4<DT>(kpos, tok * GP + (c - GR));
+          v = c < GR ? load4<DT>(lat, tok * GR + c, ntok * GR, st) : load4<DT>(kpos, tok * GP + (c - GR), ntok * GP, st);
         }
       }
-      if (c < GR) cs[kr][c] = v;
-      else ps[kr][c - GR] = v;
+      if (c < GR) {
+        if (in_bounds(st, kr * GR + c, KT * GR)) cs[kr][c] = v;
+      } else if (in_bounds(st, kr * GP + c - GR, KT * GP)) {
+        ps[kr][c - GR] = v;
+      }
     }
     __syncthreads();
     float sreg[KT];
@@ -146,9 +154,10 @@ __global__ void __launch_bounds__(THREADS) mla_fwd_kernel(const void* __restrict
 #pragma unroll
   for (int i = 0; i < GRT; ++i) {
     const float4 a = acc[i];
-    store4<DT>(out, row * GR + part + TPR * i, make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
+    store4<DT>(out, row * GR + part + TPR * i, nrows * GR, st, make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
   }
-  if (lse && part == 0) lse[row] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+  if (lse && part == 0 && in_bounds(st, static_cast<int64_t>(row), nrows))
+    lse[row] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
 }
 
 template <int R, int PD>

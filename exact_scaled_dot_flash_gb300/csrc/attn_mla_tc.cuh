@@ -158,8 +158,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (w.n == 0) {  // no key tile in this run (CTA-uniform): the rows see no key here
     if (warp < 4) {
       const int r = warp * 32 + lane;
-      if (w.row0 + r < rows_seq) {
-        const int64_t grow = grow0 + r;
+      const int64_t grow = grow0 + r;
+      if (w.row0 + r < rows_seq && in_bounds(pp.status, grow, rows_total)) {
         if (partial) {
           if (w.h == 0) pp.ws_ml[w.sp * rows_total + grow] = make_float2(-INFINITY, 0.f);
         } else {
@@ -236,6 +236,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int pidx = key / P;
           const int page = pidx < pp.max_pages ? __ldg(table + pidx) : -1;  // -1: zero-filled box
           const int y = key - pidx * P;
+          // checked build: the box lands inside its chunk of the ring stage (a
+          // skipped copy leaves the stage's barrier to time out)
+          if (!range_in_bounds(pp.status, b * box_rows, box_rows, BN)) continue;
           for (int c = 0; c < C::NCH; ++c) {
             const uint32_t dst = base + c * C::KCH_BYTES + b * box_rows * 128;
             if (c < C::NCH_LAT) tma_load_3d(dst, &tm_lat, bar(C::BAR_FULL + st), c * 64, y, page);
@@ -310,7 +313,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tP = tmem + lane_off + COL_P;
     const uint32_t tO = tmem + lane_off + COL_O;
     const int tq = (w.row0 + r) / H;
-    const int pos = !row_ok ? -1 : (pp.positions ? __ldg(pp.positions + w.q_lo + tq) : w.L - w.nq + tq);
+    const int pos = !row_ok ? -1
+                            : (pp.positions ? (in_bounds(pp.status, w.q_lo + tq, pp.num_queries)
+                                                   ? __ldg(pp.positions + w.q_lo + tq) : -1)
+                                            : w.L - w.nq + tq);
     const int causal_lim = pp.causal ? pos : 0x7fffffff;
     const int key_lim = w.L;
     const float sc = pp.scale_log2;
@@ -431,6 +437,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
       tc_fence_after();
       const bool live = l_run > 0.f;
+      const bool row_in = row_ok && in_bounds(pp.status, grow, rows_total);  // checked build
       if (partial) {
         float4* dst = reinterpret_cast<float4*>(pp.ws_o + (w.sp * rows_total + grow) * R + w.h * OC);
 #pragma unroll 1
@@ -438,14 +445,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t o[32];
           tmem_ld32(tO + 32 * c, o);
           tmem_wait_ld();
-          if (row_ok) {
+          if (row_in) {
 #pragma unroll
             for (int u = 0; u < 8; ++u)
               dst[c * 8 + u] = make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]),
                                            __uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3]));
           }
         }
-        if (row_ok && w.h == 0)
+        if (row_in && w.h == 0)
           pp.ws_ml[w.sp * rows_total + grow] = make_float2(live ? m_run : -INFINITY, live ? l_run : 0.f);
       } else {
         const float inv = live ? 1.f / l_run : __int_as_float(0x7fc00000);
@@ -455,7 +462,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t o[32];
           tmem_ld32(tO + 32 * c, o);
           tmem_wait_ld();
-          if (row_ok) {
+          if (row_in) {
             uint32_t pkd[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
@@ -468,7 +475,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               dst[c * 4 + u] = make_uint4(pkd[4 * u], pkd[4 * u + 1], pkd[4 * u + 2], pkd[4 * u + 3]);
           }
         }
-        if (row_ok && lse && w.h == 0) lse[grow] = live ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+        if (row_in && lse && w.h == 0) lse[grow] = live ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
       }
     }
   }

@@ -62,7 +62,11 @@ __global__ void __launch_bounds__(THREADS) paged_fwd_kernel(const void* __restri
   const bool row_ok = tq < nq;
   const int t = q_lo + (row_ok ? tq : 0);
   const int L = min(max(__ldg(pp.seq_lens + s), 0), pp.max_pages * pp.page_size);
-  const int pos = pp.positions ? __ldg(pp.positions + t) : L - nq + tq;
+  // extents (float4 groups, rows) for the bounds-checked build
+  int* const st = pp.status;
+  const size_t nq4 = static_cast<size_t>(pp.num_queries) * pp.Hq * G;
+  const size_t nk4 = static_cast<size_t>(pp.num_pages) * pp.page_size * pp.Hkv * G;
+  const int pos = pp.positions ? (in_bounds(st, t, pp.num_queries) ? __ldg(pp.positions + t) : -1) : L - nq + tq;
   const int key_hi_row = pp.causal ? min(L, pos + 1) : L;  // keys [0, key_hi_row) are visible to this row
   // keys any row of this CTA may see
   int key_hi = L;
@@ -75,10 +79,11 @@ __global__ void __launch_bounds__(THREADS) paged_fwd_kernel(const void* __restri
   float4 qr[GPT], acc[GPT];
 #pragma unroll
   for (int i = 0; i < GPT; ++i) {
-    qr[i] = row_ok ? load4<DT>(q, qrow + part + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    qr[i] = row_ok ? load4<DT>(q, qrow + part + 4 * i, nq4, st) : make_float4(0.f, 0.f, 0.f, 0.f);
     acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const int32_t* table = pp.block_table + static_cast<size_t>(s) * pp.max_pages;
+  const int64_t ntab = static_cast<int64_t>(pp.num_seqs) * pp.max_pages;
   float m_run = -INFINITY, l_run = 0.f;
   for (int key0 = 0; key0 < key_hi; key0 += KT) {
     __syncthreads();
@@ -86,16 +91,18 @@ __global__ void __launch_bounds__(THREADS) paged_fwd_kernel(const void* __restri
       const int kr = e / G, c = e - (e / G) * G;
       const int j = key0 + kr;
       float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-      if (j < key_hi) {
+      if (j < key_hi && in_bounds(st, static_cast<int64_t>(s) * pp.max_pages + j / pp.page_size, ntab)) {
         const int page = __ldg(table + j / pp.page_size);
         if (page >= 0 && page < pp.num_pages) {
           const size_t idx = ((static_cast<size_t>(page) * pp.page_size + j % pp.page_size) * pp.Hkv + hk) * G + c;
-          kv = load4<DT>(kc, idx);
-          vv = load4<DT>(vc, idx);
+          kv = load4<DT>(kc, idx, nk4, st);
+          vv = load4<DT>(vc, idx, nk4, st);
         }
       }
-      ks[kr][c] = kv;
-      vs[kr][c] = vv;
+      if (in_bounds(st, kr * G + c, KT * G)) {
+        ks[kr][c] = kv;
+        vs[kr][c] = vv;
+      }
     }
     __syncthreads();
     float sreg[KT];
@@ -136,9 +143,9 @@ __global__ void __launch_bounds__(THREADS) paged_fwd_kernel(const void* __restri
 #pragma unroll
   for (int i = 0; i < GPT; ++i) {
     const float4 a = acc[i];
-    store4<DT>(out, qrow + part + 4 * i, make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
+    store4<DT>(out, qrow + part + 4 * i, nq4, st, make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
   }
-  if (lse && part == 0)
+  if (lse && part == 0 && in_bounds(st, static_cast<int64_t>(t) * pp.Hq + h, static_cast<int64_t>(pp.num_queries) * pp.Hq))
     lse[static_cast<size_t>(t) * pp.Hq + h] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
 }
 
@@ -182,13 +189,21 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) paged_decode_kernel(const void
   const int R = min(nq * group, RMAX);
   if (R <= 0) return;
   const int L = min(max(__ldg(pp.seq_lens + s), 0), pp.max_pages * pp.page_size);
+  // extents (float4 groups, rows, entries) for the bounds-checked build
+  int* const st = pp.status;
+  const int64_t nrows = static_cast<int64_t>(pp.num_queries) * pp.Hq;
+  const size_t nq4 = static_cast<size_t>(nrows) * G;
+  const size_t nk4 = static_cast<size_t>(pp.num_pages) * pp.page_size * pp.Hkv * G;
+  const int64_t ntab = static_cast<int64_t>(pp.num_seqs) * pp.max_pages;
   // rows' positions and the CTA's key range
   int pos[RMAX];
   int key_hi = 0;
 #pragma unroll
   for (int r = 0; r < RMAX; ++r) {
     const int tq = r / group;
-    pos[r] = r < R ? (pp.positions ? __ldg(pp.positions + q_lo + tq) : L - nq + tq) : -1;
+    pos[r] = r < R ? (pp.positions ? (in_bounds(st, q_lo + tq, pp.num_queries) ? __ldg(pp.positions + q_lo + tq) : -1)
+                                   : L - nq + tq)
+                   : -1;
     if (r < R) key_hi = max(key_hi, pp.causal ? min(L, pos[r] + 1) : L);
   }
   for (int e = threadIdx.x; e < RMAX * G; e += DEC_WARPS * 32) {
@@ -196,9 +211,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) paged_decode_kernel(const void
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (r < R) {
       const int t = q_lo + r / group, h = hk * group + r % group;
-      v = load4<DT>(q, (static_cast<size_t>(t) * pp.Hq + h) * G + c);
+      v = load4<DT>(q, (static_cast<size_t>(t) * pp.Hq + h) * G + c, nq4, st);
     }
-    qs[r][c] = v;
+    if (in_bounds(st, r * G + c, RMAX * G)) qs[r][c] = v;
   }
   __syncthreads();
 
@@ -218,7 +233,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) paged_decode_kernel(const void
   for (int c = c_lo + warp; c < c_hi; c += DEC_WARPS) {
     const int j = c * 32 + lane;
     const bool in = j < key_hi;
-    int page = in ? __ldg(table + j / pp.page_size) : -1;
+    int page = (in && in_bounds(st, static_cast<int64_t>(s) * pp.max_pages + j / pp.page_size, ntab))
+                   ? __ldg(table + j / pp.page_size) : -1;
     const bool ok = in && page >= 0 && page < pp.num_pages;
     const size_t krow = ok ? ((static_cast<size_t>(page) * pp.page_size + j % pp.page_size) * pp.Hkv + hk) * G : 0;
     // scores of this lane's key against every row
@@ -229,7 +245,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) paged_decode_kernel(const void
 #pragma unroll 4
       for (int g2 = 0; g2 < G / 2; ++g2) {
         float4 k0, k1;
-        simt::load8<DT>(kc, krow / 2 + g2, k0, k1);
+        simt::load8<DT>(kc, krow / 2 + g2, nk4 / 2, st, k0, k1);
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) sc[r] = dot4(qs[r][2 * g2 + 1], k1, dot4(qs[r][2 * g2], k0, sc[r]));
       }
@@ -270,7 +286,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) paged_decode_kernel(const void
 #pragma unroll
         for (int i = 0; i < LG; ++i) {
           const int g = lane + 32 * i;
-          vv[b][i] = (use && g < G) ? load4<DT>(vc, vrow + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+          vv[b][i] = (use && g < G) ? load4<DT>(vc, vrow + g, nk4, st) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
 #pragma unroll
@@ -316,13 +332,15 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) paged_decode_kernel(const void
     const size_t row = static_cast<size_t>(t) * pp.Hq + h;
     if (pp.num_splits > 1) {  // partial of this split, relative to 2^M
       const size_t rr = static_cast<size_t>(blockIdx.y) * pp.num_queries * pp.Hq + row;
+      if (!in_bounds(st, static_cast<int64_t>(rr), pp.num_splits * nrows)) continue;
       reinterpret_cast<float4*>(pp.ws_o)[rr * G + g] = o;
       if (g == 0) pp.ws_ml[rr] = make_float2(M, Ls);
       continue;
     }
     const float inv = Ls > 0.f ? 1.f / Ls : __int_as_float(0x7fc00000);
-    store4<DT>(out, row * G + g, make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv));
-    if (lse && g == 0) lse[row] = Ls > 0.f ? (M + log2f(Ls)) * LN2 : -INFINITY;
+    store4<DT>(out, row * G + g, nq4, st, make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv));
+    if (lse && g == 0 && in_bounds(st, static_cast<int64_t>(row), nrows))
+      lse[row] = Ls > 0.f ? (M + log2f(Ls)) * LN2 : -INFINITY;
   }
 }
 

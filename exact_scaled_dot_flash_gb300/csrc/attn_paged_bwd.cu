@@ -29,7 +29,7 @@ int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 template <int DT>
 __global__ void __launch_bounds__(256) preprocess_kernel(const void* out, const void* dout, const float* lse,
                                                          float* dsum, float* lse2, int64_t rows, int groups8,
-                                                         int tpr_log2) {
+                                                         int tpr_log2, int* status) {
   const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> tpr_log2;
   const int tpr = 1 << tpr_log2;
   const int sub = threadIdx.x & (tpr - 1);
@@ -37,8 +37,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const void* out, const 
   if (r < rows) {
     for (int g = sub; g < groups8; g += tpr) {
       float4 a0, a1, b0, b1;
-      simt::load8<DT>(out, r * groups8 + g, a0, a1);
-      simt::load8<DT>(dout, r * groups8 + g, b0, b1);
+      simt::load8<DT>(out, r * groups8 + g, rows * groups8, status, a0, a1);
+      simt::load8<DT>(dout, r * groups8 + g, rows * groups8, status, b0, b1);
       acc = simt::dot4(a1, b1, simt::dot4(a0, b0, acc));
     }
   }
@@ -64,7 +64,7 @@ __global__ void count_kernel(const PagedParams pp, int* count) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(pp.num_seqs) * pp.max_pages) return;
   const int pg = live_page(pp, e);
-  if (pg >= 0) atomicAdd(count + pg, 1);
+  if (pg >= 0 && in_bounds(pp.status, pg, pp.num_pages)) atomicAdd(count + pg, 1);
 }
 
 // offsets[p] = sum of count[0..p), offsets[n] = the total; one CTA.
@@ -120,18 +120,24 @@ __global__ void fill_kernel(const PagedParams pp, int* count, const int* offsets
   if (e >= static_cast<int64_t>(pp.num_seqs) * pp.max_pages) return;
   const int pg = live_page(pp, e);
   if (pg < 0) return;
+  if (!in_bounds(pp.status, pg, pp.num_pages)) return;
   const int c = atomicSub(count + pg, 1);
-  refs[offsets[pg + 1] - c] = static_cast<int>(e);
+  const int slot = offsets[pg + 1] - c;  // inside [offsets[pg], offsets[pg + 1])
+  if (in_bounds(pp.status, slot, static_cast<int64_t>(pp.num_seqs) * pp.max_pages)) refs[slot] = static_cast<int>(e);
 }
 
 // Insertion sort of every page's segment (segments are short: one entry per
 // sequence or block that reads the page); pages whose reader count is not one
 // join the list (in any order: each is computed on its own).
-__global__ void sort_kernel(const int* offsets, int* refs, int* list, int pages) {
+__global__ void sort_kernel(const int* offsets, int* refs, int* list, int pages, int64_t nrefs, int* status) {
   const int p = blockIdx.x * blockDim.x + threadIdx.x;
   if (p >= pages) return;
   const int lo = offsets[p], hi = offsets[p + 1];
-  if (hi - lo != 1) list[1 + atomicAdd(list, 1)] = p;
+  if (!range_in_bounds(status, lo, hi - lo, nrefs)) return;
+  if (hi - lo != 1) {
+    const int li = 1 + atomicAdd(list, 1);
+    if (in_bounds(status, li, static_cast<int64_t>(pages) + 1)) list[li] = p;
+  }
   for (int i = lo + 1; i < hi; ++i) {
     const int x = refs[i];
     int j = i - 1;
@@ -165,7 +171,7 @@ Buffers carve(void* workspace, const Layout& lay) {
 }
 
 cudaError_t launch_preprocess(int dtype, int width, const void* out, const void* dout, const float* lse,
-                              const Buffers& b, int64_t rows, cudaStream_t st) {
+                              const Buffers& b, int64_t rows, cudaStream_t st, int* status) {
   const int groups8 = width / 8;  // widths are multiples of 16
   int tpr_log2 = 0;
   while ((2 << tpr_log2) <= groups8 && (2 << tpr_log2) <= 32) ++tpr_log2;
@@ -174,11 +180,11 @@ cudaError_t launch_preprocess(int dtype, int width, const void* out, const void*
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const unsigned nb = static_cast<unsigned>(blocks);
   if (dtype == 0)
-    preprocess_kernel<0><<<nb, 256, 0, st>>>(out, dout, lse, b.dsum, b.lse2, rows, groups8, tpr_log2);
+    preprocess_kernel<0><<<nb, 256, 0, st>>>(out, dout, lse, b.dsum, b.lse2, rows, groups8, tpr_log2, status);
   else if (dtype == 1)
-    preprocess_kernel<1><<<nb, 256, 0, st>>>(out, dout, lse, b.dsum, b.lse2, rows, groups8, tpr_log2);
+    preprocess_kernel<1><<<nb, 256, 0, st>>>(out, dout, lse, b.dsum, b.lse2, rows, groups8, tpr_log2, status);
   else
-    preprocess_kernel<2><<<nb, 256, 0, st>>>(out, dout, lse, b.dsum, b.lse2, rows, groups8, tpr_log2);
+    preprocess_kernel<2><<<nb, 256, 0, st>>>(out, dout, lse, b.dsum, b.lse2, rows, groups8, tpr_log2, status);
   return cudaGetLastError();
 }
 
@@ -193,7 +199,7 @@ cudaError_t launch_page_index(const PagedParams& pp, const Buffers& b, cudaStrea
   scan_kernel<<<1, 1024, 0, st>>>(b.count, b.offsets, pp.num_pages);
   if (eb > 0) fill_kernel<<<eb, 256, 0, st>>>(pp, b.count, b.offsets, b.refs);
   sort_kernel<<<static_cast<unsigned>((pp.num_pages + 255) / 256), 256, 0, st>>>(b.offsets, b.refs, b.list,
-                                                                                  pp.num_pages);
+                                                                                  pp.num_pages, entries, pp.status);
   return cudaGetLastError();
 }
 

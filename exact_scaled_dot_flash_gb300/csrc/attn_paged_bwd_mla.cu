@@ -50,5 +50,23 @@ cudaError_t launch_mla_bwd(int R, int Pd, int dtype, const PagedParams& pp, cons
   }
 }
 
+cudaError_t launch_mla_dkdv_shared(int R, int Pd, int dtype, const PagedParams& pp, const void* q, const void* qp,
+                                   const void* lat, const void* kp, const void* dout, const Buffers& b, void* dlat,
+                                   void* dkp, float scale, cudaStream_t st) {
+#define ATTN_MLA_SHARED(RR, PP, TT)                                                                                \
+  launch_instance<RR, PP, RR / 32, TT, true>(pp, q, qp, lat, kp, lat, dout, b, nullptr, nullptr, dlat, dkp, nullptr, \
+                                             scale, st, true)
+#define ATTN_MLA_SHARED_P(RR)                                                                  \
+  if (Pd == 0) return dtype == 1 ? ATTN_MLA_SHARED(RR, 0, 1) : ATTN_MLA_SHARED(RR, 0, 2);     \
+  if (Pd == 64) return dtype == 1 ? ATTN_MLA_SHARED(RR, 64, 1) : ATTN_MLA_SHARED(RR, 64, 2); \
+  return cudaErrorInvalidValue;
+  if (dtype != 1 && dtype != 2) return cudaErrorInvalidValue;
+  if (R == 256) { ATTN_MLA_SHARED_P(256) }
+  if (R == 512) { ATTN_MLA_SHARED_P(512) }
+  return cudaErrorInvalidValue;
+#undef ATTN_MLA_SHARED_P
+#undef ATTN_MLA_SHARED
+}
+
 }  // namespace pbwd
 }  // namespace attn

@@ -84,6 +84,9 @@ __device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap* m,
     const int key = key0 + i * box_rows;
     const int pidx = key / pp.page_size;
     const int page = pidx < pp.max_pages ? __ldg(table + pidx) : -1;  // -1: a zero-filled box
+    // checked build: the box lands inside its chunk of the tile (a skipped
+    // copy leaves the tile's barrier to time out)
+    if (!range_in_bounds(pp.status, i * box_rows, box_rows, BR)) continue;
     for (int c = 0; c < C::NCHUNK; ++c)
       tma_load_4d(dst + c * C::CHUNK_BYTES + i * box_rows * 128, m, bar, c * C::BOX_D, hk, key % pp.page_size,
                   page);
@@ -272,12 +275,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int pair = t * BR + 64 * half + 32 * u + lane;
         const int qi = pair / gp;
         const int hq = hk * group + hb * gp + (pair - qi * gp);
-        const bool in = qi < n;
-        const size_t ri = static_cast<size_t>(q0 + (in ? qi : 0)) * pp.Hq + hq;
+        const size_t ri = static_cast<size_t>(q0 + (qi < n ? qi : 0)) * pp.Hq + hq;
+        const bool in = qi < n && in_bounds(pp.status, static_cast<int64_t>(ri),
+                                            static_cast<int64_t>(pp.num_queries) * pp.Hq);
         l2v[u] = in ? __ldg(a.lse2 + ri) : -INFINITY;
         dsv[u] = in ? __ldg(a.dsum + ri) : 0.f;
         limv[u] = 0x7ffffffe;
-        if (pp.causal) limv[u] = dflt ? diag + qi : (in ? min(__ldg(pp.positions + q0 + qi), 0x7ffffffe) : -1);
+        if (pp.causal)
+          limv[u] = dflt ? diag + qi
+                         : ((in && in_bounds(pp.status, q0 + qi, pp.num_queries))
+                                ? min(__ldg(pp.positions + q0 + qi), 0x7ffffffe) : -1);
       }
     };
     if (N > 0) load_stats(0);
@@ -341,8 +348,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (__any_sync(0xffffffffu, !ok)) { ok = false; if (lane == 0) fail(); }
       }
       const int pidx = key / P;
-      int page = pidx < used ? __ldg(table + pidx) : -1;
+      int page = (pidx < used && in_bounds(pp.status, static_cast<int64_t>(s) * pp.max_pages + pidx,
+                                           static_cast<int64_t>(pp.num_seqs) * pp.max_pages))
+                     ? __ldg(table + pidx) : -1;
       if (page >= pp.num_pages || (page >= 0 && __ldg(a.offsets + page + 1) - __ldg(a.offsets + page) != 1))
+        page = -1;
+      // the key row in the cache gradient: [pages, page_size, Hkv, D]
+      const int64_t crow = ((static_cast<int64_t>(page < 0 ? 0 : page) * P + key % P) * pp.Hkv + hk) * D;
+      if (page >= 0 && !range_in_bounds(pp.status, crow, D, static_cast<int64_t>(pp.num_pages) * P * pp.Hkv * D))
         page = -1;
       void* dst = half == 0 ? a.dk : a.dv;
       if (ok) {
@@ -542,10 +555,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const bool row_ok = qi < n;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
     const size_t ri = static_cast<size_t>(q0 + (row_ok ? qi : 0)) * pp.Hq + hq;
-    const float l2 = row_ok ? __ldg(a.lse2 + ri) : -INFINITY;
+    const int64_t nrows = static_cast<int64_t>(pp.num_queries) * pp.Hq;  // extent for the checked build
+    const bool stat_ok = row_ok && in_bounds(pp.status, static_cast<int64_t>(ri), nrows);
+    const float l2 = stat_ok ? __ldg(a.lse2 + ri) : -INFINITY;
     const bool live = l2 != -INFINITY;
     const float dsi = live ? __ldg(a.dsum + ri) : 0.f;
-    const int pos = row_ok ? (dflt ? diag + qi : __ldg(pp.positions + q0 + qi)) : -1;
+    const int pos = row_ok ? (dflt ? diag + qi
+                                   : (in_bounds(pp.status, q0 + qi, pp.num_queries) ? __ldg(pp.positions + q0 + qi)
+                                                                                    : -1))
+                           : -1;
     const int causal_lim = pp.causal ? pos : 0x7fffffff;
     const float sc = pp.scale_log2;
     bool failed = false;
@@ -586,6 +604,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (ok) {
         tc_fence_after();
         uint8_t* rowp = static_cast<uint8_t*>(a.dq) + (ri * D + half * (D / 2)) * 2;
+        const bool row_in =
+            stat_ok && range_in_bounds(pp.status, static_cast<int64_t>(ri) * D + half * (D / 2), D / 2, nrows * D);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           float v[32];
@@ -599,7 +619,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = 0.f;
           }
-          if (row_ok) store_row16<BF16, 32>(rowp + c * 64, v, a.scale);
+          if (row_in) store_row16<BF16, 32>(rowp + c * 64, v, a.scale);
         }
       }
     }

@@ -210,6 +210,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int key = j * BN + i * box_rows;
             const int pidx = key / pp.page_size;
             const int page = pidx < pp.max_pages ? __ldg(table + pidx) : -1;  // -1: zero-filled box
+            // checked build: the box lands inside its chunk of the ring slot (a
+            // skipped copy leaves the slot's barrier to time out)
+            if (!range_in_bounds(pp.status, i * box_rows, box_rows, BN)) continue;
             for (int c = 0; c < C::NCHUNK; ++c)
               tma_load_4d(sb + C::OFF_KV + st * C::TILE_BYTES + c * C::CHUNK_BYTES + i * box_rows * 128, m,
                           bar(C::BAR_FULL + st), c * C::BOX_D, w.hk, key % pp.page_size, page);
@@ -302,7 +305,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int n_t = t ? w.n[1] : w.n[0];
     const int nfull_t = t ? w.nfull[1] : w.nfull[0];
     const float sc = pp.scale_log2;
-    const int pos = !row_ok ? -1 : (pp.positions ? __ldg(pp.positions + w.q_lo + tq) : w.L - w.nq + tq);
+    const int pos = !row_ok ? -1
+                            : (pp.positions ? (in_bounds(pp.status, w.q_lo + tq, pp.num_queries)
+                                                   ? __ldg(pp.positions + w.q_lo + tq) : -1)
+                                            : w.L - w.nq + tq);
     const int causal_lim = pp.causal ? pos : 0x7fffffff;
     const int key_lim = w.L;
     float m_run = -INFINITY, l_run = 0.f;
@@ -399,16 +405,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const bool live = have && l_run > 0.f;
       const size_t orow = static_cast<size_t>(w.q_lo + (row_ok ? tq : 0)) * pp.Hq + (row_ok ? head : 0);
+      const int64_t nrows = static_cast<int64_t>(pp.num_queries) * pp.Hq;  // extents for the checked build
       if (partial) {  // unnormalised output of this key run and its (m, l)
         const size_t prow = static_cast<size_t>(w.sp) * pp.num_queries * pp.Hq + orow;
         float4* dst = reinterpret_cast<float4*>(pp.ws_o + prow * D);
+        const bool row_in = row_ok && in_bounds(pp.status, static_cast<int64_t>(prow), pp.num_splits * nrows);
         if (have) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(tO + 32 * c, o);
             tmem_wait_ld();
-            if (row_ok) {
+            if (row_in) {
 #pragma unroll
               for (int u = 0; u < 8; ++u)
                 dst[c * 8 + u] = make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]),
@@ -416,10 +424,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         }
-        if (row_ok) pp.ws_ml[prow] = make_float2(live ? m_run : -INFINITY, live ? l_run : 0.f);
+        if (row_in) pp.ws_ml[prow] = make_float2(live ? m_run : -INFINITY, live ? l_run : 0.f);
       } else {
         const float inv = live ? 1.f / l_run : __int_as_float(0x7fc00000);
         uint8_t* dst = static_cast<uint8_t*>(out) + orow * D * 2;
+        const bool row_in = row_ok && in_bounds(pp.status, static_cast<int64_t>(orow), nrows);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -430,7 +439,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = 0u;
           }
-          if (row_ok) {
+          if (row_in) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -444,7 +453,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
           }
         }
-        if (row_ok && lse) lse[orow] = live ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+        if (row_in && lse) lse[orow] = live ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
       }
     }
   }

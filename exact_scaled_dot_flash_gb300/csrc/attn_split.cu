@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const KernelParams p, void* 
   const int64_t r = idx / G;
   const int g = static_cast<int>(idx - r * G);
   const int ns = p.num_splits;
+  // the bounds-checked build tests every workspace, output and lse index
+  if (!range_in_bounds(p.status, (static_cast<int64_t>(ns) - 1) * rows + r, 1, ns * rows)) return;
   float M = -INFINITY;
   for (int s = 0; s < ns; ++s) M = fmaxf(M, p.ws_ml[s * rows + r].x);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -49,6 +51,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const KernelParams p, void* 
   }
   const float inv = L > 0.f ? 1.f / L : __int_as_float(0x7fc00000);
   acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+  if (!in_bounds(p.status, r * G + g, rows * G)) return;
   if constexpr (DT == 0) {
     reinterpret_cast<float4*>(out)[r * G + g] = acc;
   } else {

@@ -472,7 +472,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // scores -> log2 domain with the bias folded in
         if (brow != nullptr) {
           const float* bp = brow + key0;
-          if (j < nfull_t && p.bias_vec4) {
+          const int64_t nbias = static_cast<int64_t>(p.bias_b) * p.bias_h * p.Sq * p.Sk;  // checked build
+          if (j < nfull_t && p.bias_vec4 && range_in_bounds(p.status, bp - p.bias, 128, nbias)) {
 #pragma unroll
             for (int i = 0; i < 128; i += 4) {
               const float4 b4 = __ldg(reinterpret_cast<const float4*>(bp + i));
@@ -485,7 +486,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
 #pragma unroll
             for (int i = 0; i < 128; ++i) {
-              const float bv = (key0 + i < key_lim) ? __ldg(bp + i) : 0.f;
+              const float bv =
+                  (key0 + i < key_lim && in_bounds(p.status, (bp - p.bias) + i, nbias)) ? __ldg(bp + i) : 0.f;
               s[i] = fmaf(s[i], sc, bv * LOG2E);
             }
           }
@@ -590,11 +592,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const size_t rr =
           (static_cast<size_t>(blockIdx.x % p.num_splits) * p.B * p.Hq + w.bh) * p.Sq +
           static_cast<size_t>(row_g);
+      // bounds-checked build: the partial row lies inside the workspace
+      const bool rr_ok = row_g < p.Sq &&
+                         in_bounds(p.status, static_cast<int64_t>(rr),
+                                   static_cast<int64_t>(p.num_splits) * p.B * p.Hq * p.Sq);
       if (failed) {
         if (lane == 0) fail();
         // m = +inf, l = NaN: the merge makes the row NaN whatever the other
         // parts (or an earlier call's scratch) hold
-        if (row_g < p.Sq) p.ws_ml[rr] = make_float2(INFINITY, __int_as_float(0x7fc00000));
+        if (rr_ok) p.ws_ml[rr] = make_float2(INFINITY, __int_as_float(0x7fc00000));
       } else {
         tc_fence_after();
         float4* wrow = reinterpret_cast<float4*>(p.ws_o + rr * D);
@@ -608,14 +614,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = 0u;
           }
-          if (row_g < p.Sq) {
+          if (rr_ok) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               wrow[8 * c + i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
                                             __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
           }
         }
-        if (row_g < p.Sq) p.ws_ml[rr] = have ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
+        if (rr_ok) p.ws_ml[rr] = have ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
       }
     } else if (!SPLIT && r0 < p.Sq) {
       const bool have = n_t > 0;
@@ -629,7 +635,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         // rows with no visible key have an undefined softmax: NaN
         const float inv = (have && l_run > 0.f) ? 1.f / l_run : __int_as_float(0x7fc00000);
-        if (EPI == EPI_O_LSE && row_g < p.Sq)
+        if (EPI == EPI_O_LSE && row_g < p.Sq &&
+            in_bounds(p.status, static_cast<int64_t>(w.bh) * p.Sq + row_g, static_cast<int64_t>(p.B) * p.Hq * p.Sq))
           p.lse[static_cast<size_t>(w.bh) * p.Sq + row_g] =
               (have && l_run > 0.f) ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
         uint8_t* stage = smem + t * C::TILE_BYTES;  // Q_t is dead: reuse it for O_t

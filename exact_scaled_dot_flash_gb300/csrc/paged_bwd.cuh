@@ -119,30 +119,38 @@ __device__ __forceinline__ void dkdv_page(const void* __restrict__ q, const void
   const int tid = threadIdx.x, part = tid % TPK, kl = tid / TPK;
   const int group = pp.Hq / pp.Hkv;
   const int P = pp.page_size;
+  // extents (float4 groups, rows, entries) for the bounds-checked build
+  int* const st = pp.status;
+  const size_t nq4 = static_cast<size_t>(pp.num_queries) * pp.Hq * G, nqp4 = static_cast<size_t>(pp.num_queries) * pp.Hq * PG;
+  const size_t nk4 = static_cast<size_t>(pp.num_pages) * P * pp.Hkv * G, nkp4 = static_cast<size_t>(pp.num_pages) * P * PG;
+  const int64_t nrows = static_cast<int64_t>(pp.num_queries) * pp.Hq;
+  const int64_t nrefs = static_cast<int64_t>(pp.num_seqs) * pp.max_pages;
   const int t0 = blockIdx.y * kpc;
   const int t = t0 + kl;
   const bool key_ok = kl < kpc && t < P;
   const size_t slot = static_cast<size_t>(page) * P + (key_ok ? t : 0);
   const size_t krow = (slot * pp.Hkv + hk) * G;
 
-  const int r_lo = __ldg(b.offsets + page), r_hi = __ldg(b.offsets + page + 1);
+  const bool page_ok = in_bounds(st, page, pp.num_pages);
+  const int r_lo = page_ok ? __ldg(b.offsets + page) : 0, r_hi = page_ok ? __ldg(b.offsets + page + 1) : 0;
 
   float4 kr[GPT], vr[GPT], dka[GPT], dva[GPT], kpr[PPT > 0 ? PPT : 1], dkpa[PPT > 0 ? PPT : 1];
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int c = 0; c < GPT; ++c) {
-    kr[c] = key_ok ? load4<DT>(k, krow + part + TPK * c) : z;
-    if constexpr (!MLA) vr[c] = key_ok ? load4<DT>(v, krow + part + TPK * c) : z;
+    kr[c] = key_ok ? load4<DT>(k, krow + part + TPK * c, nk4, st) : z;
+    if constexpr (!MLA) vr[c] = key_ok ? load4<DT>(v, krow + part + TPK * c, nk4, st) : z;
     dka[c] = dva[c] = z;
   }
 #pragma unroll
   for (int c = 0; c < PPT; ++c) {
     const int gi = part + TPK * c;
-    kpr[c] = (key_ok && gi < PG) ? load4<DT>(kp, slot * PG + gi) : z;
+    kpr[c] = (key_ok && gi < PG) ? load4<DT>(kp, slot * PG + gi, nkp4, st) : z;
     dkpa[c] = z;
   }
 
   for (int ri = r_lo; ri < r_hi; ++ri) {
+    if (!in_bounds(st, ri, nrefs)) break;
     const int code = __ldg(b.refs + ri);
     const int s = code / pp.max_pages, blk = code - s * pp.max_pages;
     const int L = keys_of(pp, s);
@@ -167,14 +175,27 @@ __device__ __forceinline__ void dkdv_page(const void* __restrict__ q, const void
       const int r = idx / (2 * G + PG), c = idx - r * (2 * G + PG);
       size_t rr;
       if (!row_of(e0 + r, rr)) return z;
-      return c < G ? load4<DT>(q, rr * G + c)
-                   : (c < 2 * G ? load4<DT>(dout, rr * G + c - G) : load4<DT>(qp, rr * PG + c - 2 * G));
+      return c < G ? load4<DT>(q, rr * G + c, nq4, st)
+                   : (c < 2 * G ? load4<DT>(dout, rr * G + c - G, nq4, st)
+                                : load4<DT>(qp, rr * PG + c - 2 * G, nqp4, st));
     };
     auto put = [&](int idx, float4 v) {
       const int r = idx / (2 * G + PG), c = idx - r * (2 * G + PG);
-      if (c < G) qs[r * G + c] = v;
-      else if (c < 2 * G) gs[r * G + c - G] = v;
-      else qps[r * PG + c - 2 * G] = v;
+      if (c < G) {
+        if (in_bounds(st, r * G + c, RT * G)) qs[r * G + c] = v;
+      } else if (c < 2 * G) {
+        if (in_bounds(st, r * G + c - G, RT * G)) gs[r * G + c - G] = v;
+      } else if (in_bounds(st, r * PG + c - 2 * G, RT * PG)) {
+        qps[r * PG + c - 2 * G] = v;
+      }
+    };
+    // the row statistics of row rr (and its position) for the staged tile
+    auto stats = [&](size_t rr, float& l2v, float& dsv, int& posv) {
+      const bool ok = in_bounds(st, static_cast<int64_t>(rr), nrows);
+      l2v = ok ? b.lse2[rr] : -INFINITY;
+      dsv = ok ? b.dsum[rr] : 0.f;
+      const int qrow = static_cast<int>(rr / pp.Hq);
+      posv = (!pp.positions || in_bounds(st, qrow, pp.num_queries)) ? position_of(pp, qrow, q0, n, L) : -1;
     };
     // full 256-thread CTAs load the next tile into registers while computing
     // this one (its latency would otherwise be paid once per tile)
@@ -192,10 +213,13 @@ __device__ __forceinline__ void dkdv_page(const void* __restrict__ q, const void
       }
       if (tid < RT) {
         size_t rr;
-        const bool in = row_of(e0 + tid, rr);
-        pre_l2 = in ? b.lse2[rr] : -INFINITY;
-        pre_ds = in ? b.dsum[rr] : 0.f;
-        pre_pos = in ? position_of(pp, static_cast<int>(rr / pp.Hq), q0, n, L) : -1;
+        if (row_of(e0 + tid, rr)) {
+          stats(rr, pre_l2, pre_ds, pre_pos);
+        } else {
+          pre_l2 = -INFINITY;
+          pre_ds = 0.f;
+          pre_pos = -1;
+        }
       }
     };
     if (pf && e_lo < npairs) fetch(e_lo);
@@ -209,10 +233,13 @@ __device__ __forceinline__ void dkdv_page(const void* __restrict__ q, const void
         for (int idx = tid; idx < TOT; idx += blockDim.x) put(idx, element(e0, idx));
         if (tid < RT) {
           size_t rr;
-          const bool in = row_of(e0 + tid, rr);
-          pre_l2 = in ? b.lse2[rr] : -INFINITY;
-          pre_ds = in ? b.dsum[rr] : 0.f;
-          pre_pos = in ? position_of(pp, static_cast<int>(rr / pp.Hq), q0, n, L) : -1;
+          if (row_of(e0 + tid, rr)) {
+            stats(rr, pre_l2, pre_ds, pre_pos);
+          } else {
+            pre_l2 = -INFINITY;
+            pre_ds = 0.f;
+            pre_pos = -1;
+          }
         }
       }
       if (tid < RT) {
@@ -267,10 +294,11 @@ __device__ __forceinline__ void dkdv_page(const void* __restrict__ q, const void
   for (int c = 0; c < GPT; ++c) {
     const float4 a = dka[c];
     if constexpr (MLA) {
-      if (dk) store4<DT>(dk, krow + part + TPK * c, a);
+      if (dk) store4<DT>(dk, krow + part + TPK * c, nk4, st, a);
     } else {
-      if (dk) store4<DT>(dk, krow + part + TPK * c, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
-      if (dv) store4<DT>(dv, krow + part + TPK * c, dva[c]);
+      if (dk)
+        store4<DT>(dk, krow + part + TPK * c, nk4, st, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
+      if (dv) store4<DT>(dv, krow + part + TPK * c, nk4, st, dva[c]);
     }
   }
 #pragma unroll
@@ -278,7 +306,7 @@ __device__ __forceinline__ void dkdv_page(const void* __restrict__ q, const void
     const int gi = part + TPK * c;
     const float4 a = dkpa[c];
     if (dkp && gi < PG)
-      store4<DT>(dkp, slot * PG + gi, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
+      store4<DT>(dkp, slot * PG + gi, nkp4, st, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
   }
 }
 
@@ -301,6 +329,7 @@ __global__ void __launch_bounds__(THREADS) dkdv_kernel(const void* __restrict__ 
   const int stride = gridDim.x / pp.Hkv;
   for (int li = unit; li < n; li += stride) {
     __syncthreads();  // the previous page's shared-memory rows are no longer read
+    if (!in_bounds(pp.status, 1 + li, static_cast<int64_t>(pp.num_pages) + 1)) break;
     dkdv_page<DK, PD, TPK, DT, MLA>(q, qp, k, kp, v, dout, b, dk, dkp, dv, pp, scale, kpc, b.list[1 + li], hk);
   }
 }
@@ -324,6 +353,12 @@ __global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q,
   const int s = blockIdx.x / pp.Hkv, hk = blockIdx.x - s * pp.Hkv;
   const int group = pp.Hq / pp.Hkv;
   const int P = pp.page_size;
+  // extents (float4 groups, rows, entries) for the bounds-checked build
+  int* const st = pp.status;
+  const size_t nq4 = static_cast<size_t>(pp.num_queries) * pp.Hq * G, nqp4 = static_cast<size_t>(pp.num_queries) * pp.Hq * PG;
+  const size_t nk4 = static_cast<size_t>(pp.num_pages) * P * pp.Hkv * G, nkp4 = static_cast<size_t>(pp.num_pages) * P * PG;
+  const int64_t nrows = static_cast<int64_t>(pp.num_queries) * pp.Hq;
+  const int64_t ntab = static_cast<int64_t>(pp.num_seqs) * pp.max_pages;
   int q0, n;
   rows_of(pp, s, q0, n);
   const int npairs = n * group;
@@ -338,20 +373,22 @@ __global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q,
   float4 qr[GPT], gr[GPT], acc[GPT], qpr[PPT > 0 ? PPT : 1], accp[PPT > 0 ? PPT : 1];
 #pragma unroll
   for (int c = 0; c < GPT; ++c) {
-    qr[c] = row_ok ? load4<DT>(q, rr * G + part + TPK * c) : z;
-    gr[c] = row_ok ? load4<DT>(dout, rr * G + part + TPK * c) : z;
+    qr[c] = row_ok ? load4<DT>(q, rr * G + part + TPK * c, nq4, st) : z;
+    gr[c] = row_ok ? load4<DT>(dout, rr * G + part + TPK * c, nq4, st) : z;
     acc[c] = z;
   }
 #pragma unroll
   for (int c = 0; c < PPT; ++c) {
     const int gi = part + TPK * c;
-    qpr[c] = (row_ok && gi < PG) ? load4<DT>(qp, rr * PG + gi) : z;
+    qpr[c] = (row_ok && gi < PG) ? load4<DT>(qp, rr * PG + gi, nqp4, st) : z;
     accp[c] = z;
   }
-  const float l2 = row_ok ? b.lse2[rr] : -INFINITY;
+  const bool stat_ok = row_ok && in_bounds(st, static_cast<int64_t>(rr), nrows);
+  const float l2 = stat_ok ? b.lse2[rr] : -INFINITY;
   const bool live = l2 != -INFINITY;
   const float dsi = live ? b.dsum[rr] : 0.f;
-  const int pos = row_ok ? position_of(pp, q0 + qi, q0, n, L) : -1;
+  const int pos = (row_ok && (!pp.positions || in_bounds(st, q0 + qi, pp.num_queries)))
+                      ? position_of(pp, q0 + qi, q0, n, L) : -1;
   // keys past every row's causal limit are not visited
   if (tid == 0) hi_s = 0;
   __syncthreads();
@@ -372,14 +409,15 @@ __global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q,
       const int r = idx / (G + VG + PG), c = idx - r * (G + VG + PG);
       const int j = key0 + r;
       int pg = -1;
-      if (idx < TOT && j < hi) pg = __ldg(pp.block_table + static_cast<size_t>(s) * pp.max_pages + j / P);
+      const int64_t te = static_cast<int64_t>(s) * pp.max_pages + j / P;
+      if (idx < TOT && j < hi && in_bounds(st, te, ntab)) pg = __ldg(pp.block_table + te);
       const bool ok = pg >= 0 && pg < pp.num_pages;  // entries outside the cache read as zero keys
       const size_t sl = ok ? static_cast<size_t>(pg) * P + j % P : 0;
       float4 x = z;
       if (ok) {
-        if (c < G) x = load4<DT>(k, (sl * pp.Hkv + hk) * G + c);
-        else if (c < G + VG) x = load4<DT>(v, (sl * pp.Hkv + hk) * G + c - G);
-        else x = load4<DT>(kp, sl * PG + c - G - VG);
+        if (c < G) x = load4<DT>(k, (sl * pp.Hkv + hk) * G + c, nk4, st);
+        else if (c < G + VG) x = load4<DT>(v, (sl * pp.Hkv + hk) * G + c - G, nk4, st);
+        else x = load4<DT>(kp, sl * PG + c - G - VG, nkp4, st);
       }
       pre[u] = x;
     }
@@ -392,9 +430,13 @@ __global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q,
       const int idx = tid + u * THREADS;
       if (idx < TOT) {
         const int r = idx / (G + VG + PG), c = idx - r * (G + VG + PG);
-        if (c < G) ks[r * G + c] = pre[u];
-        else if (c < G + VG) vs[r * VG + c - G] = pre[u];
-        else kps[r * PG + c - G - VG] = pre[u];
+        if (c < G) {
+          if (in_bounds(st, r * G + c, RT * G)) ks[r * G + c] = pre[u];
+        } else if (c < G + VG) {
+          if (in_bounds(st, r * VG + c - G, RT * VG)) vs[r * VG + c - G] = pre[u];
+        } else if (in_bounds(st, r * PG + c - G - VG, RT * PG)) {
+          kps[r * PG + c - G - VG] = pre[u];
+        }
       }
     }
     __syncthreads();
@@ -435,14 +477,15 @@ __global__ void __launch_bounds__(THREADS) dq_kernel(const void* __restrict__ q,
 #pragma unroll
   for (int c = 0; c < GPT; ++c) {
     const float4 a = acc[c];
-    if (dq) store4<DT>(dq, rr * G + part + TPK * c, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
+    if (dq)
+      store4<DT>(dq, rr * G + part + TPK * c, nq4, st, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
   }
 #pragma unroll
   for (int c = 0; c < PPT; ++c) {
     const int gi = part + TPK * c;
     const float4 a = accp[c];
     if (dqp && gi < PG)
-      store4<DT>(dqp, rr * PG + gi, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
+      store4<DT>(dqp, rr * PG + gi, nqp4, st, make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale));
   }
 }
 

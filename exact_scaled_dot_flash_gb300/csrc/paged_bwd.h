@@ -30,9 +30,10 @@ struct Buffers {
 };
 Buffers carve(void* workspace, const Layout& lay);
 
-// Row statistics of the nq * heads rows of out/dout ([rows, width] in dtype).
+// Row statistics of the nq * heads rows of out/dout ([rows, width] in dtype);
+// `status`: the device status word (bounds-checked build).
 cudaError_t launch_preprocess(int dtype, int width, const void* out, const void* dout, const float* lse,
-                              const Buffers& b, int64_t rows, cudaStream_t st);
+                              const Buffers& b, int64_t rows, cudaStream_t st, int* status = nullptr);
 
 // The reverse page index of every table entry that a sequence with queries
 // reads (block b < ceil(seq_len / page_size), page id in [0, num_pages)).
@@ -66,6 +67,21 @@ struct TcArgs {
 template <int D, bool BF16>
 cudaError_t launch_paged_bwd_tc(EncodeTiledFn enc, const PagedParams& pp, const void* q, const void* k,
                                 const void* v, const void* dout, const TcArgs& a, cudaStream_t st);
+
+// Tensor-core paged MLA backward (F16/BF16: bf16 selects BF16; R in {256,
+// 512}, Pd in {0, 64}, page_size a multiple of 8 dividing 128 or a multiple of
+// 128): dq, dqp for every row and dlatent, dkpos for the pages with exactly
+// one reader (b's reverse index; outputs may be nullptr).
+cudaError_t launch_mla_bwd_tc(EncodeTiledFn enc, int R, int Pd, bool bf16, const PagedParams& pp, const void* q,
+                              const void* qp, const void* lat, const void* kp, const void* dout, const Buffers& b,
+                              void* dq, void* dqp, void* dlat, void* dkp, float scale, cudaStream_t st);
+
+// Key-major fp32 FMA pass of paged MLA over the pages whose reader count is
+// not one, after the tensor-core kernels (R in {256, 512}, Pd in {0, 64},
+// dtype 1 f16 or 2 bf16).
+cudaError_t launch_mla_dkdv_shared(int R, int Pd, int dtype, const PagedParams& pp, const void* q, const void* qp,
+                                   const void* lat, const void* kp, const void* dout, const Buffers& b, void* dlat,
+                                   void* dkp, float scale, cudaStream_t st);
 
 // Paged MLA (Hq = heads, Hkv = 1): dq [nq, H, R], dqp [nq, H, Pd], dlatent
 // [pages, page_size, R], dkpos [pages, page_size, Pd]; outputs may be nullptr.

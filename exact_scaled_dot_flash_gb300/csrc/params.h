@@ -74,7 +74,8 @@ cudaError_t launch_bwd_tc_instance(EncodeTiledFn enc, const void* q, const void*
                                    cudaStream_t stream);
 }  // namespace bwdtc
 cudaError_t launch_bwd_preprocess(int D, int dtype, const void* out, const void* dout, const float* lse,
-                                  float* dsum, float* lse2, int64_t rows, cudaStream_t stream);
+                                  float* dsum, float* lse2, int64_t rows, cudaStream_t stream,
+                                  int* status = nullptr);
 
 // Paged key/value cache with packed variable-length queries.
 struct PagedParams {

@@ -14,6 +14,7 @@ namespace attn {
 
 // Status bits a kernel ORs into the device status word.
 constexpr int STATUS_TIMEOUT = 1;
+constexpr int STATUS_BOUNDS = 2;  // bounds-checked build: an index fell outside its buffer
 
 // Upper bound of any single wait inside a kernel. Every legitimate wait is a
 // few microseconds; after this the kernel records ATTN status and unwinds.
@@ -27,6 +28,43 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// ------------------------------------------------------------------ bounds checks
+// The bounds-checked build (compiled with ATTN_CHECKED) tests the computed
+// index of every direct global access of the paged, MLA, split and backward
+// kernels, the shared-memory index of their staged tiles and the destination
+// of their TMA copies: in_bounds(status, i, n) is true when 0 <= i < n;
+// otherwise it ORs STATUS_BOUNDS into the status word and the caller skips the
+// access (a skipped load reads zero). In the normal build it is the constant
+// true and the check compiles away. (TMA copies check their global
+// coordinates in hardware.)
+__device__ __forceinline__ bool in_bounds(int* status, int64_t i, int64_t n) {
+#ifdef ATTN_CHECKED
+  if (i >= 0 && i < n) return true;
+  if (status) atomicOr(status, STATUS_BOUNDS);
+  return false;
+#else
+  (void)status;
+  (void)i;
+  (void)n;
+  return true;
+#endif
+}
+
+// [i, i + len) inside [0, n)
+__device__ __forceinline__ bool range_in_bounds(int* status, int64_t i, int64_t len, int64_t n) {
+#ifdef ATTN_CHECKED
+  if (i >= 0 && len >= 0 && i + len <= n) return true;
+  if (status) atomicOr(status, STATUS_BOUNDS);
+  return false;
+#else
+  (void)status;
+  (void)i;
+  (void)len;
+  (void)n;
+  return true;
+#endif
 }
 
 // ------------------------------------------------------------------ mbarrier

@@ -64,6 +64,31 @@ __device__ __forceinline__ void store4(void* base, size_t idx4, float4 v) {
   }
 }
 
+// Bounds-checked forms (see in_bounds): n4 is the number of float4 groups in
+// the array; an index outside it is recorded in *status and skipped.
+template <int DT>
+__device__ __forceinline__ float4 load4(const void* base, size_t idx4, size_t n4, int* status) {
+  return in_bounds(status, static_cast<int64_t>(idx4), static_cast<int64_t>(n4))
+             ? load4<DT>(base, idx4)
+             : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+template <int DT>
+__device__ __forceinline__ void store4(void* base, size_t idx4, size_t n4, int* status, float4 v) {
+  if (in_bounds(status, static_cast<int64_t>(idx4), static_cast<int64_t>(n4))) store4<DT>(base, idx4, v);
+}
+
+// idx8 counts 8-element groups; n8 is their number in the array
+template <int DT>
+__device__ __forceinline__ void load8(const void* base, size_t idx8, size_t n8, int* status, float4& lo,
+                                      float4& hi) {
+  if (in_bounds(status, static_cast<int64_t>(idx8), static_cast<int64_t>(n8))) {
+    load8<DT>(base, idx8, lo, hi);
+  } else {
+    lo = hi = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
 __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
   acc = fmaf(a.x, b.x, acc);
   acc = fmaf(a.y, b.y, acc);

@@ -480,10 +480,20 @@ ATTN_API const char* attn_strerror(int code);
  * by attn_fwd on the calling thread (0 if none). */
 ATTN_API int attn_last_cuda_error(void);
 
+/* Bits of the device status word (attn_device_status). */
+#define ATTN_STATUS_TIMEOUT 1 /* a kernel gave up on a bounded wait and unwound */
+#define ATTN_STATUS_BOUNDS 2  /* bounds-checked build only (libattn_checked.so, compiled
+                                 with ATTN_CHECKED): a computed global or shared-memory
+                                 index of a paged, MLA, split or backward kernel fell
+                                 outside its buffer; the access was skipped */
+
 /* attn_device_status - read (and, when clear != 0, reset) the sticky error
- * word that kernels on `device` set when a bounded wait expires. Writes the
- * flags to *flags (0 = no failure seen). Synchronises with the device.
- * Returns ATTN_OK, ATTN_ERR_NULL or ATTN_ERR_CUDA. */
+ * word that kernels on `device` set when a bounded wait expires (and, in the
+ * bounds-checked build, when an index falls outside its buffer). Writes the
+ * flags to *flags (0 = no failure seen; ATTN_STATUS_* bits otherwise).
+ * Synchronises with the device. Each build of the library (libattn.so,
+ * libattn_checked.so) has its own word. Returns ATTN_OK, ATTN_ERR_NULL or
+ * ATTN_ERR_CUDA. */
 ATTN_API int attn_device_status(int device, int* flags, int clear);
 
 /* attn_fwd_host - attn_fwd on tensors in HOST memory: q, k, v, kv_lens, bias

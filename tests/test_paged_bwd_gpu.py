@@ -1,8 +1,9 @@
 """GPU parity of the backward over a paged cache (attn_paged_bwd and
 attn_paged_mla_bwd) against the float64 oracle. F16/BF16 cases with D in
-{64, 128} and page sizes of 8..256 take the tensor-core kernels (with the fp32
-FMA key-major kernel for shared and unread pages); the others the fp32 FMA
-kernels throughout.
+{64, 128} (paged attention) or R in {256, 512} and Pd in {0, 64} (MLA) and
+page sizes of 8..256 take the tensor-core kernels (with the fp32 FMA key-major
+kernel for shared and unread pages); the others the fp32 FMA kernels
+throughout.
 
 The pipeline is the user's: the CUDA paged forward with its log-sum-exp, then
 the CUDA backward on (inputs, out, dout, lse); the oracle computes every
@@ -204,6 +205,14 @@ MLA_CASES = [
     MW("mbwd_f16_r256_pd0_p32_pos", "f16", 3, 8, 256, 0, 32, (30, 300), (1, 20), seed=43, explicit_positions=True),
     MW("mbwd_bf16_r512_pd32_decode", "bf16", 4, 128, 512, 32, 64, (100, 600), (1, 1), seed=44),
     MW("mbwd_f16_r128_pd64_p8_full", "f16", 3, 8, 128, 64, 8, (20, 120), (1, 12), seed=45, causal=False),
+    # tensor-core kernels: decode-shaped (one 128-row tile per sequence, the
+    # query-major kernel longest sequence first), several row tiles per
+    # sequence, page sizes 8 and 128..256, no causal mask, Pd 0 and 64
+    MW("mbwd_bf16_r512_pd64_decode_h128", "bf16", 5, 128, 512, 64, 64, (100, 700), (1, 1), seed=47),
+    MW("mbwd_f16_r512_pd64_p128_prefill", "f16", 3, 16, 512, 64, 128, (200, 700), (5, 30), seed=48),
+    MW("mbwd_bf16_r256_pd64_p8_full", "bf16", 3, 8, 256, 64, 8, (20, 200), (1, 12), seed=49, causal=False),
+    MW("mbwd_bf16_r512_pd0_p256", "bf16", 3, 32, 512, 0, 256, (100, 600), (1, 6), seed=50),
+    MW("mbwd_f16_r512_pd64_p16_pos", "f16", 3, 16, 512, 64, 16, (40, 300), (2, 17), seed=51, explicit_positions=True),
 ]
 
 
