@@ -554,6 +554,9 @@ def bench_paged(args):
     if is_mla:
         tensor = (w.dtype != "f32" and w.R in (256, 512) and w.Pd in (0, 64) and w.page_size % 8 == 0
                   and (64 % w.page_size == 0 or w.page_size % 64 == 0))
+        # the backward's tensor-core kernels gather 128-key blocks
+        tensor_bwd = (w.dtype != "f32" and w.R in (256, 512) and w.Pd in (0, 64) and w.page_size % 8 == 0
+                      and (128 % w.page_size == 0 or w.page_size % 128 == 0))
     else:
         tensor = (w.dtype != "f32" and w.D in (64, 128) and w.page_size % 8 == 0
                   and (128 % w.page_size == 0 or w.page_size % 128 == 0))
@@ -568,7 +571,7 @@ def bench_paged(args):
         pws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
         # preprocess, page-index count / scan / fill / sort, key-major and query-major kernels
         # (tensor-core paths add the FMA key-major pass over shared pages)
-        launches = 8 if (not is_mla and tensor) else 7
+        launches = 8 if (tensor_bwd if is_mla else tensor) else 7
 
     def step():
         if bwd:
@@ -635,10 +638,22 @@ def bench_paged(args):
     # ideal time); the rest runs on the fp32 FMA pipes
     mla_hbm = is_mla and tensor and nbytes / float(peaks["hbm_gbs"]) > flops / (float(peaks["bf16_tflops"]) * 1e3)
     # the paged backward: tensor cores for F16/BF16 paged attention with D in
-    # {64, 128} (HBM-bound when decode-shaped), the fp32 FMA kernels otherwise
+    # {64, 128} (HBM-bound when decode-shaped), the fp32 FMA kernels otherwise;
+    # the MLA backward on the tensor cores is held to whichever of the tensor
+    # and HBM rooflines binds (the larger ideal time)
     bwd_tc = bwd and not is_mla and tensor
+    mla_bwd_tc = bwd and is_mla and tensor_bwd
     tc_names = "paged_dkdv_tc_kernel + paged_dq_tc_kernel (+ FMA pass over shared pages), whole call"
-    if bwd and bwd_tc and decode:
+    if mla_bwd_tc:
+        pk, bw = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+        names = "mla_bwd_tc_kernel key-major + query-major (+ FMA pass over shared pages), whole call"
+        if nbytes / bw > flops / (pk * 1e3):
+            roof = {"bound": "hbm", "achieved": gbs, "peak": bw, "unit": "GB/s", "frac": gbs / bw,
+                    "peak_kind": f"{peak_kind} HBM copy", "kernel": names}
+        else:
+            roof = {"bound": "tensor", "achieved": tf, "peak": pk, "unit": "TFLOP/s", "frac": tf / pk,
+                    "peak_kind": f"{peak_kind} bf16 dense burst", "kernel": names}
+    elif bwd and bwd_tc and decode:
         roof = {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                 "frac": gbs / float(peaks["hbm_gbs"]), "peak_kind": f"{peak_kind} HBM copy", "kernel": tc_names}
     elif bwd_tc:
