@@ -10,33 +10,65 @@
 //
 // Shape of the work: the rows of a sequence are its (query, head) pairs,
 // row = query * H + head, so a decode step with H = 128 heads is one 128-row
-// tile. A key row [c_j | kp_j] is R + Pd wide (576 for R = 512, Pd = 64) and
-// the output R wide. Each 128-row block is run by R/128 CTAs, one per
-// 128-column slice of the output: every CTA computes the full scores
-// S = [q | qp] [c | kp]^T of its rows (the same MMAs, so the same P, in each
-// CTA) and its own slice of P . c. With only 128 output columns the whole
-// query fits in tensor memory next to the scores, so shared memory holds
-// nothing but a ring of 64-key tiles, and the score MMAs are 64 keys wide: a
-// 128 x N x 16 MMA costs about the same for N = 16..64, so the width halves
-// the score cost per key against 32-key tiles.
+// block. A key row [c_j | kp_j] is R + Pd wide (576 for R = 512, Pd = 64) and
+// the output R wide; 128 x R fp32 does not fit in tensor memory next to the
+// query and the scores, so a cluster of NH = R/128 CTAs runs each row block,
+// CTA h accumulating output columns [128 h, 128 h + 128).
+//
+// The scores are computed once per row block. The block's 64-key tiles are
+// dealt round-robin to the cluster: the CTA that owns tile t (t mod NH = h)
+// issues its 36 score MMAs (the query, resident in tensor memory, times the
+// tile's nine 64-wide key chunks streamed through a ring), runs the softmax,
+// writes the 16-bit P tile and every row's (reference maximum, row sum) into
+// P slot t mod 8 of its shared memory and copies both into the same slot of
+// every other CTA of the cluster (cp.async.bulk shared::cta -> shared::cluster,
+// completing on the receiver's mbarrier). Every CTA multiplies every P tile by
+// its own two latent chunks of the tile (P from shared memory, the chunks from
+// a second ring). A CTA therefore issues 36 / NH score MMAs and 4 output MMAs
+// per tile, where computing the scores in every CTA would take 36 + 4.
+//
+// One reference maximum per row for the whole cluster. P of a tile is
+// exp2(s' - m) for the reference m its owner chose; the output accumulator of
+// every CTA is relative to that CTA's current reference m_O. Before the first
+// P, the CTAs exchange the row maxima of their first tiles through distributed
+// shared memory and all start from their maximum (a cluster barrier orders
+// the exchange). An owner then keeps m = m_O unless the tile's maximum exceeds
+// it by more than 8 (log2 units; then m = that maximum), so that in the common
+// case every tile arrives with the receiver's own reference. A receiver
+// reconciles each tile row by row: equal references add the tile's row sum; a
+// larger one rescales the row of the accumulator (after the previous P . V)
+// and the row sum and adopts it; a smaller one scales the row of P in its own
+// slot down (for its own tile only after every peer has received the copy) and
+// adds the scaled sum. Numerically this is the online softmax with lazy
+// rescaling; which reference a tile used only changes rounding.
 //
 // Tensor memory (512 columns): the query chunks (64 dims = 32 packed 16-bit
-// columns each, at most nine), S (64 fp32 columns), P (32 packed columns), the
-// 128-column output slice. The S MMA reads its A operand (the query) from
-// tensor memory and the key chunk from the ring; P . V reads P from tensor
-// memory and this slice's two latent chunks of the same ring tile as V (the
-// values are the latent rows, so no separate value load exists).
+// columns each, at most nine), S (64 fp32 columns), the 128-column output slice.
+// Shared memory: 8 P slots (16 KB), 8 (m, l) vectors (1 KB), 3 value stages
+// (this CTA's two latent chunks of a tile, 16 KB), a 4-slot ring of score
+// chunks (8 KB), the first tiles' row maxima of every CTA. The query passes
+// through the P slots and value stages on its way to tensor memory.
 //
-// Warps: 0-3 softmax (one row per thread: loads the 64 scores, frees S for the
-// next tile's MMA, masks, online softmax, waits for the previous P . V before
-// writing P and, rarely, rescaling O), 4 TMA producer (the query once through
-// ring stages 1.., then key tiles gathered page by page through 3-D views
-// [pages, page_size, R] and [pages, page_size, Pd] of the caches; an invalid
-// page id loads zeros), 5 MMA issuer, order S_0 S_1 PV_0 S_2 PV_1 ...
+// Warps: 0-3 softmax (one row per thread; each own tile's scores, then the
+// reconciliation of every tile up to it, in tile order), 4 TMA (the query, then
+// the score chunks of this CTA's tiles, with an L2 prefetch of the next own
+// tile), 6 TMA (this CTA's two value chunks of every tile), 5 MMA issuer. The
+// MMA issuer polls without blocking and issues whatever is ready: the next own
+// tile's score MMAs chunk by chunk once the softmax has read the previous S,
+// and P . V of the tiles in order as their P arrives. An in-order issuer
+// (own S, then the P . V of the tiles up to the next own one) makes every CTA's
+// next score tile wait for the peers' P tiles, which wait for theirs: measured
+// a third slower. The producers read each tile's page ids one tile ahead: a table
+// read in front of every copy put a global-load latency on each chunk. Key
+// tiles are gathered page by page through 3-D views [pages, page_size, R] and
+// [pages, page_size, Pd] of the caches; an invalid page id loads zeros. Every
+// wait is bounded; a cluster barrier after the barrier setup, one for the
+// exchange of first-tile maxima and one before exit keep the CTAs resident
+// while a peer may still write to them.
 //
-// Key-range splits: the CTA's key tiles are cut into num_splits balanced runs;
-// with more than one run each CTA writes its unnormalised partial output and
-// (m, l) and launch_split_merge combines them (the split of attn_fwd_split).
+// Key-range splits: the block's key tiles are cut into num_splits balanced
+// runs (one cluster each); with more than one run each CTA writes its
+// unnormalised partial output and (m, l) and launch_split_merge combines them.
 // Requires page_size a multiple of 8 that divides 64 or is a multiple of 64.
 #pragma once
 
@@ -49,17 +81,21 @@
 namespace attn {
 namespace mlatc {
 
-constexpr int BM = 128;           // (query, head) rows per CTA
+constexpr int BM = 128;           // (query, head) rows per cluster
 constexpr int BN = 64;            // keys per tile
 constexpr int OC = 128;           // output columns per CTA
-constexpr int NUM_THREADS = 192;  // warps 0-3 softmax, 4 TMA, 5 MMA
-constexpr int WARP_TMA = 4;
+constexpr int NUM_THREADS = 224;  // warps 0-3 softmax, 4 TMA (query, scores), 5 MMA, 6 TMA (values)
+constexpr int WARP_KEY = 4;
 constexpr int WARP_MMA = 5;
+constexpr int WARP_VAL = 6;
 constexpr int TMEM_COLS = 512;
 constexpr int COL_Q = 0;          // query chunks: columns [0, 32 NCH), NCH <= 9
 constexpr int COL_S = 288;        // S: 64 fp32 columns
-constexpr int COL_P = 352;        // P: 64 keys as 32 packed columns
 constexpr int COL_O = 384;        // output slice: columns [384, 512)
+constexpr int NPS = 8;            // P slots (a multiple of NH: slot t mod 8 has one writer)
+constexpr int NVS = 3;            // value stages
+constexpr int NSR = 4;            // score-chunk ring slots
+constexpr int BAR_SOFTMAX = 1;    // named barrier of the 128 softmax threads
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -68,42 +104,56 @@ template <int R, int PD>
 struct Cfg {
   static_assert(R == 256 || R == 512, "tensor-core MLA latent ranks are 256 and 512");
   static_assert(PD == 0 || PD == 64, "tensor-core MLA positional widths are 0 and 64");
-  static constexpr int NH = R / OC;          // CTAs per row block (output slices)
+  static constexpr int NH = R / OC;          // CTAs per cluster (output slices)
   static constexpr int NCH = (R + PD) / 64;  // 64-wide chunks of a key row
   static constexpr int NCH_LAT = R / 64;     // ... of which latent
   static constexpr int QCH_BYTES = BM * 128;
   static constexpr int KCH_BYTES = BN * 128;
-  static constexpr int STAGE_BYTES = NCH * KCH_BYTES;
-  static constexpr int RESERVE = 1024 + 256;  // base alignment + barriers
-  static constexpr int ST_FIT = (SMEM_LIMIT - RESERVE) / STAGE_BYTES;
-  static constexpr int STAGES = ST_FIT > 6 ? 6 : ST_FIT;
-  // the query passes through ring stages 1.. on its way to tensor memory
-  static constexpr int OFF_STAGING = STAGE_BYTES;
-  static_assert(STAGES >= 3, "ring too small");
-  static_assert(OFF_STAGING + NCH * QCH_BYTES <= STAGES * STAGE_BYTES, "staging overflows the ring");
-  static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
-  static constexpr int BAR_FULL = 0, BAR_EMPTY = STAGES, BAR_QST = 2 * STAGES, BAR_QT = BAR_QST + 1,
-                       BAR_S = BAR_QST + 2, BAR_SFREE = BAR_S + 1, BAR_P = BAR_S + 2, BAR_PV = BAR_S + 3,
-                       BAR_DONE = BAR_S + 4, NUM_BARS = BAR_DONE + 1;
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int ML_BYTES = BM * 8;
+  static constexpr int V_BYTES = (OC / 64) * KCH_BYTES;
+  static constexpr int OFF_P = 0;
+  static constexpr int OFF_V = OFF_P + NPS * P_BYTES;
+  static constexpr int OFF_SR = OFF_V + NVS * V_BYTES;
+  static constexpr int OFF_ML = OFF_SR + NSR * KCH_BYTES;
+  static constexpr int OFF_M0 = OFF_ML + NPS * ML_BYTES;
+  static constexpr int OFF_BAR = OFF_M0 + NH * BM * 4;
+  // the staged query may cover the P slots and the value stages, not the score ring
+  static_assert(NCH * QCH_BYTES <= OFF_SR, "query staging overlaps the score ring");
+  static_assert(NPS % NH == 0, "a P slot has one writer");
+  enum : int {
+    BAR_QST = 0,
+    BAR_QT,
+    BAR_S,
+    BAR_SFREE,
+    BAR_DONE,
+    BAR_SR_FULL,
+    BAR_SR_EMPTY = BAR_SR_FULL + NSR,
+    BAR_V_FULL = BAR_SR_EMPTY + NSR,
+    BAR_V_EMPTY = BAR_V_FULL + NVS,
+    BAR_P_ARR = BAR_V_EMPTY + NVS,      // a peer's P tile and (m, l) have landed in the slot
+    BAR_P_READY = BAR_P_ARR + NPS,      // the slot's tile is reconciled: P . V may read it
+    BAR_PV_DONE = BAR_P_READY + NPS,    // this CTA's P . V of the slot's tile is complete
+    BAR_SLOT_FREE = BAR_PV_DONE + NPS,  // every CTA's P . V of the slot's tile is complete
+    BAR_RECV = BAR_SLOT_FREE + NPS,     // every peer has received this CTA's tile in the slot
+    NUM_BARS = BAR_RECV + NPS
+  };
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
-  static_assert(COL_Q + NCH * 32 <= COL_S && COL_O + OC <= TMEM_COLS, "tensor memory");
+  static_assert(SMEM_BYTES + 4 * (kMaxRanked + 1) <= SMEM_LIMIT, "shared memory");
+  static_assert(COL_Q + NCH * 32 <= COL_S && COL_S + BN <= COL_O && COL_O + OC <= TMEM_COLS, "tensor memory");
 };
 
 struct MWork {
-  int s, sp, h, q_lo, nq, row0, L, t0, n, nfull;
+  int s, sp, q_lo, nq, row0, L, t0, n, nfull;
 };
 
-// blockIdx.x -> (sequence, 128-row block, split, output slice); the slice is
-// fastest so that the CTAs sharing key tiles run side by side. LPT: the
-// sequences longest first, for calls with one row block per sequence (decode).
+// cluster -> (sequence, 128-row block, split). LPT: the sequences longest
+// first, for calls with one row block per sequence (decode).
 template <int NH, bool LPT>
 __device__ __forceinline__ MWork make_mwork(const PagedParams& pp, int rblocks) {
   MWork w;
-  int item = static_cast<int>(blockIdx.x);
-  w.h = item % NH;
-  item /= NH;
+  int item = static_cast<int>(blockIdx.x) / NH;
   w.sp = item % pp.num_splits;
   item /= pp.num_splits;
   const int rb = item % rblocks;
@@ -135,11 +185,12 @@ __device__ __forceinline__ MWork make_mwork(const PagedParams& pp, int rblocks) 
 }
 
 template <int R, int PD, bool BF16, bool LPT>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
                   const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_kp,
                   const PagedParams pp, void* out, float* lse, int rblocks) {
   using C = Cfg<R, PD>;
+  constexpr int NH = C::NH;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -148,27 +199,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = pp.Hq;
-  const MWork w = make_mwork<C::NH, LPT>(pp, rblocks);
+  const int h = static_cast<int>(cluster_rank());  // output slice
+  const MWork w = make_mwork<NH, LPT>(pp, rblocks);
   const int rows_seq = w.nq * H;
-  if (w.row0 >= rows_seq) return;  // no rows here (CTA-uniform)
+  // every CTA of the cluster has the same work: they take the same exits,
+  // before any traffic between them
+  if (w.row0 >= rows_seq) return;
   const int64_t rows_total = static_cast<int64_t>(pp.num_queries) * H;
-  const int64_t grow0 = static_cast<int64_t>(w.q_lo) * H + w.row0;  // first global row of the CTA
+  const int64_t grow0 = static_cast<int64_t>(w.q_lo) * H + w.row0;  // first global row of the block
   const bool partial = pp.num_splits > 1;
 
-  if (w.n == 0) {  // no key tile in this run (CTA-uniform): the rows see no key here
+  if (w.n == 0) {  // no key tile in this run: the rows see no key here
     if (warp < 4) {
       const int r = warp * 32 + lane;
       const int64_t grow = grow0 + r;
       if (w.row0 + r < rows_seq && in_bounds(pp.status, grow, rows_total)) {
         if (partial) {
-          if (w.h == 0) pp.ws_ml[w.sp * rows_total + grow] = make_float2(-INFINITY, 0.f);
+          if (h == 0) pp.ws_ml[w.sp * rows_total + grow] = make_float2(-INFINITY, 0.f);
         } else {
           const uint16_t nan16 = BF16 ? 0x7fc0u : 0x7e00u;
           const uint32_t nn = static_cast<uint32_t>(nan16) * 0x10001u;
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (grow * R + w.h * OC) * 2);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (grow * R + h * OC) * 2);
 #pragma unroll 4
           for (int u = 0; u < OC / 8; ++u) dst[u] = make_uint4(nn, nn, nn, nn);
-          if (lse && w.h == 0) lse[grow] = -INFINITY;
+          if (lse && h == 0) lse[grow] = -INFINITY;
         }
       }
     }
@@ -176,35 +230,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar(C::BAR_FULL + s), 1);
-      mbar_init(bar(C::BAR_EMPTY + s), 1);
-    }
     mbar_init(bar(C::BAR_QST), 1);
     mbar_init(bar(C::BAR_QT), BM);
     mbar_init(bar(C::BAR_S), 1);
     mbar_init(bar(C::BAR_SFREE), BM);
-    mbar_init(bar(C::BAR_P), BM);
-    mbar_init(bar(C::BAR_PV), 1);
     mbar_init(bar(C::BAR_DONE), 1);
+    for (int i = 0; i < NSR; ++i) {
+      mbar_init(bar(C::BAR_SR_FULL + i), 1);
+      mbar_init(bar(C::BAR_SR_EMPTY + i), 1);
+    }
+    for (int i = 0; i < NVS; ++i) {
+      mbar_init(bar(C::BAR_V_FULL + i), 1);
+      mbar_init(bar(C::BAR_V_EMPTY + i), 1);
+    }
+    for (int i = 0; i < NPS; ++i) {
+      mbar_init(bar(C::BAR_P_ARR + i), 1);  // the local expect_tx arrival + the peer's bytes
+      mbar_init(bar(C::BAR_P_READY + i), BM);
+      mbar_init(bar(C::BAR_PV_DONE + i), 1);
+      mbar_init(bar(C::BAR_SLOT_FREE + i), NH);  // one commit from every CTA of the cluster
+      mbar_init(bar(C::BAR_RECV + i), NH - 1);   // one arrival from every peer
+    }
     mbar_init_fence();
+    // the first delivery into every slot a peer writes
+    for (int i = 0; i < NPS; ++i)
+      if (i % NH != h) mbar_arrive_expect_tx(bar(C::BAR_P_ARR + i), C::P_BYTES + C::ML_BYTES);
   }
   if (warp == WARP_MMA) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_arrive();  // every CTA's barriers exist before any remote access
+  cluster_wait();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   auto fail = [&]() {
     if (pp.status) atomicOr(pp.status, STATUS_TIMEOUT);
   };
   const int n = w.n;
+  const int32_t* table = pp.block_table + static_cast<size_t>(w.s) * pp.max_pages;
+  const int P = pp.page_size;
+  const int box_rows = P < BN ? P : BN;
+  const int boxes = BN / box_rows;
 
-  if (warp == WARP_TMA) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
+  if (warp >= 4) {
+    cluster_arrive();  // the exchange of first-tile maxima: nothing to send from these warps
+    if (warp == WARP_KEY && lane == 0) {
+      // ------------------------------------------------ TMA: query, own score chunks
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_lat);
       if constexpr (PD > 0) {
@@ -214,87 +286,194 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int gy = static_cast<int>(grow0);
       mbar_arrive_expect_tx(bar(C::BAR_QST), C::NCH * C::QCH_BYTES);
       for (int c = 0; c < C::NCH; ++c) {
-        const uint32_t dst = sb + C::OFF_STAGING + c * C::QCH_BYTES;
+        const uint32_t dst = sb + c * C::QCH_BYTES;
         if (c < C::NCH_LAT) tma_load_2d(dst, &tm_q, bar(C::BAR_QST), c * 64, gy);
         else tma_load_2d(dst, &tm_qp, bar(C::BAR_QST), (c - C::NCH_LAT) * 64, gy);
       }
-      const int32_t* table = pp.block_table + static_cast<size_t>(w.s) * pp.max_pages;
-      const int P = pp.page_size;
-      const int box_rows = P < BN ? P : BN;
-      const int boxes = BN / box_rows;
       bool ok = true;
-      int issued = 0;
-      for (int i = 0; i < n && ok; ++i, ++issued) {
-        const int st = i % C::STAGES;
-        // stages 1.. hold the staged query until it is in tensor memory
-        if (i == 1 && !mbar_wait(bar(C::BAR_QT), 0)) { ok = false; break; }
-        if (!mbar_wait(bar(C::BAR_EMPTY + st), ((i / C::STAGES) & 1) ^ 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(C::BAR_FULL + st), C::STAGE_BYTES);
-        const uint32_t base = sb + st * C::STAGE_BYTES;
-        for (int b = 0; b < boxes; ++b) {
-          const int key = (w.t0 + i) * BN + b * box_rows;
-          const int pidx = key / P;
-          const int page = pidx < pp.max_pages ? __ldg(table + pidx) : -1;  // -1: zero-filled box
-          const int y = key - pidx * P;
-          // checked build: the box lands inside its chunk of the ring stage (a
-          // skipped copy leaves the stage's barrier to time out)
-          if (!range_in_bounds(pp.status, b * box_rows, box_rows, BN)) continue;
-          for (int c = 0; c < C::NCH; ++c) {
-            const uint32_t dst = base + c * C::KCH_BYTES + b * box_rows * 128;
-            if (c < C::NCH_LAT) tma_load_3d(dst, &tm_lat, bar(C::BAR_FULL + st), c * 64, y, page);
-            else tma_load_3d(dst, &tm_kp, bar(C::BAR_FULL + st), (c - C::NCH_LAT) * 64, y, page);
+      int cnt = 0;
+      // page ids of the own tile being loaded (cur) and of the next one (nxt),
+      // read one own tile ahead so that no table read stalls a load; -1 (past
+      // the table) loads zeros
+      int cur[8], nxt[8];
+      auto read_pages = [&](int d, int (&dst)[8]) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          dst[b] = -1;
+          if (b < boxes && d < n) {
+            const int pidx = ((w.t0 + d) * BN + b * box_rows) / P;
+            if (pidx < pp.max_pages) dst[b] = __ldg(table + pidx);
+          }
+        }
+      };
+      read_pages(h, nxt);
+      for (int d = h; d < n && ok; d += NH) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) cur[b] = nxt[b];
+        read_pages(d + NH, nxt);
+        for (int c = 0; c < C::NCH; ++c, ++cnt) {
+          const int slot = cnt % NSR;
+          if (!mbar_wait(bar(C::BAR_SR_EMPTY + slot), ((cnt / NSR) & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::BAR_SR_FULL + slot), C::KCH_BYTES);
+          const uint32_t base = sb + C::OFF_SR + slot * C::KCH_BYTES;
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            if (b >= boxes) break;
+            const int key = (w.t0 + d) * BN + b * box_rows;
+            const int y = key - (key / P) * P;
+            // checked build: the box lands inside its ring slot (a skipped copy
+            // leaves the slot's barrier to time out)
+            if (!range_in_bounds(pp.status, b * box_rows, box_rows, BN)) continue;
+            const uint32_t dst = base + b * box_rows * 128;
+            if (c < C::NCH_LAT) tma_load_3d(dst, &tm_lat, bar(C::BAR_SR_FULL + slot), c * 64, y, cur[b]);
+            else tma_load_3d(dst, &tm_kp, bar(C::BAR_SR_FULL + slot), (c - C::NCH_LAT) * 64, y, cur[b]);
+          }
+        }
+        // L2 prefetch of the next own tile (pages past the table or the cache are skipped)
+        if (d + NH < n) {
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            if (b >= boxes) break;
+            if (nxt[b] < 0 || nxt[b] >= pp.num_pages) continue;
+            const int key = (w.t0 + d + NH) * BN + b * box_rows;
+            const int y = key - (key / P) * P;
+            for (int c = 0; c < C::NCH; ++c) {
+              if (c < C::NCH_LAT) tma_prefetch_3d(&tm_lat, c * 64, y, nxt[b]);
+              else tma_prefetch_3d(&tm_kp, (c - C::NCH_LAT) * 64, y, nxt[b]);
+            }
           }
         }
       }
       if (!ok) fail();
       // the CTA must not retire with copies in flight
-      for (int st = 0; st < C::STAGES && st < issued; ++st) {
-        const int fills = (issued - st + C::STAGES - 1) / C::STAGES;
-        if (!mbar_wait(bar(C::BAR_FULL + st), (fills - 1) & 1)) fail();
+      for (int slot = 0; slot < NSR && slot < cnt; ++slot) {
+        const int fills = (cnt - slot + NSR - 1) / NSR;
+        if (!mbar_wait(bar(C::BAR_SR_FULL + slot), (fills - 1) & 1)) fail();
       }
       if (!mbar_wait(bar(C::BAR_QST), 0)) fail();
-    }
-    __syncwarp();
-  } else if (warp == WARP_MMA) {
-    if (lane == 0) {
+    } else if (warp == WARP_VAL && lane == 0) {
+      // ------------------------------------------------ TMA: own value chunks of every tile
+      // page ids of tiles i (cur), i + 1 and i + 2: read two tiles ahead
+      int cur[8], nx1[8], nx2[8];
+      auto read_pages = [&](int i, int (&dst)[8]) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          dst[b] = -1;
+          if (b < boxes && i < n) {
+            const int pidx = ((w.t0 + i) * BN + b * box_rows) / P;
+            if (pidx < pp.max_pages) dst[b] = __ldg(table + pidx);
+          }
+        }
+      };
+      read_pages(0, nx1);
+      read_pages(1, nx2);
+      bool ok = mbar_wait(bar(C::BAR_QT), 0);  // the staged query covers the value stages
+      int issued = 0;
+      for (int i = 0; i < n && ok; ++i, ++issued) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          cur[b] = nx1[b];
+          nx1[b] = nx2[b];
+        }
+        read_pages(i + 2, nx2);
+        const int st = i % NVS;
+        if (!mbar_wait(bar(C::BAR_V_EMPTY + st), ((i / NVS) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(C::BAR_V_FULL + st), C::V_BYTES);
+        const uint32_t base = sb + C::OFF_V + st * C::V_BYTES;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (b >= boxes) break;
+          const int key = (w.t0 + i) * BN + b * box_rows;
+          const int y = key - (key / P) * P;
+          if (!range_in_bounds(pp.status, b * box_rows, box_rows, BN)) continue;
+#pragma unroll
+          for (int c2 = 0; c2 < OC / 64; ++c2)
+            tma_load_3d(base + c2 * C::KCH_BYTES + b * box_rows * 128, &tm_lat, bar(C::BAR_V_FULL + st),
+                        (h * (OC / 64) + c2) * 64, y, cur[b]);
+        }
+      }
+      if (!ok) fail();
+      for (int st = 0; st < NVS && st < issued; ++st) {
+        const int fills = (issued - st + NVS - 1) / NVS;
+        if (!mbar_wait(bar(C::BAR_V_FULL + st), (fills - 1) & 1)) fail();
+      }
+    } else if (warp == WARP_MMA && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t idesc_s = make_idesc_f16(BF16, BM, BN, false);
       constexpr uint32_t idesc_pv = make_idesc_f16(BF16, BM, OC, true);
-      constexpr int ST = C::STAGES;
-      constexpr uint32_t STAGE16 = C::STAGE_BYTES >> 4;
       constexpr uint32_t KCH16 = C::KCH_BYTES >> 4;
-      constexpr uint32_t VSTEP16 = (16 * 128) >> 4;
+      constexpr uint32_t P16 = C::P_BYTES >> 4;
+      constexpr uint32_t V16 = C::V_BYTES >> 4;
+      constexpr uint32_t VSTEP16 = (16 * 128) >> 4;  // 16 keys of an MN-major value chunk
+      const uint64_t d_sr = smem_desc(sb + C::OFF_SR, 16, 1024, 2u);
+      const uint64_t d_p = smem_desc(sb + C::OFF_P, 16, 1024, 2u);
+      const uint64_t d_v = smem_desc(sb + C::OFF_V, C::KCH_BYTES, 1024, 2u);
+      constexpr uint16_t all = static_cast<uint16_t>((1u << NH) - 1u);
+      // Issued as their inputs arrive: the score MMAs of the CTA's next own tile
+      // chunk by chunk (once the softmax has read the previous own S), and
+      // P . V of every tile in tile order. The two use different accumulators,
+      // so neither waits for the other.
       bool ok = mbar_wait(bar(C::BAR_QT), 0);
       tc_fence_after();
-      const uint64_t dk = smem_desc(sb, 16, 1024, 2u);
-      const uint64_t dv = smem_desc(sb + w.h * (OC / 64) * C::KCH_BYTES, C::KCH_BYTES, 1024, 2u);
-      for (int i = 0; i <= n && ok; ++i) {
-        if (i < n) {
-          const int st = i % ST;
-          if (!mbar_wait(bar(C::BAR_FULL + st), (i / ST) & 1)) { ok = false; break; }
-          // S is single-buffered: the softmax must have read S(i-1)
-          if (i > 0 && !mbar_wait(bar(C::BAR_SFREE), (i - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t b0 = dk + st * STAGE16;
-#pragma unroll
-          for (int c = 0; c < C::NCH; ++c) {
+      int cnt = 0;        // score chunks issued
+      int s_tile = h;     // own tile whose scores come next
+      int s_k = 0;        // its index among the own tiles
+      int s_c = 0;        // its next chunk
+      bool s_free = true; // S may be overwritten (the softmax has read the previous own S)
+      int j = 0;          // next tile for P . V
+      uint32_t idle = 0;
+      unsigned long long t_idle = 0;
+      while (ok && (j < n || s_tile < n)) {
+        bool progress = false;
+        if (s_tile < n) {
+          if (!s_free && mbar_test_nb(bar(C::BAR_SFREE), (s_k - 1) & 1)) s_free = true;
+          const int slot = cnt % NSR;
+          if (s_free && mbar_test_nb(bar(C::BAR_SR_FULL + slot), (cnt / NSR) & 1)) {
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_ts(tmem + COL_S, tmem + COL_Q + c * 32 + kk * 8, b0 + c * KCH16 + kk * 2, idesc_s,
-                      (c | kk) ? 1u : 0u);
+              umma_ts(tmem + COL_S, tmem + COL_Q + s_c * 32 + kk * 8, d_sr + slot * KCH16 + kk * 2, idesc_s,
+                      (s_c | kk) ? 1u : 0u);
+            umma_commit(bar(C::BAR_SR_EMPTY + slot));
+            ++cnt;
+            if (++s_c == C::NCH) {
+              umma_commit(bar(C::BAR_S));
+              s_c = 0;
+              s_tile += NH;
+              ++s_k;
+              s_free = false;
+            }
+            progress = true;
           }
-          umma_commit(bar(C::BAR_S));
         }
-        if (i >= 1) {
-          const int j = i - 1;
-          if (!mbar_wait(bar(C::BAR_P), j & 1)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t b0 = dv + (j % ST) * STAGE16;
+        if (j < n) {
+          const int slot = j % NPS, st = j % NVS;
+          if (mbar_test_nb(bar(C::BAR_P_READY + slot), (j / NPS) & 1) &&
+              mbar_test_nb(bar(C::BAR_V_FULL + st), (j / NVS) & 1)) {
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            umma_ts(tmem + COL_O, tmem + COL_P + kk * 8, b0 + kk * VSTEP16, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar(C::BAR_PV));
-          umma_commit(bar(C::BAR_EMPTY + j % ST));
+            for (int kk = 0; kk < BN / 16; ++kk)
+              umma_ss(tmem + COL_O, d_p + slot * P16 + kk * 2, d_v + st * V16 + kk * VSTEP16, idesc_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(bar(C::BAR_V_EMPTY + st));
+            umma_commit(bar(C::BAR_PV_DONE + slot));
+            umma_commit_mc(bar(C::BAR_SLOT_FREE + slot), all);
+            ++j;
+            progress = true;
+          }
+        }
+        if (progress) {
+          idle = 0;
+        } else if (++idle == 1) {
+          t_idle = globaltimer_ns();
+        } else if ((idle & 255u) == 0 && globaltimer_ns() - t_idle > WAIT_LIMIT_NS) {
+          ok = false;
         }
       }
       if (!ok) fail();
@@ -302,15 +481,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
     }
     __syncwarp();
+    cluster_wait();
   } else {
     // -------------------------------------------------------------- softmax
-    const int r = warp * 32 + lane;  // row within the CTA = tensor-memory lane
+    const int r = warp * 32 + lane;  // row within the block = tensor-memory lane
     const bool row_ok = w.row0 + r < rows_seq;
     const int64_t grow = grow0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tQ = tmem + lane_off + COL_Q;
     const uint32_t tS = tmem + lane_off + COL_S;
-    const uint32_t tP = tmem + lane_off + COL_P;
     const uint32_t tO = tmem + lane_off + COL_O;
     const int tq = (w.row0 + r) / H;
     const int pos = !row_ok ? -1
@@ -320,13 +499,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int causal_lim = pp.causal ? pos : 0x7fffffff;
     const int key_lim = w.L;
     const float sc = pp.scale_log2;
+    float2* ml = reinterpret_cast<float2*>(smem + C::OFF_ML);
     bool failed = false;
     // the query: staged shared memory (128-byte swizzled rows) -> tensor memory
     {
       const bool ok = mbar_wait(bar(C::BAR_QST), 0);
       if (__any_sync(0xffffffffu, !ok)) failed = true;
       if (!failed) {
-        const uint8_t* row = smem + C::OFF_STAGING + r * 128;
+        const uint8_t* row = smem + r * 128;
 #pragma unroll 1
         for (int c = 0; c < C::NCH; ++c) {
           uint32_t wd[32];
@@ -345,87 +525,213 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(C::BAR_QT));
     }
-    float m_run = -INFINITY, l_run = 0.f;
-    for (int i = 0; i < n && !failed; ++i) {
-      const bool ok = mbar_wait(bar(C::BAR_S), i & 1);
-      if (__any_sync(0xffffffffu, !ok)) { failed = true; break; }
-      tc_fence_after();
-      float s[BN];
-      {
+    float s[BN];
+    float tmax = -INFINITY;
+    // scores of own tile d (the k-th): load, free S for the next own tile, mask; max
+    auto load_scores = [&](int d, int k) {
+      if (!failed) {
+        const bool ok = mbar_wait(bar(C::BAR_S), k & 1);
+        if (__any_sync(0xffffffffu, !ok)) failed = true;
+      }
+      if (!failed) {
+        tc_fence_after();
         uint32_t sr[2][32];
         tmem_ld32(tS, sr[0]);
         tmem_ld32(tS + 32, sr[1]);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < BN; ++k) s[k] = __uint_as_float(sr[k >> 5][k & 31]);
+        for (int e = 0; e < BN; ++e) s[e] = __uint_as_float(sr[e >> 5][e & 31]);
       }
       tc_fence_before();
-      mbar_arrive(bar(C::BAR_SFREE));  // the next tile's scores may overwrite S
-      const int tile = w.t0 + i;
+      mbar_arrive(bar(C::BAR_SFREE));
+      if (failed) return;
+      const int tile = w.t0 + d;
       if (tile >= w.nfull) {
         const int key0 = tile * BN;
 #pragma unroll
-        for (int k = 0; k < BN; ++k) {
-          const int key = key0 + k;
-          if (key >= key_lim || key > causal_lim) s[k] = -INFINITY;
+        for (int e = 0; e < BN; ++e) {
+          const int key = key0 + e;
+          if (key >= key_lim || key > causal_lim) s[e] = -INFINITY;
         }
       }
       float c0 = fmax3(s[0], s[1], s[2]), c1 = fmax3(s[3], s[4], s[5]);
 #pragma unroll
-      for (int k = 6; k < 62; k += 4) {
-        c0 = fmax3(c0, s[k], s[k + 1]);
-        c1 = fmax3(c1, s[k + 2], s[k + 3]);
+      for (int e = 6; e < 62; e += 4) {
+        c0 = fmax3(c0, s[e], s[e + 1]);
+        c1 = fmax3(c1, s[e + 2], s[e + 3]);
       }
-      const float m_tile = fmax3(c0, c1, fmaxf(s[62], s[63])) * sc;
-      const bool need = m_tile > m_run + RESCALE_LOG2;
-      float alpha = 1.f;
-      if (need) {
-        alpha = fast_exp2(m_run - m_tile);
-        m_run = m_tile;
-        l_run *= alpha;
-      }
-      const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-      float2 sum_a = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
-      uint32_t pk[32];
+      tmax = fmax3(c0, c1, fmaxf(s[62], s[63])) * sc;
+    };
+    if (h < n) load_scores(h, 0);
+    // the row maxima of every CTA's first tile -> a common starting reference
+    __syncwarp();
+    for (int c = 0; c < NH; ++c)
+      st_cluster_f32(peer_addr(sb + C::OFF_M0 + (h * BM + r) * 4, c), failed ? -INFINITY : tmax);
+    cluster_arrive();
+    cluster_wait();
+    float m_O = -INFINITY, l = 0.f;
+    {
+      const float* m0 = reinterpret_cast<const float*>(smem + C::OFF_M0);
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        const float2 xa = ffma2(make_float2(s[2 * k], s[2 * k + 1]), make_float2(sc, sc), make_float2(neg_m, neg_m));
-        const float2 xb =
-            ffma2(make_float2(s[2 * k + 2], s[2 * k + 3]), make_float2(sc, sc), make_float2(neg_m, neg_m));
-        const float2 pa = make_float2(fast_exp2(xa.x), fast_exp2(xa.y));
-        const float2 pb = make_float2(fast_exp2(xb.x), fast_exp2(xb.y));
-        sum_a = fadd2(sum_a, pa);
-        sum_b = fadd2(sum_b, pb);
-        pk[k] = pack2<BF16>(pa.x, pa.y);
-        pk[k + 1] = pack2<BF16>(pb.x, pb.y);
+      for (int c = 0; c < NH; ++c) m_O = fmaxf(m_O, m0[c * BM + r]);
+    }
+
+    // own tile d: P and (m, l) into slot d % NPS here, then copied to the peers
+    auto own_tile = [&](int d, int k) {
+      if (k > 0) load_scores(d, k);
+      const int slot = d % NPS;
+      float m_ref = -INFINITY, l_src = 0.f;
+      uint32_t pk[32];
+      if (!failed) {
+        m_ref = (m_O == -INFINITY || tmax > m_O + RESCALE_LOG2) ? tmax : m_O;
+        const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        float2 sum_a = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float2 xa =
+              ffma2(make_float2(s[2 * e], s[2 * e + 1]), make_float2(sc, sc), make_float2(neg_m, neg_m));
+          const float2 xb =
+              ffma2(make_float2(s[2 * e + 2], s[2 * e + 3]), make_float2(sc, sc), make_float2(neg_m, neg_m));
+          const float2 pa = make_float2(fast_exp2(xa.x), fast_exp2(xa.y));
+          const float2 pb = make_float2(fast_exp2(xb.x), fast_exp2(xb.y));
+          sum_a = fadd2(sum_a, pa);
+          sum_b = fadd2(sum_b, pb);
+          pk[e] = pack2<BF16>(pa.x, pa.y);
+          pk[e + 1] = pack2<BF16>(pb.x, pb.y);
+        }
+        l_src = (sum_a.x + sum_a.y) + (sum_b.x + sum_b.y);
+        // the slot's previous tile has been multiplied in every CTA
+        if (d >= NPS) {
+          const bool ok = mbar_wait_cluster(bar(C::BAR_SLOT_FREE + slot), ((d / NPS) - 1) & 1);
+          if (__any_sync(0xffffffffu, !ok)) failed = true;
+        }
       }
-      l_run += (sum_a.x + sum_a.y) + (sum_b.x + sum_b.y);
-      // P is single-buffered and O is read by P . V: wait for the previous one
-      if (i > 0) {
-        const bool pv = mbar_wait(bar(C::BAR_PV), (i - 1) & 1);
-        if (__any_sync(0xffffffffu, !pv)) { failed = true; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {  // O holds earlier tiles relative to the old maximum
+      if (!failed) {
+        uint8_t* prow = smem + C::OFF_P + slot * C::P_BYTES + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        ml[slot * BM + r] = make_float2(m_ref, l_src);
+        fence_proxy_async_smem();  // for this CTA's MMA and the copies to the peers
+      }
+      if (bar_red_or(BAR_SOFTMAX, BM, failed)) failed = true;
+      if (!failed && r == 0) {
+        const uint32_t src_p = sb + C::OFF_P + slot * C::P_BYTES;
+        const uint32_t src_ml = sb + C::OFF_ML + slot * C::ML_BYTES;
+        for (int c = 1; c < NH; ++c) {
+          const uint32_t peer = static_cast<uint32_t>((h + c) % NH);
+          const uint32_t pbar = peer_addr(bar(C::BAR_P_ARR + slot), peer);
+          bulk_copy_to_peer(peer_addr(src_p, peer), src_p, C::P_BYTES, pbar);
+          bulk_copy_to_peer(peer_addr(src_ml, peer), src_ml, C::ML_BYTES, pbar);
+        }
+      }
+    };
+
+    // tile j: take its reference and row sum into this CTA's (m_O, l)
+    auto reconcile = [&](int j) {
+      const int slot = j % NPS, wr = j % NH;
+      if (wr != h && !failed) {
+        const bool ok = mbar_wait_cluster(bar(C::BAR_P_ARR + slot), (j / NPS) & 1);
+        if (__any_sync(0xffffffffu, !ok)) failed = true;
+        if (!failed && r == 0) {
+          if (j + NPS < n) mbar_arrive_expect_tx(bar(C::BAR_P_ARR + slot), C::P_BYTES + C::ML_BYTES);
+          mbar_arrive_peer(peer_addr(bar(C::BAR_RECV + slot), static_cast<uint32_t>(wr)));
+        }
+      }
+      bool need_o = false, need_p = false;
+      float alpha = 1.f, beta = 1.f;
+      if (!failed) {
+        const float2 v = ml[slot * BM + r];
+        const float ms = v.x, ls = v.y;
+        if (ls > 0.f) {
+          if (l == 0.f) {  // nothing accumulated yet: the tile's reference becomes the row's
+            m_O = ms;
+            l = ls;
+          } else if (ms > m_O) {
+            alpha = fast_exp2(m_O - ms);
+            l = l * alpha + ls;
+            m_O = ms;
+            need_o = true;
+          } else if (ms < m_O) {
+            beta = fast_exp2(ms - m_O);
+            l += ls * beta;
+            need_p = true;
+          } else {
+            l += ls;
+          }
+        }
+      }
+      if (__any_sync(0xffffffffu, need_o)) {
+        // O holds tiles < j relative to the old reference: after this CTA's P . V of tile j - 1
+        const int pj = j - 1;  // >= 0: a row with l > 0 has reconciled an earlier tile
+        const bool ok = mbar_wait(bar(C::BAR_PV_DONE + pj % NPS), (pj / NPS) & 1);
+        if (__any_sync(0xffffffffu, !ok)) failed = true;
+        if (!failed) {
+          tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < OC / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(tO + 32 * c, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              const float2 x = fmul2(make_float2(__uint_as_float(o[k]), __uint_as_float(o[k + 1])),
+            for (int e = 0; e < 32; e += 2) {
+              const float2 x = fmul2(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])),
                                      make_float2(alpha, alpha));
-              o[k] = __float_as_uint(x.x);
-              o[k + 1] = __float_as_uint(x.y);
+              o[e] = __float_as_uint(x.x);
+              o[e + 1] = __float_as_uint(x.y);
             }
             tmem_st32(tO + 32 * c, o);
           }
+          tmem_wait_st();
+          tc_fence_before();
         }
       }
-      tmem_st32(tP, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::BAR_P));
+      bool bad = false;
+      if (need_p && !failed) {
+        // this row of P was computed against a smaller reference: scale it down;
+        // an own tile only once every peer's copy has landed
+        bool ok = true;
+        if (wr == h) ok = mbar_wait_cluster(bar(C::BAR_RECV + slot), (j / NPS) & 1);
+        if (ok) {
+          uint8_t* prow = smem + C::OFF_P + slot * C::P_BYTES + r * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint4* q4 = reinterpret_cast<uint4*>(prow + (u << 4));
+            uint4 v = *q4;
+            uint32_t* wv = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float lo, hi;
+              if constexpr (BF16) {
+                const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&wv[e]);
+                lo = __low2float(b2);
+                hi = __high2float(b2);
+              } else {
+                const __half2 b2 = *reinterpret_cast<const __half2*>(&wv[e]);
+                lo = __low2float(b2);
+                hi = __high2float(b2);
+              }
+              wv[e] = pack2<BF16>(lo * beta, hi * beta);
+            }
+            *q4 = v;
+          }
+          fence_proxy_async_smem();
+        } else {
+          bad = true;
+        }
+      }
+      if (__any_sync(0xffffffffu, bad)) failed = true;
+      mbar_arrive(bar(C::BAR_P_READY + slot));
+    };
+
+    // own tiles in order, each followed by the reconciliation of every tile up to it
+    int last = -1;
+    for (int d = h, k = 0; last < n - 1; d += NH, ++k) {
+      if (d < n) own_tile(d, k);
+      const int upto = d < n ? d : n - 1;
+      for (int j = last + 1; j <= upto; ++j) reconcile(j);
+      last = upto;
     }
     // ---------------------------------------------------------------- epilogue
     if (!failed) {
@@ -436,10 +742,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) fail();
     } else {
       tc_fence_after();
-      const bool live = l_run > 0.f;
+      const bool live = l > 0.f;
       const bool row_in = row_ok && in_bounds(pp.status, grow, rows_total);  // checked build
       if (partial) {
-        float4* dst = reinterpret_cast<float4*>(pp.ws_o + (w.sp * rows_total + grow) * R + w.h * OC);
+        float4* dst = reinterpret_cast<float4*>(pp.ws_o + (w.sp * rows_total + grow) * R + h * OC);
 #pragma unroll 1
         for (int c = 0; c < OC / 32; ++c) {
           uint32_t o[32];
@@ -452,11 +758,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                            __uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3]));
           }
         }
-        if (row_in && w.h == 0)
-          pp.ws_ml[w.sp * rows_total + grow] = make_float2(live ? m_run : -INFINITY, live ? l_run : 0.f);
+        if (row_in && h == 0)
+          pp.ws_ml[w.sp * rows_total + grow] = make_float2(live ? m_O : -INFINITY, live ? l : 0.f);
       } else {
-        const float inv = live ? 1.f / l_run : __int_as_float(0x7fc00000);
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (grow * R + w.h * OC) * 2);
+        const float inv = live ? 1.f / l : __int_as_float(0x7fc00000);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (grow * R + h * OC) * 2);
 #pragma unroll 1
         for (int c = 0; c < OC / 32; ++c) {
           uint32_t o[32];
@@ -465,24 +771,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (row_in) {
             uint32_t pkd[16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const float2 x = fmul2(make_float2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])),
+            for (int e = 0; e < 16; ++e) {
+              const float2 x = fmul2(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])),
                                      make_float2(inv, inv));
-              pkd[k] = pack2<BF16>(x.x, x.y);
+              pkd[e] = pack2<BF16>(x.x, x.y);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u)
               dst[c * 4 + u] = make_uint4(pkd[4 * u], pkd[4 * u + 1], pkd[4 * u + 2], pkd[4 * u + 3]);
           }
         }
-        if (row_in && lse && w.h == 0) lse[grow] = live ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+        if (row_in && lse && h == 0) lse[grow] = live ? (m_O + log2f(l)) * LN2 : -INFINITY;
       }
     }
   }
+  // no CTA leaves while a peer may still copy into it or arrive on its barriers
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_arrive();
+  cluster_wait();
   if (warp == WARP_MMA) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }

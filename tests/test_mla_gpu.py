@@ -75,9 +75,10 @@ def test_mla_matches_oracle(w):
 
 
 # Tensor-core kernel (F16/BF16, R in {256, 512}, Pd in {0, 64}, page sizes
-# 8, 16, 32 or multiples of 64): 128-row blocks of (query, head) rows, one CTA
-# per 128-column output slice, 64-key tiles; several tiles and a ragged last
-# tile.
+# 8, 16, 32 or multiples of 64): 128-row blocks of (query, head) rows, a cluster
+# of R/128 CTAs per block (one 128-column output slice each) that deal the
+# 64-key tiles' scores round-robin and exchange the P tiles; several tiles and a
+# ragged last tile.
 TC_CASES = [
     MW("mla_tc_bf16_r512_p64_h128_decode", "bf16", 5, 128, 512, 64, 64, (1, 700), (1, 1), seed=11),
     MW("mla_tc_bf16_r512_p64_h16_p8", "bf16", 4, 16, 512, 64, 8, (30, 400), (1, 3), seed=12),
@@ -104,6 +105,51 @@ def test_mla_tensor_core_splits(splits):
     w2 = MW(f"mla_tc_split{splits}_r256", "f16", 3, 16, 256, 0, 16, (1, 900), (1, 1), seed=50 + splits,
             causal=False)
     check(w2, num_splits=splits)
+
+
+def _scale_key_rows(w, x, factor):
+    """Multiply the latent and positional rows of every cached key by
+    factor(position in its sequence, sequence length), rounded back to the
+    storage dtype."""
+    def widen(a):
+        if w.dtype == "bf16":
+            return (a.astype(np.uint32) << 16).view(np.float32)
+        return a.astype(np.float32)
+    lat, kp = widen(x["latent"]).copy(), widen(x["kpos"]).copy()
+    P = w.page_size
+    for s_ in range(len(x["seq_lens"])):
+        L = int(x["seq_lens"][s_])
+        for j in range(L):
+            pg = x["block_table"][s_, j // P]
+            lat[pg, j % P] *= factor(j, L)
+            kp[pg, j % P] *= factor(j, L)
+    x["latent"], x["kpos"] = synth.to_storage(lat, w.dtype), synth.to_storage(kp, w.dtype)
+    return x
+
+
+@pytest.mark.parametrize("dtype,R,Pd,kind", [("bf16", 512, 64, "grow"), ("f16", 256, 0, "grow"),
+                                             ("bf16", 512, 64, "spike"), ("bf16", 512, 0, "shrink")])
+def test_mla_tensor_core_reference_changes(dtype, R, Pd, kind):
+    # The CTAs of a cluster compute the scores of alternate 64-key tiles, each
+    # against a reference row maximum shared through the P tiles. Scores that
+    # grow along the sequence (about 4 to 55 in log2 units per tile maximum)
+    # make owners raise the reference mid-run: receivers rescale their output
+    # rows, and tiles made against an older reference are scaled down (the
+    # owner's own copy only after its peers have received it). A spike makes
+    # one tile's maximum jump; shrinking scores keep the first tiles' maxima,
+    # exchanged before the first P, as the reference.
+    w = MW(f"mla_tc_ref_{kind}_{dtype}_r{R}", dtype, 4, 16, R, Pd, 64, (1500, 3200), (1, 1), seed=70 + R + Pd)
+    x = synth.make_mla_inputs(w)
+    if kind == "grow":
+        f = lambda j, L: 1.0 + 15.0 * j / L
+    elif kind == "shrink":
+        f = lambda j, L: 16.0 - 15.0 * j / L
+    else:
+        f = lambda j, L: 40.0 if j == L // 2 else 1.0
+    x = _scale_key_rows(w, x, f)
+    check(w, x)
+    if kind == "grow":
+        check(w, x, num_splits=2)
 
 
 def test_mla_tensor_core_edges():
