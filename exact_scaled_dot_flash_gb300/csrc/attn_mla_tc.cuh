@@ -636,7 +636,7 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (__any_sync(0xffffffffu, !ok)) failed = true;
         if (!failed && r == 0) {
           if (j + NPS < n) mbar_arrive_expect_tx(bar(C::BAR_P_ARR + slot), C::P_BYTES + C::ML_BYTES);
-          mbar_arrive_peer(peer_addr(bar(C::BAR_RECV + slot), static_cast<uint32_t>(wr)));
+          mbar_arrive_peer_relaxed(peer_addr(bar(C::BAR_RECV + slot), static_cast<uint32_t>(wr)));
         }
       }
       bool need_o = false, need_p = false;

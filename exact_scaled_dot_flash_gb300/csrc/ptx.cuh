@@ -403,8 +403,11 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, ui
                : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_peer(uint32_t bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+// Arrive on another CTA's mbarrier without release semantics: for an arrival
+// that publishes no data of this thread (a cluster-scope release here cost
+// about a thousand cycles per arrival in the MLA kernel).
+__device__ __forceinline__ void mbar_arrive_peer_relaxed(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Arrive once on the mbarrier at offset `bar` in every CTA of `mask` when every
