@@ -51,8 +51,8 @@
 //
 // Warps: 0-3 softmax (one row per thread; each own tile's scores, then the
 // reconciliation of every tile up to it, in tile order), 4 TMA (the query, then
-// the score chunks of this CTA's tiles, with an L2 prefetch of the next own
-// tile), 6 TMA (this CTA's two value chunks of every tile), 5 MMA issuer. The
+// the score chunks of this CTA's tiles), 6 TMA (this CTA's two value chunks of
+// every tile), 5 MMA issuer. The
 // MMA issuer polls without blocking and issues whatever is ready: the next own
 // tile's score MMAs chunk by chunk once the softmax has read the previous S,
 // and P . V of the tiles in order as their P arrives. An in-order issuer
@@ -330,20 +330,6 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const uint32_t dst = base + b * box_rows * 128;
             if (c < C::NCH_LAT) tma_load_3d(dst, &tm_lat, bar(C::BAR_SR_FULL + slot), c * 64, y, cur[b]);
             else tma_load_3d(dst, &tm_kp, bar(C::BAR_SR_FULL + slot), (c - C::NCH_LAT) * 64, y, cur[b]);
-          }
-        }
-        // L2 prefetch of the next own tile (pages past the table or the cache are skipped)
-        if (d + NH < n) {
-#pragma unroll
-          for (int b = 0; b < 8; ++b) {
-            if (b >= boxes) break;
-            if (nxt[b] < 0 || nxt[b] >= pp.num_pages) continue;
-            const int key = (w.t0 + d + NH) * BN + b * box_rows;
-            const int y = key - (key / P) * P;
-            for (int c = 0; c < C::NCH; ++c) {
-              if (c < C::NCH_LAT) tma_prefetch_3d(&tm_lat, c * 64, y, nxt[b]);
-              else tma_prefetch_3d(&tm_kp, (c - C::NCH_LAT) * 64, y, nxt[b]);
-            }
           }
         }
       }
