@@ -130,8 +130,7 @@ struct Cfg {
     BAR_SR_FULL,
     BAR_SR_EMPTY = BAR_SR_FULL + NSR,
     BAR_V_FULL = BAR_SR_EMPTY + NSR,
-    BAR_V_EMPTY = BAR_V_FULL + NVS,
-    BAR_P_ARR = BAR_V_EMPTY + NVS,      // a peer's P tile and (m, l) have landed in the slot
+    BAR_P_ARR = BAR_V_FULL + NVS,      // a peer's P tile and (m, l) have landed in the slot
     BAR_P_READY = BAR_P_ARR + NPS,      // the slot's tile is reconciled: P . V may read it
     BAR_PV_DONE = BAR_P_READY + NPS,    // this CTA's P . V of the slot's tile is complete
     BAR_SLOT_FREE = BAR_PV_DONE + NPS,  // every CTA's P . V of the slot's tile is complete
@@ -241,7 +240,6 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < NVS; ++i) {
       mbar_init(bar(C::BAR_V_FULL + i), 1);
-      mbar_init(bar(C::BAR_V_EMPTY + i), 1);
     }
     for (int i = 0; i < NPS; ++i) {
       mbar_init(bar(C::BAR_P_ARR + i), 1);  // the local expect_tx arrival + the peer's bytes
@@ -366,7 +364,10 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         read_pages(i + 2, nx2);
         const int st = i % NVS;
-        if (!mbar_wait(bar(C::BAR_V_EMPTY + st), ((i / NVS) & 1) ^ 1)) {
+        // the stage's previous tile, i - NVS, has been multiplied (this CTA's P . V;
+        // its phase is the (i - NVS) / NPS-th of that slot's barrier, and the one
+        // before completed when this producer refilled the stage for i - NVS)
+        if (i >= NVS && !mbar_wait(bar(C::BAR_PV_DONE + (i - NVS) % NPS), ((i - NVS) / NPS) & 1)) {
           ok = false;
           break;
         }
@@ -447,7 +448,6 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             for (int kk = 0; kk < BN / 16; ++kk)
               umma_ss(tmem + COL_O, d_p + slot * P16 + kk * 2, d_v + st * V16 + kk * VSTEP16, idesc_pv,
                       (j > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(bar(C::BAR_V_EMPTY + st));
             umma_commit(bar(C::BAR_PV_DONE + slot));
             umma_commit_mc(bar(C::BAR_SLOT_FREE + slot), all);
             ++j;
