@@ -44,21 +44,23 @@
 //
 // Tensor memory (512 columns): the query chunks (64 dims = 32 packed 16-bit
 // columns each, at most nine), S (64 fp32 columns), the 128-column output slice.
-// Shared memory: 8 P slots (16 KB), 8 (m, l) vectors (1 KB), 3 value stages
-// (this CTA's two latent chunks of a tile, 16 KB), a 4-slot ring of score
+// Shared memory: 8 P slots (16 KB), 8 (m, l) vectors (1 KB), 2 value stages
+// (this CTA's two latent chunks of a tile, 16 KB), a 6-slot ring of score
 // chunks (8 KB), the first tiles' row maxima of every CTA. The query passes
-// through the P slots and value stages on its way to tensor memory.
+// through the P slots and value stages on its way to tensor memory. (Fewer P
+// slots for a deeper score ring measured slower: a slot is reused only once
+// every CTA has multiplied its tile.)
 //
 // Warps: 0-3 softmax (one row per thread; each own tile's scores, then the
 // reconciliation of every tile up to it, in tile order), 4 TMA (the query, then
 // the score chunks of this CTA's tiles), 6 TMA (this CTA's two value chunks of
-// every tile), 5 MMA issuer. The
-// MMA issuer polls without blocking and issues whatever is ready: the next own
-// tile's score MMAs chunk by chunk once the softmax has read the previous S,
-// and P . V of the tiles in order as their P arrives. An in-order issuer
-// (own S, then the P . V of the tiles up to the next own one) makes every CTA's
-// next score tile wait for the peers' P tiles, which wait for theirs: measured
-// a third slower. The producers read each tile's page ids one tile ahead: a table
+// every tile), 5 score-MMA issuer (the next own tile's 36 MMAs, chunk by chunk,
+// once the softmax has read the previous S), 7 P . V issuer (every tile in order
+// as its P arrives). A tcgen05.mma takes ~70 cycles of its issuing thread and a
+// commit ~45: one issuer for both streams spent ~4000 cycles per 4 tiles issuing
+// and made the next own score tile wait behind the P . V of the peers' tiles
+// (one thread in order: a third slower; one thread polling both streams: 25 %
+// slower than two threads). The producers read each tile's page ids one tile ahead: a table
 // read in front of every copy put a global-load latency on each chunk. Key
 // tiles are gathered page by page through 3-D views [pages, page_size, R] and
 // [pages, page_size, Pd] of the caches; an invalid page id loads zeros. Every
@@ -84,17 +86,18 @@ namespace mlatc {
 constexpr int BM = 128;           // (query, head) rows per cluster
 constexpr int BN = 64;            // keys per tile
 constexpr int OC = 128;           // output columns per CTA
-constexpr int NUM_THREADS = 224;  // warps 0-3 softmax, 4 TMA (query, scores), 5 MMA, 6 TMA (values)
+constexpr int NUM_THREADS = 256;  // warps 0-3 softmax, 4 TMA (query, scores), 5 score MMA, 6 TMA (values), 7 P.V MMA
 constexpr int WARP_KEY = 4;
 constexpr int WARP_MMA = 5;
 constexpr int WARP_VAL = 6;
+constexpr int WARP_PV = 7;
 constexpr int TMEM_COLS = 512;
 constexpr int COL_Q = 0;          // query chunks: columns [0, 32 NCH), NCH <= 9
 constexpr int COL_S = 288;        // S: 64 fp32 columns
 constexpr int COL_O = 384;        // output slice: columns [384, 512)
 constexpr int NPS = 8;            // P slots (a multiple of NH: slot t mod 8 has one writer)
-constexpr int NVS = 3;            // value stages
-constexpr int NSR = 4;            // score-chunk ring slots
+constexpr int NVS = 2;            // value stages
+constexpr int NSR = 6;            // score-chunk ring slots
 constexpr int BAR_SOFTMAX = 1;    // named barrier of the 128 softmax threads
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr float LN2 = 0.6931471805599453f;
@@ -233,7 +236,7 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar(C::BAR_QT), BM);
     mbar_init(bar(C::BAR_S), 1);
     mbar_init(bar(C::BAR_SFREE), BM);
-    mbar_init(bar(C::BAR_DONE), 1);
+    mbar_init(bar(C::BAR_DONE), 2);  // both MMA issuers
     for (int i = 0; i < NSR; ++i) {
       mbar_init(bar(C::BAR_SR_FULL + i), 1);
       mbar_init(bar(C::BAR_SR_EMPTY + i), 1);
@@ -391,76 +394,57 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait(bar(C::BAR_V_FULL + st), (fills - 1) & 1)) fail();
       }
     } else if (warp == WARP_MMA && lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
+      // ------------------------------------------------------------ score MMA issuer
       constexpr uint32_t idesc_s = make_idesc_f16(BF16, BM, BN, false);
-      constexpr uint32_t idesc_pv = make_idesc_f16(BF16, BM, OC, true);
       constexpr uint32_t KCH16 = C::KCH_BYTES >> 4;
+      const uint64_t d_sr = smem_desc(sb + C::OFF_SR, 16, 1024, 2u);
+      // score MMAs of the own tiles, chunk by chunk (once the softmax has read
+      // the previous own S); P . V is issued by another warp (WARP_PV): a
+      // tcgen05.mma takes ~70 cycles of its issuing thread
+      bool ok = mbar_wait(bar(C::BAR_QT), 0);
+      tc_fence_after();
+      int cnt = 0;
+      for (int d = h, k = 0; d < n && ok; d += NH, ++k) {
+        if (k > 0 && !mbar_wait(bar(C::BAR_SFREE), (k - 1) & 1)) { ok = false; break; }
+        for (int c = 0; c < C::NCH; ++c, ++cnt) {
+          const int slot = cnt % NSR;
+          if (!mbar_wait(bar(C::BAR_SR_FULL + slot), (cnt / NSR) & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_ts(tmem + COL_S, tmem + COL_Q + c * 32 + kk * 8, d_sr + slot * KCH16 + kk * 2, idesc_s,
+                    (c | kk) ? 1u : 0u);
+          umma_commit(bar(C::BAR_SR_EMPTY + slot));
+        }
+        if (ok) umma_commit(bar(C::BAR_S));
+      }
+      if (!ok) fail();
+      umma_commit(bar(C::BAR_DONE));
+      if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
+    } else if (warp == WARP_PV && lane == 0) {
+      // ------------------------------------------------------------ P . V issuer
+      constexpr uint32_t idesc_pv = make_idesc_f16(BF16, BM, OC, true);
       constexpr uint32_t P16 = C::P_BYTES >> 4;
       constexpr uint32_t V16 = C::V_BYTES >> 4;
       constexpr uint32_t VSTEP16 = (16 * 128) >> 4;  // 16 keys of an MN-major value chunk
-      const uint64_t d_sr = smem_desc(sb + C::OFF_SR, 16, 1024, 2u);
       const uint64_t d_p = smem_desc(sb + C::OFF_P, 16, 1024, 2u);
       const uint64_t d_v = smem_desc(sb + C::OFF_V, C::KCH_BYTES, 1024, 2u);
       constexpr uint16_t all = static_cast<uint16_t>((1u << NH) - 1u);
-      // Issued as their inputs arrive: the score MMAs of the CTA's next own tile
-      // chunk by chunk (once the softmax has read the previous own S), and
-      // P . V of every tile in tile order. The two use different accumulators,
-      // so neither waits for the other.
-      bool ok = mbar_wait(bar(C::BAR_QT), 0);
-      tc_fence_after();
-      int cnt = 0;        // score chunks issued
-      int s_tile = h;     // own tile whose scores come next
-      int s_k = 0;        // its index among the own tiles
-      int s_c = 0;        // its next chunk
-      bool s_free = true; // S may be overwritten (the softmax has read the previous own S)
-      int j = 0;          // next tile for P . V
-      uint32_t idle = 0;
-      unsigned long long t_idle = 0;
-      while (ok && (j < n || s_tile < n)) {
-        bool progress = false;
-        if (s_tile < n) {
-          if (!s_free && mbar_test_nb(bar(C::BAR_SFREE), (s_k - 1) & 1)) s_free = true;
-          const int slot = cnt % NSR;
-          if (s_free && mbar_test_nb(bar(C::BAR_SR_FULL + slot), (cnt / NSR) & 1)) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_ts(tmem + COL_S, tmem + COL_Q + s_c * 32 + kk * 8, d_sr + slot * KCH16 + kk * 2, idesc_s,
-                      (s_c | kk) ? 1u : 0u);
-            umma_commit(bar(C::BAR_SR_EMPTY + slot));
-            ++cnt;
-            if (++s_c == C::NCH) {
-              umma_commit(bar(C::BAR_S));
-              s_c = 0;
-              s_tile += NH;
-              ++s_k;
-              s_free = false;
-            }
-            progress = true;
-          }
-        }
-        if (j < n) {
-          const int slot = j % NPS, st = j % NVS;
-          if (mbar_test_nb(bar(C::BAR_P_READY + slot), (j / NPS) & 1) &&
-              mbar_test_nb(bar(C::BAR_V_FULL + st), (j / NVS) & 1)) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              umma_ss(tmem + COL_O, d_p + slot * P16 + kk * 2, d_v + st * V16 + kk * VSTEP16, idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(bar(C::BAR_PV_DONE + slot));
-            umma_commit_mc(bar(C::BAR_SLOT_FREE + slot), all);
-            ++j;
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle = 0;
-        } else if (++idle == 1) {
-          t_idle = globaltimer_ns();
-        } else if ((idle & 255u) == 0 && globaltimer_ns() - t_idle > WAIT_LIMIT_NS) {
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        const int slot = j % NPS, st = j % NVS;
+        if (!mbar_wait(bar(C::BAR_P_READY + slot), (j / NPS) & 1) ||
+            !mbar_wait(bar(C::BAR_V_FULL + st), (j / NVS) & 1)) {
           ok = false;
+          break;
         }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_ss(tmem + COL_O, d_p + slot * P16 + kk * 2, d_v + st * V16 + kk * VSTEP16, idesc_pv,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(C::BAR_PV_DONE + slot));
+        umma_commit_mc(bar(C::BAR_SLOT_FREE + slot), all);
       }
       if (!ok) fail();
       umma_commit(bar(C::BAR_DONE));
