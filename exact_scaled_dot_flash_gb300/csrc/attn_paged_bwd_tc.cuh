@@ -391,6 +391,269 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// Key blocks per CTA of the streaming key-major kernel.
+constexpr int KPC = 8;
+
+// The key-major kernel for calls whose query side per (sequence, kv head) is
+// one tile (one head block and at most 128 (query, head) pairs: a decode step,
+// or a short chunk). CTA = (sequence, kv head, run of KPC 128-key blocks):
+// the query and dout tile stays resident while the key blocks stream through
+// the two-stage ring (K and V of a block in one stage), so the setup, the
+// query loads and the row statistics are paid once per run instead of once per
+// 128 keys, and the epilogue of a block overlaps the S and dP MMAs of the next.
+// Per block: S^T = K Q^T and dP^T = V dO^T (SS), P^T and dS'^T by the
+// elementwise warps (packed into S^T's and dP^T's columns), dV = P^T dO and
+// dK = dS'^T Q (TS, one query tile: no accumulation across tiles), then the
+// elementwise warps store the block's dK and dV rows of single-reader pages
+// and compute the next block's P^T. The order makes every TMEM reuse safe: the
+// MMA issues the next block's S and dP after dK (the tensor pipe runs in
+// order), and the elementwise warps finish reading dK and dV before they
+// release the next block's P^T for the dV MMA.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    paged_dkdv_stream_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                             const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                             const PagedParams pp, const TcArgs a, int chunks) {
+  using C = Cfg<D>;
+  constexpr int BAR_KVFULL = C::BAR_FULL, BAR_KVEMPTY = C::BAR_EMPTY;  // the ring holds K, V pairs
+  constexpr int BAR_ACC = C::BAR_S + 1;                                 // dK, dV of the block complete
+  static_assert(C::STAGES >= 2, "two ring stages");
+  constexpr int NST = 2;
+  // ---- work: key blocks [kb0, kb0 + nb) of sequence s, kv head hk
+  const int lin = static_cast<int>(blockIdx.x);
+  const int ch = lin % chunks;
+  const int rest = lin / chunks;
+  const int hk = rest % pp.Hkv, s = rest / pp.Hkv;
+  const int L = seq_keys(pp, s);
+  int q0, n;
+  seq_rows(pp, s, q0, n);
+  const int P = pp.page_size;
+  const int used = (L + P - 1) / P;
+  const int kblocks_used = (used * P + BR - 1) / BR;
+  const int kb0 = ch * KPC;
+  const int nb = min(KPC, kblocks_used - kb0);
+  if (n == 0 || nb <= 0) return;  // uniform
+  const int group = pp.Hq / pp.Hkv;  // = the head block: one tile of (query, head) pairs
+  const int diag = L - n;
+  const bool dflt = pp.positions == nullptr;
+  const int32_t* table = pp.block_table + static_cast<size_t>(s) * pp.max_pages;
+
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NST; ++st) {
+      mbar_init(bar(BAR_KVFULL + st), 1);
+      mbar_init(bar(BAR_KVEMPTY + st), 1);
+    }
+    mbar_init(bar(C::BAR_RES), 1);
+    mbar_init(bar(C::BAR_S), 1);
+    mbar_init(bar(BAR_ACC), 1);
+    mbar_init(bar(C::BAR_DP), 1);
+    mbar_init(bar(C::BAR_P), 256);
+    mbar_init(bar(C::BAR_DS), 256);
+    mbar_init(bar(C::BAR_DONE), 1);
+    mbar_init_fence();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto fail = [&]() {
+    if (pp.status) atomicOr(pp.status, STATUS_TIMEOUT);
+  };
+
+  if (warp >= 8) {
+    setmaxnreg_dec<REG_OTHER>();
+    if (warp == WARP_TMA && lane == 0) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar(C::BAR_RES), 2 * C::TILE_BYTES);
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        tma_load_4d(sb + c * C::CHUNK_BYTES, &tm_q, bar(C::BAR_RES), c * C::BOX_D, 0, hk, q0);
+        tma_load_4d(sb + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_do, bar(C::BAR_RES), c * C::BOX_D, 0, hk, q0);
+      }
+      int i = 0;
+      for (; i < nb; ++i) {
+        const int st = i % NST;
+        if (!mbar_wait(bar(BAR_KVEMPTY + st), ((i / NST) & 1) ^ 1)) { fail(); break; }
+        const uint32_t dst = sb + C::OFF_RING + st * 2 * C::TILE_BYTES;
+        mbar_arrive_expect_tx(bar(BAR_KVFULL + st), 2 * C::TILE_BYTES);
+        load_kv_tile<D>(dst, &tm_k, bar(BAR_KVFULL + st), table, pp, (kb0 + i) * BR, hk);
+        load_kv_tile<D>(dst + C::TILE_BYTES, &tm_v, bar(BAR_KVFULL + st), table, pp, (kb0 + i) * BR, hk);
+      }
+      for (int st = 0; st < NST && st < i; ++st) {
+        const int fills = (i - st + NST - 1) / NST;
+        if (!mbar_wait(bar(BAR_KVFULL + st), (fills - 1) & 1)) fail();
+      }
+      if (!mbar_wait(bar(C::BAR_RES), 0)) fail();
+    } else if (warp == WARP_MMA && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc_s = make_idesc_f16(BF16, BR, BR, false);
+      constexpr uint32_t idesc_o = make_idesc_f16(BF16, BR, D, true);
+      constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
+      constexpr uint32_t RSTEP16 = (16 * 128) >> 4;
+      const uint64_t res_k = smem_desc(sb, 16, C::SBO, C::LAYOUT);                  // Q, dO as K-major B
+      const uint64_t res_mn = smem_desc(sb, C::CHUNK_BYTES, C::SBO, C::LAYOUT);     // Q, dO as MN-major B
+      const uint64_t ring_k = smem_desc(sb + C::OFF_RING, 16, C::SBO, C::LAYOUT);  // K, V as K-major A
+      bool ok = mbar_wait(bar(C::BAR_RES), 0);
+      tc_fence_after();
+      for (int i = 0; i < nb && ok; ++i) {
+        const int st = i % NST;
+        if (!mbar_wait(bar(BAR_KVFULL + st), (i / NST) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t kk = ring_k + st * 2 * TILE16;
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_D; ++k)
+          umma_ss(tmem + 0, kk + kstep16<D>(k), res_k + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
+        umma_commit(bar(C::BAR_S));
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_D; ++k)
+          umma_ss(tmem + BR, kk + TILE16 + kstep16<D>(k), res_k + TILE16 + kstep16<D>(k), idesc_s,
+                  k > 0 ? 1u : 0u);
+        umma_commit(bar(C::BAR_DP));
+        umma_commit(bar(BAR_KVEMPTY + st));  // K and V of the block are no longer read
+        if (!mbar_wait(bar(C::BAR_P), i & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_R; ++k)
+          umma_ts(tmem + 256, tmem + tmem_a_kstep(k), res_mn + TILE16 + k * RSTEP16, idesc_o, k > 0 ? 1u : 0u);
+        if (!mbar_wait(bar(C::BAR_DS), i & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_R; ++k)
+          umma_ts(tmem + 256 + D, tmem + BR + tmem_a_kstep(k), res_mn + k * RSTEP16, idesc_o, k > 0 ? 1u : 0u);
+        umma_commit(bar(BAR_ACC));
+      }
+      if (!ok) fail();
+      umma_commit(bar(C::BAR_DONE));
+      if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- elementwise
+    setmaxnreg_inc<REG_EW>();
+    const int half = warp >> 2;                // pair columns [64 half, +64) of the tile
+    const int row = ((warp & 3) << 5) + lane;  // key row of the block = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    const uint32_t tS = tmem + lane_off, tDP = tS + BR;
+    const float sc = pp.scale_log2;
+    float* st_l2 = reinterpret_cast<float*>(smem + C::OFF_STATS) + warp * C::STATS_PER_WARP;
+    float* st_ds = st_l2 + 64;
+    int* st_lim = reinterpret_cast<int*>(st_l2 + 128);
+    // the tile's column statistics, once: lse2, D and the largest visible key
+    // (-1 for a pair with no query or no visible key)
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int pair = 64 * half + 32 * u + lane;
+      const int qi = pair / group;
+      const int hq = hk * group + (pair - qi * group);
+      const size_t ri = static_cast<size_t>(q0 + (qi < n ? qi : 0)) * pp.Hq + hq;
+      const bool in = qi < n && in_bounds(pp.status, static_cast<int64_t>(ri),
+                                          static_cast<int64_t>(pp.num_queries) * pp.Hq);
+      const float l2 = in ? __ldg(a.lse2 + ri) : -INFINITY;
+      const float dsm = in ? __ldg(a.dsum + ri) : 0.f;
+      int lim = 0x7ffffffe;
+      if (pp.causal)
+        lim = dflt ? diag + qi
+                   : ((in && in_bounds(pp.status, q0 + qi, pp.num_queries))
+                          ? min(__ldg(pp.positions + q0 + qi), 0x7ffffffe) : -1);
+      const bool live = l2 != -INFINITY;
+      st_l2[32 * u + lane] = live ? l2 : 0.f;
+      st_ds[32 * u + lane] = live ? dsm : 0.f;
+      st_lim[32 * u + lane] = live ? lim : -1;
+    }
+    __syncwarp();
+    void* dst = half == 0 ? a.dk : a.dv;
+    const float mul = half == 0 ? a.scale : 1.f;
+    bool failed = false;
+    for (int i = 0; i < nb && !failed; ++i) {
+      const int key = (kb0 + i) * BR + row;
+      const int kcmp = key < L ? key : 0x7fffffff;  // keys past the sequence see nothing
+      float x[64];
+      const bool ok = mbar_wait(bar(C::BAR_S), i & 1);
+      if (__any_sync(0xffffffffu, !ok)) { failed = true; break; }
+      tc_fence_after();
+      tmem_ld64<BF16>(tS + 64 * half, x);
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = reinterpret_cast<const float4*>(st_l2)[c4];
+        const int4 m4 = reinterpret_cast<const int4*>(st_lim)[c4];
+        x[4 * c4 + 0] = kcmp <= m4.x ? fast_exp2(x[4 * c4 + 0] * sc - l4.x) : 0.f;
+        x[4 * c4 + 1] = kcmp <= m4.y ? fast_exp2(x[4 * c4 + 1] * sc - l4.y) : 0.f;
+        x[4 * c4 + 2] = kcmp <= m4.z ? fast_exp2(x[4 * c4 + 2] * sc - l4.z) : 0.f;
+        x[4 * c4 + 3] = kcmp <= m4.w ? fast_exp2(x[4 * c4 + 3] * sc - l4.w) : 0.f;
+      }
+      tmem_st_packed64<BF16>(tS + 64 * half, x);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::BAR_P));
+      const bool ok2 = mbar_wait(bar(C::BAR_DP), i & 1);
+      if (__any_sync(0xffffffffu, !ok2)) { failed = true; break; }
+      tc_fence_after();
+      float dp[64];
+      tmem_ld64<BF16>(tDP + 64 * half, dp);
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 d4 = reinterpret_cast<const float4*>(st_ds)[c4];
+        dp[4 * c4 + 0] = x[4 * c4 + 0] * (dp[4 * c4 + 0] - d4.x);
+        dp[4 * c4 + 1] = x[4 * c4 + 1] * (dp[4 * c4 + 1] - d4.y);
+        dp[4 * c4 + 2] = x[4 * c4 + 2] * (dp[4 * c4 + 2] - d4.z);
+        dp[4 * c4 + 3] = x[4 * c4 + 3] * (dp[4 * c4 + 3] - d4.w);
+      }
+      tmem_st_packed64<BF16>(tDP + 64 * half, dp);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::BAR_DS));
+      // ---- the block's rows: warpgroup 0 writes dK (scaled), warpgroup 1 dV;
+      // a key row goes to its physical slot when its page has exactly one reader
+      const int pidx = key / P;
+      int page = (pidx < used && in_bounds(pp.status, static_cast<int64_t>(s) * pp.max_pages + pidx,
+                                           static_cast<int64_t>(pp.num_seqs) * pp.max_pages))
+                     ? __ldg(table + pidx) : -1;
+      if (page >= pp.num_pages || (page >= 0 && __ldg(a.offsets + page + 1) - __ldg(a.offsets + page) != 1))
+        page = -1;
+      const int64_t crow = ((static_cast<int64_t>(page < 0 ? 0 : page) * P + key % P) * pp.Hkv + hk) * D;
+      if (page >= 0 && !range_in_bounds(pp.status, crow, D, static_cast<int64_t>(pp.num_pages) * P * pp.Hkv * D))
+        page = -1;
+      const bool ok3 = mbar_wait(bar(BAR_ACC), i & 1);
+      if (__any_sync(0xffffffffu, !ok3)) { failed = true; break; }
+      tc_fence_after();
+      const uint32_t src = tmem + lane_off + 256 + (half == 0 ? D : 0);
+      uint8_t* rowp = static_cast<uint8_t*>(dst) + crow * 2;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(src + 32 * c, r);
+        tmem_wait_ld();
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+        if (page >= 0 && dst) store_row16<BF16, 32>(rowp + c * 64, v, mul);
+      }
+      tc_fence_before();
+    }
+    if (failed && lane == 0) fail();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     paged_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -669,6 +932,7 @@ cudaError_t launch_paged_bwd_tc(EncodeTiledFn enc, const PagedParams& pp, const 
         return cudaErrorInvalidValue;
   }
   auto kv = paged_dkdv_tc_kernel<D, BF16>;
+  auto kvs = paged_dkdv_stream_kernel<D, BF16>;
   auto kq = paged_dq_tc_kernel<D, BF16>;
   constexpr int smem_kv = Cfg<D>::SMEM_BYTES;
   constexpr int smem_q = DqCfg<D>::SMEM_BYTES;
@@ -676,15 +940,22 @@ cudaError_t launch_paged_bwd_tc(EncodeTiledFn enc, const PagedParams& pp, const 
   const unsigned long long bit = pp.device >= 0 && pp.device < 64 ? 1ull << pp.device : 0ull;
   if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kvs, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   if (a.dk || a.dv) {
     const int64_t kblocks = (static_cast<int64_t>(pp.max_pages) * pp.page_size + BR - 1) / BR;
-    const int64_t ctas = static_cast<int64_t>(pp.num_seqs) * pp.Hkv * kblocks;
+    // one tile of (query, head) pairs per (sequence, kv head): stream the key blocks
+    const bool stream = gp == group && static_cast<int64_t>(pp.max_queries) * gp <= BR;
+    const int64_t chunks = (kblocks + KPC - 1) / KPC;
+    const int64_t ctas = static_cast<int64_t>(pp.num_seqs) * pp.Hkv * (stream ? chunks : kblocks);
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (ctas > 0)
+    if (ctas > 0 && stream)
+      kvs<<<static_cast<unsigned>(ctas), NUM_THREADS, smem_kv, st>>>(tq, tdo, tk, tv, pp, a,
+                                                                     static_cast<int>(chunks));
+    else if (ctas > 0)
       kv<<<static_cast<unsigned>(ctas), NUM_THREADS, smem_kv, st>>>(tq, tdo, tk, tv, pp, a,
                                                                     static_cast<int>(kblocks), gp);
     cudaError_t e = cudaGetLastError();

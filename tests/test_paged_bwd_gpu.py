@@ -108,6 +108,24 @@ def test_paged_bwd_matches_oracle(w):
     check_paged(w)
 
 
+# The key-major kernel streams the key blocks of a (sequence, kv head) through
+# one CTA per run of 8 blocks when the query side is a single tile (every head
+# of the group in one block, at most 128 (query, head) pairs): decode steps and
+# short chunks. Sequences of several runs, page sizes below and above a block,
+# explicit positions and the non-causal form.
+STREAM_CASES = [
+    PW("pbwd_stream_bf16_d128_p8_long", "bf16", 4, 16, 4, 128, 8, (1500, 3100), (1, 1), seed=41),
+    PW("pbwd_stream_f16_d64_p256_pos", "f16", 5, 8, 2, 64, 256, (200, 2600), (1, 12), seed=42,
+       explicit_positions=True),
+    PW("pbwd_stream_bf16_d128_p32_full", "bf16", 3, 8, 1, 128, 32, (900, 1400), (1, 16), seed=43, causal=False),
+]
+
+
+@pytest.mark.parametrize("w", STREAM_CASES, ids=lambda w: w.name)
+def test_paged_bwd_streamed_key_blocks(w):
+    check_paged(w)
+
+
 @pytest.mark.parametrize("P", [16, 64, 256])
 def test_paged_bwd_shared_prefix_pages_sum_both_readers(P):
     w = PW(f"pbwd_share_p{P}", "bf16", 4, 8, 2, 64, P, (2 * P + 5, 4 * P), (1, 9), seed=10 + P)
