@@ -654,6 +654,291 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// The streaming key-major kernel for a query side of at most NPN (query, head)
+// pairs (a decode step with a group of up to 32 heads, or a few queries): S^T
+// and dP^T are 128 keys x NPN pairs (MMA N = NPN instead of 128), dV and dK
+// contract over NPN pairs (2 K-steps instead of 8), one warpgroup computes P
+// and dS' for all NPN pairs of its key rows, and the small resident tiles leave
+// room for three K/V stages.
+constexpr int NPN = 32;
+
+template <int D>
+struct NarrowCfg {
+  using C = Cfg<D>;
+  static constexpr int QCHUNK = NPN * 128;  // one NPN-row x 64-column box
+  static constexpr int QTILE = C::NCHUNK * QCHUNK;
+  static constexpr int OFF_RING = (2 * QTILE + 1023) / 1024 * 1024;
+  static constexpr int KVSTAGE = 2 * C::TILE_BYTES;
+  static constexpr int NST = 3;
+  static constexpr int OFF_BAR = OFF_RING + NST * KVSTAGE;
+  static constexpr int BAR_FULL = 0, BAR_EMPTY = NST, BAR_RES = 2 * NST, BAR_S = BAR_RES + 1, BAR_DP = BAR_S + 1,
+                       BAR_P = BAR_DP + 1, BAR_DS = BAR_P + 1, BAR_ACC = BAR_DS + 1, BAR_DONE = BAR_ACC + 1,
+                       NUM_BARS = BAR_DONE + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int OFF_STATS = (OFF_MISC + 16 + 15) / 16 * 16;
+  static constexpr int STATS_PER_WARP = 3 * NPN;  // lse2, D, limit of each pair column
+  static constexpr int SMEM_BYTES = OFF_STATS + 4 * STATS_PER_WARP * 4 + 1024;
+  static_assert(SMEM_BYTES <= 232448, "narrow streaming kernel shared memory");
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    paged_dkdv_narrow_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                             const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                             const PagedParams pp, const TcArgs a, int chunks) {
+  using C = Cfg<D>;
+  using X = NarrowCfg<D>;
+  constexpr int NST = X::NST;
+  // ---- work: key blocks [kb0, kb0 + nb) of sequence s, kv head hk
+  const int lin = static_cast<int>(blockIdx.x);
+  const int ch = lin % chunks;
+  const int rest = lin / chunks;
+  const int hk = rest % pp.Hkv, s = rest / pp.Hkv;
+  const int L = seq_keys(pp, s);
+  int q0, n;
+  seq_rows(pp, s, q0, n);
+  const int P = pp.page_size;
+  const int used = (L + P - 1) / P;
+  const int kblocks_used = (used * P + BR - 1) / BR;
+  const int kb0 = ch * KPC;
+  const int nb = min(KPC, kblocks_used - kb0);
+  if (n == 0 || nb <= 0) return;  // uniform
+  const int group = pp.Hq / pp.Hkv;
+  const int diag = L - n;
+  const bool dflt = pp.positions == nullptr;
+  const int32_t* table = pp.block_table + static_cast<size_t>(s) * pp.max_pages;
+
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + X::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + X::OFF_MISC);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NST; ++st) {
+      mbar_init(bar(X::BAR_FULL + st), 1);
+      mbar_init(bar(X::BAR_EMPTY + st), 1);
+    }
+    mbar_init(bar(X::BAR_RES), 1);
+    mbar_init(bar(X::BAR_S), 1);
+    mbar_init(bar(X::BAR_DP), 1);
+    // P: warpgroup 0 has written P^T, warpgroup 1 has read the previous block's dV
+    mbar_init(bar(X::BAR_P), 256);
+    mbar_init(bar(X::BAR_DS), 128);
+    mbar_init(bar(X::BAR_ACC), 1);
+    mbar_init(bar(X::BAR_DONE), 1);
+    mbar_init_fence();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto fail = [&]() {
+    if (pp.status) atomicOr(pp.status, STATUS_TIMEOUT);
+  };
+
+  if (warp >= 8) {
+    setmaxnreg_dec<REG_OTHER>();
+    if (warp == WARP_TMA && lane == 0) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar(X::BAR_RES), 2 * X::QTILE);
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        tma_load_4d(sb + c * X::QCHUNK, &tm_q, bar(X::BAR_RES), c * C::BOX_D, 0, hk, q0);
+        tma_load_4d(sb + X::QTILE + c * X::QCHUNK, &tm_do, bar(X::BAR_RES), c * C::BOX_D, 0, hk, q0);
+      }
+      int i = 0;
+      for (; i < nb; ++i) {
+        const int st = i % NST;
+        if (!mbar_wait(bar(X::BAR_EMPTY + st), ((i / NST) & 1) ^ 1)) { fail(); break; }
+        const uint32_t dst = sb + X::OFF_RING + st * X::KVSTAGE;
+        mbar_arrive_expect_tx(bar(X::BAR_FULL + st), X::KVSTAGE);
+        load_kv_tile<D>(dst, &tm_k, bar(X::BAR_FULL + st), table, pp, (kb0 + i) * BR, hk);
+        load_kv_tile<D>(dst + C::TILE_BYTES, &tm_v, bar(X::BAR_FULL + st), table, pp, (kb0 + i) * BR, hk);
+      }
+      for (int st = 0; st < NST && st < i; ++st) {
+        const int fills = (i - st + NST - 1) / NST;
+        if (!mbar_wait(bar(X::BAR_FULL + st), (fills - 1) & 1)) fail();
+      }
+      if (!mbar_wait(bar(X::BAR_RES), 0)) fail();
+    } else if (warp == WARP_MMA && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc_s = make_idesc_f16(BF16, BR, NPN, false);
+      constexpr uint32_t idesc_o = make_idesc_f16(BF16, BR, D, true);
+      constexpr uint32_t QTILE16 = X::QTILE >> 4, QCHUNK16 = X::QCHUNK >> 4;
+      constexpr uint32_t KV16 = X::KVSTAGE >> 4, TILE16 = C::TILE_BYTES >> 4;
+      constexpr uint32_t RSTEP16 = (16 * 128) >> 4;
+      const uint64_t res_k = smem_desc(sb, 16, C::SBO, C::LAYOUT);              // Q, dO as K-major B
+      const uint64_t res_mn = smem_desc(sb, X::QCHUNK, C::SBO, C::LAYOUT);      // Q, dO as MN-major B
+      const uint64_t ring_k = smem_desc(sb + X::OFF_RING, 16, C::SBO, C::LAYOUT);  // K, V as K-major A
+      auto qstep = [](int k) -> uint32_t { return (k / 4) * QCHUNK16 + (k % 4) * 2; };
+      bool ok = mbar_wait(bar(X::BAR_RES), 0);
+      tc_fence_after();
+      for (int i = 0; i < nb && ok; ++i) {
+        const int st = i % NST;
+        if (!mbar_wait(bar(X::BAR_FULL + st), (i / NST) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t kk = ring_k + st * KV16;
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_D; ++k)
+          umma_ss(tmem + 0, kk + kstep16<D>(k), res_k + qstep(k), idesc_s, k > 0 ? 1u : 0u);
+        umma_commit(bar(X::BAR_S));
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_D; ++k)
+          umma_ss(tmem + BR, kk + TILE16 + kstep16<D>(k), res_k + QTILE16 + qstep(k), idesc_s, k > 0 ? 1u : 0u);
+        umma_commit(bar(X::BAR_DP));
+        umma_commit(bar(X::BAR_EMPTY + st));  // K and V of the block are no longer read
+        if (!mbar_wait(bar(X::BAR_P), i & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < NPN / 16; ++k)
+          umma_ts(tmem + 256, tmem + k * 8, res_mn + QTILE16 + k * RSTEP16, idesc_o, k > 0 ? 1u : 0u);
+        if (!mbar_wait(bar(X::BAR_DS), i & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < NPN / 16; ++k)
+          umma_ts(tmem + 256 + D, tmem + BR + k * 8, res_mn + k * RSTEP16, idesc_o, k > 0 ? 1u : 0u);
+        umma_commit(bar(X::BAR_ACC));
+      }
+      if (!ok) fail();
+      umma_commit(bar(X::BAR_DONE));
+      if (!mbar_wait(bar(X::BAR_DONE), 0)) fail();
+    }
+    __syncwarp();
+  } else {
+    setmaxnreg_inc<REG_EW>();
+    const int row = ((warp & 3) << 5) + lane;  // key row of the block = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    const bool ew = warp < 4;                  // warpgroup 0: P, dS' and the dK rows; 1: the dV rows
+    const float sc = pp.scale_log2;
+    float* st_l2 = reinterpret_cast<float*>(smem + X::OFF_STATS) + (warp & 3) * X::STATS_PER_WARP;
+    float* st_ds = st_l2 + NPN;
+    int* st_lim = reinterpret_cast<int*>(st_l2 + 2 * NPN);
+    if (ew) {
+      // pair column `lane`: lse2, D and the largest visible key (-1: no query or no key)
+      const int pair = lane;
+      const int qi = pair / group;
+      const int hq = hk * group + (pair - qi * group);
+      const size_t ri = static_cast<size_t>(q0 + (qi < n ? qi : 0)) * pp.Hq + hq;
+      const bool in = qi < n && in_bounds(pp.status, static_cast<int64_t>(ri),
+                                          static_cast<int64_t>(pp.num_queries) * pp.Hq);
+      const float l2 = in ? __ldg(a.lse2 + ri) : -INFINITY;
+      const float dsm = in ? __ldg(a.dsum + ri) : 0.f;
+      int lim = 0x7ffffffe;
+      if (pp.causal)
+        lim = dflt ? diag + qi
+                   : ((in && in_bounds(pp.status, q0 + qi, pp.num_queries))
+                          ? min(__ldg(pp.positions + q0 + qi), 0x7ffffffe) : -1);
+      const bool live = l2 != -INFINITY;
+      st_l2[lane] = live ? l2 : 0.f;
+      st_ds[lane] = live ? dsm : 0.f;
+      st_lim[lane] = live ? lim : -1;
+      __syncwarp();
+    }
+    void* dst = ew ? a.dk : a.dv;
+    const float mul = ew ? a.scale : 1.f;
+    bool failed = false;
+    for (int i = 0; i < nb && !failed; ++i) {
+      const int key = (kb0 + i) * BR + row;
+      // warpgroup 1: the previous block's dV rows are read, the next dV MMA may overwrite them
+      if (!ew) mbar_arrive(bar(X::BAR_P));
+      if (ew) {
+        const int kcmp = key < L ? key : 0x7fffffff;  // keys past the sequence see nothing
+        const bool ok = mbar_wait(bar(X::BAR_S), i & 1);
+        if (__any_sync(0xffffffffu, !ok)) { failed = true; break; }
+        tc_fence_after();
+        float x[NPN];
+        {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < NPN; ++c) x[c] = __uint_as_float(r[c]);
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < NPN / 4; ++c4) {
+          const float4 l4 = reinterpret_cast<const float4*>(st_l2)[c4];
+          const int4 m4 = reinterpret_cast<const int4*>(st_lim)[c4];
+          x[4 * c4 + 0] = kcmp <= m4.x ? fast_exp2(x[4 * c4 + 0] * sc - l4.x) : 0.f;
+          x[4 * c4 + 1] = kcmp <= m4.y ? fast_exp2(x[4 * c4 + 1] * sc - l4.y) : 0.f;
+          x[4 * c4 + 2] = kcmp <= m4.z ? fast_exp2(x[4 * c4 + 2] * sc - l4.z) : 0.f;
+          x[4 * c4 + 3] = kcmp <= m4.w ? fast_exp2(x[4 * c4 + 3] * sc - l4.w) : 0.f;
+        }
+        {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(x[2 * c], x[2 * c + 1]);
+          tmem_st16(tmem + lane_off, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(X::BAR_P));
+        const bool ok2 = mbar_wait(bar(X::BAR_DP), i & 1);
+        if (__any_sync(0xffffffffu, !ok2)) { failed = true; break; }
+        tc_fence_after();
+        {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + BR, r);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float d0 = x[2 * c] * (__uint_as_float(r[2 * c]) - st_ds[2 * c]);
+            const float d1 = x[2 * c + 1] * (__uint_as_float(r[2 * c + 1]) - st_ds[2 * c + 1]);
+            pk[c] = pack2<BF16>(d0, d1);
+          }
+          tmem_st16(tmem + lane_off + BR, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(X::BAR_DS));
+      }
+      // ---- the block's rows (dK by warpgroup 0, dV by warpgroup 1); a key row
+      // goes to its physical slot when its page has exactly one reader
+      const int pidx = key / P;
+      int page = (pidx < used && in_bounds(pp.status, static_cast<int64_t>(s) * pp.max_pages + pidx,
+                                           static_cast<int64_t>(pp.num_seqs) * pp.max_pages))
+                     ? __ldg(table + pidx) : -1;
+      if (page >= pp.num_pages || (page >= 0 && __ldg(a.offsets + page + 1) - __ldg(a.offsets + page) != 1))
+        page = -1;
+      const int64_t crow = ((static_cast<int64_t>(page < 0 ? 0 : page) * P + key % P) * pp.Hkv + hk) * D;
+      if (page >= 0 && !range_in_bounds(pp.status, crow, D, static_cast<int64_t>(pp.num_pages) * P * pp.Hkv * D))
+        page = -1;
+      const bool ok3 = mbar_wait(bar(X::BAR_ACC), i & 1);
+      if (__any_sync(0xffffffffu, !ok3)) { failed = true; break; }
+      tc_fence_after();
+      const uint32_t src = tmem + lane_off + 256 + (ew ? D : 0);
+      uint8_t* rowp = static_cast<uint8_t*>(dst) + crow * 2;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(src + 32 * c, r);
+        tmem_wait_ld();
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+        if (page >= 0 && dst) store_row16<BF16, 32>(rowp + c * 64, v, mul);
+      }
+      tc_fence_before();
+    }
+    if (failed && lane == 0) fail();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     paged_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -931,8 +1216,25 @@ cudaError_t launch_paged_bwd_tc(EncodeTiledFn enc, const PagedParams& pp, const 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
   }
+  // q, dout again with boxes of NPN (query, head) pairs, for the narrow kernel
+  CUtensorMap tqn, tdon;
+  const bool narrow_ok = gp == group && NPN % gp == 0;
+  if (narrow_ok) {
+    const cuuint64_t gdim[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(gp),
+                                static_cast<cuuint64_t>(pp.Hq / gp), static_cast<cuuint64_t>(pp.num_queries)};
+    const cuuint64_t gstride[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(gp) * D * 2,
+                                   static_cast<cuuint64_t>(pp.Hq) * D * 2};
+    const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(gp), 1u, static_cast<cuuint32_t>(NPN / gp)};
+    for (int i = 0; i < 2; ++i)
+      if (enc(i == 0 ? &tqn : &tdon, dt, 4, const_cast<void*>(i == 0 ? q : dout), gdim, gstride, box, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+  }
   auto kv = paged_dkdv_tc_kernel<D, BF16>;
   auto kvs = paged_dkdv_stream_kernel<D, BF16>;
+  auto kvn = paged_dkdv_narrow_kernel<D, BF16>;
+  constexpr int smem_kvn = NarrowCfg<D>::SMEM_BYTES;
   auto kq = paged_dq_tc_kernel<D, BF16>;
   constexpr int smem_kv = Cfg<D>::SMEM_BYTES;
   constexpr int smem_q = DqCfg<D>::SMEM_BYTES;
@@ -941,6 +1243,7 @@ cudaError_t launch_paged_bwd_tc(EncodeTiledFn enc, const PagedParams& pp, const 
   if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kvs, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kvn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kvn);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
@@ -952,7 +1255,12 @@ cudaError_t launch_paged_bwd_tc(EncodeTiledFn enc, const PagedParams& pp, const 
     const int64_t chunks = (kblocks + KPC - 1) / KPC;
     const int64_t ctas = static_cast<int64_t>(pp.num_seqs) * pp.Hkv * (stream ? chunks : kblocks);
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (ctas > 0 && stream)
+    // at most NPN pairs: the narrow streaming kernel
+    const bool narrow = stream && narrow_ok && static_cast<int64_t>(pp.max_queries) * gp <= NPN;
+    if (ctas > 0 && narrow)
+      kvn<<<static_cast<unsigned>(ctas), NUM_THREADS, smem_kvn, st>>>(tqn, tdon, tk, tv, pp, a,
+                                                                      static_cast<int>(chunks));
+    else if (ctas > 0 && stream)
       kvs<<<static_cast<unsigned>(ctas), NUM_THREADS, smem_kv, st>>>(tq, tdo, tk, tv, pp, a,
                                                                      static_cast<int>(chunks));
     else if (ctas > 0)

@@ -111,13 +111,17 @@ def test_paged_bwd_matches_oracle(w):
 # The key-major kernel streams the key blocks of a (sequence, kv head) through
 # one CTA per run of 8 blocks when the query side is a single tile (every head
 # of the group in one block, at most 128 (query, head) pairs): decode steps and
-# short chunks. Sequences of several runs, page sizes below and above a block,
-# explicit positions and the non-causal form.
+# short chunks; with at most 32 pairs, on 32-pair tiles. Sequences of several
+# runs, page sizes below and above a block, explicit positions and the
+# non-causal form.
 STREAM_CASES = [
     PW("pbwd_stream_bf16_d128_p8_long", "bf16", 4, 16, 4, 128, 8, (1500, 3100), (1, 1), seed=41),
     PW("pbwd_stream_f16_d64_p256_pos", "f16", 5, 8, 2, 64, 256, (200, 2600), (1, 12), seed=42,
        explicit_positions=True),
     PW("pbwd_stream_bf16_d128_p32_full", "bf16", 3, 8, 1, 128, 32, (900, 1400), (1, 16), seed=43, causal=False),
+    # at most 32 pairs: the narrow variant (32-pair tiles)
+    PW("pbwd_narrow_f16_d64_p64_pos", "f16", 4, 8, 2, 64, 64, (300, 2100), (1, 6), seed=44, explicit_positions=True),
+    PW("pbwd_narrow_bf16_d128_p128_full", "bf16", 3, 16, 2, 128, 128, (500, 1500), (1, 4), seed=45, causal=False),
 ]
 
 
