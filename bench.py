@@ -643,7 +643,8 @@ def bench_paged(args):
     # and HBM rooflines binds (the larger ideal time)
     bwd_tc = bwd and not is_mla and tensor
     mla_bwd_tc = bwd and is_mla and tensor_bwd
-    tc_names = "paged_dkdv_tc_kernel + paged_dq_tc_kernel (+ FMA pass over shared pages), whole call"
+    tc_names = (("paged_dkdv_narrow_kernel or paged_dkdv_stream_kernel" if decode else "paged_dkdv_tc_kernel")
+                + " + paged_dq_tc_kernel (+ FMA pass over shared pages), whole call")
     if mla_bwd_tc:
         pk, bw = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
         names = "mla_bwd_tc_kernel key-major + query-major (+ FMA pass over shared pages), whole call"
