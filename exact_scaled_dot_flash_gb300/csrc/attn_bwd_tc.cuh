@@ -239,8 +239,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait(bar(C::BAR_FULL + s), (fills - 1) & 1)) fail();
       }
       if (!mbar_wait(bar(C::BAR_RES), 0)) fail();
-    } else if (warp == WARP_MMA && lane == 0) {
+    } else if (warp == WARP_MMA) {
       // ------------------------------------------------------------ MMA issuer
+      // (the whole warp waits; one elected lane issues the MMAs and commits)
       constexpr uint32_t idesc_s = make_idesc_f16(BF16, BR, BR, false);  // M = keys, N = query rows
       constexpr uint32_t idesc_o = make_idesc_f16(BF16, BR, D, true);    // N = D, B MN-major
       constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
@@ -252,57 +253,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       auto issue_s = [&](int it) {  // S^T = K Q_i^T, dP^T = V dO_i^T
         const int s = it % C::STAGES;
-        if (!mbar_wait(bar(C::BAR_FULL + s), (it / C::STAGES) & 1)) return false;
+        if (!warp_wait(bar(C::BAR_FULL + s), (it / C::STAGES) & 1)) return false;
         tc_fence_after();
         const uint64_t q = ring_k + s * 2 * TILE16;
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_D; ++k)
-          umma_ss(tmem + 0, dk_a + kstep16<D>(k), q + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
-        umma_commit(bar(C::BAR_S));
+          for (int k = 0; k < C::KSTEPS_D; ++k)
+            umma_ss(tmem + 0, dk_a + kstep16<D>(k), q + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
+          umma_commit(bar(C::BAR_S));
+        }
+        __syncwarp();
         return true;
       };
       auto issue_dp = [&](int it) {
         const int s = it % C::STAGES;
         const uint64_t g = ring_k + s * 2 * TILE16 + TILE16;
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_D; ++k)
-          umma_ss(tmem + BR, dv_a + kstep16<D>(k), g + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
-        umma_commit(bar(C::BAR_DP));
+          for (int k = 0; k < C::KSTEPS_D; ++k)
+            umma_ss(tmem + BR, dv_a + kstep16<D>(k), g + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
+          umma_commit(bar(C::BAR_DP));
+        }
+        __syncwarp();
       };
       if (N > 0) {
-        if (!mbar_wait(bar(C::BAR_RES), 0)) ok = false;
+        if (!warp_wait(bar(C::BAR_RES), 0)) ok = false;
         tc_fence_after();
         if (ok && !issue_s(0)) ok = false;
         if (ok) issue_dp(0);
         for (int it = 0; it < N && ok; ++it) {
           const int s = it % C::STAGES;
           // dV += P^T dO_i   (P^T: 16-bit in S^T's columns)
-          if (!mbar_wait(bar(C::BAR_P), it & 1)) { ok = false; break; }
+          if (!warp_wait(bar(C::BAR_P), it & 1)) { ok = false; break; }
           tc_fence_after();
-          {
+          if (elect_one()) {
             const uint64_t g = ring_mn + s * 2 * TILE16 + TILE16;
 #pragma unroll
             for (int k = 0; k < C::KSTEPS_R; ++k)
               umma_ts(tmem + 256, tmem + tmem_a_kstep(k), g + k * RSTEP16, idesc_o, (it > 0 || k > 0) ? 1u : 0u);
           }
+          __syncwarp();
           if (it + 1 < N && !issue_s(it + 1)) { ok = false; break; }
           // dK += dS^T Q_i   (dS^T: 16-bit in dP^T's columns)
-          if (!mbar_wait(bar(C::BAR_DS), it & 1)) { ok = false; break; }
+          if (!warp_wait(bar(C::BAR_DS), it & 1)) { ok = false; break; }
           tc_fence_after();
-          {
+          if (elect_one()) {
             const uint64_t q = ring_mn + s * 2 * TILE16;
 #pragma unroll
             for (int k = 0; k < C::KSTEPS_R; ++k)
               umma_ts(tmem + 256 + D, tmem + BR + tmem_a_kstep(k), q + k * RSTEP16, idesc_o,
                       (it > 0 || k > 0) ? 1u : 0u);
+            umma_commit(bar(C::BAR_EMPTY + s));
           }
-          umma_commit(bar(C::BAR_EMPTY + s));
+          __syncwarp();
           if (it + 1 < N) issue_dp(it + 1);
         }
       }
-      if (!ok) fail();
-      umma_commit(bar(C::BAR_DONE));
-      if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
+      if (!ok && lane == 0) fail();
+      if (elect_one()) umma_commit(bar(C::BAR_DONE));
+      __syncwarp();
+      if (!warp_wait(bar(C::BAR_DONE), 0) && lane == 0) fail();
     }
     __syncwarp();
   } else {
@@ -539,8 +549,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int s = 0; s < Q::VST && s < nv; ++s)
         if (!mbar_wait(bar(Q::BAR_VFULL + s), (((nv - s + Q::VST - 1) / Q::VST) - 1) & 1)) fail();
       if (!mbar_wait(bar(Q::BAR_RES), 0)) fail();
-    } else if (warp == WARP_MMA && lane == 0) {
+    } else if (warp == WARP_MMA) {
       // ------------------------------------------------------------ MMA issuer
+      // (the whole warp waits; one elected lane issues the MMAs and commits)
       constexpr uint32_t idesc_s = make_idesc_f16(BF16, BR, BR, false);  // M = rows, N = keys
       constexpr uint32_t idesc_o = make_idesc_f16(BF16, BR, D, true);    // N = D, B MN-major
       constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
@@ -553,50 +564,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       auto issue_s = [&](int j) {  // S = Q K_j^T into buffer j & 1
         const int ks = j % Q::KST;
-        if (!mbar_wait(bar(Q::BAR_KFULL + ks), (j / Q::KST) & 1)) return false;
+        if (!warp_wait(bar(Q::BAR_KFULL + ks), (j / Q::KST) & 1)) return false;
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_D; ++k)
-          umma_ss(tmem + BR * (j & 1), q_a + kstep16<D>(k), k_b + ks * TILE16 + kstep16<D>(k), idesc_s,
-                  k > 0 ? 1u : 0u);
-        umma_commit(bar(Q::BAR_S + (j & 1)));
+          for (int k = 0; k < C::KSTEPS_D; ++k)
+            umma_ss(tmem + BR * (j & 1), q_a + kstep16<D>(k), k_b + ks * TILE16 + kstep16<D>(k), idesc_s,
+                    k > 0 ? 1u : 0u);
+          umma_commit(bar(Q::BAR_S + (j & 1)));
+        }
+        __syncwarp();
         return true;
       };
       auto issue_dp = [&](int j) {  // dP = dO V_j^T
         const int vs = j % Q::VST;
-        if (!mbar_wait(bar(Q::BAR_VFULL + vs), (j / Q::VST) & 1)) return false;
+        if (!warp_wait(bar(Q::BAR_VFULL + vs), (j / Q::VST) & 1)) return false;
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_D; ++k)
-          umma_ss(tmem + 2 * BR, do_a + kstep16<D>(k), v_b + vs * TILE16 + kstep16<D>(k), idesc_s,
-                  k > 0 ? 1u : 0u);
-        umma_commit(bar(Q::BAR_DP));
-        umma_commit(bar(Q::BAR_VEMPTY + vs));
+          for (int k = 0; k < C::KSTEPS_D; ++k)
+            umma_ss(tmem + 2 * BR, do_a + kstep16<D>(k), v_b + vs * TILE16 + kstep16<D>(k), idesc_s,
+                    k > 0 ? 1u : 0u);
+          umma_commit(bar(Q::BAR_DP));
+          umma_commit(bar(Q::BAR_VEMPTY + vs));
+        }
+        __syncwarp();
         return true;
       };
       if (N > 0) {
-        if (!mbar_wait(bar(Q::BAR_RES), 0)) ok = false;
+        if (!warp_wait(bar(Q::BAR_RES), 0)) ok = false;
         tc_fence_after();
         if (ok && !issue_s(0)) ok = false;
         if (ok && !issue_dp(0)) ok = false;
         if (ok && N > 1 && !issue_s(1)) ok = false;
         for (int j = 0; j < N && ok; ++j) {
           // dQ += dS K_j   (dS: 16-bit in dP's columns; K_j as an MN-major operand)
-          if (!mbar_wait(bar(Q::BAR_DS), j & 1)) { ok = false; break; }
+          if (!warp_wait(bar(Q::BAR_DS), j & 1)) { ok = false; break; }
           tc_fence_after();
           const int ks = j % Q::KST;
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < C::KSTEPS_R; ++k)
-            umma_ts(tmem + 3 * BR, tmem + 2 * BR + tmem_a_kstep(k), k_mn + ks * TILE16 + k * RSTEP16, idesc_o,
-                    (j > 0 || k > 0) ? 1u : 0u);
-          umma_commit(bar(Q::BAR_KEMPTY + ks));
+            for (int k = 0; k < C::KSTEPS_R; ++k)
+              umma_ts(tmem + 3 * BR, tmem + 2 * BR + tmem_a_kstep(k), k_mn + ks * TILE16 + k * RSTEP16, idesc_o,
+                      (j > 0 || k > 0) ? 1u : 0u);
+            umma_commit(bar(Q::BAR_KEMPTY + ks));
+          }
+          __syncwarp();
           if (j + 1 < N && !issue_dp(j + 1)) { ok = false; break; }
           if (j + 2 < N && !issue_s(j + 2)) { ok = false; break; }
         }
       }
-      if (!ok) fail();
-      umma_commit(bar(Q::BAR_DONE));
-      if (!mbar_wait(bar(Q::BAR_DONE), 0)) fail();
+      if (!ok && lane == 0) fail();
+      if (elect_one()) umma_commit(bar(Q::BAR_DONE));
+      __syncwarp();
+      if (!warp_wait(bar(Q::BAR_DONE), 0) && lane == 0) fail();
     }
     __syncwarp();
   } else {

@@ -315,8 +315,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int fills = (nit - kb + C::KBUF - 1) / C::KBUF;
         if (!mbar_wait(bar(C::BAR_KFULL + kb), (fills - 1) & 1)) fail();
       }
-    } else if (warp == WARP_MMA && lane == 0) {
+    } else if (warp == WARP_MMA) {
       // ------------------------------------------------------------ MMA issuer
+      // (the whole warp waits; one elected lane issues the MMAs and commits)
       constexpr uint32_t idesc_a = make_idesc_f16(BF16, BR, BR, false);   // S, dP: both K-major
       constexpr uint32_t idesc_g = make_idesc_f16(BF16, BR, 128, true);   // gradient slice, B MN-major
       constexpr uint32_t idesc_p = make_idesc_f16(BF16, BR, 64, true);    // positional gradient
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int rc = 0;
       for (int it = 0; it < N && ok; ++it) {
         const int kb = it % C::KBUF;
-        if (!mbar_wait(bar(C::BAR_KFULL + kb), (it / C::KBUF) & 1)) { ok = false; break; }
+        if (!warp_wait(bar(C::BAR_KFULL + kb), (it / C::KBUF) & 1)) { ok = false; break; }
         // S and dP, chunk by chunk (descriptors of chunk c's three operands)
         for (int c = 0; c < C::NCH && ok; ++c) {
           uint64_t d[3];
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               d[role] = keep_k + (kb * C::KEEP + k) * CH16;
             } else {
               const int slot = rc % C::RING;
-              if (!mbar_wait(bar(C::BAR_FULL + slot), (rc / C::RING) & 1)) { ok = false; break; }
+              if (!warp_wait(bar(C::BAR_FULL + slot), (rc / C::RING) & 1)) { ok = false; break; }
               d[role] = ring_k + slot * CH16;
               used[role] = slot;
               ++rc;
@@ -351,57 +352,87 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           // key-major: keys are M (A = key chunk); query-major: rows are M
           const uint64_t sa = KM ? d[0] : d[1], sbd = KM ? d[1] : d[0];
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_ss(tmem + COL_S, sa + kk * 2, sbd + kk * 2, idesc_a, (c | kk) ? 1u : 0u);
-          if (c < C::NCL) {
-            const uint64_t pa = KM ? d[0] : d[2], pb = KM ? d[2] : d[0];
+          if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_ss(tmem + COL_DP, pa + kk * 2, pb + kk * 2, idesc_a, (c | kk) ? 1u : 0u);
+              umma_ss(tmem + COL_S, sa + kk * 2, sbd + kk * 2, idesc_a, (c | kk) ? 1u : 0u);
           }
-          for (int role = 0; role < 3; ++role)
-            if (used[role] >= 0) umma_commit(bar(C::BAR_EMPTY + used[role]));
+          __syncwarp();
+          if (c < C::NCL) {
+            const uint64_t pa = KM ? d[0] : d[2], pb = KM ? d[2] : d[0];
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_ss(tmem + COL_DP, pa + kk * 2, pb + kk * 2, idesc_a, (c | kk) ? 1u : 0u);
+            }
+            __syncwarp();
+          }
+          if (elect_one()) {
+            for (int role = 0; role < 3; ++role)
+              if (used[role] >= 0) umma_commit(bar(C::BAR_EMPTY + used[role]));
+          }
+          __syncwarp();
         }
         if (!ok) break;
-        umma_commit(bar(C::BAR_SDP));
+        if (elect_one()) {
+          umma_commit(bar(C::BAR_SDP));
+        }
+        __syncwarp();
         // the gradient slice, once the elementwise warps have written P and dS'
-        if (!mbar_wait(bar(C::BAR_PDS), it & 1)) { ok = false; break; }
+        if (!warp_wait(bar(C::BAR_PDS), it & 1)) { ok = false; break; }
         tc_fence_after();
         const uint64_t kmn = keep_mn + kb * C::KEEP * CH16;
         if constexpr (KM) {
           // dlatent_h += P^T dout_h  (keep 2, 3)  +  dS'^T q_h  (keep 0, 1)
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            umma_ts(tmem + COL_ACC, tmem + COL_S + tmem_a_kstep(k), kmn + 2 * CH16 + k * RSTEP16, idesc_g,
-                    (it > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            umma_ts(tmem + COL_ACC, tmem + COL_DP + tmem_a_kstep(k), kmn + k * RSTEP16, idesc_g, 1u);
-          if (C::NCP && w.h == 0) {  // dkp += dS'^T qp  (keep 4)
+          if (elect_one()) {
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              umma_ts(tmem + COL_ACCP, tmem + COL_DP + tmem_a_kstep(k), kmn + 4 * CH16 + k * RSTEP16, idesc_p,
+              umma_ts(tmem + COL_ACC, tmem + COL_S + tmem_a_kstep(k), kmn + 2 * CH16 + k * RSTEP16, idesc_g,
                       (it > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              umma_ts(tmem + COL_ACC, tmem + COL_DP + tmem_a_kstep(k), kmn + k * RSTEP16, idesc_g, 1u);
+          }
+          __syncwarp();
+          if (C::NCP && w.h == 0) {  // dkp += dS'^T qp  (keep 4)
+            if (elect_one()) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                umma_ts(tmem + COL_ACCP, tmem + COL_DP + tmem_a_kstep(k), kmn + 4 * CH16 + k * RSTEP16, idesc_p,
+                        (it > 0 || k > 0) ? 1u : 0u);
+            }
+            __syncwarp();
           }
         } else {
           // dq_h += dS' c_h  (keep 0, 1);  dqp += dS' kp  (keep 2)
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            umma_ts(tmem + COL_ACC, tmem + COL_DP + tmem_a_kstep(k), kmn + k * RSTEP16, idesc_g,
-                    (it > 0 || k > 0) ? 1u : 0u);
-          if (C::NCP && w.h == 0) {
+          if (elect_one()) {
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              umma_ts(tmem + COL_ACCP, tmem + COL_DP + tmem_a_kstep(k), kmn + 2 * CH16 + k * RSTEP16, idesc_p,
+              umma_ts(tmem + COL_ACC, tmem + COL_DP + tmem_a_kstep(k), kmn + k * RSTEP16, idesc_g,
                       (it > 0 || k > 0) ? 1u : 0u);
           }
+          __syncwarp();
+          if (C::NCP && w.h == 0) {
+            if (elect_one()) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                umma_ts(tmem + COL_ACCP, tmem + COL_DP + tmem_a_kstep(k), kmn + 2 * CH16 + k * RSTEP16, idesc_p,
+                        (it > 0 || k > 0) ? 1u : 0u);
+            }
+            __syncwarp();
+          }
         }
-        umma_commit(bar(C::BAR_KFREE + kb));
+        if (elect_one()) {
+          umma_commit(bar(C::BAR_KFREE + kb));
+        }
+        __syncwarp();
       }
-      if (!ok) fail();
-      umma_commit(bar(C::BAR_DONE));
-      if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
+      if (!ok && lane == 0) fail();
+      if (elect_one()) {
+        umma_commit(bar(C::BAR_DONE));
+      }
+      __syncwarp();
+      if (!warp_wait(bar(C::BAR_DONE), 0) && lane == 0) fail();
     }
     __syncwarp();
   } else {

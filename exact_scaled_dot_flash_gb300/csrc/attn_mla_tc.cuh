@@ -393,36 +393,47 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int fills = (issued - st + NVS - 1) / NVS;
         if (!mbar_wait(bar(C::BAR_V_FULL + st), (fills - 1) & 1)) fail();
       }
-    } else if (warp == WARP_MMA && lane == 0) {
+    } else if (warp == WARP_MMA) {
       // ------------------------------------------------------------ score MMA issuer
+      // (the whole warp waits; one elected lane issues the MMAs and commits)
       constexpr uint32_t idesc_s = make_idesc_f16(BF16, BM, BN, false);
       constexpr uint32_t KCH16 = C::KCH_BYTES >> 4;
       const uint64_t d_sr = smem_desc(sb + C::OFF_SR, 16, 1024, 2u);
       // score MMAs of the own tiles, chunk by chunk (once the softmax has read
       // the previous own S); P . V is issued by another warp (WARP_PV): a
       // tcgen05.mma takes ~70 cycles of its issuing thread
-      bool ok = mbar_wait(bar(C::BAR_QT), 0);
+      bool ok = warp_wait(bar(C::BAR_QT), 0);
       tc_fence_after();
       int cnt = 0;
       for (int d = h, k = 0; d < n && ok; d += NH, ++k) {
-        if (k > 0 && !mbar_wait(bar(C::BAR_SFREE), (k - 1) & 1)) { ok = false; break; }
+        if (k > 0 && !warp_wait(bar(C::BAR_SFREE), (k - 1) & 1)) { ok = false; break; }
         for (int c = 0; c < C::NCH; ++c, ++cnt) {
           const int slot = cnt % NSR;
-          if (!mbar_wait(bar(C::BAR_SR_FULL + slot), (cnt / NSR) & 1)) { ok = false; break; }
+          if (!warp_wait(bar(C::BAR_SR_FULL + slot), (cnt / NSR) & 1)) { ok = false; break; }
           tc_fence_after();
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_ts(tmem + COL_S, tmem + COL_Q + c * 32 + kk * 8, d_sr + slot * KCH16 + kk * 2, idesc_s,
-                    (c | kk) ? 1u : 0u);
-          umma_commit(bar(C::BAR_SR_EMPTY + slot));
+            for (int kk = 0; kk < 4; ++kk)
+              umma_ts(tmem + COL_S, tmem + COL_Q + c * 32 + kk * 8, d_sr + slot * KCH16 + kk * 2, idesc_s,
+                      (c | kk) ? 1u : 0u);
+            umma_commit(bar(C::BAR_SR_EMPTY + slot));
+          }
+          __syncwarp();
         }
-        if (ok) umma_commit(bar(C::BAR_S));
+        if (elect_one()) {
+          if (ok) umma_commit(bar(C::BAR_S));
+        }
+        __syncwarp();
       }
-      if (!ok) fail();
-      umma_commit(bar(C::BAR_DONE));
-      if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
-    } else if (warp == WARP_PV && lane == 0) {
+      if (!ok && lane == 0) fail();
+      if (elect_one()) {
+        umma_commit(bar(C::BAR_DONE));
+      }
+      __syncwarp();
+      if (!warp_wait(bar(C::BAR_DONE), 0) && lane == 0) fail();
+    } else if (warp == WARP_PV) {
       // ------------------------------------------------------------ P . V issuer
+      // (the whole warp waits; one elected lane issues the MMAs and commits)
       constexpr uint32_t idesc_pv = make_idesc_f16(BF16, BM, OC, true);
       constexpr uint32_t P16 = C::P_BYTES >> 4;
       constexpr uint32_t V16 = C::V_BYTES >> 4;
@@ -433,22 +444,28 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int j = 0; j < n && ok; ++j) {
         const int slot = j % NPS, st = j % NVS;
-        if (!mbar_wait(bar(C::BAR_P_READY + slot), (j / NPS) & 1) ||
-            !mbar_wait(bar(C::BAR_V_FULL + st), (j / NVS) & 1)) {
+        if (!warp_wait(bar(C::BAR_P_READY + slot), (j / NPS) & 1) ||
+            !warp_wait(bar(C::BAR_V_FULL + st), (j / NVS) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          umma_ss(tmem + COL_O, d_p + slot * P16 + kk * 2, d_v + st * V16 + kk * VSTEP16, idesc_pv,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(C::BAR_PV_DONE + slot));
-        umma_commit_mc(bar(C::BAR_SLOT_FREE + slot), all);
+          for (int kk = 0; kk < BN / 16; ++kk)
+            umma_ss(tmem + COL_O, d_p + slot * P16 + kk * 2, d_v + st * V16 + kk * VSTEP16, idesc_pv,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar(C::BAR_PV_DONE + slot));
+          umma_commit_mc(bar(C::BAR_SLOT_FREE + slot), all);
+        }
+        __syncwarp();
       }
-      if (!ok) fail();
-      umma_commit(bar(C::BAR_DONE));
-      if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
+      if (!ok && lane == 0) fail();
+      if (elect_one()) {
+        umma_commit(bar(C::BAR_DONE));
+      }
+      __syncwarp();
+      if (!warp_wait(bar(C::BAR_DONE), 0) && lane == 0) fail();
     }
     __syncwarp();
     cluster_wait();

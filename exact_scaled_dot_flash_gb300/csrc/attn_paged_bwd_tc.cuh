@@ -184,8 +184,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait(bar(C::BAR_FULL + st), (fills - 1) & 1)) fail();
       }
       if (!mbar_wait(bar(C::BAR_RES), 0)) fail();
-    } else if (warp == WARP_MMA && lane == 0) {
+    } else if (warp == WARP_MMA) {
       // ------------------------------------------------------------ MMA issuer (the dense kernel's)
+      // (the whole warp waits; one elected lane issues the MMAs and commits)
       constexpr uint32_t idesc_s = make_idesc_f16(BF16, BR, BR, false);
       constexpr uint32_t idesc_o = make_idesc_f16(BF16, BR, D, true);
       constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
@@ -197,55 +198,73 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       auto issue_s = [&](int it) {
         const int st = it % C::STAGES;
-        if (!mbar_wait(bar(C::BAR_FULL + st), (it / C::STAGES) & 1)) return false;
+        if (!warp_wait(bar(C::BAR_FULL + st), (it / C::STAGES) & 1)) return false;
         tc_fence_after();
         const uint64_t q = ring_k + st * 2 * TILE16;
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_D; ++k)
-          umma_ss(tmem + 0, dk_a + kstep16<D>(k), q + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
-        umma_commit(bar(C::BAR_S));
+          for (int k = 0; k < C::KSTEPS_D; ++k)
+            umma_ss(tmem + 0, dk_a + kstep16<D>(k), q + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
+          umma_commit(bar(C::BAR_S));
+        }
+        __syncwarp();
         return true;
       };
       auto issue_dp = [&](int it) {
         const int st = it % C::STAGES;
         const uint64_t g = ring_k + st * 2 * TILE16 + TILE16;
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_D; ++k)
-          umma_ss(tmem + BR, dv_a + kstep16<D>(k), g + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
-        umma_commit(bar(C::BAR_DP));
+          for (int k = 0; k < C::KSTEPS_D; ++k)
+            umma_ss(tmem + BR, dv_a + kstep16<D>(k), g + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
+          umma_commit(bar(C::BAR_DP));
+        }
+        __syncwarp();
       };
       if (N > 0) {
-        if (!mbar_wait(bar(C::BAR_RES), 0)) ok = false;
+        if (!warp_wait(bar(C::BAR_RES), 0)) ok = false;
         tc_fence_after();
         if (ok && !issue_s(0)) ok = false;
         if (ok) issue_dp(0);
         for (int it = 0; it < N && ok; ++it) {
           const int st = it % C::STAGES;
-          if (!mbar_wait(bar(C::BAR_P), it & 1)) { ok = false; break; }
+          if (!warp_wait(bar(C::BAR_P), it & 1)) { ok = false; break; }
           tc_fence_after();
           {
             const uint64_t g = ring_mn + st * 2 * TILE16 + TILE16;
+            if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < C::KSTEPS_R; ++k)
-              umma_ts(tmem + 256, tmem + tmem_a_kstep(k), g + k * RSTEP16, idesc_o, (it > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < C::KSTEPS_R; ++k)
+                umma_ts(tmem + 256, tmem + tmem_a_kstep(k), g + k * RSTEP16, idesc_o, (it > 0 || k > 0) ? 1u : 0u);
+            }
+            __syncwarp();
           }
           if (it + 1 < N && !issue_s(it + 1)) { ok = false; break; }
-          if (!mbar_wait(bar(C::BAR_DS), it & 1)) { ok = false; break; }
+          if (!warp_wait(bar(C::BAR_DS), it & 1)) { ok = false; break; }
           tc_fence_after();
           {
             const uint64_t q = ring_mn + st * 2 * TILE16;
+            if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < C::KSTEPS_R; ++k)
-              umma_ts(tmem + 256 + D, tmem + BR + tmem_a_kstep(k), q + k * RSTEP16, idesc_o,
-                      (it > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < C::KSTEPS_R; ++k)
+                umma_ts(tmem + 256 + D, tmem + BR + tmem_a_kstep(k), q + k * RSTEP16, idesc_o,
+                        (it > 0 || k > 0) ? 1u : 0u);
+            }
+            __syncwarp();
           }
-          umma_commit(bar(C::BAR_EMPTY + st));
+          if (elect_one()) {
+            umma_commit(bar(C::BAR_EMPTY + st));
+          }
+          __syncwarp();
           if (it + 1 < N) issue_dp(it + 1);
         }
       }
-      if (!ok) fail();
-      umma_commit(bar(C::BAR_DONE));
-      if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
+      if (!ok && lane == 0) fail();
+      if (elect_one()) {
+        umma_commit(bar(C::BAR_DONE));
+      }
+      __syncwarp();
+      if (!warp_wait(bar(C::BAR_DONE), 0) && lane == 0) fail();
     }
     __syncwarp();
   } else {
@@ -497,8 +516,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait(bar(BAR_KVFULL + st), (fills - 1) & 1)) fail();
       }
       if (!mbar_wait(bar(C::BAR_RES), 0)) fail();
-    } else if (warp == WARP_MMA && lane == 0) {
+    } else if (warp == WARP_MMA) {
       // ------------------------------------------------------------ MMA issuer
+      // (the whole warp waits; one elected lane issues the MMAs and commits)
       constexpr uint32_t idesc_s = make_idesc_f16(BF16, BR, BR, false);
       constexpr uint32_t idesc_o = make_idesc_f16(BF16, BR, D, true);
       constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
@@ -506,38 +526,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t res_k = smem_desc(sb, 16, C::SBO, C::LAYOUT);                  // Q, dO as K-major B
       const uint64_t res_mn = smem_desc(sb, C::CHUNK_BYTES, C::SBO, C::LAYOUT);     // Q, dO as MN-major B
       const uint64_t ring_k = smem_desc(sb + C::OFF_RING, 16, C::SBO, C::LAYOUT);  // K, V as K-major A
-      bool ok = mbar_wait(bar(C::BAR_RES), 0);
+      bool ok = warp_wait(bar(C::BAR_RES), 0);
       tc_fence_after();
       for (int i = 0; i < nb && ok; ++i) {
         const int st = i % NST;
-        if (!mbar_wait(bar(BAR_KVFULL + st), (i / NST) & 1)) { ok = false; break; }
+        if (!warp_wait(bar(BAR_KVFULL + st), (i / NST) & 1)) { ok = false; break; }
         tc_fence_after();
         const uint64_t kk = ring_k + st * 2 * TILE16;
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_D; ++k)
-          umma_ss(tmem + 0, kk + kstep16<D>(k), res_k + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
-        umma_commit(bar(C::BAR_S));
+          for (int k = 0; k < C::KSTEPS_D; ++k)
+            umma_ss(tmem + 0, kk + kstep16<D>(k), res_k + kstep16<D>(k), idesc_s, k > 0 ? 1u : 0u);
+          umma_commit(bar(C::BAR_S));
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_D; ++k)
-          umma_ss(tmem + BR, kk + TILE16 + kstep16<D>(k), res_k + TILE16 + kstep16<D>(k), idesc_s,
-                  k > 0 ? 1u : 0u);
-        umma_commit(bar(C::BAR_DP));
-        umma_commit(bar(BAR_KVEMPTY + st));  // K and V of the block are no longer read
-        if (!mbar_wait(bar(C::BAR_P), i & 1)) { ok = false; break; }
+          for (int k = 0; k < C::KSTEPS_D; ++k)
+            umma_ss(tmem + BR, kk + TILE16 + kstep16<D>(k), res_k + TILE16 + kstep16<D>(k), idesc_s,
+                    k > 0 ? 1u : 0u);
+          umma_commit(bar(C::BAR_DP));
+          umma_commit(bar(BAR_KVEMPTY + st));  // K and V of the block are no longer read
+        }
+        __syncwarp();
+        if (!warp_wait(bar(C::BAR_P), i & 1)) { ok = false; break; }
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_R; ++k)
-          umma_ts(tmem + 256, tmem + tmem_a_kstep(k), res_mn + TILE16 + k * RSTEP16, idesc_o, k > 0 ? 1u : 0u);
-        if (!mbar_wait(bar(C::BAR_DS), i & 1)) { ok = false; break; }
+          for (int k = 0; k < C::KSTEPS_R; ++k)
+            umma_ts(tmem + 256, tmem + tmem_a_kstep(k), res_mn + TILE16 + k * RSTEP16, idesc_o, k > 0 ? 1u : 0u);
+        }
+        __syncwarp();
+        if (!warp_wait(bar(C::BAR_DS), i & 1)) { ok = false; break; }
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_R; ++k)
-          umma_ts(tmem + 256 + D, tmem + BR + tmem_a_kstep(k), res_mn + k * RSTEP16, idesc_o, k > 0 ? 1u : 0u);
-        umma_commit(bar(BAR_ACC));
+          for (int k = 0; k < C::KSTEPS_R; ++k)
+            umma_ts(tmem + 256 + D, tmem + BR + tmem_a_kstep(k), res_mn + k * RSTEP16, idesc_o, k > 0 ? 1u : 0u);
+          umma_commit(bar(BAR_ACC));
+        }
+        __syncwarp();
       }
-      if (!ok) fail();
-      umma_commit(bar(C::BAR_DONE));
-      if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
+      if (!ok && lane == 0) fail();
+      if (elect_one()) {
+        umma_commit(bar(C::BAR_DONE));
+      }
+      __syncwarp();
+      if (!warp_wait(bar(C::BAR_DONE), 0) && lane == 0) fail();
     }
     __syncwarp();
   } else {
@@ -768,8 +800,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait(bar(X::BAR_FULL + st), (fills - 1) & 1)) fail();
       }
       if (!mbar_wait(bar(X::BAR_RES), 0)) fail();
-    } else if (warp == WARP_MMA && lane == 0) {
+    } else if (warp == WARP_MMA) {
       // ------------------------------------------------------------ MMA issuer
+      // (the whole warp waits; one elected lane issues the MMAs and commits)
       constexpr uint32_t idesc_s = make_idesc_f16(BF16, BR, NPN, false);
       constexpr uint32_t idesc_o = make_idesc_f16(BF16, BR, D, true);
       constexpr uint32_t QTILE16 = X::QTILE >> 4, QCHUNK16 = X::QCHUNK >> 4;
@@ -779,37 +812,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t res_mn = smem_desc(sb, X::QCHUNK, C::SBO, C::LAYOUT);      // Q, dO as MN-major B
       const uint64_t ring_k = smem_desc(sb + X::OFF_RING, 16, C::SBO, C::LAYOUT);  // K, V as K-major A
       auto qstep = [](int k) -> uint32_t { return (k / 4) * QCHUNK16 + (k % 4) * 2; };
-      bool ok = mbar_wait(bar(X::BAR_RES), 0);
+      bool ok = warp_wait(bar(X::BAR_RES), 0);
       tc_fence_after();
       for (int i = 0; i < nb && ok; ++i) {
         const int st = i % NST;
-        if (!mbar_wait(bar(X::BAR_FULL + st), (i / NST) & 1)) { ok = false; break; }
+        if (!warp_wait(bar(X::BAR_FULL + st), (i / NST) & 1)) { ok = false; break; }
         tc_fence_after();
         const uint64_t kk = ring_k + st * KV16;
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_D; ++k)
-          umma_ss(tmem + 0, kk + kstep16<D>(k), res_k + qstep(k), idesc_s, k > 0 ? 1u : 0u);
-        umma_commit(bar(X::BAR_S));
+          for (int k = 0; k < C::KSTEPS_D; ++k)
+            umma_ss(tmem + 0, kk + kstep16<D>(k), res_k + qstep(k), idesc_s, k > 0 ? 1u : 0u);
+          umma_commit(bar(X::BAR_S));
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_D; ++k)
-          umma_ss(tmem + BR, kk + TILE16 + kstep16<D>(k), res_k + QTILE16 + qstep(k), idesc_s, k > 0 ? 1u : 0u);
-        umma_commit(bar(X::BAR_DP));
-        umma_commit(bar(X::BAR_EMPTY + st));  // K and V of the block are no longer read
-        if (!mbar_wait(bar(X::BAR_P), i & 1)) { ok = false; break; }
+          for (int k = 0; k < C::KSTEPS_D; ++k)
+            umma_ss(tmem + BR, kk + TILE16 + kstep16<D>(k), res_k + QTILE16 + qstep(k), idesc_s, k > 0 ? 1u : 0u);
+          umma_commit(bar(X::BAR_DP));
+          umma_commit(bar(X::BAR_EMPTY + st));  // K and V of the block are no longer read
+        }
+        __syncwarp();
+        if (!warp_wait(bar(X::BAR_P), i & 1)) { ok = false; break; }
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < NPN / 16; ++k)
-          umma_ts(tmem + 256, tmem + k * 8, res_mn + QTILE16 + k * RSTEP16, idesc_o, k > 0 ? 1u : 0u);
-        if (!mbar_wait(bar(X::BAR_DS), i & 1)) { ok = false; break; }
+          for (int k = 0; k < NPN / 16; ++k)
+            umma_ts(tmem + 256, tmem + k * 8, res_mn + QTILE16 + k * RSTEP16, idesc_o, k > 0 ? 1u : 0u);
+        }
+        __syncwarp();
+        if (!warp_wait(bar(X::BAR_DS), i & 1)) { ok = false; break; }
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < NPN / 16; ++k)
-          umma_ts(tmem + 256 + D, tmem + BR + k * 8, res_mn + k * RSTEP16, idesc_o, k > 0 ? 1u : 0u);
-        umma_commit(bar(X::BAR_ACC));
+          for (int k = 0; k < NPN / 16; ++k)
+            umma_ts(tmem + 256 + D, tmem + BR + k * 8, res_mn + k * RSTEP16, idesc_o, k > 0 ? 1u : 0u);
+          umma_commit(bar(X::BAR_ACC));
+        }
+        __syncwarp();
       }
-      if (!ok) fail();
-      umma_commit(bar(X::BAR_DONE));
-      if (!mbar_wait(bar(X::BAR_DONE), 0)) fail();
+      if (!ok && lane == 0) fail();
+      if (elect_one()) {
+        umma_commit(bar(X::BAR_DONE));
+      }
+      __syncwarp();
+      if (!warp_wait(bar(X::BAR_DONE), 0) && lane == 0) fail();
     }
     __syncwarp();
   } else {
@@ -1033,8 +1078,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int st = 0; st < Q::VST && st < nv; ++st)
         if (!mbar_wait(bar(Q::BAR_VFULL + st), (((nv - st + Q::VST - 1) / Q::VST) - 1) & 1)) fail();
       if (!mbar_wait(bar(Q::BAR_RES), 0)) fail();
-    } else if (warp == WARP_MMA && lane == 0) {
+    } else if (warp == WARP_MMA) {
       // ------------------------------------------------------------ MMA issuer (the dense kernel's)
+      // (the whole warp waits; one elected lane issues the MMAs and commits)
       constexpr uint32_t idesc_s = make_idesc_f16(BF16, BR, BR, false);
       constexpr uint32_t idesc_o = make_idesc_f16(BF16, BR, D, true);
       constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
@@ -1047,49 +1093,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       auto issue_s = [&](int j) {
         const int ks = j % Q::KST;
-        if (!mbar_wait(bar(Q::BAR_KFULL + ks), (j / Q::KST) & 1)) return false;
+        if (!warp_wait(bar(Q::BAR_KFULL + ks), (j / Q::KST) & 1)) return false;
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_D; ++k)
-          umma_ss(tmem + BR * (j & 1), q_a + kstep16<D>(k), k_b + ks * TILE16 + kstep16<D>(k), idesc_s,
-                  k > 0 ? 1u : 0u);
-        umma_commit(bar(Q::BAR_S + (j & 1)));
+          for (int k = 0; k < C::KSTEPS_D; ++k)
+            umma_ss(tmem + BR * (j & 1), q_a + kstep16<D>(k), k_b + ks * TILE16 + kstep16<D>(k), idesc_s,
+                    k > 0 ? 1u : 0u);
+          umma_commit(bar(Q::BAR_S + (j & 1)));
+        }
+        __syncwarp();
         return true;
       };
       auto issue_dp = [&](int j) {
         const int vs = j % Q::VST;
-        if (!mbar_wait(bar(Q::BAR_VFULL + vs), (j / Q::VST) & 1)) return false;
+        if (!warp_wait(bar(Q::BAR_VFULL + vs), (j / Q::VST) & 1)) return false;
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_D; ++k)
-          umma_ss(tmem + 2 * BR, do_a + kstep16<D>(k), v_b + vs * TILE16 + kstep16<D>(k), idesc_s,
-                  k > 0 ? 1u : 0u);
-        umma_commit(bar(Q::BAR_DP));
-        umma_commit(bar(Q::BAR_VEMPTY + vs));
+          for (int k = 0; k < C::KSTEPS_D; ++k)
+            umma_ss(tmem + 2 * BR, do_a + kstep16<D>(k), v_b + vs * TILE16 + kstep16<D>(k), idesc_s,
+                    k > 0 ? 1u : 0u);
+          umma_commit(bar(Q::BAR_DP));
+          umma_commit(bar(Q::BAR_VEMPTY + vs));
+        }
+        __syncwarp();
         return true;
       };
       if (N > 0) {
-        if (!mbar_wait(bar(Q::BAR_RES), 0)) ok = false;
+        if (!warp_wait(bar(Q::BAR_RES), 0)) ok = false;
         tc_fence_after();
         if (ok && !issue_s(0)) ok = false;
         if (ok && !issue_dp(0)) ok = false;
         if (ok && N > 1 && !issue_s(1)) ok = false;
         for (int j = 0; j < N && ok; ++j) {
-          if (!mbar_wait(bar(Q::BAR_DS), j & 1)) { ok = false; break; }
+          if (!warp_wait(bar(Q::BAR_DS), j & 1)) { ok = false; break; }
           tc_fence_after();
           const int ks = j % Q::KST;
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < C::KSTEPS_R; ++k)
-            umma_ts(tmem + 3 * BR, tmem + 2 * BR + tmem_a_kstep(k), k_mn + ks * TILE16 + k * RSTEP16, idesc_o,
-                    (j > 0 || k > 0) ? 1u : 0u);
-          umma_commit(bar(Q::BAR_KEMPTY + ks));
+            for (int k = 0; k < C::KSTEPS_R; ++k)
+              umma_ts(tmem + 3 * BR, tmem + 2 * BR + tmem_a_kstep(k), k_mn + ks * TILE16 + k * RSTEP16, idesc_o,
+                      (j > 0 || k > 0) ? 1u : 0u);
+            umma_commit(bar(Q::BAR_KEMPTY + ks));
+          }
+          __syncwarp();
           if (j + 1 < N && !issue_dp(j + 1)) { ok = false; break; }
           if (j + 2 < N && !issue_s(j + 2)) { ok = false; break; }
         }
       }
-      if (!ok) fail();
-      umma_commit(bar(Q::BAR_DONE));
-      if (!mbar_wait(bar(Q::BAR_DONE), 0)) fail();
+      if (!ok && lane == 0) fail();
+      if (elect_one()) {
+        umma_commit(bar(Q::BAR_DONE));
+      }
+      __syncwarp();
+      if (!warp_wait(bar(Q::BAR_DONE), 0) && lane == 0) fail();
     }
     __syncwarp();
   } else {

@@ -226,15 +226,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       for (int t = 0; t < NQ; ++t)
         if (w.n[t] > 0 && !mbar_wait(bar(C::BAR_Q + t), 0)) fail();
-    } else if (warp == WARP_MMA && lane == 0) {
+    } else if (warp == WARP_MMA) {
       // ------------------------------------------------------------ MMA issuer
+      // (the whole warp waits; one elected lane issues the MMAs and commits)
       constexpr uint32_t idesc_qk = make_idesc_f16(BF16, BM, BN, false);
       constexpr uint32_t idesc_pv = make_idesc_f16(BF16, BM, D, true);
       constexpr int ST = C::STAGES;
       const int n0 = w.n[0], n1 = w.n[1], nmax = w.nmax;
       bool ok = true;
       for (int t = 0; t < NQ && ok; ++t)
-        if ((t ? n1 : n0) > 0 && !mbar_wait(bar(C::BAR_Q + t), 0)) ok = false;
+        if ((t ? n1 : n0) > 0 && !warp_wait(bar(C::BAR_Q + t), 0)) ok = false;
       const uint64_t dq0 = smem_desc(sb, 16, C::SBO, C::LAYOUT);
       const uint64_t dk0 = smem_desc(sb + C::OFF_KV, 16, C::SBO, C::LAYOUT);
       const uint64_t dv0 = smem_desc(sb + C::OFF_KV, C::CHUNK_BYTES, C::SBO, C::LAYOUT);
@@ -242,23 +243,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t CHUNK16 = C::CHUNK_BYTES >> 4;
       constexpr uint32_t VSTEP16 = (16 * 128) >> 4;
       auto kstep = [](int k) -> uint32_t { return (k / 4) * CHUNK16 + (k % 4) * 2; };
-      auto wait_full = [&](int idx) { return mbar_wait(bar(C::BAR_FULL + idx % ST), (idx / ST) & 1); };
+      auto wait_full = [&](int idx) { return warp_wait(bar(C::BAR_FULL + idx % ST), (idx / ST) & 1); };
       auto issue_s = [&](int t, int j) {
         const uint64_t a = dq0 + t * TILE16;
         const uint64_t b = dk0 + ((2 * j) % ST) * TILE16;
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::KSTEPS_QK; ++k)
-          umma_ss(tmem + t * BN, a + kstep(k), b + kstep(k), idesc_qk, k > 0 ? 1u : 0u);
-        umma_commit(bar(C::BAR_S + t));
+          for (int k = 0; k < C::KSTEPS_QK; ++k)
+            umma_ss(tmem + t * BN, a + kstep(k), b + kstep(k), idesc_qk, k > 0 ? 1u : 0u);
+          umma_commit(bar(C::BAR_S + t));
+        }
+        __syncwarp();
       };
       auto issue_pv = [&](int t, int j) {
         const uint64_t b = dv0 + ((2 * j + 1) % ST) * TILE16;
         const uint32_t d = tmem + 256 + t * D;
         const uint32_t a = tmem + t * BN + C::COL_P;
-        umma_ts(d, a, b, idesc_pv, j > 0 ? 1u : 0u);
+        if (elect_one()) {
+          umma_ts(d, a, b, idesc_pv, j > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 1; k < C::KSTEPS_PV; ++k) umma_ts(d, a + k * 8, b + k * VSTEP16, idesc_pv, 1u);
-        if (j == (t ? n1 : n0) - 1) umma_commit(bar(C::BAR_O + t));
+          for (int k = 1; k < C::KSTEPS_PV; ++k) umma_ts(d, a + k * 8, b + k * VSTEP16, idesc_pv, 1u);
+          if (j == (t ? n1 : n0) - 1) umma_commit(bar(C::BAR_O + t));
+        }
+        __syncwarp();
       };
       // no abort-flag polling here: every wait below is bounded
       for (int j = 0; j <= nmax && ok; ++j) {
@@ -269,24 +276,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (j >= 1 && j - 1 < n1) {
           if (j - 1 >= n0 && !wait_full(2 * (j - 1) + 1)) { ok = false; break; }
-          if (!mbar_wait(bar(C::BAR_P + 1), (j - 1) & 1)) { ok = false; break; }
+          if (!warp_wait(bar(C::BAR_P + 1), (j - 1) & 1)) { ok = false; break; }
           tc_fence_after();
           issue_pv(1, j - 1);
         }
-        if (j >= 1) umma_commit(bar(C::BAR_EMPTY + (2 * (j - 1) + 1) % ST));
+        if (j >= 1) {
+          if (elect_one()) umma_commit(bar(C::BAR_EMPTY + (2 * (j - 1) + 1) % ST));
+          __syncwarp();
+        }
         if (j < nmax) {
           if (j < n1) issue_s(1, j);
-          umma_commit(bar(C::BAR_EMPTY + (2 * j) % ST));
+          if (elect_one()) umma_commit(bar(C::BAR_EMPTY + (2 * j) % ST));
+          __syncwarp();
           if (j < n0) {
-            if (!wait_full(2 * j + 1) || !mbar_wait(bar(C::BAR_P + 0), j & 1)) { ok = false; break; }
+            if (!wait_full(2 * j + 1) || !warp_wait(bar(C::BAR_P + 0), j & 1)) { ok = false; break; }
             tc_fence_after();
             issue_pv(0, j);
           }
         }
       }
-      if (!ok) fail();
-      umma_commit(bar(C::BAR_DONE));
-      if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
+      if (!ok && lane == 0) fail();
+      if (elect_one()) umma_commit(bar(C::BAR_DONE));
+      __syncwarp();
+      if (!warp_wait(bar(C::BAR_DONE), 0) && lane == 0) fail();
     }
     __syncwarp();
   } else {

@@ -18,7 +18,8 @@
 //                   O, stages it in shared memory and stores it with TMA.
 //   warp 8          TMA producer: Q tiles once, then K_j, V_j in order into a
 //                   ring of STAGES shared-memory slots (full/empty mbarriers).
-//   warp 9          MMA issuer (one thread); allocates the 512 TMEM columns.
+//   warp 9          MMA issuer (the whole warp waits, one elected lane issues);
+//                   allocates the 512 TMEM columns.
 //   warps 10, 11    idle (they complete the third warpgroup, whose registers
 //                   are handed to the softmax warpgroups with setmaxnreg).
 // MMA issue order per K/V tile j:  S_0(j), PV_1(j-1), S_1(j), PV_0(j), with
@@ -318,14 +319,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
     } else if (warp == WARP_MMA) {
       // -------------------------------------------------------------- MMA issuer
-      if (lane == 0) {
+      // The whole warp runs the loop and takes every wait; one elected lane
+      // issues the MMAs and commits.
+      {
         constexpr uint32_t idesc_qk = make_idesc_f16(BF16, BM, BN, false);
         constexpr uint32_t idesc_pv = make_idesc_f16(BF16, BM, D, true);
         constexpr int ST = C::STAGES;
         const int n0 = w.n[0], n1 = w.n[1], nmax = w.nmax;
         bool ok = true;
         for (int t = 0; t < NQ && ok; ++t)
-          if (w.n[t] > 0 && !mbar_wait(bar(C::BAR_Q + t), 0)) ok = false;
+          if (w.n[t] > 0 && !warp_wait(bar(C::BAR_Q + t), 0)) ok = false;
 
         // Descriptors of the first K-step of Q_0, of ring stage 0 as a K tile
         // (K-major) and as a V tile (MN-major). Other tiles, stages and K-steps
@@ -340,32 +343,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           return (k / C::KSTEPS_PER_CHUNK) * CHUNK16 + (k % C::KSTEPS_PER_CHUNK) * 2;
         };
         auto wait_full = [&](int idx) {
-          return mbar_wait(bar(C::BAR_FULL + idx % ST), (idx / ST) & 1);
+          return warp_wait(bar(C::BAR_FULL + idx % ST), (idx / ST) & 1);
         };
         // S_t = Q_t K_j^T
         auto issue_s = [&](int t, int j) {
           const uint64_t a = dq0 + t * TILE16;
           const uint64_t b = dk0 + ((2 * j) % ST) * TILE16;
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < C::KSTEPS_QK; ++k)
-            umma_ss(tmem + t * BN, a + kstep(k), b + kstep(k), idesc_qk, k > 0 ? 1u : 0u);
-          umma_commit(bar(C::BAR_S + t));
+            for (int k = 0; k < C::KSTEPS_QK; ++k)
+              umma_ss(tmem + t * BN, a + kstep(k), b + kstep(k), idesc_qk, k > 0 ? 1u : 0u);
+            umma_commit(bar(C::BAR_S + t));
+          }
+          __syncwarp();
         };
         // O_t += P_t V_j (P_t of tile j is in tensor memory)
         auto issue_pv = [&](int t, int j) {
           const uint64_t b = dv0 + ((2 * j + 1) % ST) * TILE16;
           const uint32_t d = tmem + 256 + t * D;
           const uint32_t a = tmem + t * BN + C::COL_P;
-          umma_ts(d, a, b, idesc_pv, j > 0 ? 1u : 0u);
+          if (elect_one()) {
+            umma_ts(d, a, b, idesc_pv, j > 0 ? 1u : 0u);
 #pragma unroll
-          for (int k = 1; k < C::KSTEPS_PV; ++k) umma_ts(d, a + k * 8, b + k * VSTEP16, idesc_pv, 1u);
-          if (j == w.n[t] - 1) umma_commit(bar(C::BAR_O + t));
+            for (int k = 1; k < C::KSTEPS_PV; ++k) umma_ts(d, a + k * 8, b + k * VSTEP16, idesc_pv, 1u);
+            if (j == w.n[t] - 1) umma_commit(bar(C::BAR_O + t));
+          }
+          __syncwarp();
         };
 
         // No abort-flag read in this loop: a shared-memory load between MMA
         // groups stalls the MMA stream (measured: 9% on the causal S=4096
         // D=128 workload). If another role fails, the next bounded wait here
-        // expires instead and this thread takes the same exit.
+        // expires instead and this warp takes the same exit.
         for (int j = 0; j <= nmax && ok; ++j) {
           if (j < nmax) {
             if (!wait_full(2 * j)) { ok = false; break; }  // K_j
@@ -375,25 +384,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (j >= 1 && j - 1 < n1) {
             // V_{j-1} was already waited for by PV_0(j-1) unless tile 0 skipped it
             if (j - 1 >= n0 && !wait_full(2 * (j - 1) + 1)) { ok = false; break; }
-            if (!mbar_wait(bar(C::BAR_P + 1), (j - 1) & 1)) { ok = false; break; }
+            if (!warp_wait(bar(C::BAR_P + 1), (j - 1) & 1)) { ok = false; break; }
             tc_fence_after();
             issue_pv(1, j - 1);
           }
-          if (j >= 1) umma_commit(bar(C::BAR_EMPTY + (2 * (j - 1) + 1) % ST));  // V_{j-1} free
+          if (j >= 1) {
+            if (elect_one()) umma_commit(bar(C::BAR_EMPTY + (2 * (j - 1) + 1) % ST));  // V_{j-1} free
+            __syncwarp();
+          }
           if (j < nmax) {
             if (j < n1) issue_s(1, j);
-            umma_commit(bar(C::BAR_EMPTY + (2 * j) % ST));  // K_j free
+            if (elect_one()) umma_commit(bar(C::BAR_EMPTY + (2 * j) % ST));  // K_j free
+            __syncwarp();
             if (j < n0) {
-              if (!wait_full(2 * j + 1) || !mbar_wait(bar(C::BAR_P + 0), j & 1)) { ok = false; break; }
+              if (!wait_full(2 * j + 1) || !warp_wait(bar(C::BAR_P + 0), j & 1)) { ok = false; break; }
               tc_fence_after();
               issue_pv(0, j);
             }
           }
         }
-        if (!ok) fail();
+        if (!ok && lane == 0) fail();
         // Drain: all MMAs issued above have completed before TMEM is freed.
-        umma_commit(bar(C::BAR_DONE));
-        if (!mbar_wait(bar(C::BAR_DONE), 0)) fail();
+        if (elect_one()) umma_commit(bar(C::BAR_DONE));
+        __syncwarp();
+        if (!warp_wait(bar(C::BAR_DONE), 0) && lane == 0) fail();
       }
       __syncwarp();
     }
