@@ -256,15 +256,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp >= 8) {
     setmaxnreg_dec<REG_OTHER>();
-    if (warp == WARP_TMA && lane == 0 && N > 0) {
+    if (warp == WARP_TMA && N > 0) {
       // ------------------------------------------------------------ producer
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_do);
-      tma_prefetch_desc(&tm_lat);
-      if constexpr (PD > 0) {
-        tma_prefetch_desc(&tm_qp);
-        tma_prefetch_desc(&tm_kp);
+      // (the whole warp waits; one elected lane issues the copies)
+      if (elect_one()) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_lat);
+        if constexpr (PD > 0) {
+          tma_prefetch_desc(&tm_qp);
+          tma_prefetch_desc(&tm_kp);
+        }
       }
+      __syncwarp();
       // chunk c of role `role` of iteration it into dst, completing on b
       auto load = [&](int it, int c, int role, uint32_t dst, uint32_t b) {
         if (role == 0) {
@@ -284,36 +288,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // the keep set of this iteration: free once the gradient MMAs of the
         // iteration that last used it completed
         const int kb = it % C::KBUF;
-        if (it >= C::KBUF && !mbar_wait(bar(C::BAR_KFREE + kb), ((it / C::KBUF) - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(C::BAR_KFULL + kb), C::KEEP * CHUNK_BYTES);
-        for (int c = 0; c < C::NCH; ++c)
-          for (int role = 0; role < 3; ++role) {
-            if (role == 2 && c >= C::NCL) continue;
-            const int k = C::keep_slot(c, role, w.h);
-            if (k >= 0)
-              load(it, c, role, sb + C::OFF_KEEP + (kb * C::KEEP + k) * CHUNK_BYTES, bar(C::BAR_KFULL + kb));
-          }
+        if (it >= C::KBUF && !warp_wait(bar(C::BAR_KFREE + kb), ((it / C::KBUF) - 1) & 1)) { ok = false; break; }
+        if (elect_one()) {
+          mbar_arrive_expect_tx(bar(C::BAR_KFULL + kb), C::KEEP * CHUNK_BYTES);
+          for (int c = 0; c < C::NCH; ++c)
+            for (int role = 0; role < 3; ++role) {
+              if (role == 2 && c >= C::NCL) continue;
+              const int k = C::keep_slot(c, role, w.h);
+              if (k >= 0)
+                load(it, c, role, sb + C::OFF_KEEP + (kb * C::KEEP + k) * CHUNK_BYTES, bar(C::BAR_KFULL + kb));
+            }
+        }
+        __syncwarp();
         ++nit;
         for (int c = 0; c < C::NCH && ok; ++c)
           for (int role = 0; role < 3; ++role) {
             if (role == 2 && c >= C::NCL) continue;
             if (C::keep_slot(c, role, w.h) >= 0) continue;
             const int slot = rc % C::RING;
-            if (!mbar_wait(bar(C::BAR_EMPTY + slot), ((rc / C::RING) & 1) ^ 1)) { ok = false; break; }
-            mbar_arrive_expect_tx(bar(C::BAR_FULL + slot), CHUNK_BYTES);
-            load(it, c, role, sb + C::OFF_RING + slot * CHUNK_BYTES, bar(C::BAR_FULL + slot));
+            if (!warp_wait(bar(C::BAR_EMPTY + slot), ((rc / C::RING) & 1) ^ 1)) { ok = false; break; }
+            if (elect_one()) {
+              mbar_arrive_expect_tx(bar(C::BAR_FULL + slot), CHUNK_BYTES);
+              load(it, c, role, sb + C::OFF_RING + slot * CHUNK_BYTES, bar(C::BAR_FULL + slot));
+            }
+            __syncwarp();
             ++rc;
           }
       }
-      if (!ok) fail();
+      if (!ok && lane == 0) fail();
       // drain: every copy issued has landed before the CTA exits
       for (int i = 0; i < C::RING && i < rc; ++i) {
         const int fills = (rc - i + C::RING - 1) / C::RING;
-        if (!mbar_wait(bar(C::BAR_FULL + i), (fills - 1) & 1)) fail();
+        if (!warp_wait(bar(C::BAR_FULL + i), (fills - 1) & 1) && lane == 0) fail();
       }
       for (int kb = 0; kb < C::KBUF && kb < nit; ++kb) {
         const int fills = (nit - kb + C::KBUF - 1) / C::KBUF;
-        if (!mbar_wait(bar(C::BAR_KFULL + kb), (fills - 1) & 1)) fail();
+        if (!warp_wait(bar(C::BAR_KFULL + kb), (fills - 1) & 1) && lane == 0) fail();
       }
     } else if (warp == WARP_MMA) {
       // ------------------------------------------------------------ MMA issuer

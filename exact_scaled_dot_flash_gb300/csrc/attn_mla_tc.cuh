@@ -56,11 +56,13 @@
 // the score chunks of this CTA's tiles), 6 TMA (this CTA's two value chunks of
 // every tile), 5 score-MMA issuer (the next own tile's 36 MMAs, chunk by chunk,
 // once the softmax has read the previous S), 7 P . V issuer (every tile in order
-// as its P arrives). A tcgen05.mma takes ~70 cycles of its issuing thread and a
-// commit ~45: one issuer for both streams spent ~4000 cycles per 4 tiles issuing
-// and made the next own score tile wait behind the P . V of the peers' tiles
-// (one thread in order: a third slower; one thread polling both streams: 25 %
-// slower than two threads). The producers read each tile's page ids one tile ahead: a table
+// as its P arrives). Every issuing warp runs its loop as a whole and issues
+// from one elected lane (from a lane-0-only region the copies and MMAs issued
+// 5-7% slower). A tcgen05.mma took ~70 cycles of its issuing thread and a
+// commit ~45 there: one issuer for both streams spent ~4000 cycles per 4 tiles
+// issuing and made the next own score tile wait behind the P . V of the peers'
+// tiles (one thread in order: a third slower; one thread polling both streams:
+// 25 % slower than two threads). The producers read each tile's page ids one tile ahead: a table
 // read in front of every copy put a global-load latency on each chunk. Key
 // tiles are gathered page by page through 3-D views [pages, page_size, R] and
 // [pages, page_size, Pd] of the caches; an invalid page id loads zeros. Every
@@ -276,21 +278,25 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
   if (warp >= 4) {
     cluster_arrive();  // the exchange of first-tile maxima: nothing to send from these warps
-    if (warp == WARP_KEY && lane == 0) {
+    if (warp == WARP_KEY) {
       // ------------------------------------------------ TMA: query, own score chunks
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_lat);
-      if constexpr (PD > 0) {
-        tma_prefetch_desc(&tm_qp);
-        tma_prefetch_desc(&tm_kp);
-      }
+      // (the whole warp waits; one elected lane issues the copies)
       const int gy = static_cast<int>(grow0);
-      mbar_arrive_expect_tx(bar(C::BAR_QST), C::NCH * C::QCH_BYTES);
-      for (int c = 0; c < C::NCH; ++c) {
-        const uint32_t dst = sb + c * C::QCH_BYTES;
-        if (c < C::NCH_LAT) tma_load_2d(dst, &tm_q, bar(C::BAR_QST), c * 64, gy);
-        else tma_load_2d(dst, &tm_qp, bar(C::BAR_QST), (c - C::NCH_LAT) * 64, gy);
+      if (elect_one()) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_lat);
+        if constexpr (PD > 0) {
+          tma_prefetch_desc(&tm_qp);
+          tma_prefetch_desc(&tm_kp);
+        }
+        mbar_arrive_expect_tx(bar(C::BAR_QST), C::NCH * C::QCH_BYTES);
+        for (int c = 0; c < C::NCH; ++c) {
+          const uint32_t dst = sb + c * C::QCH_BYTES;
+          if (c < C::NCH_LAT) tma_load_2d(dst, &tm_q, bar(C::BAR_QST), c * 64, gy);
+          else tma_load_2d(dst, &tm_qp, bar(C::BAR_QST), (c - C::NCH_LAT) * 64, gy);
+        }
       }
+      __syncwarp();
       bool ok = true;
       int cnt = 0;
       // page ids of the own tile being loaded (cur) and of the next one (nxt),
@@ -314,34 +320,37 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         read_pages(d + NH, nxt);
         for (int c = 0; c < C::NCH; ++c, ++cnt) {
           const int slot = cnt % NSR;
-          if (!mbar_wait(bar(C::BAR_SR_EMPTY + slot), ((cnt / NSR) & 1) ^ 1)) {
+          if (!warp_wait(bar(C::BAR_SR_EMPTY + slot), ((cnt / NSR) & 1) ^ 1)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(C::BAR_SR_FULL + slot), C::KCH_BYTES);
-          const uint32_t base = sb + C::OFF_SR + slot * C::KCH_BYTES;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(bar(C::BAR_SR_FULL + slot), C::KCH_BYTES);
+            const uint32_t base = sb + C::OFF_SR + slot * C::KCH_BYTES;
 #pragma unroll
-          for (int b = 0; b < 8; ++b) {
-            if (b >= boxes) break;
-            const int key = (w.t0 + d) * BN + b * box_rows;
-            const int y = key - (key / P) * P;
-            // checked build: the box lands inside its ring slot (a skipped copy
-            // leaves the slot's barrier to time out)
-            if (!range_in_bounds(pp.status, b * box_rows, box_rows, BN)) continue;
-            const uint32_t dst = base + b * box_rows * 128;
-            if (c < C::NCH_LAT) tma_load_3d(dst, &tm_lat, bar(C::BAR_SR_FULL + slot), c * 64, y, cur[b]);
-            else tma_load_3d(dst, &tm_kp, bar(C::BAR_SR_FULL + slot), (c - C::NCH_LAT) * 64, y, cur[b]);
+            for (int b = 0; b < 8; ++b) {
+              if (b >= boxes) break;
+              const int key = (w.t0 + d) * BN + b * box_rows;
+              const int y = key - (key / P) * P;
+              // checked build: the box lands inside its ring slot (a skipped copy
+              // leaves the slot's barrier to time out)
+              if (!range_in_bounds(pp.status, b * box_rows, box_rows, BN)) continue;
+              const uint32_t dst = base + b * box_rows * 128;
+              if (c < C::NCH_LAT) tma_load_3d(dst, &tm_lat, bar(C::BAR_SR_FULL + slot), c * 64, y, cur[b]);
+              else tma_load_3d(dst, &tm_kp, bar(C::BAR_SR_FULL + slot), (c - C::NCH_LAT) * 64, y, cur[b]);
+            }
           }
+          __syncwarp();
         }
       }
-      if (!ok) fail();
+      if (!ok && lane == 0) fail();
       // the CTA must not retire with copies in flight
       for (int slot = 0; slot < NSR && slot < cnt; ++slot) {
         const int fills = (cnt - slot + NSR - 1) / NSR;
-        if (!mbar_wait(bar(C::BAR_SR_FULL + slot), (fills - 1) & 1)) fail();
+        if (!warp_wait(bar(C::BAR_SR_FULL + slot), (fills - 1) & 1) && lane == 0) fail();
       }
-      if (!mbar_wait(bar(C::BAR_QST), 0)) fail();
-    } else if (warp == WARP_VAL && lane == 0) {
+      if (!warp_wait(bar(C::BAR_QST), 0) && lane == 0) fail();
+    } else if (warp == WARP_VAL) {
       // ------------------------------------------------ TMA: own value chunks of every tile
       // page ids of tiles i (cur), i + 1 and i + 2: read two tiles ahead
       int cur[8], nx1[8], nx2[8];
@@ -357,7 +366,7 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       };
       read_pages(0, nx1);
       read_pages(1, nx2);
-      bool ok = mbar_wait(bar(C::BAR_QT), 0);  // the staged query covers the value stages
+      bool ok = warp_wait(bar(C::BAR_QT), 0);  // the staged query covers the value stages
       int issued = 0;
       for (int i = 0; i < n && ok; ++i, ++issued) {
 #pragma unroll
@@ -370,28 +379,31 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         // the stage's previous tile, i - NVS, has been multiplied (this CTA's P . V;
         // its phase is the (i - NVS) / NPS-th of that slot's barrier, and the one
         // before completed when this producer refilled the stage for i - NVS)
-        if (i >= NVS && !mbar_wait(bar(C::BAR_PV_DONE + (i - NVS) % NPS), ((i - NVS) / NPS) & 1)) {
+        if (i >= NVS && !warp_wait(bar(C::BAR_PV_DONE + (i - NVS) % NPS), ((i - NVS) / NPS) & 1)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar(C::BAR_V_FULL + st), C::V_BYTES);
-        const uint32_t base = sb + C::OFF_V + st * C::V_BYTES;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(bar(C::BAR_V_FULL + st), C::V_BYTES);
+          const uint32_t base = sb + C::OFF_V + st * C::V_BYTES;
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          if (b >= boxes) break;
-          const int key = (w.t0 + i) * BN + b * box_rows;
-          const int y = key - (key / P) * P;
-          if (!range_in_bounds(pp.status, b * box_rows, box_rows, BN)) continue;
+          for (int b = 0; b < 8; ++b) {
+            if (b >= boxes) break;
+            const int key = (w.t0 + i) * BN + b * box_rows;
+            const int y = key - (key / P) * P;
+            if (!range_in_bounds(pp.status, b * box_rows, box_rows, BN)) continue;
 #pragma unroll
-          for (int c2 = 0; c2 < OC / 64; ++c2)
-            tma_load_3d(base + c2 * C::KCH_BYTES + b * box_rows * 128, &tm_lat, bar(C::BAR_V_FULL + st),
-                        (h * (OC / 64) + c2) * 64, y, cur[b]);
+            for (int c2 = 0; c2 < OC / 64; ++c2)
+              tma_load_3d(base + c2 * C::KCH_BYTES + b * box_rows * 128, &tm_lat, bar(C::BAR_V_FULL + st),
+                          (h * (OC / 64) + c2) * 64, y, cur[b]);
+          }
         }
+        __syncwarp();
       }
-      if (!ok) fail();
+      if (!ok && lane == 0) fail();
       for (int st = 0; st < NVS && st < issued; ++st) {
         const int fills = (issued - st + NVS - 1) / NVS;
-        if (!mbar_wait(bar(C::BAR_V_FULL + st), (fills - 1) & 1)) fail();
+        if (!warp_wait(bar(C::BAR_V_FULL + st), (fills - 1) & 1) && lane == 0) fail();
       }
     } else if (warp == WARP_MMA) {
       // ------------------------------------------------------------ score MMA issuer
@@ -400,8 +412,7 @@ __global__ void __cluster_dims__(R / OC, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t KCH16 = C::KCH_BYTES >> 4;
       const uint64_t d_sr = smem_desc(sb + C::OFF_SR, 16, 1024, 2u);
       // score MMAs of the own tiles, chunk by chunk (once the softmax has read
-      // the previous own S); P . V is issued by another warp (WARP_PV): a
-      // tcgen05.mma takes ~70 cycles of its issuing thread
+      // the previous own S); P . V is issued by another warp (WARP_PV)
       bool ok = warp_wait(bar(C::BAR_QT), 0);
       tc_fence_after();
       int cnt = 0;
