@@ -351,19 +351,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (__any_sync(0xffffffffu, !ok)) { failed = true; break; }
       tc_fence_after();
       tmem_ld64<BF16>(tS + 64 * half, x);
-      const bool key_vis = key < lim;
+      // every (key, query) pair of this warp's block visible: no per-element mask;
+      // a query row without a visible key takes lse2 = +inf, so its p is exactly 0
+      const bool interior = !BIAS && key0 + BR - 1 < lim && (!p.causal || key0 + BR - 1 <= i0 + diag);
+      if (interior) {
+        const float l2fa = l2a == -INFINITY ? INFINITY : l2a, l2fb = l2b == -INFINITY ? INFINITY : l2b;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int i = i0 + c;
-        const float l2 = __shfl_sync(0xffffffffu, c < 32 ? l2a : l2b, c & 31);
-        const bool vis = key_vis && (!p.causal || key <= i + diag) && l2 != -INFINITY;
-        float s2 = x[c] * sc - l2;
-        if constexpr (BIAS) {
-          const int64_t bi = (bcol - p.bias) + static_cast<int64_t>(i) * p.Sk;
-          if (vis && in_bounds(p.status, bi, static_cast<int64_t>(p.bias_b) * p.bias_h * p.Sq * p.Sk))
-            s2 = fmaf(__ldg(p.bias + bi), LOG2E, s2);
+        for (int c = 0; c < 64; ++c)
+          x[c] = fast_exp2(x[c] * sc - __shfl_sync(0xffffffffu, c < 32 ? l2fa : l2fb, c & 31));
+      } else {
+        const bool key_vis = key < lim;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const int i = i0 + c;
+          const float l2 = __shfl_sync(0xffffffffu, c < 32 ? l2a : l2b, c & 31);
+          const bool vis = key_vis && (!p.causal || key <= i + diag) && l2 != -INFINITY;
+          float s2 = x[c] * sc - l2;
+          if constexpr (BIAS) {
+            const int64_t bi = (bcol - p.bias) + static_cast<int64_t>(i) * p.Sk;
+            if (vis && in_bounds(p.status, bi, static_cast<int64_t>(p.bias_b) * p.bias_h * p.Sq * p.Sk))
+              s2 = fmaf(__ldg(p.bias + bi), LOG2E, s2);
+          }
+          x[c] = vis ? fast_exp2(s2) : 0.f;
         }
-        x[c] = vis ? fast_exp2(s2) : 0.f;
       }
       tmem_st_packed64<BF16>(tS + 64 * half, x);
       tmem_wait_st();
@@ -634,6 +644,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float l2 = stat_ok ? __ldg(a.lse2 + ri) : -INFINITY;
     const float dsi = stat_ok ? __ldg(a.dsum + ri) : 0.f;
     const bool live = row_ok && l2 != -INFINITY;
+    const float l2f = live ? l2 : INFINITY;  // interior tiles: exp2(s - inf) = 0 for a dead row
     const int causal_lim = p.causal ? i + diag : 0x7fffffff;
     const float sc = p.scale_log2;
     const float* brow = nullptr;
@@ -652,6 +663,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       tmem_ld64<BF16>(tmem + lane_off + BR * (j & 1) + 64 * half, x);
       const int kc0 = j * BR + 64 * half;
+      // every key of this warp's 64 visible to every row of the block: no
+      // per-element mask (a dead row has lse2 = +inf here, so its p is 0)
+      if (!BIAS && kc0 + 63 < lim && (!p.causal || kc0 + 63 <= q0 + diag)) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = fast_exp2(x[c] * sc - l2f);
+      } else
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const int key = kc0 + c;
