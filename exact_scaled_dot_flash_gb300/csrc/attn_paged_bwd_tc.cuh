@@ -1171,6 +1171,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                                                     : -1))
                            : -1;
     const int causal_lim = pp.causal ? pos : 0x7fffffff;
+    // the smallest visibility limit of this warp's live rows: a 64-key slice at or
+    // below it (and inside the sequence) needs no per-element test; a dead row takes
+    // lse2 = +inf there, so its p is exactly 0
+    const int warp_lim = __reduce_min_sync(0xffffffffu, live ? causal_lim : 0x7fffffff);
+    const float l2f = live ? l2 : INFINITY;
     const float sc = pp.scale_log2;
     bool failed = false;
     for (int j = 0; j < N; ++j) {
@@ -1180,11 +1185,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       tmem_ld64<BF16>(tmem + lane_off + BR * (j & 1) + 64 * half, x);
       const int kc0 = j * BR + 64 * half;
+      if (kc0 + 63 < L && kc0 + 63 <= warp_lim) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int key = kc0 + c;
-        const bool vis = live && key < L && key <= causal_lim;
-        x[c] = vis ? fast_exp2(x[c] * sc - l2) : 0.f;
+        for (int c = 0; c < 64; ++c) x[c] = fast_exp2(x[c] * sc - l2f);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const int key = kc0 + c;
+          const bool vis = live && key < L && key <= causal_lim;
+          x[c] = vis ? fast_exp2(x[c] * sc - l2) : 0.f;
+        }
       }
       const bool ok2 = mbar_wait(bar(Q::BAR_DP), j & 1);
       if (__any_sync(0xffffffffu, !ok2)) { failed = true; break; }
